@@ -1,0 +1,313 @@
+#!/usr/bin/env python
+"""Accepted tokens/s of the batched DMTP round on GB300 (one JSON line on stdout).
+
+A step is one DMTP round (steps a1-a6) over the batch. The default workload is the
+B32 serving round: 32 sequences with prompt lengths uniform in [512, 4096], vocab
+151936, d_model 2048, a 16-layer GQA target (32/4 heads x 128, ffn 6144), one MTP
+block and a 2-layer block drafter, bf16 weights and KV, random weights N(0, 0.02)
+and random prompt ids (synthetic stand-ins for the trained models and datasets the
+DMTP blog evaluates). Metric: committed tokens per second = B x rounds/s x mean
+accepted length (DMTP blog §7, per-verify length 1 + sum k hist[k] / sum hist).
+
+  value      device-timed: CUDA events on the library's stream around K graph
+             replays, inputs (weights, KV, state) resident in HBM; every round
+             streams ~7 GB (> 129 MB L2), so no flush is needed between rounds.
+  e2e        the same metric through the C ABI with host buffers: each step
+             enqueues the round and copies committed[B,8] and n[B] back to pinned
+             host memory before the next (wall clock).
+  roofline   the dominant kernel class of a profiled round (CUDA events around
+             each of its launches, on the launching stream), algorithmic bytes /
+             measured time against the measured HBM peak.
+  cpu_baseline  the float64 NumPy oracle on the host cores, on a bounded sample
+             (one sequence of the same batch, a few rounds after its prefill).
+
+--impl reference times that oracle as the reference arm instead.
+Multi-GPU: one process per GPU (torchrun), each with its own 32 sequences
+(replicas; no collective on the data path), barrier + max-over-ranks timing.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "accepted tokens/sec per GPU at B32 (rounds/s x mean accept len); % roofline"
+UNIT = "tokens/s"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampler for the timed region (200 ms period)."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.p = None
+        try:
+            self.p = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-i", str(gpu_index), "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        out, _ = self.p.communicate(timeout=10)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def oracle_sample(cfg, weights, prompts, rounds: int, budget_s: float = 30.0):
+    """Time the oracle on one sequence (the shortest prompt) of the batch: prefill
+    untimed, then up to `rounds` rounds or `budget_s` seconds timed."""
+    from oracle import OracleModel
+    b = int(np.argmin([len(p) for p in prompts]))
+    t0 = time.perf_counter()
+    om = OracleModel(cfg, {k: v.cpu() for k, v in weights.items()})
+    st = om.prefill(prompts[b])
+    setup = time.perf_counter() - t0
+    tokens, el, done = 0, 0.0, 0
+    while done < rounds and el < budget_s:
+        t = time.perf_counter()
+        rec = om.round(st, want_logits=False)
+        el += time.perf_counter() - t
+        tokens += rec["accept_len"]
+        done += 1
+    cores = len(os.sched_getaffinity(0))
+    return {"value": tokens / el, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"sequence {b} of the batch (prompt {len(prompts[b])} tokens), "
+                      f"{done} rounds after an untimed prefill ({setup:.0f} s incl. weight "
+                      f"upcast), float64 NumPy, BLAS threads = {cores}",
+            "rounds": done, "seconds": el}
+
+
+def run_reference(args, cfg):
+    import torch
+    from synth import make_prompts, make_weights
+    rank, world, _ = _dist()
+    if rank != 0:
+        return
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    weights = make_weights(cfg, dev)
+    prompts = make_prompts(cfg)
+    from oracle import OracleModel
+    b = int(np.argmin([len(p) for p in prompts]))
+    om = OracleModel(cfg, {k: v.cpu() for k, v in weights.items()})
+    del weights
+    st = om.prefill(prompts[b])
+    for _ in range(args.warmup):
+        om.round(st, want_logits=False)
+    tokens, t0 = 0, time.perf_counter()
+    for _ in range(args.steps):
+        tokens += om.round(st, want_logits=False)["accept_len"]
+    el = time.perf_counter() - t0
+    v = tokens / el
+    cores = len(os.sched_getaffinity(0))
+    line = {"metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": cfg.name, "global_batch": 1, "seq_len": len(prompts[b]),
+                       "parallelism": "none", "note": "one sequence of the B32 batch per step"},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"one round of sequence {b} (prompt {len(prompts[b])}) "
+                                       "per step, float64 NumPy"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="b32")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--profile-rounds", type=int, default=3)
+    ap.add_argument("--cpu-rounds", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    from synth import CONFIGS
+    cfg = CONFIGS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+
+    import torch
+    import torch.distributed as dist
+    from mtp_block_draft_gb300 import DmtpRound
+    from synth import make_prompts, make_weights
+
+    rank, world, local = _dist()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+
+    weights = make_weights(cfg, dev)
+    pcfg = cfg if rank == 0 else cfg.replace(seed=cfg.seed + 1000 * rank)
+    prompts = make_prompts(pcfg)
+    B = len(prompts)
+    total_rounds = args.warmup + args.steps + args.e2e_steps + args.profile_rounds + 8
+    max_ctx = max(len(p) for p in prompts) + 8 * total_rounds + 32
+    g = DmtpRound(cfg, weights, prompts, max_ctx)
+    stream = g.stream
+
+    for _ in range(args.warmup):
+        g.round()
+    _, _, h0 = g.read_state()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = Clocks(local)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        g.round()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    _, _, h1 = g.read_state()
+    dh = (h1 - h0).astype(np.int64)
+    tokens = int(np.sum((np.arange(8) + 1) * dh))
+    rounds = int(dh.sum())
+    mean_len = tokens / max(1, rounds)
+    t = torch.tensor([ms, float(tokens)], dtype=torch.float64, device=dev)
+    if world > 1:
+        tmax = t.clone()
+        dist.all_reduce(tmax[:1], op=dist.ReduceOp.MAX)
+        dist.all_reduce(t[1:], op=dist.ReduceOp.SUM)
+        ms_all, tok_all = float(tmax[0]), float(t[1])
+    else:
+        ms_all, tok_all = ms, float(tokens)
+    value = tok_all / (ms_all / 1e3)
+
+    # e2e through the C ABI with host outputs (pinned), wall clock
+    committed = torch.empty((B, 8), dtype=torch.int32, pin_memory=True).numpy()
+    nacc = torch.empty((B,), dtype=torch.int32, pin_memory=True).numpy()
+    torch.cuda.synchronize()
+    e2e_tokens, t0 = 0, time.perf_counter()
+    for _ in range(args.e2e_steps):
+        g.round_host(committed, nacc)
+        e2e_tokens += int(np.sum(nacc.astype(np.int64) + 1))
+    e2e_s = time.perf_counter() - t0
+    e2e_val = e2e_tokens / e2e_s
+    if world > 1:
+        te = torch.tensor([e2e_s, float(e2e_tokens)], dtype=torch.float64, device=dev)
+        dist.all_reduce(te[:1], op=dist.ReduceOp.MAX)
+        dist.all_reduce(te[1:], op=dist.ReduceOp.SUM)
+        e2e_val = float(te[1]) / float(te[0])
+
+    # per-kernel-class profile of real rounds (events around each launch)
+    hbm, tc_burst, tc_sus, peak_src = _peaks()
+    prof = [g.profile_round() for _ in range(args.profile_rounds)]
+    classes = ("gemm", "lm_head", "attention", "gdn", "other")
+    agg = {c: {k: sum(p[c][k] for p in prof) / len(prof) for k in ("ms", "bytes", "flops", "launches")}
+           for c in classes}
+    dom = max(classes, key=lambda c: agg[c]["ms"] if c != "other" else -1)
+    a = agg[dom]
+    launches = max(1.0, a["launches"])
+    per_launch_s = a["ms"] / 1e3 / launches
+    gbs = a["bytes"] / launches / per_launch_s / 1e9
+    tfs = a["flops"] / launches / per_launch_s / 1e12
+    t_mem = a["bytes"] / (hbm * 1e9)
+    t_tc = a["flops"] / (tc_sus * 1e12)
+    if t_tc > t_mem:
+        roof = {"bound": "tensor", "achieved": tfs, "peak": tc_sus, "unit": "TFLOP/s",
+                "frac": tfs / tc_sus}
+    else:
+        roof = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm}
+    roof.update({"kernel": dom, "traffic": None, "peak_source": f"{peak_src} (MEASURED_PEAKS.json)"
+                 if peak_src == "measured" else "fallback (profiling recipe)",
+                 "per_launch_bytes": a["bytes"] / launches})
+    breakdown = {c: {"ms_per_round": round(agg[c]["ms"], 4),
+                     "GB_per_round": round(agg[c]["bytes"] / 1e9, 4),
+                     "launches": int(agg[c]["launches"]),
+                     "GB/s": round(agg[c]["bytes"] / max(1e-12, agg[c]["ms"] / 1e3) / 1e9, 1)}
+                 for c in classes}
+    prof_round_ms = sum(p["round_ms"] for p in prof) / len(prof)
+    alg_bytes = sum(agg[c]["bytes"] for c in classes)
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_all / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded random weights N(0,0.02) and uniform prompt ids)",
+            "config": {"workload": f"{cfg.name}: B{B} DMTP round, vocab {cfg.vocab}, d {cfg.d_model}, "
+                                   f"{cfg.n_layers}-layer GQA {cfg.n_heads}/{cfg.n_kv_heads}x{cfg.head_dim} "
+                                   f"target, ffn {cfg.ffn}, 1 MTP block, {cfg.draft_layers}-layer drafter, "
+                                   f"prompts U[{cfg.ctx_lo},{cfg.ctx_hi}]",
+                       "global_batch": B * world, "seq_len": int(np.mean([len(p) for p in prompts])),
+                       "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (~7 GB of weights+KV streamed per round)",
+                       "mean_accept_len": mean_len, "rounds_per_s": rounds / (ms / 1e3)},
+            "clocks": clk,
+            "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": B * 8 * 4 + B * 4},
+            "gpu_launches": g.launches_per_round() * args.steps,
+            "roofline": roof,
+            "round_roofline": {"algorithmic_GB": alg_bytes / 1e9,
+                               "t_roof_ms": alg_bytes / (hbm * 1e9) * 1e3,
+                               "profiled_round_ms": prof_round_ms,
+                               "frac_of_timed": (alg_bytes / (hbm * 1e9) * 1e3) / (ms / args.steps)},
+            "kernels": breakdown}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_sample(cfg, weights, prompts, args.cpu_rounds)
+    g.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,185 @@
+/*
+ * dmtp.h - C ABI of the GB300 (sm_103a) DMTP speculative-decoding round.
+ *
+ * One call of dmtp_round runs one batched DMTP round for all B sequences, as the
+ * DMTP blog ("DMTP: A Better First Token for Block Drafting via MTP") states it in
+ * §5 "Inference: MTP First, DFlash Second" and §6.1 "Separating Prediction from
+ * State Advancement":
+ *   a1  T1 = argmax H RMSNorm(h_MTP) from the cached MTP hidden state;
+ *   a2  Delta = W [RMS_e(E(T1)); RMS_m(h_MTP)] (§3, the residual equation) and the
+ *       eight drafter slots [E(A), E(T1) + Delta, E(MASK) x 6];
+ *   a3  one block-bidirectional drafter forward -> T2..T7 (§2, §6.2);
+ *   a4  one target forward over rows [A, T1..T7] -> per-row picks g0..g7;
+ *   a5  greedy prefix acceptance: n = longest prefix with T_j == g_{j-1}; commit
+ *       T1..Tn and g_n; the KV watermark comes down to the standing rows and a
+ *       recurrent layer's per-row snapshot n is swapped in by pointer (colibri
+ *       speculative-decoding page, "Undoing rows on a model with recurrent state");
+ *   a6  drafter context K/V and MTP state advance over the n+1 committed rows; the
+ *       MTP output at the last one is cached as the next h_MTP.
+ *
+ * Memory ownership. The caller allocates every device buffer (weights, the
+ * workspace, round outputs) and keeps it alive while the context lives; the
+ * library allocates no device memory. The context owns host bookkeeping and one
+ * captured CUDA graph. All work is enqueued on the stream given to dmtp_init;
+ * results are valid once the caller synchronises that stream.
+ *
+ * Errors. Every int-returning call returns DMTP_OK (0) or a negative DMTP_E* code.
+ * Argument errors are detected before any launch and leave the state unchanged.
+ * DMTP_EDEVICE means a kernel's own bounds check fired (token id out of range,
+ * KV write past max_ctx, a bounded wait that gave up); the context is then
+ * poisoned: every later call but dmtp_free returns DMTP_ESTATE.
+ *
+ * Threading: a context is not thread-safe; distinct contexts are independent.
+ */
+#ifndef DMTP_H
+#define DMTP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DMTP_OK 0
+#define DMTP_EINVAL (-1)    /* bad shape, pointer or size (nothing launched)           */
+#define DMTP_ENOMEM (-2)    /* workspace smaller than dmtp_workspace_size reports      */
+#define DMTP_ECAPACITY (-3) /* a sequence would grow past max_ctx (nothing launched)   */
+#define DMTP_ECUDA (-4)     /* a CUDA runtime call failed                              */
+#define DMTP_EDEVICE (-5)   /* a device-side check fired; context poisoned             */
+#define DMTP_ESTATE (-6)    /* context poisoned by an earlier DMTP_EDEVICE             */
+
+#define DMTP_MAX_LAYERS 64
+#define DMTP_MAX_DRAFT_LAYERS 8
+#define DMTP_MAX_TAPS 8
+
+/* Model and capacity. dtype 0: fp32 weights/KV (CUDA-core path), 1: bf16 weights/KV
+ * (tcgen05 tensor-core path). layer_kind[l]: 0 attention, 1 Gated DeltaNet.
+ * Attention layers, the MTP block and the drafter share n_heads/n_kv_heads/head_dim.
+ * tap_layers: target layers whose residual stream feeds the drafter's context
+ * projection (DFlash "KV injection", DFlash vs MTP page). mask_id: the MASK token.
+ * draft_window: the drafter sees context positions max(0, a - window) .. a-1 (DMTP
+ * §6.2). max_ctx: KV capacity per sequence (prompt + 8 per round + 8 slack). */
+typedef struct {
+  int vocab, d_model, n_layers, n_heads, n_kv_heads, head_dim, ffn;
+  int gdn_heads, gdn_dk, gdn_dv;
+  uint8_t layer_kind[DMTP_MAX_LAYERS];
+  int draft_layers, draft_window;
+  int n_taps;
+  int tap_layers[DMTP_MAX_TAPS];
+  int mask_id;
+  float rms_eps, rope_theta;
+  int max_ctx, max_batch;
+  int dtype;
+} dmtp_config;
+
+/* One decoder layer, row-major [out, in] device matrices of the config's dtype.
+ * Attention: wqkv [(hq + 2 hkv) hd, d] (q rows, k rows, v rows), wo [d, hq hd].
+ * Gated DeltaNet: gdn_wqkv [H (2 dk + dv), d], gdn_wa/gdn_wb [H, d], gdn_wo [d, H dv].
+ * MLP: wgu [2F, d] (gate rows then up rows), wdown [d, F]. Norm gains [d]. */
+typedef struct {
+  const void *attn_norm, *wqkv, *wo;
+  const void *gdn_wqkv, *gdn_wa, *gdn_wb, *gdn_wo;
+  const void *mlp_norm, *wgu, *wdown;
+} dmtp_layer_weights;
+
+/* All weights (device pointers, caller-owned, alive for the context's lifetime).
+ * emb/head [V, d] are shared by target, MTP and drafter (untied). mtp_proj [d, 2d]
+ * is M of h' = M [RMSNorm(h); RMSNorm(Emb(t))] (DFlash vs MTP page, "MTP: Sequential
+ * Prediction Heads"); fuse_w [d, 2d] is the DMTP residual matrix W; dft_fc
+ * [d, n_taps d] the drafter's target-context projection. */
+typedef struct {
+  const void *emb, *head, *final_norm;
+  dmtp_layer_weights layers[DMTP_MAX_LAYERS];
+  const void *mtp_norm_h, *mtp_norm_e, *mtp_proj;
+  dmtp_layer_weights mtp;
+  const void* mtp_final_norm;
+  const void *fuse_norm_e, *fuse_norm_m, *fuse_w;
+  const void *dft_fc, *dft_norm_c;
+  dmtp_layer_weights dft[DMTP_MAX_DRAFT_LAYERS];
+  const void* dft_final_norm;
+} dmtp_weights;
+
+/* Per-round outputs: device pointers (caller-allocated), each optional (NULL: not
+ * written). Integer fields: committed [B][8] (T1..Tn, g_n, then -1), n_accepted [B],
+ * drafts [B][7] (T1..T7 as verified), picks [B][8] (g0..g7), kv_len [B] (target
+ * watermark after the round), mtp_len [B] (next MTP position = kv_len + 1), snap_slot
+ * [B] (installed snapshot row, -1 for attention-only targets). Float debug fields
+ * (fp32): t1_logits [B][V], draft_logits [B][6][V], verify_logits [B][8][V], delta
+ * [B][d] (Delta of this round), h_mtp [B][d] (the h_MTP this round started from).
+ * Requesting a float debug field runs the round uncaptured (same kernels). */
+typedef struct {
+  int32_t *committed, *n_accepted, *drafts, *picks, *kv_len, *mtp_len, *snap_slot;
+  float *t1_logits, *draft_logits, *verify_logits, *delta, *h_mtp;
+} dmtp_round_out;
+
+typedef struct dmtp_ctx dmtp_ctx;
+
+/* Bytes of device workspace needed for `batch` sequences (batch <= max_batch,
+ * batch * 8 <= 256). Returns DMTP_EINVAL for an unsupported config. */
+int dmtp_workspace_size(const dmtp_config* cfg, int batch, size_t* bytes);
+
+/* Create a context and run the prefill ("Prefill initializes all three models'
+ * states", DMTP §6.1): target over each prompt (KV, taps), A = the target's greedy
+ * token after it, drafter context K/V, and MTP rows 1..P giving h_MTP.
+ * workspace: device buffer of >= dmtp_workspace_size bytes, 256-byte aligned.
+ * prompt_ids: host int32, the B prompts concatenated; prompt_lens: host int32 [B],
+ * each >= 1. stream: a cudaStream_t (NULL: the default stream). Synchronises the
+ * stream before returning. *out receives the context (NULL on error). */
+int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, size_t ws_bytes,
+              const int32_t* prompt_ids, const int32_t* prompt_lens, int batch, void* stream,
+              dmtp_ctx** out);
+
+/* Enqueue one round (steps a1-a6) for all sequences. out: see dmtp_round_out (may be
+ * NULL). forced_drafts: NULL, or device int32 [B][7] replacing T1..T7 (T1 right after
+ * the MTP head, so the fusion and drafter see it; T2..T7 after the drafter) - the
+ * forced-draft test mode of the colibri page. Returns DMTP_ECAPACITY if a sequence
+ * might pass max_ctx - 8 (checked on the host before launch). Asynchronous. */
+int dmtp_round(dmtp_ctx* ctx, const dmtp_round_out* out, const int32_t* forced_drafts);
+
+/* One round with host outputs: enqueue the round, copy committed [B][8] and
+ * n_accepted [B] (either may be NULL) into host memory and synchronise. */
+int dmtp_round_host(dmtp_ctx* ctx, int32_t* committed_host, int32_t* n_accepted_host);
+
+/* Synchronise and read the state: kv_len [B], pending token A [B] (host arrays, each
+ * may be NULL) and the acceptance histogram hist[k] = rounds that accepted k drafts
+ * (host uint64 [8], may be NULL). Also reports DMTP_EDEVICE if a device check fired. */
+int dmtp_read_state(dmtp_ctx* ctx, int32_t* kv_len, int32_t* pending, uint64_t* hist);
+
+/* Number of kernel launches one round enqueues (for launch accounting). */
+int dmtp_round_launches(const dmtp_ctx* ctx);
+
+/* Kernel classes of dmtp_profile. */
+#define DMTP_PROF_GEMM 0   /* tcgen05 (or fp32) projection / MLP GEMMs              */
+#define DMTP_PROF_HEAD 1   /* LM-head GEMM with fused argmax (a1, a3, a4)          */
+#define DMTP_PROF_ATTN 2   /* split-K attention (partial + merge)                  */
+#define DMTP_PROF_GDN 3    /* Gated DeltaNet recurrence with snapshots             */
+#define DMTP_PROF_OTHER 4  /* norms, RoPE/KV writes, gathers, accept                */
+
+/* Per-class device time and algorithmic traffic of one round. ms: summed CUDA-event
+ * durations of the class's launches (events recorded on the context's stream around
+ * each launch); bytes/flops: what those launches must move/compute (weights and
+ * tokens read once, visible K/V read once per sequence and layer, recurrent state
+ * read once and written per snapshot); round_ms: the whole profiled round. */
+typedef struct {
+  double ms[8], bytes[8], flops[8];
+  int launches[8];
+  double round_ms;
+} dmtp_profile;
+
+/* Run one real round (state advances as with dmtp_round) uncaptured, with CUDA events
+ * around every launch, synchronise and fill *out. For measurement, not for speed. */
+int dmtp_round_profile(dmtp_ctx* ctx, dmtp_profile* out);
+
+/* Release the context (host memory and the graph). Never fails; NULL is a no-op.
+ * Does not free caller-owned device memory. */
+void dmtp_free(dmtp_ctx* ctx);
+
+/* Static description of an error code. */
+const char* dmtp_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DMTP_H */

@@ -1,0 +1,11 @@
+"""GB300-native (sm_103a) DMTP speculative-decoding round.
+
+The round lives in the C-ABI library ``libdmtp.so`` (include/dmtp.h); this package
+holds its CUDA sources (``csrc/``), the in-tree build (``build.py``) and the ctypes
+binding (``binding.py``).
+"""
+from .binding import (DmtpError, DmtpRound, default_max_ctx, load_library, make_config,
+                      make_weights)
+
+__all__ = ["DmtpError", "DmtpRound", "default_max_ctx", "load_library", "make_config",
+           "make_weights"]

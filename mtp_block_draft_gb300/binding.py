@@ -1,0 +1,273 @@
+"""ctypes binding of libdmtp.so: the C ABI of include/dmtp.h with the same names.
+
+Argument marshalling only. Every step of the round runs in the library's CUDA
+kernels; PyTorch supplies device memory (weights, workspace, outputs) and the
+stream. Importing works without a GPU; loading the library requires that it has
+been built (``__graft_entry__.build()`` or ``python -m mtp_block_draft_gb300.build``)
+and raises otherwise - there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libdmtp.so")
+
+DMTP_MAX_LAYERS = 64
+DMTP_MAX_DRAFT_LAYERS = 8
+DMTP_MAX_TAPS = 8
+
+ERRORS = {0: "DMTP_OK", -1: "DMTP_EINVAL", -2: "DMTP_ENOMEM", -3: "DMTP_ECAPACITY",
+          -4: "DMTP_ECUDA", -5: "DMTP_EDEVICE", -6: "DMTP_ESTATE"}
+
+# every symbol include/dmtp.h declares
+EXPORTS = ("dmtp_workspace_size", "dmtp_init", "dmtp_round", "dmtp_round_host",
+           "dmtp_read_state", "dmtp_round_launches", "dmtp_round_profile", "dmtp_free",
+           "dmtp_strerror")
+
+PROFILE_CLASSES = ("gemm", "lm_head", "attention", "gdn", "other")
+
+
+class dmtp_config(C.Structure):
+    _fields_ = [("vocab", C.c_int), ("d_model", C.c_int), ("n_layers", C.c_int),
+                ("n_heads", C.c_int), ("n_kv_heads", C.c_int), ("head_dim", C.c_int),
+                ("ffn", C.c_int), ("gdn_heads", C.c_int), ("gdn_dk", C.c_int),
+                ("gdn_dv", C.c_int), ("layer_kind", C.c_uint8 * DMTP_MAX_LAYERS),
+                ("draft_layers", C.c_int), ("draft_window", C.c_int), ("n_taps", C.c_int),
+                ("tap_layers", C.c_int * DMTP_MAX_TAPS), ("mask_id", C.c_int),
+                ("rms_eps", C.c_float), ("rope_theta", C.c_float), ("max_ctx", C.c_int),
+                ("max_batch", C.c_int), ("dtype", C.c_int)]
+
+
+_LAYER_FIELDS = ("attn_norm", "wqkv", "wo", "gdn_wqkv", "gdn_wa", "gdn_wb", "gdn_wo",
+                 "mlp_norm", "wgu", "wdown")
+
+
+class dmtp_layer_weights(C.Structure):
+    _fields_ = [(f, C.c_void_p) for f in _LAYER_FIELDS]
+
+
+class dmtp_weights(C.Structure):
+    _fields_ = [("emb", C.c_void_p), ("head", C.c_void_p), ("final_norm", C.c_void_p),
+                ("layers", dmtp_layer_weights * DMTP_MAX_LAYERS),
+                ("mtp_norm_h", C.c_void_p), ("mtp_norm_e", C.c_void_p), ("mtp_proj", C.c_void_p),
+                ("mtp", dmtp_layer_weights), ("mtp_final_norm", C.c_void_p),
+                ("fuse_norm_e", C.c_void_p), ("fuse_norm_m", C.c_void_p), ("fuse_w", C.c_void_p),
+                ("dft_fc", C.c_void_p), ("dft_norm_c", C.c_void_p),
+                ("dft", dmtp_layer_weights * DMTP_MAX_DRAFT_LAYERS),
+                ("dft_final_norm", C.c_void_p)]
+
+
+_OUT_INT = ("committed", "n_accepted", "drafts", "picks", "kv_len", "mtp_len", "snap_slot")
+_OUT_FLOAT = ("t1_logits", "draft_logits", "verify_logits", "delta", "h_mtp")
+
+
+class dmtp_round_out(C.Structure):
+    _fields_ = [(f, C.c_void_p) for f in _OUT_INT + _OUT_FLOAT]
+
+
+class dmtp_profile(C.Structure):
+    _fields_ = [("ms", C.c_double * 8), ("bytes", C.c_double * 8), ("flops", C.c_double * 8),
+                ("launches", C.c_int * 8), ("round_ms", C.c_double)]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libdmtp.so and declare the prototypes; raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built; run __graft_entry__.build() first")
+    lib = C.CDLL(path)
+    P = C.c_void_p
+    lib.dmtp_workspace_size.argtypes = [C.POINTER(dmtp_config), C.c_int, C.POINTER(C.c_size_t)]
+    lib.dmtp_workspace_size.restype = C.c_int
+    lib.dmtp_init.argtypes = [C.POINTER(dmtp_config), C.POINTER(dmtp_weights), P, C.c_size_t,
+                              P, P, C.c_int, P, C.POINTER(P)]
+    lib.dmtp_init.restype = C.c_int
+    lib.dmtp_round.argtypes = [P, C.POINTER(dmtp_round_out), P]
+    lib.dmtp_round.restype = C.c_int
+    lib.dmtp_round_host.argtypes = [P, P, P]
+    lib.dmtp_round_host.restype = C.c_int
+    lib.dmtp_read_state.argtypes = [P, P, P, P]
+    lib.dmtp_read_state.restype = C.c_int
+    lib.dmtp_round_launches.argtypes = [P]
+    lib.dmtp_round_launches.restype = C.c_int
+    lib.dmtp_round_profile.argtypes = [P, C.POINTER(dmtp_profile)]
+    lib.dmtp_round_profile.restype = C.c_int
+    lib.dmtp_free.argtypes = [P]
+    lib.dmtp_free.restype = None
+    lib.dmtp_strerror.argtypes = [C.c_int]
+    lib.dmtp_strerror.restype = C.c_char_p
+    _lib = lib
+    return lib
+
+
+class DmtpError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        msg = load_library().dmtp_strerror(code).decode()
+        super().__init__(f"{what}: {ERRORS.get(code, code)} ({msg})")
+        self.code = code
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        raise DmtpError(code, what)
+
+
+def make_config(cfg, max_ctx: int, max_batch: int | None = None) -> dmtp_config:
+    """dmtp_config from a synth.DmtpConfig."""
+    c = dmtp_config()
+    c.vocab, c.d_model, c.n_layers = cfg.vocab, cfg.d_model, cfg.n_layers
+    c.n_heads, c.n_kv_heads, c.head_dim, c.ffn = (cfg.n_heads, cfg.n_kv_heads, cfg.head_dim,
+                                                  cfg.ffn)
+    c.gdn_heads, c.gdn_dk, c.gdn_dv = cfg.gdn_heads, cfg.gdn_dk, cfg.gdn_dv
+    for l, k in enumerate(cfg.layer_kinds):
+        c.layer_kind[l] = k
+    c.draft_layers, c.draft_window = cfg.draft_layers, cfg.draft_window
+    c.n_taps = cfg.n_taps
+    for i, t in enumerate(cfg.taps):
+        c.tap_layers[i] = t
+    c.mask_id = cfg.mask_id
+    c.rms_eps, c.rope_theta = cfg.rms_eps, cfg.rope_theta
+    c.max_ctx = max_ctx
+    c.max_batch = cfg.batch if max_batch is None else max_batch
+    c.dtype = 0 if cfg.dtype == "fp32" else 1
+    return c
+
+
+def _ptr(t) -> int:
+    return t.data_ptr()
+
+
+def make_weights(cfg, w: dict) -> dmtp_weights:
+    """dmtp_weights of device pointers from the synth weight dict (tensors on CUDA)."""
+    s = dmtp_weights()
+    s.emb, s.head, s.final_norm = _ptr(w["emb"]), _ptr(w["head"]), _ptr(w["final_norm"])
+
+    def fill(dst, pfx):
+        for f in _LAYER_FIELDS:
+            k = f"{pfx}.{f}"
+            setattr(dst, f, _ptr(w[k]) if k in w else None)
+
+    for l in range(cfg.n_layers):
+        fill(s.layers[l], f"L{l}")
+    s.mtp_norm_h, s.mtp_norm_e, s.mtp_proj = (_ptr(w["mtp.norm_h"]), _ptr(w["mtp.norm_e"]),
+                                              _ptr(w["mtp.proj"]))
+    fill(s.mtp, "mtp")
+    s.mtp_final_norm = _ptr(w["mtp.final_norm"])
+    s.fuse_norm_e, s.fuse_norm_m, s.fuse_w = (_ptr(w["fuse.norm_e"]), _ptr(w["fuse.norm_m"]),
+                                              _ptr(w["fuse.w"]))
+    s.dft_fc, s.dft_norm_c = _ptr(w["dft.fc"]), _ptr(w["dft.norm_c"])
+    for j in range(cfg.draft_layers):
+        fill(s.dft[j], f"D{j}")
+    s.dft_final_norm = _ptr(w["dft.final_norm"])
+    return s
+
+
+def default_max_ctx(prompts, rounds: int) -> int:
+    return max(len(p) for p in prompts) + 8 * (rounds + 4) + 32
+
+
+class DmtpRound:
+    """One context of the round library: dmtp_init on construction (prefill),
+    dmtp_round per call, dmtp_free on close()."""
+
+    def __init__(self, cfg, weights: dict, prompts, max_ctx: int, stream=None):
+        import torch
+        self.lib = load_library()
+        self.cfg = cfg
+        self.B = len(prompts)
+        self.weights = weights  # keep the tensors alive
+        self.ccfg = make_config(cfg, max_ctx, max_batch=self.B)
+        self.cw = make_weights(cfg, weights)
+        nbytes = C.c_size_t()
+        _check(self.lib.dmtp_workspace_size(C.byref(self.ccfg), self.B, C.byref(nbytes)),
+               "dmtp_workspace_size")
+        dev = weights["emb"].device
+        self.workspace = torch.empty(nbytes.value, dtype=torch.uint8, device=dev)
+        ids = np.ascontiguousarray(np.concatenate([np.asarray(p, np.int32) for p in prompts]))
+        lens = np.ascontiguousarray(np.array([len(p) for p in prompts], np.int32))
+        self.stream = stream if stream is not None else torch.cuda.current_stream(dev)
+        ctx = C.c_void_p()
+        _check(self.lib.dmtp_init(C.byref(self.ccfg), C.byref(self.cw),
+                                  C.c_void_p(self.workspace.data_ptr()), nbytes.value,
+                                  ids.ctypes.data_as(C.c_void_p), lens.ctypes.data_as(C.c_void_p),
+                                  self.B, C.c_void_p(self.stream.cuda_stream), C.byref(ctx)),
+               "dmtp_init")
+        self.ctx = ctx
+        self.device = dev
+
+    # ---- rounds ----------------------------------------------------------------------
+    def round(self, out: dict | None = None, forced=None):
+        """Enqueue one round. out: name -> preallocated CUDA tensor (fields of
+        dmtp_round_out); forced: CUDA int32 [B, 7] or None."""
+        o = dmtp_round_out()
+        if out:
+            for k, t in out.items():
+                setattr(o, k, t.data_ptr())
+        f = C.c_void_p(forced.data_ptr()) if forced is not None else None
+        _check(self.lib.dmtp_round(self.ctx, C.byref(o), f), "dmtp_round")
+
+    def alloc_out(self, ints=True, floats=False):
+        import torch
+        B, V, d = self.B, self.cfg.vocab, self.cfg.d_model
+        dev = self.device
+        shapes = {"committed": (B, 8), "n_accepted": (B,), "drafts": (B, 7), "picks": (B, 8),
+                  "kv_len": (B,), "mtp_len": (B,), "snap_slot": (B,)}
+        out = {}
+        if ints:
+            for k, s in shapes.items():
+                out[k] = torch.empty(s, dtype=torch.int32, device=dev)
+        if floats:
+            fs = {"t1_logits": (B, V), "draft_logits": (B, 6, V), "verify_logits": (B, 8, V),
+                  "delta": (B, d), "h_mtp": (B, d)}
+            for k, s in fs.items():
+                out[k] = torch.empty(s, dtype=torch.float32, device=dev)
+        return out
+
+    def round_host(self, committed: np.ndarray | None = None, n_acc: np.ndarray | None = None):
+        """One round with host outputs (pinned or pageable numpy int32 arrays)."""
+        cp = committed.ctypes.data_as(C.c_void_p) if committed is not None else None
+        npt = n_acc.ctypes.data_as(C.c_void_p) if n_acc is not None else None
+        _check(self.lib.dmtp_round_host(self.ctx, cp, npt), "dmtp_round_host")
+
+    def read_state(self):
+        kv = np.zeros(self.B, np.int32)
+        A = np.zeros(self.B, np.int32)
+        hist = np.zeros(8, np.uint64)
+        _check(self.lib.dmtp_read_state(self.ctx, kv.ctypes.data_as(C.c_void_p),
+                                        A.ctypes.data_as(C.c_void_p),
+                                        hist.ctypes.data_as(C.c_void_p)), "dmtp_read_state")
+        return kv, A, hist
+
+    def profile_round(self) -> dict:
+        """One real round with CUDA events around every launch: per kernel class the
+        summed device ms, algorithmic bytes and flops, and the launch count."""
+        p = dmtp_profile()
+        _check(self.lib.dmtp_round_profile(self.ctx, C.byref(p)), "dmtp_round_profile")
+        out = {"round_ms": p.round_ms}
+        for i, name in enumerate(PROFILE_CLASSES):
+            out[name] = {"ms": p.ms[i], "bytes": p.bytes[i], "flops": p.flops[i],
+                         "launches": p.launches[i]}
+        return out
+
+    def launches_per_round(self) -> int:
+        return int(self.lib.dmtp_round_launches(self.ctx))
+
+    def close(self):
+        if getattr(self, "ctx", None):
+            self.lib.dmtp_free(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

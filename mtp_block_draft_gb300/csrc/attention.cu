@@ -1,0 +1,147 @@
+// Split-K decode attention for the 8 rows of a round against a per-sequence KV cache.
+//
+// One CTA per (KV chunk, kv head, sequence) computes, for all 8 rows x the GQA group of
+// query heads that share the kv head, a partial softmax (running max m, sum l and the
+// unnormalised P.V) over its chunk of keys, so each cached K/V byte is read once per
+// sequence and layer. A merge kernel combines the chunks.
+//
+// Visibility (DMTP blog §6.2 "Attention: One Backend, Different Visibility Rules"):
+//   target verify and MTP rows are causal: row s sees keys lo..base+s;
+//   the block drafter sees the anchor-relative window max(0, base-4096)..base-1 plus all
+//   8 block keys (no mask inside the block: DFlash's block-diagonal mask).
+// Cache layout [B][hkv][max_ctx][hd]; scores scaled by 1/sqrt(hd); softmax in fp32.
+#include "common.cuh"
+#include "ops.h"
+
+namespace dmtp {
+
+static constexpr int kTK = 32;      // keys per shared-memory tile
+static constexpr int kMaxDPT = 32;  // max head dims per thread
+
+template <typename T>
+__global__ void __launch_bounds__(256) k_attn_partial(AttnArgs a) {
+  __shared__ float Ks[kTK][128];
+  __shared__ float Vs[kTK][128];
+  const int chunk_id = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int grp = a.hq / a.hkv, QN = 8 * grp, hd = a.hd;
+  const int base = a.base[b];
+  int lo = a.lo_fixed;
+  if (a.window > 0) lo = max(lo, base - a.window);
+  const int hi_max = base + 7;
+  const int k_begin = lo + chunk_id * a.chunk;
+  const int k_end = min(k_begin + a.chunk, hi_max + 1);
+  const long pidx = ((long)b * a.hkv + g) * a.nchunk + chunk_id;
+  float* pml = a.part_ml + pidx * QN * 2;
+  float* po = a.part_o + pidx * QN * hd;
+  if (k_begin >= k_end) return;  // the merge reads only chunks that hold keys
+
+  const int TPQ = 256 / QN;  // threads per query
+  const int DPT = hd / TPQ;  // head dims per thread, interleaved: dim = sub + TPQ * i
+  const int qi = threadIdx.x / TPQ, sub = threadIdx.x % TPQ;
+  const int s = qi / grp, hh = qi % grp, h = g * grp + hh;
+  const int row_hi = a.causal ? base + s : hi_max;
+  const float scale = rsqrtf((float)hd);
+
+  float qr[kMaxDPT], acc[kMaxDPT];
+  const T* qp = (const T*)a.q + ((long)(b * 8 + s) * a.hq + h) * hd;
+#pragma unroll
+  for (int i = 0; i < kMaxDPT; ++i) {
+    qr[i] = (i < DPT) ? to_f32(qp[sub + TPQ * i]) * scale : 0.f;
+    acc[i] = 0.f;
+  }
+  float m = -INFINITY, l = 0.f;
+  const T* Kb = (const T*)a.Kc + ((long)b * a.hkv + g) * a.max_ctx * hd;
+  const T* Vb = (const T*)a.Vc + ((long)b * a.hkv + g) * a.max_ctx * hd;
+
+  for (int kt = k_begin; kt < k_end; kt += kTK) {
+    const int nk = min(kTK, k_end - kt);
+    __syncthreads();
+    for (int e = threadIdx.x; e < kTK * hd; e += blockDim.x) {
+      const int j = e / hd, dd = e % hd;
+      float kv = 0.f, vv = 0.f;
+      if (j < nk) {
+        kv = to_f32(Kb[(long)(kt + j) * hd + dd]);
+        vv = to_f32(Vb[(long)(kt + j) * hd + dd]);
+      }
+      Ks[j][dd] = kv;
+      Vs[j][dd] = vv;
+    }
+    __syncthreads();
+    float sc[kTK];
+    float mt = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kTK; ++j) {
+      float p = 0.f;
+#pragma unroll
+      for (int i = 0; i < kMaxDPT; ++i)
+        if (i < DPT) p += qr[i] * Ks[j][sub + TPQ * i];
+      for (int o = TPQ >> 1; o > 0; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
+      const bool vis = (j < nk) && (kt + j <= row_hi);
+      sc[j] = vis ? p : -INFINITY;
+      mt = fmaxf(mt, sc[j]);
+    }
+    const float m_new = fmaxf(m, mt);
+    if (m_new == -INFINITY) continue;
+    const float corr = __expf(m - m_new);
+    l *= corr;
+#pragma unroll
+    for (int i = 0; i < kMaxDPT; ++i) acc[i] *= corr;
+#pragma unroll
+    for (int j = 0; j < kTK; ++j) {
+      const float p = __expf(sc[j] - m_new);
+      l += p;
+#pragma unroll
+      for (int i = 0; i < kMaxDPT; ++i)
+        if (i < DPT) acc[i] += p * Vs[j][sub + TPQ * i];
+    }
+    m = m_new;
+  }
+#pragma unroll
+  for (int i = 0; i < kMaxDPT; ++i)
+    if (i < DPT) po[(long)qi * hd + sub + TPQ * i] = acc[i];
+  if (sub == 0) {
+    pml[qi * 2] = m;
+    pml[qi * 2 + 1] = l;
+  }
+}
+
+template <typename T>
+__global__ void k_attn_merge(AttnArgs a) {
+  const int mrow = blockIdx.x, h = blockIdx.y;
+  const int b = mrow >> 3, s = mrow & 7;
+  const int grp = a.hq / a.hkv, g = h / grp, hh = h % grp, qi = s * grp + hh, QN = 8 * grp;
+  const int base = a.base[b];
+  int lo = a.lo_fixed;
+  if (a.window > 0) lo = max(lo, base - a.window);
+  const int nact = max(1, min(a.nchunk, (base + 8 - lo + a.chunk - 1) / a.chunk));
+  const long p0 = ((long)b * a.hkv + g) * a.nchunk;
+  float M = -INFINITY;
+  for (int c = 0; c < nact; ++c) M = fmaxf(M, a.part_ml[((p0 + c) * QN + qi) * 2]);
+  float L = 0.f;
+  for (int c = 0; c < nact; ++c) {
+    const float mc = a.part_ml[((p0 + c) * QN + qi) * 2];
+    L += a.part_ml[((p0 + c) * QN + qi) * 2 + 1] * __expf(mc - M);
+  }
+  const float invL = 1.f / L;
+  for (int dd = threadIdx.x; dd < a.hd; dd += blockDim.x) {
+    float o = 0.f;
+    for (int c = 0; c < nact; ++c) {
+      const float mc = a.part_ml[((p0 + c) * QN + qi) * 2];
+      o += a.part_o[((p0 + c) * QN + qi) * a.hd + dd] * __expf(mc - M);
+    }
+    ((T*)a.out)[(long)mrow * a.hq * a.hd + h * a.hd + dd] = from_f32<T>(o * invL);
+  }
+}
+
+void op_attention(int dt, const AttnArgs& a, cudaStream_t st) {
+  dim3 g1(a.nchunk, a.hkv, a.B), g2(a.B * 8, a.hq);
+  if (dt) {
+    k_attn_partial<bf16><<<g1, 256, 0, st>>>(a);
+    k_attn_merge<bf16><<<g2, 128, 0, st>>>(a);
+  } else {
+    k_attn_partial<float><<<g1, 256, 0, st>>>(a);
+    k_attn_merge<float><<<g2, 128, 0, st>>>(a);
+  }
+}
+
+}  // namespace dmtp

@@ -1,0 +1,875 @@
+// Host side of the DMTP round library: the C ABI declared in include/dmtp.h.
+//
+// Owns no device memory: every buffer is carved out of the caller's workspace.
+// dmtp_init lays out the workspace, builds the tcgen05 GEMM plans (TMA tensor maps)
+// and runs the prefill; dmtp_round enqueues steps a1-a6 and, when no debug output is
+// requested, replays them as one captured CUDA graph (DMTP blog §6.4: prepare data on
+// the device, update fixed buffers, replay the graph). All per-sequence metadata
+// (positions, accepted lengths, snapshot slots) stays on the device; the host never
+// reads a length during normal rounds.
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <vector>
+
+#include "../../include/dmtp.h"
+#include "ops.h"
+
+using namespace dmtp;
+
+namespace {
+
+struct Gemm {
+  TcPlan tc;            // bf16 path
+  const void* W = nullptr;
+  const void* X = nullptr;
+  int N = 0, K = 0, M = 0;
+  bool argmax = false;
+};
+
+struct LayerPlans {
+  Gemm qkv, o, gu, down;       // attention (and MLP)
+  Gemm gq, ga, gb, go;         // Gated DeltaNet projections
+};
+
+}  // namespace
+
+struct dmtp_ctx {
+  dmtp_config cfg;
+  dmtp_weights w;
+  int B, M, dt, nsm;
+  cudaStream_t st;
+  int d, V, F, hq, hkv, hd, qd, kvd, qkvd, maxc, Ld, L, ntap;
+  int gH, gdk, gdv, gld, n_gdn;
+  int gdn_index[DMTP_MAX_LAYERS];
+  int tap_of_layer[DMTP_MAX_LAYERS];  // tap slot of layer l, or -1
+  int pmax;
+  int attn_chunk, attn_nchunk;
+  size_t ws_bytes;
+
+  // workspace regions
+  void* tK[DMTP_MAX_LAYERS];
+  void* tV[DMTP_MAX_LAYERS];
+  float* gstate[DMTP_MAX_LAYERS];
+  void* dK[DMTP_MAX_DRAFT_LAYERS];
+  void* dV[DMTP_MAX_DRAFT_LAYERS];
+  void *mK, *mV;
+  float2* rope;
+  float* x;
+  void* xn;
+  float* qkv;
+  void* q;
+  float *part_o, *part_ml;
+  void* att;
+  float* gu;
+  void* hmid;
+  void* taps;
+  float* hT32;
+  void* hTn;
+  void* z;
+  float* xm;
+  float* cacc;
+  void* cn;
+  float* delta;
+  float* h_mtp;
+  void* t1in;
+  void* dn;
+  float* hlast;
+  int* prompts;
+  int* plen;
+  int* forced;
+  RoundState rs;
+  unsigned* err;
+
+  // GEMM plans
+  LayerPlans tgt[DMTP_MAX_LAYERS];
+  LayerPlans dft[DMTP_MAX_DRAFT_LAYERS];
+  LayerPlans mtp;
+  Gemm dkv[DMTP_MAX_DRAFT_LAYERS];
+  Gemm fuse, head_t1, head_d, head_v, dfc, mproj;
+
+  cudaGraphExec_t graph;
+  bool poisoned;
+  long kv_bound;
+  int launches;
+  int round_launches;
+  // per-launch event profiling (dmtp_round_profile only)
+  bool prof;
+  std::vector<cudaEvent_t> pev;
+  std::vector<int> pcls;
+  std::vector<double> pbytes, pflops;
+  std::vector<int> kv_host;  // kv_len at the start of the profiled round
+};
+
+// ---------------------------------------------------------------------------------
+// workspace layout
+// ---------------------------------------------------------------------------------
+namespace {
+
+struct Bump {
+  char* base;
+  size_t off = 0;
+  template <typename T>
+  T* take(size_t bytes) {
+    off = (off + 255) & ~(size_t)255;
+    T* p = base ? (T*)(base + off) : nullptr;
+    off += bytes;
+    return p;
+  }
+};
+
+int derive(dmtp_ctx* c, const dmtp_config* cfg, int B) {
+  const dmtp_config& f = *cfg;
+  if (f.vocab < 2 || f.d_model < 32 || f.n_layers < 1 || f.n_layers > DMTP_MAX_LAYERS ||
+      f.draft_layers < 1 || f.draft_layers > DMTP_MAX_DRAFT_LAYERS || f.n_taps < 1 ||
+      f.n_taps > DMTP_MAX_TAPS || f.n_heads < 1 || f.n_kv_heads < 1 ||
+      f.n_heads % f.n_kv_heads || f.head_dim < 8 || f.head_dim > 128 || f.head_dim % 2 ||
+      f.ffn < 1 || f.max_ctx < 16 || B < 1 || B > f.max_batch || B * 8 > 256 ||
+      (f.dtype != 0 && f.dtype != 1) || f.mask_id < 0 || f.mask_id >= f.vocab ||
+      f.draft_window < 0)
+    return DMTP_EINVAL;
+  const int grp = f.n_heads / f.n_kv_heads;
+  const int QN = 8 * grp;
+  if (QN > 256 || 256 % QN || (f.head_dim * QN) % 256 || f.head_dim / (256 / QN) > 32 ||
+      (256 / QN) > 32)
+    return DMTP_EINVAL;
+  c->cfg = f;
+  c->B = B;
+  c->M = 8 * B;
+  c->dt = f.dtype;
+  c->d = f.d_model;
+  c->V = f.vocab;
+  c->F = f.ffn;
+  c->hq = f.n_heads;
+  c->hkv = f.n_kv_heads;
+  c->hd = f.head_dim;
+  c->qd = c->hq * c->hd;
+  c->kvd = c->hkv * c->hd;
+  c->qkvd = c->qd + 2 * c->kvd;
+  c->maxc = f.max_ctx;
+  c->L = f.n_layers;
+  c->Ld = f.draft_layers;
+  c->ntap = f.n_taps;
+  c->gH = f.gdn_heads;
+  c->gdk = f.gdn_dk;
+  c->gdv = f.gdn_dv;
+  c->n_gdn = 0;
+  for (int l = 0; l < c->L; ++l) {
+    c->tap_of_layer[l] = -1;
+    if (f.layer_kind[l] > 1) return DMTP_EINVAL;
+    c->gdn_index[l] = f.layer_kind[l] ? c->n_gdn++ : -1;
+  }
+  for (int i = 0; i < c->ntap; ++i) {
+    if (f.tap_layers[i] < 0 || f.tap_layers[i] >= c->L) return DMTP_EINVAL;
+    c->tap_of_layer[f.tap_layers[i]] = i;
+  }
+  if (c->n_gdn) {
+    if (c->gH < 1 || c->gdv < 8 || c->gdv > 256 || (c->gdv & (c->gdv - 1)) || c->gdk > 256 ||
+        c->gdk % (256 / c->gdv) || c->gdk / (256 / c->gdv) > 64)
+      return DMTP_EINVAL;
+  }
+  c->gld = c->n_gdn ? c->gH * (2 * c->gdk + c->gdv) + 2 * c->gH : 0;
+  if (c->dt == 1) {
+    // every GEMM reduction length must be a multiple of the 64-wide k block
+    const int ks[] = {c->d, c->qd, c->F, 2 * c->d, c->ntap * c->d, c->gH * c->gdv};
+    for (int k : ks)
+      if (k % 64) return DMTP_EINVAL;
+  }
+  c->attn_chunk = 256;
+  c->attn_nchunk = (c->maxc + 8 + c->attn_chunk - 1) / c->attn_chunk;
+  return DMTP_OK;
+}
+
+size_t layout(dmtp_ctx* c, char* base) {
+  Bump b{base};
+  const size_t es = c->dt ? 2 : 4;
+  const size_t kvsz = (size_t)c->B * c->hkv * c->maxc * c->hd * es;
+  for (int l = 0; l < c->L; ++l) {
+    c->tK[l] = c->tV[l] = nullptr;
+    c->gstate[l] = nullptr;
+    if (c->cfg.layer_kind[l] == 0) {
+      c->tK[l] = b.take<char>(kvsz);
+      c->tV[l] = b.take<char>(kvsz);
+    } else {
+      c->gstate[l] = b.take<float>((size_t)c->B * 8 * c->gH * c->gdv * c->gdk * 4);
+    }
+  }
+  for (int j = 0; j < c->Ld; ++j) {
+    c->dK[j] = b.take<char>(kvsz);
+    c->dV[j] = b.take<char>(kvsz);
+  }
+  c->mK = b.take<char>(kvsz);
+  c->mV = b.take<char>(kvsz);
+  c->rope = b.take<float2>((size_t)(c->maxc + 16) * (c->hd / 2) * sizeof(float2));
+  const size_t M = c->M, d = c->d, B = c->B;
+  const int qkvw = std::max(std::max(c->qkvd, c->gld), 2 * c->kvd);
+  c->x = b.take<float>(M * d * 4);
+  c->xn = b.take<char>(M * d * es);
+  c->qkv = b.take<float>(M * qkvw * 4);
+  c->q = b.take<char>(M * c->qd * es);
+  const int QN = 8 * (c->hq / c->hkv);
+  c->part_o = b.take<float>(B * c->hkv * c->attn_nchunk * QN * c->hd * 4);
+  c->part_ml = b.take<float>(B * c->hkv * c->attn_nchunk * QN * 2 * 4);
+  c->att = b.take<char>(M * std::max(c->qd, c->gH * c->gdv) * es);
+  c->gu = b.take<float>(M * 2 * c->F * 4);
+  c->hmid = b.take<char>(M * c->F * es);
+  c->taps = b.take<char>(M * c->ntap * d * es);
+  c->hT32 = b.take<float>(M * d * 4);
+  c->hTn = b.take<char>(M * d * es);
+  c->z = b.take<char>(M * 2 * d * es);
+  c->xm = b.take<float>(M * d * 4);
+  c->cacc = b.take<float>(M * d * 4);
+  c->cn = b.take<char>(M * d * es);
+  c->delta = b.take<float>(B * d * 4);
+  c->h_mtp = b.take<float>(B * d * 4);
+  c->t1in = b.take<char>(B * d * es);
+  c->dn = b.take<char>(6 * B * d * es);
+  c->hlast = b.take<float>(B * d * 4);
+  c->forced = b.take<int>(B * 7 * 4);
+  RoundState& s = c->rs;
+  s.kv_len = b.take<int>(B * 4);
+  s.pos0 = b.take<int>(B * 4);
+  s.A = b.take<int>(B * 4);
+  s.drafts = b.take<int>(B * 7 * 4);
+  s.g = b.take<int>(B * 8 * 4);
+  s.n_acc = b.take<int>(B * 4);
+  s.committed = b.take<int>(B * 8 * 4);
+  s.tok = b.take<int>(M * 4);
+  s.mtp_tok = b.take<int>(M * 4);
+  s.mtp_base = b.take<int>(B * 4);
+  s.mtp_cnt = b.take<int>(B * 4);
+  s.rows_valid = b.take<int>(B * 4);
+  s.snap_slot = b.take<int>(B * 4);
+  s.mtp_len = b.take<int>(B * 4);
+  s.hist = b.take<unsigned long long>(8 * 8);
+  s.keys = b.take<unsigned long long>(B * 16 * 8);
+  s.gdn_live = b.take<int>((size_t)std::max(1, c->n_gdn) * B * 4);
+  s.gdn_slot = b.take<int>((size_t)std::max(1, c->n_gdn) * B * 8 * 4);
+  s.n_gdn = c->n_gdn;
+  s.B = c->B;
+  c->err = b.take<unsigned>(256);
+  s.err = c->err;
+  c->plen = b.take<int>(B * 4);
+  return b.off;
+}
+
+// prompts are staged after the fixed layout (size depends on the prompt lengths)
+size_t prompt_bytes(int B, int pmax) { return ((size_t)B * pmax * 4 + 255) & ~(size_t)255; }
+
+int plan(dmtp_ctx* c, Gemm& g, const void* W, int N, int K, const void* X, int M, bool argmax) {
+  g.W = W;
+  g.X = X;
+  g.N = N;
+  g.K = K;
+  g.M = M;
+  g.argmax = argmax;
+  if (!W) return DMTP_EINVAL;
+  if (c->dt == 1) return tc_plan(&g.tc, W, N, K, X, M, c->nsm, argmax) ? DMTP_EINVAL : DMTP_OK;
+  return DMTP_OK;
+}
+
+int plan_layer(dmtp_ctx* c, LayerPlans& p, const dmtp_layer_weights& w, int kind, int M) {
+  int r = 0;
+  if (!w.attn_norm || !w.mlp_norm) return DMTP_EINVAL;
+  if (kind == 0) {
+    r |= plan(c, p.qkv, w.wqkv, c->qkvd, c->d, c->xn, M, false);
+    r |= plan(c, p.o, w.wo, c->d, c->qd, c->att, M, false);
+  } else {
+    r |= plan(c, p.gq, w.gdn_wqkv, c->gH * (2 * c->gdk + c->gdv), c->d, c->xn, M, false);
+    r |= plan(c, p.ga, w.gdn_wa, c->gH, c->d, c->xn, M, false);
+    r |= plan(c, p.gb, w.gdn_wb, c->gH, c->d, c->xn, M, false);
+    r |= plan(c, p.go, w.gdn_wo, c->d, c->gH * c->gdv, c->att, M, false);
+  }
+  r |= plan(c, p.gu, w.wgu, 2 * c->F, c->d, c->xn, M, false);
+  r |= plan(c, p.down, w.wdown, c->d, c->F, c->hmid, M, false);
+  return r ? DMTP_EINVAL : DMTP_OK;
+}
+
+// ---------------------------------------------------------------------------------
+// enqueue helpers
+// ---------------------------------------------------------------------------------
+enum { P_GEMM = 0, P_HEAD = 1, P_ATTN = 2, P_GDN = 3, P_OTHER = 4 };
+
+// Wraps one launch: counts it and, when profiling, brackets it with CUDA events on
+// the launching stream and records its class and algorithmic bytes / flops.
+template <typename F>
+inline void launch(dmtp_ctx* c, int cls, double bytes, double flops, F&& f) {
+  if (c->prof) {
+    const size_t i = c->pcls.size();
+    while (c->pev.size() < 2 * (i + 1)) {
+      cudaEvent_t e;
+      cudaEventCreate(&e);
+      c->pev.push_back(e);
+    }
+    cudaEventRecord(c->pev[2 * i], c->st);
+    f();
+    cudaEventRecord(c->pev[2 * i + 1], c->st);
+    c->pcls.push_back(cls);
+    c->pbytes.push_back(bytes);
+    c->pflops.push_back(flops);
+  } else {
+    f();
+  }
+  c->launches += 1;
+}
+
+inline double esz(const dmtp_ctx* c) { return c->dt ? 2.0 : 4.0; }
+
+// algorithmic bytes of out[M,N] (+)= X[M,K] W[N,K]^T: weights and tokens read once,
+// the fp32 output read and written once
+void gemm_acc(dmtp_ctx* c, const Gemm& g, float* out, int ldo) {
+  const double bytes = ((double)g.N * g.K + (double)g.M * g.K) * esz(c) + 8.0 * g.M * g.N;
+  launch(c, P_GEMM, bytes, 2.0 * g.M * g.N * g.K, [&] {
+    if (c->dt == 1)
+      op_gemm_tc_acc(g.tc, out, ldo, c->err, c->st);
+    else
+      op_gemm_simt_acc((const float*)g.W, (const float*)g.X, g.N, g.K, g.M, out, ldo, c->st);
+  });
+}
+
+void gemm_argmax(dmtp_ctx* c, const Gemm& g, unsigned long long* keys, float* logits) {
+  const double bytes = ((double)g.N * g.K + (double)g.M * g.K) * esz(c) + 8.0 * g.M;
+  launch(c, P_HEAD, bytes, 2.0 * g.M * g.N * g.K, [&] {
+    if (c->dt == 1)
+      op_gemm_tc_argmax(g.tc, keys, logits, c->V, c->err, c->st);
+    else
+      op_gemm_simt_argmax((const float*)g.W, (const float*)g.X, g.N, g.K, g.M, keys, logits,
+                          c->V, c->st);
+  });
+}
+
+void zero(dmtp_ctx* c, void* p, size_t bytes) { cudaMemsetAsync(p, 0, bytes, c->st); }
+
+void norm(dmtp_ctx* c, const float* x, const void* g, void* y, float* y32, void* tap, int rows,
+          RowMap map = RowMap()) {
+  launch(c, P_OTHER, 0, 0, [&] {
+    op_rmsnorm(c->dt, x, c->d, g, y, c->d, y32, c->d, tap, c->ntap * c->d, rows, c->d,
+               c->cfg.rms_eps, map, c->st);
+  });
+}
+
+void* tap_ptr(dmtp_ctx* c, int slot) {
+  if (slot < 0) return nullptr;
+  return (char*)c->taps + (size_t)slot * c->d * (c->dt ? 2 : 4);
+}
+
+struct AttnSpec {
+  void *Kc, *Vc;
+  const int* base;
+  int causal, lo_fixed, window;
+  int mode_base;  // 1: base = kv_len at round start (target, drafter); 2: kv_len + 1 (MTP)
+};
+
+void attn_layer(dmtp_ctx* c, const LayerPlans& p, const dmtp_layer_weights& w, float* xr,
+                const AttnSpec& a, void* tap_in) {
+  const int M = c->M;
+  norm(c, xr, w.attn_norm, c->xn, nullptr, tap_in, M);
+  zero(c, c->qkv, (size_t)M * c->qkvd * 4);
+  gemm_acc(c, p.qkv, c->qkv, c->qkvd);
+  launch(c, P_OTHER, 0, 0, [&] { op_rope_kv(c->dt, c->qkv, c->qkvd, 0, c->qd, c->qd + c->kvd, c->q, a.Kc, a.Vc, a.base, c->rope,
+             M, c->hq, c->hkv, c->hd, c->maxc, c->err, c->st); });
+  AttnArgs aa;
+  aa.Kc = a.Kc;
+  aa.Vc = a.Vc;
+  aa.q = c->q;
+  aa.part_o = c->part_o;
+  aa.part_ml = c->part_ml;
+  aa.out = c->att;
+  aa.base = a.base;
+  aa.causal = a.causal;
+  aa.lo_fixed = a.lo_fixed;
+  aa.window = a.window;
+  aa.B = c->B;
+  aa.hq = c->hq;
+  aa.hkv = c->hkv;
+  aa.hd = c->hd;
+  aa.max_ctx = c->maxc;
+  aa.chunk = c->attn_chunk;
+  aa.nchunk = c->attn_nchunk;
+  double kv_bytes = 0;
+  if (c->prof) {
+    // keys each sequence's rows can see: lo .. base+7, K and V, all kv heads
+    for (int b = 0; b < c->B; ++b) {
+      const int a0 = c->kv_host[b];
+      const int base = a.mode_base == 2 ? a0 + 1 : a0;
+      int lo = a.lo_fixed;
+      if (a.window > 0) lo = std::max(lo, base - a.window);
+      kv_bytes += (double)(base + 8 - lo) * c->kvd * esz(c) * 2;
+    }
+    kv_bytes += (double)c->M * c->qd * esz(c) * 2;  // q in, o out
+  }
+  launch(c, P_ATTN, kv_bytes, 0, [&] { op_attention(c->dt, aa, c->st); });
+  c->launches += 1;  // partial + merge
+  gemm_acc(c, p.o, xr, c->d);
+  norm(c, xr, w.mlp_norm, c->xn, nullptr, nullptr, M);
+  zero(c, c->gu, (size_t)M * 2 * c->F * 4);
+  gemm_acc(c, p.gu, c->gu, 2 * c->F);
+  launch(c, P_OTHER, 0, 0, [&] { op_swiglu(c->dt, c->gu, c->hmid, M, c->F, c->st); });
+  gemm_acc(c, p.down, xr, c->d);
+}
+
+void gdn_layer(dmtp_ctx* c, int l, float* xr, void* tap_in, bool snapshots) {
+  const LayerPlans& p = c->tgt[l];
+  const dmtp_layer_weights& w = c->w.layers[l];
+  const int M = c->M, gi = c->gdn_index[l];
+  const int nqkv = c->gH * (2 * c->gdk + c->gdv);
+  norm(c, xr, w.attn_norm, c->xn, nullptr, tap_in, M);
+  zero(c, c->qkv, (size_t)M * c->gld * 4);
+  gemm_acc(c, p.gq, c->qkv, c->gld);
+  gemm_acc(c, p.ga, c->qkv + nqkv, c->gld);
+  gemm_acc(c, p.gb, c->qkv + nqkv + c->gH, c->gld);
+  GdnArgs ga;
+  ga.qkvab = c->qkv;
+  ga.ld = c->gld;
+  ga.states = c->gstate[l];
+  ga.live = c->rs.gdn_live + (size_t)gi * c->B;
+  ga.slot = c->rs.gdn_slot + (size_t)gi * c->B * 8;
+  ga.rows_valid = c->rs.rows_valid;
+  ga.snapshots = snapshots ? 1 : 0;
+  ga.out = c->att;
+  ga.B = c->B;
+  ga.H = c->gH;
+  ga.dk = c->gdk;
+  ga.dv = c->gdv;
+  ga.err = c->err;
+  const double st_bytes = (double)c->B * c->gH * c->gdv * c->gdk * 4 * (snapshots ? 9 : 2);
+  launch(c, P_GDN, st_bytes, 0, [&] { op_gdn(c->dt, ga, c->st); });
+  gemm_acc(c, p.go, xr, c->d);
+  norm(c, xr, w.mlp_norm, c->xn, nullptr, nullptr, M);
+  zero(c, c->gu, (size_t)M * 2 * c->F * 4);
+  gemm_acc(c, p.gu, c->gu, 2 * c->F);
+  launch(c, P_OTHER, 0, 0, [&] { op_swiglu(c->dt, c->gu, c->hmid, M, c->F, c->st); });
+  gemm_acc(c, p.down, xr, c->d);
+}
+
+// target forward over the 8 rows of every sequence (tokens in rs.tok, positions pos0+s);
+// leaves the final-normed hidden in hT32 (fp32) and hTn (operand type), taps filled.
+void target_forward(dmtp_ctx* c, bool snapshots) {
+  const int M = c->M;
+  launch(c, P_OTHER, 0, 0, [&] { op_embed(c->dt, c->w.emb, c->rs.tok, c->V, c->x, M, c->d, c->err, c->st); });
+  for (int l = 0; l < c->L; ++l) {
+    void* tap_in = l > 0 ? tap_ptr(c, c->tap_of_layer[l - 1]) : nullptr;
+    if (c->cfg.layer_kind[l] == 0) {
+      AttnSpec a{c->tK[l], c->tV[l], c->rs.pos0, 1, 0, 0, 1};
+      attn_layer(c, c->tgt[l], c->w.layers[l], c->x, a, tap_in);
+    } else {
+      gdn_layer(c, l, c->x, tap_in, snapshots);
+    }
+  }
+  norm(c, c->x, c->w.final_norm, c->hTn, c->hT32, tap_ptr(c, c->tap_of_layer[c->L - 1]), M);
+}
+
+// a6 (and each prefill chunk): drafter context K/V at positions pos0+s from the taps,
+// then the MTP rows (token mtp_tok, hidden hT32 row) at positions mtp_base+s.
+void drafter_ctx(dmtp_ctx* c) {
+  const int M = c->M;
+  zero(c, c->cacc, (size_t)M * c->d * 4);
+  gemm_acc(c, c->dfc, c->cacc, c->d);
+  norm(c, c->cacc, c->w.dft_norm_c, c->cn, nullptr, nullptr, M);
+  for (int j = 0; j < c->Ld; ++j) {
+    zero(c, c->qkv, (size_t)M * 2 * c->kvd * 4);
+    gemm_acc(c, c->dkv[j], c->qkv, 2 * c->kvd);
+    launch(c, P_OTHER, 0, 0, [&] { op_rope_kv(c->dt, c->qkv, 2 * c->kvd, -1, 0, c->kvd, nullptr, c->dK[j], c->dV[j],
+               c->rs.pos0, c->rope, M, c->hq, c->hkv, c->hd, c->maxc, c->err, c->st); });
+  }
+}
+
+void mtp_advance(dmtp_ctx* c) {
+  const int M = c->M;
+  ConcatPart ph, pe;
+  ph.src32 = c->hT32;
+  ph.ld = c->d;
+  ph.g = c->w.mtp_norm_h;
+  pe.tok = c->rs.mtp_tok;
+  pe.g = c->w.mtp_norm_e;
+  launch(c, P_OTHER, 0, 0, [&] { op_concat_rms2(c->dt, c->w.emb, c->V, ph, pe, c->z, M, c->d, c->cfg.rms_eps, c->err, c->st); });
+  zero(c, c->xm, (size_t)M * c->d * 4);
+  gemm_acc(c, c->mproj, c->xm, c->d);
+  AttnSpec a{c->mK, c->mV, c->rs.mtp_base, 1, 1, 0, 2};
+  attn_layer(c, c->mtp, c->w.mtp, c->xm, a, nullptr);
+  launch(c, P_OTHER, 0, 0, [&] { op_gather_hmtp(c->xm, c->rs.mtp_cnt, c->h_mtp, c->B, c->d, c->st); });
+}
+
+struct Dbg {
+  float *t1, *dl, *vl;
+};
+
+void enqueue_round(dmtp_ctx* c, const Dbg& dbg, const int* forced) {
+  RoundState& s = c->rs;
+  const int B = c->B;
+  launch(c, P_OTHER, 0, 0, [&] { op_round_begin(s, c->st); });
+  // a1: T1 from the cached MTP hidden
+  norm(c, c->h_mtp, c->w.mtp_final_norm, c->t1in, nullptr, nullptr, B);
+  gemm_argmax(c, c->head_t1, s.keys, dbg.t1);
+  launch(c, P_OTHER, 0, 0, [&] { op_keys_to_ids(s.keys, B, 1, s.drafts, 7, 0, forced, 7, 0, c->st); });
+  // a2: Delta = W [RMS_e(E(T1)); RMS_m(h_MTP)]; slots [E(A), E(T1)+Delta, E(MASK) x 6]
+  ConcatPart pe, pm;
+  pe.tok = s.drafts;  // T1 of sequence b is drafts[b*7]
+  pe.tok_stride = 7;
+  pe.g = c->w.fuse_norm_e;
+  pm.src32 = c->h_mtp;
+  pm.ld = c->d;
+  pm.g = c->w.fuse_norm_m;
+  launch(c, P_OTHER, 0, 0, [&] { op_concat_rms2(c->dt, c->w.emb, c->V, pe, pm, c->z, B, c->d, c->cfg.rms_eps, c->err, c->st); });
+  zero(c, c->delta, (size_t)B * c->d * 4);
+  gemm_acc(c, c->fuse, c->delta, c->d);
+  launch(c, P_OTHER, 0, 0, [&] { op_build_slots(c->dt, c->w.emb, c->V, s.A, s.drafts, c->delta, c->cfg.mask_id, c->x, B, c->d,
+                 c->err, c->st); });
+  // a3: block drafter over the 8 slots
+  for (int j = 0; j < c->Ld; ++j) {
+    AttnSpec a{c->dK[j], c->dV[j], s.pos0, 0, 0, c->cfg.draft_window, 1};
+    attn_layer(c, c->dft[j], c->w.dft[j], c->x, a, nullptr);
+  }
+  RowMap m6;
+  m6.out_group = 6;
+  m6.in_group = 8;
+  m6.in_offset = 2;
+  norm(c, c->x, c->w.dft_final_norm, c->dn, nullptr, nullptr, 6 * B, m6);
+  gemm_argmax(c, c->head_d, s.keys + B, dbg.dl);
+  launch(c, P_OTHER, 0, 0, [&] { op_keys_to_ids(s.keys + B, B, 6, s.drafts, 7, 1, forced, 7, 1, c->st); });
+  // a4: target verify of [A, T1..T7]
+  launch(c, P_OTHER, 0, 0, [&] { op_verify_tokens(s, c->st); });
+  target_forward(c, true);
+  gemm_argmax(c, c->head_v, s.keys + 7 * B, dbg.vl);
+  launch(c, P_OTHER, 0, 0, [&] { op_keys_to_ids(s.keys + 7 * B, B, 8, s.g, 8, 0, nullptr, 0, 0, c->st); });
+  // a5: prefix acceptance, commit, watermarks, snapshot swap
+  launch(c, P_OTHER, 0, 0, [&] { op_accept(s, c->st); });
+  // a6: drafter context and MTP advance over the committed rows
+  drafter_ctx(c);
+  mtp_advance(c);
+}
+
+int check_err(dmtp_ctx* c) {
+  unsigned e = 0;
+  if (cudaMemcpyAsync(&e, c->err, 4, cudaMemcpyDeviceToHost, c->st) != cudaSuccess)
+    return DMTP_ECUDA;
+  if (cudaStreamSynchronize(c->st) != cudaSuccess) return DMTP_ECUDA;
+  if (e) {
+    c->poisoned = true;
+    return DMTP_EDEVICE;
+  }
+  return DMTP_OK;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------------
+// C ABI
+// ---------------------------------------------------------------------------------
+extern "C" {
+
+int dmtp_workspace_size(const dmtp_config* cfg, int batch, size_t* bytes) {
+  if (!cfg || !bytes) return DMTP_EINVAL;
+  dmtp_ctx* c = new dmtp_ctx();
+  int r = derive(c, cfg, batch);
+  if (r == DMTP_OK) *bytes = layout(c, nullptr) + prompt_bytes(batch, cfg->max_ctx);
+  delete c;
+  return r;
+}
+
+int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, size_t ws_bytes,
+              const int32_t* prompt_ids, const int32_t* prompt_lens, int batch, void* stream,
+              dmtp_ctx** out) {
+  if (!out) return DMTP_EINVAL;
+  *out = nullptr;
+  if (!cfg || !w || !workspace || !prompt_ids || !prompt_lens) return DMTP_EINVAL;
+  if ((uintptr_t)workspace & 255) return DMTP_EINVAL;
+  dmtp_ctx* c = new dmtp_ctx();
+  int r = derive(c, cfg, batch);
+  if (r) {
+    delete c;
+    return r;
+  }
+  c->w = *w;
+  c->st = (cudaStream_t)stream;
+  c->graph = nullptr;
+  c->poisoned = false;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&c->nsm, cudaDevAttrMultiProcessorCount, dev);
+  int pmax = 0;
+  long total = 0;
+  for (int b = 0; b < batch; ++b) {
+    if (prompt_lens[b] < 1) {
+      delete c;
+      return DMTP_EINVAL;
+    }
+    pmax = std::max(pmax, (int)prompt_lens[b]);
+    total += prompt_lens[b];
+  }
+  if (pmax + 24 > c->maxc) {
+    delete c;
+    return DMTP_ECAPACITY;
+  }
+  c->pmax = pmax;
+  const size_t need = layout(c, nullptr) + prompt_bytes(batch, c->maxc);
+  if (ws_bytes < need) {
+    delete c;
+    return DMTP_ENOMEM;
+  }
+  c->ws_bytes = need;
+  const size_t fixed = layout(c, (char*)workspace);
+  c->prompts = (int*)((char*)workspace + fixed);
+  if (!w->emb || !w->head || !w->final_norm || !w->mtp_norm_h || !w->mtp_norm_e ||
+      !w->mtp_final_norm || !w->fuse_norm_e || !w->fuse_norm_m || !w->dft_norm_c ||
+      !w->dft_final_norm) {
+    delete c;
+    return DMTP_EINVAL;
+  }
+  // GEMM plans
+  int pr = 0;
+  const int M = c->M, B = c->B;
+  for (int l = 0; l < c->L; ++l) pr |= plan_layer(c, c->tgt[l], w->layers[l], cfg->layer_kind[l], M);
+  for (int j = 0; j < c->Ld; ++j) {
+    pr |= plan_layer(c, c->dft[j], w->dft[j], 0, M);
+    const char* wk = (const char*)w->dft[j].wqkv;
+    pr |= plan(c, c->dkv[j], wk ? wk + (size_t)c->qd * c->d * (c->dt ? 2 : 4) : nullptr,
+               2 * c->kvd, c->d, c->cn, M, false);
+  }
+  pr |= plan_layer(c, c->mtp, w->mtp, 0, M);
+  pr |= plan(c, c->fuse, w->fuse_w, c->d, 2 * c->d, c->z, B, false);
+  pr |= plan(c, c->head_t1, w->head, c->V, c->d, c->t1in, B, true);
+  pr |= plan(c, c->head_d, w->head, c->V, c->d, c->dn, 6 * B, true);
+  pr |= plan(c, c->head_v, w->head, c->V, c->d, c->hTn, M, true);
+  pr |= plan(c, c->dfc, w->dft_fc, c->d, c->ntap * c->d, c->taps, M, false);
+  pr |= plan(c, c->mproj, w->mtp_proj, c->d, 2 * c->d, c->z, M, false);
+  if (pr) {
+    delete c;
+    return DMTP_EINVAL;
+  }
+  if (c->dt == 1 && tc_init_attributes()) {
+    delete c;
+    return DMTP_ECUDA;
+  }
+  // ---- initial device state ----
+  cudaStream_t st = c->st;
+  RoundState& s = c->rs;
+  zero(c, c->err, 4);
+  zero(c, s.hist, 64);
+  zero(c, s.keys, (size_t)B * 16 * 8);
+  for (int l = 0; l < c->L; ++l)
+    if (c->gstate[l]) zero(c, c->gstate[l], (size_t)B * 8 * c->gH * c->gdv * c->gdk * 4);
+  if (c->n_gdn) {
+    std::vector<int> live((size_t)c->n_gdn * B, 0), slot((size_t)c->n_gdn * B * 8);
+    // buffer 0 is live, buffers 1..7 hold the snapshots after rows 0..6 (slot 7 unused)
+    for (size_t i = 0; i < slot.size(); ++i) slot[i] = (i % 8) < 7 ? (int)(i % 8) + 1 : 0;
+    cudaMemcpyAsync(s.gdn_live, live.data(), live.size() * 4, cudaMemcpyHostToDevice, st);
+    cudaMemcpyAsync(s.gdn_slot, slot.data(), slot.size() * 4, cudaMemcpyHostToDevice, st);
+    cudaStreamSynchronize(st);
+  }
+  op_rope_table(c->rope, c->maxc + 16, c->hd, cfg->rope_theta, st);
+  {
+    std::vector<int> pp((size_t)B * c->maxc, 0);
+    long off = 0;
+    for (int b = 0; b < B; ++b) {
+      memcpy(&pp[(size_t)b * c->maxc], prompt_ids + off, (size_t)prompt_lens[b] * 4);
+      off += prompt_lens[b];
+    }
+    cudaMemcpyAsync(c->prompts, pp.data(), pp.size() * 4, cudaMemcpyHostToDevice, st);
+    cudaMemcpyAsync(c->plen, prompt_lens, (size_t)B * 4, cudaMemcpyHostToDevice, st);
+    cudaStreamSynchronize(st);
+  }
+  // ---- prefill: chunks of 8 positions per sequence ----
+  const int nch = (pmax + 7) / 8;
+  for (int ch = 0; ch < nch; ++ch) {
+    op_prefill_chunk(s, c->prompts, c->plen, c->maxc, ch, st);
+    target_forward(c, false);
+    op_prefill_save_last(c->hT32, c->plen, ch, c->hlast, B, c->d, st);
+    drafter_ctx(c);
+    mtp_advance(c);
+    if ((ch & 63) == 63 && cudaStreamSynchronize(st) != cudaSuccess) {
+      delete c;
+      return DMTP_ECUDA;
+    }
+  }
+  // A = the target's greedy token after the prompt; MTP consumes (h^T_{P-1}, A) at P
+  op_cast_rows(c->dt, c->hlast, c->d, c->t1in, c->d, B, c->d, RowMap(), st);
+  zero(c, s.keys, (size_t)B * 8);
+  gemm_argmax(c, c->head_t1, s.keys, nullptr);
+  op_keys_to_ids(s.keys, B, 1, s.A, 1, 0, nullptr, 0, 0, st);
+  op_prefill_final(s, c->plen, c->hlast, c->hT32, c->d, st);
+  mtp_advance(c);
+  op_prefill_done(s, c->plen, st);
+  cudaError_t ce = cudaStreamSynchronize(st);
+  if (ce != cudaSuccess) {
+    fprintf(stderr, "dmtp_init: %s\n", cudaGetErrorString(ce));
+    delete c;
+    return DMTP_ECUDA;
+  }
+  r = check_err(c);
+  if (r) {
+    delete c;
+    return r;
+  }
+  c->kv_bound = pmax;
+  c->round_launches = 0;
+  *out = c;
+  return DMTP_OK;
+}
+
+static int copy_out(dmtp_ctx* c, void* dst, const void* src, size_t bytes) {
+  if (!dst) return 0;
+  return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, c->st) != cudaSuccess;
+}
+
+int dmtp_round(dmtp_ctx* c, const dmtp_round_out* out, const int32_t* forced) {
+  if (!c) return DMTP_EINVAL;
+  if (c->poisoned) return DMTP_ESTATE;
+  const int B = c->B;
+  if (c->kv_bound + 16 >= c->maxc) {
+    std::vector<int> kv(B);
+    if (cudaMemcpyAsync(kv.data(), c->rs.kv_len, B * 4, cudaMemcpyDeviceToHost, c->st) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(c->st) != cudaSuccess)
+      return DMTP_ECUDA;
+    c->kv_bound = *std::max_element(kv.begin(), kv.end());
+    if (c->kv_bound + 16 >= c->maxc) return DMTP_ECAPACITY;
+  }
+  Dbg dbg{nullptr, nullptr, nullptr};
+  if (out) {
+    dbg.t1 = out->t1_logits;
+    dbg.dl = out->draft_logits;
+    dbg.vl = out->verify_logits;
+    if (out->h_mtp && copy_out(c, out->h_mtp, c->h_mtp, (size_t)B * c->d * 4)) return DMTP_ECUDA;
+  }
+  const bool eager = forced || dbg.t1 || dbg.dl || dbg.vl;
+  if (forced) {
+    if (cudaMemcpyAsync(c->forced, forced, (size_t)B * 7 * 4, cudaMemcpyDeviceToDevice, c->st) !=
+        cudaSuccess)
+      return DMTP_ECUDA;
+  }
+  if (eager) {
+    c->launches = 0;
+    enqueue_round(c, dbg, forced ? c->forced : nullptr);
+    c->round_launches = c->launches;
+  } else {
+    if (!c->graph) {
+      cudaGraph_t g;
+      if (cudaStreamBeginCapture(c->st, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
+        return DMTP_ECUDA;
+      c->launches = 0;
+      enqueue_round(c, dbg, nullptr);
+      c->round_launches = c->launches;
+      if (cudaStreamEndCapture(c->st, &g) != cudaSuccess) return DMTP_ECUDA;
+      if (cudaGraphInstantiate(&c->graph, g, 0) != cudaSuccess) {
+        cudaGraphDestroy(g);
+        c->graph = nullptr;
+        return DMTP_ECUDA;
+      }
+      cudaGraphDestroy(g);
+    }
+    if (cudaGraphLaunch(c->graph, c->st) != cudaSuccess) return DMTP_ECUDA;
+  }
+  if (cudaPeekAtLastError() != cudaSuccess) return DMTP_ECUDA;
+  c->kv_bound += 8;
+  if (out) {
+    const RoundState& s = c->rs;
+    int e = 0;
+    e |= copy_out(c, out->committed, s.committed, (size_t)B * 8 * 4);
+    e |= copy_out(c, out->n_accepted, s.n_acc, (size_t)B * 4);
+    e |= copy_out(c, out->drafts, s.drafts, (size_t)B * 7 * 4);
+    e |= copy_out(c, out->picks, s.g, (size_t)B * 8 * 4);
+    e |= copy_out(c, out->kv_len, s.kv_len, (size_t)B * 4);
+    e |= copy_out(c, out->snap_slot, s.snap_slot, (size_t)B * 4);
+    e |= copy_out(c, out->delta, c->delta, (size_t)B * c->d * 4);
+    e |= copy_out(c, out->mtp_len, s.mtp_len, (size_t)B * 4);
+    if (e) return DMTP_ECUDA;
+  }
+  return DMTP_OK;
+}
+
+int dmtp_round_host(dmtp_ctx* c, int32_t* committed_host, int32_t* n_host) {
+  if (!c) return DMTP_EINVAL;
+  int r = dmtp_round(c, nullptr, nullptr);
+  if (r) return r;
+  if (committed_host &&
+      cudaMemcpyAsync(committed_host, c->rs.committed, (size_t)c->B * 8 * 4,
+                      cudaMemcpyDeviceToHost, c->st) != cudaSuccess)
+    return DMTP_ECUDA;
+  if (n_host && cudaMemcpyAsync(n_host, c->rs.n_acc, (size_t)c->B * 4, cudaMemcpyDeviceToHost,
+                                c->st) != cudaSuccess)
+    return DMTP_ECUDA;
+  if (cudaStreamSynchronize(c->st) != cudaSuccess) return DMTP_ECUDA;
+  return DMTP_OK;
+}
+
+int dmtp_read_state(dmtp_ctx* c, int32_t* kv_len, int32_t* pending, uint64_t* hist) {
+  if (!c) return DMTP_EINVAL;
+  if (c->poisoned) return DMTP_ESTATE;
+  const int B = c->B;
+  if (kv_len && cudaMemcpyAsync(kv_len, c->rs.kv_len, B * 4, cudaMemcpyDeviceToHost, c->st))
+    return DMTP_ECUDA;
+  if (pending && cudaMemcpyAsync(pending, c->rs.A, B * 4, cudaMemcpyDeviceToHost, c->st))
+    return DMTP_ECUDA;
+  if (hist && cudaMemcpyAsync(hist, c->rs.hist, 64, cudaMemcpyDeviceToHost, c->st))
+    return DMTP_ECUDA;
+  return check_err(c);
+}
+
+int dmtp_round_launches(const dmtp_ctx* c) { return c ? c->round_launches : 0; }
+
+int dmtp_round_profile(dmtp_ctx* c, dmtp_profile* out) {
+  if (!c || !out) return DMTP_EINVAL;
+  if (c->poisoned) return DMTP_ESTATE;
+  const int B = c->B;
+  c->kv_host.assign(B, 0);
+  if (cudaMemcpyAsync(c->kv_host.data(), c->rs.kv_len, B * 4, cudaMemcpyDeviceToHost, c->st) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(c->st) != cudaSuccess)
+    return DMTP_ECUDA;
+  const int mx = *std::max_element(c->kv_host.begin(), c->kv_host.end());
+  if (mx + 16 >= c->maxc) return DMTP_ECAPACITY;
+  cudaEvent_t e0, e1;
+  cudaEventCreate(&e0);
+  cudaEventCreate(&e1);
+  c->prof = true;
+  c->pcls.clear();
+  c->pbytes.clear();
+  c->pflops.clear();
+  c->launches = 0;
+  cudaEventRecord(e0, c->st);
+  enqueue_round(c, Dbg{nullptr, nullptr, nullptr}, nullptr);
+  cudaEventRecord(e1, c->st);
+  c->prof = false;
+  c->kv_bound = std::max<long>(c->kv_bound, mx) + 8;
+  if (cudaStreamSynchronize(c->st) != cudaSuccess) return DMTP_ECUDA;
+  memset(out, 0, sizeof(*out));
+  for (size_t i = 0; i < c->pcls.size(); ++i) {
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, c->pev[2 * i], c->pev[2 * i + 1]);
+    const int k = c->pcls[i];
+    out->ms[k] += ms;
+    out->bytes[k] += c->pbytes[i];
+    out->flops[k] += c->pflops[i];
+    out->launches[k] += 1;
+  }
+  float tot = 0.f;
+  cudaEventElapsedTime(&tot, e0, e1);
+  out->round_ms = tot;
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  return check_err(c);
+}
+
+void dmtp_free(dmtp_ctx* c) {
+  if (!c) return;
+  if (c->graph) cudaGraphExecDestroy(c->graph);
+  for (cudaEvent_t e : c->pev) cudaEventDestroy(e);
+  delete c;
+}
+
+const char* dmtp_strerror(int code) {
+  switch (code) {
+    case DMTP_OK: return "ok";
+    case DMTP_EINVAL: return "invalid argument or unsupported configuration";
+    case DMTP_ENOMEM: return "workspace too small";
+    case DMTP_ECAPACITY: return "KV capacity (max_ctx) exceeded";
+    case DMTP_ECUDA: return "CUDA runtime error";
+    case DMTP_EDEVICE: return "device-side check failed (bad token id, position or timeout)";
+    case DMTP_ESTATE: return "context poisoned by an earlier device error";
+    default: return "unknown error";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,432 @@
+// Row-wise kernels of the DMTP round: RMSNorm (+ tap copy), embedding gathers, the
+// fusion / MTP input concat of two RMS-normalised streams, drafter slot assembly,
+// SwiGLU, RoPE + KV-cache writes, and the small integer kernels that drive a round
+// (argmax keys -> ids, verify tokens, prefix acceptance and commit, prefill chunks).
+//
+// Memory-bound and tiny next to the weight/KV sweeps; one CTA per row, vectorised
+// where the row length allows.
+#include "common.cuh"
+#include "ops.h"
+
+namespace dmtp {
+
+static inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+__device__ __forceinline__ int map_row(int r, RowMap m) {
+  return (r / m.out_group) * m.in_group + m.in_offset + (r % m.out_group);
+}
+
+// ---------------------------------------------------------------------------------
+// RMSNorm: y = x / sqrt(mean(x^2) + eps) * g
+// ---------------------------------------------------------------------------------
+template <typename T>
+__global__ void k_rmsnorm(const float* __restrict__ x, int ldx, const T* __restrict__ g,
+                          T* __restrict__ y, int ldy, float* __restrict__ y32, int ld32,
+                          T* __restrict__ tap, int ldtap, int d, float eps, RowMap map) {
+  __shared__ float red[32];
+  const int r = blockIdx.x;
+  const float* xr = x + (long)map_row(r, map) * ldx;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    float v = xr[i];
+    ss += v * v;
+    if (tap) tap[(long)r * ldtap + i] = from_f32<T>(v);
+  }
+  ss = block_sum(ss, red);
+  const float inv = rsqrtf(ss / (float)d + eps);
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    float v = xr[i] * inv * to_f32(g[i]);
+    if (y) y[(long)r * ldy + i] = from_f32<T>(v);
+    if (y32) y32[(long)r * ld32 + i] = v;
+  }
+}
+
+void op_rmsnorm(int dt, const float* x, int ldx, const void* g, void* y, int ldy, float* y32,
+                int ld32, void* tap, int ldtap, int rows, int d, float eps, RowMap map,
+                cudaStream_t st) {
+  if (rows <= 0) return;
+  if (dt)
+    k_rmsnorm<bf16><<<rows, 256, 0, st>>>(x, ldx, (const bf16*)g, (bf16*)y, ldy, y32, ld32,
+                                          (bf16*)tap, ldtap, d, eps, map);
+  else
+    k_rmsnorm<float><<<rows, 256, 0, st>>>(x, ldx, (const float*)g, (float*)y, ldy, y32, ld32,
+                                           (float*)tap, ldtap, d, eps, map);
+}
+
+// ---------------------------------------------------------------------------------
+// Embedding gather: x[m] = E[tok[m]]
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ int checked_tok(int t, int vocab, unsigned* err) {
+  if (t < 0 || t >= vocab) {
+    if (threadIdx.x == 0) set_err(err, DMTP_ERR_TOKEN);
+    return 0;
+  }
+  return t;
+}
+
+template <typename T>
+__global__ void k_embed(const T* __restrict__ E, const int* __restrict__ tok, int vocab,
+                        float* __restrict__ x, int d, unsigned* err) {
+  const int m = blockIdx.x;
+  const int t = checked_tok(tok[m], vocab, err);
+  const T* e = E + (long)t * d;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) x[(long)m * d + i] = to_f32(e[i]);
+}
+
+void op_embed(int dt, const void* E, const int* tok, int vocab, float* x, int rows, int d,
+              unsigned* err, cudaStream_t st) {
+  if (dt)
+    k_embed<bf16><<<rows, 256, 0, st>>>((const bf16*)E, tok, vocab, x, d, err);
+  else
+    k_embed<float><<<rows, 256, 0, st>>>((const float*)E, tok, vocab, x, d, err);
+}
+
+// ---------------------------------------------------------------------------------
+// z[r] = [RMS(a) * ga ; RMS(b) * gb]
+// ---------------------------------------------------------------------------------
+template <typename T>
+__device__ void rms_part(const T* E, int vocab, const ConcatPart& p, int r, T* out, int d,
+                         float eps, unsigned* err, float* red) {
+  const float* s32 = nullptr;
+  const T* se = nullptr;
+  if (p.src32) {
+    s32 = p.src32 + (long)map_row(r, p.map) * p.ld;
+  } else {
+    const int t = checked_tok(p.tok[(long)r * p.tok_stride], vocab, err);
+    se = E + (long)t * d;
+  }
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    float v = s32 ? s32[i] : to_f32(se[i]);
+    ss += v * v;
+  }
+  ss = block_sum(ss, red);
+  const float inv = rsqrtf(ss / (float)d + eps);
+  const T* g = (const T*)p.g;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    float v = s32 ? s32[i] : to_f32(se[i]);
+    out[i] = from_f32<T>(v * inv * to_f32(g[i]));
+  }
+}
+
+template <typename T>
+__global__ void k_concat_rms2(const T* E, int vocab, ConcatPart a, ConcatPart b, T* z, int d,
+                              float eps, unsigned* err) {
+  __shared__ float red[32];
+  const int r = blockIdx.x;
+  rms_part<T>(E, vocab, a, r, z + (long)r * 2 * d, d, eps, err, red);
+  __syncthreads();
+  rms_part<T>(E, vocab, b, r, z + (long)r * 2 * d + d, d, eps, err, red);
+}
+
+void op_concat_rms2(int dt, const void* E, int vocab, ConcatPart a, ConcatPart b, void* z,
+                    int rows, int d, float eps, unsigned* err, cudaStream_t st) {
+  if (dt)
+    k_concat_rms2<bf16><<<rows, 256, 0, st>>>((const bf16*)E, vocab, a, b, (bf16*)z, d, eps,
+                                              err);
+  else
+    k_concat_rms2<float><<<rows, 256, 0, st>>>((const float*)E, vocab, a, b, (float*)z, d, eps,
+                                               err);
+}
+
+// ---------------------------------------------------------------------------------
+// Drafter slots [E(A), E(T1) + delta, E(MASK) x 6]
+// ---------------------------------------------------------------------------------
+template <typename T>
+__global__ void k_build_slots(const T* __restrict__ E, int vocab, const int* __restrict__ A,
+                              const int* __restrict__ drafts, const float* __restrict__ delta,
+                              int mask_id, float* __restrict__ x, int d, unsigned* err) {
+  const int m = blockIdx.x, b = m >> 3, s = m & 7;
+  int t = (s == 0) ? A[b] : (s == 1 ? drafts[b * 7] : mask_id);
+  t = checked_tok(t, vocab, err);
+  const T* e = E + (long)t * d;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    float v = to_f32(e[i]);
+    if (s == 1) v += delta[(long)b * d + i];
+    x[(long)m * d + i] = v;
+  }
+}
+
+void op_build_slots(int dt, const void* E, int vocab, const int* A, const int* drafts,
+                    const float* delta, int mask_id, float* x, int B, int d, unsigned* err,
+                    cudaStream_t st) {
+  if (dt)
+    k_build_slots<bf16><<<B * 8, 256, 0, st>>>((const bf16*)E, vocab, A, drafts, delta, mask_id,
+                                               x, d, err);
+  else
+    k_build_slots<float><<<B * 8, 256, 0, st>>>((const float*)E, vocab, A, drafts, delta,
+                                                mask_id, x, d, err);
+}
+
+// ---------------------------------------------------------------------------------
+// SwiGLU
+// ---------------------------------------------------------------------------------
+template <typename T>
+__global__ void k_swiglu(const float* __restrict__ gu, T* __restrict__ h, int F) {
+  const int m = blockIdx.y;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= F) return;
+  const float gv = gu[(long)m * 2 * F + i], uv = gu[(long)m * 2 * F + F + i];
+  h[(long)m * F + i] = from_f32<T>(gv / (1.f + __expf(-gv)) * uv);
+}
+
+void op_swiglu(int dt, const float* gu, void* h, int rows, int F, cudaStream_t st) {
+  dim3 grid(cdiv(F, 256), rows);
+  if (dt)
+    k_swiglu<bf16><<<grid, 256, 0, st>>>(gu, (bf16*)h, F);
+  else
+    k_swiglu<float><<<grid, 256, 0, st>>>(gu, (float*)h, F);
+}
+
+// ---------------------------------------------------------------------------------
+// RoPE table: tab[p][i] = (cos, sin)(p * theta^(-2i/hd)), computed in double.
+// ---------------------------------------------------------------------------------
+__global__ void k_rope_table(float2* tab, int npos, int hd, double ltheta) {
+  const int half = hd / 2;
+  const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long)npos * half) return;
+  const int p = (int)(idx / half), i = (int)(idx % half);
+  const double ang = (double)p * exp(-ltheta * (2.0 * i) / hd);
+  double s, c;
+  sincos(ang, &s, &c);
+  tab[idx] = make_float2((float)c, (float)s);
+}
+
+void op_rope_table(float2* tab, int npos, int hd, float theta, cudaStream_t st) {
+  const long n = (long)npos * (hd / 2);
+  k_rope_table<<<(int)((n + 255) / 256), 256, 0, st>>>(tab, npos, hd, log((double)theta));
+}
+
+// ---------------------------------------------------------------------------------
+// RoPE + KV-cache write. Row m = b*8 + s at position base[b] + s. One CTA per row;
+// threads cover (head, pair). Cache layout [B][hkv][max_ctx][hd].
+// ---------------------------------------------------------------------------------
+template <typename T>
+__global__ void k_rope_kv(const float* __restrict__ src, int ld, int q_off, int k_off, int v_off,
+                          T* __restrict__ q_out, T* __restrict__ Kc, T* __restrict__ Vc,
+                          const int* __restrict__ base, const float2* __restrict__ tab, int hq,
+                          int hkv, int hd, int max_ctx, unsigned* err) {
+  const int m = blockIdx.x, b = m >> 3, s = m & 7;
+  const int pos = base[b] + s;
+  const int half = hd / 2;
+  const float* row = src + (long)m * ld;
+  const bool pos_ok = pos >= 0 && pos < max_ctx;
+  if (!pos_ok && threadIdx.x == 0) set_err(err, DMTP_ERR_POS);
+  const float2* tr = tab + (long)(pos_ok ? pos : 0) * half;
+  if (q_off >= 0) {
+    for (int idx = threadIdx.x; idx < hq * half; idx += blockDim.x) {
+      const int h = idx / half, i = idx % half;
+      const float x1 = row[q_off + h * hd + i], x2 = row[q_off + h * hd + half + i];
+      const float2 cs = tr[i];
+      T* qo = q_out + ((long)m * hq + h) * hd;
+      qo[i] = from_f32<T>(x1 * cs.x - x2 * cs.y);
+      qo[half + i] = from_f32<T>(x2 * cs.x + x1 * cs.y);
+    }
+  }
+  if (!pos_ok) return;
+  for (int idx = threadIdx.x; idx < hkv * half; idx += blockDim.x) {
+    const int h = idx / half, i = idx % half;
+    const float x1 = row[k_off + h * hd + i], x2 = row[k_off + h * hd + half + i];
+    const float2 cs = tr[i];
+    T* kc = Kc + (((long)b * hkv + h) * max_ctx + pos) * hd;
+    kc[i] = from_f32<T>(x1 * cs.x - x2 * cs.y);
+    kc[half + i] = from_f32<T>(x2 * cs.x + x1 * cs.y);
+    T* vc = Vc + (((long)b * hkv + h) * max_ctx + pos) * hd;
+    vc[i] = from_f32<T>(row[v_off + h * hd + i]);
+    vc[half + i] = from_f32<T>(row[v_off + h * hd + half + i]);
+  }
+}
+
+void op_rope_kv(int dt, const float* src, int ld, int q_off, int k_off, int v_off, void* q_out,
+                void* Kc, void* Vc, const int* base, const float2* tab, int rows, int hq, int hkv,
+                int hd, int max_ctx, unsigned* err, cudaStream_t st) {
+  if (dt)
+    k_rope_kv<bf16><<<rows, 256, 0, st>>>(src, ld, q_off, k_off, v_off, (bf16*)q_out, (bf16*)Kc,
+                                          (bf16*)Vc, base, tab, hq, hkv, hd, max_ctx, err);
+  else
+    k_rope_kv<float><<<rows, 256, 0, st>>>(src, ld, q_off, k_off, v_off, (float*)q_out,
+                                           (float*)Kc, (float*)Vc, base, tab, hq, hkv, hd,
+                                           max_ctx, err);
+}
+
+template <typename T>
+__global__ void k_cast_rows(const float* __restrict__ x, int ldx, T* __restrict__ y, int ldy,
+                            int d, RowMap map) {
+  const int r = blockIdx.x;
+  const float* xr = x + (long)map_row(r, map) * ldx;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) y[(long)r * ldy + i] = from_f32<T>(xr[i]);
+}
+
+void op_cast_rows(int dt, const float* x, int ldx, void* y, int ldy, int rows, int d, RowMap map,
+                  cudaStream_t st) {
+  if (dt)
+    k_cast_rows<bf16><<<rows, 256, 0, st>>>(x, ldx, (bf16*)y, ldy, d, map);
+  else
+    k_cast_rows<float><<<rows, 256, 0, st>>>(x, ldx, (float*)y, ldy, d, map);
+}
+
+// ---------------------------------------------------------------------------------
+// Round control
+// ---------------------------------------------------------------------------------
+__global__ void k_round_begin(RoundState s) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < s.B) s.pos0[i] = s.kv_len[i];
+  if (i < s.B) s.rows_valid[i] = 8;
+  if (i < s.B * 16) s.keys[i] = 0ull;
+}
+
+// Per round: row-0 positions from the watermarks; argmax keys zeroed (T1 keys at
+// [0, B), drafter keys at [B, 7B), verify keys at [7B, 15B)).
+void op_round_begin(const RoundState& s, cudaStream_t st) {
+  k_round_begin<<<cdiv(s.B * 16, 256), 256, 0, st>>>(s);
+}
+
+__global__ void k_keys_to_ids(const unsigned long long* __restrict__ keys, int B, int per,
+                              int* dst, int dst_stride, int dst_off, const int* forced,
+                              int forced_stride, int forced_off) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= B * per) return;
+  const int b = i / per, j = i % per;
+  int id = argmax_key_index(keys[i]);
+  if (forced) id = forced[b * forced_stride + forced_off + j];
+  dst[b * dst_stride + dst_off + j] = id;
+}
+
+void op_keys_to_ids(const unsigned long long* keys, int B, int per, int* dst, int dst_stride,
+                    int dst_off, const int* forced, int forced_stride, int forced_off,
+                    cudaStream_t st) {
+  k_keys_to_ids<<<cdiv(B * per, 128), 128, 0, st>>>(keys, B, per, dst, dst_stride, dst_off,
+                                                    forced, forced_stride, forced_off);
+}
+
+__global__ void k_verify_tokens(RoundState s) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= s.B * 8) return;
+  const int b = i >> 3, r = i & 7;
+  s.tok[i] = (r == 0) ? s.A[b] : s.drafts[b * 7 + r - 1];
+}
+
+void op_verify_tokens(const RoundState& s, cudaStream_t st) {
+  k_verify_tokens<<<cdiv(s.B * 8, 256), 256, 0, st>>>(s);
+}
+
+// Greedy prefix acceptance ([DMTP] §5): n = longest prefix with T_j == g_{j-1};
+// commit T_1..T_n and the target's pick g_n; kv_len <- pos0 + n + 1; A <- g_n.
+// Also prepares the MTP advance rows (tokens x_{pos0+1+s} = committed[s]) and swaps
+// the GDN snapshot slot n in as the live state (pointer swap, nothing copied).
+__global__ void k_accept(RoundState s) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= s.B) return;
+  const int* T = s.drafts + b * 7;
+  const int* g = s.g + b * 8;
+  int n = 0;
+  while (n < 7 && T[n] == g[n]) ++n;
+  int* c = s.committed + b * 8;
+  for (int j = 0; j < 8; ++j) c[j] = (j < n) ? T[j] : (j == n ? g[n] : -1);
+  for (int j = 0; j < 8; ++j) s.mtp_tok[b * 8 + j] = (j <= n) ? c[j] : g[n];
+  s.n_acc[b] = n;
+  const int a = s.pos0[b];
+  s.kv_len[b] = a + n + 1;
+  s.mtp_len[b] = a + n + 2;
+  s.A[b] = g[n];
+  s.mtp_base[b] = a + 1;
+  s.mtp_cnt[b] = n + 1;
+  s.snap_slot[b] = s.n_gdn > 0 ? n : -1;
+  atomicAdd(&s.hist[n], 1ull);
+  if (n < 7) {
+    for (int l = 0; l < s.n_gdn; ++l) {
+      int* live = s.gdn_live + l * s.B + b;
+      int* slot = s.gdn_slot + ((long)l * s.B + b) * 8;
+      const int tmp = *live;
+      *live = slot[n];
+      slot[n] = tmp;
+    }
+  }
+}
+
+void op_accept(const RoundState& s, cudaStream_t st) {
+  k_accept<<<cdiv(s.B, 64), 64, 0, st>>>(s);
+}
+
+__global__ void k_gather_hmtp(const float* __restrict__ x, const int* __restrict__ cnt,
+                              float* __restrict__ h, int d) {
+  const int b = blockIdx.x;
+  const int r = b * 8 + max(0, min(7, cnt[b] - 1));
+  for (int i = threadIdx.x; i < d; i += blockDim.x) h[(long)b * d + i] = x[(long)r * d + i];
+}
+
+void op_gather_hmtp(const float* x, const int* cnt, float* h, int B, int d, cudaStream_t st) {
+  k_gather_hmtp<<<B, 256, 0, st>>>(x, cnt, h, d);
+}
+
+__global__ void k_prefill_chunk(RoundState s, const int* prompts, const int* plen, int pmax,
+                                int c) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= s.B * 8) return;
+  const int b = i >> 3, r = i & 7;
+  const int P = plen[b];
+  const int p = 8 * c + r;
+  s.tok[i] = (p < P) ? prompts[(long)b * pmax + p] : 0;
+  s.mtp_tok[i] = (p + 1 < P) ? prompts[(long)b * pmax + p + 1] : 0;
+  if (r == 0) {
+    s.pos0[b] = 8 * c;
+    s.mtp_base[b] = 8 * c + 1;
+    s.rows_valid[b] = max(0, min(8, P - 8 * c));
+    s.mtp_cnt[b] = max(0, min(8, P - 1 - 8 * c));
+  }
+}
+
+void op_prefill_chunk(const RoundState& s, const int* prompts, const int* plen, int pmax, int c,
+                      cudaStream_t st) {
+  k_prefill_chunk<<<cdiv(s.B * 8, 256), 256, 0, st>>>(s, prompts, plen, pmax, c);
+}
+
+__global__ void k_prefill_save_last(const float* hT, const int* plen, int c, float* hlast,
+                                    int d) {
+  const int b = blockIdx.x;
+  const int r = plen[b] - 1 - 8 * c;
+  if (r < 0 || r >= 8) return;
+  for (int i = threadIdx.x; i < d; i += blockDim.x)
+    hlast[(long)b * d + i] = hT[((long)b * 8 + r) * d + i];
+}
+
+void op_prefill_save_last(const float* hT, const int* plen, int c, float* hlast, int B, int d,
+                          cudaStream_t st) {
+  k_prefill_save_last<<<B, 256, 0, st>>>(hT, plen, c, hlast, d);
+}
+
+// After the prompt: A = argmax of the last row (already in s.A via keys_to_ids);
+// the MTP consumes (h^T_{P-1}, A) at position P.
+__global__ void k_prefill_final(RoundState s, const int* plen, const float* hlast, float* hT,
+                                int d) {
+  const int b = blockIdx.x;
+  const int r = threadIdx.x;
+  if (r < 8) s.mtp_tok[b * 8 + r] = s.A[b];
+  if (r == 0) {
+    s.mtp_base[b] = plen[b];
+    s.mtp_cnt[b] = 1;
+  }
+  for (int j = 0; j < 8; ++j)
+    for (int i = threadIdx.x; i < d; i += blockDim.x)
+      hT[((long)b * 8 + j) * d + i] = hlast[(long)b * d + i];
+}
+
+void op_prefill_final(const RoundState& s, const int* plen, const float* hlast, float* hT, int d,
+                      cudaStream_t st) {
+  k_prefill_final<<<s.B, 256, 0, st>>>(s, plen, hlast, hT, d);
+}
+
+__global__ void k_prefill_done(RoundState s, const int* plen) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= s.B) return;
+  s.kv_len[b] = plen[b];
+  s.mtp_len[b] = plen[b] + 1;
+  s.pos0[b] = plen[b];
+  s.rows_valid[b] = 8;
+}
+
+void op_prefill_done(const RoundState& s, const int* plen, cudaStream_t st) {
+  k_prefill_done<<<cdiv(s.B, 64), 64, 0, st>>>(s, plen);
+}
+
+}  // namespace dmtp

@@ -1,0 +1,151 @@
+// Host-side launchers for the DMTP round kernels. `dt` selects the storage type of
+// weights, KV caches and GEMM operands: 0 = fp32, 1 = bf16. The residual stream,
+// GEMM outputs, softmax and the GDN state are always fp32.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace dmtp {
+
+// Row mapping shared by the row-wise kernels: output row r reads input row
+//   (r / out_group) * in_group + in_offset + (r % out_group).
+struct RowMap {
+  int out_group = 1, in_group = 1, in_offset = 0;
+};
+
+// ---- elementwise.cu --------------------------------------------------------------
+// y[r] = RMSNorm(x[map(r)]) * g, stored as dt (y) and optionally as fp32 (y32);
+// tap (optional, dt): raw copy of x[map(r)] into column block of a tap buffer.
+void op_rmsnorm(int dt, const float* x, int ldx, const void* g, void* y, int ldy, float* y32,
+                int ld32, void* tap, int ldtap, int rows, int d, float eps, RowMap map,
+                cudaStream_t st);
+// x[m] = E[tok[m]] (fp32 rows)
+void op_embed(int dt, const void* E, const int* tok, int vocab, float* x, int rows, int d,
+              unsigned* err, cudaStream_t st);
+// z[r] = [RMS(partA[r]) * gA ; RMS(partB[r]) * gB] as dt; each part is an fp32 row
+// (src32 != null, row map) or an embedding row E[tok[r]] (tok != null).
+struct ConcatPart {
+  const float* src32 = nullptr;
+  int ld = 0;
+  RowMap map;
+  const int* tok = nullptr;
+  int tok_stride = 1;
+  const void* g = nullptr;
+};
+void op_concat_rms2(int dt, const void* E, int vocab, ConcatPart a, ConcatPart b, void* z,
+                    int rows, int d, float eps, unsigned* err, cudaStream_t st);
+// Drafter slots: x[b*8+s] = E[A_b] (s=0), E[T1_b] + delta_b (s=1), E[mask] (s>=2)
+void op_build_slots(int dt, const void* E, int vocab, const int* A, const int* drafts,
+                    const float* delta, int mask_id, float* x, int B, int d, unsigned* err,
+                    cudaStream_t st);
+// h = silu(gu[:, :F]) * gu[:, F:] as dt
+void op_swiglu(int dt, const float* gu, void* h, int rows, int F, cudaStream_t st);
+// RoPE (table) + cache write. src rows m = b*8 + s at position base[b] + s.
+// q_off < 0: no q. q_out fp32 [rows][hq][hd] (dt==0) or bf16 (dt==1).
+void op_rope_kv(int dt, const float* src, int ld, int q_off, int k_off, int v_off, void* q_out,
+                void* Kc, void* Vc, const int* base, const float2* rope_tab, int rows, int hq,
+                int hkv, int hd, int max_ctx, unsigned* err, cudaStream_t st);
+// fp32 -> dt copy of rows (with row map)
+void op_cast_rows(int dt, const float* x, int ldx, void* y, int ldy, int rows, int d, RowMap map,
+                  cudaStream_t st);
+void op_rope_table(float2* tab, int npos, int hd, float theta, cudaStream_t st);
+
+// ---- round control (elementwise.cu) -------------------------------------------------
+struct RoundState {
+  int* kv_len;        // [B]
+  int* pos0;          // [B] position of row 0 in the current step
+  int* A;             // [B] pending token
+  int* drafts;        // [B][7]
+  int* g;             // [B][8]
+  int* n_acc;         // [B]
+  int* committed;     // [B][8]
+  int* tok;           // [B*8] tokens of the target rows
+  int* mtp_tok;       // [B*8] tokens of the MTP rows
+  int* mtp_base;      // [B] position of MTP row 0
+  int* mtp_cnt;       // [B] valid MTP rows
+  int* rows_valid;    // [B] valid target rows (GDN state advance)
+  int* snap_slot;     // [B]
+  int* mtp_len;       // [B] next MTP position (= kv_len + 1)
+  unsigned long long* hist;  // [8]
+  unsigned long long* keys;  // [B*16] argmax keys (T1 | drafter | verify)
+  int* gdn_live;      // [n_gdn][B] index of the live state buffer (0..8)
+  int* gdn_slot;      // [n_gdn][B][8] buffer index of each snapshot slot
+  int n_gdn;
+  int B;
+  unsigned* err;
+};
+void op_round_begin(const RoundState& s, cudaStream_t st);
+// keys -> ids: dst[b*dst_stride + dst_off + j] = id(keys[b*per + j]) (or forced value)
+void op_keys_to_ids(const unsigned long long* keys, int B, int per, int* dst, int dst_stride,
+                    int dst_off, const int* forced, int forced_stride, int forced_off,
+                    cudaStream_t st);
+void op_verify_tokens(const RoundState& s, cudaStream_t st);
+void op_accept(const RoundState& s, cudaStream_t st);
+// h_mtp[b] = x[b*8 + cnt[b]-1]
+void op_gather_hmtp(const float* x, const int* cnt, float* h_mtp, int B, int d, cudaStream_t st);
+// prefill chunk c: pos0 = 8c, tok = prompt[8c+s], mtp_tok = prompt[8c+1+s], counts
+void op_prefill_chunk(const RoundState& s, const int* prompts, const int* plen, int pmax, int c,
+                      cudaStream_t st);
+void op_prefill_save_last(const float* hT, const int* plen, int c, float* hlast, int B, int d,
+                          cudaStream_t st);
+void op_prefill_final(const RoundState& s, const int* plen, const float* hlast, float* hT, int d,
+                      cudaStream_t st);
+void op_prefill_done(const RoundState& s, const int* plen, cudaStream_t st);
+
+// ---- attention.cu ------------------------------------------------------------------
+struct AttnArgs {
+  const void* Kc;      // [B][hkv][max_ctx][hd] dt
+  const void* Vc;
+  const void* q;       // [B*8][hq][hd] (fp32 if dt==0 else bf16)
+  float* part_o;       // [B][hkv][nchunk][QN][hd]
+  float* part_ml;      // [B][hkv][nchunk][QN][2]
+  void* out;           // [B*8][hq*hd] dt
+  const int* base;     // [B] position of row 0
+  int causal;          // 1: row s sees keys <= base+s; 0: keys <= base+7
+  int lo_fixed;        // lowest key index
+  int window;          // > 0: lo = max(lo_fixed, base - window)
+  int B, hq, hkv, hd, max_ctx, chunk, nchunk;
+};
+void op_attention(int dt, const AttnArgs& a, cudaStream_t st);
+
+// ---- gemm_simt.cu (fp32 storage) ------------------------------------------------------
+// out[m*ldo + n] += sum_k X[m*K + k] * W[n*K + k]   (fp32 W and X)
+void op_gemm_simt_acc(const float* W, const float* X, int N, int K, int M, float* out, int ldo,
+                      cudaStream_t st);
+// argmax over n of sum_k X[m,k] W[n,k] -> atomicMax into keys[m]; logits optional
+void op_gemm_simt_argmax(const float* W, const float* X, int N, int K, int M,
+                         unsigned long long* keys, float* logits, long ldl, cudaStream_t st);
+
+// ---- gemm_tc.cu (bf16, tcgen05) -------------------------------------------------------
+struct TcPlan {
+  CUtensorMap tmW, tmX;
+  int N, K, M, MT, splits, stages;
+  size_t smem;
+};
+// Builds the tensor maps and launch shape for out[M,N] = X[M,K] . W[N,K]^T.
+int tc_plan(TcPlan* p, const void* W, int N, int K, const void* X, int M, int nsm,
+            bool argmax);
+void op_gemm_tc_acc(const TcPlan& p, float* out, int ldo, unsigned* err, cudaStream_t st);
+void op_gemm_tc_argmax(const TcPlan& p, unsigned long long* keys, float* logits, long ldl,
+                       unsigned* err, cudaStream_t st);
+int tc_init_attributes();
+
+// ---- gdn.cu ----------------------------------------------------------------------------
+struct GdnArgs {
+  const float* qkvab;    // [B*8][ld] fp32: q | k | v | alpha-logit | beta-logit
+  int ld;
+  float* states;         // [B][8][H][dv][dk] fp32 for this layer
+  const int* live;       // [B]
+  const int* slot;       // [B][8]
+  const int* rows_valid; // [B]
+  int snapshots;         // 1: write the state after each row r < 7 to buffer slot[b][r]
+  void* out;             // [B*8][H*dv] dt
+  int B, H, dk, dv;
+  unsigned* err;
+};
+void op_gdn(int dt, const GdnArgs& a, cudaStream_t st);
+
+}  // namespace dmtp

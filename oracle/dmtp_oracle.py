@@ -380,18 +380,22 @@ class OracleModel:
             dft_V=[z() for _ in range(c.draft_layers)],
             mtp_K=z(), mtp_V=z(), h_mtp=np.zeros(c.d_model, F64))
 
-    def prefill(self, prompt) -> SeqState:
+    def prefill(self, prompt, adopt_A=None) -> SeqState:
         """Initialise all three models' states from a prompt ([DMTP] §6.1).
 
         Target over x_0..x_{P-1}; A = argmax H h^T_{P-1}; drafter context K/V for
         positions 0..P-1; MTP rows p = 1..P (token x_p, hidden h^T_{p-1}, with
         x_P = A), so that h_MTP (the block output at P) predicts x_{P+1}.
+        ``adopt_A``: another implementation's pick for A, taken when it lies within the
+        near-tie gate of the maximum (see ``round``).
         """
         prompt = [int(t) for t in prompt]
         P = len(prompt)
         st = self.empty_state()
         hT, taps, _, _ = self.target_rows(st, prompt, 0, head=False)
-        A = argmax_first(hT[P - 1] @ self.W["head"].T)
+        log = {"gaps": {}, "adopted": [], "mismatch": []}
+        A = self._pick(hT[P - 1] @ self.W["head"].T, adopt_A, log, "A")
+        self.prefill_log = log
         for j, (k, v) in enumerate(self.drafter_ctx_kv(taps, np.arange(P))):
             st.dft_K[j], st.dft_V[j] = k, v
         out = self.mtp_rows(st, hT, prompt[1:] + [A], 1)

@@ -1,0 +1,87 @@
+"""Lock-step comparison of the CUDA round (through the C ABI) with the oracle.
+
+Both start from the same prompts and weights. Each round the GPU runs first; the
+oracle then runs the same round on each sequence, adopting the GPU's pick at any
+argmax where the oracle's own top-1 and the GPU's id are within the near-tie gate
+(0.05 in logits) - so one near tie cannot make the two diverge for the rest of the
+run. Any pick outside the gate is a mismatch. Integer fields must then agree
+exactly; float fields within `tol` max-abs.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import OracleModel
+
+GATE = 0.05
+
+
+def to_np(t):
+    return t.detach().cpu().numpy()
+
+
+class Lockstep:
+    def __init__(self, cfg, weights_gpu: dict, prompts, rounds: int, seqs=None, max_ctx=None):
+        from mtp_block_draft_gb300 import DmtpRound, default_max_ctx
+        self.cfg = cfg
+        self.prompts = prompts
+        self.seqs = list(range(len(prompts))) if seqs is None else list(seqs)
+        self.gpu = DmtpRound(cfg, weights_gpu, prompts,
+                             max_ctx or default_max_ctx(prompts, rounds))
+        self.oracle = OracleModel(cfg, {k: v.cpu() for k, v in weights_gpu.items()}, gate=GATE)
+        kv, A, _ = self.gpu.read_state()
+        self.states = {}
+        self.adopted = []
+        for b in self.seqs:
+            st = self.oracle.prefill(prompts[b], adopt_A=int(A[b]))
+            assert not self.oracle.prefill_log["mismatch"], self.oracle.prefill_log
+            self.adopted += self.oracle.prefill_log["adopted"]
+            assert st.A == int(A[b]) and st.a == int(kv[b]) == len(prompts[b])
+            self.states[b] = st
+        self.max_err = {}
+
+    def _err(self, name, a, b):
+        e = float(np.max(np.abs(np.asarray(a, np.float64) - np.asarray(b, np.float64))))
+        self.max_err[name] = max(self.max_err.get(name, 0.0), e)
+        return e
+
+    def step(self, forced: np.ndarray | None = None, floats: bool = True, tol: float = 2e-2):
+        g = self.gpu
+        out = g.alloc_out(ints=True, floats=floats)
+        ft = None
+        if forced is not None:
+            ft = torch.as_tensor(np.asarray(forced, np.int32), device=g.device)
+        g.round(out, forced=ft)
+        torch.cuda.synchronize()
+        o = {k: to_np(v) for k, v in out.items()}
+        recs = {}
+        for b in self.seqs:
+            adopt = {"g": o["picks"][b]}
+            if forced is None:
+                adopt["T"] = o["drafts"][b]
+            rec = self.oracle.round(self.states[b],
+                                    forced=None if forced is None else forced[b],
+                                    adopt=adopt, want_logits=floats)
+            log = rec["log"]
+            assert not log["mismatch"], (b, log["mismatch"])
+            self.adopted += log["adopted"]
+            assert list(o["drafts"][b]) == rec["drafts"], (b, o["drafts"][b], rec["drafts"])
+            assert list(o["picks"][b]) == rec["g"], (b, o["picks"][b], rec["g"])
+            assert int(o["n_accepted"][b]) == rec["n"]
+            assert list(o["committed"][b][:rec["n"] + 1]) == rec["committed"]
+            assert all(int(x) == -1 for x in o["committed"][b][rec["n"] + 1:])
+            assert int(o["kv_len"][b]) == rec["kv_len"]
+            assert int(o["mtp_len"][b]) == rec["mtp_len"]
+            assert int(o["snap_slot"][b]) == rec["snap_slot"]
+            if floats:
+                for name, key in (("t1_logits", "t1_logits"), ("draft_logits", "draft_logits"),
+                                  ("verify_logits", "verify_logits"), ("delta", "delta"),
+                                  ("h_mtp", "h_mtp_in")):
+                    e = self._err(name, o[name][b], rec[key])
+                    assert e <= tol, (b, name, e)
+            recs[b] = rec
+        return o, recs
+
+    def close(self):
+        self.gpu.close()

@@ -1,0 +1,140 @@
+"""Parity of the CUDA round (through the C ABI) with the oracle, in lock-step.
+
+Integer fields (drafts, picks, n, committed, kv_len, mtp_len, snapshot slot) must be
+bit-exact wherever the oracle's top-1/top-2 gap exceeds 0.05; float fields (T1,
+drafter and verify logits, Delta, h_MTP) within max-abs 2e-2. Sizes span several
+GEMM tiles (vocab and weight rows with ragged tails), several attention chunks
+(contexts > 256 keys with a ragged tail) and per-sequence ragged contexts.
+"""
+import numpy as np
+import pytest
+import torch
+
+from synth import CONFIGS, make_prompts, make_weights
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-2
+
+
+def _lockstep(cfg, rounds, fusion_std=None, seqs=None, prompts=None):
+    from lockstep import Lockstep
+    w = make_weights(cfg, "cuda", fusion_std=fusion_std)
+    prompts = make_prompts(cfg) if prompts is None else prompts
+    return Lockstep(cfg, w, prompts, rounds, seqs=seqs)
+
+
+TINY = CONFIGS["tiny"]
+# small-model shape (vocab 32000, d 1024, 8 layers of 16/16 x 64) with a shorter prompt
+SMALL_R = CONFIGS["small"].replace(ctx_lo=300, ctx_hi=300)
+# B32 shape at reduced width: 256 GEMM rows, GQA 8/2, ragged vocab (5000 = 39*128 + 8)
+B32_R = CONFIGS["b32"].replace(name="b32_r", vocab=5000, d_model=256, n_layers=2, n_heads=8,
+                               n_kv_heads=2, head_dim=64, ffn=512, ctx_lo=40, ctx_hi=300)
+# hybrid target at reduced width: GDN, GDN, GDN, attention
+HYB_R = CONFIGS["hybrid"].replace(name="hybrid_r", vocab=3000, d_model=256, n_layers=4,
+                                  layer_kinds=(1, 1, 1, 0), n_heads=4, n_kv_heads=2,
+                                  head_dim=64, ffn=512, batch=4, ctx_lo=60, ctx_hi=120,
+                                  gdn_heads=4, gdn_dk=64, gdn_dv=64)
+
+
+def test_tiny_natural_16_rounds():
+    ls = _lockstep(TINY, 16)
+    for _ in range(16):
+        ls.step(tol=TOL)
+    assert ls.max_err["verify_logits"] < 1e-3   # fp32 storage: far inside the bar
+    ls.close()
+
+
+def test_tiny_with_fusion_weights():
+    ls = _lockstep(TINY, 8, fusion_std=0.02)
+    for _ in range(8):
+        _, recs = ls.step(tol=TOL)
+        assert np.abs(recs[0]["delta"]).max() > 0
+    ls.close()
+
+
+def _greedy(ls, b, n):
+    return ls.oracle.greedy_decode(ls.prompts[b], n)
+
+
+@pytest.mark.parametrize("mode", ["all_right", "all_wrong", "alternating", "cycling"])
+def test_tiny_forced_modes(mode):
+    """The colibri page's forced-draft modes: every accepted length 0..7 is exercised,
+    and the committed stream stays the plain greedy stream."""
+    ls = _lockstep(TINY, 10)
+    greedy = _greedy(ls, 0, 8 * 10 + 9)
+    P = len(ls.prompts[0])
+    stream = [ls.states[0].A]
+    for r in range(10):
+        off = ls.states[0].a - P
+        d = list(greedy[off + 1: off + 8])
+        wrong = {"all_right": [], "all_wrong": list(range(7)),
+                 "alternating": [] if r % 2 == 0 else [0], "cycling": [r % 8] if r % 8 < 7 else []}[mode]
+        for j in wrong:
+            d[j] = (d[j] + 1) % (TINY.vocab - 1)
+        o, recs = ls.step(forced=np.array([d], np.int32), tol=TOL)
+        assert recs[0]["n"] == (min(wrong) if wrong else 7)
+        stream += recs[0]["committed"]
+    assert stream == greedy[:len(stream)]
+    ls.close()
+
+
+def test_small_shape_bf16():
+    ls = _lockstep(SMALL_R, 4)
+    for _ in range(4):
+        ls.step(tol=TOL)
+    ls.close()
+
+
+def test_b32_shape_bf16_ragged():
+    ls = _lockstep(B32_R, 3)
+    for _ in range(3):
+        ls.step(tol=TOL)
+    ls.close()
+
+
+def test_b32_shape_graph_rounds_ints_only():
+    """Rounds without float outputs replay the captured CUDA graph."""
+    ls = _lockstep(B32_R, 4, seqs=[0, 5, 31])
+    for _ in range(4):
+        ls.step(floats=False)
+    assert ls.gpu.launches_per_round() > 0
+    ls.close()
+
+
+def test_hybrid_shape_snapshot_swap():
+    ls = _lockstep(HYB_R, 6)
+    greedy = [_greedy(ls, b, 8 * 6 + 9) for b in range(HYB_R.batch)]
+    for r in range(6):
+        forced = []
+        for b in range(HYB_R.batch):
+            off = ls.states[b].a - len(ls.prompts[b])
+            d = list(greedy[b][off + 1: off + 8])
+            j = (r + b) % 8
+            if j < 7:
+                d[j] = (d[j] + 1) % (HYB_R.vocab - 1)
+            forced.append(d)
+        o, recs = ls.step(forced=np.array(forced, np.int32), tol=TOL)
+        for b in range(HYB_R.batch):
+            assert recs[b]["n"] == min((r + b) % 8, 7)
+            assert int(o["snap_slot"][b]) == recs[b]["n"]
+    ls.close()
+
+
+def test_round_host_matches_device_outputs():
+    from mtp_block_draft_gb300 import DmtpRound, default_max_ctx
+    w = make_weights(B32_R, "cuda")
+    prompts = make_prompts(B32_R)
+    a = DmtpRound(B32_R, w, prompts, default_max_ctx(prompts, 4))
+    b = DmtpRound(B32_R, w, prompts, default_max_ctx(prompts, 4))
+    for _ in range(3):
+        out = a.alloc_out()
+        a.round(out)
+        committed = np.zeros((B32_R.batch, 8), np.int32)
+        n = np.zeros(B32_R.batch, np.int32)
+        b.round_host(committed, n)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(out["committed"].cpu().numpy(), committed)
+        np.testing.assert_array_equal(out["n_accepted"].cpu().numpy(), n)
+    a.close()
+    b.close()
