@@ -43,10 +43,10 @@ __global__ void __launch_bounds__(256) k_attn_partial(AttnArgs a) {
   const float scale = rsqrtf((float)hd);
 
   float qr[kMaxDPT], acc[kMaxDPT];
-  const T* qp = (const T*)a.q + ((long)(b * 8 + s) * a.hq + h) * hd;
+  const float* qp = a.q + ((long)(b * 8 + s) * a.hq + h) * hd;
 #pragma unroll
   for (int i = 0; i < kMaxDPT; ++i) {
-    qr[i] = (i < DPT) ? to_f32(qp[sub + TPQ * i]) * scale : 0.f;
+    qr[i] = (i < DPT) ? qp[sub + TPQ * i] * scale : 0.f;
     acc[i] = 0.f;
   }
   float m = -INFINITY, l = 0.f;
@@ -129,7 +129,7 @@ __global__ void k_attn_merge(AttnArgs a) {
       const float mc = a.part_ml[((p0 + c) * QN + qi) * 2];
       o += a.part_o[((p0 + c) * QN + qi) * a.hd + dd] * __expf(mc - M);
     }
-    ((T*)a.out)[(long)mrow * a.hq * a.hd + h * a.hd + dd] = from_f32<T>(o * invL);
+    store_act((T*)a.out + (long)mrow * a.hq * a.hd + h * a.hd + dd, a.out_lo, o * invL);
   }
 }
 

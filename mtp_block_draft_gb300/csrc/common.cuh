@@ -28,6 +28,19 @@ template <typename T> __device__ __forceinline__ T from_f32(float x);
 template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
 template <> __device__ __forceinline__ bf16 from_f32<bf16>(float x) { return __float2bfloat16_rn(x); }
 
+// Store one element of a GEMM operand. bf16 storage writes the rounded value at p[0]
+// and, when lo_off != 0, the bf16 rounding remainder v - hi at p[lo_off] (the "lo"
+// half: hi + lo carries ~16 significant bits). fp32 storage keeps v itself.
+__device__ __forceinline__ void store_act(float* p, long lo_off, float v) {
+  (void)lo_off;
+  p[0] = v;
+}
+__device__ __forceinline__ void store_act(bf16* p, long lo_off, float v) {
+  const bf16 h = __float2bfloat16_rn(v);
+  p[0] = h;
+  if (lo_off) p[lo_off] = __float2bfloat16_rn(v - __bfloat162float(h));
+}
+
 __device__ __forceinline__ void set_err(unsigned* err, unsigned bit) {
   if (err) atomicOr(err, bit);
 }

@@ -46,6 +46,7 @@ struct dmtp_ctx {
   int tap_of_layer[DMTP_MAX_LAYERS];  // tap slot of layer l, or -1
   int pmax;
   int attn_chunk, attn_nchunk;
+  int mt8, mt6, mt1;  // padded GEMM token rows for 8B, 6B and B operand rows
   size_t ws_bytes;
 
   // workspace regions
@@ -59,7 +60,7 @@ struct dmtp_ctx {
   float* x;
   void* xn;
   float* qkv;
-  void* q;
+  float* q;
   float *part_o, *part_ml;
   void* att;
   float* gu;
@@ -68,6 +69,7 @@ struct dmtp_ctx {
   float* hT32;
   void* hTn;
   void* z;
+  void* zf;
   float* xm;
   float* cacc;
   void* cn;
@@ -176,6 +178,9 @@ int derive(dmtp_ctx* c, const dmtp_config* cfg, int B) {
     for (int k : ks)
       if (k % 64) return DMTP_EINVAL;
   }
+  c->mt8 = tc_mt(c->M);
+  c->mt6 = tc_mt(6 * B);
+  c->mt1 = tc_mt(B);
   c->attn_chunk = 256;
   c->attn_nchunk = (c->maxc + 8 + c->attn_chunk - 1) / c->attn_chunk;
   return DMTP_OK;
@@ -204,27 +209,32 @@ size_t layout(dmtp_ctx* c, char* base) {
   c->rope = b.take<float2>((size_t)(c->maxc + 16) * (c->hd / 2) * sizeof(float2));
   const size_t M = c->M, d = c->d, B = c->B;
   const int qkvw = std::max(std::max(c->qkvd, c->gld), 2 * c->kvd);
+  // GEMM operand buffers hold [hi; lo] halves of mt rows each on the bf16 path
+  const size_t r8 = c->dt ? 2 * (size_t)c->mt8 : M;
+  const size_t r6 = c->dt ? 2 * (size_t)c->mt6 : 6 * B;
+  const size_t r1 = c->dt ? 2 * (size_t)c->mt1 : B;
   c->x = b.take<float>(M * d * 4);
-  c->xn = b.take<char>(M * d * es);
+  c->xn = b.take<char>(r8 * d * es);
   c->qkv = b.take<float>(M * qkvw * 4);
-  c->q = b.take<char>(M * c->qd * es);
+  c->q = b.take<float>(M * c->qd * 4);
   const int QN = 8 * (c->hq / c->hkv);
   c->part_o = b.take<float>(B * c->hkv * c->attn_nchunk * QN * c->hd * 4);
   c->part_ml = b.take<float>(B * c->hkv * c->attn_nchunk * QN * 2 * 4);
-  c->att = b.take<char>(M * std::max(c->qd, c->gH * c->gdv) * es);
+  c->att = b.take<char>(r8 * std::max(c->qd, c->gH * c->gdv) * es);
   c->gu = b.take<float>(M * 2 * c->F * 4);
-  c->hmid = b.take<char>(M * c->F * es);
-  c->taps = b.take<char>(M * c->ntap * d * es);
+  c->hmid = b.take<char>(r8 * c->F * es);
+  c->taps = b.take<char>(r8 * c->ntap * d * es);
   c->hT32 = b.take<float>(M * d * 4);
-  c->hTn = b.take<char>(M * d * es);
-  c->z = b.take<char>(M * 2 * d * es);
+  c->hTn = b.take<char>(r8 * d * es);
+  c->z = b.take<char>(r8 * 2 * d * es);
+  c->zf = b.take<char>(r1 * 2 * d * es);
   c->xm = b.take<float>(M * d * 4);
   c->cacc = b.take<float>(M * d * 4);
-  c->cn = b.take<char>(M * d * es);
+  c->cn = b.take<char>(r8 * d * es);
   c->delta = b.take<float>(B * d * 4);
   c->h_mtp = b.take<float>(B * d * 4);
-  c->t1in = b.take<char>(B * d * es);
-  c->dn = b.take<char>(6 * B * d * es);
+  c->t1in = b.take<char>(r1 * d * es);
+  c->dn = b.take<char>(r6 * d * es);
   c->hlast = b.take<float>(B * d * 4);
   c->forced = b.take<int>(B * 7 * 4);
   RoundState& s = c->rs;
@@ -265,7 +275,8 @@ int plan(dmtp_ctx* c, Gemm& g, const void* W, int N, int K, const void* X, int M
   g.M = M;
   g.argmax = argmax;
   if (!W) return DMTP_EINVAL;
-  if (c->dt == 1) return tc_plan(&g.tc, W, N, K, X, M, c->nsm, argmax) ? DMTP_EINVAL : DMTP_OK;
+  if (c->dt == 1)
+    return tc_plan(&g.tc, W, N, K, X, M, c->nsm, argmax, true) ? DMTP_EINVAL : DMTP_OK;
   return DMTP_OK;
 }
 
@@ -341,10 +352,18 @@ void gemm_argmax(dmtp_ctx* c, const Gemm& g, unsigned long long* keys, float* lo
 
 void zero(dmtp_ctx* c, void* p, size_t bytes) { cudaMemsetAsync(p, 0, bytes, c->st); }
 
+// element offset of the remainder half of an operand with `mt` padded rows of `ld`
+inline long lo_of(const dmtp_ctx* c, int mt, int ld) { return c->dt ? (long)mt * ld : 0; }
+inline int mt_of_rows(const dmtp_ctx* c, int rows) {
+  return rows == c->M ? c->mt8 : (rows == 6 * c->B ? c->mt6 : c->mt1);
+}
+
 void norm(dmtp_ctx* c, const float* x, const void* g, void* y, float* y32, void* tap, int rows,
           RowMap map = RowMap()) {
   launch(c, P_OTHER, 0, 0, [&] {
-    op_rmsnorm(c->dt, x, c->d, g, y, c->d, y32, c->d, tap, c->ntap * c->d, rows, c->d,
+    const int mt = mt_of_rows(c, rows);
+    op_rmsnorm(c->dt, x, c->d, g, y, c->d, lo_of(c, mt, c->d), y32, c->d, tap, c->ntap * c->d,
+               lo_of(c, c->mt8, c->ntap * c->d), rows, c->d,
                c->cfg.rms_eps, map, c->st);
   });
 }
@@ -376,6 +395,7 @@ void attn_layer(dmtp_ctx* c, const LayerPlans& p, const dmtp_layer_weights& w, f
   aa.part_o = c->part_o;
   aa.part_ml = c->part_ml;
   aa.out = c->att;
+  aa.out_lo = lo_of(c, c->mt8, c->qd);
   aa.base = a.base;
   aa.causal = a.causal;
   aa.lo_fixed = a.lo_fixed;
@@ -405,7 +425,7 @@ void attn_layer(dmtp_ctx* c, const LayerPlans& p, const dmtp_layer_weights& w, f
   norm(c, xr, w.mlp_norm, c->xn, nullptr, nullptr, M);
   zero(c, c->gu, (size_t)M * 2 * c->F * 4);
   gemm_acc(c, p.gu, c->gu, 2 * c->F);
-  launch(c, P_OTHER, 0, 0, [&] { op_swiglu(c->dt, c->gu, c->hmid, M, c->F, c->st); });
+  launch(c, P_OTHER, 0, 0, [&] { op_swiglu(c->dt, c->gu, c->hmid, lo_of(c, c->mt8, c->F), M, c->F, c->st); });
   gemm_acc(c, p.down, xr, c->d);
 }
 
@@ -428,6 +448,7 @@ void gdn_layer(dmtp_ctx* c, int l, float* xr, void* tap_in, bool snapshots) {
   ga.rows_valid = c->rs.rows_valid;
   ga.snapshots = snapshots ? 1 : 0;
   ga.out = c->att;
+  ga.out_lo = lo_of(c, c->mt8, c->gH * c->gdv);
   ga.B = c->B;
   ga.H = c->gH;
   ga.dk = c->gdk;
@@ -439,7 +460,7 @@ void gdn_layer(dmtp_ctx* c, int l, float* xr, void* tap_in, bool snapshots) {
   norm(c, xr, w.mlp_norm, c->xn, nullptr, nullptr, M);
   zero(c, c->gu, (size_t)M * 2 * c->F * 4);
   gemm_acc(c, p.gu, c->gu, 2 * c->F);
-  launch(c, P_OTHER, 0, 0, [&] { op_swiglu(c->dt, c->gu, c->hmid, M, c->F, c->st); });
+  launch(c, P_OTHER, 0, 0, [&] { op_swiglu(c->dt, c->gu, c->hmid, lo_of(c, c->mt8, c->F), M, c->F, c->st); });
   gemm_acc(c, p.down, xr, c->d);
 }
 
@@ -483,7 +504,7 @@ void mtp_advance(dmtp_ctx* c) {
   ph.g = c->w.mtp_norm_h;
   pe.tok = c->rs.mtp_tok;
   pe.g = c->w.mtp_norm_e;
-  launch(c, P_OTHER, 0, 0, [&] { op_concat_rms2(c->dt, c->w.emb, c->V, ph, pe, c->z, M, c->d, c->cfg.rms_eps, c->err, c->st); });
+  launch(c, P_OTHER, 0, 0, [&] { op_concat_rms2(c->dt, c->w.emb, c->V, ph, pe, c->z, lo_of(c, c->mt8, 2 * c->d), M, c->d, c->cfg.rms_eps, c->err, c->st); });
   zero(c, c->xm, (size_t)M * c->d * 4);
   gemm_acc(c, c->mproj, c->xm, c->d);
   AttnSpec a{c->mK, c->mV, c->rs.mtp_base, 1, 1, 0, 2};
@@ -511,7 +532,7 @@ void enqueue_round(dmtp_ctx* c, const Dbg& dbg, const int* forced) {
   pm.src32 = c->h_mtp;
   pm.ld = c->d;
   pm.g = c->w.fuse_norm_m;
-  launch(c, P_OTHER, 0, 0, [&] { op_concat_rms2(c->dt, c->w.emb, c->V, pe, pm, c->z, B, c->d, c->cfg.rms_eps, c->err, c->st); });
+  launch(c, P_OTHER, 0, 0, [&] { op_concat_rms2(c->dt, c->w.emb, c->V, pe, pm, c->zf, lo_of(c, c->mt1, 2 * c->d), B, c->d, c->cfg.rms_eps, c->err, c->st); });
   zero(c, c->delta, (size_t)B * c->d * 4);
   gemm_acc(c, c->fuse, c->delta, c->d);
   launch(c, P_OTHER, 0, 0, [&] { op_build_slots(c->dt, c->w.emb, c->V, s.A, s.drafts, c->delta, c->cfg.mask_id, c->x, B, c->d,
@@ -628,7 +649,7 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
                2 * c->kvd, c->d, c->cn, M, false);
   }
   pr |= plan_layer(c, c->mtp, w->mtp, 0, M);
-  pr |= plan(c, c->fuse, w->fuse_w, c->d, 2 * c->d, c->z, B, false);
+  pr |= plan(c, c->fuse, w->fuse_w, c->d, 2 * c->d, c->zf, B, false);
   pr |= plan(c, c->head_t1, w->head, c->V, c->d, c->t1in, B, true);
   pr |= plan(c, c->head_d, w->head, c->V, c->d, c->dn, 6 * B, true);
   pr |= plan(c, c->head_v, w->head, c->V, c->d, c->hTn, M, true);
@@ -645,6 +666,8 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
   // ---- initial device state ----
   cudaStream_t st = c->st;
   RoundState& s = c->rs;
+  // padding rows of the GEMM operands are read (and ignored): start from zeros
+  zero(c, workspace, need);
   zero(c, c->err, 4);
   zero(c, s.hist, 64);
   zero(c, s.keys, (size_t)B * 16 * 8);
@@ -684,7 +707,8 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
     }
   }
   // A = the target's greedy token after the prompt; MTP consumes (h^T_{P-1}, A) at P
-  op_cast_rows(c->dt, c->hlast, c->d, c->t1in, c->d, B, c->d, RowMap(), st);
+  op_cast_rows(c->dt, c->hlast, c->d, c->t1in, c->d, lo_of(c, c->mt1, c->d), B, c->d, RowMap(),
+               st);
   zero(c, s.keys, (size_t)B * 8);
   gemm_argmax(c, c->head_t1, s.keys, nullptr);
   op_keys_to_ids(s.keys, B, 1, s.A, 1, 0, nullptr, 0, 0, st);

@@ -21,8 +21,9 @@ __device__ __forceinline__ int map_row(int r, RowMap m) {
 // ---------------------------------------------------------------------------------
 template <typename T>
 __global__ void k_rmsnorm(const float* __restrict__ x, int ldx, const T* __restrict__ g,
-                          T* __restrict__ y, int ldy, float* __restrict__ y32, int ld32,
-                          T* __restrict__ tap, int ldtap, int d, float eps, RowMap map) {
+                          T* __restrict__ y, int ldy, long y_lo, float* __restrict__ y32,
+                          int ld32, T* __restrict__ tap, int ldtap, long tap_lo, int d,
+                          float eps, RowMap map) {
   __shared__ float red[32];
   const int r = blockIdx.x;
   const float* xr = x + (long)map_row(r, map) * ldx;
@@ -30,27 +31,27 @@ __global__ void k_rmsnorm(const float* __restrict__ x, int ldx, const T* __restr
   for (int i = threadIdx.x; i < d; i += blockDim.x) {
     float v = xr[i];
     ss += v * v;
-    if (tap) tap[(long)r * ldtap + i] = from_f32<T>(v);
+    if (tap) store_act(tap + (long)r * ldtap + i, tap_lo, v);
   }
   ss = block_sum(ss, red);
   const float inv = rsqrtf(ss / (float)d + eps);
   for (int i = threadIdx.x; i < d; i += blockDim.x) {
     float v = xr[i] * inv * to_f32(g[i]);
-    if (y) y[(long)r * ldy + i] = from_f32<T>(v);
+    if (y) store_act(y + (long)r * ldy + i, y_lo, v);
     if (y32) y32[(long)r * ld32 + i] = v;
   }
 }
 
-void op_rmsnorm(int dt, const float* x, int ldx, const void* g, void* y, int ldy, float* y32,
-                int ld32, void* tap, int ldtap, int rows, int d, float eps, RowMap map,
-                cudaStream_t st) {
+void op_rmsnorm(int dt, const float* x, int ldx, const void* g, void* y, int ldy, long y_lo,
+                float* y32, int ld32, void* tap, int ldtap, long tap_lo, int rows, int d,
+                float eps, RowMap map, cudaStream_t st) {
   if (rows <= 0) return;
   if (dt)
-    k_rmsnorm<bf16><<<rows, 256, 0, st>>>(x, ldx, (const bf16*)g, (bf16*)y, ldy, y32, ld32,
-                                          (bf16*)tap, ldtap, d, eps, map);
+    k_rmsnorm<bf16><<<rows, 256, 0, st>>>(x, ldx, (const bf16*)g, (bf16*)y, ldy, y_lo, y32, ld32,
+                                          (bf16*)tap, ldtap, tap_lo, d, eps, map);
   else
-    k_rmsnorm<float><<<rows, 256, 0, st>>>(x, ldx, (const float*)g, (float*)y, ldy, y32, ld32,
-                                           (float*)tap, ldtap, d, eps, map);
+    k_rmsnorm<float><<<rows, 256, 0, st>>>(x, ldx, (const float*)g, (float*)y, ldy, y_lo, y32,
+                                           ld32, (float*)tap, ldtap, tap_lo, d, eps, map);
 }
 
 // ---------------------------------------------------------------------------------
@@ -85,8 +86,8 @@ void op_embed(int dt, const void* E, const int* tok, int vocab, float* x, int ro
 // z[r] = [RMS(a) * ga ; RMS(b) * gb]
 // ---------------------------------------------------------------------------------
 template <typename T>
-__device__ void rms_part(const T* E, int vocab, const ConcatPart& p, int r, T* out, int d,
-                         float eps, unsigned* err, float* red) {
+__device__ void rms_part(const T* E, int vocab, const ConcatPart& p, int r, T* out, long lo,
+                         int d, float eps, unsigned* err, float* red) {
   const float* s32 = nullptr;
   const T* se = nullptr;
   if (p.src32) {
@@ -105,28 +106,28 @@ __device__ void rms_part(const T* E, int vocab, const ConcatPart& p, int r, T* o
   const T* g = (const T*)p.g;
   for (int i = threadIdx.x; i < d; i += blockDim.x) {
     float v = s32 ? s32[i] : to_f32(se[i]);
-    out[i] = from_f32<T>(v * inv * to_f32(g[i]));
+    store_act(out + i, lo, v * inv * to_f32(g[i]));
   }
 }
 
 template <typename T>
-__global__ void k_concat_rms2(const T* E, int vocab, ConcatPart a, ConcatPart b, T* z, int d,
-                              float eps, unsigned* err) {
+__global__ void k_concat_rms2(const T* E, int vocab, ConcatPart a, ConcatPart b, T* z, long z_lo,
+                              int d, float eps, unsigned* err) {
   __shared__ float red[32];
   const int r = blockIdx.x;
-  rms_part<T>(E, vocab, a, r, z + (long)r * 2 * d, d, eps, err, red);
+  rms_part<T>(E, vocab, a, r, z + (long)r * 2 * d, z_lo, d, eps, err, red);
   __syncthreads();
-  rms_part<T>(E, vocab, b, r, z + (long)r * 2 * d + d, d, eps, err, red);
+  rms_part<T>(E, vocab, b, r, z + (long)r * 2 * d + d, z_lo, d, eps, err, red);
 }
 
 void op_concat_rms2(int dt, const void* E, int vocab, ConcatPart a, ConcatPart b, void* z,
-                    int rows, int d, float eps, unsigned* err, cudaStream_t st) {
+                    long z_lo, int rows, int d, float eps, unsigned* err, cudaStream_t st) {
   if (dt)
-    k_concat_rms2<bf16><<<rows, 256, 0, st>>>((const bf16*)E, vocab, a, b, (bf16*)z, d, eps,
-                                              err);
+    k_concat_rms2<bf16><<<rows, 256, 0, st>>>((const bf16*)E, vocab, a, b, (bf16*)z, z_lo, d,
+                                              eps, err);
   else
-    k_concat_rms2<float><<<rows, 256, 0, st>>>((const float*)E, vocab, a, b, (float*)z, d, eps,
-                                               err);
+    k_concat_rms2<float><<<rows, 256, 0, st>>>((const float*)E, vocab, a, b, (float*)z, z_lo, d,
+                                               eps, err);
 }
 
 // ---------------------------------------------------------------------------------
@@ -162,20 +163,20 @@ void op_build_slots(int dt, const void* E, int vocab, const int* A, const int* d
 // SwiGLU
 // ---------------------------------------------------------------------------------
 template <typename T>
-__global__ void k_swiglu(const float* __restrict__ gu, T* __restrict__ h, int F) {
+__global__ void k_swiglu(const float* __restrict__ gu, T* __restrict__ h, long h_lo, int F) {
   const int m = blockIdx.y;
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= F) return;
   const float gv = gu[(long)m * 2 * F + i], uv = gu[(long)m * 2 * F + F + i];
-  h[(long)m * F + i] = from_f32<T>(gv / (1.f + __expf(-gv)) * uv);
+  store_act(h + (long)m * F + i, h_lo, gv / (1.f + __expf(-gv)) * uv);
 }
 
-void op_swiglu(int dt, const float* gu, void* h, int rows, int F, cudaStream_t st) {
+void op_swiglu(int dt, const float* gu, void* h, long h_lo, int rows, int F, cudaStream_t st) {
   dim3 grid(cdiv(F, 256), rows);
   if (dt)
-    k_swiglu<bf16><<<grid, 256, 0, st>>>(gu, (bf16*)h, F);
+    k_swiglu<bf16><<<grid, 256, 0, st>>>(gu, (bf16*)h, h_lo, F);
   else
-    k_swiglu<float><<<grid, 256, 0, st>>>(gu, (float*)h, F);
+    k_swiglu<float><<<grid, 256, 0, st>>>(gu, (float*)h, h_lo, F);
 }
 
 // ---------------------------------------------------------------------------------
@@ -203,7 +204,7 @@ void op_rope_table(float2* tab, int npos, int hd, float theta, cudaStream_t st) 
 // ---------------------------------------------------------------------------------
 template <typename T>
 __global__ void k_rope_kv(const float* __restrict__ src, int ld, int q_off, int k_off, int v_off,
-                          T* __restrict__ q_out, T* __restrict__ Kc, T* __restrict__ Vc,
+                          float* __restrict__ q_out, T* __restrict__ Kc, T* __restrict__ Vc,
                           const int* __restrict__ base, const float2* __restrict__ tab, int hq,
                           int hkv, int hd, int max_ctx, unsigned* err) {
   const int m = blockIdx.x, b = m >> 3, s = m & 7;
@@ -218,9 +219,9 @@ __global__ void k_rope_kv(const float* __restrict__ src, int ld, int q_off, int 
       const int h = idx / half, i = idx % half;
       const float x1 = row[q_off + h * hd + i], x2 = row[q_off + h * hd + half + i];
       const float2 cs = tr[i];
-      T* qo = q_out + ((long)m * hq + h) * hd;
-      qo[i] = from_f32<T>(x1 * cs.x - x2 * cs.y);
-      qo[half + i] = from_f32<T>(x2 * cs.x + x1 * cs.y);
+      float* qo = q_out + ((long)m * hq + h) * hd;
+      qo[i] = x1 * cs.x - x2 * cs.y;
+      qo[half + i] = x2 * cs.x + x1 * cs.y;
     }
   }
   if (!pos_ok) return;
@@ -237,32 +238,31 @@ __global__ void k_rope_kv(const float* __restrict__ src, int ld, int q_off, int 
   }
 }
 
-void op_rope_kv(int dt, const float* src, int ld, int q_off, int k_off, int v_off, void* q_out,
+void op_rope_kv(int dt, const float* src, int ld, int q_off, int k_off, int v_off, float* q_out,
                 void* Kc, void* Vc, const int* base, const float2* tab, int rows, int hq, int hkv,
                 int hd, int max_ctx, unsigned* err, cudaStream_t st) {
   if (dt)
-    k_rope_kv<bf16><<<rows, 256, 0, st>>>(src, ld, q_off, k_off, v_off, (bf16*)q_out, (bf16*)Kc,
+    k_rope_kv<bf16><<<rows, 256, 0, st>>>(src, ld, q_off, k_off, v_off, q_out, (bf16*)Kc,
                                           (bf16*)Vc, base, tab, hq, hkv, hd, max_ctx, err);
   else
-    k_rope_kv<float><<<rows, 256, 0, st>>>(src, ld, q_off, k_off, v_off, (float*)q_out,
-                                           (float*)Kc, (float*)Vc, base, tab, hq, hkv, hd,
-                                           max_ctx, err);
+    k_rope_kv<float><<<rows, 256, 0, st>>>(src, ld, q_off, k_off, v_off, q_out, (float*)Kc,
+                                           (float*)Vc, base, tab, hq, hkv, hd, max_ctx, err);
 }
 
 template <typename T>
 __global__ void k_cast_rows(const float* __restrict__ x, int ldx, T* __restrict__ y, int ldy,
-                            int d, RowMap map) {
+                            long y_lo, int d, RowMap map) {
   const int r = blockIdx.x;
   const float* xr = x + (long)map_row(r, map) * ldx;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) y[(long)r * ldy + i] = from_f32<T>(xr[i]);
+  for (int i = threadIdx.x; i < d; i += blockDim.x) store_act(y + (long)r * ldy + i, y_lo, xr[i]);
 }
 
-void op_cast_rows(int dt, const float* x, int ldx, void* y, int ldy, int rows, int d, RowMap map,
-                  cudaStream_t st) {
+void op_cast_rows(int dt, const float* x, int ldx, void* y, int ldy, long y_lo, int rows, int d,
+                  RowMap map, cudaStream_t st) {
   if (dt)
-    k_cast_rows<bf16><<<rows, 256, 0, st>>>(x, ldx, (bf16*)y, ldy, d, map);
+    k_cast_rows<bf16><<<rows, 256, 0, st>>>(x, ldx, (bf16*)y, ldy, y_lo, d, map);
   else
-    k_cast_rows<float><<<rows, 256, 0, st>>>(x, ldx, (float*)y, ldy, d, map);
+    k_cast_rows<float><<<rows, 256, 0, st>>>(x, ldx, (float*)y, ldy, y_lo, d, map);
 }
 
 // ---------------------------------------------------------------------------------

@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(256) k_gdn(GdnArgs a) {
     for (int c = 0; c < 64; ++c)
       if (c < cpt) o += S[c] * qs[j0 + c];
     for (int w = TPR >> 1; w > 0; w >>= 1) o += __shfl_xor_sync(0xffffffffu, o, w);
-    if (sub == 0) ((T*)a.out)[(long)(b * 8 + r) * a.H * dv + h * dv + i] = from_f32<T>(o);
+    if (sub == 0) store_act((T*)a.out + (long)(b * 8 + r) * a.H * dv + h * dv + i, a.out_lo, o);
     if (a.snapshots && r < 7) {
       float* Sd = Sbuf + ((long)a.slot[b * 8 + r] * a.H + h) * hstride + (long)i * dk + j0;
 #pragma unroll

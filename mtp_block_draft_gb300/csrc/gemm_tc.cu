@@ -16,6 +16,12 @@
 //   warp 2: TMEM allocation; all 4 warps: epilogue (TMEM lane = weight row).
 // Stages are 64-element (128 B) k slices with 128-byte swizzle.
 //
+// Split activations: the token operand may come as two bf16 halves, X = X_hi + X_lo
+// (X_lo = the rounding remainder of X_hi), stored as 2*MT rows [hi; lo]. Both halves
+// are multiplied by the same weight tile (one TMA load of W, two MMA column ranges)
+// and summed in the epilogue, so the activations keep ~16 significant bits while the
+// weights stay bf16 and each weight byte is still read once.
+//
 // The LM-head variant fuses the row argmax (DMTP blog §6.5: the vocabulary output
 // layer scores every token): per column the CTA reduces its 128 vocabulary rows to a
 // packed (value, index) key and merges it with one 64-bit atomicMax per column.
@@ -37,6 +43,8 @@ static constexpr uint32_t kWBytes = kTileN * kBlockK * 2;
 
 struct TcArgs {
   int N, K, M, MT, stages;
+  int split;       // 1: X holds [hi; lo] halves of MT rows each
+  int xbox, nx;    // X rows per TMA load / MMA, loads per stage
   float* out;
   int ldo;
   unsigned long long* keys;
@@ -59,7 +67,7 @@ __global__ void __launch_bounds__(128, 1)
   uint8_t* smem =
       smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);  // 1024-B aligned tiles
   const int S = a.stages;
-  const uint32_t xbytes = (uint32_t)a.MT * kBlockK * 2;
+  const uint32_t xbytes = (uint32_t)a.xbox * a.nx * kBlockK * 2;
   uint8_t* sW = smem;
   uint8_t* sX = smem + S * kWBytes;
   uint64_t* full = (uint64_t*)(sX + S * xbytes);
@@ -73,7 +81,7 @@ __global__ void __launch_bounds__(128, 1)
   const int nkb = a.K / kBlockK;
   const int kb0 = (int)((long)blockIdx.y * nkb / gridDim.y);
   const int kb1 = (int)((long)(blockIdx.y + 1) * nkb / gridDim.y);
-  const uint32_t ncols = tmem_cols_for(a.MT);
+  const uint32_t ncols = tmem_cols_for(a.xbox * a.nx);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
@@ -101,14 +109,16 @@ __global__ void __launch_bounds__(128, 1)
       if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, a.err)) break;
       mbar_expect_tx(smem_u32(&full[s]), kWBytes + xbytes);
       tma_load_2d(smem_u32(sW + s * kWBytes), &tmW, kb * kBlockK, n0, smem_u32(&full[s]), pw);
-      tma_load_2d(smem_u32(sX + s * xbytes), &tmX, kb * kBlockK, 0, smem_u32(&full[s]), px);
+      for (int j = 0; j < a.nx; ++j)
+        tma_load_2d(smem_u32(sX + s * xbytes + j * a.xbox * kBlockK * 2), &tmX, kb * kBlockK,
+                    j * a.xbox, smem_u32(&full[s]), px);
     }
     // drain: every stage's last issued load has landed before the CTA may exit
     for (int j = (issued > S ? issued - S : 0); j < issued; ++j)
       mbar_wait(smem_u32(&full[j % S]), (j / S) & 1, a.err);
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
-    const uint32_t idesc = umma_idesc_bf16(kTileN, a.MT);
+    const uint32_t idesc = umma_idesc_bf16(kTileN, a.xbox);
     int it = 0;
     for (int kb = kb0; kb < kb1; ++kb, ++it) {
       const int s = it % S;
@@ -116,10 +126,15 @@ __global__ void __launch_bounds__(128, 1)
       if (!mbar_wait(smem_u32(&full[s]), ph, a.err)) break;
       tc_fence_after();
       const uint64_t dw = umma_desc_sw128(smem_u32(sW + s * kWBytes));
-      const uint64_t dx = umma_desc_sw128(smem_u32(sX + s * xbytes));
 #pragma unroll
-      for (int k = 0; k < kBlockK / 16; ++k)  // +32 B per K=16 step inside the swizzle atom
-        umma_bf16(tmem, dw + 2 * k, dx + 2 * k, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+      for (int k = 0; k < kBlockK / 16; ++k) {  // +32 B per K=16 step inside the swizzle atom
+        for (int j = 0; j < a.nx; ++j) {
+          const uint64_t dx =
+              umma_desc_sw128(smem_u32(sX + s * xbytes + j * a.xbox * kBlockK * 2));
+          umma_bf16(tmem + j * a.xbox, dw + 2 * k, dx + 2 * k, idesc,
+                    (kb > kb0 || k > 0) ? 1u : 0u);
+        }
+      }
       umma_commit(smem_u32(&empty[s]));
     }
     umma_commit(smem_u32(accum));  // always: the epilogue waits on it
@@ -138,6 +153,12 @@ __global__ void __launch_bounds__(128, 1)
       for (int c = 0; c < a.MT; c += 16) {
         float v[16];
         tmem_ld16(tbase + c, v);
+        if (a.split) {
+          float w[16];
+          tmem_ld16(tbase + a.MT + c, w);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] += w[j];
+        }
         if (n < a.N) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -153,6 +174,12 @@ __global__ void __launch_bounds__(128, 1)
       for (int c = 0; c < a.MT; c += 16) {
         float v[16];
         tmem_ld16(tbase + c, v);
+        if (a.split) {
+          float w[16];
+          tmem_ld16(tbase + a.MT + c, w);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] += w[j];
+        }
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int m = c + j;
@@ -220,8 +247,8 @@ static int make_tmap(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t 
   return r == CUDA_SUCCESS ? 0 : -3;
 }
 
-static size_t smem_bytes(int MT, int stages, bool argmax) {
-  size_t b = 1024 + (size_t)stages * (kWBytes + (size_t)MT * kBlockK * 2);
+static size_t smem_bytes(int MT, int xrows, int stages, bool argmax) {
+  size_t b = 1024 + (size_t)stages * (kWBytes + (size_t)xrows * kBlockK * 2);
   b += (2 * stages + 2) * 8;
   if (argmax) b += 4 * (size_t)MT * 8;
   return b;
@@ -229,16 +256,23 @@ static size_t smem_bytes(int MT, int stages, bool argmax) {
 
 static constexpr size_t kSmemBudget = 200 * 1024;
 
-int tc_plan(TcPlan* p, const void* W, int N, int K, const void* X, int M, int nsm, bool argmax) {
+int tc_mt(int M) { return std::max(16, (M + 15) / 16 * 16); }
+
+int tc_plan(TcPlan* p, const void* W, int N, int K, const void* X, int M, int nsm, bool argmax,
+            bool split) {
   if (M < 1 || M > 256 || K % kBlockK || N < 1) return -10;
   p->N = N;
   p->K = K;
   p->M = M;
-  p->MT = std::max(16, (M + 15) / 16 * 16);
+  p->MT = tc_mt(M);
+  p->split = split ? 1 : 0;
+  const int xrows = split ? 2 * p->MT : p->MT;
+  p->xbox = xrows <= 256 ? xrows : p->MT;
+  p->nx = xrows / p->xbox;
   int st = 8;
-  while (st > 2 && smem_bytes(p->MT, st, argmax) > kSmemBudget) --st;
+  while (st > 2 && smem_bytes(p->MT, xrows, st, argmax) > kSmemBudget) --st;
   p->stages = st;
-  p->smem = smem_bytes(p->MT, st, argmax);
+  p->smem = smem_bytes(p->MT, xrows, st, argmax);
   const int tiles = (N + kTileN - 1) / kTileN;
   const int nkb = K / kBlockK;
   int best = 1;
@@ -257,7 +291,8 @@ int tc_plan(TcPlan* p, const void* W, int N, int K, const void* X, int M, int ns
   p->splits = best;
   int r = make_tmap(&p->tmW, W, (uint64_t)N, (uint64_t)K, kTileN);
   if (r) return r;
-  r = make_tmap(&p->tmX, X, (uint64_t)M, (uint64_t)K, (uint32_t)p->MT);
+  // split: the tensor spans both halves (rows >= M of each half are ignored columns)
+  r = make_tmap(&p->tmX, X, (uint64_t)(split ? xrows : M), (uint64_t)K, (uint32_t)p->xbox);
   return r;
 }
 
@@ -270,14 +305,16 @@ int tc_init_attributes() {
 }
 
 void op_gemm_tc_acc(const TcPlan& p, float* out, int ldo, unsigned* err, cudaStream_t st) {
-  TcArgs a{p.N, p.K, p.M, p.MT, p.stages, out, ldo, nullptr, nullptr, 0, err};
+  TcArgs a{p.N, p.K, p.M, p.MT, p.stages, p.split, p.xbox, p.nx, out, ldo, nullptr, nullptr, 0,
+           err};
   dim3 grid((p.N + kTileN - 1) / kTileN, p.splits);
   k_gemm_tc<0><<<grid, 128, p.smem, st>>>(p.tmW, p.tmX, a);
 }
 
 void op_gemm_tc_argmax(const TcPlan& p, unsigned long long* keys, float* logits, long ldl,
                        unsigned* err, cudaStream_t st) {
-  TcArgs a{p.N, p.K, p.M, p.MT, p.stages, nullptr, 0, keys, logits, ldl, err};
+  TcArgs a{p.N, p.K, p.M, p.MT, p.stages, p.split, p.xbox, p.nx, nullptr, 0, keys, logits, ldl,
+           err};
   dim3 grid((p.N + kTileN - 1) / kTileN, 1);
   k_gemm_tc<1><<<grid, 128, p.smem, st>>>(p.tmW, p.tmX, a);
 }

@@ -19,9 +19,10 @@ struct RowMap {
 // ---- elementwise.cu --------------------------------------------------------------
 // y[r] = RMSNorm(x[map(r)]) * g, stored as dt (y) and optionally as fp32 (y32);
 // tap (optional, dt): raw copy of x[map(r)] into column block of a tap buffer.
-void op_rmsnorm(int dt, const float* x, int ldx, const void* g, void* y, int ldy, float* y32,
-                int ld32, void* tap, int ldtap, int rows, int d, float eps, RowMap map,
-                cudaStream_t st);
+// *_lo arguments: element offset of the bf16 remainder half of a split operand (0: none).
+void op_rmsnorm(int dt, const float* x, int ldx, const void* g, void* y, int ldy, long y_lo,
+                float* y32, int ld32, void* tap, int ldtap, long tap_lo, int rows, int d,
+                float eps, RowMap map, cudaStream_t st);
 // x[m] = E[tok[m]] (fp32 rows)
 void op_embed(int dt, const void* E, const int* tok, int vocab, float* x, int rows, int d,
               unsigned* err, cudaStream_t st);
@@ -36,21 +37,21 @@ struct ConcatPart {
   const void* g = nullptr;
 };
 void op_concat_rms2(int dt, const void* E, int vocab, ConcatPart a, ConcatPart b, void* z,
-                    int rows, int d, float eps, unsigned* err, cudaStream_t st);
+                    long z_lo, int rows, int d, float eps, unsigned* err, cudaStream_t st);
 // Drafter slots: x[b*8+s] = E[A_b] (s=0), E[T1_b] + delta_b (s=1), E[mask] (s>=2)
 void op_build_slots(int dt, const void* E, int vocab, const int* A, const int* drafts,
                     const float* delta, int mask_id, float* x, int B, int d, unsigned* err,
                     cudaStream_t st);
 // h = silu(gu[:, :F]) * gu[:, F:] as dt
-void op_swiglu(int dt, const float* gu, void* h, int rows, int F, cudaStream_t st);
+void op_swiglu(int dt, const float* gu, void* h, long h_lo, int rows, int F, cudaStream_t st);
 // RoPE (table) + cache write. src rows m = b*8 + s at position base[b] + s.
-// q_off < 0: no q. q_out fp32 [rows][hq][hd] (dt==0) or bf16 (dt==1).
-void op_rope_kv(int dt, const float* src, int ld, int q_off, int k_off, int v_off, void* q_out,
+// q_off < 0: no q. q_out fp32 [rows][hq][hd].
+void op_rope_kv(int dt, const float* src, int ld, int q_off, int k_off, int v_off, float* q_out,
                 void* Kc, void* Vc, const int* base, const float2* rope_tab, int rows, int hq,
                 int hkv, int hd, int max_ctx, unsigned* err, cudaStream_t st);
 // fp32 -> dt copy of rows (with row map)
-void op_cast_rows(int dt, const float* x, int ldx, void* y, int ldy, int rows, int d, RowMap map,
-                  cudaStream_t st);
+void op_cast_rows(int dt, const float* x, int ldx, void* y, int ldy, long y_lo, int rows, int d,
+                  RowMap map, cudaStream_t st);
 void op_rope_table(float2* tab, int npos, int hd, float theta, cudaStream_t st);
 
 // ---- round control (elementwise.cu) -------------------------------------------------
@@ -99,10 +100,11 @@ void op_prefill_done(const RoundState& s, const int* plen, cudaStream_t st);
 struct AttnArgs {
   const void* Kc;      // [B][hkv][max_ctx][hd] dt
   const void* Vc;
-  const void* q;       // [B*8][hq][hd] (fp32 if dt==0 else bf16)
+  const float* q;      // [B*8][hq][hd] fp32
   float* part_o;       // [B][hkv][nchunk][QN][hd]
   float* part_ml;      // [B][hkv][nchunk][QN][2]
   void* out;           // [B*8][hq*hd] dt
+  long out_lo;         // element offset of the remainder half (0: none)
   const int* base;     // [B] position of row 0
   int causal;          // 1: row s sees keys <= base+s; 0: keys <= base+7
   int lo_fixed;        // lowest key index
@@ -123,11 +125,15 @@ void op_gemm_simt_argmax(const float* W, const float* X, int N, int K, int M,
 struct TcPlan {
   CUtensorMap tmW, tmX;
   int N, K, M, MT, splits, stages;
+  int split, xbox, nx;
   size_t smem;
 };
-// Builds the tensor maps and launch shape for out[M,N] = X[M,K] . W[N,K]^T.
+// Padded token rows of an M-row operand (multiple of 16, >= 16).
+int tc_mt(int M);
+// Builds the tensor maps and launch shape for out[M,N] = X[M,K] . W[N,K]^T. split: X
+// holds 2*tc_mt(M) rows, the bf16 high halves then the low halves (X = hi + lo).
 int tc_plan(TcPlan* p, const void* W, int N, int K, const void* X, int M, int nsm,
-            bool argmax);
+            bool argmax, bool split);
 void op_gemm_tc_acc(const TcPlan& p, float* out, int ldo, unsigned* err, cudaStream_t st);
 void op_gemm_tc_argmax(const TcPlan& p, unsigned long long* keys, float* logits, long ldl,
                        unsigned* err, cudaStream_t st);
@@ -143,6 +149,7 @@ struct GdnArgs {
   const int* rows_valid; // [B]
   int snapshots;         // 1: write the state after each row r < 7 to buffer slot[b][r]
   void* out;             // [B*8][H*dv] dt
+  long out_lo;           // element offset of the remainder half (0: none)
   int B, H, dk, dv;
   unsigned* err;
 };

@@ -24,6 +24,11 @@ is id V-1; drafter slot s (2..7) predicts the token at its own position a+s; the
 drafter context K/V at position p is RoPE(Wk c_p, p), Wv c_p with
 c_p = RMS(W_fc [taps at p]); Gated DeltaNet uses L2-normalised q, k, sigmoid gates,
 no short convolution and no output scale.
+
+Storage: weights arrive already in the model's storage type; K/V caches are stored in
+it too (bf16 models keep a bf16 KV cache), so keys and values are rounded to bf16
+(through float32, as the kernels produce them) when written. Everything else,
+including the Gated DeltaNet state, is computed and kept in float64.
 """
 from __future__ import annotations
 
@@ -112,6 +117,13 @@ def l2_normalize(x: np.ndarray) -> np.ndarray:
     return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True))
 
 
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest bfloat16 (ties to even, torch's conversion), back as float64."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float64))
+    return t.to(torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
+
+
 def argmax_first(logits: np.ndarray) -> int:
     """Greedy pick; exactly equal maxima resolve to the lowest id (np.argmax)."""
     return int(np.argmax(logits))
@@ -181,11 +193,15 @@ class SeqState:
 class OracleModel:
     """Target + MTP module + fusion + block drafter, float64, from synth weights."""
 
-    def __init__(self, cfg, weights: dict, gate: float = 0.05):
+    def __init__(self, cfg, weights: dict, gate: float = 0.05, kv_store: str | None = None):
+        """kv_store: storage type of every K/V cache ("bf16" or "fp32"); by default the
+        model's storage type (cfg.dtype). Stored keys and values are rounded to it when
+        written, as a bf16 KV cache holds them; every computation stays float64."""
         self.cfg = cfg
         self.W = {k: v.detach().to("cpu").double().numpy() if hasattr(v, "detach")
                   else np.asarray(v, dtype=F64) for k, v in weights.items()}
         self.gate = gate
+        self.kv_bf16 = (kv_store or cfg.dtype) == "bf16"
         c = cfg
         self.eps, self.theta = c.rms_eps, c.rope_theta
         self.hq, self.hkv, self.hd = c.n_heads, c.n_kv_heads, c.head_dim
@@ -208,7 +224,10 @@ class OracleModel:
         q = qkv[:, :self.qd].reshape(R, self.hq, self.hd)
         k = qkv[:, self.qd:self.qd + self.kvd].reshape(R, self.hkv, self.hd)
         v = qkv[:, self.qd + self.kvd:].reshape(R, self.hkv, self.hd)
-        return rope(q, pos, self.theta), rope(k, pos, self.theta), v
+        return rope(q, pos, self.theta), self._store(rope(k, pos, self.theta)), self._store(v)
+
+    def _store(self, kv: np.ndarray) -> np.ndarray:
+        return round_bf16(kv) if self.kv_bf16 else kv
 
     def attn_layer(self, pfx: str, x: np.ndarray, K: np.ndarray, V: np.ndarray,
                    pos0: int, key0: int = 0):
@@ -300,7 +319,7 @@ class OracleModel:
             w = W[f"D{j}.wqkv"]
             k = (c @ w[self.qd:self.qd + self.kvd].T).reshape(R, self.hkv, self.hd)
             v = (c @ w[self.qd + self.kvd:].T).reshape(R, self.hkv, self.hd)
-            out.append((rope(k, pos, self.theta), v))
+            out.append((self._store(rope(k, pos, self.theta)), self._store(v)))
         return out
 
     # ---- MTP module -----------------------------------------------------------------

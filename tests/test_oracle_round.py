@@ -300,3 +300,20 @@ def test_hybrid_lossless_and_swap_equals_replay(hyb):
             else:
                 np.testing.assert_array_equal(st.tgt_K[l], rp.tgt_K[l])
     assert stream == greedy[:len(stream)]
+
+
+def test_bf16_kv_storage_keeps_the_pins(prompt):
+    """With K/V stored as bf16 the caches hold bf16 values only, and the committed
+    stream still equals plain greedy decoding of the same (bf16-KV) model."""
+    w = make_weights(TINY, "cpu")
+    m = OracleModel(TINY, w, kv_store="bf16")
+    greedy = m.greedy_decode(prompt, 40)
+    _, stream, _ = _run(m, prompt, 5)
+    assert stream == greedy[:len(stream)]
+    st = m.prefill(prompt)
+    m.round(st)
+    for arr in [st.tgt_K[0], st.tgt_V[1], st.dft_K[0], st.mtp_V]:
+        np.testing.assert_array_equal(arr, O.round_bf16(arr))
+    # and the rounding is not a no-op: the exact model's caches differ
+    st2 = OracleModel(TINY, w).prefill(prompt)
+    assert np.abs(st2.tgt_K[0] - st.tgt_K[0][:st2.a]).max() > 0
