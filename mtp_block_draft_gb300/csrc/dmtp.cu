@@ -92,6 +92,7 @@ struct dmtp_ctx {
   Gemm fuse, head_t1, head_d, head_v, dfc, mproj;
 
   cudaGraphExec_t graph;
+  cudaStream_t cap_st;  // private stream the round is captured on (the caller's may be NULL)
   bool poisoned;
   long kv_bound;
   int launches;
@@ -769,13 +770,23 @@ int dmtp_round(dmtp_ctx* c, const dmtp_round_out* out, const int32_t* forced) {
     c->round_launches = c->launches;
   } else {
     if (!c->graph) {
-      cudaGraph_t g;
-      if (cudaStreamBeginCapture(c->st, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
+      // capture records work without running it, on a private stream (the legacy
+      // default stream cannot be captured); the graph is then replayed on c->st
+      if (!c->cap_st && cudaStreamCreateWithFlags(&c->cap_st, cudaStreamNonBlocking) != cudaSuccess)
         return DMTP_ECUDA;
+      cudaGraph_t g;
+      cudaStream_t user = c->st;
+      c->st = c->cap_st;
+      if (cudaStreamBeginCapture(c->st, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+        c->st = user;
+        return DMTP_ECUDA;
+      }
       c->launches = 0;
       enqueue_round(c, dbg, nullptr);
       c->round_launches = c->launches;
-      if (cudaStreamEndCapture(c->st, &g) != cudaSuccess) return DMTP_ECUDA;
+      const cudaError_t ce = cudaStreamEndCapture(c->st, &g);
+      c->st = user;
+      if (ce != cudaSuccess) return DMTP_ECUDA;
       if (cudaGraphInstantiate(&c->graph, g, 0) != cudaSuccess) {
         cudaGraphDestroy(g);
         c->graph = nullptr;
@@ -879,6 +890,7 @@ int dmtp_round_profile(dmtp_ctx* c, dmtp_profile* out) {
 void dmtp_free(dmtp_ctx* c) {
   if (!c) return;
   if (c->graph) cudaGraphExecDestroy(c->graph);
+  if (c->cap_st) cudaStreamDestroy(c->cap_st);
   for (cudaEvent_t e : c->pev) cudaEventDestroy(e);
   delete c;
 }

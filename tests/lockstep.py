@@ -84,4 +84,6 @@ class Lockstep:
         return o, recs
 
     def close(self):
+        print(f"[lockstep] {self.cfg.name}: max float error {self.max_err}, "
+              f"near-tie adoptions {len(self.adopted)}")
         self.gpu.close()
