@@ -171,6 +171,26 @@ typedef struct {
  * around every launch, synchronise and fill *out. For measurement, not for speed. */
 int dmtp_round_profile(dmtp_ctx* ctx, dmtp_profile* out);
 
+/* First-candidate head without any allocation (the pages have no counterpart; this
+ * serves embedders that may not call cudaMalloc, e.g. engines that own a fixed memory
+ * pool or paths where an allocation's implicit synchronisation is not acceptable).
+ * Computes, like step a1 of dmtp_round, ids[r] = argmax_v H[v] . RMSNorm(h[r]) * gain
+ * (lowest id on exact ties) and, if logits != NULL, logits[r][v] (fp32).
+ * head: device bf16 [vocab][d_model] (16-byte aligned); norm_gain: device bf16
+ * [d_model]; h: device fp32 [rows][d_model]; ids: device int32 [rows]; stream: a
+ * cudaStream_t or NULL. Limits: 1 <= rows <= DMTP_NOALLOC_MAX_ROWS,
+ * 64 <= d_model <= DMTP_NOALLOC_MAX_DMODEL, d_model % 64 == 0; otherwise DMTP_EINVAL.
+ * Its scratch is a fixed library-owned device array (about 0.5 MB, held by every GPU that
+ * loads the library until exit). The first call on a device sets that device up (symbol
+ * lookup, kernel attribute) and should come before any stream capture. Calls share the
+ * array: calls that may overlap on the GPU race and must be serialised by the caller.
+ * Asynchronous on `stream`. */
+#define DMTP_NOALLOC_MAX_ROWS 32
+#define DMTP_NOALLOC_MAX_DMODEL 4096
+int dmtp_t1_head_noalloc(const void* head, const void* norm_gain, const float* h, int rows,
+                         int vocab, int d_model, float eps, int32_t* ids, float* logits,
+                         void* stream);
+
 /* Release the context (host memory and the graph). Never fails; NULL is a no-op.
  * Does not free caller-owned device memory. */
 void dmtp_free(dmtp_ctx* ctx);

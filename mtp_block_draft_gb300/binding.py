@@ -26,7 +26,7 @@ ERRORS = {0: "DMTP_OK", -1: "DMTP_EINVAL", -2: "DMTP_ENOMEM", -3: "DMTP_ECAPACIT
 # every symbol include/dmtp.h declares
 EXPORTS = ("dmtp_workspace_size", "dmtp_init", "dmtp_round", "dmtp_round_host",
            "dmtp_read_state", "dmtp_round_launches", "dmtp_round_profile", "dmtp_free",
-           "dmtp_strerror")
+           "dmtp_strerror", "dmtp_t1_head_noalloc")
 
 PROFILE_CLASSES = ("gemm", "lm_head", "attention", "gdn", "other")
 
@@ -103,6 +103,8 @@ def load_library(path: str = LIB_PATH):
     lib.dmtp_round_profile.restype = C.c_int
     lib.dmtp_free.argtypes = [P]
     lib.dmtp_free.restype = None
+    lib.dmtp_t1_head_noalloc.argtypes = [P, P, P, C.c_int, C.c_int, C.c_int, C.c_float, P, P, P]
+    lib.dmtp_t1_head_noalloc.restype = C.c_int
     lib.dmtp_strerror.argtypes = [C.c_int]
     lib.dmtp_strerror.restype = C.c_char_p
     _lib = lib

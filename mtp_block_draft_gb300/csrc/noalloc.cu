@@ -1,0 +1,76 @@
+// dmtp_t1_head_noalloc: the first-candidate head (RMSNorm, LM head, row argmax) for
+// callers that must not allocate device memory.
+//
+// Some embedders cannot call cudaMalloc: a serving engine that owns a fixed memory pool
+// and forbids allocations outside it, or a latency-critical path where cudaMalloc /
+// cudaFree would synchronise the device. The round library already takes all of its
+// memory from the caller; this entry point goes further and needs no workspace at all.
+// Its scratch - the split bf16 operand of the head GEMM and the packed argmax keys - is
+// a file-scope __device__ array of fixed size that every GPU loading the library holds
+// until the process exits.
+//
+// The first call on a device sets up that device (it looks up the array's device address
+// with cudaGetSymbolAddress and raises the GEMM kernel's shared-memory limit); make that
+// first call before any stream capture. All calls share the one array: calls that may
+// overlap on the GPU (other streams, other threads) race on it and must be serialised by
+// the caller.
+#include <mutex>
+
+#include "../../include/dmtp.h"
+#include "common.cuh"
+#include "ops.h"
+
+namespace {
+
+constexpr int kMaxRows = DMTP_NOALLOC_MAX_ROWS;  // token rows per call
+constexpr int kMaxD = DMTP_NOALLOC_MAX_DMODEL;   // hidden size
+constexpr size_t kOperandBytes = (size_t)2 * kMaxRows * kMaxD * 2;  // [hi; lo] x d, bf16
+constexpr size_t kKeyBytes = (size_t)kMaxRows * 8;
+
+// The scratch: the GEMM operand, then the argmax keys.
+static __device__ __align__(256) unsigned char g_scratch[kOperandBytes + kKeyBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_addr[kMaxDevices] = {};
+
+int device_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DMTP_ECUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return DMTP_ECUDA;
+    if (dmtp::tc_init_attributes()) return DMTP_ECUDA;
+    g_addr[dev] = p;
+  }
+  *out = g_addr[dev];
+  return DMTP_OK;
+}
+
+}  // namespace
+
+extern "C" int dmtp_t1_head_noalloc(const void* head, const void* norm_gain, const float* h,
+                                    int rows, int vocab, int d_model, float eps, int32_t* ids,
+                                    float* logits, void* stream) {
+  if (!head || !norm_gain || !h || !ids) return DMTP_EINVAL;
+  if (rows < 1 || rows > kMaxRows || d_model < 64 || d_model > kMaxD || d_model % 64 ||
+      vocab < 1 || ((uintptr_t)head & 15))
+    return DMTP_EINVAL;
+  void* base = nullptr;
+  int r = device_scratch(&base);
+  if (r) return r;
+  cudaStream_t st = (cudaStream_t)stream;
+  void* X = base;
+  unsigned long long* keys = (unsigned long long*)((char*)base + kOperandBytes);
+  const int mt = dmtp::tc_mt(rows);
+  dmtp::TcPlan plan;
+  if (dmtp::tc_plan(&plan, head, vocab, d_model, X, rows, 1, true, true)) return DMTP_EINVAL;
+  // keys start at zero for the atomic max; the operand rows are fully rewritten
+  if (cudaMemsetAsync(keys, 0, (size_t)rows * 8, st) != cudaSuccess) return DMTP_ECUDA;
+  dmtp::op_rmsnorm(1, h, d_model, norm_gain, X, d_model, (long)mt * d_model, nullptr, 0,
+                   nullptr, 0, 0, rows, d_model, eps, dmtp::RowMap(), st);
+  dmtp::op_gemm_tc_argmax(plan, keys, logits, vocab, nullptr, st);
+  dmtp::op_keys_to_ids(keys, rows, 1, ids, 1, 0, nullptr, 0, 0, st);
+  return cudaPeekAtLastError() == cudaSuccess ? DMTP_OK : DMTP_ECUDA;
+}
