@@ -9,7 +9,10 @@
 //   target verify and MTP rows are causal: row s sees keys lo..base+s;
 //   the block drafter sees the anchor-relative window max(0, base-4096)..base-1 plus all
 //   8 block keys (no mask inside the block: DFlash's block-diagonal mask).
-// Cache layout [B][hkv][max_ctx][hd]; scores scaled by 1/sqrt(hd); softmax in fp32.
+// Caches: K [B][hkv][max_ctx][hd], V transposed [B][hkv][hd][max_ctx]. Chunks lie on
+// an absolute grid of `chunk` keys (chunk c covers keys [c*chunk, (c+1)*chunk)), so
+// tiles start at aligned key indices. Scores scaled by 1/sqrt(hd); softmax in fp32.
+// This file holds the CUDA-core version (fp32 models); attention_tc.cu the tcgen05 one.
 #include "common.cuh"
 #include "ops.h"
 
@@ -28,8 +31,8 @@ __global__ void __launch_bounds__(256) k_attn_partial(AttnArgs a) {
   int lo = a.lo_fixed;
   if (a.window > 0) lo = max(lo, base - a.window);
   const int hi_max = base + 7;
-  const int k_begin = lo + chunk_id * a.chunk;
-  const int k_end = min(k_begin + a.chunk, hi_max + 1);
+  const int k_begin = max(lo, chunk_id * a.chunk);
+  const int k_end = min((chunk_id + 1) * a.chunk, hi_max + 1);
   const long pidx = ((long)b * a.hkv + g) * a.nchunk + chunk_id;
   float* pml = a.part_ml + pidx * QN * 2;
   float* po = a.part_o + pidx * QN * hd;
@@ -51,20 +54,18 @@ __global__ void __launch_bounds__(256) k_attn_partial(AttnArgs a) {
   }
   float m = -INFINITY, l = 0.f;
   const T* Kb = (const T*)a.Kc + ((long)b * a.hkv + g) * a.max_ctx * hd;
-  const T* Vb = (const T*)a.Vc + ((long)b * a.hkv + g) * a.max_ctx * hd;
+  const T* Vb = (const T*)a.Vc + ((long)b * a.hkv + g) * hd * a.max_ctx;  // [hd][max_ctx]
 
   for (int kt = k_begin; kt < k_end; kt += kTK) {
     const int nk = min(kTK, k_end - kt);
     __syncthreads();
     for (int e = threadIdx.x; e < kTK * hd; e += blockDim.x) {
       const int j = e / hd, dd = e % hd;
-      float kv = 0.f, vv = 0.f;
-      if (j < nk) {
-        kv = to_f32(Kb[(long)(kt + j) * hd + dd]);
-        vv = to_f32(Vb[(long)(kt + j) * hd + dd]);
-      }
-      Ks[j][dd] = kv;
-      Vs[j][dd] = vv;
+      Ks[j][dd] = (j < nk) ? to_f32(Kb[(long)(kt + j) * hd + dd]) : 0.f;
+    }
+    for (int e = threadIdx.x; e < kTK * hd; e += blockDim.x) {
+      const int j = e % kTK, dd = e / kTK;  // keys contiguous in the transposed V
+      Vs[j][dd] = (j < nk) ? to_f32(Vb[(long)dd * a.max_ctx + kt + j]) : 0.f;
     }
     __syncthreads();
     float sc[kTK];
@@ -113,19 +114,19 @@ __global__ void k_attn_merge(AttnArgs a) {
   const int base = a.base[b];
   int lo = a.lo_fixed;
   if (a.window > 0) lo = max(lo, base - a.window);
-  const int nact = max(1, min(a.nchunk, (base + 8 - lo + a.chunk - 1) / a.chunk));
+  const int c0 = lo / a.chunk, c1 = min(a.nchunk - 1, (base + 7) / a.chunk);
   const long p0 = ((long)b * a.hkv + g) * a.nchunk;
   float M = -INFINITY;
-  for (int c = 0; c < nact; ++c) M = fmaxf(M, a.part_ml[((p0 + c) * QN + qi) * 2]);
+  for (int c = c0; c <= c1; ++c) M = fmaxf(M, a.part_ml[((p0 + c) * QN + qi) * 2]);
   float L = 0.f;
-  for (int c = 0; c < nact; ++c) {
+  for (int c = c0; c <= c1; ++c) {
     const float mc = a.part_ml[((p0 + c) * QN + qi) * 2];
     L += a.part_ml[((p0 + c) * QN + qi) * 2 + 1] * __expf(mc - M);
   }
   const float invL = 1.f / L;
   for (int dd = threadIdx.x; dd < a.hd; dd += blockDim.x) {
     float o = 0.f;
-    for (int c = 0; c < nact; ++c) {
+    for (int c = c0; c <= c1; ++c) {
       const float mc = a.part_ml[((p0 + c) * QN + qi) * 2];
       o += a.part_o[((p0 + c) * QN + qi) * a.hd + dd] * __expf(mc - M);
     }
@@ -134,14 +135,20 @@ __global__ void k_attn_merge(AttnArgs a) {
 }
 
 void op_attention(int dt, const AttnArgs& a, cudaStream_t st) {
-  dim3 g1(a.nchunk, a.hkv, a.B), g2(a.B * 8, a.hq);
-  if (dt) {
+  dim3 g1(a.nchunk, a.hkv, a.B);
+  if (dt)
     k_attn_partial<bf16><<<g1, 256, 0, st>>>(a);
-    k_attn_merge<bf16><<<g2, 128, 0, st>>>(a);
-  } else {
+  else
     k_attn_partial<float><<<g1, 256, 0, st>>>(a);
+  op_attention_merge(dt, a, st);
+}
+
+void op_attention_merge(int dt, const AttnArgs& a, cudaStream_t st) {
+  dim3 g2(a.B * 8, a.hq);
+  if (dt)
+    k_attn_merge<bf16><<<g2, 128, 0, st>>>(a);
+  else
     k_attn_merge<float><<<g2, 128, 0, st>>>(a);
-  }
 }
 
 }  // namespace dmtp

@@ -56,6 +56,11 @@ struct dmtp_ctx {
   void* dK[DMTP_MAX_DRAFT_LAYERS];
   void* dV[DMTP_MAX_DRAFT_LAYERS];
   void *mK, *mV;
+  // tcgen05 attention tensor maps: K as [B*hkv*max_ctx, hd], V^T as [B*hkv*hd, max_ctx]
+  CUtensorMap tmK[DMTP_MAX_LAYERS], tmV[DMTP_MAX_LAYERS];
+  CUtensorMap tmKd[DMTP_MAX_DRAFT_LAYERS], tmVd[DMTP_MAX_DRAFT_LAYERS];
+  CUtensorMap tmKm, tmVm;
+  bool attn_tc;  // bf16 caches and a shape the tcgen05 attention serves
   float2* rope;
   float* x;
   void* xn;
@@ -150,7 +155,7 @@ int derive(dmtp_ctx* c, const dmtp_config* cfg, int B) {
   c->qd = c->hq * c->hd;
   c->kvd = c->hkv * c->hd;
   c->qkvd = c->qd + 2 * c->kvd;
-  c->maxc = f.max_ctx;
+  c->maxc = (f.max_ctx + 63) / 64 * 64;  // K/V row strides stay 16-byte aligned for TMA
   c->L = f.n_layers;
   c->Ld = f.draft_layers;
   c->ntap = f.n_taps;
@@ -182,7 +187,8 @@ int derive(dmtp_ctx* c, const dmtp_config* cfg, int B) {
   c->mt8 = tc_mt(c->M);
   c->mt6 = tc_mt(6 * B);
   c->mt1 = tc_mt(B);
-  c->attn_chunk = 256;
+  c->attn_tc = c->dt == 1 && (c->hd == 64 || c->hd == 128) && QN <= 64;
+  c->attn_chunk = 512;  // keys per attention partial; a multiple of the 128-key tile
   c->attn_nchunk = (c->maxc + 8 + c->attn_chunk - 1) / c->attn_chunk;
   return DMTP_OK;
 }
@@ -376,6 +382,7 @@ void* tap_ptr(dmtp_ctx* c, int slot) {
 
 struct AttnSpec {
   void *Kc, *Vc;
+  const CUtensorMap *tmK, *tmV;
   const int* base;
   int causal, lo_fixed, window;
   int mode_base;  // 1: base = kv_len at round start (target, drafter); 2: kv_len + 1 (MTP)
@@ -420,7 +427,12 @@ void attn_layer(dmtp_ctx* c, const LayerPlans& p, const dmtp_layer_weights& w, f
     }
     kv_bytes += (double)c->M * c->qd * esz(c) * 2;  // q in, o out
   }
-  launch(c, P_ATTN, kv_bytes, 0, [&] { op_attention(c->dt, aa, c->st); });
+  launch(c, P_ATTN, kv_bytes, 0, [&] {
+    if (c->attn_tc)
+      op_attention_tc(aa, *a.tmK, *a.tmV, c->err, c->st);
+    else
+      op_attention(c->dt, aa, c->st);
+  });
   c->launches += 1;  // partial + merge
   gemm_acc(c, p.o, xr, c->d);
   norm(c, xr, w.mlp_norm, c->xn, nullptr, nullptr, M);
@@ -473,7 +485,7 @@ void target_forward(dmtp_ctx* c, bool snapshots) {
   for (int l = 0; l < c->L; ++l) {
     void* tap_in = l > 0 ? tap_ptr(c, c->tap_of_layer[l - 1]) : nullptr;
     if (c->cfg.layer_kind[l] == 0) {
-      AttnSpec a{c->tK[l], c->tV[l], c->rs.pos0, 1, 0, 0, 1};
+      AttnSpec a{c->tK[l], c->tV[l], &c->tmK[l], &c->tmV[l], c->rs.pos0, 1, 0, 0, 1};
       attn_layer(c, c->tgt[l], c->w.layers[l], c->x, a, tap_in);
     } else {
       gdn_layer(c, l, c->x, tap_in, snapshots);
@@ -508,7 +520,7 @@ void mtp_advance(dmtp_ctx* c) {
   launch(c, P_OTHER, 0, 0, [&] { op_concat_rms2(c->dt, c->w.emb, c->V, ph, pe, c->z, lo_of(c, c->mt8, 2 * c->d), M, c->d, c->cfg.rms_eps, c->err, c->st); });
   zero(c, c->xm, (size_t)M * c->d * 4);
   gemm_acc(c, c->mproj, c->xm, c->d);
-  AttnSpec a{c->mK, c->mV, c->rs.mtp_base, 1, 1, 0, 2};
+  AttnSpec a{c->mK, c->mV, &c->tmKm, &c->tmVm, c->rs.mtp_base, 1, 1, 0, 2};
   attn_layer(c, c->mtp, c->w.mtp, c->xm, a, nullptr);
   launch(c, P_OTHER, 0, 0, [&] { op_gather_hmtp(c->xm, c->rs.mtp_cnt, c->h_mtp, c->B, c->d, c->st); });
 }
@@ -540,7 +552,8 @@ void enqueue_round(dmtp_ctx* c, const Dbg& dbg, const int* forced) {
                  c->err, c->st); });
   // a3: block drafter over the 8 slots
   for (int j = 0; j < c->Ld; ++j) {
-    AttnSpec a{c->dK[j], c->dV[j], s.pos0, 0, 0, c->cfg.draft_window, 1};
+    AttnSpec a{c->dK[j], c->dV[j], &c->tmKd[j], &c->tmVd[j], s.pos0, 0, 0, c->cfg.draft_window,
+               1};
     attn_layer(c, c->dft[j], c->w.dft[j], c->x, a, nullptr);
   }
   RowMap m6;
@@ -585,7 +598,7 @@ int dmtp_workspace_size(const dmtp_config* cfg, int batch, size_t* bytes) {
   if (!cfg || !bytes) return DMTP_EINVAL;
   dmtp_ctx* c = new dmtp_ctx();
   int r = derive(c, cfg, batch);
-  if (r == DMTP_OK) *bytes = layout(c, nullptr) + prompt_bytes(batch, cfg->max_ctx);
+  if (r == DMTP_OK) *bytes = layout(c, nullptr) + prompt_bytes(batch, c->maxc);
   delete c;
   return r;
 }
@@ -660,9 +673,25 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
     delete c;
     return DMTP_EINVAL;
   }
-  if (c->dt == 1 && tc_init_attributes()) {
+  if (c->dt == 1 && (tc_init_attributes() || attn_tc_init_attributes())) {
     delete c;
     return DMTP_ECUDA;
+  }
+  if (c->attn_tc) {
+    const uint64_t krows = (uint64_t)B * c->hkv * c->maxc, vrows = (uint64_t)B * c->hkv * c->hd;
+    int e = 0;
+    auto maps = [&](CUtensorMap* mk, CUtensorMap* mv, void* K, void* V) {
+      e |= tc_make_tmap(mk, K, krows, c->hd, 128);
+      e |= tc_make_tmap(mv, V, vrows, c->maxc, c->hd);
+    };
+    for (int l = 0; l < c->L; ++l)
+      if (c->tK[l]) maps(&c->tmK[l], &c->tmV[l], c->tK[l], c->tV[l]);
+    for (int j = 0; j < c->Ld; ++j) maps(&c->tmKd[j], &c->tmVd[j], c->dK[j], c->dV[j]);
+    maps(&c->tmKm, &c->tmVm, c->mK, c->mV);
+    if (e) {
+      delete c;
+      return DMTP_EINVAL;
+    }
   }
   // ---- initial device state ----
   cudaStream_t st = c->st;

@@ -232,8 +232,8 @@ static PFN_encodeTiled_t get_encode() {
 }
 
 // [rows, cols] row-major bf16, box {64, box_rows}, 128-byte swizzle, zero fill.
-static int make_tmap(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols,
-                     uint32_t box_rows) {
+int tc_make_tmap(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols,
+                 uint32_t box_rows) {
   PFN_encodeTiled_t enc = get_encode();
   if (!enc) return -1;
   if (((uintptr_t)base & 15) || (cols * 2) % 16) return -2;
@@ -289,10 +289,10 @@ int tc_plan(TcPlan* p, const void* W, int N, int K, const void* X, int M, int ns
     }
   }
   p->splits = best;
-  int r = make_tmap(&p->tmW, W, (uint64_t)N, (uint64_t)K, kTileN);
+  int r = tc_make_tmap(&p->tmW, W, (uint64_t)N, (uint64_t)K, kTileN);
   if (r) return r;
   // split: the tensor spans both halves (rows >= M of each half are ignored columns)
-  r = make_tmap(&p->tmX, X, (uint64_t)(split ? xrows : M), (uint64_t)K, (uint32_t)p->xbox);
+  r = tc_make_tmap(&p->tmX, X, (uint64_t)(split ? xrows : M), (uint64_t)K, (uint32_t)p->xbox);
   return r;
 }
 

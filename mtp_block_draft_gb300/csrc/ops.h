@@ -99,7 +99,7 @@ void op_prefill_done(const RoundState& s, const int* plen, cudaStream_t st);
 // ---- attention.cu ------------------------------------------------------------------
 struct AttnArgs {
   const void* Kc;      // [B][hkv][max_ctx][hd] dt
-  const void* Vc;
+  const void* Vc;      // [B][hkv][hd][max_ctx] dt (transposed)
   const float* q;      // [B*8][hq][hd] fp32
   float* part_o;       // [B][hkv][nchunk][QN][hd]
   float* part_ml;      // [B][hkv][nchunk][QN][2]
@@ -109,9 +109,16 @@ struct AttnArgs {
   int causal;          // 1: row s sees keys <= base+s; 0: keys <= base+7
   int lo_fixed;        // lowest key index
   int window;          // > 0: lo = max(lo_fixed, base - window)
-  int B, hq, hkv, hd, max_ctx, chunk, nchunk;
+  int B, hq, hkv, hd, max_ctx, chunk, nchunk;  // chunk: keys per partial (absolute grid)
 };
 void op_attention(int dt, const AttnArgs& a, cudaStream_t st);
+void op_attention_merge(int dt, const AttnArgs& a, cudaStream_t st);
+// tcgen05 attention (bf16 caches, head_dim 64 or 128, 8 x GQA-group <= 64 queries);
+// tmK: K cache as [B*hkv*max_ctx, hd] box {64, 128}; tmV: transposed V cache as
+// [B*hkv*hd, max_ctx] box {64, hd}. Writes the same partials as op_attention, then merges.
+void op_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                     unsigned* err, cudaStream_t st);
+int attn_tc_init_attributes();
 
 // ---- gemm_simt.cu (fp32 storage) ------------------------------------------------------
 // out[m*ldo + n] += sum_k X[m*K + k] * W[n*K + k]   (fp32 W and X)
@@ -130,6 +137,9 @@ struct TcPlan {
 };
 // Padded token rows of an M-row operand (multiple of 16, >= 16).
 int tc_mt(int M);
+// Tensor map of a row-major bf16 [rows, cols] matrix, box {64, box_rows}, 128-B swizzle.
+int tc_make_tmap(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols,
+                 uint32_t box_rows);
 // Builds the tensor maps and launch shape for out[M,N] = X[M,K] . W[N,K]^T. split: X
 // holds 2*tc_mt(M) rows, the bf16 high halves then the low halves (X = hi + lo).
 int tc_plan(TcPlan* p, const void* W, int N, int K, const void* X, int M, int nsm,
