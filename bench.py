@@ -170,12 +170,20 @@ def main():
     ap.add_argument("--profile-rounds", type=int, default=3)
     ap.add_argument("--cpu-rounds", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    # smaller cases of the same kernels, for profiler captures (not bench workloads)
+    ap.add_argument("--layers", type=int, default=None, help="override target layers")
+    ap.add_argument("--ctx", type=int, nargs=2, default=None, help="override prompt range")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
     from synth import CONFIGS
     cfg = CONFIGS[args.config]
+    if args.layers is not None:
+        cfg = cfg.replace(name=f"{cfg.name}-L{args.layers}", n_layers=args.layers)
+    if args.ctx is not None:
+        cfg = cfg.replace(name=f"{cfg.name}-ctx{args.ctx[0]}-{args.ctx[1]}", ctx_lo=args.ctx[0],
+                          ctx_hi=args.ctx[1])
     if args.impl == "reference":
         return run_reference(args, cfg)
 
@@ -208,11 +216,14 @@ def main():
     clocks = Clocks(local)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    # the profiler start/stop marks let an external profiler skip the prefill
+    torch.cuda.cudart().cudaProfilerStart()
     e0.record(stream)
     for _ in range(args.steps):
         g.round()
     e1.record(stream)
     torch.cuda.synchronize()
+    torch.cuda.cudart().cudaProfilerStop()
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
