@@ -60,12 +60,14 @@ struct dmtp_ctx {
   CUtensorMap tmK[DMTP_MAX_LAYERS], tmV[DMTP_MAX_LAYERS];
   CUtensorMap tmKd[DMTP_MAX_DRAFT_LAYERS], tmVd[DMTP_MAX_DRAFT_LAYERS];
   CUtensorMap tmKm, tmVm;
+  CUtensorMap tmQh, tmQl;  // the split query halves as [M][hq][hd], box {64, hq/hkv, 8}
   bool attn_tc;  // bf16 caches and a shape the tcgen05 attention serves
   float2* rope;
   float* x;
   void* xn;
   float* qkv;
   float* q;
+  void* qs;  // bf16 [2][M][hq][hd]: split queries for the tensor-core attention
   float *part_o, *part_ml;
   void* att;
   float* gu;
@@ -224,6 +226,7 @@ size_t layout(dmtp_ctx* c, char* base) {
   c->xn = b.take<char>(r8 * d * es);
   c->qkv = b.take<float>(M * qkvw * 4);
   c->q = b.take<float>(M * c->qd * 4);
+  c->qs = b.take<char>(2 * M * c->qd * 2);
   const int QN = 8 * (c->hq / c->hkv);
   c->part_o = b.take<float>(B * c->hkv * c->attn_nchunk * QN * c->hd * 4);
   c->part_ml = b.take<float>(B * c->hkv * c->attn_nchunk * QN * 2 * 4);
@@ -394,7 +397,7 @@ void attn_layer(dmtp_ctx* c, const LayerPlans& p, const dmtp_layer_weights& w, f
   norm(c, xr, w.attn_norm, c->xn, nullptr, tap_in, M);
   zero(c, c->qkv, (size_t)M * c->qkvd * 4);
   gemm_acc(c, p.qkv, c->qkv, c->qkvd);
-  launch(c, P_OTHER, 0, 0, [&] { op_rope_kv(c->dt, c->qkv, c->qkvd, 0, c->qd, c->qd + c->kvd, c->q, a.Kc, a.Vc, a.base, c->rope,
+  launch(c, P_OTHER, 0, 0, [&] { op_rope_kv(c->dt, c->qkv, c->qkvd, 0, c->qd, c->qd + c->kvd, c->q, c->attn_tc ? c->qs : nullptr, (long)M * c->qd, a.Kc, a.Vc, a.base, c->rope,
              M, c->hq, c->hkv, c->hd, c->maxc, c->err, c->st); });
   AttnArgs aa;
   aa.Kc = a.Kc;
@@ -429,7 +432,7 @@ void attn_layer(dmtp_ctx* c, const LayerPlans& p, const dmtp_layer_weights& w, f
   }
   launch(c, P_ATTN, kv_bytes, 0, [&] {
     if (c->attn_tc)
-      op_attention_tc(aa, *a.tmK, *a.tmV, c->err, c->st);
+      op_attention_tc(aa, *a.tmK, *a.tmV, c->tmQh, c->tmQl, c->err, c->st);
     else
       op_attention(c->dt, aa, c->st);
   });
@@ -504,7 +507,7 @@ void drafter_ctx(dmtp_ctx* c) {
   for (int j = 0; j < c->Ld; ++j) {
     zero(c, c->qkv, (size_t)M * 2 * c->kvd * 4);
     gemm_acc(c, c->dkv[j], c->qkv, 2 * c->kvd);
-    launch(c, P_OTHER, 0, 0, [&] { op_rope_kv(c->dt, c->qkv, 2 * c->kvd, -1, 0, c->kvd, nullptr, c->dK[j], c->dV[j],
+    launch(c, P_OTHER, 0, 0, [&] { op_rope_kv(c->dt, c->qkv, 2 * c->kvd, -1, 0, c->kvd, nullptr, nullptr, 0, c->dK[j], c->dV[j],
                c->rs.pos0, c->rope, M, c->hq, c->hkv, c->hd, c->maxc, c->err, c->st); });
   }
 }
@@ -688,6 +691,10 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
       if (c->tK[l]) maps(&c->tmK[l], &c->tmV[l], c->tK[l], c->tV[l]);
     for (int j = 0; j < c->Ld; ++j) maps(&c->tmKd[j], &c->tmVd[j], c->dK[j], c->dV[j]);
     maps(&c->tmKm, &c->tmVm, c->mK, c->mV);
+    const int grp = c->hq / c->hkv;
+    e |= tc_make_tmap3(&c->tmQh, c->qs, c->hd, c->hq, c->M, grp, 8);
+    e |= tc_make_tmap3(&c->tmQl, (char*)c->qs + (size_t)c->M * c->qd * 2, c->hd, c->hq, c->M,
+                       grp, 8);
     if (e) {
       delete c;
       return DMTP_EINVAL;

@@ -205,7 +205,8 @@ void op_rope_table(float2* tab, int npos, int hd, float theta, cudaStream_t st) 
 // ---------------------------------------------------------------------------------
 template <typename T>
 __global__ void k_rope_kv(const float* __restrict__ src, int ld, int q_off, int k_off, int v_off,
-                          float* __restrict__ q_out, T* __restrict__ Kc, T* __restrict__ Vc,
+                          float* __restrict__ q_out, bf16* __restrict__ q_split, long q_lo,
+                          T* __restrict__ Kc, T* __restrict__ Vc,
                           const int* __restrict__ base, const float2* __restrict__ tab, int hq,
                           int hkv, int hd, int max_ctx, unsigned* err) {
   const int m = blockIdx.x, b = m >> 3, s = m & 7;
@@ -220,9 +221,15 @@ __global__ void k_rope_kv(const float* __restrict__ src, int ld, int q_off, int 
       const int h = idx / half, i = idx % half;
       const float x1 = row[q_off + h * hd + i], x2 = row[q_off + h * hd + half + i];
       const float2 cs = tr[i];
-      float* qo = q_out + ((long)m * hq + h) * hd;
-      qo[i] = x1 * cs.x - x2 * cs.y;
-      qo[half + i] = x2 * cs.x + x1 * cs.y;
+      const float r1 = x1 * cs.x - x2 * cs.y, r2 = x2 * cs.x + x1 * cs.y;
+      const long qi = ((long)m * hq + h) * hd;
+      if (q_split) {  // bf16 hi + remainder for the tensor-core attention
+        store_act(q_split + qi + i, q_lo, r1);
+        store_act(q_split + qi + half + i, q_lo, r2);
+      } else {
+        q_out[qi + i] = r1;
+        q_out[qi + half + i] = r2;
+      }
     }
   }
   if (!pos_ok) return;
@@ -240,14 +247,16 @@ __global__ void k_rope_kv(const float* __restrict__ src, int ld, int q_off, int 
 }
 
 void op_rope_kv(int dt, const float* src, int ld, int q_off, int k_off, int v_off, float* q_out,
-                void* Kc, void* Vc, const int* base, const float2* tab, int rows, int hq, int hkv,
-                int hd, int max_ctx, unsigned* err, cudaStream_t st) {
+                void* q_split, long q_lo, void* Kc, void* Vc, const int* base, const float2* tab,
+                int rows, int hq, int hkv, int hd, int max_ctx, unsigned* err, cudaStream_t st) {
   if (dt)
-    k_rope_kv<bf16><<<rows, 256, 0, st>>>(src, ld, q_off, k_off, v_off, q_out, (bf16*)Kc,
-                                          (bf16*)Vc, base, tab, hq, hkv, hd, max_ctx, err);
+    k_rope_kv<bf16><<<rows, 256, 0, st>>>(src, ld, q_off, k_off, v_off, q_out, (bf16*)q_split,
+                                          q_lo, (bf16*)Kc, (bf16*)Vc, base, tab, hq, hkv, hd,
+                                          max_ctx, err);
   else
-    k_rope_kv<float><<<rows, 256, 0, st>>>(src, ld, q_off, k_off, v_off, q_out, (float*)Kc,
-                                           (float*)Vc, base, tab, hq, hkv, hd, max_ctx, err);
+    k_rope_kv<float><<<rows, 256, 0, st>>>(src, ld, q_off, k_off, v_off, q_out, nullptr, 0,
+                                           (float*)Kc, (float*)Vc, base, tab, hq, hkv, hd,
+                                           max_ctx, err);
 }
 
 template <typename T>

@@ -45,10 +45,12 @@ void op_build_slots(int dt, const void* E, int vocab, const int* A, const int* d
 // h = silu(gu[:, :F]) * gu[:, F:] as dt
 void op_swiglu(int dt, const float* gu, void* h, long h_lo, int rows, int F, cudaStream_t st);
 // RoPE (table) + cache write. src rows m = b*8 + s at position base[b] + s.
-// q_off < 0: no q. q_out fp32 [rows][hq][hd].
+// q_off < 0: no q. q_out fp32 [rows][hq][hd], or, when q_split != null (bf16 models),
+// q as a bf16 pair: hi at q_split, remainder at q_split + q_lo (elements).
 void op_rope_kv(int dt, const float* src, int ld, int q_off, int k_off, int v_off, float* q_out,
-                void* Kc, void* Vc, const int* base, const float2* rope_tab, int rows, int hq,
-                int hkv, int hd, int max_ctx, unsigned* err, cudaStream_t st);
+                void* q_split, long q_lo, void* Kc, void* Vc, const int* base,
+                const float2* rope_tab, int rows, int hq, int hkv, int hd, int max_ctx,
+                unsigned* err, cudaStream_t st);
 // fp32 -> dt copy of rows (with row map)
 void op_cast_rows(int dt, const float* x, int ldx, void* y, int ldy, long y_lo, int rows, int d,
                   RowMap map, cudaStream_t st);
@@ -115,9 +117,11 @@ void op_attention(int dt, const AttnArgs& a, cudaStream_t st);
 void op_attention_merge(int dt, const AttnArgs& a, cudaStream_t st);
 // tcgen05 attention (bf16 caches, head_dim 64 or 128, 8 x GQA-group <= 64 queries);
 // tmK: K cache as [B*hkv*max_ctx, hd] box {64, 128}; tmV: transposed V cache as
-// [B*hkv*hd, max_ctx] box {64, hd}. Writes the same partials as op_attention, then merges.
+// [B*hkv*hd, max_ctx] box {64, hd}; tmQh / tmQl: the bf16 query halves as 3-D
+// [B*8][hq][hd] maps, box {64, hq/hkv, 8}. Writes the partials of op_attention, merges.
 void op_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                     unsigned* err, cudaStream_t st);
+                     const CUtensorMap& tmQh, const CUtensorMap& tmQl, unsigned* err,
+                     cudaStream_t st);
 int attn_tc_init_attributes();
 
 // ---- gemm_simt.cu (fp32 storage) ------------------------------------------------------
@@ -140,6 +144,9 @@ int tc_mt(int M);
 // Tensor map of a row-major bf16 [rows, cols] matrix, box {64, box_rows}, 128-B swizzle.
 int tc_make_tmap(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols,
                  uint32_t box_rows);
+// 3-D bf16 tensor [d2][d1][d0] (d0 innermost), box {64, b1, b2}, 128-B swizzle.
+int tc_make_tmap3(CUtensorMap* tm, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                  uint32_t b1, uint32_t b2);
 // Builds the tensor maps and launch shape for out[M,N] = X[M,K] . W[N,K]^T. split: X
 // holds 2*tc_mt(M) rows, the bf16 high halves then the low halves (X = hi + lo).
 int tc_plan(TcPlan* p, const void* W, int N, int K, const void* X, int M, int nsm,
