@@ -8,16 +8,18 @@
 //                pair [Q_hi | Q_lo] along K against [K | K] (queries in operand rows
 //                0..QN-1), so S keeps the queries' fp32 precision. S is double-buffered
 //                in TMEM: the next tile's scores are computed during this tile's softmax.
-//   softmax    : warps 0,1,4,5 own TMEM lanes 0..63 (one query row per warp pair, each
-//                thread half of the tile's keys): mask (causal rows / anchor window /
-//                chunk bounds), exponentiate against a per-row reference max, and write
-//                P as a bf16 pair, P_hi in operand rows 0..63 and P_lo in rows 64..127.
+//                The queries sit in operand rows 0..63 and again in rows 64..127, so
+//                TMEM lanes r and r+64 hold the same scores.
+//   softmax    : warps 0-7, four threads per query row, each a quarter (32) of the
+//                tile's keys: mask (causal rows / anchor window / chunk bounds; skipped
+//                on interior tiles), exponentiate against a per-row reference max, and
+//                write P as a bf16 pair, P_hi in operand rows 0..63, P_lo in 64..127.
 //   O += P V   : tcgen05 M=128, N=hd, K=128 keys, B = the transposed V tile (K-major);
 //                O stays in TMEM for the whole chunk: lanes 0..63 accumulate P_hi V,
-//                lanes 64..127 P_lo V (owned by warps 2,3,6,7).
-// The reference max only moves when a row's scores exceed it by more than kRescale
-// (e^8); then both halves of that row's O are rescaled in TMEM. Keeping a stale
-// reference is exact: the same factor multiplies O and the running sum l.
+//                lanes 64..127 P_lo V; they are summed once at the end.
+// The reference max only moves when a row's scores exceed it by more than 2^11; then
+// that row's O (both halves) is rescaled in TMEM. Keeping a stale reference is exact:
+// the same factor multiplies O and the running sum l.
 // The queries arrive by TMA, already split into bf16 halves by the RoPE kernel.
 // Warp 8 lane 0 issues the TMA loads, warp 9 lane 0 the MMAs. The partial (m, l, O) of
 // each chunk goes to global memory and a merge kernel combines the chunks (attention.cu).
@@ -35,7 +37,6 @@ namespace {
 
 constexpr int kTileKeys = 128;
 constexpr int kBlk = 128 * 128;  // one 128-row x 64-element bf16 operand block (16 KB)
-constexpr float kRescale = 8.f;  // move a row's reference max only past e^8
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
@@ -79,20 +80,23 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm,
       : "memory");
 }
 
-// Shared-memory plan. Q blocks overlap: the operand for Q_hi of head dims [64j, 64j+64)
-// starts at 16K*j and its unused rows 64..127 are rows 0..63 of the Q_lo block of the
-// same dims (at 16K*j + 8K); the last Q_lo block's unused rows fall in 8 KB of padding.
+// Shared-memory plan. Each Q operand block (one 64-wide head-dim block, hi or lo half)
+// holds the QN query rows twice, at rows 0.. and 64.., so TMEM lanes r and r + 64 of S
+// carry the same scores and all eight softmax warps can read them.
 template <int HD>
 struct Smem {
   static constexpr int kDB = HD / 64;                      // 64-wide head-dim blocks
-  static constexpr uint32_t kQ = kDB * kBlk + 8192;
+  static constexpr uint32_t kQ = 2 * kDB * kBlk;           // [Q_hi blocks | Q_lo blocks]
   static constexpr uint32_t kKTile = kDB * kBlk;           // 128 keys x HD
   static constexpr uint32_t kVTile = 2 * HD * 128;         // V^T: HD rows x 128 keys
   static constexpr uint32_t kStage = kKTile + kVTile;
   static constexpr uint32_t kP = 2 * kBlk;                 // 128 rows x 128 keys
-  static constexpr uint32_t kBytes = 1024 + kQ + 2 * kStage + kP + 2048;
-  __host__ __device__ static constexpr uint32_t q_hi(int j) { return j * kBlk; }
-  __host__ __device__ static constexpr uint32_t q_lo(int j) { return j * kBlk + 8192; }
+  static constexpr uint32_t kSmall = 128 + 2048;           // barriers + tile maxima
+  static constexpr uint32_t kBig = kQ + 2 * kStage + kP;   // 1024-aligned operand region
+  // the small region sits below the aligned one; with a 1024-aligned base (the usual
+  // case) this is exactly the 227 KB a block may have for HD = 128
+  static constexpr uint32_t kBytes =
+      (kSmall + 1023) / 1024 * 1024 + kBig > 232448 ? 232448 : (kSmall + 1023) / 1024 * 1024 + kBig;
 };
 
 }  // namespace
@@ -104,6 +108,7 @@ __global__ void __launch_bounds__(320, 1)
               AttnArgs a, unsigned* err) {
   using L = Smem<HD>;
   constexpr int HALF = HD / 2;
+  constexpr float kLog2e = 1.4426950408889634f;
   extern __shared__ uint8_t smem_raw[];
   const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int grp = a.hq / a.hkv, QN = 8 * grp;
@@ -117,24 +122,27 @@ __global__ void __launch_bounds__(320, 1)
   const int t0 = k_begin / kTileKeys;
   const int ntiles = (k_end + kTileKeys - 1) / kTileKeys - t0;
 
-  uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint64_t* bars = (uint64_t*)smem_raw;
+  uint8_t* sm = smem_raw + L::kSmall;
+  sm += (1024 - (smem_u32(sm) & 1023)) & 1023;
+  if (sm + L::kBig > smem_raw + L::kBytes) {  // dynamic shared memory base not aligned enough
+    if (threadIdx.x == 0) set_err(err, DMTP_ERR_TIMEOUT);
+    return;
+  }
   uint8_t* sQ = sm;
   uint8_t* sKV = sQ + L::kQ;
   uint8_t* sP = sKV + 2 * L::kStage;
-  uint64_t* bars = (uint64_t*)(sP + L::kP);
   uint64_t* kv_full = bars;        // [2]
   uint64_t* kv_empty = bars + 2;   // [2]
   uint64_t* s_full = bars + 4;     // [2]
   uint64_t* q_full = bars + 6;
-  uint64_t* p_full = bars + 7;     // 128 query-row threads + 128 P_lo-lane threads
+  uint64_t* p_full = bars + 7;     // the 256 softmax threads wrote this tile's P
   uint64_t* o_full = bars + 8;     // one commit per tile's P V
-  uint64_t* corr_rdy = bars + 9;   // query threads have posted this tile's factors
-  uint64_t* mx = bars + 10;        // both halves of every row posted their tile maxima
-  uint64_t* fin = bars + 11;
-  uint32_t* tmem_slot = (uint32_t*)(bars + 12);
-  float* sCorr = (float*)(bars + 13);  // [2 tiles][64] rescale factors
-  float* sMax = sCorr + 128;           // [2 tiles][2 halves][64] tile maxima
-  float* sL = sMax + 256;              // [64] second-half running sums (at the end)
+  uint64_t* mx = bars + 9;         // all quarters of every row posted their tile maxima
+  uint64_t* fin = bars + 10;
+  uint32_t* tmem_slot = (uint32_t*)(bars + 11);
+  float* sMax = (float*)(bars + 16);  // [2 tiles][4 quarters][64] tile maxima (log2 units)
+  float* sL = sMax;                   // [4][64] running sums, after the loop (reuses sMax)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -146,8 +154,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(smem_u32(q_full), 1);
     mbar_init(smem_u32(p_full), 256);
     mbar_init(smem_u32(o_full), 1);
-    mbar_init(smem_u32(corr_rdy), 128);
-    mbar_init(smem_u32(mx), 128);
+    mbar_init(smem_u32(mx), 256);
     mbar_init(smem_u32(fin), 1);
     fence_mbar_init();
     tma_prefetch_desc(&tmK);
@@ -165,11 +172,13 @@ __global__ void __launch_bounds__(320, 1)
       // ---------------- TMA producer ----------------
       const uint64_t pol = policy_evict_first(), polq = policy_evict_last();
       const uint32_t qb = smem_u32(q_full);
-      mbar_expect_tx(qb, (uint32_t)(2 * L::kDB * 64 * QN * 2));
-      for (int j = 0; j < L::kDB; ++j) {
-        tma_load_3d(smem_u32(sQ + L::q_hi(j)), &tmQh, j * 64, g * grp, b * 8, qb, polq);
-        tma_load_3d(smem_u32(sQ + L::q_lo(j)), &tmQl, j * 64, g * grp, b * 8, qb, polq);
-      }
+      mbar_expect_tx(qb, (uint32_t)(4 * L::kDB * 64 * QN * 2));
+      for (int j = 0; j < L::kDB; ++j)
+        for (int dup = 0; dup < 2; ++dup) {  // rows 0.. and 64..
+          tma_load_3d(smem_u32(sQ + j * kBlk + dup * 8192), &tmQh, j * 64, g * grp, b * 8, qb, polq);
+          tma_load_3d(smem_u32(sQ + (L::kDB + j) * kBlk + dup * 8192), &tmQl, j * 64, g * grp,
+                      b * 8, qb, polq);
+        }
       const long krow0 = ((long)b * a.hkv + g) * a.max_ctx;
       const int vrow0 = (b * a.hkv + g) * HD;
       int issued = 0;
@@ -203,10 +212,8 @@ __global__ void __launch_bounds__(320, 1)
         uint8_t* st = sKV + s * L::kStage;
 #pragma unroll
         for (int kb = 0; kb < 2 * L::kDB; ++kb) {  // [Q_hi | Q_lo] against [K | K]
-          const int j = kb % L::kDB;
-          const uint32_t qoff = kb < L::kDB ? L::q_hi(j) : L::q_lo(j);
-          const uint64_t dq = umma_desc_sw128(smem_u32(sQ + qoff));
-          const uint64_t dk = umma_desc_sw128(smem_u32(st + j * kBlk));
+          const uint64_t dq = umma_desc_sw128(smem_u32(sQ + kb * kBlk));
+          const uint64_t dk = umma_desc_sw128(smem_u32(st + (kb % L::kDB) * kBlk));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             umma_bf16(tmem + s * 128, dq + 2 * kk, dk + 2 * kk, id_qk, (kb | kk) ? 1u : 0u);
@@ -237,101 +244,95 @@ __global__ void __launch_bounds__(320, 1)
       umma_commit(smem_u32(fin));  // all issued MMAs complete before TMEM is freed
     }
   } else {
-    // warps 0-7: warp w reads TMEM lanes 32*(w%4)..+31. Warps 0,1,4,5 own the query rows
-    // (lanes 0..63); warps 2,3,6,7 the P_lo V rows (lanes 64..127). Warps w and w+4
-    // share a row; hf = w/4 picks the half of the keys (softmax) or of the head dims.
+    // warps 0-7. Warp w reads TMEM lanes 32*(w%4)..+31; lanes r and r+64 hold the same
+    // scores. Thread (lane row lrow, warp w): query row r = lrow % 64, key quarter
+    // kq = 2*(w/4) + (lrow >= 64), O row lrow (P_hi V if < 64, P_lo V otherwise) and
+    // head-dim half hf = w/4.
     const int hf = warp >> 2;
     const int lrow = (warp & 3) * 32 + lane;
-    const bool qrow = lrow < 64;
-    const int r = qrow ? lrow : lrow - 64;
+    const int r = lrow & 63;
+    const int kq = 2 * hf + (lrow >> 6);
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t tOw = tO + lane_off + hf * HALF;  // this thread's half of its O row
-    float m = -INFINITY, l = 0.f;
+    const uint32_t tOw = tO + lane_off + hf * HALF;
+    float m = -INFINITY, l = 0.f;  // reference max and running sum, log2 units
     bool ok = true;
     const int srow = r / grp;
     const int row_hi = a.causal ? base + srow : hi_max;
-    const float scale = rsqrtf((float)HD);
+    const float scale = rsqrtf((float)HD) * kLog2e;
+    const int pblk = kq >> 1, pch = (kq & 1) * 4;  // P block and first 16-B chunk of the quarter
     for (int t = 0; t < ntiles && ok; ++t) {
-      if (qrow) {
-        const int s = t & 1;
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[s]), (t >> 1) & 1, err));
+      const int s = t & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[s]), (t >> 1) & 1, err));
+      if (!ok) break;
+      tc_fence_after();
+      const int kt = (t0 + t) * kTileKeys;
+      const int key0 = kt + kq * 32;
+      // interior tiles need no mask: every key of the tile is visible to every row
+      const bool interior = kt >= k_begin && kt + kTileKeys <= k_end &&
+                            (!a.causal || kt + kTileKeys <= base + 1);
+      float sv[32];
+      {
+        float v0[16], v1[16];
+        tmem_ld16(tmem + s * 128 + kq * 32 + lane_off, v0);
+        tmem_ld16(tmem + s * 128 + kq * 32 + 16 + lane_off, v1);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          sv[j] = v0[j] * scale;
+          sv[16 + j] = v1[j] * scale;
+        }
+      }
+      if (!interior) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int key = key0 + j;
+          if (!(key >= k_begin && key < k_end && key <= row_hi)) sv[j] = -INFINITY;
+        }
+      }
+      float mt = sv[0];
+#pragma unroll
+      for (int j = 1; j < 32; ++j) mt = fmaxf(mt, sv[j]);
+      float* smx = sMax + (t & 1) * 256;
+      smx[kq * 64 + r] = mt;
+      mbar_arrive(smem_u32(mx));
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(mx), t & 1, err));
+      if (!ok) break;
+      mt = fmaxf(fmaxf(smx[r], smx[64 + r]), fmaxf(smx[128 + r], smx[192 + r]));
+      // reference max: set on the first visible scores, moved only past 2^11
+      float corr = 1.f;
+      if (mt > -INFINITY && (m == -INFINITY || mt > m + 11.f)) {
+        corr = (m == -INFINITY) ? 1.f : exp2f(m - mt);
+        m = mt;
+      }
+      // P is single-buffered: the previous tile's P V must be done (it is also what a
+      // rescale of O has to wait for)
+      if (t > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(o_full), (t - 1) & 1, err));
         if (!ok) break;
         tc_fence_after();
-        const int key0 = (t0 + t) * kTileKeys + hf * 64;
-        const uint32_t tS = tmem + s * 128 + hf * 64 + lane_off;
-        float sv[64];
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          float v[16];
-          tmem_ld16(tS + cc * 16, v);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int key = key0 + cc * 16 + j;
-            const bool vis = key >= k_begin && key < k_end && key <= row_hi;
-            sv[cc * 16 + j] = vis ? v[j] * scale : -INFINITY;
-          }
-        }
-        float mt = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < 64; ++j) mt = fmaxf(mt, sv[j]);
-        float* smx = sMax + (t & 1) * 128;
-        smx[hf * 64 + r] = mt;
-        mbar_arrive(smem_u32(mx));
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(mx), t & 1, err));
-        if (!ok) break;
-        mt = fmaxf(mt, smx[(1 - hf) * 64 + r]);
-        // reference max: set on the first visible scores, moved only past e^kRescale
-        float corr = 1.f;
-        if (mt > -INFINITY && (m == -INFINITY || mt > m + kRescale)) {
-          corr = (m == -INFINITY) ? 1.f : __expf(m - mt);
-          m = mt;
-        }
-        if (hf == 0) sCorr[(t & 1) * 64 + r] = corr;
-        // P is single-buffered: the previous tile's P V must be done (it is also what a
-        // rescale of O has to wait for). The factors are posted only after it, so the
-        // P_lo-lane warps are never more than one phase behind on corr_rdy.
-        if (t > 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(o_full), (t - 1) & 1, err));
-          if (!ok) break;
-          tc_fence_after();
-        }
-        mbar_arrive(smem_u32(corr_rdy));
-        if (t > 0 && __any_sync(0xffffffffu, corr != 1.f)) tmem_scale(tOw, HALF, corr);
-        l *= corr;
-        const float mu = (m == -INFINITY) ? 0.f : m;
-        uint8_t* pblk = sP + hf * kBlk;  // block hf holds keys hf*64 .. hf*64+63
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          uint32_t ph[4], pl[4];
-#pragma unroll
-          for (int j = 0; j < 8; j += 2) {
-            const float p0 = __expf(sv[cc * 8 + j] - mu), p1 = __expf(sv[cc * 8 + j + 1] - mu);
-            l += p0 + p1;
-            const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-            const __nv_bfloat162 pr =
-                __floats2bfloat162_rn(p0 - __low2float(pb), p1 - __high2float(pb));
-            ph[j / 2] = *reinterpret_cast<const uint32_t*>(&pb);
-            pl[j / 2] = *reinterpret_cast<const uint32_t*>(&pr);
-          }
-          *(uint4*)(pblk + sw128(r, cc)) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-          *(uint4*)(pblk + sw128(r + 64, cc)) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
-        }
-        fence_proxy_async();
-        tc_fence_before();
-        mbar_arrive(smem_u32(p_full));
-      } else {
-        // P_lo V lanes: apply this tile's rescale factors (rare), then release the tile
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(corr_rdy), t & 1, err));
-        if (!ok) break;
-        const float corr = sCorr[(t & 1) * 64 + r];
-        if (t > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
-          // the query warps posted corr_rdy after this P V completed (o_full of t-1)
-          tc_fence_after();
-          tmem_scale(tOw, HALF, corr);
-        }
-        tc_fence_before();
-        mbar_arrive(smem_u32(p_full));
+        if (__any_sync(0xffffffffu, corr != 1.f)) tmem_scale(tOw, HALF, corr);
       }
+      l *= corr;
+      const float mu = (m == -INFINITY) ? 0.f : m;
+      uint8_t* pb_ = sP + pblk * kBlk;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t ph[4], pl[4];
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+          const float p0 = exp2f(sv[cc * 8 + j] - mu), p1 = exp2f(sv[cc * 8 + j + 1] - mu);
+          l += p0 + p1;
+          const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+          const __nv_bfloat162 pr =
+              __floats2bfloat162_rn(p0 - __low2float(pb), p1 - __high2float(pb));
+          ph[j / 2] = *reinterpret_cast<const uint32_t*>(&pb);
+          pl[j / 2] = *reinterpret_cast<const uint32_t*>(&pr);
+        }
+        *(uint4*)(pb_ + sw128(r, pch + cc)) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+        *(uint4*)(pb_ + sw128(r + 64, pch + cc)) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      mbar_arrive(smem_u32(p_full));
     }
     // the final O: every MMA has completed once `fin` fires; read this thread's half row
     float O[HALF];
@@ -346,19 +347,18 @@ __global__ void __launch_bounds__(320, 1)
         for (int j = 0; j < 16; ++j) O[cc * 16 + j] = v[j];
       }
     }
-    // P_lo V rows and the second half's running sum meet the first half in shared
-    // memory (the K/V stage area is idle once every MMA has completed)
+    // the P_lo V rows and the quarters' sums meet in shared memory (the K/V stage area
+    // is idle once every MMA has completed)
     float* xo = (float*)sKV;  // [64][HD + 4]
-    if (!qrow && ok) {
+    if (lrow >= 64 && ok) {
 #pragma unroll
       for (int i = 0; i < HALF; i += 4)
         *(float4*)(xo + r * (HD + 4) + hf * HALF + i) =
             make_float4(O[i], O[i + 1], O[i + 2], O[i + 3]);
-    } else if (qrow && hf == 1) {
-      sL[r] = l;
     }
+    sL[kq * 64 + r] = l;
     asm volatile("bar.sync 2, 256;" ::: "memory");
-    if (ok && qrow && r < QN) {
+    if (ok && lrow < 64 && r < QN) {
       const long pidx = ((long)b * a.hkv + g) * a.nchunk + c;
       float* po = a.part_o + (pidx * QN + r) * HD + hf * HALF;
       const float* lo_row = xo + r * (HD + 4) + hf * HALF;
@@ -367,8 +367,9 @@ __global__ void __launch_bounds__(320, 1)
         *(float4*)(po + i) = make_float4(O[i] + lo_row[i], O[i + 1] + lo_row[i + 1],
                                          O[i + 2] + lo_row[i + 2], O[i + 3] + lo_row[i + 3]);
       if (hf == 0) {
-        a.part_ml[(pidx * QN + r) * 2] = m;
-        a.part_ml[(pidx * QN + r) * 2 + 1] = l + sL[r];
+        constexpr float kLn2 = 0.6931471805599453f;
+        a.part_ml[(pidx * QN + r) * 2] = m * kLn2;  // natural units for the merge
+        a.part_ml[(pidx * QN + r) * 2 + 1] = sL[r] + sL[64 + r] + sL[128 + r] + sL[192 + r];
       }
     }
   }
