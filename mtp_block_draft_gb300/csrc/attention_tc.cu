@@ -90,7 +90,11 @@ struct Smem {
   static constexpr uint32_t kKTile = kDB * kBlk;           // 128 keys x HD
   static constexpr uint32_t kVTile = 2 * HD * 128;         // V^T: HD rows x 128 keys
   static constexpr uint32_t kStage = kKTile + kVTile;
-  static constexpr uint32_t kP = 2 * kBlk;                 // 128 rows x 128 keys
+  // P (128 rows x 128 keys, 32 KB) of tile t: in the K area of stage t%2 when that is
+  // large enough (HD = 128; K(t) is dead once S(t) is computed), else in its own
+  // double buffer. Either way P is double-buffered.
+  static constexpr bool kPinK = kKTile >= 2 * kBlk;
+  static constexpr uint32_t kP = kPinK ? 0 : 4 * kBlk;
   static constexpr uint32_t kSmall = 128 + 2048;           // barriers + tile maxima
   static constexpr uint32_t kBig = kQ + 2 * kStage + kP;   // 1024-aligned operand region
   // the small region sits below the aligned one; with a 1024-aligned base (the usual
@@ -131,7 +135,10 @@ __global__ void __launch_bounds__(320, 1)
   }
   uint8_t* sQ = sm;
   uint8_t* sKV = sQ + L::kQ;
-  uint8_t* sP = sKV + 2 * L::kStage;
+  uint8_t* sPsep = sKV + 2 * L::kStage;
+  auto p_buf = [&](int t) -> uint8_t* {
+    return L::kPinK ? sKV + (t & 1) * L::kStage : sPsep + (t & 1) * 2 * kBlk;
+  };
   uint64_t* kv_full = bars;        // [2]
   uint64_t* kv_empty = bars + 2;   // [2]
   uint64_t* s_full = bars + 4;     // [2]
@@ -231,6 +238,7 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after();
         uint8_t* st = sKV + s * L::kStage;
 #pragma unroll
+        uint8_t* sP = p_buf(t);
         for (int kb = 0; kb < 2; ++kb) {
           const uint64_t dp = umma_desc_sw128(smem_u32(sP + kb * kBlk));
           const uint64_t dv = umma_desc_sw128(smem_u32(st + L::kKTile + kb * HD * 128));
@@ -303,17 +311,17 @@ __global__ void __launch_bounds__(320, 1)
         corr = (m == -INFINITY) ? 1.f : exp2f(m - mt);
         m = mt;
       }
-      // P is single-buffered: the previous tile's P V must be done (it is also what a
-      // rescale of O has to wait for)
-      if (t > 0) {
+      // a rescale of O waits for the previous tile's P V (s_full of this tile implies
+      // every P V before it has completed, so o_full is at most one phase behind)
+      if (t > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(o_full), (t - 1) & 1, err));
         if (!ok) break;
         tc_fence_after();
-        if (__any_sync(0xffffffffu, corr != 1.f)) tmem_scale(tOw, HALF, corr);
+        tmem_scale(tOw, HALF, corr);
       }
       l *= corr;
       const float mu = (m == -INFINITY) ? 0.f : m;
-      uint8_t* pb_ = sP + pblk * kBlk;
+      uint8_t* pb_ = p_buf(t) + pblk * kBlk;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         uint32_t ph[4], pl[4];
