@@ -3,18 +3,18 @@
 // One CTA per (512-key chunk, kv head, sequence) serves all 8 rows x the GQA group of
 // query heads that share the kv head (QN <= 64 queries), so each cached K/V byte is read
 // from HBM once per sequence and layer. Keys stream through shared memory in tiles of
-// 128 (TMA, 128-byte swizzle, two stages). Per tile:
-//   S = Q K^T  : tcgen05 M=128, N=128 keys, K = 2*hd: the fp32 queries enter as a bf16
+// TK keys (TMA, 128-byte swizzle, NST stages). Per tile:
+//   S = Q K^T  : tcgen05 M=128, N=TK keys, K = 2*hd: the fp32 queries enter as a bf16
 //                pair [Q_hi | Q_lo] along K against [K | K] (queries in operand rows
 //                0..QN-1), so S keeps the queries' fp32 precision. S is double-buffered
 //                in TMEM: the next tile's scores are computed during this tile's softmax.
 //                The queries sit in operand rows 0..63 and again in rows 64..127, so
 //                TMEM lanes r and r+64 hold the same scores.
-//   softmax    : warps 0-7, four threads per query row, each a quarter (32) of the
+//   softmax    : warps 0-7, four threads per query row, each a quarter of the
 //                tile's keys: mask (causal rows / anchor window / chunk bounds; skipped
 //                on interior tiles), exponentiate against a per-row reference max, and
 //                write P as a bf16 pair, P_hi in operand rows 0..63, P_lo in 64..127.
-//   O += P V   : tcgen05 M=128, N=hd, K=128 keys, B = the transposed V tile (K-major);
+//   O += P V   : tcgen05 M=128, N=hd, K=TK keys, B = the transposed V tile (K-major);
 //                O stays in TMEM for the whole chunk: lanes 0..63 accumulate P_hi V,
 //                lanes 64..127 P_lo V; they are summed once at the end.
 // The reference max only moves when a row's scores exceed it by more than 2^11; then
@@ -35,7 +35,6 @@ namespace dmtp {
 
 namespace {
 
-constexpr int kTileKeys = 128;
 constexpr int kBlk = 128 * 128;  // one 128-row x 64-element bf16 operand block (16 KB)
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
@@ -80,38 +79,40 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm,
       : "memory");
 }
 
-// Shared-memory plan. Each Q operand block (one 64-wide head-dim block, hi or lo half)
-// holds the QN query rows twice, at rows 0.. and 64.., so TMEM lanes r and r + 64 of S
-// carry the same scores and all eight softmax warps can read them.
-template <int HD>
+// Shared-memory plan (TK keys per tile, NST stages). Each Q operand block (one 64-wide
+// head-dim block, hi or lo half) holds the QN query rows twice, at rows 0.. and 64.., so
+// TMEM lanes r and r + 64 of S carry the same scores and all eight softmax warps can
+// read them. P (128 rows x TK keys) of tile t is written into the K area of its stage
+// when that is large enough (K(t) is dead once S(t) is computed), else into a double
+// buffer of its own.
+template <int HD, int TK, int NST>
 struct Smem {
-  static constexpr int kDB = HD / 64;                      // 64-wide head-dim blocks
-  static constexpr uint32_t kQ = 2 * kDB * kBlk;           // [Q_hi blocks | Q_lo blocks]
-  static constexpr uint32_t kKTile = kDB * kBlk;           // 128 keys x HD
-  static constexpr uint32_t kVTile = 2 * HD * 128;         // V^T: HD rows x 128 keys
+  static constexpr int kDB = HD / 64;                 // 64-wide head-dim blocks
+  static constexpr uint32_t kQ = 2 * kDB * kBlk;      // [Q_hi blocks | Q_lo blocks]
+  static constexpr uint32_t kKBox = TK * 128;         // TK keys x 64 head dims
+  static constexpr uint32_t kKTile = kDB * kKBox;
+  static constexpr uint32_t kVBox = HD * 128;         // HD rows x 64 keys
+  static constexpr uint32_t kVTile = (TK / 64) * kVBox;
   static constexpr uint32_t kStage = kKTile + kVTile;
-  // P (128 rows x 128 keys, 32 KB) of tile t: in the K area of stage t%2 when that is
-  // large enough (HD = 128; K(t) is dead once S(t) is computed), else in its own
-  // double buffer. Either way P is double-buffered.
-  static constexpr bool kPinK = kKTile >= 2 * kBlk;
-  static constexpr uint32_t kP = kPinK ? 0 : 4 * kBlk;
-  static constexpr uint32_t kSmall = 128 + 2048;           // barriers + tile maxima
-  static constexpr uint32_t kBig = kQ + 2 * kStage + kP;   // 1024-aligned operand region
-  // the small region sits below the aligned one; with a 1024-aligned base (the usual
-  // case) this is exactly the 227 KB a block may have for HD = 128
-  static constexpr uint32_t kBytes =
-      (kSmall + 1023) / 1024 * 1024 + kBig > 232448 ? 232448 : (kSmall + 1023) / 1024 * 1024 + kBig;
+  static constexpr uint32_t kPTile = (TK / 64) * kBlk;  // 128 rows x TK keys
+  static constexpr bool kPinK = kKTile >= kPTile;
+  static constexpr uint32_t kP = kPinK ? 0 : 2 * kPTile;
+  static constexpr uint32_t kSmall = 256 + 2048;      // barriers + tile maxima
+  static constexpr uint32_t kBig = kQ + NST * kStage + kP;  // 1024-aligned region
+  static constexpr uint32_t kBytes = (kSmall + 1023) / 1024 * 1024 + kBig;
+  static_assert(kBytes <= 232448, "shared memory plan exceeds 227 KB");
 };
 
 }  // namespace
 
-template <int HD>
+template <int HD, int TK, int NST>
 __global__ void __launch_bounds__(320, 1)
     k_attn_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
               const __grid_constant__ CUtensorMap tmQh, const __grid_constant__ CUtensorMap tmQl,
               AttnArgs a, unsigned* err) {
-  using L = Smem<HD>;
+  using L = Smem<HD, TK, NST>;
   constexpr int HALF = HD / 2;
+  constexpr int KQ = TK / 4;  // keys per softmax thread (a quarter of the tile)
   constexpr float kLog2e = 1.4426950408889634f;
   extern __shared__ uint8_t smem_raw[];
   const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -123,8 +124,8 @@ __global__ void __launch_bounds__(320, 1)
   const int k_begin = max(lo, c * a.chunk);
   const int k_end = min((c + 1) * a.chunk, hi_max + 1);
   if (k_begin >= k_end) return;  // chunk outside this sequence's visible keys
-  const int t0 = k_begin / kTileKeys;
-  const int ntiles = (k_end + kTileKeys - 1) / kTileKeys - t0;
+  const int t0 = k_begin / TK;
+  const int ntiles = (k_end + TK - 1) / TK - t0;
 
   uint64_t* bars = (uint64_t*)smem_raw;
   uint8_t* sm = smem_raw + L::kSmall;
@@ -135,29 +136,31 @@ __global__ void __launch_bounds__(320, 1)
   }
   uint8_t* sQ = sm;
   uint8_t* sKV = sQ + L::kQ;
-  uint8_t* sPsep = sKV + 2 * L::kStage;
+  uint8_t* sPsep = sKV + NST * L::kStage;
+  auto stage = [&](int t) -> uint8_t* { return sKV + (t % NST) * L::kStage; };
   auto p_buf = [&](int t) -> uint8_t* {
-    return L::kPinK ? sKV + (t & 1) * L::kStage : sPsep + (t & 1) * 2 * kBlk;
+    return L::kPinK ? stage(t) : sPsep + (t & 1) * L::kPTile;
   };
-  uint64_t* kv_full = bars;        // [2]
-  uint64_t* kv_empty = bars + 2;   // [2]
-  uint64_t* s_full = bars + 4;     // [2]
-  uint64_t* q_full = bars + 6;
-  uint64_t* p_full = bars + 7;     // the 256 softmax threads wrote this tile's P
-  uint64_t* o_full = bars + 8;     // one commit per tile's P V
-  uint64_t* mx = bars + 9;         // all quarters of every row posted their tile maxima
-  uint64_t* fin = bars + 10;
-  uint32_t* tmem_slot = (uint32_t*)(bars + 11);
-  float* sMax = (float*)(bars + 16);  // [2 tiles][4 quarters][64] tile maxima (log2 units)
-  float* sL = sMax;                   // [4][64] running sums, after the loop (reuses sMax)
+  uint64_t* kv_full = bars;             // [NST]
+  uint64_t* kv_empty = bars + NST;      // [NST]
+  uint64_t* s_full = bars + 2 * NST;    // [2] (S is double-buffered in TMEM)
+  uint64_t* q_full = s_full + 2;
+  uint64_t* p_full = q_full + 1;        // the 256 softmax threads wrote this tile's P
+  uint64_t* o_full = p_full + 1;        // one commit per tile's P V
+  uint64_t* mx = o_full + 1;            // all quarters of every row posted their maxima
+  uint64_t* fin = mx + 1;
+  uint32_t* tmem_slot = (uint32_t*)(fin + 1);
+  float* sMax = (float*)(bars + 32);    // [2 tiles][4 quarters][64] tile maxima (log2)
+  float* sL = sMax;                     // [4][64] running sums, after the loop
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NST; ++i) {
       mbar_init(smem_u32(&kv_full[i]), 1);
       mbar_init(smem_u32(&kv_empty[i]), 1);
-      mbar_init(smem_u32(&s_full[i]), 1);
     }
+    mbar_init(smem_u32(&s_full[0]), 1);
+    mbar_init(smem_u32(&s_full[1]), 1);
     mbar_init(smem_u32(q_full), 1);
     mbar_init(smem_u32(p_full), 256);
     mbar_init(smem_u32(o_full), 1);
@@ -167,12 +170,13 @@ __global__ void __launch_bounds__(320, 1)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
-  if (warp == 8) tmem_alloc(smem_u32(tmem_slot), 512);
+  constexpr uint32_t kTmemCols = 2 * TK + HD <= 256 ? 256 : 512;
+  if (warp == 8) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tO = tmem + 256;  // S buffers at columns 0 and 128, O at 256
+  const uint32_t tO = tmem + 2 * TK;  // S buffers at columns 0 and TK, O after them
 
   if (warp == 8) {
     if (lane == 0) {
@@ -182,7 +186,8 @@ __global__ void __launch_bounds__(320, 1)
       mbar_expect_tx(qb, (uint32_t)(4 * L::kDB * 64 * QN * 2));
       for (int j = 0; j < L::kDB; ++j)
         for (int dup = 0; dup < 2; ++dup) {  // rows 0.. and 64..
-          tma_load_3d(smem_u32(sQ + j * kBlk + dup * 8192), &tmQh, j * 64, g * grp, b * 8, qb, polq);
+          tma_load_3d(smem_u32(sQ + j * kBlk + dup * 8192), &tmQh, j * 64, g * grp, b * 8, qb,
+                      polq);
           tma_load_3d(smem_u32(sQ + (L::kDB + j) * kBlk + dup * 8192), &tmQl, j * 64, g * grp,
                       b * 8, qb, polq);
         }
@@ -190,64 +195,64 @@ __global__ void __launch_bounds__(320, 1)
       const int vrow0 = (b * a.hkv + g) * HD;
       int issued = 0;
       for (int t = 0; t < ntiles; ++t, ++issued) {
-        const int s = t & 1;
-        if (!mbar_wait(smem_u32(&kv_empty[s]), ((t >> 1) & 1) ^ 1, err)) break;
+        const int s = t % NST;
+        if (!mbar_wait(smem_u32(&kv_empty[s]), ((t / NST) & 1) ^ 1, err)) break;
         const uint32_t full = smem_u32(&kv_full[s]);
         mbar_expect_tx(full, L::kStage);
-        const int key0 = (t0 + t) * kTileKeys;
-        uint8_t* st = sKV + s * L::kStage;
+        const int key0 = (t0 + t) * TK;
+        uint8_t* st = stage(t);
         for (int hb = 0; hb < L::kDB; ++hb)
-          tma_load_2d(smem_u32(st + hb * kBlk), &tmK, hb * 64, (int)(krow0 + key0), full, pol);
-        for (int kb = 0; kb < 2; ++kb)
-          tma_load_2d(smem_u32(st + L::kKTile + kb * HD * 128), &tmV, key0 + kb * 64, vrow0,
+          tma_load_2d(smem_u32(st + hb * L::kKBox), &tmK, hb * 64, (int)(krow0 + key0), full,
+                      pol);
+        for (int kb = 0; kb < TK / 64; ++kb)
+          tma_load_2d(smem_u32(st + L::kKTile + kb * L::kVBox), &tmV, key0 + kb * 64, vrow0,
                       full, pol);
       }
       mbar_wait(qb, 0, err);
-      for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j)
-        mbar_wait(smem_u32(&kv_full[j & 1]), (j >> 1) & 1, err);
+      for (int j = (issued > NST ? issued - NST : 0); j < issued; ++j)
+        mbar_wait(smem_u32(&kv_full[j % NST]), (j / NST) & 1, err);
     }
   } else if (warp == 9) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
-      const uint32_t id_qk = umma_idesc_bf16(128, kTileKeys);
+      const uint32_t id_qk = umma_idesc_bf16(128, TK);
       const uint32_t id_pv = umma_idesc_bf16(128, HD);
       bool ok = mbar_wait(smem_u32(q_full), 0, err);
       auto issue_qk = [&](int t) -> bool {
-        const int s = t & 1;
-        if (!mbar_wait(smem_u32(&kv_full[s]), (t >> 1) & 1, err)) return false;
+        const int s = t % NST;
+        if (!mbar_wait(smem_u32(&kv_full[s]), (t / NST) & 1, err)) return false;
         tc_fence_after();
-        uint8_t* st = sKV + s * L::kStage;
+        uint8_t* st = stage(t);
 #pragma unroll
         for (int kb = 0; kb < 2 * L::kDB; ++kb) {  // [Q_hi | Q_lo] against [K | K]
           const uint64_t dq = umma_desc_sw128(smem_u32(sQ + kb * kBlk));
-          const uint64_t dk = umma_desc_sw128(smem_u32(st + (kb % L::kDB) * kBlk));
+          const uint64_t dk = umma_desc_sw128(smem_u32(st + (kb % L::kDB) * L::kKBox));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem + s * 128, dq + 2 * kk, dk + 2 * kk, id_qk, (kb | kk) ? 1u : 0u);
+            umma_bf16(tmem + (t & 1) * TK, dq + 2 * kk, dk + 2 * kk, id_qk, (kb | kk) ? 1u : 0u);
         }
-        umma_commit(smem_u32(&s_full[s]));
+        umma_commit(smem_u32(&s_full[t & 1]));
         return true;
       };
       ok = ok && issue_qk(0);
       for (int t = 0; t < ntiles && ok; ++t) {
-        const int s = t & 1;
         // the next tile's scores overlap this tile's softmax (its S buffer was released
         // by the p_full arrival of tile t-1, waited for in the previous iteration)
         if (t + 1 < ntiles && !issue_qk(t + 1)) break;
         if (!mbar_wait(smem_u32(p_full), t & 1, err)) break;
         tc_fence_after();
-        uint8_t* st = sKV + s * L::kStage;
-#pragma unroll
+        uint8_t* st = stage(t);
         uint8_t* sP = p_buf(t);
-        for (int kb = 0; kb < 2; ++kb) {
+#pragma unroll
+        for (int kb = 0; kb < TK / 64; ++kb) {
           const uint64_t dp = umma_desc_sw128(smem_u32(sP + kb * kBlk));
-          const uint64_t dv = umma_desc_sw128(smem_u32(st + L::kKTile + kb * HD * 128));
+          const uint64_t dv = umma_desc_sw128(smem_u32(st + L::kKTile + kb * L::kVBox));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             umma_bf16(tO, dp + 2 * kk, dv + 2 * kk, id_pv, (t | kb | kk) ? 1u : 0u);
         }
         umma_commit(smem_u32(o_full));
-        umma_commit(smem_u32(&kv_empty[s]));
+        umma_commit(smem_u32(&kv_empty[t % NST]));
       }
       umma_commit(smem_u32(fin));  // all issued MMAs complete before TMEM is freed
     }
@@ -267,38 +272,35 @@ __global__ void __launch_bounds__(320, 1)
     const int srow = r / grp;
     const int row_hi = a.causal ? base + srow : hi_max;
     const float scale = rsqrtf((float)HD) * kLog2e;
-    const int pblk = kq >> 1, pch = (kq & 1) * 4;  // P block and first 16-B chunk of the quarter
+    // the quarter's keys in P: block (kq*KQ)/64, first 16-byte chunk ((kq*KQ)%64)/8
+    const int pblk = (kq * KQ) / 64, pch = ((kq * KQ) % 64) / 8;
     for (int t = 0; t < ntiles && ok; ++t) {
-      const int s = t & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[s]), (t >> 1) & 1, err));
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[t & 1]), (t >> 1) & 1, err));
       if (!ok) break;
       tc_fence_after();
-      const int kt = (t0 + t) * kTileKeys;
-      const int key0 = kt + kq * 32;
+      const int kt = (t0 + t) * TK;
+      const int key0 = kt + kq * KQ;
       // interior tiles need no mask: every key of the tile is visible to every row
-      const bool interior = kt >= k_begin && kt + kTileKeys <= k_end &&
-                            (!a.causal || kt + kTileKeys <= base + 1);
-      float sv[32];
-      {
-        float v0[16], v1[16];
-        tmem_ld16(tmem + s * 128 + kq * 32 + lane_off, v0);
-        tmem_ld16(tmem + s * 128 + kq * 32 + 16 + lane_off, v1);
+      const bool interior =
+          kt >= k_begin && kt + TK <= k_end && (!a.causal || kt + TK <= base + 1);
+      float sv[KQ];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          sv[j] = v0[j] * scale;
-          sv[16 + j] = v1[j] * scale;
-        }
+      for (int cc = 0; cc < KQ / 16; ++cc) {
+        float v[16];
+        tmem_ld16(tmem + (t & 1) * TK + kq * KQ + cc * 16 + lane_off, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) sv[cc * 16 + j] = v[j] * scale;
       }
       if (!interior) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < KQ; ++j) {
           const int key = key0 + j;
           if (!(key >= k_begin && key < k_end && key <= row_hi)) sv[j] = -INFINITY;
         }
       }
       float mt = sv[0];
 #pragma unroll
-      for (int j = 1; j < 32; ++j) mt = fmaxf(mt, sv[j]);
+      for (int j = 1; j < KQ; ++j) mt = fmaxf(mt, sv[j]);
       float* smx = sMax + (t & 1) * 256;
       smx[kq * 64 + r] = mt;
       mbar_arrive(smem_u32(mx));
@@ -323,7 +325,7 @@ __global__ void __launch_bounds__(320, 1)
       const float mu = (m == -INFINITY) ? 0.f : m;
       uint8_t* pb_ = p_buf(t) + pblk * kBlk;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < KQ / 8; ++cc) {
         uint32_t ph[4], pl[4];
 #pragma unroll
         for (int j = 0; j < 8; j += 2) {
@@ -387,15 +389,21 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   if (warp == 8) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
+// tile keys and stage count per head dim
+constexpr int kTK128 = 64, kNST128 = 4;
+constexpr int kTK64 = 64, kNST64 = 4;
+
 int attn_tc_init_attributes() {
-  cudaError_t e1 = cudaFuncSetAttribute(k_attn_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)Smem<128>::kBytes);
-  cudaError_t e2 = cudaFuncSetAttribute(k_attn_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)Smem<64>::kBytes);
+  cudaError_t e1 = cudaFuncSetAttribute(k_attn_tc<128, kTK128, kNST128>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)Smem<128, kTK128, kNST128>::kBytes);
+  cudaError_t e2 = cudaFuncSetAttribute(k_attn_tc<64, kTK64, kNST64>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)Smem<64, kTK64, kNST64>::kBytes);
   return (e1 == cudaSuccess && e2 == cudaSuccess) ? 0 : -1;
 }
 
@@ -404,9 +412,11 @@ void op_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMa
                      cudaStream_t st) {
   dim3 grid(a.nchunk, a.hkv, a.B);
   if (a.hd == 128)
-    k_attn_tc<128><<<grid, 320, Smem<128>::kBytes, st>>>(tmK, tmV, tmQh, tmQl, a, err);
+    k_attn_tc<128, kTK128, kNST128><<<grid, 320, Smem<128, kTK128, kNST128>::kBytes, st>>>(
+        tmK, tmV, tmQh, tmQl, a, err);
   else
-    k_attn_tc<64><<<grid, 320, Smem<64>::kBytes, st>>>(tmK, tmV, tmQh, tmQl, a, err);
+    k_attn_tc<64, kTK64, kNST64><<<grid, 320, Smem<64, kTK64, kNST64>::kBytes, st>>>(
+        tmK, tmV, tmQh, tmQl, a, err);
   op_attention_merge(1, a, st);
 }
 

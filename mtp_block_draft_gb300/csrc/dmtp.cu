@@ -684,7 +684,7 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
     const uint64_t krows = (uint64_t)B * c->hkv * c->maxc, vrows = (uint64_t)B * c->hkv * c->hd;
     int e = 0;
     auto maps = [&](CUtensorMap* mk, CUtensorMap* mv, void* K, void* V) {
-      e |= tc_make_tmap(mk, K, krows, c->hd, 128);
+      e |= tc_make_tmap(mk, K, krows, c->hd, 64);  // 64-key tiles
       e |= tc_make_tmap(mv, V, vrows, c->maxc, c->hd);
     };
     for (int l = 0; l < c->L; ++l)
