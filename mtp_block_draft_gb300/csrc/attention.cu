@@ -9,7 +9,8 @@
 //   target verify and MTP rows are causal: row s sees keys lo..base+s;
 //   the block drafter sees the anchor-relative window max(0, base-4096)..base-1 plus all
 //   8 block keys (no mask inside the block: DFlash's block-diagonal mask).
-// Caches: K [B][hkv][max_ctx][hd], V transposed [B][hkv][hd][max_ctx]. Chunks lie on
+// Caches: K [B][hkv][max_ctx][hd], V transposed and blocked by 64 keys
+// [B][hkv][max_ctx/64][hd][64]. Chunks lie on
 // an absolute grid of `chunk` keys (chunk c covers keys [c*chunk, (c+1)*chunk)), so
 // tiles start at aligned key indices. Scores scaled by 1/sqrt(hd); softmax in fp32.
 // This file holds the CUDA-core version (fp32 models); attention_tc.cu the tcgen05 one.
@@ -54,7 +55,7 @@ __global__ void __launch_bounds__(256) k_attn_partial(AttnArgs a) {
   }
   float m = -INFINITY, l = 0.f;
   const T* Kb = (const T*)a.Kc + ((long)b * a.hkv + g) * a.max_ctx * hd;
-  const T* Vb = (const T*)a.Vc + ((long)b * a.hkv + g) * hd * a.max_ctx;  // [hd][max_ctx]
+  const T* Vb = (const T*)a.Vc + ((long)b * a.hkv + g) * hd * a.max_ctx;  // [max_ctx/64][hd][64]
 
   for (int kt = k_begin; kt < k_end; kt += kTK) {
     const int nk = min(kTK, k_end - kt);
@@ -65,7 +66,8 @@ __global__ void __launch_bounds__(256) k_attn_partial(AttnArgs a) {
     }
     for (int e = threadIdx.x; e < kTK * hd; e += blockDim.x) {
       const int j = e % kTK, dd = e / kTK;  // keys contiguous in the transposed V
-      Vs[j][dd] = (j < nk) ? to_f32(Vb[(long)dd * a.max_ctx + kt + j]) : 0.f;
+      const int key = kt + j;
+      Vs[j][dd] = (j < nk) ? to_f32(Vb[((long)(key / 64) * hd + dd) * 64 + key % 64]) : 0.f;
     }
     __syncthreads();
     float sc[kTK];

@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(320, 1)
                       b * 8, qb, polq);
         }
       const long krow0 = ((long)b * a.hkv + g) * a.max_ctx;
-      const int vrow0 = (b * a.hkv + g) * HD;
+      const long vblk0 = ((long)b * a.hkv + g) * (a.max_ctx / 64);  // 64-key V^T blocks
       int issued = 0;
       for (int t = 0; t < ntiles; ++t, ++issued) {
         const int s = t % NST;
@@ -205,8 +205,8 @@ __global__ void __launch_bounds__(320, 1)
           tma_load_2d(smem_u32(st + hb * L::kKBox), &tmK, hb * 64, (int)(krow0 + key0), full,
                       pol);
         for (int kb = 0; kb < TK / 64; ++kb)
-          tma_load_2d(smem_u32(st + L::kKTile + kb * L::kVBox), &tmV, key0 + kb * 64, vrow0,
-                      full, pol);
+          tma_load_2d(smem_u32(st + L::kKTile + kb * L::kVBox), &tmV, 0,
+                      (int)((vblk0 + key0 / 64 + kb) * HD), full, pol);
       }
       mbar_wait(qb, 0, err);
       for (int j = (issued > NST ? issued - NST : 0); j < issued; ++j)

@@ -190,7 +190,7 @@ int derive(dmtp_ctx* c, const dmtp_config* cfg, int B) {
   c->mt6 = tc_mt(6 * B);
   c->mt1 = tc_mt(B);
   c->attn_tc = c->dt == 1 && (c->hd == 64 || c->hd == 128) && QN <= 64;
-  c->attn_chunk = 512;  // keys per attention partial; a multiple of the 128-key tile
+  c->attn_chunk = 1024;  // keys per attention partial; a multiple of the 64-key tile
   c->attn_nchunk = (c->maxc + 8 + c->attn_chunk - 1) / c->attn_chunk;
   return DMTP_OK;
 }
@@ -681,11 +681,13 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
     return DMTP_ECUDA;
   }
   if (c->attn_tc) {
-    const uint64_t krows = (uint64_t)B * c->hkv * c->maxc, vrows = (uint64_t)B * c->hkv * c->hd;
+    // K: [B*hkv*max_ctx, hd]; V^T blocked by 64 keys: [B*hkv*(max_ctx/64)*hd, 64]
+    const uint64_t krows = (uint64_t)B * c->hkv * c->maxc;
+    const uint64_t vrows = (uint64_t)B * c->hkv * (c->maxc / 64) * c->hd;
     int e = 0;
     auto maps = [&](CUtensorMap* mk, CUtensorMap* mv, void* K, void* V) {
       e |= tc_make_tmap(mk, K, krows, c->hd, 64);  // 64-key tiles
-      e |= tc_make_tmap(mv, V, vrows, c->maxc, c->hd);
+      e |= tc_make_tmap(mv, V, vrows, 64, c->hd);
     };
     for (int l = 0; l < c->L; ++l)
       if (c->tK[l]) maps(&c->tmK[l], &c->tmV[l], c->tK[l], c->tV[l]);

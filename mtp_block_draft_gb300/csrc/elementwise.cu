@@ -200,8 +200,9 @@ void op_rope_table(float2* tab, int npos, int hd, float theta, cudaStream_t st) 
 
 // ---------------------------------------------------------------------------------
 // RoPE + KV-cache write. Row m = b*8 + s at position base[b] + s. One CTA per row;
-// threads cover (head, pair). K cache [B][hkv][max_ctx][hd]; V cache transposed,
-// [B][hkv][hd][max_ctx], so that P.V reads it K-major on the tensor cores.
+// threads cover (head, pair). K cache [B][hkv][max_ctx][hd]; V cache transposed and
+// blocked by 64 keys, [B][hkv][max_ctx/64][hd][64], so that P.V reads it K-major on the
+// tensor cores and a 64-key tile of it is one contiguous block.
 // ---------------------------------------------------------------------------------
 template <typename T>
 __global__ void k_rope_kv(const float* __restrict__ src, int ld, int q_off, int k_off, int v_off,
@@ -240,9 +241,10 @@ __global__ void k_rope_kv(const float* __restrict__ src, int ld, int q_off, int 
     T* kc = Kc + (((long)b * hkv + h) * max_ctx + pos) * hd;
     kc[i] = from_f32<T>(x1 * cs.x - x2 * cs.y);
     kc[half + i] = from_f32<T>(x2 * cs.x + x1 * cs.y);
-    T* vc = Vc + ((long)b * hkv + h) * hd * max_ctx + pos;  // transposed [hd][max_ctx]
-    vc[(long)i * max_ctx] = from_f32<T>(row[v_off + h * hd + i]);
-    vc[(long)(half + i) * max_ctx] = from_f32<T>(row[v_off + h * hd + half + i]);
+    // transposed and blocked by 64 keys: [max_ctx/64][hd][64]
+    T* vc = Vc + (((long)b * hkv + h) * (max_ctx / 64) + pos / 64) * hd * 64 + (pos % 64);
+    vc[(long)i * 64] = from_f32<T>(row[v_off + h * hd + i]);
+    vc[(long)(half + i) * 64] = from_f32<T>(row[v_off + h * hd + half + i]);
   }
 }
 

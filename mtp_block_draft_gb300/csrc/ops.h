@@ -101,7 +101,7 @@ void op_prefill_done(const RoundState& s, const int* plen, cudaStream_t st);
 // ---- attention.cu ------------------------------------------------------------------
 struct AttnArgs {
   const void* Kc;      // [B][hkv][max_ctx][hd] dt
-  const void* Vc;      // [B][hkv][hd][max_ctx] dt (transposed)
+  const void* Vc;      // [B][hkv][max_ctx/64][hd][64] dt (transposed, blocked by 64 keys)
   const float* q;      // [B*8][hq][hd] fp32
   float* part_o;       // [B][hkv][nchunk][QN][hd]
   float* part_ml;      // [B][hkv][nchunk][QN][2]
@@ -117,7 +117,7 @@ void op_attention(int dt, const AttnArgs& a, cudaStream_t st);
 void op_attention_merge(int dt, const AttnArgs& a, cudaStream_t st);
 // tcgen05 attention (bf16 caches, head_dim 64 or 128, 8 x GQA-group <= 64 queries);
 // tmK: K cache as [B*hkv*max_ctx, hd] box {64, 128}; tmV: transposed V cache as
-// [B*hkv*hd, max_ctx] box {64, hd}; tmQh / tmQl: the bf16 query halves as 3-D
+// blocked [B*hkv*(max_ctx/64)*hd, 64] box {64, hd}; tmQh / tmQl: the bf16 query halves as 3-D
 // [B*8][hq][hd] maps, box {64, hq/hkv, 8}. Writes the partials of op_attention, merges.
 void op_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV,
                      const CUtensorMap& tmQh, const CUtensorMap& tmQl, unsigned* err,
