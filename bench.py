@@ -231,8 +231,8 @@ def main():
     _, _, h1 = g.read_state()
     dh = (h1 - h0).astype(np.int64)
     tokens = int(np.sum((np.arange(8) + 1) * dh))
-    rounds = int(dh.sum())
-    mean_len = tokens / max(1, rounds)
+    seq_rounds = int(dh.sum())  # one histogram entry per sequence per round
+    mean_len = tokens / max(1, seq_rounds)
     t = torch.tensor([ms, float(tokens)], dtype=torch.float64, device=dev)
     if world > 1:
         tmax = t.clone()
@@ -300,7 +300,7 @@ def main():
                        "global_batch": B * world, "seq_len": int(np.mean([len(p) for p in prompts])),
                        "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (~7 GB of weights+KV streamed per round)",
-                       "mean_accept_len": mean_len, "rounds_per_s": rounds / (ms / 1e3)},
+                       "mean_accept_len": mean_len, "rounds_per_s": args.steps / (ms / 1e3)},
             "clocks": clk,
             "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": B * 8 * 4 + B * 4},

@@ -1,0 +1,123 @@
+"""Parity at the workloads' full sizes, in the launch configuration bench.py times.
+
+* small (B=1, 2048-token prompt, vocab 32000): the whole batch in lock-step with the
+  oracle.
+* B32 (32 sequences, prompts U[512, 4096], vocab 151936, 16 layers): the GPU runs the
+  full batch; the oracle computes one sampled sequence (the shortest prompt) by itself,
+  since sequences are independent.
+* hybrid (48 layers, 36 Gated DeltaNet with 32 heads of 128 x 128 state): full model
+  dimensions against the oracle at a short prompt (the oracle's recurrence runs row by
+  row), and the full 8 x 4096 batch through properties.
+* long (4 x 32768) and full hybrid: the oracle cannot prefill these, so properties that
+  hold at any size are checked instead. Drafts forced to be wrong make every round plain
+  one-token greedy decoding through the verify path; feeding that stream back as forced
+  drafts must then accept all 7 drafts every round and commit the same tokens
+  (losslessness and block == chain, the colibri forced-draft modes). Where the two
+  disagree, the verify logits must show a near tie (gap <= 0.05).
+"""
+import numpy as np
+import pytest
+import torch
+
+from synth import CONFIGS, make_prompts, make_weights
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-2
+GATE = 0.05
+
+
+def test_small_full_size_lockstep():
+    from lockstep import Lockstep
+    cfg = CONFIGS["small"]
+    ls = Lockstep(cfg, make_weights(cfg, "cuda"), make_prompts(cfg), rounds=3)
+    for _ in range(3):
+        ls.step(tol=TOL)
+    ls.close()
+
+
+def test_b32_full_size_sampled_sequence():
+    from lockstep import Lockstep
+    cfg = CONFIGS["b32"]
+    prompts = make_prompts(cfg)
+    b = int(np.argmin([len(p) for p in prompts]))
+    ls = Lockstep(cfg, make_weights(cfg, "cuda"), prompts, rounds=2, seqs=[b])
+    for _ in range(2):
+        ls.step(tol=TOL)
+    ls.close()
+
+
+def test_hybrid_full_dims_lockstep():
+    from lockstep import Lockstep
+    cfg = CONFIGS["hybrid"].replace(batch=2, ctx_lo=96, ctx_hi=160)
+    ls = Lockstep(cfg, make_weights(cfg, "cuda"), make_prompts(cfg), rounds=3)
+    for r in range(3):
+        ls.step(tol=TOL)
+    ls.close()
+
+
+def _rounds(cfg, w, prompts, rounds, forced_fn, want_logits=False):
+    """Run `rounds` rounds; forced_fn(r, streams) -> int32 [B, 7] drafts."""
+    from mtp_block_draft_gb300 import DmtpRound, default_max_ctx
+    g = DmtpRound(cfg, w, prompts, default_max_ctx(prompts, rounds))
+    _, A, _ = g.read_state()
+    streams = [[int(a)] for a in A]
+    recs = []
+    for r in range(rounds):
+        forced = torch.as_tensor(forced_fn(r, streams), dtype=torch.int32, device="cuda")
+        out = g.alloc_out(ints=True, floats=False)
+        if want_logits:
+            out["verify_logits"] = torch.empty((len(prompts), 8, cfg.vocab), dtype=torch.float32,
+                                               device="cuda")
+        g.round(out, forced=forced)
+        torch.cuda.synchronize()
+        o = {k: v.cpu().numpy() for k, v in out.items()}
+        for b in range(len(prompts)):
+            streams[b] += [int(t) for t in o["committed"][b][:o["n_accepted"][b] + 1]]
+        recs.append(o)
+    g.close()
+    return streams, recs
+
+
+def _forced_stream_property(cfg, rounds):
+    w = make_weights(cfg, "cuda")
+    prompts = make_prompts(cfg)
+    V = cfg.vocab
+    # 1) every draft wrong: one token per round, plain greedy decoding
+    def wrong(r, streams):
+        return [[(s[-1] + 1 + j) % (V - 1) for j in range(7)] for s in streams]
+
+    greedy, recs = _rounds(cfg, w, prompts, 8 * rounds, wrong)
+    for o in recs:
+        assert (o["n_accepted"] == 0).all()
+    # 2) drafts forced to that stream: all 7 accepted, same tokens
+    def right(r, streams):
+        out = []
+        for b, s in enumerate(streams):
+            k = len(s)
+            ref = greedy[b]
+            out.append([ref[k + j] if k + j < len(ref) else 0 for j in range(7)])
+        return out
+
+    streams, recs = _rounds(cfg, w, prompts, rounds, right, want_logits=True)
+    for b in range(len(prompts)):
+        k = 0  # stream index of the round's pending token
+        for r, o in enumerate(recs):
+            n = int(o["n_accepted"][b])
+            committed = [int(t) for t in o["committed"][b][:n + 1]]
+            assert committed[:n] == greedy[b][k + 1:k + 1 + n], (b, r)
+            ref = greedy[b][k + 1 + n]  # the draft (n < 7) or the bonus token (n = 7)
+            if committed[n] != ref or n < 7:
+                # only a near tie between the target's pick and the reference may differ
+                lg = o["verify_logits"][b][n]
+                pick = int(o["picks"][b][n])
+                assert abs(float(lg[pick]) - float(lg[ref])) <= GATE, (b, r, n, pick, ref)
+                break
+            k += 8
+
+
+def test_long_full_size_forced_stream():
+    _forced_stream_property(CONFIGS["long"], rounds=2)
+
+
+def test_hybrid_full_size_forced_stream():
+    _forced_stream_property(CONFIGS["hybrid"], rounds=2)
