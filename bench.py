@@ -52,6 +52,23 @@ def _peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+def _traffic(kernel: str, alg_bytes_per_launch: float):
+    """DRAM bytes per launch of `kernel` from the ncu captures summarised in profiles/
+    (DRAM / algorithmic ratio of that kernel), or None once the kernel source changed."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None, None
+    rec = json.load(open(p)).get(kernel)
+    if not rec:
+        return None, None
+    src = os.path.join(ROOT, rec["source"])
+    if hashlib.sha1(open(src, "rb").read()).hexdigest() != rec["sha1"]:
+        return None, "kernel changed since the ncu capture"
+    return alg_bytes_per_launch * rec["dram_over_algorithmic"], \
+        f"ncu DRAM/algorithmic ratio {rec['dram_over_algorithmic']} (profiles/{rec['capture']})"
+
+
 class Clocks:
     """nvidia-smi sampler for the timed region (200 ms period)."""
 
@@ -278,7 +295,9 @@ def main():
                 "frac": tfs / tc_sus}
     else:
         roof = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm}
-    roof.update({"kernel": dom, "traffic": None, "peak_source": f"{peak_src} (MEASURED_PEAKS.json)"
+    traffic, tsrc = _traffic(dom, a["bytes"] / launches)
+    roof.update({"kernel": dom, "traffic": traffic, "traffic_source": tsrc,
+                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json)"
                  if peak_src == "measured" else "fallback (profiling recipe)",
                  "per_launch_bytes": a["bytes"] / launches})
     breakdown = {c: {"ms_per_round": round(agg[c]["ms"], 4),
