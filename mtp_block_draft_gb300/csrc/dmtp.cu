@@ -277,7 +277,10 @@ size_t layout(dmtp_ctx* c, char* base) {
 // prompts are staged after the fixed layout (size depends on the prompt lengths)
 size_t prompt_bytes(int B, int pmax) { return ((size_t)B * pmax * 4 + 255) & ~(size_t)255; }
 
-int plan(dmtp_ctx* c, Gemm& g, const void* W, int N, int K, const void* X, int M, bool argmax) {
+// split: X holds [hi; lo] bf16 halves (all GEMMs but the LM head, whose single bf16
+// operand keeps the logit error near 1e-3 at half the tensor-core work)
+int plan(dmtp_ctx* c, Gemm& g, const void* W, int N, int K, const void* X, int M, bool argmax,
+         bool split = true) {
   g.W = W;
   g.X = X;
   g.N = N;
@@ -286,7 +289,7 @@ int plan(dmtp_ctx* c, Gemm& g, const void* W, int N, int K, const void* X, int M
   g.argmax = argmax;
   if (!W) return DMTP_EINVAL;
   if (c->dt == 1)
-    return tc_plan(&g.tc, W, N, K, X, M, c->nsm, argmax, true) ? DMTP_EINVAL : DMTP_OK;
+    return tc_plan(&g.tc, W, N, K, X, M, c->nsm, argmax, split) ? DMTP_EINVAL : DMTP_OK;
   return DMTP_OK;
 }
 
@@ -369,10 +372,11 @@ inline int mt_of_rows(const dmtp_ctx* c, int rows) {
 }
 
 void norm(dmtp_ctx* c, const float* x, const void* g, void* y, float* y32, void* tap, int rows,
-          RowMap map = RowMap()) {
+          RowMap map = RowMap(), bool split = true) {
   launch(c, P_OTHER, 0, 0, [&] {
     const int mt = mt_of_rows(c, rows);
-    op_rmsnorm(c->dt, x, c->d, g, y, c->d, lo_of(c, mt, c->d), y32, c->d, tap, c->ntap * c->d,
+    op_rmsnorm(c->dt, x, c->d, g, y, c->d, split ? lo_of(c, mt, c->d) : 0, y32, c->d, tap,
+               c->ntap * c->d,
                lo_of(c, c->mt8, c->ntap * c->d), rows, c->d,
                c->cfg.rms_eps, map, c->st);
   });
@@ -494,7 +498,8 @@ void target_forward(dmtp_ctx* c, bool snapshots) {
       gdn_layer(c, l, c->x, tap_in, snapshots);
     }
   }
-  norm(c, c->x, c->w.final_norm, c->hTn, c->hT32, tap_ptr(c, c->tap_of_layer[c->L - 1]), M);
+  norm(c, c->x, c->w.final_norm, c->hTn, c->hT32, tap_ptr(c, c->tap_of_layer[c->L - 1]), M,
+       RowMap(), false);
 }
 
 // a6 (and each prefill chunk): drafter context K/V at positions pos0+s from the taps,
@@ -537,7 +542,7 @@ void enqueue_round(dmtp_ctx* c, const Dbg& dbg, const int* forced) {
   const int B = c->B;
   launch(c, P_OTHER, 0, 0, [&] { op_round_begin(s, c->st); });
   // a1: T1 from the cached MTP hidden
-  norm(c, c->h_mtp, c->w.mtp_final_norm, c->t1in, nullptr, nullptr, B);
+  norm(c, c->h_mtp, c->w.mtp_final_norm, c->t1in, nullptr, nullptr, B, RowMap(), false);
   gemm_argmax(c, c->head_t1, s.keys, dbg.t1);
   launch(c, P_OTHER, 0, 0, [&] { op_keys_to_ids(s.keys, B, 1, s.drafts, 7, 0, forced, 7, 0, c->st); });
   // a2: Delta = W [RMS_e(E(T1)); RMS_m(h_MTP)]; slots [E(A), E(T1)+Delta, E(MASK) x 6]
@@ -563,7 +568,7 @@ void enqueue_round(dmtp_ctx* c, const Dbg& dbg, const int* forced) {
   m6.out_group = 6;
   m6.in_group = 8;
   m6.in_offset = 2;
-  norm(c, c->x, c->w.dft_final_norm, c->dn, nullptr, nullptr, 6 * B, m6);
+  norm(c, c->x, c->w.dft_final_norm, c->dn, nullptr, nullptr, 6 * B, m6, false);
   gemm_argmax(c, c->head_d, s.keys + B, dbg.dl);
   launch(c, P_OTHER, 0, 0, [&] { op_keys_to_ids(s.keys + B, B, 6, s.drafts, 7, 1, forced, 7, 1, c->st); });
   // a4: target verify of [A, T1..T7]
@@ -667,9 +672,9 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
   }
   pr |= plan_layer(c, c->mtp, w->mtp, 0, M);
   pr |= plan(c, c->fuse, w->fuse_w, c->d, 2 * c->d, c->zf, B, false);
-  pr |= plan(c, c->head_t1, w->head, c->V, c->d, c->t1in, B, true);
-  pr |= plan(c, c->head_d, w->head, c->V, c->d, c->dn, 6 * B, true);
-  pr |= plan(c, c->head_v, w->head, c->V, c->d, c->hTn, M, true);
+  pr |= plan(c, c->head_t1, w->head, c->V, c->d, c->t1in, B, true, false);
+  pr |= plan(c, c->head_d, w->head, c->V, c->d, c->dn, 6 * B, true, false);
+  pr |= plan(c, c->head_v, w->head, c->V, c->d, c->hTn, M, true, false);
   pr |= plan(c, c->dfc, w->dft_fc, c->d, c->ntap * c->d, c->taps, M, false);
   pr |= plan(c, c->mproj, w->mtp_proj, c->d, 2 * c->d, c->z, M, false);
   if (pr) {
@@ -746,8 +751,7 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
     }
   }
   // A = the target's greedy token after the prompt; MTP consumes (h^T_{P-1}, A) at P
-  op_cast_rows(c->dt, c->hlast, c->d, c->t1in, c->d, lo_of(c, c->mt1, c->d), B, c->d, RowMap(),
-               st);
+  op_cast_rows(c->dt, c->hlast, c->d, c->t1in, c->d, 0, B, c->d, RowMap(), st);
   zero(c, s.keys, (size_t)B * 8);
   gemm_argmax(c, c->head_t1, s.keys, nullptr);
   op_keys_to_ids(s.keys, B, 1, s.A, 1, 0, nullptr, 0, 0, st);

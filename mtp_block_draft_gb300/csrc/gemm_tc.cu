@@ -18,9 +18,11 @@
 //
 // Split activations: the token operand may come as two bf16 halves, X = X_hi + X_lo
 // (X_lo = the rounding remainder of X_hi), stored as 2*MT rows [hi; lo]. Both halves
-// are multiplied by the same weight tile (one TMA load of W, two MMA column ranges)
-// and summed in the epilogue, so the activations keep ~16 significant bits while the
-// weights stay bf16 and each weight byte is still read once.
+// are multiplied by the same weight tile (one TMA load of W). Up to 128 token rows the
+// halves are one load and one MMA of 2*MT columns, summed in the epilogue; above that
+// they are two loads and two MMAs accumulating into the same TMEM columns. Either way
+// the activations keep ~16 significant bits while the weights stay bf16 and each
+// weight byte is still read once.
 //
 // The LM-head variant fuses the row argmax (DMTP blog §6.5: the vocabulary output
 // layer scores every token): per column the CTA reduces its 128 vocabulary rows to a
@@ -81,7 +83,10 @@ __global__ void __launch_bounds__(128, 1)
   const int nkb = a.K / kBlockK;
   const int kb0 = (int)((long)blockIdx.y * nkb / gridDim.y);
   const int kb1 = (int)((long)(blockIdx.y + 1) * nkb / gridDim.y);
-  const uint32_t ncols = tmem_cols_for(a.xbox * a.nx);
+  // one accumulator of xbox columns; with two loads per stage (nx = 2: the hi and lo
+  // halves of more than 128 token rows) both products accumulate into it
+  const uint32_t ncols = tmem_cols_for(a.xbox);
+  const bool lo_cols = a.split && a.nx == 1;  // hi and lo in one load: lo in columns MT..
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
@@ -131,8 +136,7 @@ __global__ void __launch_bounds__(128, 1)
         for (int j = 0; j < a.nx; ++j) {
           const uint64_t dx =
               umma_desc_sw128(smem_u32(sX + s * xbytes + j * a.xbox * kBlockK * 2));
-          umma_bf16(tmem + j * a.xbox, dw + 2 * k, dx + 2 * k, idesc,
-                    (kb > kb0 || k > 0) ? 1u : 0u);
+          umma_bf16(tmem, dw + 2 * k, dx + 2 * k, idesc, (kb > kb0 || k > 0 || j > 0) ? 1u : 0u);
         }
       }
       umma_commit(smem_u32(&empty[s]));
@@ -153,7 +157,7 @@ __global__ void __launch_bounds__(128, 1)
       for (int c = 0; c < a.MT; c += 16) {
         float v[16];
         tmem_ld16(tbase + c, v);
-        if (a.split) {
+        if (lo_cols) {
           float w[16];
           tmem_ld16(tbase + a.MT + c, w);
 #pragma unroll
@@ -174,7 +178,7 @@ __global__ void __launch_bounds__(128, 1)
       for (int c = 0; c < a.MT; c += 16) {
         float v[16];
         tmem_ld16(tbase + c, v);
-        if (a.split) {
+        if (lo_cols) {
           float w[16];
           tmem_ld16(tbase + a.MT + c, w);
 #pragma unroll

@@ -5,7 +5,7 @@
 // and forbids allocations outside it, or a latency-critical path where cudaMalloc /
 // cudaFree would synchronise the device. The round library already takes all of its
 // memory from the caller; this entry point goes further and needs no workspace at all.
-// Its scratch - the split bf16 operand of the head GEMM and the packed argmax keys - is
+// Its scratch - the bf16 operand of the head GEMM and the packed argmax keys - is
 // a file-scope __device__ array of fixed size that every GPU loading the library holds
 // until the process exits.
 //
@@ -24,7 +24,7 @@ namespace {
 
 constexpr int kMaxRows = DMTP_NOALLOC_MAX_ROWS;  // token rows per call
 constexpr int kMaxD = DMTP_NOALLOC_MAX_DMODEL;   // hidden size
-constexpr size_t kOperandBytes = (size_t)2 * kMaxRows * kMaxD * 2;  // [hi; lo] x d, bf16
+constexpr size_t kOperandBytes = (size_t)kMaxRows * kMaxD * 2;  // rows x d, bf16
 constexpr size_t kKeyBytes = (size_t)kMaxRows * 8;
 
 // The scratch: the GEMM operand, then the argmax keys.
@@ -63,12 +63,12 @@ extern "C" int dmtp_t1_head_noalloc(const void* head, const void* norm_gain, con
   cudaStream_t st = (cudaStream_t)stream;
   void* X = base;
   unsigned long long* keys = (unsigned long long*)((char*)base + kOperandBytes);
-  const int mt = dmtp::tc_mt(rows);
   dmtp::TcPlan plan;
-  if (dmtp::tc_plan(&plan, head, vocab, d_model, X, rows, 1, true, true)) return DMTP_EINVAL;
+  // the same single-bf16 operand as the round's LM-head GEMMs
+  if (dmtp::tc_plan(&plan, head, vocab, d_model, X, rows, 1, true, false)) return DMTP_EINVAL;
   // keys start at zero for the atomic max; the operand rows are fully rewritten
   if (cudaMemsetAsync(keys, 0, (size_t)rows * 8, st) != cudaSuccess) return DMTP_ECUDA;
-  dmtp::op_rmsnorm(1, h, d_model, norm_gain, X, d_model, (long)mt * d_model, nullptr, 0,
+  dmtp::op_rmsnorm(1, h, d_model, norm_gain, X, d_model, 0, nullptr, 0,
                    nullptr, 0, 0, rows, d_model, eps, dmtp::RowMap(), st);
   dmtp::op_gemm_tc_argmax(plan, keys, logits, vocab, nullptr, st);
   dmtp::op_keys_to_ids(keys, rows, 1, ids, 1, 0, nullptr, 0, 0, st);
