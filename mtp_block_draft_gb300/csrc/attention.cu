@@ -136,6 +136,79 @@ __global__ void k_attn_merge(AttnArgs a) {
   }
 }
 
+// Warp form: one warp per (row, query head), hd / 32 dimensions per lane; the lanes
+// stride over the chunks for the maxima and sums.
+template <typename T, int DPL>
+__global__ void __launch_bounds__(256) k_attn_merge_w(AttnArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y * 8 + warp;
+  if (h >= a.hq) return;
+  const int mrow = blockIdx.x;
+  const int b = mrow >> 3, s = mrow & 7;
+  const int grp = a.hq / a.hkv, g = h / grp, hh = h % grp, qi = s * grp + hh, QN = 8 * grp;
+  const int base = a.base[b];
+  int lo = a.lo_fixed;
+  if (a.window > 0) lo = max(lo, base - a.window);
+  const int c0 = lo / a.chunk, c1 = min(a.nchunk - 1, (base + 7) / a.chunk);
+  const long p0 = ((long)b * a.hkv + g) * a.nchunk;
+  const float* ml = a.part_ml + (p0 * QN + qi) * 2;  // chunk c at ml[c * QN * 2]
+  float M = -INFINITY;
+  for (int c = c0 + lane; c <= c1; c += 32) M = fmaxf(M, ml[(long)c * QN * 2]);
+  M = warp_max(M);
+  float L = 0.f;
+  for (int c = c0 + lane; c <= c1; c += 32)
+    L += ml[(long)c * QN * 2 + 1] * __expf(ml[(long)c * QN * 2] - M);
+  L = warp_sum(L);
+  const float invL = 1.f / L;
+  float acc[DPL];
+#pragma unroll
+  for (int j = 0; j < DPL; ++j) acc[j] = 0.f;
+  const float* po = a.part_o + (p0 * QN + qi) * a.hd + lane * DPL;
+  for (int c = c0; c <= c1; ++c) {
+    const float w = __expf(ml[(long)c * QN * 2] - M);
+    const float* pc = po + (long)c * QN * a.hd;
+    if (DPL % 4 == 0) {
+#pragma unroll
+      for (int j = 0; j < DPL; j += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(pc + j);
+        acc[j] += v.x * w;
+        acc[j + 1] += v.y * w;
+        acc[j + 2] += v.z * w;
+        acc[j + 3] += v.w * w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) acc[j] += pc[j] * w;
+    }
+  }
+  T* out = (T*)a.out + (long)mrow * a.hq * a.hd + h * a.hd + lane * DPL;
+  if (DPL % 4 == 0) {
+#pragma unroll
+    for (int j = 0; j < DPL; j += 4)
+      store_act4(out + j, a.out_lo,
+                 make_float4(acc[j] * invL, acc[j + 1] * invL, acc[j + 2] * invL,
+                             acc[j + 3] * invL));
+  } else {
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) store_act(out + j, a.out_lo, acc[j] * invL);
+  }
+}
+
+template <typename T>
+static bool merge_w(const AttnArgs& a, cudaStream_t st) {
+  const unsigned eo = sizeof(T) * 4;
+  if (a.hd % 32 || !aligned_to(a.part_o, 16) || !aligned_to(a.out, eo) || a.out_lo % 4)
+    return false;
+  dim3 g(a.B * 8, (a.hq + 7) / 8);
+  switch (a.hd / 32) {
+    case 1: k_attn_merge_w<T, 1><<<g, 256, 0, st>>>(a); return true;
+    case 2: k_attn_merge_w<T, 2><<<g, 256, 0, st>>>(a); return true;
+    case 4: k_attn_merge_w<T, 4><<<g, 256, 0, st>>>(a); return true;
+    case 8: k_attn_merge_w<T, 8><<<g, 256, 0, st>>>(a); return true;
+    default: return false;
+  }
+}
+
 void op_attention(int dt, const AttnArgs& a, cudaStream_t st) {
   dim3 g1(a.nchunk, a.hkv, a.B);
   if (dt)
@@ -146,6 +219,7 @@ void op_attention(int dt, const AttnArgs& a, cudaStream_t st) {
 }
 
 void op_attention_merge(int dt, const AttnArgs& a, cudaStream_t st) {
+  if (dt ? merge_w<bf16>(a, st) : merge_w<float>(a, st)) return;
   dim3 g2(a.B * 8, a.hq);
   if (dt)
     k_attn_merge<bf16><<<g2, 128, 0, st>>>(a);

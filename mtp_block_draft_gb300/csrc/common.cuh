@@ -41,6 +41,42 @@ __device__ __forceinline__ void store_act(bf16* p, long lo_off, float v) {
   if (lo_off) p[lo_off] = __float2bfloat16_rn(v - __bfloat162float(h));
 }
 
+// Four consecutive elements: p 16-byte aligned (fp32) or 8-byte aligned (bf16), and,
+// for bf16, p + lo_off 8-byte aligned. Same rounding as four store_act calls.
+__device__ __forceinline__ void store_act4(float* p, long lo_off, float4 v) {
+  (void)lo_off;
+  *reinterpret_cast<float4*>(p) = v;
+}
+__device__ __forceinline__ void store_act4(bf16* p, long lo_off, float4 v) {
+  const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y);
+  const __nv_bfloat162 h23 = __floats2bfloat162_rn(v.z, v.w);
+  uint2 hv;
+  hv.x = *reinterpret_cast<const uint32_t*>(&h01);
+  hv.y = *reinterpret_cast<const uint32_t*>(&h23);
+  *reinterpret_cast<uint2*>(p) = hv;
+  if (lo_off) {
+    const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+    const __nv_bfloat162 l01 = __floats2bfloat162_rn(v.x - f01.x, v.y - f01.y);
+    const __nv_bfloat162 l23 = __floats2bfloat162_rn(v.z - f23.x, v.w - f23.y);
+    uint2 lv;
+    lv.x = *reinterpret_cast<const uint32_t*>(&l01);
+    lv.y = *reinterpret_cast<const uint32_t*>(&l23);
+    *reinterpret_cast<uint2*>(p + lo_off) = lv;
+  }
+}
+__device__ __forceinline__ float4 load4(const float* p) {
+  return *reinterpret_cast<const float4*>(p);
+}
+__device__ __forceinline__ float4 load4(const bf16* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+__host__ __device__ inline bool aligned_to(const void* p, unsigned bytes) {
+  return ((uintptr_t)p % bytes) == 0;
+}
+
 __device__ __forceinline__ void set_err(unsigned* err, unsigned bit) {
   if (err) atomicOr(err, bit);
 }

@@ -371,14 +371,15 @@ inline int mt_of_rows(const dmtp_ctx* c, int rows) {
   return rows == c->M ? c->mt8 : (rows == 6 * c->B ? c->mt6 : c->mt1);
 }
 
+// zero / nz: also clears the first nz floats of each of the `rows` rows of zero (the
+// accumulator of the GEMM that reads y), instead of a separate memset.
 void norm(dmtp_ctx* c, const float* x, const void* g, void* y, float* y32, void* tap, int rows,
-          RowMap map = RowMap(), bool split = true) {
+          RowMap map = RowMap(), bool split = true, float* zero = nullptr, int nz = 0) {
   launch(c, P_OTHER, 0, 0, [&] {
     const int mt = mt_of_rows(c, rows);
     op_rmsnorm(c->dt, x, c->d, g, y, c->d, split ? lo_of(c, mt, c->d) : 0, y32, c->d, tap,
-               c->ntap * c->d,
-               lo_of(c, c->mt8, c->ntap * c->d), rows, c->d,
-               c->cfg.rms_eps, map, c->st);
+               c->ntap * c->d, lo_of(c, c->mt8, c->ntap * c->d), rows, c->d, c->cfg.rms_eps,
+               map, c->st, zero, nz, nz);
   });
 }
 
@@ -398,8 +399,7 @@ struct AttnSpec {
 void attn_layer(dmtp_ctx* c, const LayerPlans& p, const dmtp_layer_weights& w, float* xr,
                 const AttnSpec& a, void* tap_in) {
   const int M = c->M;
-  norm(c, xr, w.attn_norm, c->xn, nullptr, tap_in, M);
-  zero(c, c->qkv, (size_t)M * c->qkvd * 4);
+  norm(c, xr, w.attn_norm, c->xn, nullptr, tap_in, M, RowMap(), true, c->qkv, c->qkvd);
   gemm_acc(c, p.qkv, c->qkv, c->qkvd);
   launch(c, P_OTHER, 0, 0, [&] { op_rope_kv(c->dt, c->qkv, c->qkvd, 0, c->qd, c->qd + c->kvd, c->q, c->attn_tc ? c->qs : nullptr, (long)M * c->qd, a.Kc, a.Vc, a.base, c->rope,
              M, c->hq, c->hkv, c->hd, c->maxc, c->err, c->st); });
@@ -442,8 +442,7 @@ void attn_layer(dmtp_ctx* c, const LayerPlans& p, const dmtp_layer_weights& w, f
   });
   c->launches += 1;  // partial + merge
   gemm_acc(c, p.o, xr, c->d);
-  norm(c, xr, w.mlp_norm, c->xn, nullptr, nullptr, M);
-  zero(c, c->gu, (size_t)M * 2 * c->F * 4);
+  norm(c, xr, w.mlp_norm, c->xn, nullptr, nullptr, M, RowMap(), true, c->gu, 2 * c->F);
   gemm_acc(c, p.gu, c->gu, 2 * c->F);
   launch(c, P_OTHER, 0, 0, [&] { op_swiglu(c->dt, c->gu, c->hmid, lo_of(c, c->mt8, c->F), M, c->F, c->st); });
   gemm_acc(c, p.down, xr, c->d);
@@ -454,8 +453,7 @@ void gdn_layer(dmtp_ctx* c, int l, float* xr, void* tap_in, bool snapshots) {
   const dmtp_layer_weights& w = c->w.layers[l];
   const int M = c->M, gi = c->gdn_index[l];
   const int nqkv = c->gH * (2 * c->gdk + c->gdv);
-  norm(c, xr, w.attn_norm, c->xn, nullptr, tap_in, M);
-  zero(c, c->qkv, (size_t)M * c->gld * 4);
+  norm(c, xr, w.attn_norm, c->xn, nullptr, tap_in, M, RowMap(), true, c->qkv, c->gld);
   gemm_acc(c, p.gq, c->qkv, c->gld);
   gemm_acc(c, p.ga, c->qkv + nqkv, c->gld);
   gemm_acc(c, p.gb, c->qkv + nqkv + c->gH, c->gld);
@@ -477,8 +475,7 @@ void gdn_layer(dmtp_ctx* c, int l, float* xr, void* tap_in, bool snapshots) {
   const double st_bytes = (double)c->B * c->gH * c->gdv * c->gdk * 4 * (snapshots ? 9 : 2);
   launch(c, P_GDN, st_bytes, 0, [&] { op_gdn(c->dt, ga, c->st); });
   gemm_acc(c, p.go, xr, c->d);
-  norm(c, xr, w.mlp_norm, c->xn, nullptr, nullptr, M);
-  zero(c, c->gu, (size_t)M * 2 * c->F * 4);
+  norm(c, xr, w.mlp_norm, c->xn, nullptr, nullptr, M, RowMap(), true, c->gu, 2 * c->F);
   gemm_acc(c, p.gu, c->gu, 2 * c->F);
   launch(c, P_OTHER, 0, 0, [&] { op_swiglu(c->dt, c->gu, c->hmid, lo_of(c, c->mt8, c->F), M, c->F, c->st); });
   gemm_acc(c, p.down, xr, c->d);
@@ -508,9 +505,10 @@ void drafter_ctx(dmtp_ctx* c) {
   const int M = c->M;
   zero(c, c->cacc, (size_t)M * c->d * 4);
   gemm_acc(c, c->dfc, c->cacc, c->d);
-  norm(c, c->cacc, c->w.dft_norm_c, c->cn, nullptr, nullptr, M);
+  norm(c, c->cacc, c->w.dft_norm_c, c->cn, nullptr, nullptr, M, RowMap(), true, c->qkv,
+       2 * c->kvd);
   for (int j = 0; j < c->Ld; ++j) {
-    zero(c, c->qkv, (size_t)M * 2 * c->kvd * 4);
+    if (j > 0) zero(c, c->qkv, (size_t)M * 2 * c->kvd * 4);
     gemm_acc(c, c->dkv[j], c->qkv, 2 * c->kvd);
     launch(c, P_OTHER, 0, 0, [&] { op_rope_kv(c->dt, c->qkv, 2 * c->kvd, -1, 0, c->kvd, nullptr, nullptr, 0, c->dK[j], c->dV[j],
                c->rs.pos0, c->rope, M, c->hq, c->hkv, c->hd, c->maxc, c->err, c->st); });

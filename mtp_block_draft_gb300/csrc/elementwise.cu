@@ -18,12 +18,15 @@ __device__ __forceinline__ int map_row(int r, RowMap m) {
 
 // ---------------------------------------------------------------------------------
 // RMSNorm: y = x / sqrt(mean(x^2) + eps) * g
+// Optionally also: tap = x (operand copy), y32 = y (fp32), and zero[r][0..nz) = 0 (the
+// accumulator of the GEMM that consumes y, cleared in the same pass).
 // ---------------------------------------------------------------------------------
+// Generic form: any d and alignment, one CTA of 256 threads per row.
 template <typename T>
 __global__ void k_rmsnorm(const float* __restrict__ x, int ldx, const T* __restrict__ g,
                           T* __restrict__ y, int ldy, long y_lo, float* __restrict__ y32,
                           int ld32, T* __restrict__ tap, int ldtap, long tap_lo, int d,
-                          float eps, RowMap map) {
+                          float eps, RowMap map, float* __restrict__ zero, int ldz, int nz) {
   __shared__ float red[32];
   const int r = blockIdx.x;
   const float* xr = x + (long)map_row(r, map) * ldx;
@@ -33,6 +36,8 @@ __global__ void k_rmsnorm(const float* __restrict__ x, int ldx, const T* __restr
     ss += v * v;
     if (tap) store_act(tap + (long)r * ldtap + i, tap_lo, v);
   }
+  if (zero)
+    for (int i = threadIdx.x; i < nz; i += blockDim.x) zero[(long)r * ldz + i] = 0.f;
   ss = block_sum(ss, red);
   const float inv = rsqrtf(ss / (float)d + eps);
   for (int i = threadIdx.x; i < d; i += blockDim.x) {
@@ -42,16 +47,90 @@ __global__ void k_rmsnorm(const float* __restrict__ x, int ldx, const T* __restr
   }
 }
 
+// Vector form: the row stays in registers, NV float4 per thread, 128 threads per row;
+// 16-byte loads and 8/16-byte stores. Same arithmetic per element as the generic form.
+template <typename T, int NV>
+__global__ void __launch_bounds__(128)
+    k_rmsnorm_v(const float* __restrict__ x, int ldx, const T* __restrict__ g,
+                T* __restrict__ y, int ldy, long y_lo, float* __restrict__ y32, int ld32,
+                T* __restrict__ tap, int ldtap, long tap_lo, int d, float eps, RowMap map,
+                float* __restrict__ zero, int ldz, int nz) {
+  __shared__ float red[32];
+  const int r = blockIdx.x, d4 = d >> 2;
+  const float* xr = x + (long)map_row(r, map) * ldx;
+  float4 v[NV];
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int i = threadIdx.x + k * 128;
+    v[k] = i < d4 ? load4(xr + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+  }
+  if (tap) {
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int i = threadIdx.x + k * 128;
+      if (i < d4) store_act4(tap + (long)r * ldtap + 4 * i, tap_lo, v[k]);
+    }
+  }
+  if (zero)
+    for (int i = threadIdx.x; i < (nz >> 2); i += 128)
+      *reinterpret_cast<float4*>(zero + (long)r * ldz + 4 * i) = make_float4(0.f, 0.f, 0.f, 0.f);
+  ss = block_sum(ss, red);
+  const float inv = rsqrtf(ss / (float)d + eps);
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int i = threadIdx.x + k * 128;
+    if (i < d4) {
+      const float4 gg = load4(g + 4 * i);
+      const float4 o = make_float4(v[k].x * inv * gg.x, v[k].y * inv * gg.y,
+                                   v[k].z * inv * gg.z, v[k].w * inv * gg.w);
+      if (y) store_act4(y + (long)r * ldy + 4 * i, y_lo, o);
+      if (y32) *reinterpret_cast<float4*>(y32 + (long)r * ld32 + 4 * i) = o;
+    }
+  }
+}
+
+template <typename T>
+static void rmsnorm_t(const float* x, int ldx, const T* g, T* y, int ldy, long y_lo, float* y32,
+                      int ld32, T* tap, int ldtap, long tap_lo, int rows, int d, float eps,
+                      RowMap map, float* zero, int ldz, int nz, cudaStream_t st) {
+  const unsigned ea = sizeof(T) * 4;  // bytes of four operand elements
+  const bool vec = d % 4 == 0 && d <= 4096 && aligned_to(x, 16) && ldx % 4 == 0 &&
+                   aligned_to(g, ea) && (!y || (aligned_to(y, ea) && ldy % 4 == 0 && y_lo % 4 == 0)) &&
+                   (!y32 || (aligned_to(y32, 16) && ld32 % 4 == 0)) &&
+                   (!tap || (aligned_to(tap, ea) && ldtap % 4 == 0 && tap_lo % 4 == 0)) &&
+                   (!zero || (aligned_to(zero, 16) && ldz % 4 == 0 && nz % 4 == 0));
+  if (!vec) {
+    k_rmsnorm<T><<<rows, 256, 0, st>>>(x, ldx, g, y, ldy, y_lo, y32, ld32, tap, ldtap, tap_lo, d,
+                                       eps, map, zero, ldz, nz);
+    return;
+  }
+  const int nv = (d / 4 + 127) / 128;
+#define DMTP_RMS_V(NV)                                                                        \
+  k_rmsnorm_v<T, NV><<<rows, 128, 0, st>>>(x, ldx, g, y, ldy, y_lo, y32, ld32, tap, ldtap,    \
+                                           tap_lo, d, eps, map, zero, ldz, nz)
+  if (nv <= 1)
+    DMTP_RMS_V(1);
+  else if (nv <= 2)
+    DMTP_RMS_V(2);
+  else if (nv <= 4)
+    DMTP_RMS_V(4);
+  else
+    DMTP_RMS_V(8);
+#undef DMTP_RMS_V
+}
+
 void op_rmsnorm(int dt, const float* x, int ldx, const void* g, void* y, int ldy, long y_lo,
                 float* y32, int ld32, void* tap, int ldtap, long tap_lo, int rows, int d,
-                float eps, RowMap map, cudaStream_t st) {
+                float eps, RowMap map, cudaStream_t st, float* zero, int ldz, int nz) {
   if (rows <= 0) return;
   if (dt)
-    k_rmsnorm<bf16><<<rows, 256, 0, st>>>(x, ldx, (const bf16*)g, (bf16*)y, ldy, y_lo, y32, ld32,
-                                          (bf16*)tap, ldtap, tap_lo, d, eps, map);
+    rmsnorm_t<bf16>(x, ldx, (const bf16*)g, (bf16*)y, ldy, y_lo, y32, ld32, (bf16*)tap, ldtap,
+                    tap_lo, rows, d, eps, map, zero, ldz, nz, st);
   else
-    k_rmsnorm<float><<<rows, 256, 0, st>>>(x, ldx, (const float*)g, (float*)y, ldy, y_lo, y32,
-                                           ld32, (float*)tap, ldtap, tap_lo, d, eps, map);
+    rmsnorm_t<float>(x, ldx, (const float*)g, (float*)y, ldy, y_lo, y32, ld32, (float*)tap,
+                     ldtap, tap_lo, rows, d, eps, map, zero, ldz, nz, st);
 }
 
 // ---------------------------------------------------------------------------------
@@ -160,7 +239,7 @@ void op_build_slots(int dt, const void* E, int vocab, const int* A, const int* d
 }
 
 // ---------------------------------------------------------------------------------
-// SwiGLU
+// SwiGLU: h = silu(g) * u, from the [g | u] rows of the gate/up GEMM.
 // ---------------------------------------------------------------------------------
 template <typename T>
 __global__ void k_swiglu(const float* __restrict__ gu, T* __restrict__ h, long h_lo, int F) {
@@ -170,8 +249,30 @@ __global__ void k_swiglu(const float* __restrict__ gu, T* __restrict__ h, long h
   const float gv = gu[(long)m * 2 * F + i], uv = gu[(long)m * 2 * F + F + i];
   store_act(h + (long)m * F + i, h_lo, gv / (1.f + __expf(-gv)) * uv);
 }
+// four elements per thread (F % 4 == 0, aligned rows)
+template <typename T>
+__global__ void k_swiglu4(const float* __restrict__ gu, T* __restrict__ h, long h_lo, int F) {
+  const int m = blockIdx.y;
+  const int i = 4 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (i >= F) return;
+  const float4 gv = load4(gu + (long)m * 2 * F + i), uv = load4(gu + (long)m * 2 * F + F + i);
+  const float4 o = make_float4(gv.x / (1.f + __expf(-gv.x)) * uv.x,
+                               gv.y / (1.f + __expf(-gv.y)) * uv.y,
+                               gv.z / (1.f + __expf(-gv.z)) * uv.z,
+                               gv.w / (1.f + __expf(-gv.w)) * uv.w);
+  store_act4(h + (long)m * F + i, h_lo, o);
+}
 
 void op_swiglu(int dt, const float* gu, void* h, long h_lo, int rows, int F, cudaStream_t st) {
+  const unsigned ea = dt ? 8 : 16;
+  if (F % 4 == 0 && aligned_to(gu, 16) && aligned_to(h, ea) && h_lo % 4 == 0) {
+    dim3 grid(cdiv(F / 4, 128), rows);
+    if (dt)
+      k_swiglu4<bf16><<<grid, 128, 0, st>>>(gu, (bf16*)h, h_lo, F);
+    else
+      k_swiglu4<float><<<grid, 128, 0, st>>>(gu, (float*)h, h_lo, F);
+    return;
+  }
   dim3 grid(cdiv(F, 256), rows);
   if (dt)
     k_swiglu<bf16><<<grid, 256, 0, st>>>(gu, (bf16*)h, h_lo, F);
@@ -248,9 +349,89 @@ __global__ void k_rope_kv(const float* __restrict__ src, int ld, int q_off, int 
   }
 }
 
+// Vector form (rows = 8 per sequence, hd % 8 == 0, aligned rows): CTAs 0..rows-1 rotate
+// q and K of one row, four pairs per thread, 16-byte loads and 8/16-byte stores; CTAs
+// rows.. write the transposed V of one (sequence, kv head) for the sequence's 8 rows,
+// thread (dim, row) with the row fastest, so that the 8 new positions of a dimension
+// are one contiguous run.
+template <typename T>
+__global__ void __launch_bounds__(256)
+    k_rope_kv4(const float* __restrict__ src, int ld, int q_off, int k_off, int v_off,
+               float* __restrict__ q_out, bf16* __restrict__ q_split, long q_lo,
+               T* __restrict__ Kc, T* __restrict__ Vc, const int* __restrict__ base,
+               const float2* __restrict__ tab, int rows, int hq, int hkv, int hd, int max_ctx,
+               unsigned* err) {
+  const int half = hd / 2, nquad = half / 4;
+  if ((int)blockIdx.x < rows) {
+    const int m = blockIdx.x, b = m >> 3, s = m & 7;
+    const int pos = base[b] + s;
+    const bool pos_ok = pos >= 0 && pos < max_ctx;
+    if (!pos_ok && threadIdx.x == 0) set_err(err, DMTP_ERR_POS);
+    const float2* tr = tab + (long)(pos_ok ? pos : 0) * half;
+    const float* row = src + (long)m * ld;
+    const int nq = q_off >= 0 ? hq * nquad : 0;
+    const int nk = pos_ok ? hkv * nquad : 0;
+    for (int idx = threadIdx.x; idx < nq + nk; idx += blockDim.x) {
+      const bool isq = idx < nq;
+      const int j = isq ? idx : idx - nq;
+      const int h = j / nquad, i = 4 * (j % nquad);
+      const float* xs = row + (isq ? q_off : k_off) + h * hd;
+      const float4 x1 = load4(xs + i), x2 = load4(xs + half + i);
+      const float4 c01 = *reinterpret_cast<const float4*>(tr + i);  // (cos, sin) of i, i+1
+      const float4 c23 = *reinterpret_cast<const float4*>(tr + i + 2);
+      const float4 r1 = make_float4(x1.x * c01.x - x2.x * c01.y, x1.y * c01.z - x2.y * c01.w,
+                                    x1.z * c23.x - x2.z * c23.y, x1.w * c23.z - x2.w * c23.w);
+      const float4 r2 = make_float4(x2.x * c01.x + x1.x * c01.y, x2.y * c01.z + x1.y * c01.w,
+                                    x2.z * c23.x + x1.z * c23.y, x2.w * c23.z + x1.w * c23.w);
+      if (isq) {
+        const long qi = ((long)m * hq + h) * hd;
+        if (q_split) {
+          store_act4(q_split + qi + i, q_lo, r1);
+          store_act4(q_split + qi + half + i, q_lo, r2);
+        } else {
+          store_act4(q_out + qi + i, 0, r1);
+          store_act4(q_out + qi + half + i, 0, r2);
+        }
+      } else {
+        T* kc = Kc + (((long)b * hkv + h) * max_ctx + pos) * hd;
+        store_act4(kc + i, 0, r1);
+        store_act4(kc + half + i, 0, r2);
+      }
+    }
+  } else {
+    const int b = (blockIdx.x - rows) / hkv, h = (blockIdx.x - rows) % hkv;
+    const int p0 = base[b];
+    for (int idx = threadIdx.x; idx < hd * 8; idx += blockDim.x) {
+      const int s = idx & 7, i = idx >> 3;
+      const int pos = p0 + s;
+      if (pos < 0 || pos >= max_ctx) continue;  // reported by the row CTAs
+      const float v = src[(long)(b * 8 + s) * ld + v_off + h * hd + i];
+      Vc[(((long)b * hkv + h) * (max_ctx / 64) + pos / 64) * hd * 64 + (long)i * 64 + pos % 64] =
+          from_f32<T>(v);
+    }
+  }
+}
+
 void op_rope_kv(int dt, const float* src, int ld, int q_off, int k_off, int v_off, float* q_out,
                 void* q_split, long q_lo, void* Kc, void* Vc, const int* base, const float2* tab,
                 int rows, int hq, int hkv, int hd, int max_ctx, unsigned* err, cudaStream_t st) {
+  const unsigned ek = dt ? 8 : 16;
+  const bool vec = rows % 8 == 0 && hd % 8 == 0 && ld % 4 == 0 && aligned_to(src, 16) &&
+                   aligned_to(tab, 16) && k_off % 4 == 0 && aligned_to(Kc, ek) &&
+                   (q_off < 0 || (q_off % 4 == 0 &&
+                                  (q_split ? aligned_to(q_split, 8) && q_lo % 4 == 0
+                                           : aligned_to(q_out, 16))));
+  if (vec) {
+    if (dt)
+      k_rope_kv4<bf16><<<rows + rows / 8 * hkv, 256, 0, st>>>(
+          src, ld, q_off, k_off, v_off, q_out, (bf16*)q_split, q_lo, (bf16*)Kc, (bf16*)Vc, base,
+          tab, rows, hq, hkv, hd, max_ctx, err);
+    else
+      k_rope_kv4<float><<<rows + rows / 8 * hkv, 256, 0, st>>>(
+          src, ld, q_off, k_off, v_off, q_out, nullptr, 0, (float*)Kc, (float*)Vc, base, tab,
+          rows, hq, hkv, hd, max_ctx, err);
+    return;
+  }
   if (dt)
     k_rope_kv<bf16><<<rows, 256, 0, st>>>(src, ld, q_off, k_off, v_off, q_out, (bf16*)q_split,
                                           q_lo, (bf16*)Kc, (bf16*)Vc, base, tab, hq, hkv, hd,

@@ -20,9 +20,11 @@ struct RowMap {
 // y[r] = RMSNorm(x[map(r)]) * g, stored as dt (y) and optionally as fp32 (y32);
 // tap (optional, dt): raw copy of x[map(r)] into column block of a tap buffer.
 // *_lo arguments: element offset of the bf16 remainder half of a split operand (0: none).
+// zero (optional): rows [rows][ldz] of which the first nz floats are set to 0.
 void op_rmsnorm(int dt, const float* x, int ldx, const void* g, void* y, int ldy, long y_lo,
                 float* y32, int ld32, void* tap, int ldtap, long tap_lo, int rows, int d,
-                float eps, RowMap map, cudaStream_t st);
+                float eps, RowMap map, cudaStream_t st, float* zero = nullptr, int ldz = 0,
+                int nz = 0);
 // x[m] = E[tok[m]] (fp32 rows)
 void op_embed(int dt, const void* E, const int* tok, int vocab, float* x, int rows, int d,
               unsigned* err, cudaStream_t st);
