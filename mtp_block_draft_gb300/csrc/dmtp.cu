@@ -8,6 +8,7 @@
 // (positions, accepted lengths, snapshot slots) stays on the device; the host never
 // reads a length during normal rounds.
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <algorithm>
@@ -26,6 +27,7 @@ struct Gemm {
   const void* X = nullptr;
   int N = 0, K = 0, M = 0;
   bool argmax = false;
+  bool split = true;    // X is the [hi; lo] bf16 pair
 };
 
 struct LayerPlans {
@@ -287,6 +289,7 @@ int plan(dmtp_ctx* c, Gemm& g, const void* W, int N, int K, const void* X, int M
   g.K = K;
   g.M = M;
   g.argmax = argmax;
+  g.split = split;
   if (!W) return DMTP_EINVAL;
   if (c->dt == 1)
     return tc_plan(&g.tc, W, N, K, X, M, c->nsm, argmax, split) ? DMTP_EINVAL : DMTP_OK;
@@ -597,6 +600,123 @@ int check_err(dmtp_ctx* c) {
 
 // ---------------------------------------------------------------------------------
 // C ABI
+// ---- GEMM tile selection by measurement ----
+// Every distinct GEMM shape (N, K, M, operand, epilogue) is timed on the device with
+// each tile shape (128 or 256 weight rows per CTA, one or two token halves, K splits
+// around the wave-count choice), cold: the L2 is flushed by a 256 MB read before each
+// run, as in the round, where each weight matrix is streamed once. The fastest shape
+// serves every GEMM of that shape. Outputs go to scratch (the gate/up accumulator and
+// the argmax keys), which the round clears before use.
+namespace {
+struct TuneKey {
+  int N, K, M;
+  bool split, argmax;
+  bool operator==(const TuneKey& o) const {
+    return N == o.N && K == o.K && M == o.M && split == o.split && argmax == o.argmax;
+  }
+};
+struct TuneChoice {
+  int wide, msplit, splits;
+};
+
+void collect(LayerPlans& p, std::vector<Gemm*>& v) {
+  for (Gemm* g : {&p.qkv, &p.o, &p.gu, &p.down, &p.gq, &p.ga, &p.gb, &p.go}) v.push_back(g);
+}
+
+float time_plan(dmtp_ctx* c, const TcPlan& p, bool argmax, const void* flush,
+                size_t flush_bytes, cudaEvent_t e0, cudaEvent_t e1) {
+  float best = 1e30f;
+  for (int rep = 0; rep < 3; ++rep) {
+    op_l2_flush(flush, flush_bytes, c->err, c->st);
+    cudaEventRecord(e0, c->st);
+    if (argmax)
+      op_gemm_tc_argmax(p, c->rs.keys, nullptr, 0, c->err, c->st);
+    else
+      op_gemm_tc_acc(p, c->gu, p.N, c->err, c->st);
+    cudaEventRecord(e1, c->st);
+    float ms = 1e30f;
+    if (cudaEventSynchronize(e1) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess)
+      return 1e30f;
+    best = std::min(best, ms);
+  }
+  return best;
+}
+
+int autotune(dmtp_ctx* c, const void* flush, size_t flush_bytes) {
+  if (c->dt != 1) return DMTP_OK;
+  std::vector<Gemm*> all;
+  for (int l = 0; l < c->L; ++l) collect(c->tgt[l], all);
+  for (int j = 0; j < c->Ld; ++j) {
+    collect(c->dft[j], all);
+    all.push_back(&c->dkv[j]);
+  }
+  collect(c->mtp, all);
+  for (Gemm* g : {&c->fuse, &c->head_t1, &c->head_d, &c->head_v, &c->dfc, &c->mproj})
+    all.push_back(g);
+  const size_t scratch = (size_t)c->M * 2 * c->F;  // floats of the gate/up accumulator
+  cudaEvent_t e0, e1;
+  if (cudaEventCreate(&e0) != cudaSuccess) return DMTP_ECUDA;
+  if (cudaEventCreate(&e1) != cudaSuccess) {
+    cudaEventDestroy(e0);
+    return DMTP_ECUDA;
+  }
+  const bool verbose = getenv("DMTP_VERBOSE") != nullptr;
+  std::vector<std::pair<TuneKey, TuneChoice>> cache;
+  int rc = DMTP_OK;
+  for (Gemm* g : all) {
+    if (!g->W) continue;
+    if (!g->argmax && (size_t)g->M * g->N > scratch) continue;  // keeps the default shape
+    const TuneKey key{g->N, g->K, g->M, g->split, g->argmax};
+    const TuneChoice* hit = nullptr;
+    for (auto& e : cache)
+      if (e.first == key) hit = &e.second;
+    if (hit) {
+      if (tc_plan_shape(&g->tc, g->W, g->N, g->K, g->X, g->M, c->nsm, g->argmax, g->split,
+                        hit->wide, hit->msplit, hit->splits))
+        rc = DMTP_EINVAL;
+      continue;
+    }
+    TuneChoice best{g->tc.wide, g->tc.msplit, g->tc.splits};
+    float best_ms = time_plan(c, g->tc, g->argmax, flush, flush_bytes, e0, e1);
+    for (int wide = 1; wide <= 2; ++wide)
+      for (int ms = 1; ms <= 2; ++ms) {
+        TcPlan p0;
+        if (tc_plan_shape(&p0, g->W, g->N, g->K, g->X, g->M, c->nsm, g->argmax, g->split, wide,
+                          ms, 0))
+          continue;
+        const int cand[3] = {p0.splits, std::max(1, p0.splits / 2),
+                             std::min(32, 2 * p0.splits)};
+        const int ncand = g->argmax ? 1 : 3;
+        for (int i = 0; i < ncand; ++i) {
+          if (i > 0 && (cand[i] == cand[0] || (i == 2 && cand[2] == cand[1]))) continue;
+          TcPlan p;
+          if (tc_plan_shape(&p, g->W, g->N, g->K, g->X, g->M, c->nsm, g->argmax, g->split,
+                            wide, ms, cand[i]))
+            continue;
+          const float t = time_plan(c, p, g->argmax, flush, flush_bytes, e0, e1);
+          if (t < best_ms) {
+            best_ms = t;
+            best = TuneChoice{wide, ms, p.splits};
+          }
+        }
+      }
+    if (tc_plan_shape(&g->tc, g->W, g->N, g->K, g->X, g->M, c->nsm, g->argmax, g->split,
+                      best.wide, best.msplit, best.splits))
+      rc = DMTP_EINVAL;
+    cache.push_back({key, best});
+    if (verbose)
+      fprintf(stderr, "dmtp: gemm N=%d K=%d M=%d%s%s: %d x 128 weight rows, %d token part(s), "
+              "%d K split(s), %.1f us\n", g->N, g->K, g->M, g->split ? " split" : "",
+              g->argmax ? " argmax" : "", best.wide, best.msplit, best.splits, best_ms * 1e3f);
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (cudaStreamSynchronize(c->st) != cudaSuccess) return DMTP_ECUDA;
+  return rc;
+}
+}  // namespace
+
 // ---------------------------------------------------------------------------------
 extern "C" {
 
@@ -710,6 +830,13 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
   RoundState& s = c->rs;
   // padding rows of the GEMM operands are read (and ignored): start from zeros
   zero(c, workspace, need);
+  {
+    const int r = autotune(c, workspace, std::min(need, (size_t)256 << 20));
+    if (r) {
+      delete c;
+      return r;
+    }
+  }
   zero(c, c->err, 4);
   zero(c, s.hist, 64);
   zero(c, s.keys, (size_t)B * 16 * 8);

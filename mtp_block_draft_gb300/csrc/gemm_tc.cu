@@ -39,14 +39,18 @@
 
 namespace dmtp {
 
-static constexpr int kTileN = 128;   // weight rows per CTA (MMA M)
+static constexpr int kHalfN = 128;  // weight rows per MMA (M) and per accumulator
 static constexpr int kBlockK = 64;   // k elements per stage (128 B of bf16)
-static constexpr uint32_t kWBytes = kTileN * kBlockK * 2;
+static constexpr uint32_t kHalfBytes = kHalfN * kBlockK * 2;  // one 128-row weight k slice
 
 struct TcArgs {
   int N, K, M, MT, stages;
+  int wide;        // weight halves of 128 rows per CTA (1 or 2), one accumulator each
+  int mct;         // token rows per CTA (MT, or MT / 2 with two token halves)
   int split;       // 1: X holds [hi; lo] halves of MT rows each
-  int xbox, nx;    // X rows per TMA load / MMA, loads per stage
+  int xbox, nx;    // X rows per TMA load, loads per stage
+  int merged;      // split with hi and lo adjacent in shared memory: one MMA of 2*mct columns
+  int acc_cols;    // TMEM columns per accumulator
   float* out;
   int ldo;
   unsigned long long* keys;
@@ -55,13 +59,39 @@ struct TcArgs {
   unsigned* err;
 };
 
-__host__ __device__ inline uint32_t tmem_cols_for(int MT) {
+// Column of a 16-column block that lane `lane` holds after warp_colmax16.
+__device__ __forceinline__ int col16(int lane) {
+  return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+}
+// k[0..15]: this lane's keys of 16 columns. On return k[0] is the maximum over the 32
+// lanes of column col16(lane). Each step exchanges the half of the columns the partner
+// keeps: 8 + 4 + 2 + 1 + 1 shuffles instead of 5 per column.
+__device__ __forceinline__ void warp_colmax16(unsigned long long (&k)[16], int lane) {
+#pragma unroll
+  for (int half = 8, off = 16; half >= 1; half >>= 1, off >>= 1) {
+    const bool upper = (lane & off) != 0;  // keeps columns half..2*half-1 of the block
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const unsigned long long keep = upper ? k[half + i] : k[i];
+      const unsigned long long give = upper ? k[i] : k[half + i];
+      const unsigned long long got = __shfl_xor_sync(0xffffffffu, give, off);
+      k[i] = got > keep ? got : keep;
+    }
+  }
+  const unsigned long long got = __shfl_xor_sync(0xffffffffu, k[0], 1);
+  k[0] = got > k[0] ? got : k[0];
+}
+
+__host__ __device__ inline uint32_t tmem_cols_for(int cols) {
   uint32_t c = 32;
-  while (c < (uint32_t)MT) c <<= 1;
+  while (c < (uint32_t)cols) c <<= 1;
   return c;
 }
 
-template <int EPI>  // 0: atomic add into out, 1: argmax keys (+ logits)
+// EPI 0: atomic add into out, 1: argmax keys (+ logits). WIDE, NMMA (MMAs per k step
+// and weight half) and MERGED are compile-time copies of a.wide, (merged ? 1 : nx) and
+// a.merged, so that the issue loop and the epilogue have no runtime trip counts.
+template <int EPI, int WIDE, int NMMA, bool MERGED>
 __global__ void __launch_bounds__(128, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
               TcArgs a) {
@@ -69,24 +99,25 @@ __global__ void __launch_bounds__(128, 1)
   uint8_t* smem =
       smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);  // 1024-B aligned tiles
   const int S = a.stages;
+  const uint32_t wbytes = (uint32_t)WIDE * kHalfBytes;
   const uint32_t xbytes = (uint32_t)a.xbox * a.nx * kBlockK * 2;
   uint8_t* sW = smem;
-  uint8_t* sX = smem + S * kWBytes;
+  uint8_t* sX = smem + S * wbytes;
   uint64_t* full = (uint64_t*)(sX + S * xbytes);
   uint64_t* empty = full + S;
   uint64_t* accum = empty + S;
   uint32_t* tmem_slot = (uint32_t*)(accum + 1);
-  unsigned long long* red = (unsigned long long*)(accum + 2);  // [4][MT] (argmax)
+  unsigned long long* red = (unsigned long long*)(accum + 2);  // [4][mct] (argmax)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * kTileN;
+  // grid: (token halves, weight tiles, K splits); CTAs sharing a weight tile are
+  // adjacent in launch order, so its second read comes from L2
+  const int mrow0 = blockIdx.x * a.mct;
+  const int n0 = blockIdx.y * kHalfN * WIDE;
   const int nkb = a.K / kBlockK;
-  const int kb0 = (int)((long)blockIdx.y * nkb / gridDim.y);
-  const int kb1 = (int)((long)(blockIdx.y + 1) * nkb / gridDim.y);
-  // one accumulator of xbox columns; with two loads per stage (nx = 2: the hi and lo
-  // halves of more than 128 token rows) both products accumulate into it
-  const uint32_t ncols = tmem_cols_for(a.xbox);
-  const bool lo_cols = a.split && a.nx == 1;  // hi and lo in one load: lo in columns MT..
+  const int kb0 = (int)((long)blockIdx.z * nkb / gridDim.z);
+  const int kb1 = (int)((long)(blockIdx.z + 1) * nkb / gridDim.z);
+  const uint32_t ncols = tmem_cols_for(WIDE * a.acc_cols);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
@@ -112,33 +143,42 @@ __global__ void __launch_bounds__(128, 1)
       const int s = issued % S;
       const uint32_t ph = (issued / S) & 1;
       if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, a.err)) break;
-      mbar_expect_tx(smem_u32(&full[s]), kWBytes + xbytes);
-      tma_load_2d(smem_u32(sW + s * kWBytes), &tmW, kb * kBlockK, n0, smem_u32(&full[s]), pw);
+      mbar_expect_tx(smem_u32(&full[s]), wbytes + xbytes);
+      tma_load_2d(smem_u32(sW + s * wbytes), &tmW, kb * kBlockK, n0, smem_u32(&full[s]), pw);
+      // one box of [hi; lo] rows, or hi rows then (split) remainder rows
       for (int j = 0; j < a.nx; ++j)
         tma_load_2d(smem_u32(sX + s * xbytes + j * a.xbox * kBlockK * 2), &tmX, kb * kBlockK,
-                    j * a.xbox, smem_u32(&full[s]), px);
+                    j * a.MT + mrow0, smem_u32(&full[s]), px);
     }
     // drain: every stage's last issued load has landed before the CTA may exit
     for (int j = (issued > S ? issued - S : 0); j < issued; ++j)
       mbar_wait(smem_u32(&full[j % S]), (j / S) & 1, a.err);
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
-    const uint32_t idesc = umma_idesc_bf16(kTileN, a.xbox);
+    // merged: N = 2*mct over [hi; lo] (lo accumulates in columns mct..); otherwise the
+    // nx token loads each get an MMA of N = mct into the same accumulator columns
+    const uint32_t idesc = umma_idesc_bf16(kHalfN, MERGED ? 2 * a.mct : a.mct);
     int it = 0;
     for (int kb = kb0; kb < kb1; ++kb, ++it) {
       const int s = it % S;
       const uint32_t ph = (it / S) & 1;
       if (!mbar_wait(smem_u32(&full[s]), ph, a.err)) break;
       tc_fence_after();
-      const uint64_t dw = umma_desc_sw128(smem_u32(sW + s * kWBytes));
+      uint64_t dw[WIDE], dx[NMMA];
 #pragma unroll
-      for (int k = 0; k < kBlockK / 16; ++k) {  // +32 B per K=16 step inside the swizzle atom
-        for (int j = 0; j < a.nx; ++j) {
-          const uint64_t dx =
-              umma_desc_sw128(smem_u32(sX + s * xbytes + j * a.xbox * kBlockK * 2));
-          umma_bf16(tmem, dw + 2 * k, dx + 2 * k, idesc, (kb > kb0 || k > 0 || j > 0) ? 1u : 0u);
-        }
-      }
+      for (int h = 0; h < WIDE; ++h)
+        dw[h] = umma_desc_sw128(smem_u32(sW + s * wbytes + h * kHalfBytes));
+#pragma unroll
+      for (int j = 0; j < NMMA; ++j)
+        dx[j] = umma_desc_sw128(smem_u32(sX + s * xbytes + j * a.mct * kBlockK * 2));
+#pragma unroll
+      for (int k = 0; k < kBlockK / 16; ++k)  // +32 B per K=16 step inside the swizzle atom
+#pragma unroll
+        for (int h = 0; h < WIDE; ++h)
+#pragma unroll
+          for (int j = 0; j < NMMA; ++j)
+            umma_bf16(tmem + h * a.acc_cols, dw[h] + 2 * k, dx[j] + 2 * k, idesc,
+                      (kb > kb0 || k > 0 || j > 0) ? 1u : 0u);
       umma_commit(smem_u32(&empty[s]));
     }
     umma_commit(smem_u32(accum));  // always: the epilogue waits on it
@@ -149,25 +189,27 @@ __global__ void __launch_bounds__(128, 1)
   bool ok = mbar_wait(smem_u32(accum), 0, a.err);
   ok = __all_sync(0xffffffffu, ok);
   tc_fence_after();
-  const int row = warp * 32 + lane;
-  const int n = n0 + row;
-  const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16);
   if (EPI == 0) {
     if (ok) {
-      for (int c = 0; c < a.MT; c += 16) {
-        float v[16];
-        tmem_ld16(tbase + c, v);
-        if (lo_cols) {
-          float w[16];
-          tmem_ld16(tbase + a.MT + c, w);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] += w[j];
-        }
-        if (n < a.N) {
+      for (int h = 0; h < WIDE; ++h) {
+        const int n = n0 + h * kHalfN + warp * 32 + lane;
+        const uint32_t tbase = tmem + h * a.acc_cols + ((uint32_t)(warp * 32) << 16);
+        for (int c = 0; c < a.mct; c += 16) {
+          float v[16];
+          tmem_ld16(tbase + c, v);
+          if (MERGED) {
+            float w[16];
+            tmem_ld16(tbase + a.mct + c, w);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int m = c + j;
-            if (m < a.M) atomicAdd(&a.out[(long)m * a.ldo + n], v[j]);
+            for (int j = 0; j < 16; ++j) v[j] += w[j];
+          }
+          if (n < a.N) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int m = mrow0 + c + j;
+              if (m < a.M) atomicAdd(&a.out[(long)m * a.ldo + n], v[j]);
+            }
           }
         }
       }
@@ -175,33 +217,43 @@ __global__ void __launch_bounds__(128, 1)
   } else {
     const bool okb = __syncthreads_and(ok);
     if (okb) {
-      for (int c = 0; c < a.MT; c += 16) {
-        float v[16];
-        tmem_ld16(tbase + c, v);
-        if (lo_cols) {
-          float w[16];
-          tmem_ld16(tbase + a.MT + c, w);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] += w[j];
-        }
+      for (int h = 0; h < WIDE; ++h) {
+        const int n = n0 + h * kHalfN + warp * 32 + lane;
+        const uint32_t tbase = tmem + h * a.acc_cols + ((uint32_t)(warp * 32) << 16);
+        for (int c = 0; c < a.mct; c += 16) {
+          float v[16];
+          tmem_ld16(tbase + c, v);
+          if (MERGED) {
+            float w[16];
+            tmem_ld16(tbase + a.mct + c, w);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int m = c + j;
-          unsigned long long key = (n < a.N) ? argmax_key(v[j], n) : 0ull;
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
-            key = other > key ? other : key;
+            for (int j = 0; j < 16; ++j) v[j] += w[j];
           }
-          if (lane == 0) red[warp * a.MT + m] = key;
-          if (a.logits && n < a.N && m < a.M) a.logits[(long)m * a.ldl + n] = v[j];
+          if (a.logits && n < a.N) {  // debug copy of the scores
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (mrow0 + c + j < a.M) a.logits[(long)(mrow0 + c + j) * a.ldl + n] = v[j];
+          }
+          // column maxima over the warp's 32 rows: a butterfly that halves the columns
+          // each lane keeps at every step (16 -> 8 -> 4 -> 2 -> 1), then pairs agree
+          unsigned long long key[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) key[j] = (n < a.N) ? argmax_key(v[j], n) : 0ull;
+          warp_colmax16(key, lane);
+          // lane holds column col16(lane) (lanes 2i and 2i+1 the same one)
+          if ((lane & 1) == 0) {
+            const int ml = c + col16(lane);
+            unsigned long long* r = &red[warp * a.mct + ml];
+            *r = (h == 0 || key[0] > *r) ? key[0] : *r;
+          }
         }
       }
       __syncthreads();
-      for (int m = threadIdx.x; m < a.M; m += blockDim.x) {
-        unsigned long long k = red[m];
-        for (int w = 1; w < 4; ++w) k = red[w * a.MT + m] > k ? red[w * a.MT + m] : k;
-        atomicMax(&a.keys[m], k);
+      for (int ml = threadIdx.x; ml < a.mct && mrow0 + ml < a.M; ml += blockDim.x) {
+        unsigned long long k = red[ml];
+        for (int w = 1; w < 4; ++w) k = red[w * a.mct + ml] > k ? red[w * a.mct + ml] : k;
+        atomicMax(&a.keys[mrow0 + ml], k);
       }
     }
   }
@@ -266,10 +318,10 @@ int tc_make_tmap3(CUtensorMap* tm, const void* base, uint64_t d0, uint64_t d1, u
   return r == CUDA_SUCCESS ? 0 : -3;
 }
 
-static size_t smem_bytes(int MT, int xrows, int stages, bool argmax) {
-  size_t b = 1024 + (size_t)stages * (kWBytes + (size_t)xrows * kBlockK * 2);
+static size_t smem_bytes(int wide, int mct, int xrows, int stages, bool argmax) {
+  size_t b = 1024 + (size_t)stages * (wide * kHalfBytes + (size_t)xrows * kBlockK * 2);
   b += (2 * stages + 2) * 8;
-  if (argmax) b += 4 * (size_t)MT * 8;
+  if (argmax) b += 4 * (size_t)mct * 8;
   return b;
 }
 
@@ -277,25 +329,40 @@ static constexpr size_t kSmemBudget = 200 * 1024;
 
 int tc_mt(int M) { return std::max(16, (M + 15) / 16 * 16); }
 
-int tc_plan(TcPlan* p, const void* W, int N, int K, const void* X, int M, int nsm, bool argmax,
-            bool split) {
-  if (M < 1 || M > 256 || K % kBlockK || N < 1) return -10;
+int tc_plan_shape(TcPlan* p, const void* W, int N, int K, const void* X, int M, int nsm,
+                  bool argmax, bool split, int wide, int msplit, int splits) {
+  if (M < 1 || M > 256 || K % kBlockK || N < 1 || (wide != 1 && wide != 2) ||
+      (msplit != 1 && msplit != 2))
+    return -10;
   p->N = N;
   p->K = K;
   p->M = M;
   p->MT = tc_mt(M);
   p->split = split ? 1 : 0;
-  const int xrows = split ? 2 * p->MT : p->MT;
-  p->xbox = xrows <= 256 ? xrows : p->MT;
-  p->nx = xrows / p->xbox;
+  p->wide = wide;
+  p->msplit = msplit;
+  if (p->MT % (16 * msplit)) return -10;
+  p->mct = p->MT / msplit;
+  if (split && msplit == 1 && 2 * p->MT <= 256) {  // [hi; lo] rows adjacent: one load
+    p->xbox = 2 * p->MT;
+    p->nx = 1;
+  } else {
+    p->xbox = p->mct;
+    p->nx = split ? 2 : 1;
+  }
+  p->merged = split && 2 * p->mct <= 256;
+  p->acc_cols = p->merged ? 2 * p->mct : p->mct;
+  if (wide * p->acc_cols > 512) return -10;
+  const int xrows = p->xbox * p->nx;
   int st = 8;
-  while (st > 2 && smem_bytes(p->MT, xrows, st, argmax) > kSmemBudget) --st;
+  while (st > 2 && smem_bytes(wide, p->mct, xrows, st, argmax) > kSmemBudget) --st;
   p->stages = st;
-  p->smem = smem_bytes(p->MT, xrows, st, argmax);
-  const int tiles = (N + kTileN - 1) / kTileN;
+  p->smem = smem_bytes(wide, p->mct, xrows, st, argmax);
+  if (p->smem > kSmemBudget) return -10;
+  const int tiles = (N + kHalfN * wide - 1) / (kHalfN * wide) * msplit;
   const int nkb = K / kBlockK;
-  int best = 1;
-  if (!argmax) {
+  int best = splits > 0 ? std::min(splits, nkb) : 1;
+  if (!argmax && splits <= 0) {
     // minimise waves(tiles * s) * (k blocks per CTA + fixed cost of ~3 k blocks)
     double best_cost = 1e30;
     for (int s = 1; s <= std::min(nkb, 32); ++s) {
@@ -307,35 +374,60 @@ int tc_plan(TcPlan* p, const void* W, int N, int K, const void* X, int M, int ns
       }
     }
   }
+  if (argmax) best = 1;
   p->splits = best;
-  int r = tc_make_tmap(&p->tmW, W, (uint64_t)N, (uint64_t)K, kTileN);
+  int r = tc_make_tmap(&p->tmW, W, (uint64_t)N, (uint64_t)K, (uint32_t)(kHalfN * wide));
   if (r) return r;
   // split: the tensor spans both halves (rows >= M of each half are ignored columns)
-  r = tc_make_tmap(&p->tmX, X, (uint64_t)(split ? xrows : M), (uint64_t)K, (uint32_t)p->xbox);
+  r = tc_make_tmap(&p->tmX, X, (uint64_t)(split ? 2 * p->MT : M), (uint64_t)K,
+                   (uint32_t)p->xbox);
   return r;
 }
 
+int tc_plan(TcPlan* p, const void* W, int N, int K, const void* X, int M, int nsm, bool argmax,
+            bool split) {
+  return tc_plan_shape(p, W, N, K, X, M, nsm, argmax, split, 1, 1, 0);
+}
+
+// The kernel instantiation for a plan: (wide, MMAs per k step, merged).
+template <int EPI>
+static void (*kernel_for(const TcPlan& p))(const CUtensorMap, const CUtensorMap, TcArgs) {
+  const int nmma = p.merged ? 1 : p.nx;
+  if (p.wide == 1) {
+    if (p.merged) return k_gemm_tc<EPI, 1, 1, true>;
+    return nmma == 1 ? k_gemm_tc<EPI, 1, 1, false> : k_gemm_tc<EPI, 1, 2, false>;
+  }
+  if (p.merged) return k_gemm_tc<EPI, 2, 1, true>;
+  return nmma == 1 ? k_gemm_tc<EPI, 2, 1, false> : k_gemm_tc<EPI, 2, 2, false>;
+}
+
 int tc_init_attributes() {
-  cudaError_t e1 = cudaFuncSetAttribute(k_gemm_tc<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)(kSmemBudget + 8 * 1024));
-  cudaError_t e2 = cudaFuncSetAttribute(k_gemm_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)(kSmemBudget + 8 * 1024));
-  return (e1 == cudaSuccess && e2 == cudaSuccess) ? 0 : -1;
+  const int bytes = (int)(kSmemBudget + 8 * 1024);
+  void (*ks[])(const CUtensorMap, const CUtensorMap, TcArgs) = {
+      k_gemm_tc<0, 1, 1, true>,  k_gemm_tc<0, 1, 1, false>, k_gemm_tc<0, 1, 2, false>,
+      k_gemm_tc<0, 2, 1, true>,  k_gemm_tc<0, 2, 1, false>, k_gemm_tc<0, 2, 2, false>,
+      k_gemm_tc<1, 1, 1, true>,  k_gemm_tc<1, 1, 1, false>, k_gemm_tc<1, 1, 2, false>,
+      k_gemm_tc<1, 2, 1, true>,  k_gemm_tc<1, 2, 1, false>, k_gemm_tc<1, 2, 2, false>};
+  for (auto k : ks)
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+        cudaSuccess)
+      return -1;
+  return 0;
 }
 
 void op_gemm_tc_acc(const TcPlan& p, float* out, int ldo, unsigned* err, cudaStream_t st) {
-  TcArgs a{p.N, p.K, p.M, p.MT, p.stages, p.split, p.xbox, p.nx, out, ldo, nullptr, nullptr, 0,
-           err};
-  dim3 grid((p.N + kTileN - 1) / kTileN, p.splits);
-  k_gemm_tc<0><<<grid, 128, p.smem, st>>>(p.tmW, p.tmX, a);
+  TcArgs a{p.N,     p.K,  p.M,     p.MT,       p.stages, p.wide, p.mct, p.split, p.xbox,
+           p.nx,    p.merged, p.acc_cols, out, ldo,     nullptr, nullptr, 0,  err};
+  dim3 grid(p.msplit, (p.N + kHalfN * p.wide - 1) / (kHalfN * p.wide), p.splits);
+  kernel_for<0>(p)<<<grid, 128, p.smem, st>>>(p.tmW, p.tmX, a);
 }
 
 void op_gemm_tc_argmax(const TcPlan& p, unsigned long long* keys, float* logits, long ldl,
                        unsigned* err, cudaStream_t st) {
-  TcArgs a{p.N, p.K, p.M, p.MT, p.stages, p.split, p.xbox, p.nx, nullptr, 0, keys, logits, ldl,
-           err};
-  dim3 grid((p.N + kTileN - 1) / kTileN, 1);
-  k_gemm_tc<1><<<grid, 128, p.smem, st>>>(p.tmW, p.tmX, a);
+  TcArgs a{p.N,  p.K,      p.M,        p.MT,    p.stages, p.wide, p.mct, p.split, p.xbox,
+           p.nx, p.merged, p.acc_cols, nullptr, 0,        keys,   logits, ldl,  err};
+  dim3 grid(p.msplit, (p.N + kHalfN * p.wide - 1) / (kHalfN * p.wide), 1);
+  kernel_for<1>(p)<<<grid, 128, p.smem, st>>>(p.tmW, p.tmX, a);
 }
 
 }  // namespace dmtp

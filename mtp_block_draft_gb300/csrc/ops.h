@@ -45,6 +45,9 @@ void op_build_slots(int dt, const void* E, int vocab, const int* A, const int* d
                     const float* delta, int mask_id, float* x, int B, int d, unsigned* err,
                     cudaStream_t st);
 // h = silu(gu[:, :F]) * gu[:, F:] as dt
+// Read `bytes` (multiple of 16, 16-byte aligned) of buf to evict the L2; sink[1] is a
+// write target that is never written in practice.
+void op_l2_flush(const void* buf, size_t bytes, unsigned* sink, cudaStream_t st);
 void op_swiglu(int dt, const float* gu, void* h, long h_lo, int rows, int F, cudaStream_t st);
 // RoPE (table) + cache write. src rows m = b*8 + s at position base[b] + s.
 // q_off < 0: no q. q_out fp32 [rows][hq][hd], or, when q_split != null (bf16 models),
@@ -138,7 +141,13 @@ void op_gemm_simt_argmax(const float* W, const float* X, int N, int K, int M,
 struct TcPlan {
   CUtensorMap tmW, tmX;
   int N, K, M, MT, splits, stages;
-  int split, xbox, nx;
+  int wide;       // 128-row weight halves per CTA (1 or 2)
+  int msplit;     // token halves: CTAs per weight tile (1 or 2)
+  int mct;        // token rows per CTA
+  int split;      // X is the [hi; lo] bf16 pair
+  int xbox, nx;   // X rows per TMA load, loads per stage
+  int merged;     // hi and lo in one MMA of 2*mct columns
+  int acc_cols;   // TMEM columns per accumulator
   size_t smem;
 };
 // Padded token rows of an M-row operand (multiple of 16, >= 16).
@@ -153,6 +162,9 @@ int tc_make_tmap3(CUtensorMap* tm, const void* base, uint64_t d0, uint64_t d1, u
 // holds 2*tc_mt(M) rows, the bf16 high halves then the low halves (X = hi + lo).
 int tc_plan(TcPlan* p, const void* W, int N, int K, const void* X, int M, int nsm,
             bool argmax, bool split);
+// tc_plan with the tile shape given: wide (1, 2), msplit (1, 2) and splits (<= 0: chosen).
+int tc_plan_shape(TcPlan* p, const void* W, int N, int K, const void* X, int M, int nsm,
+                  bool argmax, bool split, int wide, int msplit, int splits);
 void op_gemm_tc_acc(const TcPlan& p, float* out, int ldo, unsigned* err, cudaStream_t st);
 void op_gemm_tc_argmax(const TcPlan& p, unsigned long long* keys, float* logits, long ldl,
                        unsigned* err, cudaStream_t st);
