@@ -1,9 +1,15 @@
-// Split-K decode attention on the 5th-generation tensor cores (sm_103a).
+// Decode attention on the 5th-generation tensor cores (sm_103a), persistent and
+// evenly split over the SMs.
 //
-// One CTA per (512-key chunk, kv head, sequence) serves all 8 rows x the GQA group of
-// query heads that share the kv head (QN <= 64 queries), so each cached K/V byte is read
-// from HBM once per sequence and layer. Keys stream through shared memory in tiles of
-// TK keys (TMA, 128-byte swizzle, NST stages). Per tile:
+// Work: for every (sequence, kv head) segment, the 64-key tiles its 8 rows can see.
+// All segments' tiles are laid end to end and the grid (one CTA per SM) takes equal
+// contiguous ranges of that list, so every CTA streams the same number of tiles
+// whatever the context lengths; a CTA's range covers pieces of one or more segments.
+// Each piece serves all 8 rows x the GQA group of query heads of its kv head (QN <= 64
+// queries), so each cached K/V byte is read from HBM once per sequence and layer, and
+// leaves a partial (m, l, O) for the merge kernel. Keys stream through shared memory
+// in tiles of TK keys (TMA, 128-byte swizzle, NST stages) continuously across pieces.
+// Per tile:
 //   S = Q K^T  : tcgen05 M=128, N=TK keys, K = 2*hd: the fp32 queries enter as a bf16
 //                pair [Q_hi | Q_lo] along K against [K | K] (queries in operand rows
 //                0..QN-1), so S keeps the queries' fp32 precision. S is double-buffered
@@ -11,18 +17,19 @@
 //                The queries sit in operand rows 0..63 and again in rows 64..127, so
 //                TMEM lanes r and r+64 hold the same scores.
 //   softmax    : warps 0-7, four threads per query row, each a quarter of the
-//                tile's keys: mask (causal rows / anchor window / chunk bounds; skipped
+//                tile's keys: mask (causal rows / anchor window / segment bounds; skipped
 //                on interior tiles), exponentiate against a per-row reference max, and
 //                write P as a bf16 pair, P_hi in operand rows 0..63, P_lo in 64..127.
 //   O += P V   : tcgen05 M=128, N=hd, K=TK keys, B = the transposed V tile (K-major);
-//                O stays in TMEM for the whole chunk: lanes 0..63 accumulate P_hi V,
-//                lanes 64..127 P_lo V; they are summed once at the end.
+//                O stays in TMEM for the whole piece: lanes 0..63 accumulate P_hi V,
+//                lanes 64..127 P_lo V; they are summed once at the end of the piece.
 // The reference max only moves when a row's scores exceed it by more than 2^11; then
 // that row's O (both halves) is rescaled in TMEM. Keeping a stale reference is exact:
 // the same factor multiplies O and the running sum l.
-// The queries arrive by TMA, already split into bf16 halves by the RoPE kernel.
-// Warp 8 lane 0 issues the TMA loads, warp 9 lane 0 the MMAs. The partial (m, l, O) of
-// each chunk goes to global memory and a merge kernel combines the chunks (attention.cu).
+// The queries arrive by TMA, already split into bf16 halves by the RoPE kernel; the
+// next piece's queries are loaded as soon as the current piece's last S is computed.
+// Warp 8 lane 0 issues the K/V loads, warp 10 lane 0 the query loads, warp 9 lane 0
+// the MMAs.
 //
 // Visibility follows the DMTP blog §6.2: target and MTP rows are causal over their
 // cache; the drafter sees its anchor-relative window and the whole 8-slot block.
@@ -79,6 +86,18 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm,
       : "memory");
 }
 
+
+// First visible key of a sequence whose block rows start at `base`; the last is base+7.
+__device__ __forceinline__ int vis_lo(const AttnArgs& a, int base) {
+  int lo = a.lo_fixed;
+  if (a.window > 0) lo = max(lo, base - a.window);
+  return lo;
+}
+// Visible key tiles of a sequence (tile size tk).
+__device__ __forceinline__ int vis_tiles(const AttnArgs& a, int base, int tk) {
+  return (base + 7) / tk - vis_lo(a, base) / tk + 1;
+}
+
 // Shared-memory plan (TK keys per tile, NST stages). Each Q operand block (one 64-wide
 // head-dim block, hi or lo half) holds the QN query rows twice, at rows 0.. and 64.., so
 // TMEM lanes r and r + 64 of S carry the same scores and all eight softmax warps can
@@ -97,8 +116,10 @@ struct Smem {
   static constexpr uint32_t kPTile = (TK / 64) * kBlk;  // 128 rows x TK keys
   static constexpr bool kPinK = kKTile >= kPTile;
   static constexpr uint32_t kP = kPinK ? 0 : 2 * kPTile;
-  static constexpr uint32_t kSmall = 256 + 2048;      // barriers + tile maxima
-  static constexpr uint32_t kBig = kQ + NST * kStage + kP;  // 1024-aligned region
+  static constexpr uint32_t kX = 64 * (HD / 2 + 4) * 4;  // P_lo V half rows, final sum
+  // barriers, tile maxima [2][4][64], running sums [4][64], tile-count prefix [B + 1]
+  static constexpr uint32_t kSmall = 256 + 2048 + 1024 + 4 * (kAttnMaxB + 1);
+  static constexpr uint32_t kBig = kQ + NST * kStage + kP + kX;  // 1024-aligned region
   static constexpr uint32_t kBytes = (kSmall + 1023) / 1024 * 1024 + kBig;
   static_assert(kBytes <= 232448, "shared memory plan exceeds 227 KB");
 };
@@ -106,7 +127,7 @@ struct Smem {
 }  // namespace
 
 template <int HD, int TK, int NST>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     k_attn_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
               const __grid_constant__ CUtensorMap tmQh, const __grid_constant__ CUtensorMap tmQl,
               AttnArgs a, unsigned* err) {
@@ -115,19 +136,50 @@ __global__ void __launch_bounds__(320, 1)
   constexpr int KQ = TK / 4;  // keys per softmax thread (a quarter of the tile)
   constexpr float kLog2e = 1.4426950408889634f;
   extern __shared__ uint8_t smem_raw[];
-  const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-  const int grp = a.hq / a.hkv, QN = 8 * grp;
-  const int base = a.base[b];
-  int lo = a.lo_fixed;
-  if (a.window > 0) lo = max(lo, base - a.window);
-  const int hi_max = base + 7;
-  const int k_begin = max(lo, c * a.chunk);
-  const int k_end = min((c + 1) * a.chunk, hi_max + 1);
-  if (k_begin >= k_end) return;  // chunk outside this sequence's visible keys
-  const int t0 = k_begin / TK;
-  const int ntiles = (k_end + TK - 1) / TK - t0;
-
+  const int grp = a.hq / a.hkv, QN = 8 * grp, B = a.B, hkv = a.hkv;
   uint64_t* bars = (uint64_t*)smem_raw;
+  float* sMax = (float*)(bars + 32);  // [2 tiles][4 quarters][64] tile maxima (log2)
+  float* sL = sMax + 512;             // [4][64] running sums at the end of a piece
+  int* s_pref = (int*)(sL + 256);     // [B + 1] prefix sums of per-sequence tile counts
+
+  // ---- schedule: this CTA's range [x0, x1) of the global tile list ----
+  if (threadIdx.x < 32) {  // warp 0: inclusive scan of the tile counts, 32 at a time
+    const int ln = threadIdx.x;
+    int carry = 0;
+    if (ln == 0) s_pref[0] = 0;
+    for (int b0 = 0; b0 < B; b0 += 32) {
+      int v = b0 + ln < B ? vis_tiles(a, a.base[b0 + ln], TK) : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, v, o);
+        if (ln >= o) v += u;
+      }
+      if (b0 + ln < B) s_pref[b0 + ln + 1] = carry + v;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+  }
+  __syncthreads();
+  const long T = (long)hkv * s_pref[B];
+  const long x0 = T * blockIdx.x / gridDim.x, x1 = T * (blockIdx.x + 1) / gridDim.x;
+  if (x0 >= x1) return;
+  // the piece that starts at global tile x: sequence b, kv head g, first key tile kt0
+  // (absolute), tile count nt, and the sequence's base position
+  auto piece = [&](long x, int& b, int& g, int& kt0, int& nt, int& base) {
+    int lo_b = 0, hi_b = B;  // largest b with hkv * s_pref[b] <= x
+    while (hi_b - lo_b > 1) {
+      const int mid = (lo_b + hi_b) >> 1;
+      if ((long)hkv * s_pref[mid] <= x) lo_b = mid; else hi_b = mid;
+    }
+    b = lo_b;
+    const int nb = s_pref[b + 1] - s_pref[b];
+    const long r = x - (long)hkv * s_pref[b];
+    g = (int)(r / nb);
+    const int off = (int)(r % nb);
+    base = a.base[b];
+    kt0 = vis_lo(a, base) / TK + off;
+    nt = (int)min((long)(nb - off), x1 - x);
+  };
+
   uint8_t* sm = smem_raw + L::kSmall;
   sm += (1024 - (smem_u32(sm) & 1023)) & 1023;
   if (sm + L::kBig > smem_raw + L::kBytes) {  // dynamic shared memory base not aligned enough
@@ -137,6 +189,7 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* sQ = sm;
   uint8_t* sKV = sQ + L::kQ;
   uint8_t* sPsep = sKV + NST * L::kStage;
+  float* xo = (float*)(sPsep + L::kP);  // [64][HALF + 4]
   auto stage = [&](int t) -> uint8_t* { return sKV + (t % NST) * L::kStage; };
   auto p_buf = [&](int t) -> uint8_t* {
     return L::kPinK ? stage(t) : sPsep + (t & 1) * L::kPTile;
@@ -144,14 +197,15 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* kv_full = bars;             // [NST]
   uint64_t* kv_empty = bars + NST;      // [NST]
   uint64_t* s_full = bars + 2 * NST;    // [2] (S is double-buffered in TMEM)
-  uint64_t* q_full = s_full + 2;
-  uint64_t* p_full = q_full + 1;        // the 256 softmax threads wrote this tile's P
+  uint64_t* q_full = s_full + 2;        // a piece's queries landed
+  uint64_t* q_free = q_full + 1;        // a piece's last S completed: queries reloadable
+  uint64_t* p_full = q_free + 1;        // the 256 softmax threads wrote this tile's P
   uint64_t* o_full = p_full + 1;        // one commit per tile's P V
   uint64_t* mx = o_full + 1;            // all quarters of every row posted their maxima
-  uint64_t* fin = mx + 1;
+  uint64_t* pfin = mx + 1;              // a piece's last P V completed
+  uint64_t* o_drained = pfin + 1;       // the 256 softmax threads read a piece's O
+  uint64_t* fin = o_drained + 1;
   uint32_t* tmem_slot = (uint32_t*)(fin + 1);
-  float* sMax = (float*)(bars + 32);    // [2 tiles][4 quarters][64] tile maxima (log2)
-  float* sL = sMax;                     // [4][64] running sums, after the loop
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -162,9 +216,12 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(smem_u32(&s_full[0]), 1);
     mbar_init(smem_u32(&s_full[1]), 1);
     mbar_init(smem_u32(q_full), 1);
+    mbar_init(smem_u32(q_free), 1);
     mbar_init(smem_u32(p_full), 256);
     mbar_init(smem_u32(o_full), 1);
     mbar_init(smem_u32(mx), 256);
+    mbar_init(smem_u32(pfin), 1);
+    mbar_init(smem_u32(o_drained), 256);
     mbar_init(smem_u32(fin), 1);
     fence_mbar_init();
     tma_prefetch_desc(&tmK);
@@ -180,79 +237,130 @@ __global__ void __launch_bounds__(320, 1)
 
   if (warp == 8) {
     if (lane == 0) {
-      // ---------------- TMA producer ----------------
-      const uint64_t pol = policy_evict_first(), polq = policy_evict_last();
-      const uint32_t qb = smem_u32(q_full);
-      mbar_expect_tx(qb, (uint32_t)(4 * L::kDB * 64 * QN * 2));
-      for (int j = 0; j < L::kDB; ++j)
-        for (int dup = 0; dup < 2; ++dup) {  // rows 0.. and 64..
-          tma_load_3d(smem_u32(sQ + j * kBlk + dup * 8192), &tmQh, j * 64, g * grp, b * 8, qb,
-                      polq);
-          tma_load_3d(smem_u32(sQ + (L::kDB + j) * kBlk + dup * 8192), &tmQl, j * 64, g * grp,
-                      b * 8, qb, polq);
+      // ---------------- K/V producer: every tile of the range, in order ----------------
+      const uint64_t pol = policy_evict_first();
+      int gt = 0;
+      bool ok = true;
+      for (long x = x0; x < x1 && ok;) {
+        int b, g, kt0, nt, base;
+        piece(x, b, g, kt0, nt, base);
+        const long krow0 = ((long)b * hkv + g) * a.max_ctx;
+        const long vblk0 = ((long)b * hkv + g) * (a.max_ctx / 64);  // 64-key V^T blocks
+        for (int t = 0; t < nt; ++t, ++gt) {
+          const int s = gt % NST;
+          if (!mbar_wait(smem_u32(&kv_empty[s]), ((gt / NST) & 1) ^ 1, err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full = smem_u32(&kv_full[s]);
+          mbar_expect_tx(full, L::kStage);
+          const int key0 = (kt0 + t) * TK;
+          uint8_t* st = stage(gt);
+          for (int hb = 0; hb < L::kDB; ++hb)
+            tma_load_2d(smem_u32(st + hb * L::kKBox), &tmK, hb * 64, (int)(krow0 + key0), full,
+                        pol);
+          for (int kb = 0; kb < TK / 64; ++kb)
+            tma_load_2d(smem_u32(st + L::kKTile + kb * L::kVBox), &tmV, 0,
+                        (int)((vblk0 + key0 / 64 + kb) * HD), full, pol);
         }
-      const long krow0 = ((long)b * a.hkv + g) * a.max_ctx;
-      const long vblk0 = ((long)b * a.hkv + g) * (a.max_ctx / 64);  // 64-key V^T blocks
-      int issued = 0;
-      for (int t = 0; t < ntiles; ++t, ++issued) {
-        const int s = t % NST;
-        if (!mbar_wait(smem_u32(&kv_empty[s]), ((t / NST) & 1) ^ 1, err)) break;
-        const uint32_t full = smem_u32(&kv_full[s]);
-        mbar_expect_tx(full, L::kStage);
-        const int key0 = (t0 + t) * TK;
-        uint8_t* st = stage(t);
-        for (int hb = 0; hb < L::kDB; ++hb)
-          tma_load_2d(smem_u32(st + hb * L::kKBox), &tmK, hb * 64, (int)(krow0 + key0), full,
-                      pol);
-        for (int kb = 0; kb < TK / 64; ++kb)
-          tma_load_2d(smem_u32(st + L::kKTile + kb * L::kVBox), &tmV, 0,
-                      (int)((vblk0 + key0 / 64 + kb) * HD), full, pol);
+        x += nt;
       }
-      mbar_wait(qb, 0, err);
-      for (int j = (issued > NST ? issued - NST : 0); j < issued; ++j)
+      for (int j = (gt > NST ? gt - NST : 0); j < gt; ++j)
         mbar_wait(smem_u32(&kv_full[j % NST]), (j / NST) & 1, err);
+    }
+  } else if (warp == 10) {
+    if (lane == 0) {
+      // ---------------- query producer: one load per piece ----------------
+      const uint64_t polq = policy_evict_last();
+      const uint32_t qb = smem_u32(q_full);
+      int p = 0;
+      for (long x = x0; x < x1; ++p) {
+        int b, g, kt0, nt, base;
+        piece(x, b, g, kt0, nt, base);
+        if (p > 0 && !mbar_wait(smem_u32(q_free), (p - 1) & 1, err)) break;
+        mbar_expect_tx(qb, (uint32_t)(4 * L::kDB * 64 * QN * 2));
+        for (int j = 0; j < L::kDB; ++j)
+          for (int dup = 0; dup < 2; ++dup) {  // rows 0.. and 64..
+            tma_load_3d(smem_u32(sQ + j * kBlk + dup * 8192), &tmQh, j * 64, g * grp, b * 8, qb,
+                        polq);
+            tma_load_3d(smem_u32(sQ + (L::kDB + j) * kBlk + dup * 8192), &tmQl, j * 64, g * grp,
+                        b * 8, qb, polq);
+          }
+        x += nt;
+      }
+      if (p > 0) mbar_wait(qb, (p - 1) & 1, err);  // the last queries landed
     }
   } else if (warp == 9) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
       const uint32_t id_qk = umma_idesc_bf16(128, TK);
       const uint32_t id_pv = umma_idesc_bf16(128, HD);
-      bool ok = mbar_wait(smem_u32(q_full), 0, err);
-      auto issue_qk = [&](int t) -> bool {
-        const int s = t % NST;
-        if (!mbar_wait(smem_u32(&kv_full[s]), (t / NST) & 1, err)) return false;
+      auto issue_qk = [&](int xg) -> bool {
+        const int s = xg % NST;
+        if (!mbar_wait(smem_u32(&kv_full[s]), (xg / NST) & 1, err)) return false;
         tc_fence_after();
-        uint8_t* st = stage(t);
+        uint8_t* st = stage(xg);
 #pragma unroll
         for (int kb = 0; kb < 2 * L::kDB; ++kb) {  // [Q_hi | Q_lo] against [K | K]
           const uint64_t dq = umma_desc_sw128(smem_u32(sQ + kb * kBlk));
           const uint64_t dk = umma_desc_sw128(smem_u32(st + (kb % L::kDB) * L::kKBox));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem + (t & 1) * TK, dq + 2 * kk, dk + 2 * kk, id_qk, (kb | kk) ? 1u : 0u);
+            umma_bf16(tmem + (xg & 1) * TK, dq + 2 * kk, dk + 2 * kk, id_qk,
+                      (kb | kk) ? 1u : 0u);
         }
-        umma_commit(smem_u32(&s_full[t & 1]));
+        umma_commit(smem_u32(&s_full[xg & 1]));
         return true;
       };
-      ok = ok && issue_qk(0);
-      for (int t = 0; t < ntiles && ok; ++t) {
-        // the next tile's scores overlap this tile's softmax (its S buffer was released
-        // by the p_full arrival of tile t-1, waited for in the previous iteration)
-        if (t + 1 < ntiles && !issue_qk(t + 1)) break;
-        if (!mbar_wait(smem_u32(p_full), t & 1, err)) break;
+      int gt = 0, p = 0;
+      bool ok = true;
+      for (long x = x0; x < x1 && ok; ++p) {
+        int b, g, kt0, nt, base;
+        piece(x, b, g, kt0, nt, base);
+        ok = mbar_wait(smem_u32(q_full), p & 1, err);
+        if (!ok) break;
         tc_fence_after();
-        uint8_t* st = stage(t);
-        uint8_t* sP = p_buf(t);
+        // S of the piece's first tile (its buffer was released by the p_full of the
+        // tile before, waited for in the previous iteration)
+        ok = issue_qk(gt);
+        if (ok && nt == 1) umma_commit(smem_u32(q_free));
+        for (int t = 0; t < nt && ok; ++t) {
+          const int xg = gt + t;
+          // the next tile's scores overlap this tile's softmax
+          if (t + 1 < nt) {
+            if (!issue_qk(xg + 1)) {
+              ok = false;
+              break;
+            }
+            if (t + 2 == nt) umma_commit(smem_u32(q_free));  // the piece's last S
+          }
+          if (!mbar_wait(smem_u32(p_full), xg & 1, err)) {
+            ok = false;
+            break;
+          }
+          // the first P V of a piece overwrites O: the previous piece's O has been read
+          if (t == 0 && p > 0 && !mbar_wait(smem_u32(o_drained), (p - 1) & 1, err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint8_t* st = stage(xg);
+          uint8_t* sP = p_buf(xg);
 #pragma unroll
-        for (int kb = 0; kb < TK / 64; ++kb) {
-          const uint64_t dp = umma_desc_sw128(smem_u32(sP + kb * kBlk));
-          const uint64_t dv = umma_desc_sw128(smem_u32(st + L::kKTile + kb * L::kVBox));
+          for (int kb = 0; kb < TK / 64; ++kb) {
+            const uint64_t dp = umma_desc_sw128(smem_u32(sP + kb * kBlk));
+            const uint64_t dv = umma_desc_sw128(smem_u32(st + L::kKTile + kb * L::kVBox));
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tO, dp + 2 * kk, dv + 2 * kk, id_pv, (t | kb | kk) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16(tO, dp + 2 * kk, dv + 2 * kk, id_pv, (t | kb | kk) ? 1u : 0u);
+          }
+          umma_commit(smem_u32(o_full));
+          umma_commit(smem_u32(&kv_empty[xg % NST]));
         }
-        umma_commit(smem_u32(o_full));
-        umma_commit(smem_u32(&kv_empty[t % NST]));
+        if (!ok) break;
+        umma_commit(smem_u32(pfin));
+        gt += nt;
+        x += nt;
       }
       umma_commit(smem_u32(fin));  // all issued MMAs complete before TMEM is freed
     }
@@ -267,120 +375,133 @@ __global__ void __launch_bounds__(320, 1)
     const int kq = 2 * hf + (lrow >> 6);
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tOw = tO + lane_off + hf * HALF;
-    float m = -INFINITY, l = 0.f;  // reference max and running sum, log2 units
-    bool ok = true;
     const int srow = r / grp;
-    const int row_hi = a.causal ? base + srow : hi_max;
     const float scale = rsqrtf((float)HD) * kLog2e;
     // the quarter's keys in P: block (kq*KQ)/64, first 16-byte chunk ((kq*KQ)%64)/8
     const int pblk = (kq * KQ) / 64, pch = ((kq * KQ) % 64) / 8;
-    for (int t = 0; t < ntiles && ok; ++t) {
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[t & 1]), (t >> 1) & 1, err));
-      if (!ok) break;
-      tc_fence_after();
-      const int kt = (t0 + t) * TK;
-      const int key0 = kt + kq * KQ;
-      // interior tiles need no mask: every key of the tile is visible to every row
-      const bool interior =
-          kt >= k_begin && kt + TK <= k_end && (!a.causal || kt + TK <= base + 1);
-      float sv[KQ];
-#pragma unroll
-      for (int cc = 0; cc < KQ / 16; ++cc) {
-        float v[16];
-        tmem_ld16(tmem + (t & 1) * TK + kq * KQ + cc * 16 + lane_off, v);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) sv[cc * 16 + j] = v[j] * scale;
-      }
-      if (!interior) {
-#pragma unroll
-        for (int j = 0; j < KQ; ++j) {
-          const int key = key0 + j;
-          if (!(key >= k_begin && key < k_end && key <= row_hi)) sv[j] = -INFINITY;
-        }
-      }
-      float mt = sv[0];
-#pragma unroll
-      for (int j = 1; j < KQ; ++j) mt = fmaxf(mt, sv[j]);
-      float* smx = sMax + (t & 1) * 256;
-      smx[kq * 64 + r] = mt;
-      mbar_arrive(smem_u32(mx));
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(mx), t & 1, err));
-      if (!ok) break;
-      mt = fmaxf(fmaxf(smx[r], smx[64 + r]), fmaxf(smx[128 + r], smx[192 + r]));
-      // reference max: set on the first visible scores, moved only past 2^11
-      float corr = 1.f;
-      if (mt > -INFINITY && (m == -INFINITY || mt > m + 11.f)) {
-        corr = (m == -INFINITY) ? 1.f : exp2f(m - mt);
-        m = mt;
-      }
-      // a rescale of O waits for the previous tile's P V (s_full of this tile implies
-      // every P V before it has completed, so o_full is at most one phase behind)
-      if (t > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(o_full), (t - 1) & 1, err));
+    bool ok = true;
+    int gt = 0, p = 0;
+    // Every thread runs the same pieces and the same named barriers, whether or not a
+    // wait timed out (then the work is skipped), so the barriers always complete.
+    for (long x = x0; x < x1; ++p) {
+      int b, g, kt0, nt, base;
+      piece(x, b, g, kt0, nt, base);
+      const int lo = vis_lo(a, base), k_end = base + 8;
+      const int row_hi = a.causal ? base + srow : base + 7;
+      float m = -INFINITY, l = 0.f;  // reference max and running sum, log2 units
+      for (int t = 0; t < nt && ok; ++t) {
+        const int xg = gt + t;
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[xg & 1]), (xg >> 1) & 1, err));
         if (!ok) break;
         tc_fence_after();
-        tmem_scale(tOw, HALF, corr);
-      }
-      l *= corr;
-      const float mu = (m == -INFINITY) ? 0.f : m;
-      uint8_t* pb_ = p_buf(t) + pblk * kBlk;
+        const int kt = (kt0 + t) * TK;
+        const int key0 = kt + kq * KQ;
+        // interior tiles need no mask: every key of the tile is visible to every row
+        const bool interior =
+            kt >= lo && kt + TK <= k_end && (!a.causal || kt + TK <= base + 1);
+        float sv[KQ];
 #pragma unroll
-      for (int cc = 0; cc < KQ / 8; ++cc) {
-        uint32_t ph[4], pl[4];
+        for (int cc = 0; cc < KQ / 16; ++cc) {
+          float v[16];
+          tmem_ld16(tmem + (xg & 1) * TK + kq * KQ + cc * 16 + lane_off, v);
 #pragma unroll
-        for (int j = 0; j < 8; j += 2) {
-          const float p0 = exp2f(sv[cc * 8 + j] - mu), p1 = exp2f(sv[cc * 8 + j + 1] - mu);
-          l += p0 + p1;
-          const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-          const __nv_bfloat162 pr =
-              __floats2bfloat162_rn(p0 - __low2float(pb), p1 - __high2float(pb));
-          ph[j / 2] = *reinterpret_cast<const uint32_t*>(&pb);
-          pl[j / 2] = *reinterpret_cast<const uint32_t*>(&pr);
+          for (int j = 0; j < 16; ++j) sv[cc * 16 + j] = v[j] * scale;
         }
-        *(uint4*)(pb_ + sw128(r, pch + cc)) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-        *(uint4*)(pb_ + sw128(r + 64, pch + cc)) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+        if (!interior) {
+#pragma unroll
+          for (int j = 0; j < KQ; ++j) {
+            const int key = key0 + j;
+            if (!(key >= lo && key < k_end && key <= row_hi)) sv[j] = -INFINITY;
+          }
+        }
+        float mt = sv[0];
+#pragma unroll
+        for (int j = 1; j < KQ; ++j) mt = fmaxf(mt, sv[j]);
+        float* smx = sMax + (xg & 1) * 256;
+        smx[kq * 64 + r] = mt;
+        mbar_arrive(smem_u32(mx));
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(mx), xg & 1, err));
+        if (!ok) break;
+        mt = fmaxf(fmaxf(smx[r], smx[64 + r]), fmaxf(smx[128 + r], smx[192 + r]));
+        // reference max: set on the first visible scores, moved only past 2^11
+        float corr = 1.f;
+        if (mt > -INFINITY && (m == -INFINITY || mt > m + 11.f)) {
+          corr = (m == -INFINITY) ? 1.f : exp2f(m - mt);
+          m = mt;
+        }
+        // a rescale of O waits for the previous tile's P V (s_full of this tile implies
+        // every P V before it has completed, so o_full is at most one phase behind)
+        if (t > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(o_full), (xg - 1) & 1, err));
+          if (!ok) break;
+          tc_fence_after();
+          tmem_scale(tOw, HALF, corr);
+        }
+        l *= corr;
+        const float mu = (m == -INFINITY) ? 0.f : m;
+        uint8_t* pb_ = p_buf(xg) + pblk * kBlk;
+#pragma unroll
+        for (int cc = 0; cc < KQ / 8; ++cc) {
+          uint32_t ph[4], pl[4];
+#pragma unroll
+          for (int j = 0; j < 8; j += 2) {
+            const float p0 = exp2f(sv[cc * 8 + j] - mu), p1 = exp2f(sv[cc * 8 + j + 1] - mu);
+            l += p0 + p1;
+            const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+            const __nv_bfloat162 pr =
+                __floats2bfloat162_rn(p0 - __low2float(pb), p1 - __high2float(pb));
+            ph[j / 2] = *reinterpret_cast<const uint32_t*>(&pb);
+            pl[j / 2] = *reinterpret_cast<const uint32_t*>(&pr);
+          }
+          *(uint4*)(pb_ + sw128(r, pch + cc)) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+          *(uint4*)(pb_ + sw128(r + 64, pch + cc)) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        mbar_arrive(smem_u32(p_full));
       }
-      fence_proxy_async();
+      // ---- end of the piece: O once its last P V completed ----
+      float O[HALF];
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(pfin), p & 1, err));
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < HALF / 16; ++cc) {
+          float v[16];
+          tmem_ld16(tOw + cc * 16, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) O[cc * 16 + j] = v[j];
+        }
+      }
+      sL[kq * 64 + r] = l;
+      const long slot = (long)blockIdx.x + (long)b * hkv + g;  // partial of (CTA, segment)
+      // the P_lo V rows meet the P_hi V rows in shared memory, one head-dim half at a time
+      for (int pass = 0; pass < 2; ++pass) {
+        if (hf == pass && lrow >= 64 && ok) {
+#pragma unroll
+          for (int i = 0; i < HALF; i += 4)
+            *(float4*)(xo + r * (HALF + 4) + i) = make_float4(O[i], O[i + 1], O[i + 2], O[i + 3]);
+        }
+        asm volatile("bar.sync 2, 256;" ::: "memory");
+        if (hf == pass && lrow < 64 && r < QN && ok) {
+          float* po = a.part_o + (slot * QN + r) * HD + hf * HALF;
+          const float* lo_row = xo + r * (HALF + 4);
+#pragma unroll
+          for (int i = 0; i < HALF; i += 4)
+            *(float4*)(po + i) = make_float4(O[i] + lo_row[i], O[i + 1] + lo_row[i + 1],
+                                             O[i + 2] + lo_row[i + 2], O[i + 3] + lo_row[i + 3]);
+          if (hf == 0) {
+            constexpr float kLn2 = 0.6931471805599453f;
+            a.part_ml[(slot * QN + r) * 2] = m * kLn2;  // natural units for the merge
+            a.part_ml[(slot * QN + r) * 2 + 1] = sL[r] + sL[64 + r] + sL[128 + r] + sL[192 + r];
+          }
+        }
+        asm volatile("bar.sync 2, 256;" ::: "memory");
+      }
       tc_fence_before();
-      mbar_arrive(smem_u32(p_full));
-    }
-    // the final O: every MMA has completed once `fin` fires; read this thread's half row
-    float O[HALF];
-    ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(fin), 0, err));
-    if (ok) {
-      tc_fence_after();
-#pragma unroll
-      for (int cc = 0; cc < HALF / 16; ++cc) {
-        float v[16];
-        tmem_ld16(tOw + cc * 16, v);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) O[cc * 16 + j] = v[j];
-      }
-    }
-    // the P_lo V rows and the quarters' sums meet in shared memory (the K/V stage area
-    // is idle once every MMA has completed)
-    float* xo = (float*)sKV;  // [64][HD + 4]
-    if (lrow >= 64 && ok) {
-#pragma unroll
-      for (int i = 0; i < HALF; i += 4)
-        *(float4*)(xo + r * (HD + 4) + hf * HALF + i) =
-            make_float4(O[i], O[i + 1], O[i + 2], O[i + 3]);
-    }
-    sL[kq * 64 + r] = l;
-    asm volatile("bar.sync 2, 256;" ::: "memory");
-    if (ok && lrow < 64 && r < QN) {
-      const long pidx = ((long)b * a.hkv + g) * a.nchunk + c;
-      float* po = a.part_o + (pidx * QN + r) * HD + hf * HALF;
-      const float* lo_row = xo + r * (HD + 4) + hf * HALF;
-#pragma unroll
-      for (int i = 0; i < HALF; i += 4)
-        *(float4*)(po + i) = make_float4(O[i] + lo_row[i], O[i + 1] + lo_row[i + 1],
-                                         O[i + 2] + lo_row[i + 2], O[i + 3] + lo_row[i + 3]);
-      if (hf == 0) {
-        constexpr float kLn2 = 0.6931471805599453f;
-        a.part_ml[(pidx * QN + r) * 2] = m * kLn2;  // natural units for the merge
-        a.part_ml[(pidx * QN + r) * 2 + 1] = sL[r] + sL[64 + r] + sL[128 + r] + sL[192 + r];
-      }
+      mbar_arrive(smem_u32(o_drained));
+      gt += nt;
+      x += nt;
     }
   }
   __syncwarp();
@@ -393,9 +514,69 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
+// Combine the partials of the persistent kernel: one warp per (row, query head); the
+// (CTA, segment) partials of a segment are those of the CTAs whose tile ranges meet it.
+template <int DPL>
+__global__ void __launch_bounds__(256) k_attn_merge_p(AttnArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y * 8 + warp;
+  if (h >= a.hq) return;
+  const int mrow = blockIdx.x, b = mrow >> 3, s = mrow & 7;
+  const int grp = a.hq / a.hkv, g = h / grp, hh = h % grp, qi = s * grp + hh, QN = 8 * grp;
+  const int TK = a.ptk, G = a.pgrid;
+  int pre = 0, tot = 0;
+  for (int bb = lane; bb < a.B; bb += 32) {
+    const int n = vis_tiles(a, a.base[bb], TK);
+    tot += n;
+    if (bb < b) pre += n;
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    pre += __shfl_xor_sync(0xffffffffu, pre, o);
+    tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  }
+  const long T = (long)a.hkv * tot;
+  const int nb = vis_tiles(a, a.base[b], TK);
+  const long xf = (long)a.hkv * pre + (long)g * nb, xl = xf + nb - 1;
+  // CTA i covers [floor(T i / G), floor(T (i+1) / G)): the owner of x is
+  // floor(((x + 1) G - 1) / T)
+  const int c0 = (int)(((xf + 1) * G - 1) / T), c1 = (int)(((xl + 1) * G - 1) / T);
+  const long seg = (long)b * a.hkv + g;
+  // CTAs with an empty range (more CTAs than tiles) wrote nothing
+  auto empty = [&](int i) { return T * i / G == T * (i + 1) / G; };
+  float M = -INFINITY;
+  for (int i = c0 + lane; i <= c1; i += 32)
+    if (!empty(i)) M = fmaxf(M, a.part_ml[((i + seg) * QN + qi) * 2]);
+  M = warp_max(M);
+  float Lsum = 0.f;
+  for (int i = c0 + lane; i <= c1; i += 32) {
+    if (empty(i)) continue;
+    const float* ml = a.part_ml + ((i + seg) * QN + qi) * 2;
+    Lsum += ml[1] * __expf(ml[0] - M);
+  }
+  Lsum = warp_sum(Lsum);
+  const float invL = 1.f / Lsum;
+  float acc[DPL];
+#pragma unroll
+  for (int j = 0; j < DPL; ++j) acc[j] = 0.f;
+  for (int i = c0; i <= c1; ++i) {
+    if (empty(i)) continue;
+    const float w = __expf(a.part_ml[((i + seg) * QN + qi) * 2] - M);
+    const float* pc = a.part_o + ((i + seg) * QN + qi) * a.hd + lane * DPL;
+#pragma unroll
+    for (int j = 0; j < DPL; j += 2) {
+      const float2 v = *reinterpret_cast<const float2*>(pc + j);
+      acc[j] += v.x * w;
+      acc[j + 1] += v.y * w;
+    }
+  }
+  bf16* out = (bf16*)a.out + (long)mrow * a.hq * a.hd + h * a.hd + lane * DPL;
+#pragma unroll
+  for (int j = 0; j < DPL; ++j) store_act(out + j, a.out_lo, acc[j] * invL);
+}
+
 // tile keys and stage count per head dim
-constexpr int kTK128 = 64, kNST128 = 4;
-constexpr int kTK64 = 64, kNST64 = 4;
+constexpr int kTK128 = kAttnTile, kNST128 = 4;
+constexpr int kTK64 = kAttnTile, kNST64 = 4;
 
 int attn_tc_init_attributes() {
   cudaError_t e1 = cudaFuncSetAttribute(k_attn_tc<128, kTK128, kNST128>,
@@ -410,14 +591,18 @@ int attn_tc_init_attributes() {
 void op_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV,
                      const CUtensorMap& tmQh, const CUtensorMap& tmQl, unsigned* err,
                      cudaStream_t st) {
-  dim3 grid(a.nchunk, a.hkv, a.B);
+  if (a.B > kAttnMaxB || a.pgrid < 1 || a.ptk != kAttnTile) return;  // excluded by the caller
   if (a.hd == 128)
-    k_attn_tc<128, kTK128, kNST128><<<grid, 320, Smem<128, kTK128, kNST128>::kBytes, st>>>(
+    k_attn_tc<128, kTK128, kNST128><<<a.pgrid, 352, Smem<128, kTK128, kNST128>::kBytes, st>>>(
         tmK, tmV, tmQh, tmQl, a, err);
   else
-    k_attn_tc<64, kTK64, kNST64><<<grid, 320, Smem<64, kTK64, kNST64>::kBytes, st>>>(
+    k_attn_tc<64, kTK64, kNST64><<<a.pgrid, 352, Smem<64, kTK64, kNST64>::kBytes, st>>>(
         tmK, tmV, tmQh, tmQl, a, err);
-  op_attention_merge(1, a, st);
+  dim3 g(a.B * 8, (a.hq + 7) / 8);
+  if (a.hd == 128)
+    k_attn_merge_p<4><<<g, 256, 0, st>>>(a);
+  else
+    k_attn_merge_p<2><<<g, 256, 0, st>>>(a);
 }
 
 }  // namespace dmtp

@@ -48,6 +48,7 @@ struct dmtp_ctx {
   int tap_of_layer[DMTP_MAX_LAYERS];  // tap slot of layer l, or -1
   int pmax;
   int attn_chunk, attn_nchunk;
+  int attn_grid;  // CTAs of the persistent tensor-core attention (SM count)
   int mt8, mt6, mt1;  // padded GEMM token rows for 8B, 6B and B operand rows
   size_t ws_bytes;
 
@@ -191,7 +192,15 @@ int derive(dmtp_ctx* c, const dmtp_config* cfg, int B) {
   c->mt8 = tc_mt(c->M);
   c->mt6 = tc_mt(6 * B);
   c->mt1 = tc_mt(B);
-  c->attn_tc = c->dt == 1 && (c->hd == 64 || c->hd == 128) && QN <= 64;
+  c->attn_tc = c->dt == 1 && (c->hd == 64 || c->hd == 128) && QN <= 64 && B <= kAttnMaxB;
+  {  // the persistent tensor-core attention runs one CTA per SM
+    int dev = 0, nsm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        nsm < 1)
+      nsm = 256;
+    c->attn_grid = nsm;
+  }
   c->attn_chunk = 1024;  // keys per attention partial; a multiple of the 64-key tile
   c->attn_nchunk = (c->maxc + 8 + c->attn_chunk - 1) / c->attn_chunk;
   return DMTP_OK;
@@ -230,8 +239,12 @@ size_t layout(dmtp_ctx* c, char* base) {
   c->q = b.take<float>(M * c->qd * 4);
   c->qs = b.take<char>(2 * M * c->qd * 2);
   const int QN = 8 * (c->hq / c->hkv);
-  c->part_o = b.take<float>(B * c->hkv * c->attn_nchunk * QN * c->hd * 4);
-  c->part_ml = b.take<float>(B * c->hkv * c->attn_nchunk * QN * 2 * 4);
+  // partials: per (sequence, kv head, chunk) for the chunked path, per (CTA, segment)
+  // slot for the persistent one
+  const size_t slots = std::max((size_t)B * c->hkv * c->attn_nchunk,
+                                (size_t)c->attn_grid + (size_t)B * c->hkv);
+  c->part_o = b.take<float>(slots * QN * c->hd * 4);
+  c->part_ml = b.take<float>(slots * QN * 2 * 4);
   c->att = b.take<char>(r8 * std::max(c->qd, c->gH * c->gdv) * es);
   c->gu = b.take<float>(M * 2 * c->F * 4);
   c->hmid = b.take<char>(r8 * c->F * es);
@@ -425,6 +438,8 @@ void attn_layer(dmtp_ctx* c, const LayerPlans& p, const dmtp_layer_weights& w, f
   aa.max_ctx = c->maxc;
   aa.chunk = c->attn_chunk;
   aa.nchunk = c->attn_nchunk;
+  aa.pgrid = c->attn_grid;
+  aa.ptk = kAttnTile;
   double kv_bytes = 0;
   if (c->prof) {
     // keys each sequence's rows can see: lo .. base+7, K and V, all kv heads
