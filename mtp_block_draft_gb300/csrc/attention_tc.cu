@@ -10,12 +10,12 @@
 // leaves a partial (m, l, O) for the merge kernel. Keys stream through shared memory
 // in tiles of TK keys (TMA, 128-byte swizzle, NST stages) continuously across pieces.
 // Per tile:
-//   S = Q K^T  : tcgen05 M=128, N=TK keys, K = 2*hd: the fp32 queries enter as a bf16
-//                pair [Q_hi | Q_lo] along K against [K | K] (queries in operand rows
-//                0..QN-1), so S keeps the queries' fp32 precision. S is double-buffered
-//                in TMEM: the next tile's scores are computed during this tile's softmax.
-//                The queries sit in operand rows 0..63 and again in rows 64..127, so
-//                TMEM lanes r and r+64 hold the same scores.
+//   S = Q K^T  : tcgen05 M=128, N=TK keys, K = 2*hd, A from TMEM: the fp32 queries
+//                enter as a bf16 pair [Q_hi | Q_lo] along K against [K | K] (queries in
+//                operand rows 0..QN-1), so S keeps the queries' fp32 precision. S is
+//                double-buffered in TMEM: the next tile's scores are computed during this
+//                tile's softmax. The queries sit in operand rows 0..63 and again in rows
+//                64..127, so TMEM lanes r and r+64 hold the same scores.
 //   softmax    : warps 0-7, four threads per query row, each a quarter of the
 //                tile's keys: mask (causal rows / anchor window / segment bounds; skipped
 //                on interior tiles), exponentiate against a per-row reference max, and
@@ -26,10 +26,11 @@
 // The reference max only moves when a row's scores exceed it by more than 2^11; then
 // that row's O (both halves) is rescaled in TMEM. Keeping a stale reference is exact:
 // the same factor multiplies O and the running sum l.
-// The queries arrive by TMA, already split into bf16 halves by the RoPE kernel; the
-// next piece's queries are loaded as soon as the current piece's last S is computed.
-// Warp 8 lane 0 issues the K/V loads, warp 10 lane 0 the query loads, warp 9 lane 0
-// the MMAs.
+// The queries, already split into bf16 halves by the RoPE kernel, live in TMEM as the
+// A operand of S (written by the softmax warps at the start of each piece), which
+// leaves the shared memory to the K/V ring: six 32 KB stages keep ~190 KB of K/V in
+// flight per SM, what the HBM latency under full load asks for.
+// Warp 8 lane 0 issues the K/V loads, warp 9 lane 0 the MMAs.
 //
 // Visibility follows the DMTP blog §6.2: target and MTP rows are causal over their
 // cache; the drafter sees its anchor-relative window and the whole 8-slot block.
@@ -67,6 +68,28 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
       : "memory");
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem]^T, bf16 inputs, fp32 accumulate (kind::f16). A holds
+// row m in TMEM lane m, two consecutive k elements per 32-bit column (even k low).
+__device__ __forceinline__ void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// 32 lanes x 16 consecutive 32-bit columns from registers (no wait).
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
+}
+
 // scale `n` TMEM columns of this warp's 32 lanes by a per-lane factor f
 __device__ __forceinline__ void tmem_scale(uint32_t taddr, int n, float f) {
   for (int cc = 0; cc < n; cc += 16) {
@@ -98,16 +121,12 @@ __device__ __forceinline__ int vis_tiles(const AttnArgs& a, int base, int tk) {
   return (base + 7) / tk - vis_lo(a, base) / tk + 1;
 }
 
-// Shared-memory plan (TK keys per tile, NST stages). Each Q operand block (one 64-wide
-// head-dim block, hi or lo half) holds the QN query rows twice, at rows 0.. and 64.., so
-// TMEM lanes r and r + 64 of S carry the same scores and all eight softmax warps can
-// read them. P (128 rows x TK keys) of tile t is written into the K area of its stage
-// when that is large enough (K(t) is dead once S(t) is computed), else into a double
-// buffer of its own.
+// Shared-memory plan (TK keys per tile, NST stages). P (128 rows x TK keys) of tile t is
+// written into the K area of its stage when that is large enough (K(t) is dead once S(t)
+// is computed), else into a double buffer of its own.
 template <int HD, int TK, int NST>
 struct Smem {
   static constexpr int kDB = HD / 64;                 // 64-wide head-dim blocks
-  static constexpr uint32_t kQ = 2 * kDB * kBlk;      // [Q_hi blocks | Q_lo blocks]
   static constexpr uint32_t kKBox = TK * 128;         // TK keys x 64 head dims
   static constexpr uint32_t kKTile = kDB * kKBox;
   static constexpr uint32_t kVBox = HD * 128;         // HD rows x 64 keys
@@ -119,7 +138,7 @@ struct Smem {
   static constexpr uint32_t kX = 64 * (HD / 2 + 4) * 4;  // P_lo V half rows, final sum
   // barriers, tile maxima [2][4][64], running sums [4][64], tile-count prefix [B + 1]
   static constexpr uint32_t kSmall = 256 + 2048 + 1024 + 4 * (kAttnMaxB + 1);
-  static constexpr uint32_t kBig = kQ + NST * kStage + kP + kX;  // 1024-aligned region
+  static constexpr uint32_t kBig = NST * kStage + kP + kX;  // 1024-aligned region
   static constexpr uint32_t kBytes = (kSmall + 1023) / 1024 * 1024 + kBig;
   static_assert(kBytes <= 232448, "shared memory plan exceeds 227 KB");
 };
@@ -127,7 +146,7 @@ struct Smem {
 }  // namespace
 
 template <int HD, int TK, int NST>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(320, 1)
     k_attn_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
               const __grid_constant__ CUtensorMap tmQh, const __grid_constant__ CUtensorMap tmQl,
               AttnArgs a, unsigned* err) {
@@ -186,8 +205,7 @@ __global__ void __launch_bounds__(352, 1)
     if (threadIdx.x == 0) set_err(err, DMTP_ERR_TIMEOUT);
     return;
   }
-  uint8_t* sQ = sm;
-  uint8_t* sKV = sQ + L::kQ;
+  uint8_t* sKV = sm;
   uint8_t* sPsep = sKV + NST * L::kStage;
   float* xo = (float*)(sPsep + L::kP);  // [64][HALF + 4]
   auto stage = [&](int t) -> uint8_t* { return sKV + (t % NST) * L::kStage; };
@@ -197,9 +215,8 @@ __global__ void __launch_bounds__(352, 1)
   uint64_t* kv_full = bars;             // [NST]
   uint64_t* kv_empty = bars + NST;      // [NST]
   uint64_t* s_full = bars + 2 * NST;    // [2] (S is double-buffered in TMEM)
-  uint64_t* q_full = s_full + 2;        // a piece's queries landed
-  uint64_t* q_free = q_full + 1;        // a piece's last S completed: queries reloadable
-  uint64_t* p_full = q_free + 1;        // the 256 softmax threads wrote this tile's P
+  uint64_t* q_full = s_full + 2;        // the 256 softmax threads wrote a piece's queries
+  uint64_t* p_full = q_full + 1;        // the 256 softmax threads wrote this tile's P
   uint64_t* o_full = p_full + 1;        // one commit per tile's P V
   uint64_t* mx = o_full + 1;            // all quarters of every row posted their maxima
   uint64_t* pfin = mx + 1;              // a piece's last P V completed
@@ -215,8 +232,7 @@ __global__ void __launch_bounds__(352, 1)
     }
     mbar_init(smem_u32(&s_full[0]), 1);
     mbar_init(smem_u32(&s_full[1]), 1);
-    mbar_init(smem_u32(q_full), 1);
-    mbar_init(smem_u32(q_free), 1);
+    mbar_init(smem_u32(q_full), 256);
     mbar_init(smem_u32(p_full), 256);
     mbar_init(smem_u32(o_full), 1);
     mbar_init(smem_u32(mx), 256);
@@ -227,13 +243,16 @@ __global__ void __launch_bounds__(352, 1)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
-  constexpr uint32_t kTmemCols = 2 * TK + HD <= 256 ? 256 : 512;
+  // S buffers at columns 0 and TK, O (HD columns) after them, then Q: 2*HD bf16 per
+  // row = HD columns
+  constexpr uint32_t kTmemCols = 2 * TK + 2 * HD <= 256 ? 256 : 512;
   if (warp == 8) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tO = tmem + 2 * TK;  // S buffers at columns 0 and TK, O after them
+  const uint32_t tO = tmem + 2 * TK;
+  const uint32_t tQ = tO + HD;
 
   if (warp == 8) {
     if (lane == 0) {
@@ -268,28 +287,6 @@ __global__ void __launch_bounds__(352, 1)
       for (int j = (gt > NST ? gt - NST : 0); j < gt; ++j)
         mbar_wait(smem_u32(&kv_full[j % NST]), (j / NST) & 1, err);
     }
-  } else if (warp == 10) {
-    if (lane == 0) {
-      // ---------------- query producer: one load per piece ----------------
-      const uint64_t polq = policy_evict_last();
-      const uint32_t qb = smem_u32(q_full);
-      int p = 0;
-      for (long x = x0; x < x1; ++p) {
-        int b, g, kt0, nt, base;
-        piece(x, b, g, kt0, nt, base);
-        if (p > 0 && !mbar_wait(smem_u32(q_free), (p - 1) & 1, err)) break;
-        mbar_expect_tx(qb, (uint32_t)(4 * L::kDB * 64 * QN * 2));
-        for (int j = 0; j < L::kDB; ++j)
-          for (int dup = 0; dup < 2; ++dup) {  // rows 0.. and 64..
-            tma_load_3d(smem_u32(sQ + j * kBlk + dup * 8192), &tmQh, j * 64, g * grp, b * 8, qb,
-                        polq);
-            tma_load_3d(smem_u32(sQ + (L::kDB + j) * kBlk + dup * 8192), &tmQl, j * 64, g * grp,
-                        b * 8, qb, polq);
-          }
-        x += nt;
-      }
-      if (p > 0) mbar_wait(qb, (p - 1) & 1, err);  // the last queries landed
-    }
   } else if (warp == 9) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
@@ -302,12 +299,11 @@ __global__ void __launch_bounds__(352, 1)
         uint8_t* st = stage(xg);
 #pragma unroll
         for (int kb = 0; kb < 2 * L::kDB; ++kb) {  // [Q_hi | Q_lo] against [K | K]
-          const uint64_t dq = umma_desc_sw128(smem_u32(sQ + kb * kBlk));
           const uint64_t dk = umma_desc_sw128(smem_u32(st + (kb % L::kDB) * L::kKBox));
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem + (xg & 1) * TK, dq + 2 * kk, dk + 2 * kk, id_qk,
-                      (kb | kk) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk)  // 16 k = 8 TMEM columns of Q per MMA
+            umma_bf16_ta(tmem + (xg & 1) * TK, tQ + kb * 32 + kk * 8, dk + 2 * kk, id_qk,
+                         (kb | kk) ? 1u : 0u);
         }
         umma_commit(smem_u32(&s_full[xg & 1]));
         return true;
@@ -323,7 +319,6 @@ __global__ void __launch_bounds__(352, 1)
         // S of the piece's first tile (its buffer was released by the p_full of the
         // tile before, waited for in the previous iteration)
         ok = issue_qk(gt);
-        if (ok && nt == 1) umma_commit(smem_u32(q_free));
         for (int t = 0; t < nt && ok; ++t) {
           const int xg = gt + t;
           // the next tile's scores overlap this tile's softmax
@@ -332,7 +327,6 @@ __global__ void __launch_bounds__(352, 1)
               ok = false;
               break;
             }
-            if (t + 2 == nt) umma_commit(smem_u32(q_free));  // the piece's last S
           }
           if (!mbar_wait(smem_u32(p_full), xg & 1, err)) {
             ok = false;
@@ -381,6 +375,44 @@ __global__ void __launch_bounds__(352, 1)
     const int pblk = (kq * KQ) / 64, pch = ((kq * KQ) % 64) / 8;
     bool ok = true;
     int gt = 0, p = 0;
+    // The queries of a piece into TMEM (A operand of S): lane lrow holds query row
+    // lrow % 64 (zeros past QN); warps 0-3 write the hi half (columns 0..HD/2-1 of the
+    // Q region), warps 4-7 the lo half. Called when no S of the previous piece is
+    // pending (the softmax warps have consumed them all).
+    auto write_q = [&](int b, int g) {
+      uint32_t w[HALF];
+      if (r < QN) {
+        const int s_ = r / grp, hh = r % grp;
+        const bf16* src = (const bf16*)a.qs + ((long)(b * 8 + s_) * a.hq + g * grp + hh) * HD +
+                          (hf ? a.qs_lo : 0);
+#pragma unroll
+        for (int i = 0; i < HALF; i += 4) {
+          const uint4 u = *reinterpret_cast<const uint4*>(src + 2 * i);
+          w[i] = u.x;
+          w[i + 1] = u.y;
+          w[i + 2] = u.z;
+          w[i + 3] = u.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < HALF; ++i) w[i] = 0u;
+      }
+#pragma unroll
+      for (int c16 = 0; c16 < HALF / 16; ++c16) {
+        uint32_t v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = w[c16 * 16 + i];
+        tmem_st16u(tQ + lane_off + hf * HALF + c16 * 16, v);
+      }
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      mbar_arrive(smem_u32(q_full));
+    };
+    {
+      int b, g, kt0, nt, base;
+      piece(x0, b, g, kt0, nt, base);
+      write_q(b, g);
+    }
     // Every thread runs the same pieces and the same named barriers, whether or not a
     // wait timed out (then the work is skipped), so the barriers always complete.
     for (long x = x0; x < x1; ++p) {
@@ -502,6 +534,11 @@ __global__ void __launch_bounds__(352, 1)
       mbar_arrive(smem_u32(o_drained));
       gt += nt;
       x += nt;
+      if (x < x1) {  // the next piece's queries: every S of this piece has been consumed
+        int b2, g2, kt2, nt2, base2;
+        piece(x, b2, g2, kt2, nt2, base2);
+        write_q(b2, g2);
+      }
     }
   }
   __syncwarp();
@@ -575,7 +612,7 @@ __global__ void __launch_bounds__(256) k_attn_merge_p(AttnArgs a) {
 }
 
 // tile keys and stage count per head dim
-constexpr int kTK128 = kAttnTile, kNST128 = 4;
+constexpr int kTK128 = kAttnTile, kNST128 = 3;
 constexpr int kTK64 = kAttnTile, kNST64 = 4;
 
 int attn_tc_init_attributes() {
@@ -593,10 +630,10 @@ void op_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMa
                      cudaStream_t st) {
   if (a.B > kAttnMaxB || a.pgrid < 1 || a.ptk != kAttnTile) return;  // excluded by the caller
   if (a.hd == 128)
-    k_attn_tc<128, kTK128, kNST128><<<a.pgrid, 352, Smem<128, kTK128, kNST128>::kBytes, st>>>(
+    k_attn_tc<128, kTK128, kNST128><<<a.pgrid, 320, Smem<128, kTK128, kNST128>::kBytes, st>>>(
         tmK, tmV, tmQh, tmQl, a, err);
   else
-    k_attn_tc<64, kTK64, kNST64><<<a.pgrid, 352, Smem<64, kTK64, kNST64>::kBytes, st>>>(
+    k_attn_tc<64, kTK64, kNST64><<<a.pgrid, 320, Smem<64, kTK64, kNST64>::kBytes, st>>>(
         tmK, tmV, tmQh, tmQl, a, err);
   dim3 g(a.B * 8, (a.hq + 7) / 8);
   if (a.hd == 128)

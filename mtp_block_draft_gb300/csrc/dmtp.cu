@@ -438,6 +438,8 @@ void attn_layer(dmtp_ctx* c, const LayerPlans& p, const dmtp_layer_weights& w, f
   aa.max_ctx = c->maxc;
   aa.chunk = c->attn_chunk;
   aa.nchunk = c->attn_nchunk;
+  aa.qs = c->qs;
+  aa.qs_lo = (long)c->M * c->qd;
   aa.pgrid = c->attn_grid;
   aa.ptk = kAttnTile;
   double kv_bytes = 0;
@@ -824,7 +826,7 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
     const uint64_t vrows = (uint64_t)B * c->hkv * (c->maxc / 64) * c->hd;
     int e = 0;
     auto maps = [&](CUtensorMap* mk, CUtensorMap* mv, void* K, void* V) {
-      e |= tc_make_tmap(mk, K, krows, c->hd, 64);  // 64-key tiles
+      e |= tc_make_tmap(mk, K, krows, c->hd, kAttnTile);  // one box per key tile
       e |= tc_make_tmap(mv, V, vrows, 64, c->hd);
     };
     for (int l = 0; l < c->L; ++l)

@@ -117,15 +117,17 @@ struct AttnArgs {
   int lo_fixed;        // lowest key index
   int window;          // > 0: lo = max(lo_fixed, base - window)
   int B, hq, hkv, hd, max_ctx, chunk, nchunk;  // chunk: keys per partial (absolute grid)
+  const void* qs;      // tensor-core path: queries as bf16 hi [B*8][hq][hd] ...
+  long qs_lo;          // ... and remainder at qs + qs_lo
   int pgrid;           // tensor-core path: persistent CTAs; partials [pgrid + B*hkv]
   int ptk;             // tensor-core path: keys per tile (kAttnTile)
 };
 void op_attention(int dt, const AttnArgs& a, cudaStream_t st);
 void op_attention_merge(int dt, const AttnArgs& a, cudaStream_t st);
-constexpr int kAttnTile = 64;   // keys per tile of the tensor-core attention
+constexpr int kAttnTile = 128;  // keys per tile of the tensor-core attention
 constexpr int kAttnMaxB = 1024; // sequences its in-kernel schedule handles
 // tcgen05 attention (bf16 caches, head_dim 64 or 128, 8 x GQA-group <= 64 queries);
-// tmK: K cache as [B*hkv*max_ctx, hd] box {64, 128}; tmV: transposed V cache as
+// tmK: K cache as [B*hkv*max_ctx, hd] box {64, kAttnTile}; tmV: transposed V cache as
 // blocked [B*hkv*(max_ctx/64)*hd, 64] box {64, hd}; tmQh / tmQl: the bf16 query halves as 3-D
 // [B*8][hq][hd] maps, box {64, hq/hkv, 8}. Persistent: a.pgrid CTAs split the visible key
 // tiles of all (sequence, kv head) pairs evenly; partial (CTA i, pair seg) goes to slot
