@@ -10,12 +10,14 @@
 // leaves a partial (m, l, O) for the merge kernel. Keys stream through shared memory
 // in tiles of TK keys (TMA, 128-byte swizzle, NST stages) continuously across pieces.
 // Per tile:
-//   S = Q K^T  : tcgen05 M=128, N=TK keys, K = 2*hd, A from TMEM: the fp32 queries
-//                enter as a bf16 pair [Q_hi | Q_lo] along K against [K | K] (queries in
-//                operand rows 0..QN-1), so S keeps the queries' fp32 precision. S is
+//   S = Q K^T  : tcgen05 M=128, N=TK keys, K = hd, A from TMEM: the fp32 queries enter
+//                as a bf16 pair, Q_hi in operand rows 0..63 and Q_lo in rows 64..127, so
+//                TMEM lanes r and r+64 hold Q_hi K^T and Q_lo K^T of query row r; the
+//                softmax threads of the two lanes swap a quarter of the tile through
+//                shared memory and each sums its own quarter, which keeps the queries'
+//                fp32 precision at half the MMA work of a pair along K. S is
 //                double-buffered in TMEM: the next tile's scores are computed during this
-//                tile's softmax. The queries sit in operand rows 0..63 and again in rows
-//                64..127, so TMEM lanes r and r+64 hold the same scores.
+//                tile's softmax.
 //   softmax    : warps 0-7, four threads per query row, each a quarter of the
 //                tile's keys: mask (causal rows / anchor window / segment bounds; skipped
 //                on interior tiles), exponentiate against a per-row reference max, and
@@ -28,8 +30,7 @@
 // the same factor multiplies O and the running sum l.
 // The queries, already split into bf16 halves by the RoPE kernel, live in TMEM as the
 // A operand of S (written by the softmax warps at the start of each piece), which
-// leaves the shared memory to the K/V ring: six 32 KB stages keep ~190 KB of K/V in
-// flight per SM, what the HBM latency under full load asks for.
+// leaves the shared memory to the K/V ring: three 64 KB stages.
 // Warp 8 lane 0 issues the K/V loads, warp 9 lane 0 the MMAs.
 //
 // Visibility follows the DMTP blog §6.2: target and MTP rows are causal over their
@@ -222,7 +223,8 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* pfin = mx + 1;              // a piece's last P V completed
   uint64_t* o_drained = pfin + 1;       // the 256 softmax threads read a piece's O
   uint64_t* fin = o_drained + 1;
-  uint32_t* tmem_slot = (uint32_t*)(fin + 1);
+  uint64_t* xb = fin + 1;               // the 256 softmax threads posted their swap quarter
+  uint32_t* tmem_slot = (uint32_t*)(xb + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -239,13 +241,14 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(smem_u32(pfin), 1);
     mbar_init(smem_u32(o_drained), 256);
     mbar_init(smem_u32(fin), 1);
+    mbar_init(smem_u32(xb), 256);
     fence_mbar_init();
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
-  // S buffers at columns 0 and TK, O (HD columns) after them, then Q: 2*HD bf16 per
-  // row = HD columns
-  constexpr uint32_t kTmemCols = 2 * TK + 2 * HD <= 256 ? 256 : 512;
+  // S buffers at columns 0 and TK, O (HD columns) after them, then Q: HD bf16 per lane
+  // = HD/2 columns
+  constexpr uint32_t kTmemCols = 2 * TK + HD + HD / 2 <= 256 ? 256 : 512;
   if (warp == 8) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
   tc_fence_before();
   __syncthreads();
@@ -298,8 +301,8 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after();
         uint8_t* st = stage(xg);
 #pragma unroll
-        for (int kb = 0; kb < 2 * L::kDB; ++kb) {  // [Q_hi | Q_lo] against [K | K]
-          const uint64_t dk = umma_desc_sw128(smem_u32(st + (kb % L::kDB) * L::kKBox));
+        for (int kb = 0; kb < L::kDB; ++kb) {  // [Q_hi; Q_lo] rows against K
+          const uint64_t dk = umma_desc_sw128(smem_u32(st + kb * L::kKBox));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)  // 16 k = 8 TMEM columns of Q per MMA
             umma_bf16_ta(tmem + (xg & 1) * TK, tQ + kb * 32 + kk * 8, dk + 2 * kk, id_qk,
@@ -376,17 +379,19 @@ __global__ void __launch_bounds__(320, 1)
     bool ok = true;
     int gt = 0, p = 0;
     // The queries of a piece into TMEM (A operand of S): lane lrow holds query row
-    // lrow % 64 (zeros past QN); warps 0-3 write the hi half (columns 0..HD/2-1 of the
-    // Q region), warps 4-7 the lo half. Called when no S of the previous piece is
-    // pending (the softmax warps have consumed them all).
+    // lrow % 64 (zeros past QN), the hi half in lanes 0..63 and the lo half in lanes
+    // 64..127; the warps of head-dim half hf write columns hf*HD/4.. of the lane's
+    // HD/2. Called when no S of the previous piece is pending (the softmax warps have
+    // consumed them all).
     auto write_q = [&](int b, int g) {
-      uint32_t w[HALF];
+      constexpr int NW = HD / 4;  // 32-bit columns per thread
+      uint32_t w[NW];
       if (r < QN) {
         const int s_ = r / grp, hh = r % grp;
         const bf16* src = (const bf16*)a.qs + ((long)(b * 8 + s_) * a.hq + g * grp + hh) * HD +
-                          (hf ? a.qs_lo : 0);
+                          (lrow >= 64 ? a.qs_lo : 0) + hf * (HD / 2);
 #pragma unroll
-        for (int i = 0; i < HALF; i += 4) {
+        for (int i = 0; i < NW; i += 4) {
           const uint4 u = *reinterpret_cast<const uint4*>(src + 2 * i);
           w[i] = u.x;
           w[i + 1] = u.y;
@@ -395,14 +400,14 @@ __global__ void __launch_bounds__(320, 1)
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < HALF; ++i) w[i] = 0u;
+        for (int i = 0; i < NW; ++i) w[i] = 0u;
       }
 #pragma unroll
-      for (int c16 = 0; c16 < HALF / 16; ++c16) {
+      for (int c16 = 0; c16 < NW / 16; ++c16) {
         uint32_t v[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] = w[c16 * 16 + i];
-        tmem_st16u(tQ + lane_off + hf * HALF + c16 * 16, v);
+        tmem_st16u(tQ + lane_off + hf * NW + c16 * 16, v);
       }
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
@@ -431,14 +436,32 @@ __global__ void __launch_bounds__(320, 1)
         // interior tiles need no mask: every key of the tile is visible to every row
         const bool interior =
             kt >= lo && kt + TK <= k_end && (!a.causal || kt + TK <= base + 1);
+        // The partner thread (lane lrow ^ 64, same warp group) holds the other half
+        // (hi or lo) of this row's scores: post its quarter (kq ^ 1) of this lane's half
+        // in the tile's P buffer (free until P is written, after the mx barrier), take
+        // this quarter of the partner's half back.
+        float* xch = (float*)p_buf(xg);  // [KQ][256], thread-minor
+        const int tid = threadIdx.x, ptid = (((warp & 4) | ((warp & 3) ^ 2)) << 5) | lane;
+#pragma unroll
+        for (int cc = 0; cc < KQ / 16; ++cc) {
+          float v[16];
+          tmem_ld16(tmem + (xg & 1) * TK + (kq ^ 1) * KQ + cc * 16 + lane_off, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) xch[(cc * 16 + j) * 256 + tid] = v[j];
+        }
+        mbar_arrive(smem_u32(xb));
         float sv[KQ];
 #pragma unroll
         for (int cc = 0; cc < KQ / 16; ++cc) {
           float v[16];
           tmem_ld16(tmem + (xg & 1) * TK + kq * KQ + cc * 16 + lane_off, v);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) sv[cc * 16 + j] = v[j] * scale;
+          for (int j = 0; j < 16; ++j) sv[cc * 16 + j] = v[j];
         }
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(xb), xg & 1, err));
+        if (!ok) break;
+#pragma unroll
+        for (int j = 0; j < KQ; ++j) sv[j] = (sv[j] + xch[j * 256 + ptid]) * scale;
         if (!interior) {
 #pragma unroll
           for (int j = 0; j < KQ; ++j) {
