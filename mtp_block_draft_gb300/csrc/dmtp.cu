@@ -28,6 +28,7 @@ struct Gemm {
   int N = 0, K = 0, M = 0;
   bool argmax = false;
   bool split = true;    // X is the [hi; lo] bf16 pair
+  bool swiglu = false;  // gate/up with the SwiGLU epilogue (bf16 path); N = 2F
 };
 
 struct LayerPlans {
@@ -309,6 +310,18 @@ int plan(dmtp_ctx* c, Gemm& g, const void* W, int N, int K, const void* X, int M
   return DMTP_OK;
 }
 
+// Gate/up GEMM: on the bf16 path with the SwiGLU epilogue (writes the down GEMM's
+// operand directly), on the fp32 path a plain GEMM followed by op_swiglu.
+int plan_gu(dmtp_ctx* c, Gemm& g, const void* W, int M) {
+  const int r = plan(c, g, W, 2 * c->F, c->d, c->xn, M, false);
+  if (r || c->dt != 1) return r;
+  g.swiglu = true;
+  const int mt = tc_mt(M);
+  const int ms = (mt > 128 && mt % 32 == 0) ? 2 : 1;
+  return tc_plan_swiglu(&g.tc, W, c->F, c->d, c->xn, M, c->nsm, true, ms) ? DMTP_EINVAL
+                                                                          : DMTP_OK;
+}
+
 int plan_layer(dmtp_ctx* c, LayerPlans& p, const dmtp_layer_weights& w, int kind, int M) {
   int r = 0;
   if (!w.attn_norm || !w.mlp_norm) return DMTP_EINVAL;
@@ -321,7 +334,7 @@ int plan_layer(dmtp_ctx* c, LayerPlans& p, const dmtp_layer_weights& w, int kind
     r |= plan(c, p.gb, w.gdn_wb, c->gH, c->d, c->xn, M, false);
     r |= plan(c, p.go, w.gdn_wo, c->d, c->gH * c->gdv, c->att, M, false);
   }
-  r |= plan(c, p.gu, w.wgu, 2 * c->F, c->d, c->xn, M, false);
+  r |= plan_gu(c, p.gu, w.wgu, M);
   r |= plan(c, p.down, w.wdown, c->d, c->F, c->hmid, M, false);
   return r ? DMTP_EINVAL : DMTP_OK;
 }
@@ -379,6 +392,13 @@ void gemm_argmax(dmtp_ctx* c, const Gemm& g, unsigned long long* keys, float* lo
   });
 }
 
+void gemm_swiglu(dmtp_ctx* c, const Gemm& g, void* h, long h_lo) {
+  const double bytes = ((double)g.N * g.K + (double)g.M * g.K * 2) * esz(c) +
+                       (double)g.M * (g.N / 2) * esz(c) * 2;
+  launch(c, P_GEMM, bytes, 2.0 * g.M * g.N * g.K,
+         [&] { op_gemm_tc_swiglu(g.tc, h, h_lo, c->err, c->st); });
+}
+
 void zero(dmtp_ctx* c, void* p, size_t bytes) { cudaMemsetAsync(p, 0, bytes, c->st); }
 
 // element offset of the remainder half of an operand with `mt` padded rows of `ld`
@@ -411,6 +431,20 @@ struct AttnSpec {
   int causal, lo_fixed, window;
   int mode_base;  // 1: base = kv_len at round start (target, drafter); 2: kv_len + 1 (MTP)
 };
+
+// MLP block: x += down(SwiGLU(gate/up(RMS(x)))).
+void mlp(dmtp_ctx* c, const LayerPlans& p, const dmtp_layer_weights& w, float* xr) {
+  const int M = c->M;
+  if (p.gu.swiglu) {
+    norm(c, xr, w.mlp_norm, c->xn, nullptr, nullptr, M);
+    gemm_swiglu(c, p.gu, c->hmid, lo_of(c, c->mt8, c->F));
+  } else {
+    norm(c, xr, w.mlp_norm, c->xn, nullptr, nullptr, M, RowMap(), true, c->gu, 2 * c->F);
+    gemm_acc(c, p.gu, c->gu, 2 * c->F);
+    launch(c, P_OTHER, 0, 0, [&] { op_swiglu(c->dt, c->gu, c->hmid, lo_of(c, c->mt8, c->F), M, c->F, c->st); });
+  }
+  gemm_acc(c, p.down, xr, c->d);
+}
 
 void attn_layer(dmtp_ctx* c, const LayerPlans& p, const dmtp_layer_weights& w, float* xr,
                 const AttnSpec& a, void* tap_in) {
@@ -462,10 +496,7 @@ void attn_layer(dmtp_ctx* c, const LayerPlans& p, const dmtp_layer_weights& w, f
   });
   c->launches += 1;  // partial + merge
   gemm_acc(c, p.o, xr, c->d);
-  norm(c, xr, w.mlp_norm, c->xn, nullptr, nullptr, M, RowMap(), true, c->gu, 2 * c->F);
-  gemm_acc(c, p.gu, c->gu, 2 * c->F);
-  launch(c, P_OTHER, 0, 0, [&] { op_swiglu(c->dt, c->gu, c->hmid, lo_of(c, c->mt8, c->F), M, c->F, c->st); });
-  gemm_acc(c, p.down, xr, c->d);
+  mlp(c, p, w, xr);
 }
 
 void gdn_layer(dmtp_ctx* c, int l, float* xr, void* tap_in, bool snapshots) {
@@ -495,10 +526,7 @@ void gdn_layer(dmtp_ctx* c, int l, float* xr, void* tap_in, bool snapshots) {
   const double st_bytes = (double)c->B * c->gH * c->gdv * c->gdk * 4 * (snapshots ? 9 : 2);
   launch(c, P_GDN, st_bytes, 0, [&] { op_gdn(c->dt, ga, c->st); });
   gemm_acc(c, p.go, xr, c->d);
-  norm(c, xr, w.mlp_norm, c->xn, nullptr, nullptr, M, RowMap(), true, c->gu, 2 * c->F);
-  gemm_acc(c, p.gu, c->gu, 2 * c->F);
-  launch(c, P_OTHER, 0, 0, [&] { op_swiglu(c->dt, c->gu, c->hmid, lo_of(c, c->mt8, c->F), M, c->F, c->st); });
-  gemm_acc(c, p.down, xr, c->d);
+  mlp(c, p, w, xr);
 }
 
 // target forward over the 8 rows of every sequence (tokens in rs.tok, positions pos0+s);
@@ -660,6 +688,23 @@ float time_plan(dmtp_ctx* c, const TcPlan& p, bool argmax, const void* flush,
   return best;
 }
 
+float time_swiglu(dmtp_ctx* c, const TcPlan& p, const void* flush, size_t flush_bytes,
+                  cudaEvent_t e0, cudaEvent_t e1) {
+  float best = 1e30f;
+  for (int rep = 0; rep < 3; ++rep) {
+    op_l2_flush(flush, flush_bytes, c->err, c->st);
+    cudaEventRecord(e0, c->st);
+    op_gemm_tc_swiglu(p, c->hmid, (long)c->mt8 * c->F, c->err, c->st);
+    cudaEventRecord(e1, c->st);
+    float ms = 1e30f;
+    if (cudaEventSynchronize(e1) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess)
+      return 1e30f;
+    best = std::min(best, ms);
+  }
+  return best;
+}
+
 int autotune(dmtp_ctx* c, const void* flush, size_t flush_bytes) {
   if (c->dt != 1) return DMTP_OK;
   std::vector<Gemm*> all;
@@ -683,6 +728,23 @@ int autotune(dmtp_ctx* c, const void* flush, size_t flush_bytes) {
   int rc = DMTP_OK;
   for (Gemm* g : all) {
     if (!g->W) continue;
+    if (g->swiglu) {  // tile shape: one or two token halves; no K split
+      TcPlan best_p = g->tc;
+      float best_t = time_swiglu(c, g->tc, flush, flush_bytes, e0, e1);
+      for (int ms = 1; ms <= 2; ++ms) {
+        TcPlan p;
+        if (ms == g->tc.msplit ||
+            tc_plan_swiglu(&p, g->W, c->F, g->K, g->X, g->M, c->nsm, g->split, ms))
+          continue;
+        const float t = time_swiglu(c, p, flush, flush_bytes, e0, e1);
+        if (t < best_t) {
+          best_t = t;
+          best_p = p;
+        }
+      }
+      g->tc = best_p;
+      continue;
+    }
     if (!g->argmax && (size_t)g->M * g->N > scratch) continue;  // keeps the default shape
     const TuneKey key{g->N, g->K, g->M, g->split, g->argmax};
     const TuneChoice* hit = nullptr;

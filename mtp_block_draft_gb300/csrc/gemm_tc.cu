@@ -56,8 +56,25 @@ struct TcArgs {
   unsigned long long* keys;
   float* logits;
   long ldl;
+  bf16* h;         // EPI 2: SwiGLU output [M][F] (hi), remainder at h + h_lo
+  long h_lo;
+  int F;           // EPI 2: gate rows 0..F-1, up rows F..2F-1 of W
   unsigned* err;
 };
+
+// 16 accumulator columns of this warp's lanes at taddr, plus (merged) the lo columns
+// mct further: both loads in flight before one wait.
+template <bool MERGED>
+__device__ __forceinline__ void acc_ld16(uint32_t taddr, int mct, float (&v)[16]) {
+  uint32_t rv[16], rw[16];
+  tmem_ld16_raw(taddr, rv);
+  if (MERGED) tmem_ld16_raw(taddr + mct, rw);
+  tmem_wait_ld16(rv);
+  if (MERGED) reg_fence16(rw);
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    v[j] = MERGED ? __uint_as_float(rv[j]) + __uint_as_float(rw[j]) : __uint_as_float(rv[j]);
+}
 
 // Column of a 16-column block that lane `lane` holds after warp_colmax16.
 __device__ __forceinline__ int col16(int lane) {
@@ -88,9 +105,11 @@ __host__ __device__ inline uint32_t tmem_cols_for(int cols) {
   return c;
 }
 
-// EPI 0: atomic add into out, 1: argmax keys (+ logits). WIDE, NMMA (MMAs per k step
-// and weight half) and MERGED are compile-time copies of a.wide, (merged ? 1 : nx) and
-// a.merged, so that the issue loop and the epilogue have no runtime trip counts.
+// EPI 0: atomic add into out, 1: argmax keys (+ logits), 2: SwiGLU (WIDE = 2, no K
+// split: weight half 0 = gate rows n0.., half 1 = the matching up rows F + n0.., and the
+// epilogue writes silu(g) * u as the next GEMM's bf16 pair). WIDE, NMMA (MMAs per k
+// step and weight half) and MERGED are compile-time copies of a.wide, (merged ? 1 : nx)
+// and a.merged, so that the issue loop and the epilogue have no runtime trip counts.
 template <int EPI, int WIDE, int NMMA, bool MERGED>
 __global__ void __launch_bounds__(128, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
@@ -113,7 +132,7 @@ __global__ void __launch_bounds__(128, 1)
   // grid: (token halves, weight tiles, K splits); CTAs sharing a weight tile are
   // adjacent in launch order, so its second read comes from L2
   const int mrow0 = blockIdx.x * a.mct;
-  const int n0 = blockIdx.y * kHalfN * WIDE;
+  const int n0 = blockIdx.y * kHalfN * (EPI == 2 ? 1 : WIDE);
   const int nkb = a.K / kBlockK;
   const int kb0 = (int)((long)blockIdx.z * nkb / gridDim.z);
   const int kb1 = (int)((long)(blockIdx.z + 1) * nkb / gridDim.z);
@@ -144,7 +163,13 @@ __global__ void __launch_bounds__(128, 1)
       const uint32_t ph = (issued / S) & 1;
       if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, a.err)) break;
       mbar_expect_tx(smem_u32(&full[s]), wbytes + xbytes);
-      tma_load_2d(smem_u32(sW + s * wbytes), &tmW, kb * kBlockK, n0, smem_u32(&full[s]), pw);
+      if (EPI == 2) {  // gate rows n0.. and up rows F + n0.., one 128-row box each
+        tma_load_2d(smem_u32(sW + s * wbytes), &tmW, kb * kBlockK, n0, smem_u32(&full[s]), pw);
+        tma_load_2d(smem_u32(sW + s * wbytes + kHalfBytes), &tmW, kb * kBlockK, a.F + n0,
+                    smem_u32(&full[s]), pw);
+      } else {
+        tma_load_2d(smem_u32(sW + s * wbytes), &tmW, kb * kBlockK, n0, smem_u32(&full[s]), pw);
+      }
       // one box of [hi; lo] rows, or hi rows then (split) remainder rows
       for (int j = 0; j < a.nx; ++j)
         tma_load_2d(smem_u32(sX + s * xbytes + j * a.xbox * kBlockK * 2), &tmX, kb * kBlockK,
@@ -197,19 +222,48 @@ __global__ void __launch_bounds__(128, 1)
         const uint32_t tbase = tmem + h * a.acc_cols + ((uint32_t)(warp * 32) << 16);
         for (int c = 0; c < a.mct; c += 16) {
           float v[16];
-          tmem_ld16(tbase + c, v);
-          if (MERGED) {
-            float w[16];
-            tmem_ld16(tbase + a.mct + c, w);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] += w[j];
-          }
+          acc_ld16<MERGED>(tbase + c, a.mct, v);
           if (n < a.N) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const int m = mrow0 + c + j;
               if (m < a.M) atomicAdd(&a.out[(long)m * a.ldo + n], v[j]);
             }
+          }
+        }
+      }
+    }
+  } else if (EPI == 2) {
+    if (ok) {
+      const int n = n0 + warp * 32 + lane;  // feature
+      const uint32_t tg = tmem + ((uint32_t)(warp * 32) << 16);
+      const uint32_t tu = tg + a.acc_cols;
+      for (int c = 0; c < a.mct; c += 16) {
+        uint32_t rg[16], ru[16], rgl[16], rul[16];
+        tmem_ld16_raw(tg + c, rg);
+        tmem_ld16_raw(tu + c, ru);
+        if (MERGED) {
+          tmem_ld16_raw(tg + a.mct + c, rgl);
+          tmem_ld16_raw(tu + a.mct + c, rul);
+        }
+        tmem_wait_ld16(rg);
+        reg_fence16(ru);
+        if (MERGED) {
+          reg_fence16(rgl);
+          reg_fence16(rul);
+        }
+        if (n < a.F) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int m = mrow0 + c + j;
+            float g = __uint_as_float(rg[j]), u = __uint_as_float(ru[j]);
+            if (MERGED) {
+              g += __uint_as_float(rgl[j]);
+              u += __uint_as_float(rul[j]);
+            }
+            // silu(g) u = g sigmoid(g) u
+            if (m < a.M)
+              store_act(a.h + (long)m * a.F + n, a.h_lo, g * __frcp_rn(1.f + __expf(-g)) * u);
           }
         }
       }
@@ -223,13 +277,7 @@ __global__ void __launch_bounds__(128, 1)
         const uint32_t tbase = tmem + h * a.acc_cols + ((uint32_t)(warp * 32) << 16);
         for (int c = 0; c < a.mct; c += 16) {
           float v[16];
-          tmem_ld16(tbase + c, v);
-          if (MERGED) {
-            float w[16];
-            tmem_ld16(tbase + a.mct + c, w);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] += w[j];
-          }
+          acc_ld16<MERGED>(tbase + c, a.mct, v);
           if (a.logits && n < a.N) {  // debug copy of the scores
 #pragma unroll
             for (int j = 0; j < 16; ++j)
@@ -337,6 +385,8 @@ int tc_plan_shape(TcPlan* p, const void* W, int N, int K, const void* X, int M, 
   p->N = N;
   p->K = K;
   p->M = M;
+  p->swiglu = 0;
+  p->F = 0;
   p->MT = tc_mt(M);
   p->split = split ? 1 : 0;
   p->wide = wide;
@@ -384,6 +434,16 @@ int tc_plan_shape(TcPlan* p, const void* W, int N, int K, const void* X, int M, 
   return r;
 }
 
+int tc_plan_swiglu(TcPlan* p, const void* W, int F, int K, const void* X, int M, int nsm,
+                   bool split, int msplit) {
+  int r = tc_plan_shape(p, W, 2 * F, K, X, M, nsm, false, split, 2, msplit, 1);
+  if (r) return r;
+  p->swiglu = 1;
+  p->F = F;
+  // one 128-row box per weight half (gate and up rows are F apart)
+  return tc_make_tmap(&p->tmW, W, (uint64_t)2 * F, (uint64_t)K, (uint32_t)kHalfN);
+}
+
 int tc_plan(TcPlan* p, const void* W, int N, int K, const void* X, int M, int nsm, bool argmax,
             bool split) {
   return tc_plan_shape(p, W, N, K, X, M, nsm, argmax, split, 1, 1, 0);
@@ -393,6 +453,10 @@ int tc_plan(TcPlan* p, const void* W, int N, int K, const void* X, int M, int ns
 template <int EPI>
 static void (*kernel_for(const TcPlan& p))(const CUtensorMap, const CUtensorMap, TcArgs) {
   const int nmma = p.merged ? 1 : p.nx;
+  if (EPI == 2) {
+    if (p.merged) return k_gemm_tc<2, 2, 1, true>;
+    return nmma == 1 ? k_gemm_tc<2, 2, 1, false> : k_gemm_tc<2, 2, 2, false>;
+  }
   if (p.wide == 1) {
     if (p.merged) return k_gemm_tc<EPI, 1, 1, true>;
     return nmma == 1 ? k_gemm_tc<EPI, 1, 1, false> : k_gemm_tc<EPI, 1, 2, false>;
@@ -407,7 +471,8 @@ int tc_init_attributes() {
       k_gemm_tc<0, 1, 1, true>,  k_gemm_tc<0, 1, 1, false>, k_gemm_tc<0, 1, 2, false>,
       k_gemm_tc<0, 2, 1, true>,  k_gemm_tc<0, 2, 1, false>, k_gemm_tc<0, 2, 2, false>,
       k_gemm_tc<1, 1, 1, true>,  k_gemm_tc<1, 1, 1, false>, k_gemm_tc<1, 1, 2, false>,
-      k_gemm_tc<1, 2, 1, true>,  k_gemm_tc<1, 2, 1, false>, k_gemm_tc<1, 2, 2, false>};
+      k_gemm_tc<1, 2, 1, true>,  k_gemm_tc<1, 2, 1, false>, k_gemm_tc<1, 2, 2, false>,
+      k_gemm_tc<2, 2, 1, true>,  k_gemm_tc<2, 2, 1, false>, k_gemm_tc<2, 2, 2, false>};
   for (auto k : ks)
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
         cudaSuccess)
@@ -415,9 +480,18 @@ int tc_init_attributes() {
   return 0;
 }
 
+void op_gemm_tc_swiglu(const TcPlan& p, void* h, long h_lo, unsigned* err, cudaStream_t st) {
+  TcArgs a{p.N,  p.K,      p.M,        p.MT,    p.stages, p.wide, p.mct,   p.split,
+           p.xbox, p.nx,   p.merged,   p.acc_cols, nullptr, 0, nullptr, nullptr,
+           0,    (bf16*)h, h_lo,       p.F,     err};
+  dim3 grid(p.msplit, (p.F + kHalfN - 1) / kHalfN, 1);
+  kernel_for<2>(p)<<<grid, 128, p.smem, st>>>(p.tmW, p.tmX, a);
+}
+
 void op_gemm_tc_acc(const TcPlan& p, float* out, int ldo, unsigned* err, cudaStream_t st) {
   TcArgs a{p.N,     p.K,  p.M,     p.MT,       p.stages, p.wide, p.mct, p.split, p.xbox,
-           p.nx,    p.merged, p.acc_cols, out, ldo,     nullptr, nullptr, 0,  err};
+           p.nx,    p.merged, p.acc_cols, out, ldo,     nullptr, nullptr, 0,  nullptr, 0, 0,
+           err};
   dim3 grid(p.msplit, (p.N + kHalfN * p.wide - 1) / (kHalfN * p.wide), p.splits);
   kernel_for<0>(p)<<<grid, 128, p.smem, st>>>(p.tmW, p.tmX, a);
 }
@@ -425,7 +499,8 @@ void op_gemm_tc_acc(const TcPlan& p, float* out, int ldo, unsigned* err, cudaStr
 void op_gemm_tc_argmax(const TcPlan& p, unsigned long long* keys, float* logits, long ldl,
                        unsigned* err, cudaStream_t st) {
   TcArgs a{p.N,  p.K,      p.M,        p.MT,    p.stages, p.wide, p.mct, p.split, p.xbox,
-           p.nx, p.merged, p.acc_cols, nullptr, 0,        keys,   logits, ldl,  err};
+           p.nx, p.merged, p.acc_cols, nullptr, 0,        keys,   logits, ldl,  nullptr, 0, 0,
+           err};
   dim3 grid(p.msplit, (p.N + kHalfN * p.wide - 1) / (kHalfN * p.wide), 1);
   kernel_for<1>(p)<<<grid, 128, p.smem, st>>>(p.tmW, p.tmX, a);
 }

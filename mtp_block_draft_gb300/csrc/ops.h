@@ -156,6 +156,7 @@ struct TcPlan {
   int xbox, nx;   // X rows per TMA load, loads per stage
   int merged;     // hi and lo in one MMA of 2*mct columns
   int acc_cols;   // TMEM columns per accumulator
+  int swiglu, F;  // SwiGLU epilogue: W = [gate; up] of F rows each
   size_t smem;
 };
 // Padded token rows of an M-row operand (multiple of 16, >= 16).
@@ -170,6 +171,12 @@ int tc_make_tmap3(CUtensorMap* tm, const void* base, uint64_t d0, uint64_t d1, u
 // holds 2*tc_mt(M) rows, the bf16 high halves then the low halves (X = hi + lo).
 int tc_plan(TcPlan* p, const void* W, int N, int K, const void* X, int M, int nsm,
             bool argmax, bool split);
+// Gate/up GEMM with the SwiGLU epilogue: W = [gate; up] ([2F, K]), each CTA pairs gate
+// rows n0.. with up rows F + n0.. (two accumulators) and writes h = silu(g) * u, a bf16
+// pair [M][F] (remainder at h + h_lo), so no fp32 output or separate SwiGLU pass.
+int tc_plan_swiglu(TcPlan* p, const void* W, int F, int K, const void* X, int M, int nsm,
+                   bool split, int msplit);
+void op_gemm_tc_swiglu(const TcPlan& p, void* h, long h_lo, unsigned* err, cudaStream_t st);
 // tc_plan with the tile shape given: wide (1, 2), msplit (1, 2) and splits (<= 0: chosen).
 int tc_plan_shape(TcPlan* p, const void* W, int N, int K, const void* X, int M, int nsm,
                   bool argmax, bool split, int wide, int msplit, int splits);
