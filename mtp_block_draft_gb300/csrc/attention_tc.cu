@@ -219,12 +219,10 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* q_full = s_full + 2;        // the 256 softmax threads wrote a piece's queries
   uint64_t* p_full = q_full + 1;        // the 256 softmax threads wrote this tile's P
   uint64_t* o_full = p_full + 1;        // one commit per tile's P V
-  uint64_t* mx = o_full + 1;            // all quarters of every row posted their maxima
-  uint64_t* pfin = mx + 1;              // a piece's last P V completed
+  uint64_t* pfin = o_full + 1;          // a piece's last P V completed
   uint64_t* o_drained = pfin + 1;       // the 256 softmax threads read a piece's O
   uint64_t* fin = o_drained + 1;
-  uint64_t* xb = fin + 1;               // the 256 softmax threads posted their swap quarter
-  uint32_t* tmem_slot = (uint32_t*)(xb + 1);
+  uint32_t* tmem_slot = (uint32_t*)(fin + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -237,11 +235,9 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(smem_u32(q_full), 256);
     mbar_init(smem_u32(p_full), 256);
     mbar_init(smem_u32(o_full), 1);
-    mbar_init(smem_u32(mx), 256);
     mbar_init(smem_u32(pfin), 1);
     mbar_init(smem_u32(o_drained), 256);
     mbar_init(smem_u32(fin), 1);
-    mbar_init(smem_u32(xb), 256);
     fence_mbar_init();
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
@@ -426,11 +422,14 @@ __global__ void __launch_bounds__(320, 1)
       const int lo = vis_lo(a, base), k_end = base + 8;
       const int row_hi = a.causal ? base + srow : base + 7;
       float m = -INFINITY, l = 0.f;  // reference max and running sum, log2 units
-      for (int t = 0; t < nt && ok; ++t) {
+      // Every iteration runs both named barriers (bar 3: swap posted, bar 4: maxima
+      // posted) on every thread, whether or not a wait timed out, so they complete.
+      for (int t = 0; t < nt; ++t) {
         const int xg = gt + t;
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[xg & 1]), (xg >> 1) & 1, err));
-        if (!ok) break;
-        tc_fence_after();
+        if (ok) {
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[xg & 1]), (xg >> 1) & 1, err));
+          tc_fence_after();
+        }
         const int kt = (kt0 + t) * TK;
         const int key0 = kt + kq * KQ;
         // interior tiles need no mask: every key of the tile is visible to every row
@@ -438,81 +437,84 @@ __global__ void __launch_bounds__(320, 1)
             kt >= lo && kt + TK <= k_end && (!a.causal || kt + TK <= base + 1);
         // The partner thread (lane lrow ^ 64, same warp group) holds the other half
         // (hi or lo) of this row's scores: post its quarter (kq ^ 1) of this lane's half
-        // in the tile's P buffer (free until P is written, after the mx barrier), take
-        // this quarter of the partner's half back.
+        // in the tile's P buffer (free until P is written, after barrier 4), take this
+        // quarter of the partner's half back.
         float* xch = (float*)p_buf(xg);  // [KQ][256], thread-minor
         const int tid = threadIdx.x, ptid = (((warp & 4) | ((warp & 3) ^ 2)) << 5) | lane;
-#pragma unroll
-        for (int cc = 0; cc < KQ / 16; ++cc) {
-          float v[16];
-          tmem_ld16(tmem + (xg & 1) * TK + (kq ^ 1) * KQ + cc * 16 + lane_off, v);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) xch[(cc * 16 + j) * 256 + tid] = v[j];
-        }
-        mbar_arrive(smem_u32(xb));
         float sv[KQ];
+        if (ok) {
 #pragma unroll
-        for (int cc = 0; cc < KQ / 16; ++cc) {
-          float v[16];
-          tmem_ld16(tmem + (xg & 1) * TK + kq * KQ + cc * 16 + lane_off, v);
+          for (int cc = 0; cc < KQ / 16; ++cc) {
+            float v[16];
+            tmem_ld16(tmem + (xg & 1) * TK + (kq ^ 1) * KQ + cc * 16 + lane_off, v);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) sv[cc * 16 + j] = v[j];
-        }
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(xb), xg & 1, err));
-        if (!ok) break;
+            for (int j = 0; j < 16; ++j) xch[(cc * 16 + j) * 256 + tid] = v[j];
+          }
 #pragma unroll
-        for (int j = 0; j < KQ; ++j) sv[j] = (sv[j] + xch[j * 256 + ptid]) * scale;
-        if (!interior) {
+          for (int cc = 0; cc < KQ / 16; ++cc) {
+            float v[16];
+            tmem_ld16(tmem + (xg & 1) * TK + kq * KQ + cc * 16 + lane_off, v);
 #pragma unroll
-          for (int j = 0; j < KQ; ++j) {
-            const int key = key0 + j;
-            if (!(key >= lo && key < k_end && key <= row_hi)) sv[j] = -INFINITY;
+            for (int j = 0; j < 16; ++j) sv[cc * 16 + j] = v[j];
           }
         }
-        float mt = sv[0];
-#pragma unroll
-        for (int j = 1; j < KQ; ++j) mt = fmaxf(mt, sv[j]);
+        asm volatile("bar.sync 3, 256;" ::: "memory");
         float* smx = sMax + (xg & 1) * 256;
-        smx[kq * 64 + r] = mt;
-        mbar_arrive(smem_u32(mx));
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(mx), xg & 1, err));
-        if (!ok) break;
-        mt = fmaxf(fmaxf(smx[r], smx[64 + r]), fmaxf(smx[128 + r], smx[192 + r]));
-        // reference max: set on the first visible scores, moved only past 2^11
-        float corr = 1.f;
-        if (mt > -INFINITY && (m == -INFINITY || mt > m + 11.f)) {
-          corr = (m == -INFINITY) ? 1.f : exp2f(m - mt);
-          m = mt;
-        }
-        // a rescale of O waits for the previous tile's P V (s_full of this tile implies
-        // every P V before it has completed, so o_full is at most one phase behind)
-        if (t > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(o_full), (xg - 1) & 1, err));
-          if (!ok) break;
-          tc_fence_after();
-          tmem_scale(tOw, HALF, corr);
-        }
-        l *= corr;
-        const float mu = (m == -INFINITY) ? 0.f : m;
-        uint8_t* pb_ = p_buf(xg) + pblk * kBlk;
+        if (ok) {
 #pragma unroll
-        for (int cc = 0; cc < KQ / 8; ++cc) {
-          uint32_t ph[4], pl[4];
+          for (int j = 0; j < KQ; ++j) sv[j] = (sv[j] + xch[j * 256 + ptid]) * scale;
+          if (!interior) {
 #pragma unroll
-          for (int j = 0; j < 8; j += 2) {
-            const float p0 = exp2f(sv[cc * 8 + j] - mu), p1 = exp2f(sv[cc * 8 + j + 1] - mu);
-            l += p0 + p1;
-            const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-            const __nv_bfloat162 pr =
-                __floats2bfloat162_rn(p0 - __low2float(pb), p1 - __high2float(pb));
-            ph[j / 2] = *reinterpret_cast<const uint32_t*>(&pb);
-            pl[j / 2] = *reinterpret_cast<const uint32_t*>(&pr);
+            for (int j = 0; j < KQ; ++j) {
+              const int key = key0 + j;
+              if (!(key >= lo && key < k_end && key <= row_hi)) sv[j] = -INFINITY;
+            }
           }
-          *(uint4*)(pb_ + sw128(r, pch + cc)) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-          *(uint4*)(pb_ + sw128(r + 64, pch + cc)) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+          float mt = sv[0];
+#pragma unroll
+          for (int j = 1; j < KQ; ++j) mt = fmaxf(mt, sv[j]);
+          smx[kq * 64 + r] = mt;
         }
-        fence_proxy_async();
-        tc_fence_before();
+        asm volatile("bar.sync 4, 256;" ::: "memory");
+        if (ok) {
+          const float mt = fmaxf(fmaxf(smx[r], smx[64 + r]), fmaxf(smx[128 + r], smx[192 + r]));
+          // reference max: set on the first visible scores, moved only past 2^11
+          float corr = 1.f;
+          if (mt > -INFINITY && (m == -INFINITY || mt > m + 11.f)) {
+            corr = (m == -INFINITY) ? 1.f : exp2f(m - mt);
+            m = mt;
+          }
+          // a rescale of O waits for the previous tile's P V (s_full of this tile implies
+          // every P V before it has completed, so o_full is at most one phase behind)
+          if (t > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
+            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(o_full), (xg - 1) & 1, err));
+            if (ok) {
+              tc_fence_after();
+              tmem_scale(tOw, HALF, corr);
+            }
+          }
+          l *= corr;
+          const float mu = (m == -INFINITY) ? 0.f : m;
+          uint8_t* pb_ = p_buf(xg) + pblk * kBlk;
+#pragma unroll
+          for (int cc = 0; cc < KQ / 8; ++cc) {
+            uint32_t ph[4], pl[4];
+#pragma unroll
+            for (int j = 0; j < 8; j += 2) {
+              const float p0 = exp2f(sv[cc * 8 + j] - mu), p1 = exp2f(sv[cc * 8 + j + 1] - mu);
+              l += p0 + p1;
+              const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+              const __nv_bfloat162 pr =
+                  __floats2bfloat162_rn(p0 - __low2float(pb), p1 - __high2float(pb));
+              ph[j / 2] = *reinterpret_cast<const uint32_t*>(&pb);
+              pl[j / 2] = *reinterpret_cast<const uint32_t*>(&pr);
+            }
+            *(uint4*)(pb_ + sw128(r, pch + cc)) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+            *(uint4*)(pb_ + sw128(r + 64, pch + cc)) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+          }
+          fence_proxy_async();
+          tc_fence_before();
+        }
         mbar_arrive(smem_u32(p_full));
       }
       // ---- end of the piece: O once its last P V completed ----
