@@ -439,30 +439,48 @@ __global__ void __launch_bounds__(320, 1)
         // (hi or lo) of this row's scores: post its quarter (kq ^ 1) of this lane's half
         // in the tile's P buffer (free until P is written, after barrier 4), take this
         // quarter of the partner's half back.
-        float* xch = (float*)p_buf(xg);  // [KQ][256], thread-minor
+        float4* xch = (float4*)p_buf(xg);  // [KQ/4][256] float4, thread-minor
         const int tid = threadIdx.x, ptid = (((warp & 4) | ((warp & 3) ^ 2)) << 5) | lane;
         float sv[KQ];
         if (ok) {
+          static_assert(KQ == 32, "the swap loads two 16-column blocks per quarter");
+          // all four loads in flight before one wait
+          uint32_t q0[16], q1[16], o0[16], o1[16];
+          const uint32_t ts = tmem + (xg & 1) * TK + lane_off;
+          tmem_ld16_raw(ts + (kq ^ 1) * KQ, q0);
+          tmem_ld16_raw(ts + (kq ^ 1) * KQ + 16, q1);
+          tmem_ld16_raw(ts + kq * KQ, o0);
+          tmem_ld16_raw(ts + kq * KQ + 16, o1);
+          tmem_wait_ld16(q0);
+          reg_fence16(q1);
+          reg_fence16(o0);
+          reg_fence16(o1);
 #pragma unroll
-          for (int cc = 0; cc < KQ / 16; ++cc) {
-            float v[16];
-            tmem_ld16(tmem + (xg & 1) * TK + (kq ^ 1) * KQ + cc * 16 + lane_off, v);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) xch[(cc * 16 + j) * 256 + tid] = v[j];
+          for (int j = 0; j < 16; j += 4) {
+            xch[(j / 4) * 256 + tid] =
+                make_float4(__uint_as_float(q0[j]), __uint_as_float(q0[j + 1]),
+                            __uint_as_float(q0[j + 2]), __uint_as_float(q0[j + 3]));
+            xch[(4 + j / 4) * 256 + tid] =
+                make_float4(__uint_as_float(q1[j]), __uint_as_float(q1[j + 1]),
+                            __uint_as_float(q1[j + 2]), __uint_as_float(q1[j + 3]));
           }
 #pragma unroll
-          for (int cc = 0; cc < KQ / 16; ++cc) {
-            float v[16];
-            tmem_ld16(tmem + (xg & 1) * TK + kq * KQ + cc * 16 + lane_off, v);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) sv[cc * 16 + j] = v[j];
+          for (int j = 0; j < 16; ++j) {
+            sv[j] = __uint_as_float(o0[j]);
+            sv[16 + j] = __uint_as_float(o1[j]);
           }
         }
         asm volatile("bar.sync 3, 256;" ::: "memory");
         float* smx = sMax + (xg & 1) * 256;
         if (ok) {
 #pragma unroll
-          for (int j = 0; j < KQ; ++j) sv[j] = (sv[j] + xch[j * 256 + ptid]) * scale;
+          for (int j = 0; j < KQ; j += 4) {
+            const float4 o = xch[(j / 4) * 256 + ptid];
+            sv[j] = (sv[j] + o.x) * scale;
+            sv[j + 1] = (sv[j + 1] + o.y) * scale;
+            sv[j + 2] = (sv[j + 2] + o.z) * scale;
+            sv[j + 3] = (sv[j + 3] + o.w) * scale;
+          }
           if (!interior) {
 #pragma unroll
             for (int j = 0; j < KQ; ++j) {
