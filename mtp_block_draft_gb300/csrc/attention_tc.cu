@@ -274,12 +274,9 @@ __global__ void __launch_bounds__(320, 1)
           mbar_expect_tx(full, L::kStage);
           const int key0 = (kt0 + t) * TK;
           uint8_t* st = stage(gt);
-          for (int hb = 0; hb < L::kDB; ++hb)
-            tma_load_2d(smem_u32(st + hb * L::kKBox), &tmK, hb * 64, (int)(krow0 + key0), full,
-                        pol);
-          for (int kb = 0; kb < TK / 64; ++kb)
-            tma_load_2d(smem_u32(st + L::kKTile + kb * L::kVBox), &tmV, 0,
-                        (int)((vblk0 + key0 / 64 + kb) * HD), full, pol);
+          // K: the tile's keys x all head-dim slabs; V^T: its 64-key blocks; one request each
+          tma_load_3d(smem_u32(st), &tmK, 0, (int)(krow0 + key0), 0, full, pol);
+          tma_load_3d(smem_u32(st + L::kKTile), &tmV, 0, 0, (int)(vblk0 + key0 / 64), full, pol);
         }
         x += nt;
       }

@@ -883,13 +883,15 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
     return DMTP_ECUDA;
   }
   if (c->attn_tc) {
-    // K: [B*hkv*max_ctx, hd]; V^T blocked by 64 keys: [B*hkv*(max_ctx/64)*hd, 64]
+    // K: [B*hkv*max_ctx][hd]; V^T blocked by 64 keys: [B*hkv*(max_ctx/64)][hd][64]; each
+    // key tile of either is one TMA request (a 3-D box over its 64-wide slabs)
     const uint64_t krows = (uint64_t)B * c->hkv * c->maxc;
-    const uint64_t vrows = (uint64_t)B * c->hkv * (c->maxc / 64) * c->hd;
+    const uint64_t vblocks = (uint64_t)B * c->hkv * (c->maxc / 64);
+    const uint64_t hd = c->hd;
     int e = 0;
     auto maps = [&](CUtensorMap* mk, CUtensorMap* mv, void* K, void* V) {
-      e |= tc_make_tmap(mk, K, krows, c->hd, kAttnTile);  // one box per key tile
-      e |= tc_make_tmap(mv, V, vrows, 64, c->hd);
+      e |= tc_make_tmap3s(mk, K, 64, krows, hd / 64, hd * 2, 128, kAttnTile, (uint32_t)(hd / 64));
+      e |= tc_make_tmap3s(mv, V, 64, hd, vblocks, 128, hd * 128, (uint32_t)hd, kAttnTile / 64);
     };
     for (int l = 0; l < c->L; ++l)
       if (c->tK[l]) maps(&c->tmK[l], &c->tmV[l], c->tK[l], c->tV[l]);

@@ -366,6 +366,21 @@ int tc_make_tmap3(CUtensorMap* tm, const void* base, uint64_t d0, uint64_t d1, u
   return r == CUDA_SUCCESS ? 0 : -3;
 }
 
+int tc_make_tmap3s(CUtensorMap* tm, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                   uint64_t s1, uint64_t s2, uint32_t b1, uint32_t b2) {
+  PFN_encodeTiled_t enc = get_encode();
+  if (!enc) return -1;
+  if (((uintptr_t)base & 15) || (d0 * 2) % 16 || s1 % 16 || s2 % 16) return -2;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {s1, s2};
+  cuuint32_t box[3] = {(cuuint32_t)kBlockK, b1, b2};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                   strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -3;
+}
+
 static size_t smem_bytes(int wide, int mct, int xrows, int stages, bool argmax) {
   size_t b = 1024 + (size_t)stages * (wide * kHalfBytes + (size_t)xrows * kBlockK * 2);
   b += (2 * stages + 2) * 8;

@@ -127,8 +127,10 @@ void op_attention_merge(int dt, const AttnArgs& a, cudaStream_t st);
 constexpr int kAttnTile = 128;  // keys per tile of the tensor-core attention
 constexpr int kAttnMaxB = 1024; // sequences its in-kernel schedule handles
 // tcgen05 attention (bf16 caches, head_dim 64 or 128, 8 x GQA-group <= 64 queries);
-// tmK: K cache as [B*hkv*max_ctx, hd] box {64, kAttnTile}; tmV: transposed V cache as
-// blocked [B*hkv*(max_ctx/64)*hd, 64] box {64, hd}; tmQh / tmQl: the bf16 query halves as 3-D
+// tmK: K cache as 3-D {64 dims, B*hkv*max_ctx keys (stride hd*2 B), hd/64 blocks (stride
+// 128 B)}, box {64, kAttnTile, hd/64}; tmV: transposed V cache blocked by 64 keys as 3-D
+// {64 keys, hd rows (stride 128 B), B*hkv*max_ctx/64 blocks (stride hd*128 B)}, box
+// {64, hd, kAttnTile/64}: one request per tile for each; tmQh / tmQl: the bf16 query halves as 3-D
 // [B*8][hq][hd] maps, box {64, hq/hkv, 8}. Persistent: a.pgrid CTAs split the visible key
 // tiles of all (sequence, kv head) pairs evenly; partial (CTA i, pair seg) goes to slot
 // i + seg of part_o / part_ml (pgrid + B*hkv slots); then merges into out.
@@ -167,6 +169,10 @@ int tc_make_tmap(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols
 // 3-D bf16 tensor [d2][d1][d0] (d0 innermost), box {64, b1, b2}, 128-B swizzle.
 int tc_make_tmap3(CUtensorMap* tm, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                   uint32_t b1, uint32_t b2);
+// 3-D bf16 view with explicit byte strides s1 (dim 1) and s2 (dim 2), box {64, b1, b2},
+// 128-B swizzle: one TMA request moves b2 slabs of b1 rows x 128 B.
+int tc_make_tmap3s(CUtensorMap* tm, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                   uint64_t s1, uint64_t s2, uint32_t b1, uint32_t b2);
 // Builds the tensor maps and launch shape for out[M,N] = X[M,K] . W[N,K]^T. split: X
 // holds 2*tc_mt(M) rows, the bf16 high halves then the low halves (X = hi + lo).
 int tc_plan(TcPlan* p, const void* W, int N, int K, const void* X, int M, int nsm,
