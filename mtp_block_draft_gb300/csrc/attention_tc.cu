@@ -101,14 +101,6 @@ __device__ __forceinline__ void tmem_scale(uint32_t taddr, int n, float f) {
     tmem_st16(taddr + cc, v);
   }
 }
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm, int x, int y,
-                                            int z, uint32_t bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-      "l"((uint64_t)tm), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
-      : "memory");
-}
 
 
 // First visible key of a sequence whose block rows start at `base`; the last is base+7.

@@ -48,7 +48,8 @@ struct TcArgs {
   int wide;        // weight halves of 128 rows per CTA (1 or 2), one accumulator each
   int mct;         // token rows per CTA (MT, or MT / 2 with two token halves)
   int split;       // 1: X holds [hi; lo] halves of MT rows each
-  int xbox, nx;    // X rows per TMA load, loads per stage
+  int xbox, nx;    // X rows per box, boxes per stage
+  int x3d;         // the nx boxes (hi rows, lo rows) come as one 3-D request
   int merged;      // split with hi and lo adjacent in shared memory: one MMA of 2*mct columns
   int acc_cols;    // TMEM columns per accumulator
   float* out;
@@ -170,10 +171,15 @@ __global__ void __launch_bounds__(128, 1)
       } else {
         tma_load_2d(smem_u32(sW + s * wbytes), &tmW, kb * kBlockK, n0, smem_u32(&full[s]), pw);
       }
-      // one box of [hi; lo] rows, or hi rows then (split) remainder rows
-      for (int j = 0; j < a.nx; ++j)
-        tma_load_2d(smem_u32(sX + s * xbytes + j * a.xbox * kBlockK * 2), &tmX, kb * kBlockK,
-                    j * a.MT + mrow0, smem_u32(&full[s]), px);
+      // one box of [hi; lo] rows, or hi rows then (split) remainder rows: one 3-D
+      // request over both halves, or a request per half
+      if (a.x3d)
+        tma_load_3d(smem_u32(sX + s * xbytes), &tmX, kb * kBlockK, mrow0, 0, smem_u32(&full[s]),
+                    px);
+      else
+        for (int j = 0; j < a.nx; ++j)
+          tma_load_2d(smem_u32(sX + s * xbytes + j * a.xbox * kBlockK * 2), &tmX, kb * kBlockK,
+                      j * a.MT + mrow0, smem_u32(&full[s]), px);
     }
     // drain: every stage's last issued load has landed before the CTA may exit
     for (int j = (issued > S ? issued - S : 0); j < issued; ++j)
@@ -443,7 +449,12 @@ int tc_plan_shape(TcPlan* p, const void* W, int N, int K, const void* X, int M, 
   p->splits = best;
   int r = tc_make_tmap(&p->tmW, W, (uint64_t)N, (uint64_t)K, (uint32_t)(kHalfN * wide));
   if (r) return r;
-  // split: the tensor spans both halves (rows >= M of each half are ignored columns)
+  // split: the tensor spans both halves (rows >= M of each half are ignored columns);
+  // two boxes per stage become one 3-D request over {k, row, half}
+  p->x3d = split && p->nx == 2;
+  if (p->x3d)
+    return tc_make_tmap3s(&p->tmX, X, (uint64_t)K, (uint64_t)p->MT, 2, (uint64_t)K * 2,
+                          (uint64_t)p->MT * K * 2, (uint32_t)p->xbox, 2);
   r = tc_make_tmap(&p->tmX, X, (uint64_t)(split ? 2 * p->MT : M), (uint64_t)K,
                    (uint32_t)p->xbox);
   return r;
@@ -496,16 +507,18 @@ int tc_init_attributes() {
 }
 
 void op_gemm_tc_swiglu(const TcPlan& p, void* h, long h_lo, unsigned* err, cudaStream_t st) {
-  TcArgs a{p.N,  p.K,      p.M,        p.MT,    p.stages, p.wide, p.mct,   p.split,
-           p.xbox, p.nx,   p.merged,   p.acc_cols, nullptr, 0, nullptr, nullptr,
-           0,    (bf16*)h, h_lo,       p.F,     err};
+  TcArgs a{p.N,        p.K,     p.M,   p.MT,     p.stages,   p.wide,  p.mct,
+           p.split,    p.xbox,  p.nx,  p.x3d,    p.merged,   p.acc_cols, nullptr,
+           0,          nullptr, nullptr, 0,      (bf16*)h,   h_lo,    p.F,
+           err};
   dim3 grid(p.msplit, (p.F + kHalfN - 1) / kHalfN, 1);
   kernel_for<2>(p)<<<grid, 128, p.smem, st>>>(p.tmW, p.tmX, a);
 }
 
 void op_gemm_tc_acc(const TcPlan& p, float* out, int ldo, unsigned* err, cudaStream_t st) {
-  TcArgs a{p.N,     p.K,  p.M,     p.MT,       p.stages, p.wide, p.mct, p.split, p.xbox,
-           p.nx,    p.merged, p.acc_cols, out, ldo,     nullptr, nullptr, 0,  nullptr, 0, 0,
+  TcArgs a{p.N,        p.K,     p.M,     p.MT,     p.stages,   p.wide,  p.mct,
+           p.split,    p.xbox,  p.nx,    p.x3d,    p.merged,   p.acc_cols, out,
+           ldo,        nullptr, nullptr, 0,        nullptr,    0,       0,
            err};
   dim3 grid(p.msplit, (p.N + kHalfN * p.wide - 1) / (kHalfN * p.wide), p.splits);
   kernel_for<0>(p)<<<grid, 128, p.smem, st>>>(p.tmW, p.tmX, a);
@@ -513,8 +526,9 @@ void op_gemm_tc_acc(const TcPlan& p, float* out, int ldo, unsigned* err, cudaStr
 
 void op_gemm_tc_argmax(const TcPlan& p, unsigned long long* keys, float* logits, long ldl,
                        unsigned* err, cudaStream_t st) {
-  TcArgs a{p.N,  p.K,      p.M,        p.MT,    p.stages, p.wide, p.mct, p.split, p.xbox,
-           p.nx, p.merged, p.acc_cols, nullptr, 0,        keys,   logits, ldl,  nullptr, 0, 0,
+  TcArgs a{p.N,        p.K,     p.M,     p.MT,     p.stages,   p.wide,  p.mct,
+           p.split,    p.xbox,  p.nx,    p.x3d,    p.merged,   p.acc_cols, nullptr,
+           0,          keys,    logits,  ldl,      nullptr,    0,       0,
            err};
   dim3 grid(p.msplit, (p.N + kHalfN * p.wide - 1) / (kHalfN * p.wide), 1);
   kernel_for<1>(p)<<<grid, 128, p.smem, st>>>(p.tmW, p.tmX, a);

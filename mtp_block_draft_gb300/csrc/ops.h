@@ -155,7 +155,8 @@ struct TcPlan {
   int msplit;     // token halves: CTAs per weight tile (1 or 2)
   int mct;        // token rows per CTA
   int split;      // X is the [hi; lo] bf16 pair
-  int xbox, nx;   // X rows per TMA load, loads per stage
+  int xbox, nx;   // X rows per box, boxes per stage
+  int x3d;        // the two halves' boxes as one 3-D request
   int merged;     // hi and lo in one MMA of 2*mct columns
   int acc_cols;   // TMEM columns per accumulator
   int swiglu, F;  // SwiGLU epilogue: W = [gate; up] of F rows each
