@@ -141,6 +141,64 @@ def oracle_sample(cfg, weights, prompts, rounds: int, budget_s: float = 30.0):
             "rounds": done, "seconds": el}
 
 
+# DMTP per-verify acceptance lengths of the DMTP blog §7 ("Acceptance Length and End-to-End
+# Throughput", trained Qwen3.6 models at temperature 1): used only for a labelled
+# projection of the measured rounds/s, never as a measurement.
+PAGE_PER_VERIFY = {"Code": 3.795, "Math": 4.056, "MT-Bench": 3.250, "Agent": 4.709,
+                   "SWE": 3.173, "Long-horizon": 4.656}
+
+
+def forced_accept(cfg, weights, prompts, warmup, steps):
+    """Rounds with every draft accepted: the drafts are forced to the target's own greedy
+    continuation, collected first on a separate context by rounds whose drafts are forced
+    wrong (each commits exactly the greedy tokens up to its first rejection), then replayed
+    as the forced-draft graph on a fresh context from the same prompts. The histogram of
+    the timed rounds gives the accept length actually reached (8 unless a near tie in the
+    target's logits flips a pick between the two runs)."""
+    import torch
+    from mtp_block_draft_gb300 import DmtpRound
+    B, V, R = len(prompts), cfg.vocab, warmup + steps
+    max_ctx = max(len(p) for p in prompts) + 8 * R + 64
+    g1 = DmtpRound(cfg, weights, prompts, max_ctx)
+    _, A, _ = g1.read_state()
+    streams = [[int(a)] for a in A]
+    forced = torch.empty((B, 7), dtype=torch.int32, device="cuda")
+    out = g1.alloc_out(ints=True, floats=False)
+    while min(len(st) for st in streams) < 8 * R + 1:
+        wrong = [[(st[-1] + 1 + j) % (V - 1) for j in range(7)] for st in streams]
+        forced.copy_(torch.tensor(wrong, dtype=torch.int32))
+        g1.round(out, forced=forced)
+        com, n = out["committed"].cpu().numpy(), out["n_accepted"].cpu().numpy()
+        for b in range(B):
+            streams[b] += [int(t) for t in com[b][:n[b] + 1]]
+    g1.close()
+    del g1
+    plan = torch.tensor([[[streams[b][8 * r + 1 + j] for j in range(7)] for b in range(B)]
+                         for r in range(R)], dtype=torch.int32, device="cuda")
+    torch.cuda.empty_cache()
+    g2 = DmtpRound(cfg, weights, prompts, max_ctx)
+    stream = g2.stream
+    for r in range(warmup):
+        g2.round(forced=plan[r])
+    _, _, h0 = g2.read_state()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for r in range(warmup, R):
+        g2.round(forced=plan[r])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    _, _, h1 = g2.read_state()
+    g2.close()
+    dh = (h1 - h0).astype(np.int64)
+    mean_len = float(np.sum((np.arange(8) + 1) * dh)) / max(1, int(dh.sum()))
+    rps = steps / (ms / 1e3)
+    return {"rounds_per_s": rps, "mean_accept_len": mean_len, "tokens_per_s": B * rps * mean_len,
+            "steps": steps, "warmup": warmup,
+            "drafts": "forced to the target's own greedy continuation (every draft accepted)"}
+
+
 def run_reference(args, cfg):
     import torch
     from synth import make_prompts, make_weights
@@ -187,6 +245,8 @@ def main():
     ap.add_argument("--profile-rounds", type=int, default=3)
     ap.add_argument("--cpu-rounds", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--forced-steps", type=int, default=16,
+                    help="timed rounds of the forced-accept run (0: skip)")
     # smaller cases of the same kernels, for profiler captures (not bench workloads)
     ap.add_argument("--layers", type=int, default=None, help="override target layers")
     ap.add_argument("--ctx", type=int, nargs=2, default=None, help="override prompt range")
@@ -330,9 +390,17 @@ def main():
                                "profiled_round_ms": prof_round_ms,
                                "frac_of_timed": (alg_bytes / (hbm * 1e9) * 1e3) / (ms / args.steps)},
             "kernels": breakdown}
+    rps_nat = args.steps / (ms / 1e3)
+    line["projection"] = {
+        "note": "B x measured rounds/s x the DMTP blog's per-verify acceptance lengths "
+                "(trained models); a projection, not a measurement",
+        "tokens_per_s": {k: B * rps_nat * v for k, v in PAGE_PER_VERIFY.items()}}
+    g.close()
+    del g
+    if args.forced_steps > 0:
+        line["forced_accept"] = forced_accept(cfg, weights, prompts, 4, args.forced_steps)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_sample(cfg, weights, prompts, args.cpu_rounds)
-    g.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

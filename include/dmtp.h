@@ -19,8 +19,9 @@
  *
  * Memory ownership. The caller allocates every device buffer (weights, the
  * workspace, round outputs) and keeps it alive while the context lives; the
- * library allocates no device memory. The context owns host bookkeeping and one
- * captured CUDA graph. All work is enqueued on the stream given to dmtp_init;
+ * library allocates no device memory. The context owns host bookkeeping and up to
+ * two captured CUDA graphs (the round, and the round with forced drafts). All work is
+ * enqueued on the stream given to dmtp_init;
  * results are valid once the caller synchronises that stream.
  *
  * Errors. Every int-returning call returns DMTP_OK (0) or a negative DMTP_E* code.
@@ -133,8 +134,10 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
 /* Enqueue one round (steps a1-a6) for all sequences. out: see dmtp_round_out (may be
  * NULL). forced_drafts: NULL, or device int32 [B][7] replacing T1..T7 (T1 right after
  * the MTP head, so the fusion and drafter see it; T2..T7 after the drafter) - the
- * forced-draft test mode of the colibri page. Returns DMTP_ECAPACITY if a sequence
- * might pass max_ctx - 8 (checked on the host before launch). Asynchronous. */
+ * forced-draft test mode of the colibri page; they are copied into the context and
+ * the round runs as its own captured graph. Requesting debug logits in `out` runs the
+ * round eagerly instead. Returns DMTP_ECAPACITY if a sequence might pass
+ * max_ctx - 8 (checked on the host before launch). Asynchronous. */
 int dmtp_round(dmtp_ctx* ctx, const dmtp_round_out* out, const int32_t* forced_drafts);
 
 /* One round with host outputs: enqueue the round, copy committed [B][8] and

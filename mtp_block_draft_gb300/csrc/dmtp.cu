@@ -12,6 +12,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <mutex>
 #include <vector>
 
 #include "../../include/dmtp.h"
@@ -102,7 +103,8 @@ struct dmtp_ctx {
   Gemm dkv[DMTP_MAX_DRAFT_LAYERS];
   Gemm fuse, head_t1, head_d, head_v, dfc, mproj;
 
-  cudaGraphExec_t graph;
+  cudaGraphExec_t graph;         // the round
+  cudaGraphExec_t graph_forced;  // the round with drafts read from `forced`
   cudaStream_t cap_st;  // private stream the round is captured on (the caller's may be NULL)
   bool poisoned;
   long kv_bound;
@@ -654,15 +656,20 @@ int check_err(dmtp_ctx* c) {
 // the argmax keys), which the round clears before use.
 namespace {
 struct TuneKey {
-  int N, K, M;
-  bool split, argmax;
+  int dev, N, K, M;
+  bool split, argmax, swiglu;
   bool operator==(const TuneKey& o) const {
-    return N == o.N && K == o.K && M == o.M && split == o.split && argmax == o.argmax;
+    return dev == o.dev && N == o.N && K == o.K && M == o.M && split == o.split &&
+           argmax == o.argmax && swiglu == o.swiglu;
   }
 };
 struct TuneChoice {
   int wide, msplit, splits;
 };
+// Choices are kept for the life of the process: a later context on the same device
+// reuses them (same kernels, same reduction order, no second timing pass).
+std::mutex g_tune_mu;
+std::vector<std::pair<TuneKey, TuneChoice>> g_tune;
 
 void collect(LayerPlans& p, std::vector<Gemm*>& v) {
   for (Gemm* g : {&p.qkv, &p.o, &p.gu, &p.down, &p.gq, &p.ga, &p.gb, &p.go}) v.push_back(g);
@@ -724,10 +731,26 @@ int autotune(dmtp_ctx* c, const void* flush, size_t flush_bytes) {
     return DMTP_ECUDA;
   }
   const bool verbose = getenv("DMTP_VERBOSE") != nullptr;
-  std::vector<std::pair<TuneKey, TuneChoice>> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lk(g_tune_mu);
   int rc = DMTP_OK;
   for (Gemm* g : all) {
     if (!g->W) continue;
+    if (!g->swiglu && !g->argmax && (size_t)g->M * g->N > scratch) continue;  // default shape
+    const TuneKey key{dev, g->N, g->K, g->M, g->split, g->argmax, g->swiglu};
+    const TuneChoice* hit = nullptr;
+    for (auto& e : g_tune)
+      if (e.first == key) hit = &e.second;
+    if (hit) {
+      const int r = g->swiglu ? tc_plan_swiglu(&g->tc, g->W, c->F, g->K, g->X, g->M, c->nsm,
+                                               g->split, hit->msplit)
+                              : tc_plan_shape(&g->tc, g->W, g->N, g->K, g->X, g->M, c->nsm,
+                                              g->argmax, g->split, hit->wide, hit->msplit,
+                                              hit->splits);
+      if (r) rc = DMTP_EINVAL;
+      continue;
+    }
     if (g->swiglu) {  // tile shape: one or two token halves; no K split
       TcPlan best_p = g->tc;
       float best_t = time_swiglu(c, g->tc, flush, flush_bytes, e0, e1);
@@ -743,17 +766,7 @@ int autotune(dmtp_ctx* c, const void* flush, size_t flush_bytes) {
         }
       }
       g->tc = best_p;
-      continue;
-    }
-    if (!g->argmax && (size_t)g->M * g->N > scratch) continue;  // keeps the default shape
-    const TuneKey key{g->N, g->K, g->M, g->split, g->argmax};
-    const TuneChoice* hit = nullptr;
-    for (auto& e : cache)
-      if (e.first == key) hit = &e.second;
-    if (hit) {
-      if (tc_plan_shape(&g->tc, g->W, g->N, g->K, g->X, g->M, c->nsm, g->argmax, g->split,
-                        hit->wide, hit->msplit, hit->splits))
-        rc = DMTP_EINVAL;
+      g_tune.push_back({key, TuneChoice{2, best_p.msplit, 1}});
       continue;
     }
     TuneChoice best{g->tc.wide, g->tc.msplit, g->tc.splits};
@@ -783,7 +796,7 @@ int autotune(dmtp_ctx* c, const void* flush, size_t flush_bytes) {
     if (tc_plan_shape(&g->tc, g->W, g->N, g->K, g->X, g->M, c->nsm, g->argmax, g->split,
                       best.wide, best.msplit, best.splits))
       rc = DMTP_EINVAL;
-    cache.push_back({key, best});
+    g_tune.push_back({key, best});
     if (verbose)
       fprintf(stderr, "dmtp: gemm N=%d K=%d M=%d%s%s: %d x 128 weight rows, %d token part(s), "
               "%d K split(s), %.1f us\n", g->N, g->K, g->M, g->split ? " split" : "",
@@ -824,6 +837,7 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
   c->w = *w;
   c->st = (cudaStream_t)stream;
   c->graph = nullptr;
+  c->graph_forced = nullptr;
   c->poisoned = false;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1006,7 +1020,7 @@ int dmtp_round(dmtp_ctx* c, const dmtp_round_out* out, const int32_t* forced) {
     dbg.vl = out->verify_logits;
     if (out->h_mtp && copy_out(c, out->h_mtp, c->h_mtp, (size_t)B * c->d * 4)) return DMTP_ECUDA;
   }
-  const bool eager = forced || dbg.t1 || dbg.dl || dbg.vl;
+  const bool eager = dbg.t1 || dbg.dl || dbg.vl;
   if (forced) {
     if (cudaMemcpyAsync(c->forced, forced, (size_t)B * 7 * 4, cudaMemcpyDeviceToDevice, c->st) !=
         cudaSuccess)
@@ -1017,7 +1031,10 @@ int dmtp_round(dmtp_ctx* c, const dmtp_round_out* out, const int32_t* forced) {
     enqueue_round(c, dbg, forced ? c->forced : nullptr);
     c->round_launches = c->launches;
   } else {
-    if (!c->graph) {
+    // one graph per mode; forced drafts are read from the context's own buffer, which
+    // the copy above fills before the replay
+    cudaGraphExec_t& graph = forced ? c->graph_forced : c->graph;
+    if (!graph) {
       // capture records work without running it, on a private stream (the legacy
       // default stream cannot be captured); the graph is then replayed on c->st
       if (!c->cap_st && cudaStreamCreateWithFlags(&c->cap_st, cudaStreamNonBlocking) != cudaSuccess)
@@ -1030,19 +1047,19 @@ int dmtp_round(dmtp_ctx* c, const dmtp_round_out* out, const int32_t* forced) {
         return DMTP_ECUDA;
       }
       c->launches = 0;
-      enqueue_round(c, dbg, nullptr);
+      enqueue_round(c, dbg, forced ? c->forced : nullptr);
       c->round_launches = c->launches;
       const cudaError_t ce = cudaStreamEndCapture(c->st, &g);
       c->st = user;
       if (ce != cudaSuccess) return DMTP_ECUDA;
-      if (cudaGraphInstantiate(&c->graph, g, 0) != cudaSuccess) {
+      if (cudaGraphInstantiate(&graph, g, 0) != cudaSuccess) {
         cudaGraphDestroy(g);
-        c->graph = nullptr;
+        graph = nullptr;
         return DMTP_ECUDA;
       }
       cudaGraphDestroy(g);
     }
-    if (cudaGraphLaunch(c->graph, c->st) != cudaSuccess) return DMTP_ECUDA;
+    if (cudaGraphLaunch(graph, c->st) != cudaSuccess) return DMTP_ECUDA;
   }
   if (cudaPeekAtLastError() != cudaSuccess) return DMTP_ECUDA;
   c->kv_bound += 8;
@@ -1138,6 +1155,7 @@ int dmtp_round_profile(dmtp_ctx* c, dmtp_profile* out) {
 void dmtp_free(dmtp_ctx* c) {
   if (!c) return;
   if (c->graph) cudaGraphExecDestroy(c->graph);
+  if (c->graph_forced) cudaGraphExecDestroy(c->graph_forced);
   if (c->cap_st) cudaStreamDestroy(c->cap_st);
   for (cudaEvent_t e : c->pev) cudaEventDestroy(e);
   delete c;
