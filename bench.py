@@ -117,6 +117,26 @@ def _dist():
     return rank, world, local
 
 
+def rank_config(cfg, rank: int):
+    """Each rank serves its own batch (replicas, weak scaling): rank 0 the workload's
+    prompts, rank r the same configuration with prompt seed + 1000 r."""
+    return cfg if rank == 0 else cfg.replace(seed=cfg.seed + 1000 * rank)
+
+
+def combine_ranks(ms, tokens, e2e_s, e2e_tokens, world: int, device):
+    """Whole-job numbers over the ranks: the slowest rank's times (device-timed and end
+    to end), the sum of the committed tokens."""
+    if world == 1:
+        return float(ms), float(tokens), float(e2e_s), float(e2e_tokens)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms, e2e_s], dtype=torch.float64, device=device)
+    n = torch.tensor([float(tokens), float(e2e_tokens)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t[0]), float(n[0]), float(t[1]), float(n[1])
+
+
 def oracle_sample(cfg, weights, prompts, rounds: int, budget_s: float = 30.0):
     """Time the oracle on one sequence (the shortest prompt) of the batch: prefill
     untimed, then up to `rounds` rounds or `budget_s` seconds timed."""
@@ -276,7 +296,7 @@ def main():
     dev = torch.device("cuda", local)
 
     weights = make_weights(cfg, dev)
-    pcfg = cfg if rank == 0 else cfg.replace(seed=cfg.seed + 1000 * rank)
+    pcfg = rank_config(cfg, rank)
     prompts = make_prompts(pcfg)
     B = len(prompts)
     total_rounds = args.warmup + args.steps + args.e2e_steps + args.profile_rounds + 8
@@ -310,15 +330,6 @@ def main():
     tokens = int(np.sum((np.arange(8) + 1) * dh))
     seq_rounds = int(dh.sum())  # one histogram entry per sequence per round
     mean_len = tokens / max(1, seq_rounds)
-    t = torch.tensor([ms, float(tokens)], dtype=torch.float64, device=dev)
-    if world > 1:
-        tmax = t.clone()
-        dist.all_reduce(tmax[:1], op=dist.ReduceOp.MAX)
-        dist.all_reduce(t[1:], op=dist.ReduceOp.SUM)
-        ms_all, tok_all = float(tmax[0]), float(t[1])
-    else:
-        ms_all, tok_all = ms, float(tokens)
-    value = tok_all / (ms_all / 1e3)
 
     # e2e through the C ABI with host outputs (pinned), wall clock
     committed = torch.empty((B, 8), dtype=torch.int32, pin_memory=True).numpy()
@@ -329,12 +340,10 @@ def main():
         g.round_host(committed, nacc)
         e2e_tokens += int(np.sum(nacc.astype(np.int64) + 1))
     e2e_s = time.perf_counter() - t0
-    e2e_val = e2e_tokens / e2e_s
-    if world > 1:
-        te = torch.tensor([e2e_s, float(e2e_tokens)], dtype=torch.float64, device=dev)
-        dist.all_reduce(te[:1], op=dist.ReduceOp.MAX)
-        dist.all_reduce(te[1:], op=dist.ReduceOp.SUM)
-        e2e_val = float(te[1]) / float(te[0])
+    ms_all, tok_all, e2e_s_all, e2e_tok_all = combine_ranks(ms, tokens, e2e_s, e2e_tokens,
+                                                             world, dev)
+    value = tok_all / (ms_all / 1e3)
+    e2e_val = e2e_tok_all / e2e_s_all
 
     # per-kernel-class profile of real rounds (events around each launch)
     hbm, tc_burst, tc_sus, peak_src = _peaks()
@@ -397,7 +406,7 @@ def main():
         "tokens_per_s": {k: B * rps_nat * v for k, v in PAGE_PER_VERIFY.items()}}
     g.close()
     del g
-    if args.forced_steps > 0:
+    if args.forced_steps > 0 and world == 1:
         line["forced_accept"] = forced_accept(cfg, weights, prompts, 4, args.forced_steps)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_sample(cfg, weights, prompts, args.cpu_rounds)
