@@ -37,6 +37,8 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
+from .sampling import sampled_scores
+
 F64 = np.float64
 
 
@@ -169,6 +171,7 @@ class SeqState:
     mtp_K/mtp_V: MTP private KV for positions 1..a (array row p-1);
     h_mtp: the MTP block output at position a, the hidden state that predicts T1.
     tokens: prompt + every emitted token (ends with A).
+    b: the sequence's index in its batch (keys the sampling noise).
     """
     a: int
     A: int
@@ -181,6 +184,7 @@ class SeqState:
     mtp_V: np.ndarray
     h_mtp: np.ndarray
     tokens: list = field(default_factory=list)
+    b: int = 0
 
     def clone(self) -> "SeqState":
         return copy.deepcopy(self)
@@ -193,11 +197,15 @@ class SeqState:
 class OracleModel:
     """Target + MTP module + fusion + block drafter, float64, from synth weights."""
 
-    def __init__(self, cfg, weights: dict, gate: float = 0.05, kv_store: str | None = None):
+    def __init__(self, cfg, weights: dict, gate: float = 0.05, kv_store: str | None = None,
+                 temperature: float = 0.0, sample_seed: int = 0):
         """kv_store: storage type of every K/V cache ("bf16" or "fp32"); by default the
         model's storage type (cfg.dtype). Stored keys and values are rounded to it when
-        written, as a bf16 KV cache holds them; every computation stays float64."""
+        written, as a bf16 KV cache holds them; every computation stays float64.
+        temperature > 0: the verify picks are target samples (sampling.py) with the given
+        sampling seed; 0: argmax picks."""
         self.cfg = cfg
+        self.temperature, self.sample_seed = float(temperature), int(sample_seed)
         self.W = {k: v.detach().to("cpu").double().numpy() if hasattr(v, "detach")
                   else np.asarray(v, dtype=F64) for k, v in weights.items()}
         self.gate = gate
@@ -399,18 +407,21 @@ class OracleModel:
             dft_V=[z() for _ in range(c.draft_layers)],
             mtp_K=z(), mtp_V=z(), h_mtp=np.zeros(c.d_model, F64))
 
-    def prefill(self, prompt, adopt_A=None) -> SeqState:
+    def prefill(self, prompt, adopt_A=None, b: int = 0) -> SeqState:
         """Initialise all three models' states from a prompt ([DMTP] §6.1).
 
         Target over x_0..x_{P-1}; A = argmax H h^T_{P-1}; drafter context K/V for
         positions 0..P-1; MTP rows p = 1..P (token x_p, hidden h^T_{p-1}, with
         x_P = A), so that h_MTP (the block output at P) predicts x_{P+1}.
         ``adopt_A``: another implementation's pick for A, taken when it lies within the
-        near-tie gate of the maximum (see ``round``).
+        near-tie gate of the maximum (see ``round``). A is an argmax pick at any
+        temperature (reading: sampling starts with the round's verify picks). ``b``: the
+        sequence's index in its batch.
         """
         prompt = [int(t) for t in prompt]
         P = len(prompt)
         st = self.empty_state()
+        st.b = int(b)
         hT, taps, _, _ = self.target_rows(st, prompt, 0, head=False)
         log = {"gaps": {}, "adopted": [], "mismatch": []}
         A = self._pick(hT[P - 1] @ self.W["head"].T, adopt_A, log, "A")
@@ -441,6 +452,23 @@ class OracleModel:
             out.append(tok)
         return out[:n_new]
 
+    def sampled_decode(self, prompt, n_new: int, b: int = 0) -> list[int]:
+        """Plain one-token-per-forward decoding with the target's samples: the token at
+        position p is argmax(l / temperature + G(b, p)) of the one-row forward at p - 1
+        (sampling.py); A, the first token after the prompt, is the argmax pick. The
+        losslessness reference of sampled verification ([DMTP] §5 target-only
+        verification, [colibri] verify contract)."""
+        st = self.prefill(prompt, b=b)
+        out = [st.A]
+        tok, pos = st.A, st.a
+        while len(out) < n_new:
+            _, _, logits, _ = self.target_rows(st, [tok], pos)
+            tok = argmax_first(sampled_scores(logits[0], self.temperature, self.sample_seed,
+                                              b, pos + 1))
+            pos += 1
+            out.append(tok)
+        return out[:n_new]
+
     # ---- one DMTP round ------------------------------------------------------------------
 
     def _pick(self, logits, adopt, log, where):
@@ -465,7 +493,8 @@ class OracleModel:
           a3 one block-drafter forward -> T2..T7;
           a4 target verify of rows [A, T1..T7] at positions a..a+7, each row by the
              one-row decode routine ([colibri]: every verify row gets a decode step's
-             bits) -> g_0..g_7;
+             bits) -> g_0..g_7 (argmax picks, or at temperature > 0 the target's
+             samples for positions a+1..a+8, sampling.py);
           a5 n = longest prefix with T_j = g_{j-1}; commit T_1..T_n and g_n; the target
              KV keeps a+n+1 positions; a GDN state takes the snapshot after row n;
           a6 drafter context K/V for positions a..a+n from the verify taps; MTP rows at
@@ -506,7 +535,7 @@ class OracleModel:
         # a4: each row by the one-row routine on a working copy of the caches
         work = st.clone()
         rows = [A] + drafts
-        hT_rows, tap_rows, vlog, g = [], [], [], []
+        hT_rows, tap_rows, vlog, g, vsc = [], [], [], [], []
         snaps = {}
         adg = adopt.get("g")
         for s in range(8):
@@ -514,7 +543,12 @@ class OracleModel:
             hT_rows.append(hT[0]); tap_rows.append(taps[0]); vlog.append(logits[0])
             for l, lst in sn.items():
                 snaps.setdefault(l, []).append(lst[0])
-            g.append(self._pick(logits[0], adg[s] if adg is not None else None, log, f"g{s}"))
+            sc = logits[0]
+            if self.temperature > 0:  # the target's sample for position a + s + 1
+                sc = sampled_scores(logits[0], self.temperature, self.sample_seed, st.b,
+                                    a + s + 1)
+                vsc.append(sc)
+            g.append(self._pick(sc, adg[s] if adg is not None else None, log, f"g{s}"))
         # a5
         n = 0
         while n < 7 and drafts[n] == g[n]:
@@ -544,4 +578,6 @@ class OracleModel:
                    hT_rows=hT_rows)
         if want_logits:
             rec.update(t1_logits=t1_logits, draft_logits=dlog, verify_logits=np.stack(vlog))
+            if vsc:
+                rec["verify_scores"] = np.stack(vsc)
         return rec
