@@ -143,8 +143,9 @@ def oracle_sample(cfg, weights, prompts, rounds: int, budget_s: float = 30.0):
     from oracle import OracleModel
     b = int(np.argmin([len(p) for p in prompts]))
     t0 = time.perf_counter()
-    om = OracleModel(cfg, {k: v.cpu() for k, v in weights.items()})
-    st = om.prefill(prompts[b])
+    om = OracleModel(cfg, {k: v.cpu() for k, v in weights.items()},
+                     temperature=cfg.temperature, sample_seed=cfg.sample_seed)
+    st = om.prefill(prompts[b], b=b)
     setup = time.perf_counter() - t0
     tokens, el, done = 0, 0.0, 0
     while done < rounds and el < budget_s:
@@ -230,9 +231,10 @@ def run_reference(args, cfg):
     prompts = make_prompts(cfg)
     from oracle import OracleModel
     b = int(np.argmin([len(p) for p in prompts]))
-    om = OracleModel(cfg, {k: v.cpu() for k, v in weights.items()})
+    om = OracleModel(cfg, {k: v.cpu() for k, v in weights.items()},
+                     temperature=cfg.temperature, sample_seed=cfg.sample_seed)
     del weights
-    st = om.prefill(prompts[b])
+    st = om.prefill(prompts[b], b=b)
     for _ in range(args.warmup):
         om.round(st, want_logits=False)
     tokens, t0 = 0, time.perf_counter()
@@ -267,6 +269,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--forced-steps", type=int, default=16,
                     help="timed rounds of the forced-accept run (0: skip)")
+    ap.add_argument("--temperature", type=float, default=0.0,
+                    help="0: greedy verification (the workloads' setting); > 0: target-only "
+                         "sampled verification at this temperature")
+    ap.add_argument("--sample-seed", type=int, default=1)
     # smaller cases of the same kernels, for profiler captures (not bench workloads)
     ap.add_argument("--layers", type=int, default=None, help="override target layers")
     ap.add_argument("--ctx", type=int, nargs=2, default=None, help="override prompt range")
@@ -281,6 +287,9 @@ def main():
     if args.ctx is not None:
         cfg = cfg.replace(name=f"{cfg.name}-ctx{args.ctx[0]}-{args.ctx[1]}", ctx_lo=args.ctx[0],
                           ctx_hi=args.ctx[1])
+    if args.temperature > 0:
+        cfg = cfg.replace(name=f"{cfg.name}-T{args.temperature:g}", temperature=args.temperature,
+                          sample_seed=args.sample_seed)
     if args.impl == "reference":
         return run_reference(args, cfg)
 
@@ -385,6 +394,8 @@ def main():
                                    f"{cfg.n_layers}-layer GQA {cfg.n_heads}/{cfg.n_kv_heads}x{cfg.head_dim} "
                                    f"target, ffn {cfg.ffn}, 1 MTP block, {cfg.draft_layers}-layer drafter, "
                                    f"prompts U[{cfg.ctx_lo},{cfg.ctx_hi}]",
+                       "verify": ("greedy" if cfg.temperature == 0 else
+                                  f"sampled, temperature {cfg.temperature:g}"),
                        "global_batch": B * world, "seq_len": int(np.mean([len(p) for p in prompts])),
                        "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (~7 GB of weights+KV streamed per round)",

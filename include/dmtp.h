@@ -60,7 +60,16 @@ extern "C" {
  * tap_layers: target layers whose residual stream feeds the drafter's context
  * projection (DFlash "KV injection", DFlash vs MTP page). mask_id: the MASK token.
  * draft_window: the drafter sees context positions max(0, a - window) .. a-1 (DMTP
- * §6.2). max_ctx: KV capacity per sequence (prompt + 8 per round + 8 slack). */
+ * §6.2). max_ctx: KV capacity per sequence (prompt + 8 per round + 8 slack).
+ * temperature: 0 = greedy verification (the target's picks g_0..g_7 are argmax picks);
+ * > 0 (at least 1e-4, finite) = target-only sampled verification (DMTP §5: drafts are
+ * checked against the target's samples): the pick for position p of sequence b is
+ * argmax_v (l_v / temperature + G_v), an exact draw from softmax(l / temperature),
+ * with Gumbel noise G_v = -log(-log u_v), u_v = ((w >> 8) + 1/2) 2^-24 and w word v % 4
+ * of the Philox4x32-10 block (Salmon et al., SC 2011) of counter (v / 4, p, b, 0) and key
+ * (low, high 32 bits of sample_seed). The noise depends on the position only, so the
+ * committed stream equals plain one-token sampled decoding with the same noise. A (the
+ * prefill's first token) and the drafts T1..T7 stay argmax picks. */
 typedef struct {
   int vocab, d_model, n_layers, n_heads, n_kv_heads, head_dim, ffn;
   int gdn_heads, gdn_dk, gdn_dv;
@@ -72,6 +81,8 @@ typedef struct {
   float rms_eps, rope_theta;
   int max_ctx, max_batch;
   int dtype;
+  float temperature;
+  uint64_t sample_seed;
 } dmtp_config;
 
 /* One decoder layer, row-major [out, in] device matrices of the config's dtype.

@@ -39,7 +39,8 @@ class dmtp_config(C.Structure):
                 ("draft_layers", C.c_int), ("draft_window", C.c_int), ("n_taps", C.c_int),
                 ("tap_layers", C.c_int * DMTP_MAX_TAPS), ("mask_id", C.c_int),
                 ("rms_eps", C.c_float), ("rope_theta", C.c_float), ("max_ctx", C.c_int),
-                ("max_batch", C.c_int), ("dtype", C.c_int)]
+                ("max_batch", C.c_int), ("dtype", C.c_int), ("temperature", C.c_float),
+                ("sample_seed", C.c_uint64)]
 
 
 _LAYER_FIELDS = ("attn_norm", "wqkv", "wo", "gdn_wqkv", "gdn_wa", "gdn_wb", "gdn_wo",
@@ -141,6 +142,8 @@ def make_config(cfg, max_ctx: int, max_batch: int | None = None) -> dmtp_config:
     c.max_ctx = max_ctx
     c.max_batch = cfg.batch if max_batch is None else max_batch
     c.dtype = 0 if cfg.dtype == "fp32" else 1
+    c.temperature = cfg.temperature
+    c.sample_seed = cfg.sample_seed
     return c
 
 

@@ -122,6 +122,50 @@ __device__ __forceinline__ float argmax_key_value(unsigned long long k) {
 }
 
 // ---------------------------------------------------------------------------------
+// Sampling noise for target-only sampled verification
+// ---------------------------------------------------------------------------------
+// Philox4x32 with 10 rounds (Salmon, Moraes, Dror and Shaw, "Parallel random numbers:
+// as easy as 1, 2, 3", SC 2011): each round multiplies counter words 0 and 2 by the
+// two round constants and forms (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1,
+// lo(M0 c0)); the key then takes one Weyl step.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+__device__ __forceinline__ uint32_t word4(const uint4& b, int i) {
+  return i == 0 ? b.x : i == 1 ? b.y : i == 2 ? b.z : b.w;
+}
+// Gumbel(0, 1) noise G = -log(-log u) of one generator word, u = ((w >> 8) + 1/2) 2^-24
+// in (0, 1). E = -log u is formed without cancellation: for t = 1 - u < 2^-6 (exact in
+// fp32 there) by the series t + t^2/2 + t^3/3 + t^4/4 of -log(1 - t), whose relative
+// truncation error is below t^4/5; elsewhere E >= 0.0157 and the fp32 logarithm of u
+// (rounded to fp32) is accurate to ~1e-5 relative. G's absolute error is then ~1e-5.
+__device__ __forceinline__ float gumbel_of_word(uint32_t w) {
+  const uint32_t k = w >> 8;
+  const float u = ((float)k + 0.5f) * 5.9604644775390625e-8f;
+  const float t = ((float)(16777216u - k) - 0.5f) * 5.9604644775390625e-8f;
+  const float series = t * fmaf(t, fmaf(t, fmaf(t, 0.25f, 0.33333334f), 0.5f), 1.f);
+  const float e = t < 0.015625f ? series : -__logf(u);
+  return -__logf(e);
+}
+// Sampled verification: row m of the verify head is sequence b = m / group at position
+// p = pos0[b] + m % group; its sample for position p + 1 is argmax_v (l_v / tau + G_v),
+// G_v from the Philox block of counter (v / 4, p + 1, b, 0) and key (k0, k1), word v % 4.
+__device__ __forceinline__ uint4 sample_block(int v4, int m, const int* pos0, int group,
+                                              uint32_t k0, uint32_t k1) {
+  const int b = m / group;
+  const int p = __ldg(pos0 + b) + (m - b * group) + 1;
+  return philox4x32_10(make_uint4((uint32_t)v4, (uint32_t)p, (uint32_t)b, 0u), k0, k1);
+}
+
+// ---------------------------------------------------------------------------------
 // mbarrier / TMA / tcgen05 (inline PTX)
 // ---------------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

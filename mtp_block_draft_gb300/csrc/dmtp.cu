@@ -143,7 +143,8 @@ int derive(dmtp_ctx* c, const dmtp_config* cfg, int B) {
       f.n_heads % f.n_kv_heads || f.head_dim < 8 || f.head_dim > 128 || f.head_dim % 2 ||
       f.ffn < 1 || f.max_ctx < 16 || B < 1 || B > f.max_batch || B * 8 > 256 ||
       (f.dtype != 0 && f.dtype != 1) || f.mask_id < 0 || f.mask_id >= f.vocab ||
-      f.draft_window < 0)
+      f.draft_window < 0 || !(f.temperature == 0.f || (f.temperature >= 1e-4f &&
+                                                        f.temperature <= 3.0e38f)))
     return DMTP_EINVAL;
   const int grp = f.n_heads / f.n_kv_heads;
   const int QN = 8 * grp;
@@ -383,14 +384,16 @@ void gemm_acc(dmtp_ctx* c, const Gemm& g, float* out, int ldo) {
   });
 }
 
-void gemm_argmax(dmtp_ctx* c, const Gemm& g, unsigned long long* keys, float* logits) {
+// smp: the verify head's sampled picks (nullptr: argmax picks)
+void gemm_argmax(dmtp_ctx* c, const Gemm& g, unsigned long long* keys, float* logits,
+                 const SampleArgs* smp = nullptr) {
   const double bytes = ((double)g.N * g.K + (double)g.M * g.K) * esz(c) + 8.0 * g.M;
   launch(c, P_HEAD, bytes, 2.0 * g.M * g.N * g.K, [&] {
     if (c->dt == 1)
-      op_gemm_tc_argmax(g.tc, keys, logits, c->V, c->err, c->st);
+      op_gemm_tc_argmax(g.tc, keys, logits, c->V, smp, c->err, c->st);
     else
       op_gemm_simt_argmax((const float*)g.W, (const float*)g.X, g.N, g.K, g.M, keys, logits,
-                          c->V, c->st);
+                          c->V, smp, c->st);
   });
 }
 
@@ -622,7 +625,13 @@ void enqueue_round(dmtp_ctx* c, const Dbg& dbg, const int* forced) {
   // a4: target verify of [A, T1..T7]
   launch(c, P_OTHER, 0, 0, [&] { op_verify_tokens(s, c->st); });
   target_forward(c, true);
-  gemm_argmax(c, c->head_v, s.keys + 7 * B, dbg.vl);
+  if (c->cfg.temperature > 0.f) {  // target-only sampled verification (DMTP §5)
+    const SampleArgs smp{1.f / c->cfg.temperature, (uint32_t)c->cfg.sample_seed,
+                         (uint32_t)(c->cfg.sample_seed >> 32), s.pos0, 8};
+    gemm_argmax(c, c->head_v, s.keys + 7 * B, dbg.vl, &smp);
+  } else {
+    gemm_argmax(c, c->head_v, s.keys + 7 * B, dbg.vl);
+  }
   launch(c, P_OTHER, 0, 0, [&] { op_keys_to_ids(s.keys + 7 * B, B, 8, s.g, 8, 0, nullptr, 0, 0, c->st); });
   // a5: prefix acceptance, commit, watermarks, snapshot swap
   launch(c, P_OTHER, 0, 0, [&] { op_accept(s, c->st); });
@@ -682,7 +691,7 @@ float time_plan(dmtp_ctx* c, const TcPlan& p, bool argmax, const void* flush,
     op_l2_flush(flush, flush_bytes, c->err, c->st);
     cudaEventRecord(e0, c->st);
     if (argmax)
-      op_gemm_tc_argmax(p, c->rs.keys, nullptr, 0, c->err, c->st);
+      op_gemm_tc_argmax(p, c->rs.keys, nullptr, 0, nullptr, c->err, c->st);
     else
       op_gemm_tc_acc(p, c->gu, p.N, c->err, c->st);
     cudaEventRecord(e1, c->st);

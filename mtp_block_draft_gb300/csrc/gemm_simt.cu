@@ -9,12 +9,14 @@ namespace dmtp {
 
 static constexpr int BN = 64, BM = 32, BK = 16;
 
-template <int MODE>  // 0: out += acc, 1: argmax keys (+ logits)
+// MODE 0: out += acc, 1: argmax keys (+ logits); with smp.inv_tau > 0 the keys rank
+// the sampled scores l * inv_tau + G (common.cuh) instead of the logits.
+template <int MODE>
 __global__ void __launch_bounds__(256) k_gemm_simt(const float* __restrict__ W,
                                                    const float* __restrict__ X, int N, int K,
                                                    int M, float* out, int ldo,
                                                    unsigned long long* keys, float* logits,
-                                                   long ldl) {
+                                                   long ldl, SampleArgs smp) {
   __shared__ float Ws[BK][BN + 1];
   __shared__ float Xs[BK][BM + 1];
   const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
@@ -47,7 +49,12 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const float* __restrict__ W,
     if (MODE == 0) {
       if (n < N && m < M) out[(long)m * ldo + n] += acc[j];
     } else {
-      unsigned long long key = (n < N && m < M) ? argmax_key(acc[j], n) : 0ull;
+      float score = acc[j];
+      if (smp.inv_tau > 0.f && n < N && m < M) {
+        const uint4 blk = sample_block(n >> 2, m, smp.pos0, smp.group, smp.seed_lo, smp.seed_hi);
+        score = fmaf(acc[j], smp.inv_tau, gumbel_of_word(word4(blk, n & 3)));
+      }
+      unsigned long long key = (n < N && m < M) ? argmax_key(score, n) : 0ull;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, o);
@@ -62,13 +69,16 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const float* __restrict__ W,
 void op_gemm_simt_acc(const float* W, const float* X, int N, int K, int M, float* out, int ldo,
                       cudaStream_t st) {
   dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
-  k_gemm_simt<0><<<grid, 256, 0, st>>>(W, X, N, K, M, out, ldo, nullptr, nullptr, 0);
+  k_gemm_simt<0><<<grid, 256, 0, st>>>(W, X, N, K, M, out, ldo, nullptr, nullptr, 0,
+                                       SampleArgs{});
 }
 
 void op_gemm_simt_argmax(const float* W, const float* X, int N, int K, int M,
-                         unsigned long long* keys, float* logits, long ldl, cudaStream_t st) {
+                         unsigned long long* keys, float* logits, long ldl,
+                         const SampleArgs* smp, cudaStream_t st) {
   dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
-  k_gemm_simt<1><<<grid, 256, 0, st>>>(W, X, N, K, M, nullptr, 0, keys, logits, ldl);
+  k_gemm_simt<1><<<grid, 256, 0, st>>>(W, X, N, K, M, nullptr, 0, keys, logits, ldl,
+                                       smp ? *smp : SampleArgs{});
 }
 
 }  // namespace dmtp

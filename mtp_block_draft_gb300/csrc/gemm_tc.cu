@@ -61,6 +61,7 @@ struct TcArgs {
   long h_lo;
   int F;           // EPI 2: gate rows 0..F-1, up rows F..2F-1 of W
   unsigned* err;
+  SampleArgs smp;  // EPI 1: sampled picks when smp.inv_tau > 0
 };
 
 // 16 accumulator columns of this warp's lanes at taddr, plus (merged) the lo columns
@@ -98,6 +99,36 @@ __device__ __forceinline__ void warp_colmax16(unsigned long long (&k)[16], int l
   }
   const unsigned long long got = __shfl_xor_sync(0xffffffffu, k[0], 1);
   k[0] = got > k[0] ? got : k[0];
+}
+
+// Keys of the sampled scores v[j] * inv_tau + G (common.cuh) of token rows m0 + j,
+// j = 0..15, for this lane's vocabulary row n. The four lanes of a quad hold rows
+// n = 4q + r that share Philox counter word q: lane r computes the blocks of token rows
+// m0 + 4t + r (t = 0..3), and three exchanges per t hand every lane word r of each of
+// the quad's four blocks. Token rows past M take row M - 1's block (keys unused).
+__device__ __forceinline__ void sample_keys16(const TcArgs& a, int n, int m0, int lane,
+                                              const float (&v)[16],
+                                              unsigned long long (&key)[16]) {
+  const int r = lane & 3;
+  uint32_t w[16];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const int m = min(m0 + 4 * t + r, a.M - 1);
+    const uint4 blk = sample_block(n >> 2, m, a.smp.pos0, a.smp.group, a.smp.seed_lo,
+                                   a.smp.seed_hi);
+    uint32_t q[4];  // q[x]: word r of the block of token row m0 + 4t + (r ^ x)
+    q[0] = word4(blk, r);
+#pragma unroll
+    for (int x = 1; x < 4; ++x) q[x] = __shfl_xor_sync(0xffffffffu, word4(blk, r ^ x), x);
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const int x = r ^ s;
+      w[4 * t + s] = x == 0 ? q[0] : x == 1 ? q[1] : x == 2 ? q[2] : q[3];
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    key[j] = (n < a.N) ? argmax_key(fmaf(v[j], a.smp.inv_tau, gumbel_of_word(w[j])), n) : 0ull;
 }
 
 __host__ __device__ inline uint32_t tmem_cols_for(int cols) {
@@ -292,8 +323,12 @@ __global__ void __launch_bounds__(128, 1)
           // column maxima over the warp's 32 rows: a butterfly that halves the columns
           // each lane keeps at every step (16 -> 8 -> 4 -> 2 -> 1), then pairs agree
           unsigned long long key[16];
+          if (a.smp.inv_tau > 0.f) {
+            sample_keys16(a, n, mrow0 + c, lane, v, key);
+          } else {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) key[j] = (n < a.N) ? argmax_key(v[j], n) : 0ull;
+            for (int j = 0; j < 16; ++j) key[j] = (n < a.N) ? argmax_key(v[j], n) : 0ull;
+          }
           warp_colmax16(key, lane);
           // lane holds column col16(lane) (lanes 2i and 2i+1 the same one)
           if ((lane & 1) == 0) {
@@ -525,11 +560,11 @@ void op_gemm_tc_acc(const TcPlan& p, float* out, int ldo, unsigned* err, cudaStr
 }
 
 void op_gemm_tc_argmax(const TcPlan& p, unsigned long long* keys, float* logits, long ldl,
-                       unsigned* err, cudaStream_t st) {
+                       const SampleArgs* smp, unsigned* err, cudaStream_t st) {
   TcArgs a{p.N,        p.K,     p.M,     p.MT,     p.stages,   p.wide,  p.mct,
            p.split,    p.xbox,  p.nx,    p.x3d,    p.merged,   p.acc_cols, nullptr,
            0,          keys,    logits,  ldl,      nullptr,    0,       0,
-           err};
+           err,        smp ? *smp : SampleArgs{}};
   dim3 grid(p.msplit, (p.N + kHalfN * p.wide - 1) / (kHalfN * p.wide), 1);
   kernel_for<1>(p)<<<grid, 128, p.smem, st>>>(p.tmW, p.tmX, a);
 }

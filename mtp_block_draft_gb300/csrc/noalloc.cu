@@ -70,7 +70,7 @@ extern "C" int dmtp_t1_head_noalloc(const void* head, const void* norm_gain, con
   if (cudaMemsetAsync(keys, 0, (size_t)rows * 8, st) != cudaSuccess) return DMTP_ECUDA;
   dmtp::op_rmsnorm(1, h, d_model, norm_gain, X, d_model, 0, nullptr, 0,
                    nullptr, 0, 0, rows, d_model, eps, dmtp::RowMap(), st);
-  dmtp::op_gemm_tc_argmax(plan, keys, logits, vocab, nullptr, st);
+  dmtp::op_gemm_tc_argmax(plan, keys, logits, vocab, nullptr, nullptr, st);
   dmtp::op_keys_to_ids(keys, rows, 1, ids, 1, 0, nullptr, 0, 0, st);
   return cudaPeekAtLastError() == cudaSuccess ? DMTP_OK : DMTP_ECUDA;
 }

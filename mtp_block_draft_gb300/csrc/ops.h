@@ -139,13 +139,26 @@ void op_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMa
                      cudaStream_t st);
 int attn_tc_init_attributes();
 
+// Target-only sampled verification in the verify head's argmax epilogue: row m is
+// sequence m / group at position pos0[m / group] + m % group, and its pick is the
+// sample argmax_v (l_v * inv_tau + G_v) for the next position (Philox4x32-10 Gumbel
+// noise keyed by (seed_lo, seed_hi), common.cuh). nullptr / inv_tau 0: greedy argmax.
+struct SampleArgs {
+  float inv_tau;
+  uint32_t seed_lo, seed_hi;
+  const int* pos0;
+  int group;
+};
+
 // ---- gemm_simt.cu (fp32 storage) ------------------------------------------------------
 // out[m*ldo + n] += sum_k X[m*K + k] * W[n*K + k]   (fp32 W and X)
 void op_gemm_simt_acc(const float* W, const float* X, int N, int K, int M, float* out, int ldo,
                       cudaStream_t st);
 // argmax over n of sum_k X[m,k] W[n,k] -> atomicMax into keys[m]; logits optional
+// smp: sampled picks (nullptr: argmax of the logits)
 void op_gemm_simt_argmax(const float* W, const float* X, int N, int K, int M,
-                         unsigned long long* keys, float* logits, long ldl, cudaStream_t st);
+                         unsigned long long* keys, float* logits, long ldl,
+                         const SampleArgs* smp, cudaStream_t st);
 
 // ---- gemm_tc.cu (bf16, tcgen05) -------------------------------------------------------
 struct TcPlan {
@@ -188,8 +201,9 @@ void op_gemm_tc_swiglu(const TcPlan& p, void* h, long h_lo, unsigned* err, cudaS
 int tc_plan_shape(TcPlan* p, const void* W, int N, int K, const void* X, int M, int nsm,
                   bool argmax, bool split, int wide, int msplit, int splits);
 void op_gemm_tc_acc(const TcPlan& p, float* out, int ldo, unsigned* err, cudaStream_t st);
+// smp: sampled picks (nullptr: argmax of the logits)
 void op_gemm_tc_argmax(const TcPlan& p, unsigned long long* keys, float* logits, long ldl,
-                       unsigned* err, cudaStream_t st);
+                       const SampleArgs* smp, unsigned* err, cudaStream_t st);
 int tc_init_attributes();
 
 // ---- gdn.cu ----------------------------------------------------------------------------

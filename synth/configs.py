@@ -62,6 +62,10 @@ class DmtpConfig:
     draft_window: int = 4096
     rms_eps: float = 1e-6
     rope_theta: float = 10000.0
+    # verification: 0.0 greedy; > 0 the target's picks are samples at this temperature,
+    # drawn with the given sampling seed
+    temperature: float = 0.0
+    sample_seed: int = 0
 
     def __post_init__(self):
         if not self.layer_kinds:

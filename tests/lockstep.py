@@ -3,8 +3,8 @@
 Both start from the same prompts and weights. Each round the GPU runs first; the
 oracle then runs the same round on each sequence, adopting the GPU's pick at any
 argmax where the oracle's own top-1 and the GPU's id are within the near-tie gate
-(0.05 in logits) - so one near tie cannot make the two diverge for the rest of the
-run. Any pick outside the gate is a mismatch. Integer fields must then agree
+(0.05 in logits, or in the scores l / temperature + G under sampled verification) -
+so one near tie cannot make the two diverge for the rest of the run. Any pick outside the gate is a mismatch. Integer fields must then agree
 exactly; float fields within `tol` max-abs.
 """
 from __future__ import annotations
@@ -29,12 +29,13 @@ class Lockstep:
         self.seqs = list(range(len(prompts))) if seqs is None else list(seqs)
         self.gpu = DmtpRound(cfg, weights_gpu, prompts,
                              max_ctx or default_max_ctx(prompts, rounds))
-        self.oracle = OracleModel(cfg, {k: v.cpu() for k, v in weights_gpu.items()}, gate=GATE)
+        self.oracle = OracleModel(cfg, {k: v.cpu() for k, v in weights_gpu.items()}, gate=GATE,
+                                  temperature=cfg.temperature, sample_seed=cfg.sample_seed)
         kv, A, _ = self.gpu.read_state()
         self.states = {}
         self.adopted = []
         for b in self.seqs:
-            st = self.oracle.prefill(prompts[b], adopt_A=int(A[b]))
+            st = self.oracle.prefill(prompts[b], adopt_A=int(A[b]), b=b)
             assert not self.oracle.prefill_log["mismatch"], self.oracle.prefill_log
             self.adopted += self.oracle.prefill_log["adopted"]
             assert st.A == int(A[b]) and st.a == int(kv[b]) == len(prompts[b])

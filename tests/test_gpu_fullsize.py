@@ -46,6 +46,19 @@ def test_b32_full_size_sampled_sequence():
     ls.close()
 
 
+def test_b32_full_size_sampled_verification():
+    """Target-only sampled verification at temperature 1 on the full B32 batch, in the
+    head's bench launch shape; the oracle follows one sequence."""
+    from lockstep import Lockstep
+    cfg = CONFIGS["b32"].replace(temperature=1.0, sample_seed=12345)
+    prompts = make_prompts(cfg)
+    b = int(np.argmin([len(p) for p in prompts]))
+    ls = Lockstep(cfg, make_weights(cfg, "cuda"), prompts, rounds=2, seqs=[b])
+    for _ in range(2):
+        ls.step(tol=TOL)
+    ls.close()
+
+
 def test_hybrid_full_dims_lockstep():
     from lockstep import Lockstep
     cfg = CONFIGS["hybrid"].replace(batch=2, ctx_lo=96, ctx_hi=160)

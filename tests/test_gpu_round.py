@@ -37,6 +37,11 @@ HYB_R = CONFIGS["hybrid"].replace(name="hybrid_r", vocab=3000, d_model=256, n_la
                                   gdn_heads=4, gdn_dk=64, gdn_dv=64)
 
 
+# target-only sampled verification (DMTP §5): the verify picks are the target's samples
+TINY_S = TINY.replace(name="tiny_sampled", temperature=0.8, sample_seed=20260611)
+B32_RS = B32_R.replace(name="b32_r_sampled", temperature=1.0, sample_seed=0x5EED_0000_0007)
+
+
 def test_tiny_natural_16_rounds():
     ls = _lockstep(TINY, 16)
     for _ in range(16):
@@ -138,3 +143,78 @@ def test_round_host_matches_device_outputs():
         np.testing.assert_array_equal(out["n_accepted"].cpu().numpy(), n)
     a.close()
     b.close()
+
+
+def _sampled_stream(ls, b, n):
+    return ls.oracle.sampled_decode(ls.prompts[b], n, b=b)
+
+
+def test_tiny_sampled_natural_rounds():
+    """Sampled picks (CUDA-core head) in lock-step with the oracle's scores l / T + G,
+    and the committed stream equals plain one-token sampled decoding."""
+    ls = _lockstep(TINY_S, 12)
+    ref = _sampled_stream(ls, 0, 8 * 12 + 9)
+    assert ref != _greedy(ls, 0, len(ref))
+    stream = [ls.states[0].A]
+    for _ in range(12):
+        _, recs = ls.step(tol=TOL)
+        stream += recs[0]["committed"]
+    if not ls.adopted:   # an adopted near tie may branch off the oracle's own decode
+        assert stream == ref[:len(stream)]
+    ls.close()
+
+
+def test_tiny_noise_dominated_picks():
+    """At temperature 1000 the logits move the scores by < 1e-3: the picks are the argmax
+    of the Gumbel noise alone, so the noise's counter, word and sequence layout must
+    match the oracle's generator element for element."""
+    ls = _lockstep(TINY_S.replace(temperature=1000.0), 4)
+    for _ in range(4):
+        ls.step(tol=TOL)
+    ls.close()
+
+
+@pytest.mark.parametrize("wrong", [None, 0, 4, 6])
+def test_tiny_sampled_forced(wrong):
+    """Drafts forced to the sampled stream are all accepted; one wrong draft at row j
+    accepts j and commits the target's sample there; the stream stays the sampled one."""
+    ls = _lockstep(TINY_S, 8)
+    ref = _sampled_stream(ls, 0, 8 * 8 + 9)
+    P = len(ls.prompts[0])
+    stream = [ls.states[0].A]
+    for _ in range(8):
+        off = ls.states[0].a - P
+        d = list(ref[off + 1: off + 8])
+        if wrong is not None:
+            d[wrong] = (d[wrong] + 1) % (TINY.vocab - 1)
+        _, recs = ls.step(forced=np.array([d], np.int32), tol=TOL)
+        assert recs[0]["n"] == (7 if wrong is None else wrong)
+        stream += recs[0]["committed"]
+    if not ls.adopted:
+        assert stream == ref[:len(stream)]
+    ls.close()
+
+
+def test_b32_shape_sampled_tensor_core_head():
+    """Sampled picks from the tcgen05 head's epilogue (quad-shared Philox blocks) over
+    256 verify rows and a ragged vocabulary, float outputs within 2e-2."""
+    ls = _lockstep(B32_RS, 3)
+    for _ in range(3):
+        ls.step(tol=TOL)
+    ls.close()
+
+
+def test_b32_shape_sampled_graph_rounds():
+    """Captured-graph replays of sampled rounds: the noise follows each round's positions."""
+    ls = _lockstep(B32_RS, 4, seqs=[0, 9, 31])
+    for _ in range(4):
+        ls.step(floats=False)
+    ls.close()
+
+
+def test_temperature_validation():
+    from mtp_block_draft_gb300 import DmtpError, DmtpRound
+    w = make_weights(TINY, "cuda")
+    for t in (-1.0, 1e-6, float("nan"), float("inf")):
+        with pytest.raises(DmtpError):
+            DmtpRound(TINY.replace(temperature=t), w, make_prompts(TINY), 256)
