@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdmtp.so")
 
-SOURCES = ["dmtp.cu", "elementwise.cu", "attention.cu", "gemm_simt.cu", "gemm_tc.cu", "gdn.cu", "noalloc.cu", "attention_tc.cu"]
+SOURCES = ["dmtp.cu", "elementwise.cu", "attention.cu", "gemm_simt.cu", "gemm_tc.cu", "gdn.cu", "noalloc.cu", "attention_tc.cu", "head_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include"), "-I", CSRC]

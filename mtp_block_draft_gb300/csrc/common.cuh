@@ -142,18 +142,22 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 __device__ __forceinline__ uint32_t word4(const uint4& b, int i) {
   return i == 0 ? b.x : i == 1 ? b.y : i == 2 ? b.z : b.w;
 }
-// Gumbel(0, 1) noise G = -log(-log u) of one generator word, u = ((w >> 8) + 1/2) 2^-24
-// in (0, 1). E = -log u is formed without cancellation: for t = 1 - u < 2^-6 (exact in
-// fp32 there) by the series t + t^2/2 + t^3/3 + t^4/4 of -log(1 - t), whose relative
-// truncation error is below t^4/5; elsewhere E >= 0.0157 and the fp32 logarithm of u
-// (rounded to fp32) is accurate to ~1e-5 relative. G's absolute error is then ~1e-5.
-__device__ __forceinline__ float gumbel_of_word(uint32_t w) {
-  const uint32_t k = w >> 8;
-  const float u = ((float)k + 0.5f) * 5.9604644775390625e-8f;
-  const float t = ((float)(16777216u - k) - 0.5f) * 5.9604644775390625e-8f;
-  const float series = t * fmaf(t, fmaf(t, fmaf(t, 0.25f, 0.33333334f), 0.5f), 1.f);
-  const float e = t < 0.015625f ? series : -__logf(u);
-  return -__logf(e);
+// Gumbel(0, 1) noise of one generator word, in base-2 units: G = -ln(-ln u) with
+// u = ((w >> 8) + 1/2) 2^-24 in (0, 1) equals ln2 * G2 - ln(ln 2) for the returned
+// G2 = -log2(e2), e2 = -log2(u). So argmax_v (l_v / T + G_v) = argmax_v (l_v log2(e) / T
+// + G2_v): the sampled scores compare in this scaled form (one exact monotone map).
+// e2 is formed without cancellation: for t = 1 - u < 2^-6 (exact in fp32 there) from
+// the series -ln(1 - t) = t + t^2/2 + t^3/3 + ... (three terms: relative error below
+// t^3/4 < 1e-6), elsewhere (e2 > 0.022) from the fp32 base-2 logarithm of u. G2's
+// absolute error stays near 1e-5.
+__device__ __forceinline__ float gumbel2_of_word(uint32_t w) {
+  const float k = (float)(w >> 8);
+  const float u = fmaf(k, 5.9604644775390625e-8f, 2.98023223876953125e-8f);
+  const float t = fmaf(-k, 5.9604644775390625e-8f, 1.f) - 2.98023223876953125e-8f;
+  const float series =  // log2(e) (t + t^2/2 + t^3/3)
+      t * fmaf(t, fmaf(t, 0.48089834696298783f, 0.72134752044448170f), 1.4426950408889634f);
+  const float e2 = t < 0.015625f ? series : -__log2f(u);
+  return -__log2f(e2);
 }
 // Sampled verification: row m of the verify head is sequence b = m / group at position
 // p = pos0[b] + m % group; its sample for position p + 1 is argmax_v (l_v / tau + G_v),

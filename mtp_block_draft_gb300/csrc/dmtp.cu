@@ -24,6 +24,7 @@ namespace {
 
 struct Gemm {
   TcPlan tc;            // bf16 path
+  HeadPlan hp;          // bf16 path, argmax heads
   const void* W = nullptr;
   const void* X = nullptr;
   int N = 0, K = 0, M = 0;
@@ -308,8 +309,10 @@ int plan(dmtp_ctx* c, Gemm& g, const void* W, int N, int K, const void* X, int M
   g.argmax = argmax;
   g.split = split;
   if (!W) return DMTP_EINVAL;
+  if (c->dt == 1 && argmax)  // LM heads: one bf16 operand, token-major argmax kernel
+    return split || head_plan(&g.hp, W, N, K, X, M, c->nsm, 256, 8) ? DMTP_EINVAL : DMTP_OK;
   if (c->dt == 1)
-    return tc_plan(&g.tc, W, N, K, X, M, c->nsm, argmax, split) ? DMTP_EINVAL : DMTP_OK;
+    return tc_plan(&g.tc, W, N, K, X, M, c->nsm, split) ? DMTP_EINVAL : DMTP_OK;
   return DMTP_OK;
 }
 
@@ -384,13 +387,19 @@ void gemm_acc(dmtp_ctx* c, const Gemm& g, float* out, int ldo) {
   });
 }
 
+// The verify head's sampling: row m = b*8 + j of sequence b at position pos0[b] + j.
+SampleArgs verify_sampling(const dmtp_ctx* c) {
+  return SampleArgs{1.4426950408889634f / c->cfg.temperature, (uint32_t)c->cfg.sample_seed,
+                    (uint32_t)(c->cfg.sample_seed >> 32), c->rs.pos0, 8};
+}
+
 // smp: the verify head's sampled picks (nullptr: argmax picks)
 void gemm_argmax(dmtp_ctx* c, const Gemm& g, unsigned long long* keys, float* logits,
                  const SampleArgs* smp = nullptr) {
   const double bytes = ((double)g.N * g.K + (double)g.M * g.K) * esz(c) + 8.0 * g.M;
   launch(c, P_HEAD, bytes, 2.0 * g.M * g.N * g.K, [&] {
     if (c->dt == 1)
-      op_gemm_tc_argmax(g.tc, keys, logits, c->V, smp, c->err, c->st);
+      op_head_tc(g.hp, keys, logits, c->V, smp, c->err, c->st);
     else
       op_gemm_simt_argmax((const float*)g.W, (const float*)g.X, g.N, g.K, g.M, keys, logits,
                           c->V, smp, c->st);
@@ -626,8 +635,7 @@ void enqueue_round(dmtp_ctx* c, const Dbg& dbg, const int* forced) {
   launch(c, P_OTHER, 0, 0, [&] { op_verify_tokens(s, c->st); });
   target_forward(c, true);
   if (c->cfg.temperature > 0.f) {  // target-only sampled verification (DMTP §5)
-    const SampleArgs smp{1.f / c->cfg.temperature, (uint32_t)c->cfg.sample_seed,
-                         (uint32_t)(c->cfg.sample_seed >> 32), s.pos0, 8};
+    const SampleArgs smp = verify_sampling(c);
     gemm_argmax(c, c->head_v, s.keys + 7 * B, dbg.vl, &smp);
   } else {
     gemm_argmax(c, c->head_v, s.keys + 7 * B, dbg.vl);
@@ -661,19 +669,22 @@ int check_err(dmtp_ctx* c) {
 // each tile shape (128 or 256 weight rows per CTA, one or two token halves, K splits
 // around the wave-count choice), cold: the L2 is flushed by a 256 MB read before each
 // run, as in the round, where each weight matrix is streamed once. The fastest shape
-// serves every GEMM of that shape. Outputs go to scratch (the gate/up accumulator and
-// the argmax keys), which the round clears before use.
+// serves every GEMM of that shape. The LM heads are timed the same way over their tile
+// (128 or 256 vocabulary rows) and epilogue width (4 or 8 warps), the verify head with
+// its sampling epilogue when the context samples. Outputs go to scratch (the gate/up
+// accumulator and the argmax keys), which the round clears before use.
 namespace {
 struct TuneKey {
   int dev, N, K, M;
-  bool split, argmax, swiglu;
+  bool split, argmax, swiglu, sample;
   bool operator==(const TuneKey& o) const {
     return dev == o.dev && N == o.N && K == o.K && M == o.M && split == o.split &&
-           argmax == o.argmax && swiglu == o.swiglu;
+           argmax == o.argmax && swiglu == o.swiglu && sample == o.sample;
   }
 };
 struct TuneChoice {
-  int wide, msplit, splits;
+  int wide, msplit, splits;  // projection GEMMs
+  int nv, ew;                // LM heads: vocabulary rows per tile, epilogue warps
 };
 // Choices are kept for the life of the process: a later context on the same device
 // reuses them (same kernels, same reduction order, no second timing pass).
@@ -684,16 +695,30 @@ void collect(LayerPlans& p, std::vector<Gemm*>& v) {
   for (Gemm* g : {&p.qkv, &p.o, &p.gu, &p.down, &p.gq, &p.ga, &p.gb, &p.go}) v.push_back(g);
 }
 
-float time_plan(dmtp_ctx* c, const TcPlan& p, bool argmax, const void* flush,
+float time_plan(dmtp_ctx* c, const TcPlan& p, const void* flush, size_t flush_bytes,
+                cudaEvent_t e0, cudaEvent_t e1) {
+  float best = 1e30f;
+  for (int rep = 0; rep < 3; ++rep) {
+    op_l2_flush(flush, flush_bytes, c->err, c->st);
+    cudaEventRecord(e0, c->st);
+    op_gemm_tc_acc(p, c->gu, p.N, c->err, c->st);
+    cudaEventRecord(e1, c->st);
+    float ms = 1e30f;
+    if (cudaEventSynchronize(e1) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess)
+      return 1e30f;
+    best = std::min(best, ms);
+  }
+  return best;
+}
+
+float time_head(dmtp_ctx* c, const HeadPlan& p, const SampleArgs* smp, const void* flush,
                 size_t flush_bytes, cudaEvent_t e0, cudaEvent_t e1) {
   float best = 1e30f;
   for (int rep = 0; rep < 3; ++rep) {
     op_l2_flush(flush, flush_bytes, c->err, c->st);
     cudaEventRecord(e0, c->st);
-    if (argmax)
-      op_gemm_tc_argmax(p, c->rs.keys, nullptr, 0, nullptr, c->err, c->st);
-    else
-      op_gemm_tc_acc(p, c->gu, p.N, c->err, c->st);
+    op_head_tc(p, c->rs.keys, nullptr, 0, smp, c->err, c->st);
     cudaEventRecord(e1, c->st);
     float ms = 1e30f;
     if (cudaEventSynchronize(e1) != cudaSuccess ||
@@ -747,15 +772,23 @@ int autotune(dmtp_ctx* c, const void* flush, size_t flush_bytes) {
   for (Gemm* g : all) {
     if (!g->W) continue;
     if (!g->swiglu && !g->argmax && (size_t)g->M * g->N > scratch) continue;  // default shape
-    const TuneKey key{dev, g->N, g->K, g->M, g->split, g->argmax, g->swiglu};
+    // the verify head under sampled verification runs the sampling epilogue
+    const bool sample = g == &c->head_v && c->cfg.temperature > 0.f;
+    const SampleArgs smp = sample ? verify_sampling(c) : SampleArgs{};
+    const TuneKey key{dev, g->N, g->K, g->M, g->split, g->argmax, g->swiglu, sample};
     const TuneChoice* hit = nullptr;
     for (auto& e : g_tune)
       if (e.first == key) hit = &e.second;
+    if (hit && g->argmax) {
+      if (head_plan(&g->hp, g->W, g->N, g->K, g->X, g->M, c->nsm, hit->nv, hit->ew))
+        rc = DMTP_EINVAL;
+      continue;
+    }
     if (hit) {
       const int r = g->swiglu ? tc_plan_swiglu(&g->tc, g->W, c->F, g->K, g->X, g->M, c->nsm,
                                                g->split, hit->msplit)
                               : tc_plan_shape(&g->tc, g->W, g->N, g->K, g->X, g->M, c->nsm,
-                                              g->argmax, g->split, hit->wide, hit->msplit,
+                                              g->split, hit->wide, hit->msplit,
                                               hit->splits);
       if (r) rc = DMTP_EINVAL;
       continue;
@@ -775,41 +808,60 @@ int autotune(dmtp_ctx* c, const void* flush, size_t flush_bytes) {
         }
       }
       g->tc = best_p;
-      g_tune.push_back({key, TuneChoice{2, best_p.msplit, 1}});
+      g_tune.push_back({key, TuneChoice{2, best_p.msplit, 1, 0, 0}});
       continue;
     }
-    TuneChoice best{g->tc.wide, g->tc.msplit, g->tc.splits};
-    float best_ms = time_plan(c, g->tc, g->argmax, flush, flush_bytes, e0, e1);
+    if (g->argmax) {  // LM head: vocabulary tile of 128 or 256 rows, 4 or 8 epilogue warps
+      HeadPlan best_p = g->hp;
+      float best_t = 1e30f;
+      for (int nv = 128; nv <= 256; nv *= 2)
+        for (int ew = 4; ew <= 8; ew *= 2) {
+          HeadPlan p;
+          if (head_plan(&p, g->W, g->N, g->K, g->X, g->M, c->nsm, nv, ew)) continue;
+          const float t = time_head(c, p, sample ? &smp : nullptr, flush, flush_bytes, e0, e1);
+          if (t < best_t) {
+            best_t = t;
+            best_p = p;
+          }
+        }
+      g->hp = best_p;
+      g_tune.push_back({key, TuneChoice{0, 0, 0, best_p.NV, best_p.ew}});
+      if (verbose)
+        fprintf(stderr, "dmtp: head V=%d K=%d M=%d%s: %d vocabulary rows per tile, %d epilogue "
+                "warps, %.1f us\n", g->N, g->K, g->M, sample ? " sampled" : "", best_p.NV,
+                best_p.ew, best_t * 1e3f);
+      continue;
+    }
+    TuneChoice best{g->tc.wide, g->tc.msplit, g->tc.splits, 0, 0};
+    float best_ms = time_plan(c, g->tc, flush, flush_bytes, e0, e1);
     for (int wide = 1; wide <= 2; ++wide)
       for (int ms = 1; ms <= 2; ++ms) {
         TcPlan p0;
-        if (tc_plan_shape(&p0, g->W, g->N, g->K, g->X, g->M, c->nsm, g->argmax, g->split, wide,
-                          ms, 0))
+        if (tc_plan_shape(&p0, g->W, g->N, g->K, g->X, g->M, c->nsm, g->split, wide, ms, 0))
           continue;
         const int cand[3] = {p0.splits, std::max(1, p0.splits / 2),
                              std::min(32, 2 * p0.splits)};
-        const int ncand = g->argmax ? 1 : 3;
-        for (int i = 0; i < ncand; ++i) {
+        for (int i = 0; i < 3; ++i) {
           if (i > 0 && (cand[i] == cand[0] || (i == 2 && cand[2] == cand[1]))) continue;
           TcPlan p;
-          if (tc_plan_shape(&p, g->W, g->N, g->K, g->X, g->M, c->nsm, g->argmax, g->split,
-                            wide, ms, cand[i]))
+          if (tc_plan_shape(&p, g->W, g->N, g->K, g->X, g->M, c->nsm, g->split, wide, ms,
+                            cand[i]))
             continue;
-          const float t = time_plan(c, p, g->argmax, flush, flush_bytes, e0, e1);
+          const float t = time_plan(c, p, flush, flush_bytes, e0, e1);
           if (t < best_ms) {
             best_ms = t;
-            best = TuneChoice{wide, ms, p.splits};
+            best = TuneChoice{wide, ms, p.splits, 0, 0};
           }
         }
       }
-    if (tc_plan_shape(&g->tc, g->W, g->N, g->K, g->X, g->M, c->nsm, g->argmax, g->split,
-                      best.wide, best.msplit, best.splits))
+    if (tc_plan_shape(&g->tc, g->W, g->N, g->K, g->X, g->M, c->nsm, g->split, best.wide,
+                      best.msplit, best.splits))
       rc = DMTP_EINVAL;
     g_tune.push_back({key, best});
     if (verbose)
-      fprintf(stderr, "dmtp: gemm N=%d K=%d M=%d%s%s: %d x 128 weight rows, %d token part(s), "
+      fprintf(stderr, "dmtp: gemm N=%d K=%d M=%d%s: %d x 128 weight rows, %d token part(s), "
               "%d K split(s), %.1f us\n", g->N, g->K, g->M, g->split ? " split" : "",
-              g->argmax ? " argmax" : "", best.wide, best.msplit, best.splits, best_ms * 1e3f);
+              best.wide, best.msplit, best.splits, best_ms * 1e3f);
   }
   cudaEventDestroy(e0);
   cudaEventDestroy(e1);
@@ -901,7 +953,8 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
     delete c;
     return DMTP_EINVAL;
   }
-  if (c->dt == 1 && (tc_init_attributes() || attn_tc_init_attributes())) {
+  if (c->dt == 1 && (tc_init_attributes() || attn_tc_init_attributes() ||
+                     head_init_attributes())) {
     delete c;
     return DMTP_ECUDA;
   }

@@ -9,8 +9,8 @@ namespace dmtp {
 
 static constexpr int BN = 64, BM = 32, BK = 16;
 
-// MODE 0: out += acc, 1: argmax keys (+ logits); with smp.inv_tau > 0 the keys rank
-// the sampled scores l * inv_tau + G (common.cuh) instead of the logits.
+// MODE 0: out += acc, 1: argmax keys (+ logits); with smp.scale2 > 0 the keys rank
+// the sampled scores l * scale2 + G2 (common.cuh) instead of the logits.
 template <int MODE>
 __global__ void __launch_bounds__(256) k_gemm_simt(const float* __restrict__ W,
                                                    const float* __restrict__ X, int N, int K,
@@ -50,9 +50,9 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const float* __restrict__ W,
       if (n < N && m < M) out[(long)m * ldo + n] += acc[j];
     } else {
       float score = acc[j];
-      if (smp.inv_tau > 0.f && n < N && m < M) {
+      if (smp.scale2 > 0.f && n < N && m < M) {
         const uint4 blk = sample_block(n >> 2, m, smp.pos0, smp.group, smp.seed_lo, smp.seed_hi);
-        score = fmaf(acc[j], smp.inv_tau, gumbel_of_word(word4(blk, n & 3)));
+        score = fmaf(acc[j], smp.scale2, gumbel2_of_word(word4(blk, n & 3)));
       }
       unsigned long long key = (n < N && m < M) ? argmax_key(score, n) : 0ull;
 #pragma unroll

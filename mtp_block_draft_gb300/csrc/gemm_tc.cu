@@ -24,9 +24,7 @@
 // the activations keep ~16 significant bits while the weights stay bf16 and each
 // weight byte is still read once.
 //
-// The LM-head variant fuses the row argmax (DMTP blog §6.5: the vocabulary output
-// layer scores every token): per column the CTA reduces its 128 vocabulary rows to a
-// packed (value, index) key and merges it with one 64-bit atomicMax per column.
+// The LM heads (GEMM fused with the row argmax) run token-major in head_tc.cu.
 //
 // Every mbarrier wait is bounded (common.cuh); a timeout sets the error word, the
 // producer drains its in-flight copies and the CTA frees its TMEM before returning.
@@ -54,14 +52,10 @@ struct TcArgs {
   int acc_cols;    // TMEM columns per accumulator
   float* out;
   int ldo;
-  unsigned long long* keys;
-  float* logits;
-  long ldl;
   bf16* h;         // EPI 2: SwiGLU output [M][F] (hi), remainder at h + h_lo
   long h_lo;
   int F;           // EPI 2: gate rows 0..F-1, up rows F..2F-1 of W
   unsigned* err;
-  SampleArgs smp;  // EPI 1: sampled picks when smp.inv_tau > 0
 };
 
 // 16 accumulator columns of this warp's lanes at taddr, plus (merged) the lo columns
@@ -78,66 +72,13 @@ __device__ __forceinline__ void acc_ld16(uint32_t taddr, int mct, float (&v)[16]
     v[j] = MERGED ? __uint_as_float(rv[j]) + __uint_as_float(rw[j]) : __uint_as_float(rv[j]);
 }
 
-// Column of a 16-column block that lane `lane` holds after warp_colmax16.
-__device__ __forceinline__ int col16(int lane) {
-  return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
-}
-// k[0..15]: this lane's keys of 16 columns. On return k[0] is the maximum over the 32
-// lanes of column col16(lane). Each step exchanges the half of the columns the partner
-// keeps: 8 + 4 + 2 + 1 + 1 shuffles instead of 5 per column.
-__device__ __forceinline__ void warp_colmax16(unsigned long long (&k)[16], int lane) {
-#pragma unroll
-  for (int half = 8, off = 16; half >= 1; half >>= 1, off >>= 1) {
-    const bool upper = (lane & off) != 0;  // keeps columns half..2*half-1 of the block
-#pragma unroll
-    for (int i = 0; i < half; ++i) {
-      const unsigned long long keep = upper ? k[half + i] : k[i];
-      const unsigned long long give = upper ? k[i] : k[half + i];
-      const unsigned long long got = __shfl_xor_sync(0xffffffffu, give, off);
-      k[i] = got > keep ? got : keep;
-    }
-  }
-  const unsigned long long got = __shfl_xor_sync(0xffffffffu, k[0], 1);
-  k[0] = got > k[0] ? got : k[0];
-}
-
-// Keys of the sampled scores v[j] * inv_tau + G (common.cuh) of token rows m0 + j,
-// j = 0..15, for this lane's vocabulary row n. The four lanes of a quad hold rows
-// n = 4q + r that share Philox counter word q: lane r computes the blocks of token rows
-// m0 + 4t + r (t = 0..3), and three exchanges per t hand every lane word r of each of
-// the quad's four blocks. Token rows past M take row M - 1's block (keys unused).
-__device__ __forceinline__ void sample_keys16(const TcArgs& a, int n, int m0, int lane,
-                                              const float (&v)[16],
-                                              unsigned long long (&key)[16]) {
-  const int r = lane & 3;
-  uint32_t w[16];
-#pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    const int m = min(m0 + 4 * t + r, a.M - 1);
-    const uint4 blk = sample_block(n >> 2, m, a.smp.pos0, a.smp.group, a.smp.seed_lo,
-                                   a.smp.seed_hi);
-    uint32_t q[4];  // q[x]: word r of the block of token row m0 + 4t + (r ^ x)
-    q[0] = word4(blk, r);
-#pragma unroll
-    for (int x = 1; x < 4; ++x) q[x] = __shfl_xor_sync(0xffffffffu, word4(blk, r ^ x), x);
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      const int x = r ^ s;
-      w[4 * t + s] = x == 0 ? q[0] : x == 1 ? q[1] : x == 2 ? q[2] : q[3];
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < 16; ++j)
-    key[j] = (n < a.N) ? argmax_key(fmaf(v[j], a.smp.inv_tau, gumbel_of_word(w[j])), n) : 0ull;
-}
-
 __host__ __device__ inline uint32_t tmem_cols_for(int cols) {
   uint32_t c = 32;
   while (c < (uint32_t)cols) c <<= 1;
   return c;
 }
 
-// EPI 0: atomic add into out, 1: argmax keys (+ logits), 2: SwiGLU (WIDE = 2, no K
+// EPI 0: atomic add into out, 2: SwiGLU (WIDE = 2, no K
 // split: weight half 0 = gate rows n0.., half 1 = the matching up rows F + n0.., and the
 // epilogue writes silu(g) * u as the next GEMM's bf16 pair). WIDE, NMMA (MMAs per k
 // step and weight half) and MERGED are compile-time copies of a.wide, (merged ? 1 : nx)
@@ -158,7 +99,6 @@ __global__ void __launch_bounds__(128, 1)
   uint64_t* empty = full + S;
   uint64_t* accum = empty + S;
   uint32_t* tmem_slot = (uint32_t*)(accum + 1);
-  unsigned long long* red = (unsigned long long*)(accum + 2);  // [4][mct] (argmax)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // grid: (token halves, weight tiles, K splits); CTAs sharing a weight tile are
@@ -305,46 +245,6 @@ __global__ void __launch_bounds__(128, 1)
         }
       }
     }
-  } else {
-    const bool okb = __syncthreads_and(ok);
-    if (okb) {
-#pragma unroll
-      for (int h = 0; h < WIDE; ++h) {
-        const int n = n0 + h * kHalfN + warp * 32 + lane;
-        const uint32_t tbase = tmem + h * a.acc_cols + ((uint32_t)(warp * 32) << 16);
-        for (int c = 0; c < a.mct; c += 16) {
-          float v[16];
-          acc_ld16<MERGED>(tbase + c, a.mct, v);
-          if (a.logits && n < a.N) {  // debug copy of the scores
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (mrow0 + c + j < a.M) a.logits[(long)(mrow0 + c + j) * a.ldl + n] = v[j];
-          }
-          // column maxima over the warp's 32 rows: a butterfly that halves the columns
-          // each lane keeps at every step (16 -> 8 -> 4 -> 2 -> 1), then pairs agree
-          unsigned long long key[16];
-          if (a.smp.inv_tau > 0.f) {
-            sample_keys16(a, n, mrow0 + c, lane, v, key);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) key[j] = (n < a.N) ? argmax_key(v[j], n) : 0ull;
-          }
-          warp_colmax16(key, lane);
-          // lane holds column col16(lane) (lanes 2i and 2i+1 the same one)
-          if ((lane & 1) == 0) {
-            const int ml = c + col16(lane);
-            unsigned long long* r = &red[warp * a.mct + ml];
-            *r = (h == 0 || key[0] > *r) ? key[0] : *r;
-          }
-        }
-      }
-      __syncthreads();
-      for (int ml = threadIdx.x; ml < a.mct && mrow0 + ml < a.M; ml += blockDim.x) {
-        unsigned long long k = red[ml];
-        for (int w = 1; w < 4; ++w) k = red[w * a.mct + ml] > k ? red[w * a.mct + ml] : k;
-        atomicMax(&a.keys[mrow0 + ml], k);
-      }
-    }
   }
   tc_fence_before();
   __syncthreads();
@@ -422,10 +322,9 @@ int tc_make_tmap3s(CUtensorMap* tm, const void* base, uint64_t d0, uint64_t d1, 
   return r == CUDA_SUCCESS ? 0 : -3;
 }
 
-static size_t smem_bytes(int wide, int mct, int xrows, int stages, bool argmax) {
+static size_t smem_bytes(int wide, int xrows, int stages) {
   size_t b = 1024 + (size_t)stages * (wide * kHalfBytes + (size_t)xrows * kBlockK * 2);
   b += (2 * stages + 2) * 8;
-  if (argmax) b += 4 * (size_t)mct * 8;
   return b;
 }
 
@@ -434,7 +333,7 @@ static constexpr size_t kSmemBudget = 200 * 1024;
 int tc_mt(int M) { return std::max(16, (M + 15) / 16 * 16); }
 
 int tc_plan_shape(TcPlan* p, const void* W, int N, int K, const void* X, int M, int nsm,
-                  bool argmax, bool split, int wide, int msplit, int splits) {
+                  bool split, int wide, int msplit, int splits) {
   if (M < 1 || M > 256 || K % kBlockK || N < 1 || (wide != 1 && wide != 2) ||
       (msplit != 1 && msplit != 2))
     return -10;
@@ -461,14 +360,14 @@ int tc_plan_shape(TcPlan* p, const void* W, int N, int K, const void* X, int M, 
   if (wide * p->acc_cols > 512) return -10;
   const int xrows = p->xbox * p->nx;
   int st = 8;
-  while (st > 2 && smem_bytes(wide, p->mct, xrows, st, argmax) > kSmemBudget) --st;
+  while (st > 2 && smem_bytes(wide, xrows, st) > kSmemBudget) --st;
   p->stages = st;
-  p->smem = smem_bytes(wide, p->mct, xrows, st, argmax);
+  p->smem = smem_bytes(wide, xrows, st);
   if (p->smem > kSmemBudget) return -10;
   const int tiles = (N + kHalfN * wide - 1) / (kHalfN * wide) * msplit;
   const int nkb = K / kBlockK;
   int best = splits > 0 ? std::min(splits, nkb) : 1;
-  if (!argmax && splits <= 0) {
+  if (splits <= 0) {
     // minimise waves(tiles * s) * (k blocks per CTA + fixed cost of ~3 k blocks)
     double best_cost = 1e30;
     for (int s = 1; s <= std::min(nkb, 32); ++s) {
@@ -480,7 +379,6 @@ int tc_plan_shape(TcPlan* p, const void* W, int N, int K, const void* X, int M, 
       }
     }
   }
-  if (argmax) best = 1;
   p->splits = best;
   int r = tc_make_tmap(&p->tmW, W, (uint64_t)N, (uint64_t)K, (uint32_t)(kHalfN * wide));
   if (r) return r;
@@ -497,7 +395,7 @@ int tc_plan_shape(TcPlan* p, const void* W, int N, int K, const void* X, int M, 
 
 int tc_plan_swiglu(TcPlan* p, const void* W, int F, int K, const void* X, int M, int nsm,
                    bool split, int msplit) {
-  int r = tc_plan_shape(p, W, 2 * F, K, X, M, nsm, false, split, 2, msplit, 1);
+  int r = tc_plan_shape(p, W, 2 * F, K, X, M, nsm, split, 2, msplit, 1);
   if (r) return r;
   p->swiglu = 1;
   p->F = F;
@@ -505,9 +403,8 @@ int tc_plan_swiglu(TcPlan* p, const void* W, int F, int K, const void* X, int M,
   return tc_make_tmap(&p->tmW, W, (uint64_t)2 * F, (uint64_t)K, (uint32_t)kHalfN);
 }
 
-int tc_plan(TcPlan* p, const void* W, int N, int K, const void* X, int M, int nsm, bool argmax,
-            bool split) {
-  return tc_plan_shape(p, W, N, K, X, M, nsm, argmax, split, 1, 1, 0);
+int tc_plan(TcPlan* p, const void* W, int N, int K, const void* X, int M, int nsm, bool split) {
+  return tc_plan_shape(p, W, N, K, X, M, nsm, split, 1, 1, 0);
 }
 
 // The kernel instantiation for a plan: (wide, MMAs per k step, merged).
@@ -531,8 +428,6 @@ int tc_init_attributes() {
   void (*ks[])(const CUtensorMap, const CUtensorMap, TcArgs) = {
       k_gemm_tc<0, 1, 1, true>,  k_gemm_tc<0, 1, 1, false>, k_gemm_tc<0, 1, 2, false>,
       k_gemm_tc<0, 2, 1, true>,  k_gemm_tc<0, 2, 1, false>, k_gemm_tc<0, 2, 2, false>,
-      k_gemm_tc<1, 1, 1, true>,  k_gemm_tc<1, 1, 1, false>, k_gemm_tc<1, 1, 2, false>,
-      k_gemm_tc<1, 2, 1, true>,  k_gemm_tc<1, 2, 1, false>, k_gemm_tc<1, 2, 2, false>,
       k_gemm_tc<2, 2, 1, true>,  k_gemm_tc<2, 2, 1, false>, k_gemm_tc<2, 2, 2, false>};
   for (auto k : ks)
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
@@ -542,31 +437,19 @@ int tc_init_attributes() {
 }
 
 void op_gemm_tc_swiglu(const TcPlan& p, void* h, long h_lo, unsigned* err, cudaStream_t st) {
-  TcArgs a{p.N,        p.K,     p.M,   p.MT,     p.stages,   p.wide,  p.mct,
-           p.split,    p.xbox,  p.nx,  p.x3d,    p.merged,   p.acc_cols, nullptr,
-           0,          nullptr, nullptr, 0,      (bf16*)h,   h_lo,    p.F,
-           err};
+  TcArgs a{p.N,     p.K,     p.M,     p.MT,     p.stages, p.wide, p.mct,
+           p.split, p.xbox,  p.nx,    p.x3d,    p.merged, p.acc_cols, nullptr,
+           0,       (bf16*)h, h_lo,   p.F,      err};
   dim3 grid(p.msplit, (p.F + kHalfN - 1) / kHalfN, 1);
   kernel_for<2>(p)<<<grid, 128, p.smem, st>>>(p.tmW, p.tmX, a);
 }
 
 void op_gemm_tc_acc(const TcPlan& p, float* out, int ldo, unsigned* err, cudaStream_t st) {
-  TcArgs a{p.N,        p.K,     p.M,     p.MT,     p.stages,   p.wide,  p.mct,
-           p.split,    p.xbox,  p.nx,    p.x3d,    p.merged,   p.acc_cols, out,
-           ldo,        nullptr, nullptr, 0,        nullptr,    0,       0,
-           err};
+  TcArgs a{p.N,     p.K,     p.M,     p.MT,     p.stages, p.wide, p.mct,
+           p.split, p.xbox,  p.nx,    p.x3d,    p.merged, p.acc_cols, out,
+           ldo,     nullptr, 0,       0,        err};
   dim3 grid(p.msplit, (p.N + kHalfN * p.wide - 1) / (kHalfN * p.wide), p.splits);
   kernel_for<0>(p)<<<grid, 128, p.smem, st>>>(p.tmW, p.tmX, a);
-}
-
-void op_gemm_tc_argmax(const TcPlan& p, unsigned long long* keys, float* logits, long ldl,
-                       const SampleArgs* smp, unsigned* err, cudaStream_t st) {
-  TcArgs a{p.N,        p.K,     p.M,     p.MT,     p.stages,   p.wide,  p.mct,
-           p.split,    p.xbox,  p.nx,    p.x3d,    p.merged,   p.acc_cols, nullptr,
-           0,          keys,    logits,  ldl,      nullptr,    0,       0,
-           err,        smp ? *smp : SampleArgs{}};
-  dim3 grid(p.msplit, (p.N + kHalfN * p.wide - 1) / (kHalfN * p.wide), 1);
-  kernel_for<1>(p)<<<grid, 128, p.smem, st>>>(p.tmW, p.tmX, a);
 }
 
 }  // namespace dmtp

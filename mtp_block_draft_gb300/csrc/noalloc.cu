@@ -10,7 +10,7 @@
 // until the process exits.
 //
 // The first call on a device sets up that device (it looks up the array's device address
-// with cudaGetSymbolAddress and raises the GEMM kernel's shared-memory limit); make that
+// with cudaGetSymbolAddress and raises the head kernel's shared-memory limit); make that
 // first call before any stream capture. All calls share the one array: calls that may
 // overlap on the GPU (other streams, other threads) race on it and must be serialised by
 // the caller.
@@ -33,18 +33,23 @@ static __device__ __align__(256) unsigned char g_scratch[kOperandBytes + kKeyByt
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_addr[kMaxDevices] = {};
+int g_nsm[kMaxDevices] = {};
 
-int device_scratch(void** out) {
+int device_scratch(void** out, int* nsm) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DMTP_ECUDA;
   std::lock_guard<std::mutex> lk(g_mu);
   if (!g_addr[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return DMTP_ECUDA;
-    if (dmtp::tc_init_attributes()) return DMTP_ECUDA;
+    if (dmtp::head_init_attributes()) return DMTP_ECUDA;
+    if (cudaDeviceGetAttribute(&g_nsm[dev], cudaDevAttrMultiProcessorCount, dev) !=
+        cudaSuccess)
+      return DMTP_ECUDA;
     g_addr[dev] = p;
   }
   *out = g_addr[dev];
+  *nsm = g_nsm[dev];
   return DMTP_OK;
 }
 
@@ -58,19 +63,20 @@ extern "C" int dmtp_t1_head_noalloc(const void* head, const void* norm_gain, con
       vocab < 1 || ((uintptr_t)head & 15))
     return DMTP_EINVAL;
   void* base = nullptr;
-  int r = device_scratch(&base);
+  int nsm = 0;
+  int r = device_scratch(&base, &nsm);
   if (r) return r;
   cudaStream_t st = (cudaStream_t)stream;
   void* X = base;
   unsigned long long* keys = (unsigned long long*)((char*)base + kOperandBytes);
-  dmtp::TcPlan plan;
-  // the same single-bf16 operand as the round's LM-head GEMMs
-  if (dmtp::tc_plan(&plan, head, vocab, d_model, X, rows, 1, true, false)) return DMTP_EINVAL;
+  dmtp::HeadPlan plan;
+  // the round's LM-head kernel on the same single-bf16 operand
+  if (dmtp::head_plan(&plan, head, vocab, d_model, X, rows, nsm, 256, 8)) return DMTP_EINVAL;
   // keys start at zero for the atomic max; the operand rows are fully rewritten
   if (cudaMemsetAsync(keys, 0, (size_t)rows * 8, st) != cudaSuccess) return DMTP_ECUDA;
   dmtp::op_rmsnorm(1, h, d_model, norm_gain, X, d_model, 0, nullptr, 0,
                    nullptr, 0, 0, rows, d_model, eps, dmtp::RowMap(), st);
-  dmtp::op_gemm_tc_argmax(plan, keys, logits, vocab, nullptr, nullptr, st);
+  dmtp::op_head_tc(plan, keys, logits, vocab, nullptr, nullptr, st);
   dmtp::op_keys_to_ids(keys, rows, 1, ids, 1, 0, nullptr, 0, 0, st);
   return cudaPeekAtLastError() == cudaSuccess ? DMTP_OK : DMTP_ECUDA;
 }

@@ -141,10 +141,11 @@ int attn_tc_init_attributes();
 
 // Target-only sampled verification in the verify head's argmax epilogue: row m is
 // sequence m / group at position pos0[m / group] + m % group, and its pick is the
-// sample argmax_v (l_v * inv_tau + G_v) for the next position (Philox4x32-10 Gumbel
-// noise keyed by (seed_lo, seed_hi), common.cuh). nullptr / inv_tau 0: greedy argmax.
+// sample argmax_v (l_v / T + G_v) for the next position (Philox4x32-10 Gumbel noise
+// keyed by (seed_lo, seed_hi), common.cuh), compared as l_v * scale2 + G2_v with
+// scale2 = log2(e) / T. nullptr / scale2 0: greedy argmax.
 struct SampleArgs {
-  float inv_tau;
+  float scale2;
   uint32_t seed_lo, seed_hi;
   const int* pos0;
   int group;
@@ -189,8 +190,7 @@ int tc_make_tmap3s(CUtensorMap* tm, const void* base, uint64_t d0, uint64_t d1, 
                    uint64_t s1, uint64_t s2, uint32_t b1, uint32_t b2);
 // Builds the tensor maps and launch shape for out[M,N] = X[M,K] . W[N,K]^T. split: X
 // holds 2*tc_mt(M) rows, the bf16 high halves then the low halves (X = hi + lo).
-int tc_plan(TcPlan* p, const void* W, int N, int K, const void* X, int M, int nsm,
-            bool argmax, bool split);
+int tc_plan(TcPlan* p, const void* W, int N, int K, const void* X, int M, int nsm, bool split);
 // Gate/up GEMM with the SwiGLU epilogue: W = [gate; up] ([2F, K]), each CTA pairs gate
 // rows n0.. with up rows F + n0.. (two accumulators) and writes h = silu(g) * u, a bf16
 // pair [M][F] (remainder at h + h_lo), so no fp32 output or separate SwiGLU pass.
@@ -199,12 +199,28 @@ int tc_plan_swiglu(TcPlan* p, const void* W, int F, int K, const void* X, int M,
 void op_gemm_tc_swiglu(const TcPlan& p, void* h, long h_lo, unsigned* err, cudaStream_t st);
 // tc_plan with the tile shape given: wide (1, 2), msplit (1, 2) and splits (<= 0: chosen).
 int tc_plan_shape(TcPlan* p, const void* W, int N, int K, const void* X, int M, int nsm,
-                  bool argmax, bool split, int wide, int msplit, int splits);
+                  bool split, int wide, int msplit, int splits);
 void op_gemm_tc_acc(const TcPlan& p, float* out, int ldo, unsigned* err, cudaStream_t st);
-// smp: sampled picks (nullptr: argmax of the logits)
-void op_gemm_tc_argmax(const TcPlan& p, unsigned long long* keys, float* logits, long ldl,
-                       const SampleArgs* smp, unsigned* err, cudaStream_t st);
 int tc_init_attributes();
+
+// ---- head_tc.cu (bf16 LM head with fused argmax, tcgen05) -------------------------------
+// keys[m] = max over v of argmax_key(l[m][v], v) with l = X[m] . W[v] (X [M, K] bf16, one
+// operand; W [V, K] bf16), or of the sampled scores l * scale2 + G2 under smp. Token-major
+// persistent kernel: tokens are the MMA's M side (TH halves of 128 rows), NV (128 or
+// 256) vocabulary rows per tile, one CTA per SM.
+struct HeadPlan {
+  CUtensorMap tmW, tmX;
+  int V, K, M, MT, TH, NV, ew, tiles, grid, stages;
+  size_t smem;
+};
+// ew: epilogue warps (4 or 8)
+int head_plan(HeadPlan* p, const void* W, int V, int K, const void* X, int M, int nsm, int nv,
+              int ew);
+// logits (optional, fp32 [M][ldl]) receives the raw logits; smp: sampled picks (nullptr:
+// argmax of the logits). keys must hold zeros (or earlier keys to combine with).
+void op_head_tc(const HeadPlan& p, unsigned long long* keys, float* logits, long ldl,
+                const SampleArgs* smp, unsigned* err, cudaStream_t st);
+int head_init_attributes();
 
 // ---- gdn.cu ----------------------------------------------------------------------------
 struct GdnArgs {
