@@ -32,6 +32,7 @@ import json
 import os
 import statistics
 import subprocess
+import threading
 import sys
 import time
 
@@ -70,7 +71,9 @@ def _traffic(kernel: str, alg_bytes_per_launch: float):
 
 
 class Clocks:
-    """nvidia-smi sampler for the timed region (200 ms period)."""
+    """nvidia-smi sampler for the timed region (200 ms period). The samples are read by a
+    thread; ready() waits for the first one, so the sampler is running before the timed
+    region starts."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -78,6 +81,8 @@ class Clocks:
 
     def __init__(self, gpu_index: int):
         self.p = None
+        self.lines = []
+        self.t = None
         try:
             self.p = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
@@ -85,15 +90,32 @@ class Clocks:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.p = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.p.stdout:
+            self.lines.append(line)
+
+    def ready(self, timeout: float = 10.0):
+        t0 = time.time()
+        while self.p is not None and not self.lines and time.time() - t0 < timeout:
+            time.sleep(0.02)
+        self.n0 = len(self.lines)  # samples taken before the timed region are not used
 
     def stop(self):
         if self.p is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        lines = list(self.lines[getattr(self, "n0", 0):])
         self.p.terminate()
-        out, _ = self.p.communicate(timeout=10)
+        try:
+            self.p.wait(timeout=10)
+        except Exception:
+            pass
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
+        for line in lines:
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
@@ -259,7 +281,7 @@ def run_reference(args, cfg):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="b32")
@@ -320,6 +342,7 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     clocks = Clocks(local)
+    clocks.ready()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     # the profiler start/stop marks let an external profiler skip the prefill

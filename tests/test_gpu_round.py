@@ -212,6 +212,16 @@ def test_b32_shape_sampled_graph_rounds():
     ls.close()
 
 
+def test_hybrid_shape_sampled_with_snapshots():
+    """Sampled verification on the hybrid target (Gated DeltaNet snapshots): the noise
+    follows each sequence's own positions while the rollback swaps snapshot slots."""
+    cfg = HYB_R.replace(name="hybrid_r_sampled", temperature=0.9, sample_seed=4242)
+    ls = _lockstep(cfg, 4)
+    for _ in range(4):
+        ls.step(tol=TOL)
+    ls.close()
+
+
 def test_temperature_validation():
     from mtp_block_draft_gb300 import DmtpError, DmtpRound
     w = make_weights(TINY, "cuda")
