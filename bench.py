@@ -166,7 +166,8 @@ def oracle_sample(cfg, weights, prompts, rounds: int, budget_s: float = 30.0):
     b = int(np.argmin([len(p) for p in prompts]))
     t0 = time.perf_counter()
     om = OracleModel(cfg, {k: v.cpu() for k, v in weights.items()},
-                     temperature=cfg.temperature, sample_seed=cfg.sample_seed)
+                     temperature=cfg.temperature, sample_seed=cfg.sample_seed,
+                     draft_head_fp8=cfg.draft_head_fp8)
     st = om.prefill(prompts[b], b=b)
     setup = time.perf_counter() - t0
     tokens, el, done = 0, 0.0, 0
@@ -242,6 +243,39 @@ def forced_accept(cfg, weights, prompts, warmup, steps):
             "drafts": "forced to the target's own greedy continuation (every draft accepted)"}
 
 
+def fp8_draft_heads(cfg, weights, prompts, warmup, steps):
+    """The same workload with the T1 and drafter heads on the E4M3 head copy (DMTP blog
+    §6.5 drafting-side head quantisation; verification stays bf16): natural rounds, graph
+    replayed, timed like the headline."""
+    import torch
+    from mtp_block_draft_gb300 import DmtpRound
+    c8 = cfg.replace(draft_head_fp8=True)
+    R = warmup + steps
+    g = DmtpRound(c8, weights, prompts, max(len(p) for p in prompts) + 8 * R + 64)
+    for _ in range(warmup):
+        g.round()
+    _, _, h0 = g.read_state()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(g.stream)
+    for _ in range(steps):
+        g.round()
+    e1.record(g.stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    _, _, h1 = g.read_state()
+    prof = g.profile_round()
+    g.close()
+    dh = (h1 - h0).astype(np.int64)
+    mean_len = float(np.sum((np.arange(8) + 1) * dh)) / max(1, int(dh.sum()))
+    rps = steps / (ms / 1e3)
+    return {"rounds_per_s": rps, "ms_per_step": ms / steps, "mean_accept_len": mean_len,
+            "tokens_per_s": len(prompts) * rps * mean_len, "steps": steps, "warmup": warmup,
+            "lm_head_ms_per_round": prof["lm_head"]["ms"],
+            "note": "T1 and drafter heads read an E4M3 copy of the vocabulary matrix "
+                    "(per-row power-of-two scales); the verify head stays bf16"}
+
+
 def run_reference(args, cfg):
     import torch
     from synth import make_prompts, make_weights
@@ -254,7 +288,8 @@ def run_reference(args, cfg):
     from oracle import OracleModel
     b = int(np.argmin([len(p) for p in prompts]))
     om = OracleModel(cfg, {k: v.cpu() for k, v in weights.items()},
-                     temperature=cfg.temperature, sample_seed=cfg.sample_seed)
+                     temperature=cfg.temperature, sample_seed=cfg.sample_seed,
+                     draft_head_fp8=cfg.draft_head_fp8)
     del weights
     st = om.prefill(prompts[b], b=b)
     for _ in range(args.warmup):
@@ -291,6 +326,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--forced-steps", type=int, default=16,
                     help="timed rounds of the forced-accept run (0: skip)")
+    ap.add_argument("--fp8-steps", type=int, default=100,
+                    help="timed rounds of the run with E4M3 draft heads (0: skip)")
     ap.add_argument("--temperature", type=float, default=0.0,
                     help="0: greedy verification (the workloads' setting); > 0: target-only "
                          "sampled verification at this temperature")
@@ -442,6 +479,8 @@ def main():
     del g
     if args.forced_steps > 0 and world == 1:
         line["forced_accept"] = forced_accept(cfg, weights, prompts, 4, args.forced_steps)
+    if args.fp8_steps > 0 and world == 1 and cfg.dtype == "bf16" and cfg.d_model % 128 == 0:
+        line["fp8_draft_heads"] = fp8_draft_heads(cfg, weights, prompts, 16, args.fp8_steps)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_sample(cfg, weights, prompts, args.cpu_rounds)
     if rank == 0:

@@ -69,7 +69,14 @@ extern "C" {
  * of the Philox4x32-10 block (Salmon et al., SC 2011) of counter (v / 4, p, b, 0) and key
  * (low, high 32 bits of sample_seed). The noise depends on the position only, so the
  * committed stream equals plain one-token sampled decoding with the same noise. A (the
- * prefill's first token) and the drafts T1..T7 stay argmax picks. */
+ * prefill's first token) and the drafts T1..T7 stay argmax picks.
+ * draft_head_fp8 (bf16 models only): the heads that only draft (T1 and the drafter's
+ * T2..T7; DMTP §6.5 drafting-side head quantisation) read an E4M3 copy of the head, made
+ * in the workspace by dmtp_init: per row a power-of-two scale s = 2^e, e the smallest
+ * integer with max|row| <= 448 s, and q = round-to-nearest-even(row / s); each head input
+ * row (the normalised hidden) is quantised the same way, and the draft logits are
+ * s_x s_v (q_x . q_v). The verify head stays bf16, so the committed tokens do not
+ * change; only the drafts (and so the acceptance) can. */
 typedef struct {
   int vocab, d_model, n_layers, n_heads, n_kv_heads, head_dim, ffn;
   int gdn_heads, gdn_dk, gdn_dv;
@@ -83,6 +90,7 @@ typedef struct {
   int dtype;
   float temperature;
   uint64_t sample_seed;
+  int draft_head_fp8;
 } dmtp_config;
 
 /* One decoder layer, row-major [out, in] device matrices of the config's dtype.

@@ -40,7 +40,7 @@ class dmtp_config(C.Structure):
                 ("tap_layers", C.c_int * DMTP_MAX_TAPS), ("mask_id", C.c_int),
                 ("rms_eps", C.c_float), ("rope_theta", C.c_float), ("max_ctx", C.c_int),
                 ("max_batch", C.c_int), ("dtype", C.c_int), ("temperature", C.c_float),
-                ("sample_seed", C.c_uint64)]
+                ("sample_seed", C.c_uint64), ("draft_head_fp8", C.c_int)]
 
 
 _LAYER_FIELDS = ("attn_norm", "wqkv", "wo", "gdn_wqkv", "gdn_wa", "gdn_wb", "gdn_wo",
@@ -144,6 +144,7 @@ def make_config(cfg, max_ctx: int, max_batch: int | None = None) -> dmtp_config:
     c.dtype = 0 if cfg.dtype == "fp32" else 1
     c.temperature = cfg.temperature
     c.sample_seed = cfg.sample_seed
+    c.draft_head_fp8 = 1 if cfg.draft_head_fp8 else 0
     return c
 
 

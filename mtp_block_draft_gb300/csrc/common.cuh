@@ -9,6 +9,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -90,6 +91,35 @@ __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
+}
+
+// Maximum over a block of up to 1024 threads; `red` is >= 32 floats of shared memory.
+__device__ __forceinline__ float block_max(float v, float* red) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  v = warp_max(v);
+  __syncthreads();
+  if (lane == 0) red[wid] = v;
+  __syncthreads();
+  float t = (lane < nw) ? red[lane] : -INFINITY;
+  return warp_max(t);
+}
+
+// E4M3 rows (draft-head quantisation): a row with largest magnitude amax gets the scale
+// 2^e, e the smallest integer with amax <= 448 * 2^e (0 for an all-zero row), and its
+// values are stored as round-to-nearest-even E4M3 of value * 2^-e (exact scaling).
+__device__ __forceinline__ int e4m3_scale_exp(float amax) {
+  if (!(amax > 0.f)) return 0;
+  int e;
+  frexpf(amax * (1.f / 448.f), &e);  // a guess within one step; made exact below
+  while (amax > ldexpf(448.f, e)) ++e;
+  while (amax <= ldexpf(448.f, e - 1)) --e;
+  return e;
+}
+// Four values (already scaled into [-448, 448]) as four E4M3 bytes, x at the lowest address.
+__device__ __forceinline__ uint32_t e4m3x4(float4 v) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(v.x, v.y), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(v.z, v.w), __NV_SATFINITE, __NV_E4M3);
+  return lo | (hi << 16);
 }
 
 // Sum over a block of up to 1024 threads; `red` is >= 32 floats of shared memory.

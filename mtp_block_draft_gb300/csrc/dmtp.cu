@@ -3,8 +3,8 @@
 // Owns no device memory: every buffer is carved out of the caller's workspace.
 // dmtp_init lays out the workspace, builds the tcgen05 GEMM plans (TMA tensor maps)
 // and runs the prefill; dmtp_round enqueues steps a1-a6 and, when no debug output is
-// requested, replays them as one captured CUDA graph (DMTP blog §6.4: prepare data on
-// the device, update fixed buffers, replay the graph). All per-sequence metadata
+// requested, replays them as one captured CUDA graph (DMTP blog §6.4: the round's inputs are
+// staged on the device into buffers whose addresses never change, then the graph runs). All per-sequence metadata
 // (positions, accepted lengths, snapshot slots) stays on the device; the host never
 // reads a length during normal rounds.
 #include <stdio.h>
@@ -90,6 +90,12 @@ struct dmtp_ctx {
   float* h_mtp;
   void* t1in;
   void* dn;
+  // E4M3 draft heads: the head copy and scales, the T1 and drafter head inputs
+  void* h8;
+  float* h8s;
+  void *t1q, *dnq;
+  float *t1qs, *dnqs;
+  bool fp8;
   float* hlast;
   int* prompts;
   int* plen;
@@ -103,6 +109,7 @@ struct dmtp_ctx {
   LayerPlans mtp;
   Gemm dkv[DMTP_MAX_DRAFT_LAYERS];
   Gemm fuse, head_t1, head_d, head_v, dfc, mproj;
+  Gemm head_a;  // A after the prompt: the target's own (bf16) head on the T1 input rows
 
   cudaGraphExec_t graph;         // the round
   cudaGraphExec_t graph_forced;  // the round with drafts read from `forced`
@@ -145,7 +152,9 @@ int derive(dmtp_ctx* c, const dmtp_config* cfg, int B) {
       f.ffn < 1 || f.max_ctx < 16 || B < 1 || B > f.max_batch || B * 8 > 256 ||
       (f.dtype != 0 && f.dtype != 1) || f.mask_id < 0 || f.mask_id >= f.vocab ||
       f.draft_window < 0 || !(f.temperature == 0.f || (f.temperature >= 1e-4f &&
-                                                        f.temperature <= 3.0e38f)))
+                                                        f.temperature <= 3.0e38f)) ||
+      (f.draft_head_fp8 != 0 && f.draft_head_fp8 != 1) ||
+      (f.draft_head_fp8 && (f.dtype != 1 || f.d_model % 128)))
     return DMTP_EINVAL;
   const int grp = f.n_heads / f.n_kv_heads;
   const int QN = 8 * grp;
@@ -156,6 +165,7 @@ int derive(dmtp_ctx* c, const dmtp_config* cfg, int B) {
   c->B = B;
   c->M = 8 * B;
   c->dt = f.dtype;
+  c->fp8 = f.draft_head_fp8 != 0;
   c->d = f.d_model;
   c->V = f.vocab;
   c->F = f.ffn;
@@ -265,6 +275,15 @@ size_t layout(dmtp_ctx* c, char* base) {
   c->h_mtp = b.take<float>(B * d * 4);
   c->t1in = b.take<char>(r1 * d * es);
   c->dn = b.take<char>(r6 * d * es);
+  if (c->fp8) {
+    const size_t vpad = ((size_t)c->V + 255) / 256 * 256;  // scales read tile-wide
+    c->h8 = b.take<char>((size_t)c->V * d);
+    c->h8s = b.take<float>(vpad * 4);
+    c->t1q = b.take<char>((size_t)B * d);
+    c->t1qs = b.take<float>((size_t)B * 4);
+    c->dnq = b.take<char>((size_t)6 * B * d);
+    c->dnqs = b.take<float>((size_t)6 * B * 4);
+  }
   c->hlast = b.take<float>(B * d * 4);
   c->forced = b.take<int>(B * 7 * 4);
   RoundState& s = c->rs;
@@ -396,7 +415,8 @@ SampleArgs verify_sampling(const dmtp_ctx* c) {
 // smp: the verify head's sampled picks (nullptr: argmax picks)
 void gemm_argmax(dmtp_ctx* c, const Gemm& g, unsigned long long* keys, float* logits,
                  const SampleArgs* smp = nullptr) {
-  const double bytes = ((double)g.N * g.K + (double)g.M * g.K) * esz(c) + 8.0 * g.M;
+  const double ew = (c->dt == 1 && g.hp.fp8) ? 1.0 : esz(c);  // bytes per operand element
+  const double bytes = ((double)g.N * g.K + (double)g.M * g.K) * ew + 8.0 * g.M;
   launch(c, P_HEAD, bytes, 2.0 * g.M * g.N * g.K, [&] {
     if (c->dt == 1)
       op_head_tc(g.hp, keys, logits, c->V, smp, c->err, c->st);
@@ -602,7 +622,10 @@ void enqueue_round(dmtp_ctx* c, const Dbg& dbg, const int* forced) {
   const int B = c->B;
   launch(c, P_OTHER, 0, 0, [&] { op_round_begin(s, c->st); });
   // a1: T1 from the cached MTP hidden
-  norm(c, c->h_mtp, c->w.mtp_final_norm, c->t1in, nullptr, nullptr, B, RowMap(), false);
+  if (c->fp8)
+    launch(c, P_OTHER, 0, 0, [&] { op_rmsnorm_e4m3(c->h_mtp, c->d, c->w.mtp_final_norm, c->t1q, c->d, c->t1qs, B, c->d, c->cfg.rms_eps, RowMap(), c->st); });
+  else
+    norm(c, c->h_mtp, c->w.mtp_final_norm, c->t1in, nullptr, nullptr, B, RowMap(), false);
   gemm_argmax(c, c->head_t1, s.keys, dbg.t1);
   launch(c, P_OTHER, 0, 0, [&] { op_keys_to_ids(s.keys, B, 1, s.drafts, 7, 0, forced, 7, 0, c->st); });
   // a2: Delta = W [RMS_e(E(T1)); RMS_m(h_MTP)]; slots [E(A), E(T1)+Delta, E(MASK) x 6]
@@ -628,7 +651,10 @@ void enqueue_round(dmtp_ctx* c, const Dbg& dbg, const int* forced) {
   m6.out_group = 6;
   m6.in_group = 8;
   m6.in_offset = 2;
-  norm(c, c->x, c->w.dft_final_norm, c->dn, nullptr, nullptr, 6 * B, m6, false);
+  if (c->fp8)
+    launch(c, P_OTHER, 0, 0, [&] { op_rmsnorm_e4m3(c->x, c->d, c->w.dft_final_norm, c->dnq, c->d, c->dnqs, 6 * B, c->d, c->cfg.rms_eps, m6, c->st); });
+  else
+    norm(c, c->x, c->w.dft_final_norm, c->dn, nullptr, nullptr, 6 * B, m6, false);
   gemm_argmax(c, c->head_d, s.keys + B, dbg.dl);
   launch(c, P_OTHER, 0, 0, [&] { op_keys_to_ids(s.keys + B, B, 6, s.drafts, 7, 1, forced, 7, 1, c->st); });
   // a4: target verify of [A, T1..T7]
@@ -676,10 +702,10 @@ int check_err(dmtp_ctx* c) {
 namespace {
 struct TuneKey {
   int dev, N, K, M;
-  bool split, argmax, swiglu, sample;
+  bool split, argmax, swiglu, sample, fp8;
   bool operator==(const TuneKey& o) const {
     return dev == o.dev && N == o.N && K == o.K && M == o.M && split == o.split &&
-           argmax == o.argmax && swiglu == o.swiglu && sample == o.sample;
+           argmax == o.argmax && swiglu == o.swiglu && sample == o.sample && fp8 == o.fp8;
   }
 };
 struct TuneChoice {
@@ -755,7 +781,8 @@ int autotune(dmtp_ctx* c, const void* flush, size_t flush_bytes) {
     all.push_back(&c->dkv[j]);
   }
   collect(c->mtp, all);
-  for (Gemm* g : {&c->fuse, &c->head_t1, &c->head_d, &c->head_v, &c->dfc, &c->mproj})
+  for (Gemm* g : {&c->fuse, &c->head_t1, &c->head_d, &c->head_v, &c->head_a, &c->dfc,
+                  &c->mproj})
     all.push_back(g);
   const size_t scratch = (size_t)c->M * 2 * c->F;  // floats of the gate/up accumulator
   cudaEvent_t e0, e1;
@@ -775,13 +802,19 @@ int autotune(dmtp_ctx* c, const void* flush, size_t flush_bytes) {
     // the verify head under sampled verification runs the sampling epilogue
     const bool sample = g == &c->head_v && c->cfg.temperature > 0.f;
     const SampleArgs smp = sample ? verify_sampling(c) : SampleArgs{};
-    const TuneKey key{dev, g->N, g->K, g->M, g->split, g->argmax, g->swiglu, sample};
+    const bool fp8 = g->argmax && g->hp.fp8;
+    const TuneKey key{dev, g->N, g->K, g->M, g->split, g->argmax, g->swiglu, sample, fp8};
     const TuneChoice* hit = nullptr;
     for (auto& e : g_tune)
       if (e.first == key) hit = &e.second;
+    // a head plan with another tile and warp count, same operands
+    auto replan = [&](HeadPlan* p, int nv, int ew) {
+      return fp8 ? head_plan_e4m3(p, g->W, g->hp.wscale, g->N, g->K, g->X, g->hp.xscale, g->M,
+                                  c->nsm, nv, ew)
+                 : head_plan(p, g->W, g->N, g->K, g->X, g->M, c->nsm, nv, ew);
+    };
     if (hit && g->argmax) {
-      if (head_plan(&g->hp, g->W, g->N, g->K, g->X, g->M, c->nsm, hit->nv, hit->ew))
-        rc = DMTP_EINVAL;
+      if (replan(&g->hp, hit->nv, hit->ew)) rc = DMTP_EINVAL;
       continue;
     }
     if (hit) {
@@ -817,7 +850,7 @@ int autotune(dmtp_ctx* c, const void* flush, size_t flush_bytes) {
       for (int nv = 128; nv <= 256; nv *= 2)
         for (int ew = 4; ew <= 8; ew *= 2) {
           HeadPlan p;
-          if (head_plan(&p, g->W, g->N, g->K, g->X, g->M, c->nsm, nv, ew)) continue;
+          if (replan(&p, nv, ew)) continue;
           const float t = time_head(c, p, sample ? &smp : nullptr, flush, flush_bytes, e0, e1);
           if (t < best_t) {
             best_t = t;
@@ -827,9 +860,9 @@ int autotune(dmtp_ctx* c, const void* flush, size_t flush_bytes) {
       g->hp = best_p;
       g_tune.push_back({key, TuneChoice{0, 0, 0, best_p.NV, best_p.ew}});
       if (verbose)
-        fprintf(stderr, "dmtp: head V=%d K=%d M=%d%s: %d vocabulary rows per tile, %d epilogue "
-                "warps, %.1f us\n", g->N, g->K, g->M, sample ? " sampled" : "", best_p.NV,
-                best_p.ew, best_t * 1e3f);
+        fprintf(stderr, "dmtp: head V=%d K=%d M=%d%s%s: %d vocabulary rows per tile, %d "
+                "epilogue warps, %.1f us\n", g->N, g->K, g->M, sample ? " sampled" : "",
+                fp8 ? " e4m3" : "", best_p.NV, best_p.ew, best_t * 1e3f);
       continue;
     }
     TuneChoice best{g->tc.wide, g->tc.msplit, g->tc.splits, 0, 0};
@@ -944,8 +977,25 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
   }
   pr |= plan_layer(c, c->mtp, w->mtp, 0, M);
   pr |= plan(c, c->fuse, w->fuse_w, c->d, 2 * c->d, c->zf, B, false);
-  pr |= plan(c, c->head_t1, w->head, c->V, c->d, c->t1in, B, true, false);
-  pr |= plan(c, c->head_d, w->head, c->V, c->d, c->dn, 6 * B, true, false);
+  if (c->fp8) {  // draft heads on the E4M3 head copy (DMTP §6.5)
+    c->head_t1.argmax = c->head_d.argmax = true;
+    c->head_t1.W = c->head_d.W = c->h8;
+    c->head_t1.N = c->head_d.N = c->V;
+    c->head_t1.K = c->head_d.K = c->d;
+    c->head_t1.X = c->t1q;
+    c->head_t1.M = B;
+    c->head_d.X = c->dnq;
+    c->head_d.M = 6 * B;
+    c->head_t1.split = c->head_d.split = false;
+    pr |= head_plan_e4m3(&c->head_t1.hp, c->h8, c->h8s, c->V, c->d, c->t1q, c->t1qs, B,
+                         c->nsm, 256, 8) ? DMTP_EINVAL : 0;
+    pr |= head_plan_e4m3(&c->head_d.hp, c->h8, c->h8s, c->V, c->d, c->dnq, c->dnqs, 6 * B,
+                         c->nsm, 256, 8) ? DMTP_EINVAL : 0;
+  } else {
+    pr |= plan(c, c->head_t1, w->head, c->V, c->d, c->t1in, B, true, false);
+    pr |= plan(c, c->head_d, w->head, c->V, c->d, c->dn, 6 * B, true, false);
+  }
+  pr |= plan(c, c->head_a, w->head, c->V, c->d, c->t1in, B, true, false);
   pr |= plan(c, c->head_v, w->head, c->V, c->d, c->hTn, M, true, false);
   pr |= plan(c, c->dfc, w->dft_fc, c->d, c->ntap * c->d, c->taps, M, false);
   pr |= plan(c, c->mproj, w->mtp_proj, c->d, 2 * c->d, c->z, M, false);
@@ -987,6 +1037,7 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
   RoundState& s = c->rs;
   // padding rows of the GEMM operands are read (and ignored): start from zeros
   zero(c, workspace, need);
+  if (c->fp8) op_quant_rows_e4m3(w->head, c->V, c->d, c->h8, c->h8s, st);
   {
     const int r = autotune(c, workspace, std::min(need, (size_t)256 << 20));
     if (r) {
@@ -1035,7 +1086,7 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
   // A = the target's greedy token after the prompt; MTP consumes (h^T_{P-1}, A) at P
   op_cast_rows(c->dt, c->hlast, c->d, c->t1in, c->d, 0, B, c->d, RowMap(), st);
   zero(c, s.keys, (size_t)B * 8);
-  gemm_argmax(c, c->head_t1, s.keys, nullptr);
+  gemm_argmax(c, c->head_a, s.keys, nullptr);
   op_keys_to_ids(s.keys, B, 1, s.A, 1, 0, nullptr, 0, 0, st);
   op_prefill_final(s, c->plen, c->hlast, c->hT32, c->d, st);
   mtp_advance(c);

@@ -134,6 +134,98 @@ void op_rmsnorm(int dt, const float* x, int ldx, const void* g, void* y, int ldy
 }
 
 // ---------------------------------------------------------------------------------
+// E4M3 rows: draft-head quantisation (common.cuh). The head copy once at init, and each
+// head input row RMSNorm(x[map(r)]) * g straight from its fp32 values.
+// ---------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_quant_rows_e4m3(const bf16* __restrict__ W, int d,
+                                                         uint8_t* __restrict__ q,
+                                                         float* __restrict__ qs) {
+  __shared__ float red[32];
+  const long r = blockIdx.x;
+  const bf16* w = W + r * d;
+  float amax = 0.f;
+  for (int i = threadIdx.x * 4; i < d; i += 1024) {
+    const float4 v = load4(w + i);
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  }
+  amax = block_max(amax, red);
+  const int e = e4m3_scale_exp(amax);
+  for (int i = threadIdx.x * 4; i < d; i += 1024) {
+    const float4 v = load4(w + i);
+    const float4 t = make_float4(ldexpf(v.x, -e), ldexpf(v.y, -e), ldexpf(v.z, -e), ldexpf(v.w, -e));
+    *reinterpret_cast<uint32_t*>(q + r * d + i) = e4m3x4(t);
+  }
+  if (threadIdx.x == 0) qs[r] = ldexpf(1.f, e);
+}
+
+void op_quant_rows_e4m3(const void* W, int rows, int d, void* q, float* qs, cudaStream_t st) {
+  if (rows > 0) k_quant_rows_e4m3<<<rows, 256, 0, st>>>((const bf16*)W, d, (uint8_t*)q, qs);
+}
+
+template <int NV>
+__global__ void __launch_bounds__(128) k_rmsnorm_e4m3(const float* __restrict__ x, int ldx,
+                                                      const bf16* __restrict__ g,
+                                                      uint8_t* __restrict__ q, int ldq,
+                                                      float* __restrict__ qs, int d, float eps,
+                                                      RowMap map) {
+  __shared__ float red[32];
+  const int r = blockIdx.x, d4 = d >> 2;
+  const float* xr = x + (long)map_row(r, map) * ldx;
+  float4 v[NV];
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int i = threadIdx.x + k * 128;
+    v[k] = i < d4 ? load4(xr + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+  }
+  ss = block_sum(ss, red);
+  const float inv = rsqrtf(ss / (float)d + eps);
+  float amax = 0.f;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int i = threadIdx.x + k * 128;
+    if (i < d4) {
+      const float4 gg = load4(g + 4 * i);
+      v[k] = make_float4(v[k].x * inv * gg.x, v[k].y * inv * gg.y, v[k].z * inv * gg.z,
+                         v[k].w * inv * gg.w);
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[k].x), fabsf(v[k].y)),
+                               fmaxf(fabsf(v[k].z), fabsf(v[k].w))));
+    }
+  }
+  amax = block_max(amax, red);
+  const int e = e4m3_scale_exp(amax);
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int i = threadIdx.x + k * 128;
+    if (i < d4) {
+      const float4 t = make_float4(ldexpf(v[k].x, -e), ldexpf(v[k].y, -e), ldexpf(v[k].z, -e),
+                                   ldexpf(v[k].w, -e));
+      *reinterpret_cast<uint32_t*>(q + (long)r * ldq + 4 * i) = e4m3x4(t);
+    }
+  }
+  if (threadIdx.x == 0) qs[r] = ldexpf(1.f, e);
+}
+
+void op_rmsnorm_e4m3(const float* x, int ldx, const void* g, void* q, int ldq, float* qs,
+                     int rows, int d, float eps, RowMap map, cudaStream_t st) {
+  if (rows <= 0) return;
+  const int nv = (d / 4 + 127) / 128;
+#define DMTP_RMS_Q(NV_)                                                                      \
+  k_rmsnorm_e4m3<NV_><<<rows, 128, 0, st>>>(x, ldx, (const bf16*)g, (uint8_t*)q, ldq, qs, d, \
+                                            eps, map)
+  if (nv <= 1)
+    DMTP_RMS_Q(1);
+  else if (nv <= 2)
+    DMTP_RMS_Q(2);
+  else if (nv <= 4)
+    DMTP_RMS_Q(4);
+  else
+    DMTP_RMS_Q(8);
+#undef DMTP_RMS_Q
+}
+
+// ---------------------------------------------------------------------------------
 // Embedding gather: x[m] = E[tok[m]]
 // ---------------------------------------------------------------------------------
 __device__ __forceinline__ int checked_tok(int t, int vocab, unsigned* err) {

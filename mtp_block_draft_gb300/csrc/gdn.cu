@@ -4,9 +4,10 @@
 //   S <- alpha * S (I - beta k k^T) + beta v k^T  =  alpha * S + u k^T,
 //   u = beta * v - alpha * beta * (S k);   o = S q.
 // Snapshots and the pointer swap follow the colibri speculative-decoding page,
-// "Undoing rows on a model with recurrent state": a verify copies the state after each
-// of its rows but the last, one slot per row; a rejection after row r swaps slot r in
-// by pointer, nothing is recomputed.
+// "Undoing rows on a model with recurrent state": the verify keeps a copy of the state
+// as it stands after every row except the final one (slot r holds the state after row
+// r), and when row r is the last accepted, slot r becomes the live state by an index
+// swap, with no recomputation.
 //
 // One CTA per (sequence, head) keeps the fp32 state [dv][dk] in registers (256 / dv
 // threads per state row), reads it once, writes the snapshots after rows 0..6 into the slot

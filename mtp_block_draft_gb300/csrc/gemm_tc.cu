@@ -292,6 +292,23 @@ int tc_make_tmap(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols
   return r == CUDA_SUCCESS ? 0 : -3;
 }
 
+// [rows, cols] row-major bytes (E4M3), box {128, box_rows}, 128-byte swizzle: the same
+// shared-memory layout as a bf16 box of 64 columns.
+int tc_make_tmap_u8(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows) {
+  PFN_encodeTiled_t enc = get_encode();
+  if (!enc) return -1;
+  if (((uintptr_t)base & 15) || cols % 16) return -2;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -3;
+}
+
 int tc_make_tmap3(CUtensorMap* tm, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                   uint32_t b1, uint32_t b2) {
   PFN_encodeTiled_t enc = get_encode();

@@ -24,7 +24,7 @@ namespace dmtp {
 
 namespace {
 
-constexpr int kBK = 64;                       // k elements per stage (128 B of bf16)
+constexpr int kRowB = 128;  // bytes of one operand row per stage: 64 bf16 or 128 E4M3 k
 constexpr size_t kHeadSmemBudget = 200 * 1024;
 
 __device__ __forceinline__ void arrive(uint32_t bar) {
@@ -38,15 +38,45 @@ struct HeadArgs {
   long ldl;
   SampleArgs smp;
   unsigned* err;
+  const float* wscale;  // E4M3 operands: per vocabulary row scale (padded past V)
+  const float* xscale;  // E4M3 operands: per token row scale
 };
 
+// D[tmem] (+)= A[smem] * B[smem]^T, E4M3 inputs, fp32 accumulate (kind::f8f6f4).
+__device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Instruction descriptor: D fp32, A and B E4M3 (format code 0), both K-major, M x N.
+constexpr uint32_t umma_idesc_e4m3(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 // Running (best value, first index) of one token row over 16 columns n0 + j; FULL: all
-// 16 columns are inside the vocabulary (else only j < lim).
-template <bool SAMPLE, bool FULL>
+// 16 columns are inside the vocabulary (else only j < lim). FP8: the accumulators are
+// scaled by the columns' power-of-two scales (exact; the row's own scale is common to
+// the row and left out of the comparison).
+template <bool SAMPLE, bool FULL, bool FP8>
 __device__ __forceinline__ void scan16(const uint32_t (&r)[16], int n0, int lim, float& best,
-                                       int& bidx, const SampleArgs& s, int pos, int seq) {
+                                       int& bidx, const SampleArgs& s, int pos, int seq,
+                                       const float* wscale) {
   float sc[16];
-  if (SAMPLE) {
+  if (FP8) {
+    const float4* ws = reinterpret_cast<const float4*>(wscale + n0);
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const float4 w4 = __ldg(ws + g);
+      sc[4 * g + 0] = __uint_as_float(r[4 * g + 0]) * w4.x;
+      sc[4 * g + 1] = __uint_as_float(r[4 * g + 1]) * w4.y;
+      sc[4 * g + 2] = __uint_as_float(r[4 * g + 2]) * w4.z;
+      sc[4 * g + 3] = __uint_as_float(r[4 * g + 3]) * w4.w;
+    }
+  } else if (SAMPLE) {
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       const uint4 blk = philox4x32_10(
@@ -71,16 +101,17 @@ __device__ __forceinline__ void scan16(const uint32_t (&r)[16], int n0, int lim,
 }
 
 // EW epilogue warps (4 or 8): with 8, two warps share each TMEM lane quarter and take
-// alternate 32-column chunks of every accumulator.
-template <int NV, int TH, bool SAMPLE, int EW>
+// alternate 32-column chunks of every accumulator. FP8: E4M3 operands (draft heads).
+template <int NV, int TH, bool SAMPLE, int EW, bool FP8>
 __global__ void __launch_bounds__(64 + 32 * EW, 1)
     k_head_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
               HeadArgs a) {
   constexpr int NB = (2 * TH * NV <= 512) ? 2 : 1;  // accumulator buffers
   constexpr int ACC = TH * NV;                       // TMEM columns per buffer
   constexpr uint32_t kCols = NB * ACC;               // 256 or 512
-  constexpr uint32_t kWBytes = NV * kBK * 2;
-  constexpr uint32_t kXSlot = TH * 128 * kBK * 2;    // smem per stage for token rows
+  constexpr int kBK = FP8 ? 128 : 64;               // k elements per stage
+  constexpr uint32_t kWBytes = NV * kRowB;
+  constexpr uint32_t kXSlot = TH * 128 * kRowB;      // smem per stage for token rows
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   const int S = a.stages;
@@ -95,7 +126,7 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = a.K / kBK;
-  const uint32_t xbytes = (uint32_t)a.MT * kBK * 2;
+  const uint32_t xbytes = (uint32_t)a.MT * kRowB;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
@@ -144,7 +175,7 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
-      const uint32_t idesc = umma_idesc_bf16(128, NV);
+      const uint32_t idesc = FP8 ? umma_idesc_e4m3(128, NV) : umma_idesc_bf16(128, NV);
       int it = 0, tl = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < a.tiles && ok; t += gridDim.x, ++tl) {
@@ -164,13 +195,18 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
           uint64_t dx[TH];
 #pragma unroll
           for (int h = 0; h < TH; ++h)
-            dx[h] = umma_desc_sw128(smem_u32(sX + (size_t)s * kXSlot + h * 128 * kBK * 2));
+            dx[h] = umma_desc_sw128(smem_u32(sX + (size_t)s * kXSlot + h * 128 * kRowB));
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)  // +32 B per K=16 step inside the swizzle atom
+          for (int k = 0; k < 4; ++k)  // +32 B per MMA step (16 bf16 or 32 E4M3 k)
 #pragma unroll
-            for (int h = 0; h < TH; ++h)
-              umma_bf16(dacc + h * NV, dx[h] + 2 * k, dw + 2 * k, idesc,
-                        (kb > 0 || k > 0) ? 1u : 0u);
+            for (int h = 0; h < TH; ++h) {
+              if (FP8)
+                umma_e4m3(dacc + h * NV, dx[h] + 2 * k, dw + 2 * k, idesc,
+                          (kb > 0 || k > 0) ? 1u : 0u);
+              else
+                umma_bf16(dacc + h * NV, dx[h] + 2 * k, dw + 2 * k, idesc,
+                          (kb > 0 || k > 0) ? 1u : 0u);
+            }
           umma_commit(smem_u32(&empty[s]));
         }
         if (ok) umma_commit(smem_u32(&acc_full[buf]));
@@ -216,19 +252,25 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
           reg_fence16(r1);
           if (a.logits && m[h] < a.M) {  // debug copy of the logits
             float* lp = a.logits + (long)m[h] * a.ldl + n0 + c;
+            const float xs = FP8 ? a.xscale[m[h]] : 1.f;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              if (c + j < lim) lp[j] = __uint_as_float(r0[j]);
-              if (c + 16 + j < lim) lp[16 + j] = __uint_as_float(r1[j]);
+              const float w0 = FP8 ? a.wscale[n0 + c + j] * xs : 1.f;
+              const float w1 = FP8 ? a.wscale[n0 + c + 16 + j] * xs : 1.f;
+              if (c + j < lim) lp[j] = __uint_as_float(r0[j]) * w0;
+              if (c + 16 + j < lim) lp[16 + j] = __uint_as_float(r1[j]) * w1;
             }
           }
           if (c + 32 <= lim) {
-            scan16<SAMPLE, true>(r0, n0 + c, 0, best[h], bidx[h], a.smp, pos[h], seq[h]);
-            scan16<SAMPLE, true>(r1, n0 + c + 16, 0, best[h], bidx[h], a.smp, pos[h], seq[h]);
+            scan16<SAMPLE, true, FP8>(r0, n0 + c, 0, best[h], bidx[h], a.smp, pos[h], seq[h],
+                                      a.wscale);
+            scan16<SAMPLE, true, FP8>(r1, n0 + c + 16, 0, best[h], bidx[h], a.smp, pos[h],
+                                      seq[h], a.wscale);
           } else {  // the vocabulary's ragged end
-            scan16<SAMPLE, false>(r0, n0 + c, lim - c, best[h], bidx[h], a.smp, pos[h], seq[h]);
-            scan16<SAMPLE, false>(r1, n0 + c + 16, lim - c - 16, best[h], bidx[h], a.smp,
-                                  pos[h], seq[h]);
+            scan16<SAMPLE, false, FP8>(r0, n0 + c, lim - c, best[h], bidx[h], a.smp, pos[h],
+                                       seq[h], a.wscale);
+            scan16<SAMPLE, false, FP8>(r1, n0 + c + 16, lim - c - 16, best[h], bidx[h], a.smp,
+                                       pos[h], seq[h], a.wscale);
           }
         }
       }
@@ -249,28 +291,28 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
   }
 }
 
-template <int NV, int TH, bool SAMPLE, int EW>
+template <int NV, int TH, bool SAMPLE, int EW, bool FP8>
 int set_attr(size_t smem) {
-  return cudaFuncSetAttribute(k_head_tc<NV, TH, SAMPLE, EW>,
+  return cudaFuncSetAttribute(k_head_tc<NV, TH, SAMPLE, EW, FP8>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
          cudaSuccess;
 }
+// instances: greedy and sampled bf16 heads, greedy E4M3 draft heads
 template <int NV, int TH>
 int set_attrs(size_t smem) {
-  return set_attr<NV, TH, false, 4>(smem) | set_attr<NV, TH, true, 4>(smem) |
-         set_attr<NV, TH, false, 8>(smem) | set_attr<NV, TH, true, 8>(smem);
+  return set_attr<NV, TH, false, 4, false>(smem) | set_attr<NV, TH, true, 4, false>(smem) |
+         set_attr<NV, TH, false, 8, false>(smem) | set_attr<NV, TH, true, 8, false>(smem) |
+         set_attr<NV, TH, false, 4, true>(smem) | set_attr<NV, TH, false, 8, true>(smem);
 }
 
 size_t head_smem(int nv, int th, int stages) {
-  return 1024 + (size_t)stages * ((size_t)nv * kBK * 2 + (size_t)th * 128 * kBK * 2) +
+  return 1024 + (size_t)stages * ((size_t)nv * kRowB + (size_t)th * 128 * kRowB) +
          (size_t)(2 * stages + 5) * 8 + 16;
 }
 
-}  // namespace
-
-int head_plan(HeadPlan* p, const void* W, int V, int K, const void* X, int M, int nsm, int nv,
-              int ew) {
-  if (!W || !X || V < 1 || K < kBK || K % kBK || M < 1 || M > 256 || nsm < 1 ||
+int plan_common(HeadPlan* p, const void* W, int V, int K, const void* X, int M, int nsm, int nv,
+                int ew, int kbk) {
+  if (!W || !X || V < 1 || K < kbk || K % kbk || M < 1 || M > 256 || nsm < 1 ||
       (nv != 128 && nv != 256) || (ew != 4 && ew != 8) || ((uintptr_t)W & 15) ||
       ((uintptr_t)X & 15))
     return -10;
@@ -287,10 +329,33 @@ int head_plan(HeadPlan* p, const void* W, int V, int K, const void* X, int M, in
   while (st > 2 && head_smem(nv, p->TH, st) > kHeadSmemBudget) --st;
   p->stages = st;
   p->smem = head_smem(nv, p->TH, st);
-  if (p->smem > kHeadSmemBudget) return -10;
-  int r = tc_make_tmap(&p->tmW, W, (uint64_t)V, (uint64_t)K, (uint32_t)nv);
+  p->fp8 = 0;
+  p->wscale = p->xscale = nullptr;
+  return p->smem > kHeadSmemBudget ? -10 : 0;
+}
+
+}  // namespace
+
+int head_plan(HeadPlan* p, const void* W, int V, int K, const void* X, int M, int nsm, int nv,
+              int ew) {
+  int r = plan_common(p, W, V, K, X, M, nsm, nv, ew, 64);
+  if (r) return r;
+  r = tc_make_tmap(&p->tmW, W, (uint64_t)V, (uint64_t)K, (uint32_t)nv);
   if (r) return r;
   return tc_make_tmap(&p->tmX, X, (uint64_t)M, (uint64_t)K, (uint32_t)p->MT);
+}
+
+int head_plan_e4m3(HeadPlan* p, const void* W8, const float* wscale, int V, int K,
+                   const void* X8, const float* xscale, int M, int nsm, int nv, int ew) {
+  if (!wscale || !xscale || ((uintptr_t)wscale & 15)) return -10;
+  int r = plan_common(p, W8, V, K, X8, M, nsm, nv, ew, 128);
+  if (r) return r;
+  p->fp8 = 1;
+  p->wscale = wscale;
+  p->xscale = xscale;
+  r = tc_make_tmap_u8(&p->tmW, W8, (uint64_t)V, (uint64_t)K, (uint32_t)nv);
+  if (r) return r;
+  return tc_make_tmap_u8(&p->tmX, X8, (uint64_t)M, (uint64_t)K, (uint32_t)p->MT);
 }
 
 int head_init_attributes() {
@@ -301,10 +366,13 @@ int head_init_attributes() {
 
 template <int NV, int TH, int EW>
 void launch_ew(const HeadPlan& p, const HeadArgs& a, bool sample, cudaStream_t st) {
-  if (sample)
-    k_head_tc<NV, TH, true, EW><<<p.grid, 64 + 32 * EW, p.smem, st>>>(p.tmW, p.tmX, a);
+  const int threads = 64 + 32 * EW;
+  if (p.fp8)
+    k_head_tc<NV, TH, false, EW, true><<<p.grid, threads, p.smem, st>>>(p.tmW, p.tmX, a);
+  else if (sample)
+    k_head_tc<NV, TH, true, EW, false><<<p.grid, threads, p.smem, st>>>(p.tmW, p.tmX, a);
   else
-    k_head_tc<NV, TH, false, EW><<<p.grid, 64 + 32 * EW, p.smem, st>>>(p.tmW, p.tmX, a);
+    k_head_tc<NV, TH, false, EW, false><<<p.grid, threads, p.smem, st>>>(p.tmW, p.tmX, a);
 }
 template <int NV, int TH>
 void launch(const HeadPlan& p, const HeadArgs& a, bool sample, cudaStream_t st) {
@@ -316,9 +384,10 @@ void launch(const HeadPlan& p, const HeadArgs& a, bool sample, cudaStream_t st) 
 
 void op_head_tc(const HeadPlan& p, unsigned long long* keys, float* logits, long ldl,
                 const SampleArgs* smp, unsigned* err, cudaStream_t st) {
-  const bool sample = smp && smp->scale2 > 0.f;
+  // the E4M3 draft heads never sample (only the verify head does)
+  const bool sample = !p.fp8 && smp && smp->scale2 > 0.f;
   const HeadArgs a{p.V,  p.K,    p.M,   p.MT, p.stages, p.tiles,
-                   keys, logits, ldl,   sample ? *smp : SampleArgs{}, err};
+                   keys, logits, ldl,   sample ? *smp : SampleArgs{}, err, p.wscale, p.xscale};
   if (p.NV == 128)
     p.TH == 1 ? launch<128, 1>(p, a, sample, st) : launch<128, 2>(p, a, sample, st);
   else

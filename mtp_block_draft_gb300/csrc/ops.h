@@ -25,6 +25,12 @@ void op_rmsnorm(int dt, const float* x, int ldx, const void* g, void* y, int ldy
                 float* y32, int ld32, void* tap, int ldtap, long tap_lo, int rows, int d,
                 float eps, RowMap map, cudaStream_t st, float* zero = nullptr, int ldz = 0,
                 int nz = 0);
+// Draft-head quantisation to E4M3 rows with power-of-two scales (common.cuh):
+// q [rows][d] bytes and qs [rows] scales of the bf16 matrix W [rows][d] (d % 4 == 0) ...
+void op_quant_rows_e4m3(const void* W, int rows, int d, void* q, float* qs, cudaStream_t st);
+// ... and of RMSNorm(x[map(r)]) * g (bf16 gain; d % 4 == 0, d <= 4096), row pitch ldq.
+void op_rmsnorm_e4m3(const float* x, int ldx, const void* g, void* q, int ldq, float* qs,
+                     int rows, int d, float eps, RowMap map, cudaStream_t st);
 // x[m] = E[tok[m]] (fp32 rows)
 void op_embed(int dt, const void* E, const int* tok, int vocab, float* x, int rows, int d,
               unsigned* err, cudaStream_t st);
@@ -181,6 +187,10 @@ int tc_mt(int M);
 // Tensor map of a row-major bf16 [rows, cols] matrix, box {64, box_rows}, 128-B swizzle.
 int tc_make_tmap(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols,
                  uint32_t box_rows);
+// Tensor map of a row-major byte matrix [rows, cols] (E4M3), box {128, box_rows}, 128-B
+// swizzle.
+int tc_make_tmap_u8(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows);
 // 3-D bf16 tensor [d2][d1][d0] (d0 innermost), box {64, b1, b2}, 128-B swizzle.
 int tc_make_tmap3(CUtensorMap* tm, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                   uint32_t b1, uint32_t b2);
@@ -211,11 +221,19 @@ int tc_init_attributes();
 struct HeadPlan {
   CUtensorMap tmW, tmX;
   int V, K, M, MT, TH, NV, ew, tiles, grid, stages;
+  int fp8;                       // E4M3 operands (draft heads)
+  const float *wscale, *xscale;  // E4M3 row scales of W (padded past V) and of X
   size_t smem;
 };
 // ew: epilogue warps (4 or 8)
 int head_plan(HeadPlan* p, const void* W, int V, int K, const void* X, int M, int nsm, int nv,
               int ew);
+// Draft head on E4M3 operands (op_quant_rows_e4m3 / op_rmsnorm_e4m3): W8 [V][K] bytes with
+// scales wscale (readable up to the vocabulary rounded up to 256 rows), X8 [M][K] bytes
+// with xscale [M]; K % 128 == 0. The argmax ranks acc * wscale[v] (xscale[m] is common to
+// the row); debug logits are acc * wscale[v] * xscale[m].
+int head_plan_e4m3(HeadPlan* p, const void* W8, const float* wscale, int V, int K,
+                   const void* X8, const float* xscale, int M, int nsm, int nv, int ew);
 // logits (optional, fp32 [M][ldl]) receives the raw logits; smp: sampled picks (nullptr:
 // argmax of the logits). keys must hold zeros (or earlier keys to combine with).
 void op_head_tc(const HeadPlan& p, unsigned long long* keys, float* logits, long ldl,

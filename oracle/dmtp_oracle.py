@@ -37,6 +37,7 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
+from .fp8 import fp8_logits, quantize_rows
 from .sampling import sampled_scores
 
 F64 = np.float64
@@ -198,18 +199,23 @@ class OracleModel:
     """Target + MTP module + fusion + block drafter, float64, from synth weights."""
 
     def __init__(self, cfg, weights: dict, gate: float = 0.05, kv_store: str | None = None,
-                 temperature: float = 0.0, sample_seed: int = 0):
+                 temperature: float = 0.0, sample_seed: int = 0,
+                 draft_head_fp8: bool = False):
         """kv_store: storage type of every K/V cache ("bf16" or "fp32"); by default the
         model's storage type (cfg.dtype). Stored keys and values are rounded to it when
         written, as a bf16 KV cache holds them; every computation stays float64.
         temperature > 0: the verify picks are target samples (sampling.py) with the given
-        sampling seed; 0: argmax picks."""
+        sampling seed; 0: argmax picks. draft_head_fp8: the T1 and drafter heads score
+        with the E4M3-quantised head (fp8.py); the verify head stays exact."""
         self.cfg = cfg
         self.temperature, self.sample_seed = float(temperature), int(sample_seed)
         self.W = {k: v.detach().to("cpu").double().numpy() if hasattr(v, "detach")
                   else np.asarray(v, dtype=F64) for k, v in weights.items()}
         self.gate = gate
         self.kv_bf16 = (kv_store or cfg.dtype) == "bf16"
+        self.draft_fp8 = bool(draft_head_fp8)
+        if self.draft_fp8:
+            self.Hq, self.Hs = quantize_rows(self.W["head"])
         c = cfg
         self.eps, self.theta = c.rms_eps, c.rope_theta
         self.hq, self.hkv, self.hd = c.n_heads, c.n_kv_heads, c.head_dim
@@ -349,10 +355,17 @@ class OracleModel:
         x, st.mtp_K, st.mtp_V = self.attn_layer("mtp", x, st.mtp_K, st.mtp_V, pos0)
         return x
 
+    def draft_head(self, Y: np.ndarray) -> np.ndarray:
+        """Draft logits H Y^T of normalised rows Y: exact, or with the E4M3 head copy
+        ([DMTP] §6.5 drafting-side head quantization; fp8.py)."""
+        if self.draft_fp8:
+            return fp8_logits(Y, self.Hq, self.Hs)
+        return Y @ self.W["head"].T
+
     def t1_head(self, h_mtp: np.ndarray) -> np.ndarray:
         """Logits of the first candidate: H RMS_f(h_MTP) ([DMTP] §5 step 1, §6.5)."""
         W = self.W
-        return rms_norm(h_mtp[None], W["mtp.final_norm"], self.eps)[0] @ W["head"].T
+        return self.draft_head(rms_norm(h_mtp[None], W["mtp.final_norm"], self.eps))[0]
 
     # ---- fusion and block drafter -----------------------------------------------------
 
@@ -373,7 +386,7 @@ class OracleModel:
         """One parallel block forward over the 8 slots at positions a..a+7.
 
         Every slot attends to the context K/V at positions max(0, a - window)..a-1
-        ([DMTP] §6.2: the last 4096 positions relative to the anchor) and to all 8
+        ([DMTP] §6.2: a 4096-position window ending just before the anchor) and to all 8
         block slots with no mask inside the block ([DFvsMTP], block-diagonal mask).
         Returns drafter logits [6, V] for slots 2..7 (each predicts the token at its
         own position).
@@ -390,7 +403,7 @@ class OracleModel:
             X = X + o.reshape(8, -1) @ W[f"{pfx}.wo"].T
             X = X + self._mlp(pfx, X)
         hn = rms_norm(X[2:8], W["dft.final_norm"], self.eps)
-        return hn @ W["head"].T
+        return self.draft_head(hn)
 
     # ---- prefill ----------------------------------------------------------------------
 

@@ -1,12 +1,12 @@
 """Target-only sampled verification: random numbers and the sampled pick (TEST
 INFRASTRUCTURE ONLY).
 
-[DMTP] "DMTP: A Better First Token for Block Drafting via MTP", §5 ("We use target-only
-verification throughout these experiments. We check candidates token by token against
-Target samples and accept the consecutive matching prefix") and §7 (all methods at
-temperature 1); [colibri] verify contract ("The picks come from the exact logits,
-greedy or sampled. A draft never reaches the sampler: a sampled token that happens to
-equal a draft is an accepted draft").
+[DMTP] "DMTP: A Better First Token for Block Drafting via MTP", §5: the experiments
+verify against the target alone, comparing each candidate in turn with the token the
+target samples there and keeping the matched prefix; §7 runs every method at temperature
+1. [colibri] verify contract: the picks are made from the exact logits, greedy or
+sampled, and drafts never feed the sampler, so a sample equal to a draft is an accepted
+draft.
 
 Reading (the pages name no sampler or generator): the target's token at position p of
 sequence b is the Gumbel-max sample argmax_v (l_v / temperature + G_v) of its logits

@@ -66,6 +66,8 @@ class DmtpConfig:
     # drawn with the given sampling seed
     temperature: float = 0.0
     sample_seed: int = 0
+    # the T1 and drafter heads read an E4M3 copy of the head (bf16 models only)
+    draft_head_fp8: bool = False
 
     def __post_init__(self):
         if not self.layer_kinds:
@@ -110,7 +112,7 @@ class DmtpConfig:
 
 
 def _hybrid_kinds(n_layers: int) -> tuple[int, ...]:
-    # three of every four layers are Gated DeltaNet; every fourth is attention
+    # layer l is attention when l % 4 == 3, Gated DeltaNet otherwise
     return tuple(0 if (l % 4 == 3) else 1 for l in range(n_layers))
 
 

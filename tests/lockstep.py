@@ -30,7 +30,8 @@ class Lockstep:
         self.gpu = DmtpRound(cfg, weights_gpu, prompts,
                              max_ctx or default_max_ctx(prompts, rounds))
         self.oracle = OracleModel(cfg, {k: v.cpu() for k, v in weights_gpu.items()}, gate=GATE,
-                                  temperature=cfg.temperature, sample_seed=cfg.sample_seed)
+                                  temperature=cfg.temperature, sample_seed=cfg.sample_seed,
+                                  draft_head_fp8=cfg.draft_head_fp8)
         kv, A, _ = self.gpu.read_state()
         self.states = {}
         self.adopted = []

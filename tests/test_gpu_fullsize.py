@@ -59,6 +59,19 @@ def test_b32_full_size_sampled_verification():
     ls.close()
 
 
+def test_b32_full_size_fp8_draft_heads():
+    """E4M3 draft heads at the full B32 size (vocabulary 151936), bench launch shapes;
+    the oracle follows one sequence."""
+    from lockstep import Lockstep
+    cfg = CONFIGS["b32"].replace(draft_head_fp8=True)
+    prompts = make_prompts(cfg)
+    b = int(np.argmin([len(p) for p in prompts]))
+    ls = Lockstep(cfg, make_weights(cfg, "cuda"), prompts, rounds=2, seqs=[b])
+    for _ in range(2):
+        ls.step(tol=TOL)
+    ls.close()
+
+
 def test_hybrid_full_dims_lockstep():
     from lockstep import Lockstep
     cfg = CONFIGS["hybrid"].replace(batch=2, ctx_lo=96, ctx_hi=160)

@@ -222,9 +222,45 @@ def test_hybrid_shape_sampled_with_snapshots():
     ls.close()
 
 
+def test_b32_shape_fp8_draft_heads():
+    """T1 and drafter heads on the E4M3 head copy (tcgen05 kind::f8f6f4): drafts and their
+    logits against the oracle's quantised heads; the verify head stays bf16."""
+    ls = _lockstep(B32_R.replace(name="b32_r_fp8", draft_head_fp8=True), 3)
+    for _ in range(3):
+        ls.step(tol=TOL)
+    ls.close()
+
+
+def test_fp8_draft_heads_forced_stay_lossless():
+    """With quantised draft heads, drafts forced to the greedy stream are all accepted and
+    the commit is the plain greedy decode (only the drafts may change)."""
+    cfg = B32_R.replace(name="b32_r_fp8", draft_head_fp8=True, batch=2)
+    ls = _lockstep(cfg, 4)
+    greedy = [_greedy(ls, b, 8 * 4 + 9) for b in range(2)]
+    streams = [[ls.states[b].A] for b in range(2)]
+    for r in range(4):
+        forced = []
+        for b in range(2):
+            off = ls.states[b].a - len(ls.prompts[b])
+            d = list(greedy[b][off + 1: off + 8])
+            if r % 2:
+                d[3] = (d[3] + 1) % (cfg.vocab - 1)
+            forced.append(d)
+        o, recs = ls.step(forced=np.array(forced, np.int32), tol=TOL)
+        for b in range(2):
+            assert recs[b]["n"] == (3 if r % 2 else 7)
+            streams[b] += recs[b]["committed"]
+    for b in range(2):
+        if not ls.adopted:
+            assert streams[b] == greedy[b][:len(streams[b])]
+    ls.close()
+
+
 def test_temperature_validation():
     from mtp_block_draft_gb300 import DmtpError, DmtpRound
     w = make_weights(TINY, "cuda")
     for t in (-1.0, 1e-6, float("nan"), float("inf")):
         with pytest.raises(DmtpError):
             DmtpRound(TINY.replace(temperature=t), w, make_prompts(TINY), 256)
+    with pytest.raises(DmtpError):  # E4M3 draft heads need a bf16 model
+        DmtpRound(TINY.replace(draft_head_fp8=True), w, make_prompts(TINY), 256)
