@@ -382,14 +382,14 @@ class OracleModel:
         E = self.W["emb"]
         return np.stack([E[A], E[T1] + delta] + [E[self.cfg.mask_id]] * 6)
 
-    def drafter_forward(self, X: np.ndarray, st: SeqState, a: int):
+    def drafter_forward(self, X: np.ndarray, st: SeqState, a: int, with_head_in: bool = False):
         """One parallel block forward over the 8 slots at positions a..a+7.
 
         Every slot attends to the context K/V at positions max(0, a - window)..a-1
         ([DMTP] §6.2: a 4096-position window ending just before the anchor) and to all 8
         block slots with no mask inside the block ([DFvsMTP], block-diagonal mask).
         Returns drafter logits [6, V] for slots 2..7 (each predicts the token at its
-        own position).
+        own position), and with ``with_head_in`` also the normalised rows the head reads.
         """
         W, c = self.W, self.cfg
         lo = max(0, a - c.draft_window)
@@ -403,7 +403,7 @@ class OracleModel:
             X = X + o.reshape(8, -1) @ W[f"{pfx}.wo"].T
             X = X + self._mlp(pfx, X)
         hn = rms_norm(X[2:8], W["dft.final_norm"], self.eps)
-        return self.draft_head(hn)
+        return (self.draft_head(hn), hn) if with_head_in else self.draft_head(hn)
 
     # ---- prefill ----------------------------------------------------------------------
 
@@ -530,6 +530,7 @@ class OracleModel:
 
         # a1
         t1_logits = self.t1_head(h_mtp)
+        rec["t1_head_in"] = rms_norm(h_mtp[None], W["mtp.final_norm"], self.eps)
         ad = adopt.get("T")
         T1 = self._pick(t1_logits, ad[0] if ad is not None else adopt.get("T1"), log, "T1")
         if forced is not None:
@@ -538,7 +539,7 @@ class OracleModel:
         delta = self.fusion_delta(T1, h_mtp)
         X = self.drafter_slots(A, T1, delta)
         # a3
-        dlog = self.drafter_forward(X, st, a)
+        dlog, rec["draft_head_in"] = self.drafter_forward(X, st, a, with_head_in=True)
         drafts = [T1]
         for s in range(6):
             drafts.append(self._pick(dlog[s], ad[s + 1] if ad is not None else None,

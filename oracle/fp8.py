@@ -75,3 +75,26 @@ def fp8_logits(Y: np.ndarray, Hq: np.ndarray, Hs: np.ndarray) -> np.ndarray:
     """Draft logits of the quantised head: s_y s_v (q_y . q_v) for every row of Y."""
     qy, sy = quantize_rows(Y)
     return (qy @ Hq.T) * sy[:, None] * Hs[None, :]
+
+
+def fp8_logit_bounds(Y: np.ndarray, Hq: np.ndarray, Hs: np.ndarray, delta: float):
+    """Quantised draft logits of rows Y, and how far another implementation's quantised
+    logits can be from them when its rows differ from Y by at most ``delta`` per element:
+    for each row scale it could pick (the one of Y, and those of max|row| +- delta), its
+    element y' / s' rounds to a grid value between round(y/s' - delta/s') and
+    round(y/s' + delta/s') (rounding is monotone), so its dequantised element deviates from
+    Y's by at most dev_k; the logit of head row v then by at most sum_k |H_vk| dev_k.
+    Returns (logits, width)."""
+    Y = np.atleast_2d(np.asarray(Y, dtype=np.float64))
+    qy, sy = quantize_rows(Y)
+    logits = (qy @ Hq.T) * sy[:, None] * Hs[None, :]
+    dev = np.zeros_like(Y)
+    for i, y in enumerate(Y):
+        amax = np.max(np.abs(y))
+        ref = qy[i] * sy[i]
+        for sc in {sy[i], pow2_scale(amax + delta), pow2_scale(max(amax - delta, 0.0))}:
+            lo = round_e4m3(np.clip((y - delta) / sc, -E4M3_MAX, E4M3_MAX)) * sc
+            hi = round_e4m3(np.clip((y + delta) / sc, -E4M3_MAX, E4M3_MAX)) * sc
+            dev[i] = np.maximum(dev[i], np.maximum(np.abs(hi - ref), np.abs(lo - ref)))
+    width = dev @ (np.abs(Hq) * Hs[:, None]).T
+    return logits, width

@@ -13,8 +13,13 @@ import numpy as np
 import torch
 
 from oracle import OracleModel
+from oracle.fp8 import fp8_logit_bounds
 
 GATE = 0.05
+# E4M3 draft heads: the head inputs (normalised hidden rows) of the two sides agree within
+# this much per element (the hidden-state bar is 2e-2; measured ~3e-3), which bounds how
+# far each side's quantised input, and so each draft logit, can move
+FP8_INPUT_DELTA = 1e-2
 
 
 def to_np(t):
@@ -77,9 +82,23 @@ class Lockstep:
             assert int(o["mtp_len"][b]) == rec["mtp_len"]
             assert int(o["snap_slot"][b]) == rec["snap_slot"]
             if floats:
+                fp8 = self.cfg.draft_head_fp8
                 for name, key in (("t1_logits", "t1_logits"), ("draft_logits", "draft_logits"),
                                   ("verify_logits", "verify_logits"), ("delta", "delta"),
                                   ("h_mtp", "h_mtp_in")):
+                    if fp8 and name in ("t1_logits", "draft_logits"):
+                        # quantised draft heads: within the interval the input difference
+                        # allows (oracle/fp8.py), plus the float bar
+                        hin = rec["t1_head_in" if name == "t1_logits" else "draft_head_in"]
+                        ref, width = fp8_logit_bounds(hin, self.oracle.Hq, self.oracle.Hs,
+                                                      FP8_INPUT_DELTA)
+                        gpu = np.asarray(o[name][b], np.float64).reshape(ref.shape)
+                        excess = float(np.max(np.abs(gpu - ref) - width))
+                        self.max_err[name + "_beyond_bound"] = max(
+                            self.max_err.get(name + "_beyond_bound", -1e30), excess)
+                        self._err(name, gpu, ref)
+                        assert excess <= tol, (b, name, excess)
+                        continue
                     e = self._err(name, o[name][b], rec[key])
                     assert e <= tol, (b, name, e)
             recs[b] = rec

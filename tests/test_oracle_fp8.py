@@ -7,6 +7,8 @@
 * Power-of-two row scales: tight (max|row| in (224 s, 448 s]) and exact division.
 * Special case that reduces to exact arithmetic: rows already on the scaled E4M3 grid
   give the exact logits.
+* The lock-step bound (fp8_logit_bounds): inputs perturbed within delta quantise to
+  logits inside it, and it is zero for delta = 0.
 * Losslessness with quantised draft heads ([DMTP] §6.5: verification unchanged): the
   committed stream is still plain greedy decoding of the target, naturally and with
   forced drafts, while the draft logits do change.
@@ -16,7 +18,8 @@ import pytest
 import torch
 
 from oracle import OracleModel
-from oracle.fp8 import E4M3_MAX, e4m3_grid, fp8_logits, pow2_scale, quantize_rows, round_e4m3
+from oracle.fp8 import (E4M3_MAX, e4m3_grid, fp8_logit_bounds, fp8_logits, pow2_scale,
+                        quantize_rows, round_e4m3)
 from synth import CONFIGS, make_prompts, make_weights
 
 TINY = CONFIGS["tiny"]
@@ -75,6 +78,28 @@ def test_on_grid_rows_give_exact_logits():
     Y[:, 5] = -448.0 * 2.0 ** -7
     Hq, Hs = quantize_rows(H)
     np.testing.assert_array_equal(fp8_logits(Y, Hq, Hs), Y @ H.T)
+
+
+def test_logit_bounds_cover_perturbed_inputs():
+    """Rows perturbed by at most delta per element quantise to logits within the bound;
+    with delta = 0 the bound is zero."""
+    rng = np.random.default_rng(3)
+    H = rng.normal(0, 0.02, (300, 128))
+    Hq, Hs = quantize_rows(H)
+    Y = rng.normal(0, 1, (6, 128))
+    Y[0, 7] = 448.0 * 2.0 ** -7 * 0.9999        # near a scale boundary
+    l0, w0 = fp8_logit_bounds(Y, Hq, Hs, 0.0)
+    np.testing.assert_array_equal(w0, 0.0)
+    np.testing.assert_array_equal(l0, fp8_logits(Y, Hq, Hs))
+    delta = 1e-2
+    logits, width = fp8_logit_bounds(Y, Hq, Hs, delta)
+    worst = 0.0
+    for _ in range(200):
+        Yp = Y + rng.uniform(-delta, delta, Y.shape)
+        d = np.abs(fp8_logits(Yp, Hq, Hs) - logits)
+        assert np.all(d <= width + 1e-12)
+        worst = max(worst, float((d / np.maximum(width, 1e-30)).max()))
+    assert worst > 0.05     # the bound is not vacuous
 
 
 @pytest.fixture(scope="module")
