@@ -96,8 +96,6 @@ struct dmtp_ctx {
   void *t1q, *dnq;
   float *t1qs, *dnqs;
   bool fp8;
-  float* swp;  // gate/up GEMM with a K split: parked partial sums and per-tile counters
-  int* swcnt;
   float* hlast;
   int* prompts;
   int* plen;
@@ -275,10 +273,6 @@ size_t layout(dmtp_ctx* c, char* base) {
   c->cn = b.take<char>(r8 * d * es);
   c->delta = b.take<float>(B * d * 4);
   c->h_mtp = b.take<float>(B * d * 4);
-  if (c->dt == 1) {
-    c->swp = b.take<float>(tc_swiglu_part_floats(c->F, M) * 4);
-    c->swcnt = b.take<int>((size_t)((c->F + 127) / 128) * 2 * 4);
-  }
   c->t1in = b.take<char>(r1 * d * es);
   c->dn = b.take<char>(r6 * d * es);
   if (c->fp8) {
@@ -349,7 +343,7 @@ int plan_gu(dmtp_ctx* c, Gemm& g, const void* W, int M) {
   g.swiglu = true;
   const int mt = tc_mt(M);
   const int ms = (mt > 128 && mt % 32 == 0) ? 2 : 1;
-  return tc_plan_swiglu(&g.tc, W, c->F, c->d, c->xn, M, c->nsm, true, ms, 1) ? DMTP_EINVAL
+  return tc_plan_swiglu(&g.tc, W, c->F, c->d, c->xn, M, c->nsm, true, ms) ? DMTP_EINVAL
                                                                           : DMTP_OK;
 }
 
@@ -436,7 +430,7 @@ void gemm_swiglu(dmtp_ctx* c, const Gemm& g, void* h, long h_lo) {
   const double bytes = ((double)g.N * g.K + (double)g.M * g.K * 2) * esz(c) +
                        (double)g.M * (g.N / 2) * esz(c) * 2;
   launch(c, P_GEMM, bytes, 2.0 * g.M * g.N * g.K,
-         [&] { op_gemm_tc_swiglu(g.tc, h, h_lo, c->swp, c->swcnt, c->err, c->st); });
+         [&] { op_gemm_tc_swiglu(g.tc, h, h_lo, c->err, c->st); });
 }
 
 void zero(dmtp_ctx* c, void* p, size_t bytes) { cudaMemsetAsync(p, 0, bytes, c->st); }
@@ -767,7 +761,7 @@ float time_swiglu(dmtp_ctx* c, const TcPlan& p, const void* flush, size_t flush_
   for (int rep = 0; rep < 3; ++rep) {
     op_l2_flush(flush, flush_bytes, c->err, c->st);
     cudaEventRecord(e0, c->st);
-    op_gemm_tc_swiglu(p, c->hmid, (long)c->mt8 * c->F, c->swp, c->swcnt, c->err, c->st);
+    op_gemm_tc_swiglu(p, c->hmid, (long)c->mt8 * c->F, c->err, c->st);
     cudaEventRecord(e1, c->st);
     float ms = 1e30f;
     if (cudaEventSynchronize(e1) != cudaSuccess ||
@@ -825,33 +819,29 @@ int autotune(dmtp_ctx* c, const void* flush, size_t flush_bytes) {
     }
     if (hit) {
       const int r = g->swiglu ? tc_plan_swiglu(&g->tc, g->W, c->F, g->K, g->X, g->M, c->nsm,
-                                               g->split, hit->msplit, hit->splits)
+                                               g->split, hit->msplit)
                               : tc_plan_shape(&g->tc, g->W, g->N, g->K, g->X, g->M, c->nsm,
                                               g->split, hit->wide, hit->msplit,
                                               hit->splits);
       if (r) rc = DMTP_EINVAL;
       continue;
     }
-    if (g->swiglu) {  // tile shape: one or two token halves, 1..4 K parts
+    if (g->swiglu) {  // tile shape: one or two token halves; no K split
       TcPlan best_p = g->tc;
       float best_t = time_swiglu(c, g->tc, flush, flush_bytes, e0, e1);
-      for (int ms = 1; ms <= 2; ++ms)
-        for (int ks = 1; ks <= 4; ++ks) {
-          TcPlan p;
-          if ((ms == g->tc.msplit && ks == g->tc.splits) ||
-              tc_plan_swiglu(&p, g->W, c->F, g->K, g->X, g->M, c->nsm, g->split, ms, ks))
-            continue;
-          const float t = time_swiglu(c, p, flush, flush_bytes, e0, e1);
-          if (t < best_t) {
-            best_t = t;
-            best_p = p;
-          }
+      for (int ms = 1; ms <= 2; ++ms) {
+        TcPlan p;
+        if (ms == g->tc.msplit ||
+            tc_plan_swiglu(&p, g->W, c->F, g->K, g->X, g->M, c->nsm, g->split, ms))
+          continue;
+        const float t = time_swiglu(c, p, flush, flush_bytes, e0, e1);
+        if (t < best_t) {
+          best_t = t;
+          best_p = p;
         }
+      }
       g->tc = best_p;
-      g_tune.push_back({key, TuneChoice{2, best_p.msplit, best_p.splits, 0, 0}});
-      if (verbose)
-        fprintf(stderr, "dmtp: gate/up N=%d K=%d M=%d: %d token part(s), %d K part(s), "
-                "%.1f us\n", g->N, g->K, g->M, best_p.msplit, best_p.splits, best_t * 1e3f);
+      g_tune.push_back({key, TuneChoice{2, best_p.msplit, 1, 0, 0}});
       continue;
     }
     if (g->argmax) {  // LM head: vocabulary tile of 128 or 256 rows, 4 or 8 epilogue warps

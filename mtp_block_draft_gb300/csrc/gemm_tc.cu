@@ -38,7 +38,6 @@
 namespace dmtp {
 
 static constexpr int kHalfN = 128;  // weight rows per MMA (M) and per accumulator
-static constexpr int kSwigluMaxSplit = 4;  // K parts of the gate/up GEMM
 static constexpr int kBlockK = 64;   // k elements per stage (128 B of bf16)
 static constexpr uint32_t kHalfBytes = kHalfN * kBlockK * 2;  // one 128-row weight k slice
 
@@ -57,8 +56,6 @@ struct TcArgs {
   long h_lo;
   int F;           // EPI 2: gate rows 0..F-1, up rows F..2F-1 of W
   unsigned* err;
-  float* part;     // EPI 2 with a K split: parked partial sums [tile][split][2][mct][128]
-  int* cnt;        // EPI 2 with a K split: arrivals per tile (left at 0 after each launch)
 };
 
 // 16 accumulator columns of this warp's lanes at taddr, plus (merged) the lo columns
@@ -214,58 +211,10 @@ __global__ void __launch_bounds__(128, 1)
       }
     }
   } else if (EPI == 2) {
-    const int n = n0 + warp * 32 + lane;  // feature
-    const uint32_t tg = tmem + ((uint32_t)(warp * 32) << 16);
-    const uint32_t tu = tg + a.acc_cols;
-    const int zs = gridDim.z;
-    const long tile = (long)blockIdx.y * gridDim.x + blockIdx.x;
-    const long pstride = 2L * a.mct * kHalfN;  // floats of one parked partial
-    bool last = true;
-    if (zs > 1) {
-      // K split: every CTA parks its partial gate and up sums ([2][mct][128 rows], rows
-      // = TMEM lanes, so a warp's stores are contiguous); the CTA that arrives last on
-      // the tile's counter adds the others' to its own and applies SwiGLU.
-      __shared__ int s_last;
-      float* mine = a.part + (tile * zs + blockIdx.z) * pstride + warp * 32 + lane;
-      if (ok) {
-        for (int c = 0; c < a.mct; c += 16) {
-          uint32_t rg[16], ru[16], rgl[16], rul[16];
-          tmem_ld16_raw(tg + c, rg);
-          tmem_ld16_raw(tu + c, ru);
-          if (MERGED) {
-            tmem_ld16_raw(tg + a.mct + c, rgl);
-            tmem_ld16_raw(tu + a.mct + c, rul);
-          }
-          tmem_wait_ld16(rg);
-          reg_fence16(ru);
-          if (MERGED) {
-            reg_fence16(rgl);
-            reg_fence16(rul);
-          }
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            float g = __uint_as_float(rg[j]), u = __uint_as_float(ru[j]);
-            if (MERGED) {
-              g += __uint_as_float(rgl[j]);
-              u += __uint_as_float(rul[j]);
-            }
-            mine[(long)(c + j) * kHalfN] = g;
-            mine[(long)(a.mct + c + j) * kHalfN] = u;
-          }
-        }
-      }
-      __threadfence();
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        s_last = atomicAdd(&a.cnt[tile], 1) == zs - 1;
-        if (s_last) a.cnt[tile] = 0;  // every CTA of the tile has arrived
-      }
-      __syncthreads();
-      last = s_last != 0;
-      __threadfence();
-    }
-    if (ok && last) {
-      const float* base = a.part + tile * zs * pstride + warp * 32 + lane;
+    if (ok) {
+      const int n = n0 + warp * 32 + lane;  // feature
+      const uint32_t tg = tmem + ((uint32_t)(warp * 32) << 16);
+      const uint32_t tu = tg + a.acc_cols;
       for (int c = 0; c < a.mct; c += 16) {
         uint32_t rg[16], ru[16], rgl[16], rul[16];
         tmem_ld16_raw(tg + c, rg);
@@ -288,11 +237,6 @@ __global__ void __launch_bounds__(128, 1)
             if (MERGED) {
               g += __uint_as_float(rgl[j]);
               u += __uint_as_float(rul[j]);
-            }
-            for (int z = 0; z < zs; ++z) {  // the other K parts' parked sums
-              if (z == (int)blockIdx.z) continue;
-              g += __ldcg(base + z * pstride + (long)(c + j) * kHalfN);
-              u += __ldcg(base + z * pstride + (long)(a.mct + c + j) * kHalfN);
             }
             // silu(g) u = g sigmoid(g) u
             if (m < a.M)
@@ -467,9 +411,8 @@ int tc_plan_shape(TcPlan* p, const void* W, int N, int K, const void* X, int M, 
 }
 
 int tc_plan_swiglu(TcPlan* p, const void* W, int F, int K, const void* X, int M, int nsm,
-                   bool split, int msplit, int ksplit) {
-  if (ksplit < 1 || ksplit > kSwigluMaxSplit) return -10;
-  int r = tc_plan_shape(p, W, 2 * F, K, X, M, nsm, split, 2, msplit, ksplit);
+                   bool split, int msplit) {
+  int r = tc_plan_shape(p, W, 2 * F, K, X, M, nsm, split, 2, msplit, 1);
   if (r) return r;
   p->swiglu = 1;
   p->F = F;
@@ -510,17 +453,11 @@ int tc_init_attributes() {
   return 0;
 }
 
-size_t tc_swiglu_part_floats(int F, int M) {
-  return (size_t)((F + kHalfN - 1) / kHalfN) * kSwigluMaxSplit * 2 * tc_mt(M) * kHalfN;
-}
-
-void op_gemm_tc_swiglu(const TcPlan& p, void* h, long h_lo, float* part, int* cnt,
-                       unsigned* err, cudaStream_t st) {
+void op_gemm_tc_swiglu(const TcPlan& p, void* h, long h_lo, unsigned* err, cudaStream_t st) {
   TcArgs a{p.N,     p.K,     p.M,     p.MT,     p.stages, p.wide, p.mct,
            p.split, p.xbox,  p.nx,    p.x3d,    p.merged, p.acc_cols, nullptr,
-           0,       (bf16*)h, h_lo,   p.F,      err,      part,   cnt};
-  if (p.splits > 1 && (!part || !cnt)) return;  // excluded by the caller
-  dim3 grid(p.msplit, (p.F + kHalfN - 1) / kHalfN, p.splits);
+           0,       (bf16*)h, h_lo,   p.F,      err};
+  dim3 grid(p.msplit, (p.F + kHalfN - 1) / kHalfN, 1);
   kernel_for<2>(p)<<<grid, 128, p.smem, st>>>(p.tmW, p.tmX, a);
 }
 

@@ -204,15 +204,9 @@ int tc_plan(TcPlan* p, const void* W, int N, int K, const void* X, int M, int ns
 // Gate/up GEMM with the SwiGLU epilogue: W = [gate; up] ([2F, K]), each CTA pairs gate
 // rows n0.. with up rows F + n0.. (two accumulators) and writes h = silu(g) * u, a bf16
 // pair [M][F] (remainder at h + h_lo), so no fp32 output or separate SwiGLU pass.
-// ksplit (1..4) K parts per tile: each parks its partial sums in `part`, and the last to
-// arrive on the tile's counter in `cnt` (zeroed once; every launch leaves it at 0) sums
-// them and applies SwiGLU. part holds tc_swiglu_part_floats(F, M) floats, cnt one int per
-// (tile, token part).
 int tc_plan_swiglu(TcPlan* p, const void* W, int F, int K, const void* X, int M, int nsm,
-                   bool split, int msplit, int ksplit);
-size_t tc_swiglu_part_floats(int F, int M);
-void op_gemm_tc_swiglu(const TcPlan& p, void* h, long h_lo, float* part, int* cnt,
-                       unsigned* err, cudaStream_t st);
+                   bool split, int msplit);
+void op_gemm_tc_swiglu(const TcPlan& p, void* h, long h_lo, unsigned* err, cudaStream_t st);
 // tc_plan with the tile shape given: wide (1, 2), msplit (1, 2) and splits (<= 0: chosen).
 int tc_plan_shape(TcPlan* p, const void* W, int N, int K, const void* X, int M, int nsm,
                   bool split, int wide, int msplit, int splits);
