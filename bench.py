@@ -470,6 +470,12 @@ def main():
                                "profiled_round_ms": prof_round_ms,
                                "frac_of_timed": (alg_bytes / (hbm * 1e9) * 1e3) / (ms / args.steps)},
             "kernels": breakdown}
+    pf_ms, pf_tok = g.prefill_stats()
+    line["prefill"] = {"tokens": pf_tok, "ms": pf_ms,
+                       "tokens_per_s": pf_tok / (pf_ms / 1e3) if pf_ms > 0 else None,
+                       "note": "dmtp_init's prefill of the batch's prompts (target, drafter "
+                               "context, MTP rows), device time; the round's kernels, 8 "
+                               "positions per sequence per step"}
     rps_nat = args.steps / (ms / 1e3)
     line["projection"] = {
         "note": "B x measured rounds/s x the DMTP blog's per-verify acceptance lengths "

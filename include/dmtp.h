@@ -171,6 +171,12 @@ int dmtp_read_state(dmtp_ctx* ctx, int32_t* kv_len, int32_t* pending, uint64_t* 
 /* Number of kernel launches one round enqueues (for launch accounting). */
 int dmtp_round_launches(const dmtp_ctx* ctx);
 
+/* Device time of the prefill dmtp_init ran (ms, from CUDA events on its stream around
+ * the target, drafter-context and MTP passes over every prompt position and the pick of
+ * A; -1 if the events failed) and the prompt tokens it processed. Either pointer may be
+ * NULL. The prefill runs the round's kernels 8 positions per sequence at a time. */
+int dmtp_prefill_stats(const dmtp_ctx* ctx, double* ms, int64_t* tokens);
+
 /* Kernel classes of dmtp_profile. */
 #define DMTP_PROF_GEMM 0   /* tcgen05 (or fp32) projection / MLP GEMMs              */
 #define DMTP_PROF_HEAD 1   /* LM-head GEMM with fused argmax (a1, a3, a4)          */

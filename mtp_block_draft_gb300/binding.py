@@ -26,7 +26,7 @@ ERRORS = {0: "DMTP_OK", -1: "DMTP_EINVAL", -2: "DMTP_ENOMEM", -3: "DMTP_ECAPACIT
 # every symbol include/dmtp.h declares
 EXPORTS = ("dmtp_workspace_size", "dmtp_init", "dmtp_round", "dmtp_round_host",
            "dmtp_read_state", "dmtp_round_launches", "dmtp_round_profile", "dmtp_free",
-           "dmtp_strerror", "dmtp_t1_head_noalloc")
+           "dmtp_strerror", "dmtp_t1_head_noalloc", "dmtp_prefill_stats")
 
 PROFILE_CLASSES = ("gemm", "lm_head", "attention", "gdn", "other")
 
@@ -100,6 +100,8 @@ def load_library(path: str = LIB_PATH):
     lib.dmtp_read_state.restype = C.c_int
     lib.dmtp_round_launches.argtypes = [P]
     lib.dmtp_round_launches.restype = C.c_int
+    lib.dmtp_prefill_stats.argtypes = [P, C.POINTER(C.c_double), C.POINTER(C.c_int64)]
+    lib.dmtp_prefill_stats.restype = C.c_int
     lib.dmtp_round_profile.argtypes = [P, C.POINTER(dmtp_profile)]
     lib.dmtp_round_profile.restype = C.c_int
     lib.dmtp_free.argtypes = [P]
@@ -263,6 +265,14 @@ class DmtpRound:
             out[name] = {"ms": p.ms[i], "bytes": p.bytes[i], "flops": p.flops[i],
                          "launches": p.launches[i]}
         return out
+
+    def prefill_stats(self) -> tuple[float, int]:
+        """(device ms, prompt tokens) of the prefill dmtp_init ran."""
+        ms = C.c_double()
+        tok = C.c_int64()
+        _check(self.lib.dmtp_prefill_stats(self.ctx, C.byref(ms), C.byref(tok)),
+               "dmtp_prefill_stats")
+        return ms.value, tok.value
 
     def launches_per_round(self) -> int:
         return int(self.lib.dmtp_round_launches(self.ctx))

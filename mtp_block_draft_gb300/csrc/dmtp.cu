@@ -118,6 +118,8 @@ struct dmtp_ctx {
   long kv_bound;
   int launches;
   int round_launches;
+  double prefill_ms;     // device time of dmtp_init's prefill (CUDA events), -1 if unknown
+  long prefill_tokens;   // prompt tokens it processed
   // per-launch event profiling (dmtp_round_profile only)
   bool prof;
   std::vector<cudaEvent_t> pev;
@@ -1071,6 +1073,9 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
     cudaStreamSynchronize(st);
   }
   // ---- prefill: chunks of 8 positions per sequence ----
+  cudaEvent_t pe0 = nullptr, pe1 = nullptr;
+  if (cudaEventCreate(&pe0) == cudaSuccess && cudaEventCreate(&pe1) == cudaSuccess)
+    cudaEventRecord(pe0, st);
   const int nch = (pmax + 7) / 8;
   for (int ch = 0; ch < nch; ++ch) {
     op_prefill_chunk(s, c->prompts, c->plen, c->maxc, ch, st);
@@ -1091,7 +1096,16 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
   op_prefill_final(s, c->plen, c->hlast, c->hT32, c->d, st);
   mtp_advance(c);
   op_prefill_done(s, c->plen, st);
+  if (pe1) cudaEventRecord(pe1, st);
   cudaError_t ce = cudaStreamSynchronize(st);
+  c->prefill_ms = -1.0;
+  c->prefill_tokens = total;
+  if (pe1) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, pe0, pe1) == cudaSuccess) c->prefill_ms = ms;
+  }
+  if (pe0) cudaEventDestroy(pe0);
+  if (pe1) cudaEventDestroy(pe1);
   if (ce != cudaSuccess) {
     fprintf(stderr, "dmtp_init: %s\n", cudaGetErrorString(ce));
     delete c;
@@ -1221,6 +1235,13 @@ int dmtp_read_state(dmtp_ctx* c, int32_t* kv_len, int32_t* pending, uint64_t* hi
 }
 
 int dmtp_round_launches(const dmtp_ctx* c) { return c ? c->round_launches : 0; }
+
+int dmtp_prefill_stats(const dmtp_ctx* c, double* ms, int64_t* tokens) {
+  if (!c) return DMTP_EINVAL;
+  if (ms) *ms = c->prefill_ms;
+  if (tokens) *tokens = c->prefill_tokens;
+  return DMTP_OK;
+}
 
 int dmtp_round_profile(dmtp_ctx* c, dmtp_profile* out) {
   if (!c || !out) return DMTP_EINVAL;

@@ -256,6 +256,16 @@ def test_fp8_draft_heads_forced_stay_lossless():
     ls.close()
 
 
+def test_prefill_stats():
+    """dmtp_prefill_stats: the prompt tokens dmtp_init prefilled and a positive device time."""
+    from mtp_block_draft_gb300 import DmtpRound, default_max_ctx
+    prompts = make_prompts(B32_R)
+    g = DmtpRound(B32_R, make_weights(B32_R, "cuda"), prompts, default_max_ctx(prompts, 2))
+    ms, tok = g.prefill_stats()
+    assert tok == sum(len(p) for p in prompts) and ms > 0
+    g.close()
+
+
 def test_temperature_validation():
     from mtp_block_draft_gb300 import DmtpError, DmtpRound
     w = make_weights(TINY, "cuda")
