@@ -52,6 +52,7 @@ struct TcArgs {
   int acc_cols;    // TMEM columns per accumulator
   float* out;
   int ldo;
+  int tma_out;     // EPI 0: add the tile into out with TMA bulk reductions (tmO)
   bf16* h;         // EPI 2: SwiGLU output [M][F] (hi), remainder at h + h_lo
   long h_lo;
   int F;           // EPI 2: gate rows 0..F-1, up rows F..2F-1 of W
@@ -86,7 +87,7 @@ __host__ __device__ inline uint32_t tmem_cols_for(int cols) {
 template <int EPI, int WIDE, int NMMA, bool MERGED>
 __global__ void __launch_bounds__(128, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-              TcArgs a) {
+              const __grid_constant__ CUtensorMap tmO, TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);  // 1024-B aligned tiles
@@ -191,7 +192,36 @@ __global__ void __launch_bounds__(128, 1)
   bool ok = mbar_wait(smem_u32(accum), 0, a.err);
   ok = __all_sync(0xffffffffu, ok);
   tc_fence_after();
-  if (EPI == 0) {
+  if (EPI == 0 && a.tma_out) {
+    // Each weight half's [mct tokens][128 rows] fp32 tile is staged in the idle stage
+    // buffers (rows = TMEM lanes: a warp's stores are contiguous) and added into `out`
+    // by one TMA bulk reduction, in place of mct scattered atomics per thread.
+    const bool okb = __syncthreads_and(ok);
+    float* stg = reinterpret_cast<float*>(smem);
+#pragma unroll
+    for (int h = 0; h < WIDE; ++h) {
+      if (h > 0) {  // the previous reduction has read the staging tile
+        if (threadIdx.x == 0) bulk_wait_read0();
+        __syncthreads();
+      }
+      if (okb) {
+        const uint32_t tbase = tmem + h * a.acc_cols + ((uint32_t)(warp * 32) << 16);
+        for (int c = 0; c < a.mct; c += 16) {
+          float v[16];
+          acc_ld16<MERGED>(tbase + c, a.mct, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) stg[(c + j) * kHalfN + warp * 32 + lane] = v[j];
+        }
+      }
+      fence_proxy_async_smem();
+      __syncthreads();
+      if (threadIdx.x == 0 && okb && n0 + h * kHalfN < a.N && mrow0 < a.M) {
+        tma_reduce_add_2d(&tmO, n0 + h * kHalfN, mrow0, smem_u32(stg));
+        bulk_commit();
+      }
+    }
+    if (threadIdx.x == 0) bulk_wait_read0();  // the staging tile is read before exit
+  } else if (EPI == 0) {
     if (ok) {
 #pragma unroll
       for (int h = 0; h < WIDE; ++h) {
@@ -292,6 +322,23 @@ int tc_make_tmap(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols
   return r == CUDA_SUCCESS ? 0 : -3;
 }
 
+// [rows, cols] fp32 with a row pitch of ld elements, box {box_cols, box_rows}, no swizzle
+// (the plain row-major layout of a staged output tile).
+int tc_make_tmap_f32(CUtensorMap* tm, void* base, uint64_t rows, uint64_t cols, uint64_t ld,
+                     uint32_t box_cols, uint32_t box_rows) {
+  PFN_encodeTiled_t enc = get_encode();
+  if (!enc) return -1;
+  if (((uintptr_t)base & 15) || (ld * 4) % 16 || box_cols * 4 % 16) return -2;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld * 4};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -3;
+}
+
 // [rows, cols] row-major bytes (E4M3), box {128, box_rows}, 128-byte swizzle: the same
 // shared-memory layout as a bf16 box of 64 columns.
 int tc_make_tmap_u8(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols,
@@ -380,6 +427,7 @@ int tc_plan_shape(TcPlan* p, const void* W, int N, int K, const void* X, int M, 
   while (st > 2 && smem_bytes(wide, xrows, st) > kSmemBudget) --st;
   p->stages = st;
   p->smem = smem_bytes(wide, xrows, st);
+  p->stage_area = (size_t)st * (wide * kHalfBytes + (size_t)xrows * kBlockK * 2);
   if (p->smem > kSmemBudget) return -10;
   const int tiles = (N + kHalfN * wide - 1) / (kHalfN * wide) * msplit;
   const int nkb = K / kBlockK;
@@ -426,7 +474,8 @@ int tc_plan(TcPlan* p, const void* W, int N, int K, const void* X, int M, int ns
 
 // The kernel instantiation for a plan: (wide, MMAs per k step, merged).
 template <int EPI>
-static void (*kernel_for(const TcPlan& p))(const CUtensorMap, const CUtensorMap, TcArgs) {
+static void (*kernel_for(const TcPlan& p))(const CUtensorMap, const CUtensorMap,
+                                             const CUtensorMap, TcArgs) {
   const int nmma = p.merged ? 1 : p.nx;
   if (EPI == 2) {
     if (p.merged) return k_gemm_tc<2, 2, 1, true>;
@@ -442,7 +491,7 @@ static void (*kernel_for(const TcPlan& p))(const CUtensorMap, const CUtensorMap,
 
 int tc_init_attributes() {
   const int bytes = (int)(kSmemBudget + 8 * 1024);
-  void (*ks[])(const CUtensorMap, const CUtensorMap, TcArgs) = {
+  void (*ks[])(const CUtensorMap, const CUtensorMap, const CUtensorMap, TcArgs) = {
       k_gemm_tc<0, 1, 1, true>,  k_gemm_tc<0, 1, 1, false>, k_gemm_tc<0, 1, 2, false>,
       k_gemm_tc<0, 2, 1, true>,  k_gemm_tc<0, 2, 1, false>, k_gemm_tc<0, 2, 2, false>,
       k_gemm_tc<2, 2, 1, true>,  k_gemm_tc<2, 2, 1, false>, k_gemm_tc<2, 2, 2, false>};
@@ -456,17 +505,24 @@ int tc_init_attributes() {
 void op_gemm_tc_swiglu(const TcPlan& p, void* h, long h_lo, unsigned* err, cudaStream_t st) {
   TcArgs a{p.N,     p.K,     p.M,     p.MT,     p.stages, p.wide, p.mct,
            p.split, p.xbox,  p.nx,    p.x3d,    p.merged, p.acc_cols, nullptr,
-           0,       (bf16*)h, h_lo,   p.F,      err};
+           0,       0,       (bf16*)h, h_lo,    p.F,      err};
   dim3 grid(p.msplit, (p.F + kHalfN - 1) / kHalfN, 1);
-  kernel_for<2>(p)<<<grid, 128, p.smem, st>>>(p.tmW, p.tmX, a);
+  kernel_for<2>(p)<<<grid, 128, p.smem, st>>>(p.tmW, p.tmX, p.tmW, a);
 }
 
 void op_gemm_tc_acc(const TcPlan& p, float* out, int ldo, unsigned* err, cudaStream_t st) {
+  // the TMA bulk-reduction epilogue when a weight half's tile fits the stage buffers and
+  // out can be described by a tensor map; else per-element atomics
+  CUtensorMap tmO = p.tmW;
+  int tma = 0;
+  if (p.stage_area >= (size_t)p.mct * kHalfN * 4 && ldo % 4 == 0 && aligned_to(out, 16))
+    tma = tc_make_tmap_f32(&tmO, out, (uint64_t)p.M, (uint64_t)p.N, (uint64_t)ldo, kHalfN,
+                           (uint32_t)p.mct) == 0;
   TcArgs a{p.N,     p.K,     p.M,     p.MT,     p.stages, p.wide, p.mct,
            p.split, p.xbox,  p.nx,    p.x3d,    p.merged, p.acc_cols, out,
-           ldo,     nullptr, 0,       0,        err};
+           ldo,     tma,     nullptr, 0,        0,        err};
   dim3 grid(p.msplit, (p.N + kHalfN * p.wide - 1) / (kHalfN * p.wide), p.splits);
-  kernel_for<0>(p)<<<grid, 128, p.smem, st>>>(p.tmW, p.tmX, a);
+  kernel_for<0>(p)<<<grid, 128, p.smem, st>>>(p.tmW, p.tmX, tmO, a);
 }
 
 }  // namespace dmtp

@@ -181,12 +181,17 @@ struct TcPlan {
   int acc_cols;   // TMEM columns per accumulator
   int swiglu, F;  // SwiGLU epilogue: W = [gate; up] of F rows each
   size_t smem;
+  size_t stage_area;  // bytes of the stage ring (reused to stage output tiles)
 };
 // Padded token rows of an M-row operand (multiple of 16, >= 16).
 int tc_mt(int M);
 // Tensor map of a row-major bf16 [rows, cols] matrix, box {64, box_rows}, 128-B swizzle.
 int tc_make_tmap(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols,
                  uint32_t box_rows);
+// Tensor map of a row-major fp32 matrix [rows, cols] with row pitch ld elements, box
+// {box_cols, box_rows}, no swizzle.
+int tc_make_tmap_f32(CUtensorMap* tm, void* base, uint64_t rows, uint64_t cols, uint64_t ld,
+                     uint32_t box_cols, uint32_t box_rows);
 // Tensor map of a row-major byte matrix [rows, cols] (E4M3), box {128, box_rows}, 128-B
 // swizzle.
 int tc_make_tmap_u8(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols,
