@@ -289,6 +289,14 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* tm, int x, 
       ::"l"((uint64_t)tm), "r"(x), "r"(y), "r"(smem)
       : "memory");
 }
+// Bulk tensor store of the shared-memory tile at smem to global coordinates (x, y, z).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* tm, int x, int y, int z,
+                                             uint32_t smem) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];"
+      ::"l"((uint64_t)tm), "r"(x), "r"(y), "r"(z), "r"(smem)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

@@ -240,6 +240,51 @@ __global__ void __launch_bounds__(128, 1)
         }
       }
     }
+  } else if (EPI == 2 && a.tma_out) {
+    // silu(g) u as the down GEMM's bf16 pair, staged as [hi | lo][mct tokens][128
+    // features] in the idle stage ring and written by one 3-D TMA store
+    const bool okb = __syncthreads_and(ok);
+    bf16* sh = reinterpret_cast<bf16*>(smem);
+    const int row = warp * 32 + lane;
+    if (okb) {
+      const uint32_t tg = tmem + ((uint32_t)(warp * 32) << 16);
+      const uint32_t tu = tg + a.acc_cols;
+      for (int c = 0; c < a.mct; c += 16) {
+        uint32_t rg[16], ru[16], rgl[16], rul[16];
+        tmem_ld16_raw(tg + c, rg);
+        tmem_ld16_raw(tu + c, ru);
+        if (MERGED) {
+          tmem_ld16_raw(tg + a.mct + c, rgl);
+          tmem_ld16_raw(tu + a.mct + c, rul);
+        }
+        tmem_wait_ld16(rg);
+        reg_fence16(ru);
+        if (MERGED) {
+          reg_fence16(rgl);
+          reg_fence16(rul);
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          float g = __uint_as_float(rg[j]), u = __uint_as_float(ru[j]);
+          if (MERGED) {
+            g += __uint_as_float(rgl[j]);
+            u += __uint_as_float(rul[j]);
+          }
+          // silu(g) u = g sigmoid(g) u
+          const float v = g * __frcp_rn(1.f + __expf(-g)) * u;
+          const bf16 hi = __float2bfloat16_rn(v);
+          sh[(c + j) * kHalfN + row] = hi;
+          sh[(a.mct + c + j) * kHalfN + row] = __float2bfloat16_rn(v - __bfloat162float(hi));
+        }
+      }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (threadIdx.x == 0 && okb && n0 < a.F && mrow0 < a.M) {
+      tma_store_3d(&tmO, n0, mrow0, 0, smem_u32(sh));
+      bulk_commit();
+      bulk_wait_read0();
+    }
   } else if (EPI == 2) {
     if (ok) {
       const int n = n0 + warp * 32 + lane;  // feature
@@ -334,6 +379,23 @@ int tc_make_tmap_f32(CUtensorMap* tm, void* base, uint64_t rows, uint64_t cols, 
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t es[2] = {1, 1};
   CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -3;
+}
+
+// 3-D bf16 view [d2][d1][d0] with byte strides s1, s2 and an unswizzled box {b0, b1, b2}
+// (a plain row-major staging layout; used for output tiles).
+int tc_make_tmap3s_box(CUtensorMap* tm, void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                       uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2) {
+  PFN_encodeTiled_t enc = get_encode();
+  if (!enc) return -1;
+  if (((uintptr_t)base & 15) || s1 % 16 || s2 % 16 || (b0 * 2) % 16) return -2;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {s1, s2};
+  cuuint32_t box[3] = {b0, b1, b2};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? 0 : -3;
@@ -503,11 +565,18 @@ int tc_init_attributes() {
 }
 
 void op_gemm_tc_swiglu(const TcPlan& p, void* h, long h_lo, unsigned* err, cudaStream_t st) {
+  // the TMA-store epilogue when the [hi | lo] tile fits the stage buffers
+  CUtensorMap tmO = p.tmW;
+  int tma = 0;
+  if (p.stage_area >= (size_t)p.mct * kHalfN * 4 && h_lo > 0 && aligned_to(h, 16) &&
+      (p.F * 2) % 16 == 0 && (h_lo * 2) % 16 == 0)
+    tma = tc_make_tmap3s_box(&tmO, h, (uint64_t)p.F, (uint64_t)p.M, 2, (uint64_t)p.F * 2,
+                             (uint64_t)h_lo * 2, kHalfN, (uint32_t)p.mct, 2) == 0;
   TcArgs a{p.N,     p.K,     p.M,     p.MT,     p.stages, p.wide, p.mct,
            p.split, p.xbox,  p.nx,    p.x3d,    p.merged, p.acc_cols, nullptr,
-           0,       0,       (bf16*)h, h_lo,    p.F,      err};
+           0,       tma,     (bf16*)h, h_lo,    p.F,      err};
   dim3 grid(p.msplit, (p.F + kHalfN - 1) / kHalfN, 1);
-  kernel_for<2>(p)<<<grid, 128, p.smem, st>>>(p.tmW, p.tmX, p.tmW, a);
+  kernel_for<2>(p)<<<grid, 128, p.smem, st>>>(p.tmW, p.tmX, tmO, a);
 }
 
 void op_gemm_tc_acc(const TcPlan& p, float* out, int ldo, unsigned* err, cudaStream_t st) {

@@ -192,6 +192,9 @@ int tc_make_tmap(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols
 // {box_cols, box_rows}, no swizzle.
 int tc_make_tmap_f32(CUtensorMap* tm, void* base, uint64_t rows, uint64_t cols, uint64_t ld,
                      uint32_t box_cols, uint32_t box_rows);
+// 3-D bf16 view [d2][d1][d0] with byte strides s1, s2, unswizzled box {b0, b1, b2}.
+int tc_make_tmap3s_box(CUtensorMap* tm, void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                       uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2);
 // Tensor map of a row-major byte matrix [rows, cols] (E4M3), box {128, box_rows}, 128-B
 // swizzle.
 int tc_make_tmap_u8(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols,
