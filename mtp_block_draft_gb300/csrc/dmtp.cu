@@ -694,7 +694,7 @@ int check_err(dmtp_ctx* c) {
 // C ABI
 // ---- GEMM tile selection by measurement ----
 // Every distinct GEMM shape (N, K, M, operand, epilogue) is timed on the device with
-// each tile shape (128 or 256 weight rows per CTA, one or two token halves, K splits
+// each tile shape (128 or 256 weight rows per CTA, one to four token parts, K splits
 // around the wave-count choice), cold: the L2 is flushed by a 256 MB read before each
 // run, as in the round, where each weight matrix is streamed once. The fastest shape
 // serves every GEMM of that shape. The LM heads are timed the same way over their tile
@@ -828,10 +828,10 @@ int autotune(dmtp_ctx* c, const void* flush, size_t flush_bytes) {
       if (r) rc = DMTP_EINVAL;
       continue;
     }
-    if (g->swiglu) {  // tile shape: one or two token halves; no K split
+    if (g->swiglu) {  // tile shape: one to four token parts; no K split
       TcPlan best_p = g->tc;
       float best_t = time_swiglu(c, g->tc, flush, flush_bytes, e0, e1);
-      for (int ms = 1; ms <= 2; ++ms) {
+      for (int ms = 1; ms <= 4; ++ms) {
         TcPlan p;
         if (ms == g->tc.msplit ||
             tc_plan_swiglu(&p, g->W, c->F, g->K, g->X, g->M, c->nsm, g->split, ms))
@@ -870,7 +870,7 @@ int autotune(dmtp_ctx* c, const void* flush, size_t flush_bytes) {
     TuneChoice best{g->tc.wide, g->tc.msplit, g->tc.splits, 0, 0};
     float best_ms = time_plan(c, g->tc, flush, flush_bytes, e0, e1);
     for (int wide = 1; wide <= 2; ++wide)
-      for (int ms = 1; ms <= 2; ++ms) {
+      for (int ms = 1; ms <= 4; ++ms) {
         TcPlan p0;
         if (tc_plan_shape(&p0, g->W, g->N, g->K, g->X, g->M, c->nsm, g->split, wide, ms, 0))
           continue;

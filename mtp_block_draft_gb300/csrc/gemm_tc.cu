@@ -460,8 +460,8 @@ int tc_mt(int M) { return std::max(16, (M + 15) / 16 * 16); }
 
 int tc_plan_shape(TcPlan* p, const void* W, int N, int K, const void* X, int M, int nsm,
                   bool split, int wide, int msplit, int splits) {
-  if (M < 1 || M > 256 || K % kBlockK || N < 1 || (wide != 1 && wide != 2) ||
-      (msplit != 1 && msplit != 2))
+  if (M < 1 || M > 256 || K % kBlockK || N < 1 || (wide != 1 && wide != 2) || msplit < 1 ||
+      msplit > 4)
     return -10;
   p->N = N;
   p->K = K;
@@ -472,8 +472,11 @@ int tc_plan_shape(TcPlan* p, const void* W, int N, int K, const void* X, int M, 
   p->split = split ? 1 : 0;
   p->wide = wide;
   p->msplit = msplit;
-  if (p->MT % (16 * msplit)) return -10;
-  p->mct = p->MT / msplit;
+  // token parts of mct rows (a multiple of 16); the last part may be short: its rows past
+  // MT read as zeros (tensor-map bounds) and are not written
+  p->mct = (p->MT / msplit + 15) / 16 * 16;
+  if (p->mct * msplit < p->MT) p->mct += 16;
+  if (p->mct * (msplit - 1) >= p->MT) return -10;  // every part has rows
   if (split && msplit == 1 && 2 * p->MT <= 256) {  // [hi; lo] rows adjacent: one load
     p->xbox = 2 * p->MT;
     p->nx = 1;

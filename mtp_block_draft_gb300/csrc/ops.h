@@ -172,7 +172,7 @@ struct TcPlan {
   CUtensorMap tmW, tmX;
   int N, K, M, MT, splits, stages;
   int wide;       // 128-row weight halves per CTA (1 or 2)
-  int msplit;     // token halves: CTAs per weight tile (1 or 2)
+  int msplit;     // token parts: CTAs per weight tile (1..4; the last part may be short)
   int mct;        // token rows per CTA
   int split;      // X is the [hi; lo] bf16 pair
   int xbox, nx;   // X rows per box, boxes per stage
@@ -215,7 +215,7 @@ int tc_plan(TcPlan* p, const void* W, int N, int K, const void* X, int M, int ns
 int tc_plan_swiglu(TcPlan* p, const void* W, int F, int K, const void* X, int M, int nsm,
                    bool split, int msplit);
 void op_gemm_tc_swiglu(const TcPlan& p, void* h, long h_lo, unsigned* err, cudaStream_t st);
-// tc_plan with the tile shape given: wide (1, 2), msplit (1, 2) and splits (<= 0: chosen).
+// tc_plan with the tile shape given: wide (1, 2), msplit (1..4) and splits (<= 0: chosen).
 int tc_plan_shape(TcPlan* p, const void* W, int N, int K, const void* X, int M, int nsm,
                   bool split, int wide, int msplit, int splits);
 void op_gemm_tc_acc(const TcPlan& p, float* out, int ldo, unsigned* err, cudaStream_t st);
