@@ -844,6 +844,9 @@ int autotune(dmtp_ctx* c, const void* flush, size_t flush_bytes) {
       }
       g->tc = best_p;
       g_tune.push_back({key, TuneChoice{2, best_p.msplit, 1, 0, 0}});
+      if (verbose)
+        fprintf(stderr, "dmtp: gate/up F=%d K=%d M=%d: %d token part(s), %.1f us\n", c->F,
+                g->K, g->M, best_p.msplit, best_t * 1e3f);
       continue;
     }
     if (g->argmax) {  // LM head: vocabulary tile of 128 or 256 rows, 4 or 8 epilogue warps
