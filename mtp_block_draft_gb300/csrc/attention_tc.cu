@@ -612,32 +612,46 @@ __global__ void __launch_bounds__(256) k_attn_merge_p(AttnArgs a) {
   const long seg = (long)b * a.hkv + g;
   // CTAs with an empty range (more CTAs than tiles) wrote nothing
   auto empty = [&](int i) { return T * i / G == T * (i + 1) / G; };
-  float M = -INFINITY;
-  for (int i = c0 + lane; i <= c1; i += 32)
-    if (!empty(i)) M = fmaxf(M, a.part_ml[((i + seg) * QN + qi) * 2]);
-  M = warp_max(M);
-  float Lsum = 0.f;
-  for (int i = c0 + lane; i <= c1; i += 32) {
-    if (empty(i)) continue;
-    const float* ml = a.part_ml + ((i + seg) * QN + qi) * 2;
-    Lsum += ml[1] * __expf(ml[0] - M);
-  }
-  Lsum = warp_sum(Lsum);
-  const float invL = 1.f / Lsum;
+  // online merge over the contributing CTAs, four at a time with all of a batch's loads
+  // in flight: running maximum Mx, sum L and output acc, rescaled as the maximum moves
+  float Mx = -INFINITY, L = 0.f;
   float acc[DPL];
 #pragma unroll
   for (int j = 0; j < DPL; ++j) acc[j] = 0.f;
-  for (int i = c0; i <= c1; ++i) {
-    if (empty(i)) continue;
-    const float w = __expf(a.part_ml[((i + seg) * QN + qi) * 2] - M);
-    const float* pc = a.part_o + ((i + seg) * QN + qi) * a.hd + lane * DPL;
+  for (int i0 = c0; i0 <= c1; i0 += 4) {
+    float mi[4], li[4];
+    float2 oi[4][DPL / 2];
+    bool vi[4];
 #pragma unroll
-    for (int j = 0; j < DPL; j += 2) {
-      const float2 v = *reinterpret_cast<const float2*>(pc + j);
-      acc[j] += v.x * w;
-      acc[j + 1] += v.y * w;
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u;
+      vi[u] = i <= c1 && !empty(i);
+      mi[u] = -INFINITY;
+      li[u] = 0.f;
+      if (vi[u]) {
+        const float* ml = a.part_ml + ((i + seg) * QN + qi) * 2;
+        mi[u] = ml[0];
+        li[u] = ml[1];
+        const float* pc = a.part_o + ((i + seg) * QN + qi) * a.hd + lane * DPL;
+#pragma unroll
+        for (int j = 0; j < DPL / 2; ++j) oi[u][j] = *reinterpret_cast<const float2*>(pc + 2 * j);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (!vi[u] || mi[u] == -INFINITY) continue;  // a partial with no visible key
+      const float Mn = fmaxf(Mx, mi[u]);
+      const float s0 = __expf(Mx - Mn), s1 = __expf(mi[u] - Mn);  // Mx = -inf: s0 = 0
+      L = L * s0 + li[u] * s1;
+#pragma unroll
+      for (int j = 0; j < DPL / 2; ++j) {
+        acc[2 * j] = acc[2 * j] * s0 + oi[u][j].x * s1;
+        acc[2 * j + 1] = acc[2 * j + 1] * s0 + oi[u][j].y * s1;
+      }
+      Mx = Mn;
     }
   }
+  const float invL = 1.f / L;
   bf16* out = (bf16*)a.out + (long)mrow * a.hq * a.hd + h * a.hd + lane * DPL;
 #pragma unroll
   for (int j = 0; j < DPL; ++j) store_act(out + j, a.out_lo, acc[j] * invL);
