@@ -234,16 +234,17 @@ __global__ void __launch_bounds__(320, 1)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
-  // S buffers at columns 0 and TK, O (HD columns) after them, then Q: HD bf16 per lane
-  // = HD/2 columns
-  constexpr uint32_t kTmemCols = 2 * TK + HD + HD / 2 <= 256 ? 256 : 512;
+  // S buffers at columns 0 and TK, O (HD columns) after them, then two Q buffers (one per
+  // piece parity): HD bf16 per lane = HD/2 columns each
+  constexpr uint32_t kTmemCols = 2 * TK + 2 * HD <= 256 ? 256 : 512;
+  static_assert(2 * TK + 2 * HD <= 512, "TMEM plan exceeds 512 columns");
   if (warp == 8) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tO = tmem + 2 * TK;
-  const uint32_t tQ = tO + HD;
+  auto tQb = [&](int buf) -> uint32_t { return tO + HD + (uint32_t)buf * (HD / 2); };
 
   if (warp == 8) {
     if (lane == 0) {
@@ -280,7 +281,7 @@ __global__ void __launch_bounds__(320, 1)
       // ---------------- MMA issuer ----------------
       const uint32_t id_qk = umma_idesc_bf16(128, TK);
       const uint32_t id_pv = umma_idesc_bf16(128, HD);
-      auto issue_qk = [&](int xg) -> bool {
+      auto issue_qk = [&](int xg, uint32_t tQ) -> bool {
         const int s = xg % NST;
         if (!mbar_wait(smem_u32(&kv_full[s]), (xg / NST) & 1, err)) return false;
         tc_fence_after();
@@ -304,14 +305,15 @@ __global__ void __launch_bounds__(320, 1)
         ok = mbar_wait(smem_u32(q_full), p & 1, err);
         if (!ok) break;
         tc_fence_after();
+        const uint32_t tQ = tQb(p & 1);
         // S of the piece's first tile (its buffer was released by the p_full of the
         // tile before, waited for in the previous iteration)
-        ok = issue_qk(gt);
+        ok = issue_qk(gt, tQ);
         for (int t = 0; t < nt && ok; ++t) {
           const int xg = gt + t;
           // the next tile's scores overlap this tile's softmax
           if (t + 1 < nt) {
-            if (!issue_qk(xg + 1)) {
+            if (!issue_qk(xg + 1, tQ)) {
               ok = false;
               break;
             }
@@ -363,12 +365,12 @@ __global__ void __launch_bounds__(320, 1)
     const int pblk = (kq * KQ) / 64, pch = ((kq * KQ) % 64) / 8;
     bool ok = true;
     int gt = 0, p = 0;
-    // The queries of a piece into TMEM (A operand of S): lane lrow holds query row
-    // lrow % 64 (zeros past QN), the hi half in lanes 0..63 and the lo half in lanes
-    // 64..127; the warps of head-dim half hf write columns hf*HD/4.. of the lane's
-    // HD/2. Called when no S of the previous piece is pending (the softmax warps have
-    // consumed them all).
-    auto write_q = [&](int b, int g) {
+    // The queries of a piece into TMEM Q buffer `buf` (A operand of S): lane lrow holds
+    // query row lrow % 64 (zeros past QN), the hi half in lanes 0..63 and the lo half in
+    // lanes 64..127; the warps of head-dim half hf write columns hf*HD/4.. of the lane's
+    // HD/2. The buffer was last read by the S of the piece before the previous one, all
+    // consumed by then.
+    auto write_q = [&](int b, int g, int buf) {
       constexpr int NW = HD / 4;  // 32-bit columns per thread
       uint32_t w[NW];
       if (r < QN) {
@@ -392,7 +394,7 @@ __global__ void __launch_bounds__(320, 1)
         uint32_t v[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] = w[c16 * 16 + i];
-        tmem_st16u(tQ + lane_off + hf * NW + c16 * 16, v);
+        tmem_st16u(tQb(buf) + lane_off + hf * NW + c16 * 16, v);
       }
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
@@ -401,7 +403,7 @@ __global__ void __launch_bounds__(320, 1)
     {
       int b, g, kt0, nt, base;
       piece(x0, b, g, kt0, nt, base);
-      write_q(b, g);
+      write_q(b, g, 0);
     }
     // Every thread runs the same pieces and the same named barriers, whether or not a
     // wait timed out (then the work is skipped), so the barriers always complete.
@@ -524,7 +526,15 @@ __global__ void __launch_bounds__(320, 1)
         }
         mbar_arrive(smem_u32(p_full));
       }
-      // ---- end of the piece: O once its last P V completed ----
+      // ---- end of the piece ----
+      // the next piece's queries into the other Q buffer first, so that its first S is
+      // computed while this piece's O is read out and written
+      if (x + nt < x1) {
+        int b2, g2, kt2, nt2, base2;
+        piece(x + nt, b2, g2, kt2, nt2, base2);
+        write_q(b2, g2, (p + 1) & 1);
+      }
+      // O once its last P V completed
       float O[HALF];
       ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(pfin), p & 1, err));
       if (ok) {
@@ -566,11 +576,6 @@ __global__ void __launch_bounds__(320, 1)
       mbar_arrive(smem_u32(o_drained));
       gt += nt;
       x += nt;
-      if (x < x1) {  // the next piece's queries: every S of this piece has been consumed
-        int b2, g2, kt2, nt2, base2;
-        piece(x, b2, g2, kt2, nt2, base2);
-        write_q(b2, g2);
-      }
     }
   }
   __syncwarp();
