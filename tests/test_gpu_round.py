@@ -256,6 +256,16 @@ def test_fp8_draft_heads_forced_stay_lossless():
     ls.close()
 
 
+def test_b32_shape_sampled_with_fp8_draft_heads():
+    """Sampled verification and E4M3 draft heads together: the drafts come from the
+    quantised heads, the verify picks from the bf16 head's sampling epilogue."""
+    cfg = B32_RS.replace(name="b32_r_sampled_fp8", draft_head_fp8=True)
+    ls = _lockstep(cfg, 2, seqs=[0, 17, 31])
+    for _ in range(2):
+        ls.step(tol=TOL)
+    ls.close()
+
+
 def test_prefill_stats():
     """dmtp_prefill_stats: the prompt tokens dmtp_init prefilled and a positive device time."""
     from mtp_block_draft_gb300 import DmtpRound, default_max_ctx
