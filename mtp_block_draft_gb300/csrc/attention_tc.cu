@@ -24,8 +24,7 @@
 //                write P as a bf16 pair, P_hi in operand rows 0..63, P_lo in 64..127.
 //   O += P V   : tcgen05 M=128, N=hd, K=TK keys, B = the transposed V tile (K-major);
 //                O stays in TMEM for the whole piece: lanes 0..63 accumulate P_hi V,
-//                lanes 64..127 P_lo V; both halves go to the partial as they are (with
-//                each key quarter's running sum), and the merge adds them.
+//                lanes 64..127 P_lo V; they are summed once at the end of the piece.
 // The reference max only moves when a row's scores exceed it by more than 2^11; then
 // that row's O (both halves) is rescaled in TMEM. Keeping a stale reference is exact:
 // the same factor multiplies O and the running sum l.
@@ -129,9 +128,10 @@ struct Smem {
   static constexpr uint32_t kPTile = (TK / 64) * kBlk;  // 128 rows x TK keys
   static constexpr bool kPinK = kKTile >= kPTile;
   static constexpr uint32_t kP = kPinK ? 0 : 2 * kPTile;
-  // barriers, tile maxima [2][4][64], (unused [4][64]), tile-count prefix [B + 1]
+  static constexpr uint32_t kX = 64 * (HD / 2 + 4) * 4;  // P_lo V half rows, final sum
+  // barriers, tile maxima [2][4][64], running sums [4][64], tile-count prefix [B + 1]
   static constexpr uint32_t kSmall = 256 + 2048 + 1024 + 4 * (kAttnMaxB + 1);
-  static constexpr uint32_t kBig = NST * kStage + kP;  // 1024-aligned region
+  static constexpr uint32_t kBig = NST * kStage + kP + kX;  // 1024-aligned region
   static constexpr uint32_t kBytes = (kSmall + 1023) / 1024 * 1024 + kBig;
   static_assert(kBytes <= 232448, "shared memory plan exceeds 227 KB");
 };
@@ -151,7 +151,8 @@ __global__ void __launch_bounds__(320, 1)
   const int grp = a.hq / a.hkv, QN = 8 * grp, B = a.B, hkv = a.hkv;
   uint64_t* bars = (uint64_t*)smem_raw;
   float* sMax = (float*)(bars + 32);  // [2 tiles][4 quarters][64] tile maxima (log2)
-  int* s_pref = (int*)(sMax + 768);   // [B + 1] prefix sums of per-sequence tile counts
+  float* sL = sMax + 512;             // [4][64] running sums at the end of a piece
+  int* s_pref = (int*)(sL + 256);     // [B + 1] prefix sums of per-sequence tile counts
 
   // ---- schedule: this CTA's range [x0, x1) of the global tile list ----
   if (threadIdx.x < 32) {  // warp 0: inclusive scan of the tile counts, 32 at a time
@@ -199,6 +200,7 @@ __global__ void __launch_bounds__(320, 1)
   }
   uint8_t* sKV = sm;
   uint8_t* sPsep = sKV + NST * L::kStage;
+  float* xo = (float*)(sPsep + L::kP);  // [64][HALF + 4]
   auto stage = [&](int t) -> uint8_t* { return sKV + (t % NST) * L::kStage; };
   auto p_buf = [&](int t) -> uint8_t* {
     return L::kPinK ? stage(t) : sPsep + (t & 1) * L::kPTile;
@@ -545,20 +547,30 @@ __global__ void __launch_bounds__(320, 1)
           for (int j = 0; j < 16; ++j) O[cc * 16 + j] = v[j];
         }
       }
-      // the partial of (CTA, segment): this thread's O rows (P_hi V or P_lo V, one
-      // head-dim half) and its key quarter's sum; the merge adds the halves and quarters
-      const long slot = (long)blockIdx.x + (long)b * hkv + g;
-      if (ok && r < QN) {
-        float* po = a.part_o + (lrow >= 64 ? a.po_lo : 0) + (slot * QN + r) * HD + hf * HALF;
+      sL[kq * 64 + r] = l;
+      const long slot = (long)blockIdx.x + (long)b * hkv + g;  // partial of (CTA, segment)
+      // the P_lo V rows meet the P_hi V rows in shared memory, one head-dim half at a time
+      for (int pass = 0; pass < 2; ++pass) {
+        if (hf == pass && lrow >= 64 && ok) {
 #pragma unroll
-        for (int i = 0; i < HALF; i += 4)
-          *(float4*)(po + i) = make_float4(O[i], O[i + 1], O[i + 2], O[i + 3]);
-        float* pml = a.part_ml + (slot * QN + r) * 8;
-        pml[1 + kq] = l;
-        if (kq == 0) {
-          constexpr float kLn2 = 0.6931471805599453f;
-          pml[0] = m * kLn2;  // natural units for the merge
+          for (int i = 0; i < HALF; i += 4)
+            *(float4*)(xo + r * (HALF + 4) + i) = make_float4(O[i], O[i + 1], O[i + 2], O[i + 3]);
         }
+        asm volatile("bar.sync 2, 256;" ::: "memory");
+        if (hf == pass && lrow < 64 && r < QN && ok) {
+          float* po = a.part_o + (slot * QN + r) * HD + hf * HALF;
+          const float* lo_row = xo + r * (HALF + 4);
+#pragma unroll
+          for (int i = 0; i < HALF; i += 4)
+            *(float4*)(po + i) = make_float4(O[i] + lo_row[i], O[i + 1] + lo_row[i + 1],
+                                             O[i + 2] + lo_row[i + 2], O[i + 3] + lo_row[i + 3]);
+          if (hf == 0) {
+            constexpr float kLn2 = 0.6931471805599453f;
+            a.part_ml[(slot * QN + r) * 2] = m * kLn2;  // natural units for the merge
+            a.part_ml[(slot * QN + r) * 2 + 1] = sL[r] + sL[64 + r] + sL[128 + r] + sL[192 + r];
+          }
+        }
+        asm volatile("bar.sync 2, 256;" ::: "memory");
       }
       tc_fence_before();
       mbar_arrive(smem_u32(o_drained));
@@ -622,17 +634,12 @@ __global__ void __launch_bounds__(256) k_attn_merge_p(AttnArgs a) {
       mi[u] = -INFINITY;
       li[u] = 0.f;
       if (vi[u]) {
-        const float4* ml = reinterpret_cast<const float4*>(a.part_ml + ((i + seg) * QN + qi) * 8);
-        const float4 m0 = ml[0], m1 = ml[1];  // max, quarter sums 0..2 | quarter sum 3
-        mi[u] = m0.x;
-        li[u] = (m0.y + m0.z) + (m0.w + m1.x);
+        const float* ml = a.part_ml + ((i + seg) * QN + qi) * 2;
+        mi[u] = ml[0];
+        li[u] = ml[1];
         const float* pc = a.part_o + ((i + seg) * QN + qi) * a.hd + lane * DPL;
 #pragma unroll
-        for (int j = 0; j < DPL / 2; ++j) {
-          const float2 hi = *reinterpret_cast<const float2*>(pc + 2 * j);
-          const float2 lo = *reinterpret_cast<const float2*>(pc + a.po_lo + 2 * j);
-          oi[u][j] = make_float2(hi.x + lo.x, hi.y + lo.y);
-        }
+        for (int j = 0; j < DPL / 2; ++j) oi[u][j] = *reinterpret_cast<const float2*>(pc + 2 * j);
       }
     }
 #pragma unroll

@@ -75,7 +75,6 @@ struct dmtp_ctx {
   float* q;
   void* qs;  // bf16 [2][M][hq][hd]: split queries for the tensor-core attention
   float *part_o, *part_ml;
-  long po_lo;
   void* att;
   float* gu;
   void* hmid;
@@ -261,11 +260,8 @@ size_t layout(dmtp_ctx* c, char* base) {
   // slot for the persistent one
   const size_t slots = std::max((size_t)B * c->hkv * c->attn_nchunk,
                                 (size_t)c->attn_grid + (size_t)B * c->hkv);
-  // the tensor-core path keeps the P_hi V and P_lo V halves of each partial apart and
-  // four key-quarter sums per row (the merge adds them)
-  c->part_o = b.take<float>(slots * QN * c->hd * 4 * 2);
-  c->part_ml = b.take<float>(slots * QN * 8 * 4);
-  c->po_lo = (long)(slots * QN * c->hd);
+  c->part_o = b.take<float>(slots * QN * c->hd * 4);
+  c->part_ml = b.take<float>(slots * QN * 2 * 4);
   c->att = b.take<char>(r8 * std::max(c->qd, c->gH * c->gdv) * es);
   c->gu = b.take<float>(M * 2 * c->F * 4);
   c->hmid = b.take<char>(r8 * c->F * es);
@@ -499,7 +495,6 @@ void attn_layer(dmtp_ctx* c, const LayerPlans& p, const dmtp_layer_weights& w, f
   aa.q = c->q;
   aa.part_o = c->part_o;
   aa.part_ml = c->part_ml;
-  aa.po_lo = c->po_lo;
   aa.out = c->att;
   aa.out_lo = lo_of(c, c->mt8, c->qd);
   aa.base = a.base;

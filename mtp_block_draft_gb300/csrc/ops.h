@@ -114,11 +114,8 @@ struct AttnArgs {
   const void* Kc;      // [B][hkv][max_ctx][hd] dt
   const void* Vc;      // [B][hkv][max_ctx/64][hd][64] dt (transposed, blocked by 64 keys)
   const float* q;      // [B*8][hq][hd] fp32
-  float* part_o;       // [B][hkv][nchunk][QN][hd]; tensor-core path: [slot][QN][hd] for
-                       // the P_hi V rows, then the P_lo V rows at part_o + po_lo
-  float* part_ml;      // [B][hkv][nchunk][QN][2]; tensor-core path: [slot][QN][8] = the
-                       // reference max, then the four key quarters' sums
-  long po_lo;          // tensor-core path: offset (floats) of the P_lo V partials
+  float* part_o;       // [B][hkv][nchunk][QN][hd]
+  float* part_ml;      // [B][hkv][nchunk][QN][2]
   void* out;           // [B*8][hq*hd] dt
   long out_lo;         // element offset of the remainder half (0: none)
   const int* base;     // [B] position of row 0
