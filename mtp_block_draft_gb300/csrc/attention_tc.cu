@@ -1,7 +1,7 @@
 // Decode attention on the 5th-generation tensor cores (sm_103a), persistent and
 // evenly split over the SMs.
 //
-// Work: for every (sequence, kv head) segment, the 64-key tiles its 8 rows can see.
+// Work: for every (sequence, kv head) segment, the 128-key tiles its 8 rows can see.
 // All segments' tiles are laid end to end and the grid (one CTA per SM) takes equal
 // contiguous ranges of that list, so every CTA streams the same number of tiles
 // whatever the context lengths; a CTA's range covers pieces of one or more segments.

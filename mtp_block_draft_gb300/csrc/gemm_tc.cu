@@ -5,15 +5,19 @@
 // The round multiplies few token rows (M = 8 .. 256) by large weight matrices, so the
 // kernel is "swap-AB": 128 weight rows form the MMA's M side (TMEM lanes) and all M
 // token rows (padded to MT, a multiple of 16, <= 256) form its N side (TMEM columns).
-// Each weight byte is loaded by exactly one CTA. CTAs split the weight rows in tiles
-// of 128 and, where that leaves SMs idle, the K range (split-K); partial sums are
-// reduced with fp32 atomic adds into the output (which may be the residual stream,
-// so the residual add is fused).
+// CTAs split the weight rows in tiles of 128 (or 256), the token rows in 1..4 parts
+// (each part re-reads its weight tile, the second read from L2) and, where that leaves
+// SMs idle, the K range (split-K). Each CTA stages its output tile in the idle stage ring
+// and adds it into the output with one TMA bulk reduction (element-wise atomic, so the
+// split-K parts and the residual add into the residual stream need no other pass);
+// outputs a tensor map cannot describe fall back to per-element fp32 atomics.
 //
 // Pipeline per CTA (128 threads):
 //   warp 0 lane 0: TMA producer, weights with L2 evict-first, tokens evict-last;
 //   warp 1 lane 0: MMA issuer, 4 x (M=128, N=MT, K=16) per 64-wide k block;
 //   warp 2: TMEM allocation; all 4 warps: epilogue (TMEM lane = weight row).
+// The gate/up GEMM pairs gate and up rows in one CTA and writes silu(g) u as the next
+// GEMM's bf16 pair with one TMA store.
 // Stages are 64-element (128 B) k slices with 128-byte swizzle.
 //
 // Split activations: the token operand may come as two bf16 halves, X = X_hi + X_lo

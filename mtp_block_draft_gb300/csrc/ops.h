@@ -218,6 +218,8 @@ void op_gemm_tc_swiglu(const TcPlan& p, void* h, long h_lo, unsigned* err, cudaS
 // tc_plan with the tile shape given: wide (1, 2), msplit (1..4) and splits (<= 0: chosen).
 int tc_plan_shape(TcPlan* p, const void* W, int N, int K, const void* X, int M, int nsm,
                   bool split, int wide, int msplit, int splits);
+// out[m*ldo + n] += (X W^T)[m][n] for the plan's M x N (out fp32, zeroed or holding the
+// residual; K parts and CTAs add element-wise atomically).
 void op_gemm_tc_acc(const TcPlan& p, float* out, int ldo, unsigned* err, cudaStream_t st);
 int tc_init_attributes();
 
