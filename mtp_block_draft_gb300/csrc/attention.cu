@@ -54,8 +54,9 @@ __global__ void __launch_bounds__(256) k_attn_partial(AttnArgs a) {
     acc[i] = 0.f;
   }
   float m = -INFINITY, l = 0.f;
-  const T* Kb = (const T*)a.Kc + ((long)b * a.hkv + g) * a.max_ctx * hd;
-  const T* Vb = (const T*)a.Vc + ((long)b * a.hkv + g) * hd * a.max_ctx;  // [max_ctx/64][hd][64]
+  const int cb = a.cseq ? a.cseq[b] : b;  // cache sequence of the row group
+  const T* Kb = (const T*)a.Kc + ((long)cb * a.hkv + g) * a.max_ctx * hd;
+  const T* Vb = (const T*)a.Vc + ((long)cb * a.hkv + g) * hd * a.max_ctx;  // [max_ctx/64][hd][64]
 
   for (int kt = k_begin; kt < k_end; kt += kTK) {
     const int nk = min(kTK, k_end - kt);

@@ -255,8 +255,9 @@ __global__ void __launch_bounds__(320, 1)
       for (long x = x0; x < x1 && ok;) {
         int b, g, kt0, nt, base;
         piece(x, b, g, kt0, nt, base);
-        const long krow0 = ((long)b * hkv + g) * a.max_ctx;
-        const long vblk0 = ((long)b * hkv + g) * (a.max_ctx / 64);  // 64-key V^T blocks
+        const int cb = a.cseq ? a.cseq[b] : b;  // cache sequence of the row group
+        const long krow0 = ((long)cb * hkv + g) * a.max_ctx;
+        const long vblk0 = ((long)cb * hkv + g) * (a.max_ctx / 64);  // 64-key V^T blocks
         for (int t = 0; t < nt; ++t, ++gt) {
           const int s = gt % NST;
           if (!mbar_wait(smem_u32(&kv_empty[s]), ((gt / NST) & 1) ^ 1, err)) {

@@ -98,6 +98,7 @@ struct dmtp_ctx {
   bool fp8;
   float* hlast;
   int* prompts;
+  int2* psched;  // prefill schedule: (sequence, chunk) of each row group of each step
   int* plen;
   int* forced;
   RoundState rs;
@@ -301,6 +302,7 @@ size_t layout(dmtp_ctx* c, char* base) {
   s.mtp_base = b.take<int>(B * 4);
   s.mtp_cnt = b.take<int>(B * 4);
   s.rows_valid = b.take<int>(B * 4);
+  s.cseq = b.take<int>(B * 4);
   s.snap_slot = b.take<int>(B * 4);
   s.mtp_len = b.take<int>(B * 4);
   s.hist = b.take<unsigned long long>(8 * 8);
@@ -316,7 +318,10 @@ size_t layout(dmtp_ctx* c, char* base) {
 }
 
 // prompts are staged after the fixed layout (size depends on the prompt lengths)
-size_t prompt_bytes(int B, int pmax) { return ((size_t)B * pmax * 4 + 255) & ~(size_t)255; }
+// the prompts [B][max_ctx] and the prefill schedule (at most B (max_ctx/8 + 2) chunks)
+size_t prompt_bytes(int B, int pmax) {
+  return (((size_t)B * pmax * 4 + 255) & ~(size_t)255) + (size_t)B * (pmax / 8 + 2) * 8;
+}
 
 // split: X holds [hi; lo] bf16 halves (all GEMMs but the LM head, whose single bf16
 // operand keeps the logit error near 1e-3 at half the tensor-core work)
@@ -487,7 +492,7 @@ void attn_layer(dmtp_ctx* c, const LayerPlans& p, const dmtp_layer_weights& w, f
   const int M = c->M;
   norm(c, xr, w.attn_norm, c->xn, nullptr, tap_in, M, RowMap(), true, c->qkv, c->qkvd);
   gemm_acc(c, p.qkv, c->qkv, c->qkvd);
-  launch(c, P_OTHER, 0, 0, [&] { op_rope_kv(c->dt, c->qkv, c->qkvd, 0, c->qd, c->qd + c->kvd, c->q, c->attn_tc ? c->qs : nullptr, (long)M * c->qd, a.Kc, a.Vc, a.base, c->rope,
+  launch(c, P_OTHER, 0, 0, [&] { op_rope_kv(c->dt, c->qkv, c->qkvd, 0, c->qd, c->qd + c->kvd, c->q, c->attn_tc ? c->qs : nullptr, (long)M * c->qd, a.Kc, a.Vc, a.base, c->rs.cseq, c->rope,
              M, c->hq, c->hkv, c->hd, c->maxc, c->err, c->st); });
   AttnArgs aa;
   aa.Kc = a.Kc;
@@ -498,6 +503,7 @@ void attn_layer(dmtp_ctx* c, const LayerPlans& p, const dmtp_layer_weights& w, f
   aa.out = c->att;
   aa.out_lo = lo_of(c, c->mt8, c->qd);
   aa.base = a.base;
+  aa.cseq = c->rs.cseq;
   aa.causal = a.causal;
   aa.lo_fixed = a.lo_fixed;
   aa.window = a.window;
@@ -595,7 +601,7 @@ void drafter_ctx(dmtp_ctx* c) {
     if (j > 0) zero(c, c->qkv, (size_t)M * 2 * c->kvd * 4);
     gemm_acc(c, c->dkv[j], c->qkv, 2 * c->kvd);
     launch(c, P_OTHER, 0, 0, [&] { op_rope_kv(c->dt, c->qkv, 2 * c->kvd, -1, 0, c->kvd, nullptr, nullptr, 0, c->dK[j], c->dV[j],
-               c->rs.pos0, c->rope, M, c->hq, c->hkv, c->hd, c->maxc, c->err, c->st); });
+               c->rs.pos0, c->rs.cseq, c->rope, M, c->hq, c->hkv, c->hd, c->maxc, c->err, c->st); });
   }
 }
 
@@ -964,6 +970,8 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
   c->ws_bytes = need;
   const size_t fixed = layout(c, (char*)workspace);
   c->prompts = (int*)((char*)workspace + fixed);
+  c->psched = (int2*)((char*)c->prompts +
+                      ((((size_t)batch * c->maxc * 4) + 255) & ~(size_t)255));
   if (!w->emb || !w->head || !w->final_norm || !w->mtp_norm_h || !w->mtp_norm_e ||
       !w->mtp_final_norm || !w->fuse_norm_e || !w->fuse_norm_m || !w->dft_norm_c ||
       !w->dft_final_norm) {
@@ -1075,18 +1083,40 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
     cudaMemcpyAsync(c->plen, prompt_lens, (size_t)B * 4, cudaMemcpyHostToDevice, st);
     cudaStreamSynchronize(st);
   }
-  // ---- prefill: chunks of 8 positions per sequence ----
+  // ---- prefill: steps of B row groups, each 8 positions of one prompt ----
+  // Row group pb of a step takes chunk (sequence, index) of the schedule. Attention-only
+  // targets take every prompt's chunks in order, several chunks of one prompt in a step
+  // where they fit: all of the step's K/V rows are written before its attention reads
+  // them, so each chunk sees the chunks before it. Groups past the last chunk repeat the
+  // chunk just past the last prompt's end (their K/V rows land in its unused tail). A
+  // Gated DeltaNet state advances one chunk per step, so hybrid targets take chunk t of
+  // every prompt in step t.
+  std::vector<int2> sched;
+  if (c->n_gdn == 0) {
+    for (int b = 0; b < B; ++b)
+      for (int ch = 0; ch < (prompt_lens[b] + 7) / 8; ++ch) sched.push_back(make_int2(b, ch));
+    const int2 pad = make_int2(B - 1, (prompt_lens[B - 1] + 7) / 8);
+    while (sched.size() % B) sched.push_back(pad);
+  } else {
+    for (int ch = 0; ch < (pmax + 7) / 8; ++ch)
+      for (int b = 0; b < B; ++b) sched.push_back(make_int2(b, ch));
+  }
+  const int nsteps = (int)(sched.size() / B);
   cudaEvent_t pe0 = nullptr, pe1 = nullptr;
   if (cudaEventCreate(&pe0) == cudaSuccess && cudaEventCreate(&pe1) == cudaSuccess)
     cudaEventRecord(pe0, st);
-  const int nch = (pmax + 7) / 8;
-  for (int ch = 0; ch < nch; ++ch) {
-    op_prefill_chunk(s, c->prompts, c->plen, c->maxc, ch, st);
+  if (cudaMemcpyAsync(c->psched, sched.data(), sched.size() * sizeof(int2),
+                      cudaMemcpyHostToDevice, st) != cudaSuccess) {
+    delete c;
+    return DMTP_ECUDA;
+  }
+  for (int t = 0; t < nsteps; ++t) {
+    op_prefill_chunk(s, c->prompts, c->plen, c->maxc, c->psched + (size_t)t * B, st);
     target_forward(c, false);
-    op_prefill_save_last(c->hT32, c->plen, ch, c->hlast, B, c->d, st);
+    op_prefill_save_last(c->hT32, c->plen, c->psched + (size_t)t * B, c->hlast, B, c->d, st);
     drafter_ctx(c);
     mtp_advance(c);
-    if ((ch & 63) == 63 && cudaStreamSynchronize(st) != cudaSuccess) {
+    if ((t & 63) == 63 && cudaStreamSynchronize(st) != cudaSuccess) {
       delete c;
       return DMTP_ECUDA;
     }

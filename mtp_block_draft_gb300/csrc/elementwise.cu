@@ -401,9 +401,11 @@ template <typename T>
 __global__ void k_rope_kv(const float* __restrict__ src, int ld, int q_off, int k_off, int v_off,
                           float* __restrict__ q_out, bf16* __restrict__ q_split, long q_lo,
                           T* __restrict__ Kc, T* __restrict__ Vc,
-                          const int* __restrict__ base, const float2* __restrict__ tab, int hq,
-                          int hkv, int hd, int max_ctx, unsigned* err) {
+                          const int* __restrict__ base, const int* __restrict__ cseq,
+                          const float2* __restrict__ tab, int hq, int hkv, int hd, int max_ctx,
+                          unsigned* err) {
   const int m = blockIdx.x, b = m >> 3, s = m & 7;
+  const int cb = cseq ? cseq[b] : b;  // cache sequence of the row group
   const int pos = base[b] + s;
   const int half = hd / 2;
   const float* row = src + (long)m * ld;
@@ -431,11 +433,11 @@ __global__ void k_rope_kv(const float* __restrict__ src, int ld, int q_off, int 
     const int h = idx / half, i = idx % half;
     const float x1 = row[k_off + h * hd + i], x2 = row[k_off + h * hd + half + i];
     const float2 cs = tr[i];
-    T* kc = Kc + (((long)b * hkv + h) * max_ctx + pos) * hd;
+    T* kc = Kc + (((long)cb * hkv + h) * max_ctx + pos) * hd;
     kc[i] = from_f32<T>(x1 * cs.x - x2 * cs.y);
     kc[half + i] = from_f32<T>(x2 * cs.x + x1 * cs.y);
     // transposed and blocked by 64 keys: [max_ctx/64][hd][64]
-    T* vc = Vc + (((long)b * hkv + h) * (max_ctx / 64) + pos / 64) * hd * 64 + (pos % 64);
+    T* vc = Vc + (((long)cb * hkv + h) * (max_ctx / 64) + pos / 64) * hd * 64 + (pos % 64);
     vc[(long)i * 64] = from_f32<T>(row[v_off + h * hd + i]);
     vc[(long)(half + i) * 64] = from_f32<T>(row[v_off + h * hd + half + i]);
   }
@@ -451,8 +453,8 @@ __global__ void __launch_bounds__(256)
     k_rope_kv4(const float* __restrict__ src, int ld, int q_off, int k_off, int v_off,
                float* __restrict__ q_out, bf16* __restrict__ q_split, long q_lo,
                T* __restrict__ Kc, T* __restrict__ Vc, const int* __restrict__ base,
-               const float2* __restrict__ tab, int rows, int hq, int hkv, int hd, int max_ctx,
-               unsigned* err) {
+               const int* __restrict__ cseq, const float2* __restrict__ tab, int rows, int hq,
+               int hkv, int hd, int max_ctx, unsigned* err) {
   const int half = hd / 2, nquad = half / 4;
   if ((int)blockIdx.x < rows) {
     const int m = blockIdx.x, b = m >> 3, s = m & 7;
@@ -485,28 +487,29 @@ __global__ void __launch_bounds__(256)
           store_act4(q_out + qi + half + i, 0, r2);
         }
       } else {
-        T* kc = Kc + (((long)b * hkv + h) * max_ctx + pos) * hd;
+        T* kc = Kc + (((long)(cseq ? cseq[b] : b) * hkv + h) * max_ctx + pos) * hd;
         store_act4(kc + i, 0, r1);
         store_act4(kc + half + i, 0, r2);
       }
     }
   } else {
     const int b = (blockIdx.x - rows) / hkv, h = (blockIdx.x - rows) % hkv;
-    const int p0 = base[b];
+    const int p0 = base[b], cb = cseq ? cseq[b] : b;
     for (int idx = threadIdx.x; idx < hd * 8; idx += blockDim.x) {
       const int s = idx & 7, i = idx >> 3;
       const int pos = p0 + s;
       if (pos < 0 || pos >= max_ctx) continue;  // reported by the row CTAs
       const float v = src[(long)(b * 8 + s) * ld + v_off + h * hd + i];
-      Vc[(((long)b * hkv + h) * (max_ctx / 64) + pos / 64) * hd * 64 + (long)i * 64 + pos % 64] =
+      Vc[(((long)cb * hkv + h) * (max_ctx / 64) + pos / 64) * hd * 64 + (long)i * 64 + pos % 64] =
           from_f32<T>(v);
     }
   }
 }
 
 void op_rope_kv(int dt, const float* src, int ld, int q_off, int k_off, int v_off, float* q_out,
-                void* q_split, long q_lo, void* Kc, void* Vc, const int* base, const float2* tab,
-                int rows, int hq, int hkv, int hd, int max_ctx, unsigned* err, cudaStream_t st) {
+                void* q_split, long q_lo, void* Kc, void* Vc, const int* base, const int* cseq,
+                const float2* tab, int rows, int hq, int hkv, int hd, int max_ctx, unsigned* err,
+                cudaStream_t st) {
   const unsigned ek = dt ? 8 : 16;
   const bool vec = rows % 8 == 0 && hd % 8 == 0 && ld % 4 == 0 && aligned_to(src, 16) &&
                    aligned_to(tab, 16) && k_off % 4 == 0 && aligned_to(Kc, ek) &&
@@ -517,20 +520,20 @@ void op_rope_kv(int dt, const float* src, int ld, int q_off, int k_off, int v_of
     if (dt)
       k_rope_kv4<bf16><<<rows + rows / 8 * hkv, 256, 0, st>>>(
           src, ld, q_off, k_off, v_off, q_out, (bf16*)q_split, q_lo, (bf16*)Kc, (bf16*)Vc, base,
-          tab, rows, hq, hkv, hd, max_ctx, err);
+          cseq, tab, rows, hq, hkv, hd, max_ctx, err);
     else
       k_rope_kv4<float><<<rows + rows / 8 * hkv, 256, 0, st>>>(
-          src, ld, q_off, k_off, v_off, q_out, nullptr, 0, (float*)Kc, (float*)Vc, base, tab,
-          rows, hq, hkv, hd, max_ctx, err);
+          src, ld, q_off, k_off, v_off, q_out, nullptr, 0, (float*)Kc, (float*)Vc, base, cseq,
+          tab, rows, hq, hkv, hd, max_ctx, err);
     return;
   }
   if (dt)
     k_rope_kv<bf16><<<rows, 256, 0, st>>>(src, ld, q_off, k_off, v_off, q_out, (bf16*)q_split,
-                                          q_lo, (bf16*)Kc, (bf16*)Vc, base, tab, hq, hkv, hd,
-                                          max_ctx, err);
+                                          q_lo, (bf16*)Kc, (bf16*)Vc, base, cseq, tab, hq, hkv,
+                                          hd, max_ctx, err);
   else
     k_rope_kv<float><<<rows, 256, 0, st>>>(src, ld, q_off, k_off, v_off, q_out, nullptr, 0,
-                                           (float*)Kc, (float*)Vc, base, tab, hq, hkv, hd,
+                                           (float*)Kc, (float*)Vc, base, cseq, tab, hq, hkv, hd,
                                            max_ctx, err);
 }
 
@@ -663,40 +666,47 @@ void op_gather_hmtp(const float* x, const int* cnt, float* h, int B, int d, cuda
   k_gather_hmtp<<<B, 256, 0, st>>>(x, cnt, h, d);
 }
 
+// Prefill step: row group pb covers 8 positions of one prompt, chunk sched[pb] =
+// (sequence, chunk index), tokens x_p and MTP tokens x_{p+1} of positions p = 8 chunk + r.
 __global__ void k_prefill_chunk(RoundState s, const int* prompts, const int* plen, int pmax,
-                                int c) {
+                                const int2* sched) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= s.B * 8) return;
-  const int b = i >> 3, r = i & 7;
+  const int pb = i >> 3, r = i & 7;
+  const int2 e = sched[pb];
+  const int b = e.x, c = e.y;
   const int P = plen[b];
   const int p = 8 * c + r;
   s.tok[i] = (p < P) ? prompts[(long)b * pmax + p] : 0;
   s.mtp_tok[i] = (p + 1 < P) ? prompts[(long)b * pmax + p + 1] : 0;
   if (r == 0) {
-    s.pos0[b] = 8 * c;
-    s.mtp_base[b] = 8 * c + 1;
-    s.rows_valid[b] = max(0, min(8, P - 8 * c));
-    s.mtp_cnt[b] = max(0, min(8, P - 1 - 8 * c));
+    s.pos0[pb] = 8 * c;
+    s.mtp_base[pb] = 8 * c + 1;
+    s.rows_valid[pb] = max(0, min(8, P - 8 * c));
+    s.mtp_cnt[pb] = max(0, min(8, P - 1 - 8 * c));
+    s.cseq[pb] = b;
   }
 }
 
-void op_prefill_chunk(const RoundState& s, const int* prompts, const int* plen, int pmax, int c,
-                      cudaStream_t st) {
-  k_prefill_chunk<<<cdiv(s.B * 8, 256), 256, 0, st>>>(s, prompts, plen, pmax, c);
+void op_prefill_chunk(const RoundState& s, const int* prompts, const int* plen, int pmax,
+                      const int2* sched, cudaStream_t st) {
+  k_prefill_chunk<<<cdiv(s.B * 8, 256), 256, 0, st>>>(s, prompts, plen, pmax, sched);
 }
 
-__global__ void k_prefill_save_last(const float* hT, const int* plen, int c, float* hlast,
-                                    int d) {
-  const int b = blockIdx.x;
-  const int r = plen[b] - 1 - 8 * c;
+// The final hidden of each prompt's last position, from the row group whose chunk holds it.
+__global__ void k_prefill_save_last(const float* hT, const int* plen, const int2* sched,
+                                    float* hlast, int d) {
+  const int pb = blockIdx.x;
+  const int2 e = sched[pb];
+  const int r = plen[e.x] - 1 - 8 * e.y;
   if (r < 0 || r >= 8) return;
   for (int i = threadIdx.x; i < d; i += blockDim.x)
-    hlast[(long)b * d + i] = hT[((long)b * 8 + r) * d + i];
+    hlast[(long)e.x * d + i] = hT[((long)pb * 8 + r) * d + i];
 }
 
-void op_prefill_save_last(const float* hT, const int* plen, int c, float* hlast, int B, int d,
-                          cudaStream_t st) {
-  k_prefill_save_last<<<B, 256, 0, st>>>(hT, plen, c, hlast, d);
+void op_prefill_save_last(const float* hT, const int* plen, const int2* sched, float* hlast,
+                          int B, int d, cudaStream_t st) {
+  k_prefill_save_last<<<B, 256, 0, st>>>(hT, plen, sched, hlast, d);
 }
 
 // After the prompt: A = argmax of the last row (already in s.A via keys_to_ids);
@@ -709,6 +719,7 @@ __global__ void k_prefill_final(RoundState s, const int* plen, const float* hlas
   if (r == 0) {
     s.mtp_base[b] = plen[b];
     s.mtp_cnt[b] = 1;
+    s.cseq[b] = b;  // row group b is sequence b from here on
   }
   for (int j = 0; j < 8; ++j)
     for (int i = threadIdx.x; i < d; i += blockDim.x)

@@ -59,9 +59,9 @@ void op_swiglu(int dt, const float* gu, void* h, long h_lo, int rows, int F, cud
 // q_off < 0: no q. q_out fp32 [rows][hq][hd], or, when q_split != null (bf16 models),
 // q as a bf16 pair: hi at q_split, remainder at q_split + q_lo (elements).
 void op_rope_kv(int dt, const float* src, int ld, int q_off, int k_off, int v_off, float* q_out,
-                void* q_split, long q_lo, void* Kc, void* Vc, const int* base,
-                const float2* rope_tab, int rows, int hq, int hkv, int hd, int max_ctx,
-                unsigned* err, cudaStream_t st);
+                void* q_split, long q_lo, void* Kc, void* Vc, const int* base, const int* cseq,
+                const float2* tab, int rows, int hq, int hkv, int hd, int max_ctx, unsigned* err,
+                cudaStream_t st);
 // fp32 -> dt copy of rows (with row map)
 void op_cast_rows(int dt, const float* x, int ldx, void* y, int ldy, long y_lo, int rows, int d,
                   RowMap map, cudaStream_t st);
@@ -81,6 +81,8 @@ struct RoundState {
   int* mtp_base;      // [B] position of MTP row 0
   int* mtp_cnt;       // [B] valid MTP rows
   int* rows_valid;    // [B] valid target rows (GDN state advance)
+  int* cseq;          // [B] cache sequence of each row group (the group itself in rounds;
+                      // a prefill step may give several groups one sequence)
   int* snap_slot;     // [B]
   int* mtp_len;       // [B] next MTP position (= kv_len + 1)
   unsigned long long* hist;  // [8]
@@ -100,11 +102,12 @@ void op_verify_tokens(const RoundState& s, cudaStream_t st);
 void op_accept(const RoundState& s, cudaStream_t st);
 // h_mtp[b] = x[b*8 + cnt[b]-1]
 void op_gather_hmtp(const float* x, const int* cnt, float* h_mtp, int B, int d, cudaStream_t st);
-// prefill chunk c: pos0 = 8c, tok = prompt[8c+s], mtp_tok = prompt[8c+1+s], counts
-void op_prefill_chunk(const RoundState& s, const int* prompts, const int* plen, int pmax, int c,
-                      cudaStream_t st);
-void op_prefill_save_last(const float* hT, const int* plen, int c, float* hlast, int B, int d,
-                          cudaStream_t st);
+// Prefill step: row group pb takes chunk sched[pb] = (sequence, chunk of 8 positions);
+// sets tokens, positions, MTP rows and the cache-sequence map of every row group.
+void op_prefill_chunk(const RoundState& s, const int* prompts, const int* plen, int pmax,
+                      const int2* sched, cudaStream_t st);
+void op_prefill_save_last(const float* hT, const int* plen, const int2* sched, float* hlast,
+                          int B, int d, cudaStream_t st);
 void op_prefill_final(const RoundState& s, const int* plen, const float* hlast, float* hT, int d,
                       cudaStream_t st);
 void op_prefill_done(const RoundState& s, const int* plen, cudaStream_t st);
@@ -119,6 +122,7 @@ struct AttnArgs {
   void* out;           // [B*8][hq*hd] dt
   long out_lo;         // element offset of the remainder half (0: none)
   const int* base;     // [B] position of row 0
+  const int* cseq;     // [B] cache sequence of each row group (nullptr: the group itself)
   int causal;          // 1: row s sees keys <= base+s; 0: keys <= base+7
   int lo_fixed;        // lowest key index
   int window;          // > 0: lo = max(lo_fixed, base - window)
