@@ -314,13 +314,14 @@ size_t layout(dmtp_ctx* c, char* base) {
   c->err = b.take<unsigned>(256);
   s.err = c->err;
   c->plen = b.take<int>(B * 4);
-  return b.off;
+  return (b.off + 255) & ~(size_t)255;  // the staged prompts start 256-byte aligned
 }
 
-// prompts are staged after the fixed layout (size depends on the prompt lengths)
-// the prompts [B][max_ctx] and the prefill schedule (at most B (max_ctx/8 + 2) chunks)
-size_t prompt_bytes(int B, int pmax) {
-  return (((size_t)B * pmax * 4 + 255) & ~(size_t)255) + (size_t)B * (pmax / 8 + 2) * 8;
+// After the fixed layout: the prompts [B][max_ctx] int32, then (256-byte aligned, for its
+// 8-byte entries) the prefill schedule of at most B (max_ctx/8 + 2) (sequence, chunk) pairs.
+size_t sched_offset(int B, int max_ctx) { return ((size_t)B * max_ctx * 4 + 255) & ~(size_t)255; }
+size_t prompt_bytes(int B, int max_ctx) {
+  return sched_offset(B, max_ctx) + (size_t)B * (max_ctx / 8 + 2) * 8;
 }
 
 // split: X holds [hi; lo] bf16 halves (all GEMMs but the LM head, whose single bf16
@@ -970,8 +971,11 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
   c->ws_bytes = need;
   const size_t fixed = layout(c, (char*)workspace);
   c->prompts = (int*)((char*)workspace + fixed);
-  c->psched = (int2*)((char*)c->prompts +
-                      ((((size_t)batch * c->maxc * 4) + 255) & ~(size_t)255));
+  c->psched = (int2*)((char*)c->prompts + sched_offset(batch, c->maxc));
+  if (((uintptr_t)c->prompts | (uintptr_t)c->psched) & 255) {  // 8-byte schedule loads
+    delete c;
+    return DMTP_EINVAL;
+  }
   if (!w->emb || !w->head || !w->final_norm || !w->mtp_norm_h || !w->mtp_norm_e ||
       !w->mtp_final_norm || !w->fuse_norm_e || !w->fuse_norm_m || !w->dft_norm_c ||
       !w->dft_final_norm) {
