@@ -276,6 +276,51 @@ def fp8_draft_heads(cfg, weights, prompts, warmup, steps):
                     "(per-row power-of-two scales); the verify head stays bf16"}
 
 
+def hybrid_round(warmup, steps, hbm_gbs):
+    """The hybrid workload (B8, 48 layers of which 36 Gated DeltaNet, prompts of 4096):
+    natural rounds, graph replayed, timed like the headline; the Gated DeltaNet class
+    (state read, 7 snapshots, live write per layer) with its bandwidth against the HBM
+    peak. A side measurement, not the headline."""
+    import torch
+    from mtp_block_draft_gb300 import DmtpRound
+    from synth import CONFIGS, make_prompts, make_weights
+    cfg = CONFIGS["hybrid"]
+    weights = make_weights(cfg, torch.device("cuda", torch.cuda.current_device()))
+    prompts = make_prompts(cfg)
+    R = warmup + steps
+    g = DmtpRound(cfg, weights, prompts, max(len(p) for p in prompts) + 8 * R + 64)
+    for _ in range(warmup):
+        g.round()
+    _, _, h0 = g.read_state()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(g.stream)
+    for _ in range(steps):
+        g.round()
+    e1.record(g.stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    _, _, h1 = g.read_state()
+    prof = g.profile_round()
+    pf_ms, pf_tokens = g.prefill_stats()
+    g.close()
+    del weights
+    dh = (h1 - h0).astype(np.int64)
+    mean_len = float(np.sum((np.arange(8) + 1) * dh)) / max(1, int(dh.sum()))
+    rps = steps / (ms / 1e3)
+    gdn = prof["gdn"]
+    gdn_gbs = gdn["bytes"] / max(1e-12, gdn["ms"] / 1e3) / 1e9
+    return {"workload": f"hybrid: B{len(prompts)}, {cfg.n_layers} layers "
+                        f"({sum(cfg.layer_kinds)} Gated DeltaNet, H {cfg.gdn_heads}, "
+                        f"dk {cfg.gdn_dk}, dv {cfg.gdn_dv}), prompts {cfg.ctx_lo}",
+            "rounds_per_s": rps, "ms_per_step": ms / steps, "mean_accept_len": mean_len,
+            "tokens_per_s": len(prompts) * rps * mean_len, "steps": steps, "warmup": warmup,
+            "gdn": {"ms_per_round": gdn["ms"], "GB_per_round": gdn["bytes"] / 1e9,
+                    "launches": int(gdn["launches"]), "GB/s": gdn_gbs,
+                    "frac_of_hbm": gdn_gbs / hbm_gbs},
+            "prefill_tokens_per_s": pf_tokens / (pf_ms / 1e3) if pf_ms > 0 else None}
+
+
 def run_reference(args, cfg):
     import torch
     from synth import make_prompts, make_weights
@@ -333,6 +378,8 @@ def main():
                          "sampled verification at this temperature")
     ap.add_argument("--sample-seed", type=int, default=1)
     # smaller cases of the same kernels, for profiler captures (not bench workloads)
+    ap.add_argument("--hybrid-steps", type=int, default=100,
+                    help="side measurement of the hybrid workload (0: off)")
     ap.add_argument("--layers", type=int, default=None, help="override target layers")
     ap.add_argument("--ctx", type=int, nargs=2, default=None, help="override prompt range")
     args = ap.parse_args()
@@ -487,6 +534,11 @@ def main():
         line["forced_accept"] = forced_accept(cfg, weights, prompts, 4, args.forced_steps)
     if args.fp8_steps > 0 and world == 1 and cfg.dtype == "bf16" and cfg.d_model % 128 == 0:
         line["fp8_draft_heads"] = fp8_draft_heads(cfg, weights, prompts, 16, args.fp8_steps)
+    if args.hybrid_steps > 0 and world == 1 and args.config == "b32" and args.layers is None:
+        try:
+            line["hybrid"] = hybrid_round(5, args.hybrid_steps, hbm)
+        except Exception as e:  # a side field never takes the headline line down
+            line["hybrid"] = {"error": f"{type(e).__name__}: {e}"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_sample(cfg, weights, prompts, args.cpu_rounds)
     if rank == 0:
