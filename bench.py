@@ -321,6 +321,14 @@ def hybrid_round(warmup, steps, hbm_gbs):
             "prefill_tokens_per_s": pf_tokens / (pf_ms / 1e3) if pf_ms > 0 else None}
 
 
+def workload_name(cfg, B):
+    """The workload as both arms name it in config.workload."""
+    return (f"{cfg.name}: B{B} DMTP round, vocab {cfg.vocab}, d {cfg.d_model}, "
+            f"{cfg.n_layers}-layer GQA {cfg.n_heads}/{cfg.n_kv_heads}x{cfg.head_dim} "
+            f"target, ffn {cfg.ffn}, 1 MTP block, {cfg.draft_layers}-layer drafter, "
+            f"prompts U[{cfg.ctx_lo},{cfg.ctx_hi}]")
+
+
 def run_reference(args, cfg):
     import torch
     from synth import make_prompts, make_weights
@@ -349,8 +357,10 @@ def run_reference(args, cfg):
             "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": cfg.name, "global_batch": 1, "seq_len": len(prompts[b]),
-                       "parallelism": "none", "note": "one sequence of the B32 batch per step"},
+            "config": {"workload": workload_name(cfg, len(prompts)), "global_batch": 1,
+                       "seq_len": len(prompts[b]), "parallelism": "none",
+                       "note": f"one round of one sequence of the B{len(prompts)} batch per "
+                               "step (a bounded sample of the workload)"},
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": f"one round of sequence {b} (prompt {len(prompts[b])}) "
                                        "per step, float64 NumPy"},
@@ -497,10 +507,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_all / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded random weights N(0,0.02) and uniform prompt ids)",
-            "config": {"workload": f"{cfg.name}: B{B} DMTP round, vocab {cfg.vocab}, d {cfg.d_model}, "
-                                   f"{cfg.n_layers}-layer GQA {cfg.n_heads}/{cfg.n_kv_heads}x{cfg.head_dim} "
-                                   f"target, ffn {cfg.ffn}, 1 MTP block, {cfg.draft_layers}-layer drafter, "
-                                   f"prompts U[{cfg.ctx_lo},{cfg.ctx_hi}]",
+            "config": {"workload": workload_name(cfg, B),
                        "verify": ("greedy" if cfg.temperature == 0 else
                                   f"sampled, temperature {cfg.temperature:g}"),
                        "global_batch": B * world, "seq_len": int(np.mean([len(p) for p in prompts])),
