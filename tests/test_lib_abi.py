@@ -67,3 +67,69 @@ def test_init_rejects_null_arguments(lib):
     assert lib.dmtp_init(None, None, None, 0, None, None, 1, None, ctypes.byref(ctx)) == -1
     assert not ctx.value
     lib.dmtp_free(None)   # NULL is a no-op
+
+
+def _aligned_host_buffer(nbytes):
+    """A 256-byte aligned host address; dmtp_init's failure paths below return before
+    they touch the workspace or the device."""
+    raw = ctypes.create_string_buffer(nbytes + 256)
+    addr = (ctypes.addressof(raw) + 255) & ~255
+    return raw, addr
+
+
+def _init(lib, cfg, max_ctx, lens, ws_bytes, ws_addr=None):
+    c = make_config(cfg, max_ctx)
+    w = binding.dmtp_weights()
+    n = len(lens)
+    ids = (ctypes.c_int32 * max(1, sum(lens)))()
+    plen = (ctypes.c_int32 * n)(*lens)
+    raw = None
+    if ws_addr is None:
+        raw, ws_addr = _aligned_host_buffer(256)
+    ctx = ctypes.c_void_p()
+    r = lib.dmtp_init(ctypes.byref(c), ctypes.byref(w), ws_addr, ws_bytes, ids, plen, n,
+                      None, ctypes.byref(ctx))
+    del raw
+    return r, ctx
+
+
+def _ws_size(lib, cfg, max_ctx, batch):
+    c = make_config(cfg, max_ctx)
+    n = ctypes.c_size_t()
+    assert lib.dmtp_workspace_size(ctypes.byref(c), batch, ctypes.byref(n)) == 0
+    return n.value
+
+
+def test_init_workspace_too_small_is_enomem(lib):
+    """A workspace one byte short of dmtp_workspace_size: DMTP_ENOMEM, no context."""
+    cfg = CONFIGS["b32"].replace(batch=3)
+    need = _ws_size(lib, cfg, 1024, 3)
+    r, ctx = _init(lib, cfg, 1024, [100, 37, 900], need - 1)
+    assert r == -2 and not ctx.value
+
+
+def test_init_prompt_past_capacity_is_ecapacity(lib):
+    """A prompt that leaves no room for a round below max_ctx: DMTP_ECAPACITY before any
+    launch, whatever the workspace."""
+    cfg = CONFIGS["b32"].replace(batch=2)
+    need = _ws_size(lib, cfg, 1024, 2)
+    r, ctx = _init(lib, cfg, 1024, [100, 1024], need)
+    assert r == -3 and not ctx.value
+
+
+def test_init_rejects_empty_prompt_and_unaligned_workspace(lib):
+    cfg = CONFIGS["b32"].replace(batch=2)
+    need = _ws_size(lib, cfg, 1024, 2)
+    r, ctx = _init(lib, cfg, 1024, [100, 0], need)
+    assert r == -1 and not ctx.value
+    raw, addr = _aligned_host_buffer(256)
+    r, ctx = _init(lib, cfg, 1024, [100, 50], need, ws_addr=addr + 16)
+    assert r == -1 and not ctx.value
+
+
+def test_workspace_size_grows_with_batch_and_context(lib):
+    """Odd and even batches alike: more sequences or a longer context never need less."""
+    cfg = CONFIGS["b32"]
+    sizes = [_ws_size(lib, cfg.replace(batch=b), 2048, b) for b in (1, 2, 3, 5, 8)]
+    assert all(a < b for a, b in zip(sizes, sizes[1:]))
+    assert _ws_size(lib, cfg, 4096, 3) > _ws_size(lib, cfg, 2048, 3)
