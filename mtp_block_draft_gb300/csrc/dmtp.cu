@@ -1109,21 +1109,22 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
   cudaEvent_t pe0 = nullptr, pe1 = nullptr;
   if (cudaEventCreate(&pe0) == cudaSuccess && cudaEventCreate(&pe1) == cudaSuccess)
     cudaEventRecord(pe0, st);
-  if (cudaMemcpyAsync(c->psched, sched.data(), sched.size() * sizeof(int2),
-                      cudaMemcpyHostToDevice, st) != cudaSuccess) {
+  auto fail_prefill = [&]() {
+    if (pe0) cudaEventDestroy(pe0);
+    if (pe1) cudaEventDestroy(pe1);
     delete c;
     return DMTP_ECUDA;
-  }
+  };
+  if (cudaMemcpyAsync(c->psched, sched.data(), sched.size() * sizeof(int2),
+                      cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return fail_prefill();
   for (int t = 0; t < nsteps; ++t) {
     op_prefill_chunk(s, c->prompts, c->plen, c->maxc, c->psched + (size_t)t * B, st);
     target_forward(c, false);
     op_prefill_save_last(c->hT32, c->plen, c->psched + (size_t)t * B, c->hlast, B, c->d, st);
     drafter_ctx(c);
     mtp_advance(c);
-    if ((t & 63) == 63 && cudaStreamSynchronize(st) != cudaSuccess) {
-      delete c;
-      return DMTP_ECUDA;
-    }
+    if ((t & 63) == 63 && cudaStreamSynchronize(st) != cudaSuccess) return fail_prefill();
   }
   // A = the target's greedy token after the prompt; MTP consumes (h^T_{P-1}, A) at P
   op_cast_rows(c->dt, c->hlast, c->d, c->t1in, c->d, 0, B, c->d, RowMap(), st);
