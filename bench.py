@@ -192,6 +192,17 @@ PAGE_PER_VERIFY = {"Code": 3.795, "Math": 4.056, "MT-Bench": 3.250, "Agent": 4.7
                    "SWE": 3.173, "Long-horizon": 4.656}
 
 
+def acceptance(dh):
+    """Per-position acceptance from the histogram deltas of the timed rounds: entry n
+    counts sequence-rounds that accepted n drafts (accept length n + 1); p_len_ge[k - 1]
+    is the cumulative P(accept length >= k) for k = 1..8 (the DMTP blog's cumulative
+    acceptance curve)."""
+    dh = np.asarray(dh, dtype=np.int64)
+    tot = max(1, int(dh.sum()))
+    return {"hist_n_accepted": [int(x) for x in dh],
+            "p_len_ge": [float(dh[k - 1:].sum()) / tot for k in range(1, 9)]}
+
+
 def forced_accept(cfg, weights, prompts, warmup, steps):
     """Rounds with every draft accepted: the drafts are forced to the target's own greedy
     continuation, collected first on a separate context by rounds whose drafts are forced
@@ -239,7 +250,7 @@ def forced_accept(cfg, weights, prompts, warmup, steps):
     mean_len = float(np.sum((np.arange(8) + 1) * dh)) / max(1, int(dh.sum()))
     rps = steps / (ms / 1e3)
     return {"rounds_per_s": rps, "mean_accept_len": mean_len, "tokens_per_s": B * rps * mean_len,
-            "steps": steps, "warmup": warmup,
+            "steps": steps, "warmup": warmup, "acceptance": acceptance(dh),
             "drafts": "forced to the target's own greedy continuation (every draft accepted)"}
 
 
@@ -518,6 +529,7 @@ def main():
             "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": B * 8 * 4 + B * 4},
             "gpu_launches": g.launches_per_round() * args.steps,
+            "acceptance": acceptance(dh),
             "roofline": roof,
             "round_roofline": {"algorithmic_GB": alg_bytes / 1e9,
                                "t_roof_ms": alg_bytes / (hbm * 1e9) * 1e3,

@@ -1,6 +1,7 @@
-"""bench.py's reference arm (the oracle timed on the host cores) on CPU: one JSON line with
-the contract's keys, the same metric and workload naming as the GPU arm, and under a
-multi-rank launch only rank 0 prints. No GPU."""
+"""bench.py on CPU: the reference arm (the oracle timed on the host cores) prints one JSON
+line with the contract's keys, the same metric and workload naming as the GPU arm, and
+under a multi-rank launch only rank 0 prints; the acceptance curve is computed from the
+histogram as the DMTP blog defines it. No GPU."""
 import json
 import os
 import subprocess
@@ -45,3 +46,15 @@ def test_reference_line_keys():
 
 def test_reference_other_ranks_print_nothing():
     assert _run({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}) == []
+
+
+def test_acceptance_curve_from_histogram():
+    """P(accept length >= k) from per-n counts: a hand-worked histogram."""
+    sys.path.insert(0, ROOT)
+    import bench
+    # 10 sequence-rounds: 4 accepted no draft (length 1), 3 accepted 2 (length 3),
+    # 2 accepted 6 (length 7), 1 accepted all 7 (length 8)
+    a = bench.acceptance([4, 0, 3, 0, 0, 0, 2, 1])
+    assert a["hist_n_accepted"] == [4, 0, 3, 0, 0, 0, 2, 1]
+    assert a["p_len_ge"] == [1.0, 0.6, 0.6, 0.3, 0.3, 0.3, 0.3, 0.1]
+    assert bench.acceptance([0] * 8)["p_len_ge"] == [0.0] * 8
