@@ -99,10 +99,11 @@ class DepthGate:
     def rho(self) -> float:
         if 1 not in self.T:
             return RHO0
-        xs = [n - 1 for n in self.T if n >= 2]
-        if not xs:
+        rows = sorted(n for n in self.T if n >= 2)       # increasing row count
+        if not rows:
             return RHO0
-        ys = [self.T[n] / self.T[1] - 1.0 for n in self.T if n >= 2]
+        xs = [float(n - 1) for n in rows]
+        ys = [self.T[n] / self.T[1] - 1.0 for n in rows]
         return float(sum(x * y for x, y in zip(xs, ys)) / sum(x * x for x in xs))
 
     def t_rel(self, n: int) -> float:
