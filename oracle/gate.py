@@ -102,9 +102,12 @@ class DepthGate:
         rows = sorted(n for n in self.T if n >= 2)       # increasing row count
         if not rows:
             return RHO0
-        xs = [float(n - 1) for n in rows]
-        ys = [self.T[n] / self.T[1] - 1.0 for n in rows]
-        return float(sum(x * y for x, y in zip(xs, ys)) / sum(x * x for x in xs))
+        sxy = sxx = 0.0                                  # plain left-to-right sums
+        for n in rows:
+            x, y = float(n - 1), self.T[n] / self.T[1] - 1.0
+            sxy += x * y
+            sxx += x * x
+        return sxy / sxx
 
     def t_rel(self, n: int) -> float:
         """T(n) / T(1): measured where both are, else 1 + (n - 1) rho."""
