@@ -23,10 +23,17 @@ DMTP_MAX_TAPS = 8
 ERRORS = {0: "DMTP_OK", -1: "DMTP_EINVAL", -2: "DMTP_ENOMEM", -3: "DMTP_ECAPACITY",
           -4: "DMTP_ECUDA", -5: "DMTP_EDEVICE", -6: "DMTP_ESTATE"}
 
-# every symbol include/dmtp.h declares
+# every symbol include/dmtp.h and include/dmtp_gate.h declare
 EXPORTS = ("dmtp_workspace_size", "dmtp_init", "dmtp_round", "dmtp_round_host",
            "dmtp_read_state", "dmtp_round_launches", "dmtp_round_profile", "dmtp_free",
-           "dmtp_strerror", "dmtp_t1_head_noalloc", "dmtp_prefill_stats")
+           "dmtp_strerror", "dmtp_t1_head_noalloc", "dmtp_prefill_stats",
+           "dmtp_gate_create", "dmtp_gate_forward", "dmtp_gate_draft_cost",
+           "dmtp_gate_result", "dmtp_gate_pick", "dmtp_gate_pick_p", "dmtp_gate_read",
+           "dmtp_gate_free")
+
+DMTP_GATE_MAX_DRAFTS = 32
+DMTP_GATE_MAX_ROWS = 64
+DMTP_GATE_BINS = 10
 
 PROFILE_CLASSES = ("gemm", "lm_head", "attention", "gdn", "other")
 
@@ -70,6 +77,14 @@ class dmtp_round_out(C.Structure):
     _fields_ = [(f, C.c_void_p) for f in _OUT_INT + _OUT_FLOAT]
 
 
+class dmtp_gate_stats(C.Structure):
+    _fields_ = [("max_drafts", C.c_int), ("a", C.c_double * DMTP_GATE_MAX_DRAFTS),
+                ("t", C.c_double * (DMTP_GATE_MAX_ROWS + 1)), ("d", C.c_double),
+                ("d_measured", C.c_int), ("rho", C.c_double), ("picks", C.c_longlong),
+                ("since_plain", C.c_longlong), ("bin_judged", C.c_longlong * DMTP_GATE_BINS),
+                ("bin_accepted", C.c_longlong * DMTP_GATE_BINS)]
+
+
 class dmtp_profile(C.Structure):
     _fields_ = [("ms", C.c_double * 8), ("bytes", C.c_double * 8), ("flops", C.c_double * 8),
                 ("launches", C.c_int * 8), ("round_ms", C.c_double)]
@@ -110,6 +125,18 @@ def load_library(path: str = LIB_PATH):
     lib.dmtp_t1_head_noalloc.restype = C.c_int
     lib.dmtp_strerror.argtypes = [C.c_int]
     lib.dmtp_strerror.restype = C.c_char_p
+    D = C.POINTER(C.c_double)
+    lib.dmtp_gate_create.argtypes = [C.c_int, D, C.POINTER(P)]
+    lib.dmtp_gate_forward.argtypes = [P, C.c_int, C.c_double]
+    lib.dmtp_gate_draft_cost.argtypes = [P, C.c_double]
+    lib.dmtp_gate_result.argtypes = [P, C.c_int, C.c_int, D]
+    lib.dmtp_gate_pick.argtypes = [P, C.c_int, C.POINTER(C.c_int), D]
+    lib.dmtp_gate_pick_p.argtypes = [P, C.c_int, D, C.POINTER(C.c_int), D]
+    lib.dmtp_gate_read.argtypes = [P, C.POINTER(dmtp_gate_stats)]
+    for f in ("create", "forward", "draft_cost", "result", "pick", "pick_p", "read"):
+        getattr(lib, "dmtp_gate_" + f).restype = C.c_int
+    lib.dmtp_gate_free.argtypes = [P]
+    lib.dmtp_gate_free.restype = None
     _lib = lib
     return lib
 
@@ -281,6 +308,66 @@ class DmtpRound:
         if getattr(self, "ctx", None):
             self.lib.dmtp_free(self.ctx)
             self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _doubles(xs):
+    if xs is None:
+        return None
+    xs = [float(x) for x in xs]
+    return (C.c_double * max(1, len(xs)))(*xs)
+
+
+class DmtpGate:
+    """The draft-depth gate of include/dmtp_gate.h (host-only; argument marshalling)."""
+
+    def __init__(self, max_drafts: int, priors=None):
+        self.lib = load_library()
+        self.g = C.c_void_p()
+        _check(self.lib.dmtp_gate_create(int(max_drafts), _doubles(priors), C.byref(self.g)),
+               "dmtp_gate_create")
+
+    def forward(self, rows: int, seconds: float):
+        _check(self.lib.dmtp_gate_forward(self.g, int(rows), float(seconds)), "dmtp_gate_forward")
+
+    def draft_cost(self, seconds: float):
+        _check(self.lib.dmtp_gate_draft_cost(self.g, float(seconds)), "dmtp_gate_draft_cost")
+
+    def result(self, judged: int, accepted: int, p=None):
+        _check(self.lib.dmtp_gate_result(self.g, int(judged), int(accepted), _doubles(p)),
+               "dmtp_gate_result")
+
+    def pick(self, proposed: int):
+        k, v = C.c_int(), C.c_double()
+        _check(self.lib.dmtp_gate_pick(self.g, int(proposed), C.byref(k), C.byref(v)),
+               "dmtp_gate_pick")
+        return k.value, v.value
+
+    def pick_p(self, p):
+        k, v = C.c_int(), C.c_double()
+        _check(self.lib.dmtp_gate_pick_p(self.g, len(p), _doubles(p), C.byref(k), C.byref(v)),
+               "dmtp_gate_pick_p")
+        return k.value, v.value
+
+    def read(self) -> dict:
+        st = dmtp_gate_stats()
+        _check(self.lib.dmtp_gate_read(self.g, C.byref(st)), "dmtp_gate_read")
+        K = st.max_drafts
+        return {"a": list(st.a[:K]), "t": {n: st.t[n] for n in range(1, DMTP_GATE_MAX_ROWS + 1)
+                                          if st.t[n] > 0},
+                "d": st.d if st.d_measured else None, "rho": st.rho, "picks": st.picks,
+                "since_plain": st.since_plain, "bin_judged": list(st.bin_judged),
+                "bin_accepted": list(st.bin_accepted)}
+
+    def close(self):
+        if self.g:
+            self.lib.dmtp_gate_free(self.g)
+            self.g = C.c_void_p()
 
     def __del__(self):
         try:

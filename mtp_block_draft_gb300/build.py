@@ -18,7 +18,10 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdmtp.so")
 
-SOURCES = ["dmtp.cu", "elementwise.cu", "attention.cu", "gemm_simt.cu", "gemm_tc.cu", "gdn.cu", "noalloc.cu", "attention_tc.cu", "head_tc.cu"]
+SOURCES = ["dmtp.cu", "elementwise.cu", "attention.cu", "gemm_simt.cu", "gemm_tc.cu", "gdn.cu", "noalloc.cu", "attention_tc.cu", "head_tc.cu", "gate.cpp"]
+# host-only units whose double arithmetic must round the same on every host: no fused
+# multiply-adds (aarch64 compilers contract them by default)
+EXTRA = {"gate.cpp": ["-Xcompiler", "-ffp-contract=off"]}
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include"), "-I", CSRC]
@@ -33,7 +36,7 @@ def _nvcc() -> str:
 
 def _compile(src: str, verbose: bool) -> str:
     obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-    cmd = [_nvcc(), *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+    cmd = [_nvcc(), *ARCH, *FLAGS, *EXTRA.get(src, []), "-c", os.path.join(CSRC, src), "-o", obj]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     r = subprocess.run(cmd, capture_output=True, text=True)
