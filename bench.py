@@ -159,9 +159,9 @@ def combine_ranks(ms, tokens, e2e_s, e2e_tokens, world: int, device):
     return float(t[0]), float(n[0]), float(t[1]), float(n[1])
 
 
-def oracle_sample(cfg, weights, prompts, rounds: int, budget_s: float = 30.0):
+def oracle_sample(cfg, weights, prompts, rounds: int, limit_s: float = 30.0):
     """Time the oracle on one sequence (the shortest prompt) of the batch: prefill
-    untimed, then up to `rounds` rounds or `budget_s` seconds timed."""
+    untimed, then up to `rounds` rounds or `limit_s` seconds timed."""
     from oracle import OracleModel
     b = int(np.argmin([len(p) for p in prompts]))
     t0 = time.perf_counter()
@@ -171,7 +171,7 @@ def oracle_sample(cfg, weights, prompts, rounds: int, budget_s: float = 30.0):
     st = om.prefill(prompts[b], b=b)
     setup = time.perf_counter() - t0
     tokens, el, done = 0, 0.0, 0
-    while done < rounds and el < budget_s:
+    while done < rounds and el < limit_s:
         t = time.perf_counter()
         rec = om.round(st, want_logits=False)
         el += time.perf_counter() - t
