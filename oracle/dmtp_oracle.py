@@ -497,7 +497,8 @@ class OracleModel:
         log["mismatch"].append((where, top, adopt, float(logits[top] - logits[adopt])))
         return top
 
-    def round(self, st: SeqState, forced=None, adopt=None, want_logits: bool = True):
+    def round(self, st: SeqState, forced=None, adopt=None, want_logits: bool = True,
+              depth=7):
         """One DMTP round on one sequence, in place on ``st``.
 
         Steps ([DMTP] §5 and §6.1):
@@ -518,7 +519,12 @@ class OracleModel:
         fusion and drafter see it; T2..T7 after a3). ``adopt``: dict with optional
         'T1', 'T' (7 ids) and 'g' (8 ids) from another implementation; at any argmax
         where that id is within ``gate`` of the maximum it is taken instead (near-tie
-        lock-step). Returns a record of every intermediate.
+        lock-step). ``depth``: how many drafts the verify carries (0..7; 7 is the DMTP
+        round), or a callable (drafts, confidences) -> depth called after a3 with each
+        draft head's probability of its own pick (gate.head_confidence): the verify is
+        then rows [A, T1..T_depth] and at most depth drafts are accepted (colibri doc: a
+        verify of k drafts is one forward of k + 1 rows). Returns a record of every
+        intermediate.
         """
         c, W = self.cfg, self.W
         adopt = adopt or {}
@@ -546,13 +552,22 @@ class OracleModel:
                                      log, f"T{s + 2}"))
         if forced is not None:
             drafts = [T1] + [int(t) for t in forced[1:7]]
+        if callable(depth):
+            from .gate import head_confidence
+            conf = [head_confidence(t1_logits)] + [head_confidence(dlog[s]) for s in range(6)]
+            rec["draft_confidence"] = conf
+            depth = depth(list(drafts), conf)
+        depth = int(depth)
+        if not 0 <= depth <= 7:
+            raise ValueError("depth in 0..7")
+        rec["depth"] = depth
         # a4: each row by the one-row routine on a working copy of the caches
         work = st.clone()
         rows = [A] + drafts
         hT_rows, tap_rows, vlog, g, vsc = [], [], [], [], []
         snaps = {}
         adg = adopt.get("g")
-        for s in range(8):
+        for s in range(depth + 1):
             hT, taps, logits, sn = self.target_rows(work, [rows[s]], a + s, collect_snaps=True)
             hT_rows.append(hT[0]); tap_rows.append(taps[0]); vlog.append(logits[0])
             for l, lst in sn.items():
@@ -565,7 +580,7 @@ class OracleModel:
             g.append(self._pick(sc, adg[s] if adg is not None else None, log, f"g{s}"))
         # a5
         n = 0
-        while n < 7 and drafts[n] == g[n]:
+        while n < depth and drafts[n] == g[n]:
             n += 1
         committed = drafts[:n] + [g[n]]
         keep = a + n + 1

@@ -53,6 +53,16 @@ RHO0 = 0.5
 N_BINS = 10
 
 
+def head_confidence(logits, window: float = 20.0) -> float:
+    """A draft head's probability of its own (argmax) token: the softmax over the scores
+    within `window` of the best (the per-step paragraph's estimate for MTP heads),
+    1 / sum over {v : l_v >= l_max - window} of exp(l_v - l_max)."""
+    l = np.asarray(logits, dtype=np.float64)
+    m = float(l.max())
+    near = l[l >= m - window]
+    return float(1.0 / np.sum(np.exp(near - m)))
+
+
 class DepthGate:
     def __init__(self, max_drafts: int, priors=None):
         if max_drafts < 1:
