@@ -135,3 +135,78 @@ def test_workspace_size_grows_with_batch_and_context(lib):
     sizes = [_ws_size(lib, cfg.replace(batch=b), 2048, b) for b in (1, 2, 3, 5, 8)]
     assert all(a < b for a, b in zip(sizes, sizes[1:]))
     assert _ws_size(lib, cfg, 4096, 3) > _ws_size(lib, cfg, 2048, 3)
+
+
+_C_GATE = r"""
+#include <stdio.h>
+#include "dmtp_gate.h"
+int main(void) {
+  dmtp_gate* g = NULL;
+  if (dmtp_gate_create(7, NULL, &g) != DMTP_OK) return 1;
+  const double p[7] = {0.93, 0.88, 0.4, 0.97, 0.12, 0.5, 0.99};
+  for (int r = 0; r < 40; ++r) {
+    int k = 0;
+    double v = 0.0;
+    if (dmtp_gate_forward(g, 1 + r % 8, 1.0 + 0.07 * (r % 8) + 0.001 * r) != DMTP_OK) return 2;
+    if (r % 5 == 4 && dmtp_gate_draft_cost(g, 0.01 * r) != DMTP_OK) return 3;
+    if (dmtp_gate_pick(g, 7, &k, &v) != DMTP_OK) return 4;
+    printf("pick %d %.17g\n", k, v);
+    if (dmtp_gate_pick_p(g, 7, p, &k, &v) != DMTP_OK) return 5;
+    printf("pick_p %d %.17g\n", k, v);
+    const int acc = r % 4, judged = acc + 1;
+    if (dmtp_gate_result(g, judged, acc, p) != DMTP_OK) return 6;
+  }
+  dmtp_gate_stats st;
+  if (dmtp_gate_read(g, &st) != DMTP_OK) return 7;
+  printf("rho %.17g\n", st.rho);
+  if (dmtp_gate_result(g, 3, 1, NULL) != DMTP_EINVAL) return 8;
+  dmtp_gate_free(g);
+  dmtp_gate_free(NULL);
+  return 0;
+}
+"""
+
+
+def test_headers_compile_as_c99_and_a_c_caller_runs_the_gate(lib, tmp_path):
+    """include/*.h compile as strict C99; a C program linked against libdmtp.so drives
+    the host-only gate and prints what the oracle computes for the same calls."""
+    import shutil
+    import subprocess
+    from oracle.gate import DepthGate
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    inc = os.path.join(ROOT, "include")
+    for h in sorted(os.listdir(inc)):
+        src = tmp_path / f"hdr_{h}.c"
+        src.write_text(f'#include "{h}"\nint main(void) {{ return 0; }}\n')
+        subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", inc,
+                        "-c", str(src), "-o", str(tmp_path / f"hdr_{h}.o")], check=True)
+    src = tmp_path / "gate_caller.c"
+    src.write_text(_C_GATE)
+    libdir = os.path.dirname(binding.LIB_PATH)
+    exe = tmp_path / "gate_caller"
+    subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", inc, str(src), "-o", str(exe),
+                    "-L", libdir, "-ldmtp", f"-Wl,-rpath,{libdir}"], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, out.returncode
+    got = out.stdout.split("\n")
+    g = DepthGate(7)
+    p = [0.93, 0.88, 0.4, 0.97, 0.12, 0.5, 0.99]
+    want = []
+    for r in range(40):
+        g.forward(1 + r % 8, 1.0 + 0.07 * (r % 8) + 0.001 * r)
+        if r % 5 == 4:
+            g.draft_cost(0.01 * r)
+        k, v = g.pick(7)
+        want.append(f"pick {k} {v!r}")
+        k, v = g.pick_p(p)
+        want.append(f"pick_p {k} {v!r}")
+        g.result(r % 4 + 1, r % 4, p)
+    want.append(f"rho {g.rho()!r}")
+    parsed = []
+    for line in got[:len(want)]:
+        name, *rest = line.split()
+        vals = [rest[0], repr(float(rest[1]))] if name != "rho" else [repr(float(rest[0]))]
+        parsed.append(" ".join([name] + vals))
+    assert parsed == want
