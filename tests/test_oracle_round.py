@@ -137,7 +137,9 @@ def test_w_zero_reduction(tiny, prompt):
         E = tiny.W["emb"]
         T1 = int(np.argmax(tiny.t1_head(pre.h_mtp)))
         X = np.stack([E[pre.A], E[T1]] + [E[TINY.mask_id]] * 6)
+        np.testing.assert_array_equal(rec["slots"], X)          # [E(A), E(T1), E(MASK) x 6]
         dl = tiny.drafter_forward(X, pre, pre.a)
+        np.testing.assert_array_equal(rec["draft_logits"], dl)
         assert rec["drafts"] == [T1] + [int(np.argmax(r)) for r in dl]
 
 
