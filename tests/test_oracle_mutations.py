@@ -97,6 +97,33 @@ def test_round_pins_catch_slips(monkeypatch):
     _fails(R.test_mtp_uses_embedding_of_pending_token, prompt)
 
 
+def test_drafter_pins_catch_slips(monkeypatch):
+    tiny, prompt = R._model(), R.make_prompts(R.TINY)[0]
+    att = O.attend_rows
+
+    def causal_block(q, K, V, hi, lo=0):                                         # mask in block
+        hi = np.asarray(hi)
+        if hi.size == 8 and np.all(hi == hi[0]):
+            hi = hi - 7 + np.arange(8)
+        return att(q, K, V, hi, lo)
+    monkeypatch.setattr(O, "attend_rows", causal_block)
+    _fails(R.test_drafter_block_is_bidirectional, tiny, prompt)
+    monkeypatch.undo()
+
+    real = O.OracleModel.drafter_forward
+    for shift in (1, -1):                                                        # window off by one
+        def shifted(self, X, st, a, with_head_in=False, _s=shift):
+            cfg = self.cfg
+            self.cfg = cfg.replace(draft_window=cfg.draft_window + _s)
+            try:
+                return real(self, X, st, a, with_head_in)
+            finally:
+                self.cfg = cfg
+        monkeypatch.setattr(O.OracleModel, "drafter_forward", shifted)
+        _fails(R.test_drafter_window)
+        monkeypatch.undo()
+
+
 def test_sampling_pin_catches_a_swapped_key(monkeypatch):
     ph = sampling_mod.philox4x32_10
     monkeypatch.setattr(S, "philox4x32_10", lambda ctr, key: ph(ctr, np.asarray(key)[::-1]))
