@@ -131,6 +131,27 @@ def test_sampling_pin_catches_a_swapped_key(monkeypatch):
            (0xA4093822, 0x299F31D0), (0xD16CFE09, 0x94FDCCEB, 0x5001E420, 0x24126EA1))
 
 
+def test_sampling_pin_catches_a_flipped_noise_sign(monkeypatch):
+    gum = sampling_mod.gumbel
+    flipped = lambda seed, b, pos, vocab: -gum(seed, b, pos, vocab)            # Gumbel-min
+    monkeypatch.setattr(sampling_mod, "gumbel", flipped)
+    monkeypatch.setattr(S, "gumbel", flipped)
+    _fails(S.test_gumbel_max_draws_from_softmax)
+
+
+def test_fp8_scale_and_metric_pins_catch_slips(monkeypatch):
+    ps = fp8_mod.pow2_scale
+    loose = lambda amax: 2.0 * ps(amax)                                           # one power off
+    monkeypatch.setattr(fp8_mod, "pow2_scale", loose)
+    monkeypatch.setattr(F, "pow2_scale", loose)
+    _fails(F.test_pow2_scales_tight_and_exact)
+    monkeypatch.undo()
+
+    mal = O.mean_accept_len
+    monkeypatch.setattr(O, "mean_accept_len", lambda h: mal(h) - 1.0)            # no bonus token
+    _fails(P.test_accept_metrics_hand_histograms)
+
+
 def test_fp8_pin_catches_ties_away_from_zero(monkeypatch):
     grid = fp8_mod.e4m3_grid()
     mids = (grid[1:] + grid[:-1]) / 2
