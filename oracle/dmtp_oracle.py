@@ -498,7 +498,7 @@ class OracleModel:
         return top
 
     def round(self, st: SeqState, forced=None, adopt=None, want_logits: bool = True,
-              depth=7):
+              depth=7, draft_list=None):
         """One DMTP round on one sequence, in place on ``st``.
 
         Steps ([DMTP] §5 and §6.1):
@@ -523,7 +523,10 @@ class OracleModel:
         round), or a callable (drafts, confidences) -> depth called after a3 with each
         draft head's probability of its own pick (gate.head_confidence): the verify is
         then rows [A, T1..T_depth] and at most depth drafts are accepted (colibri doc: a
-        verify of k drafts is one forward of k + 1 rows). Returns a record of every
+        verify of k drafts is one forward of k + 1 rows). ``draft_list``: None, or a
+        boolean mask [V] of the tokens the draft heads score (shortlist.VocabList.members,
+        colibri doc's frequent-token list): T1..T7 are then the argmax over the listed
+        tokens, while the verify still scores every token. Returns a record of every
         intermediate.
         """
         c, W = self.cfg, self.W
@@ -537,8 +540,11 @@ class OracleModel:
         # a1
         t1_logits = self.t1_head(h_mtp)
         rec["t1_head_in"] = rms_norm(h_mtp[None], W["mtp.final_norm"], self.eps)
+        listed = ((lambda l: l) if draft_list is None else
+                  (lambda l: np.where(draft_list, l, -np.inf)))
         ad = adopt.get("T")
-        T1 = self._pick(t1_logits, ad[0] if ad is not None else adopt.get("T1"), log, "T1")
+        T1 = self._pick(listed(t1_logits), ad[0] if ad is not None else adopt.get("T1"), log,
+                        "T1")
         if forced is not None:
             T1 = int(forced[0])
         # a2
@@ -548,7 +554,7 @@ class OracleModel:
         dlog, rec["draft_head_in"] = self.drafter_forward(X, st, a, with_head_in=True)
         drafts = [T1]
         for s in range(6):
-            drafts.append(self._pick(dlog[s], ad[s + 1] if ad is not None else None,
+            drafts.append(self._pick(listed(dlog[s]), ad[s + 1] if ad is not None else None,
                                      log, f"T{s + 2}"))
         if forced is not None:
             drafts = [T1] + [int(t) for t in forced[1:7]]

@@ -207,3 +207,33 @@ def test_head_confidence_pin_catches_a_narrow_window(monkeypatch):
     hc = gate_mod.head_confidence
     monkeypatch.setattr(D, "head_confidence", lambda l, window=20.0: hc(l, 10.0))
     _fails(D.test_head_confidence_closed_forms)
+
+
+def test_shortlist_pins_catch_slips(monkeypatch):
+    import test_oracle_shortlist as L
+    from oracle import shortlist as sl
+    monkeypatch.setattr(sl, "HALVE_EVERY", 1000)                             # halving period
+    _fails(L.test_halving_every_1024_counted_tokens)
+    monkeypatch.undo()
+
+    def half_rule(self):                                                     # 1/2 for 3/4
+        order = np.lexsort((np.arange(self.V), -self.counts))
+        last = int(self.counts[order[:self.size][-1]])
+        members = 2 * self.counts >= last
+        members[order[:self.size]] = True
+        for t in self.conv:
+            members[t] = True
+        self.members = members
+        self.rebuilds += 1
+    monkeypatch.setattr(sl.VocabList, "rebuild", half_rule)
+    _fails(L.test_list_composition, 3)
+    monkeypatch.undo()
+
+    pk = sl.VocabList.picked
+
+    def no_join(self, tokens):                                               # picks not joined
+        before = self.members.copy()
+        pk(self, tokens)
+        self.members = before
+    monkeypatch.setattr(sl.VocabList, "picked", no_join)
+    _fails(L.test_picked_tokens_join_at_once_and_count)
