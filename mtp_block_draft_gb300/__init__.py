@@ -1,12 +1,12 @@
 """GB300-native (sm_103a) DMTP speculative-decoding round.
 
 The round lives in the C-ABI library ``libdmtp.so`` (include/dmtp.h; the draft-depth
-gate in include/dmtp_gate.h); this package
-holds its CUDA sources (``csrc/``), the in-tree build (``build.py``) and the ctypes
-binding (``binding.py``).
+gate in include/dmtp_gate.h; the draft heads' token list in include/dmtp_vocab.h); this
+package holds its CUDA sources (``csrc/``), the in-tree build (``build.py``) and the
+ctypes binding (``binding.py``).
 """
-from .binding import (DmtpError, DmtpGate, DmtpRound, default_max_ctx, load_library,
-                      make_config, make_weights)
+from .binding import (DmtpError, DmtpGate, DmtpRound, DmtpVocabList, default_max_ctx,
+                      load_library, make_config, make_weights)
 
-__all__ = ["DmtpError", "DmtpGate", "DmtpRound", "default_max_ctx", "load_library",
-           "make_config", "make_weights"]
+__all__ = ["DmtpError", "DmtpGate", "DmtpRound", "DmtpVocabList", "default_max_ctx",
+           "load_library", "make_config", "make_weights"]

@@ -23,13 +23,15 @@ DMTP_MAX_TAPS = 8
 ERRORS = {0: "DMTP_OK", -1: "DMTP_EINVAL", -2: "DMTP_ENOMEM", -3: "DMTP_ECAPACITY",
           -4: "DMTP_ECUDA", -5: "DMTP_EDEVICE", -6: "DMTP_ESTATE"}
 
-# every symbol include/dmtp.h and include/dmtp_gate.h declare
+# every symbol the headers under include/ declare
 EXPORTS = ("dmtp_workspace_size", "dmtp_init", "dmtp_round", "dmtp_round_host",
            "dmtp_read_state", "dmtp_round_launches", "dmtp_round_profile", "dmtp_free",
            "dmtp_strerror", "dmtp_t1_head_noalloc", "dmtp_prefill_stats",
            "dmtp_gate_create", "dmtp_gate_forward", "dmtp_gate_draft_cost",
            "dmtp_gate_result", "dmtp_gate_pick", "dmtp_gate_pick_p", "dmtp_gate_read",
-           "dmtp_gate_free")
+           "dmtp_gate_free", "dmtp_vocab_create", "dmtp_vocab_begin_request",
+           "dmtp_vocab_picked", "dmtp_vocab_ids", "dmtp_vocab_mask", "dmtp_vocab_counts",
+           "dmtp_vocab_stats_read", "dmtp_vocab_free")
 
 DMTP_GATE_MAX_DRAFTS = 32
 DMTP_GATE_MAX_ROWS = 64
@@ -85,6 +87,12 @@ class dmtp_gate_stats(C.Structure):
                 ("bin_accepted", C.c_longlong * DMTP_GATE_BINS)]
 
 
+class dmtp_vocab_stats(C.Structure):
+    _fields_ = [("vocab", C.c_int), ("listed", C.c_int), ("counted", C.c_int),
+                ("rebuilds", C.c_int64), ("appended", C.c_int64), ("picks", C.c_int64),
+                ("picks_in", C.c_int64)]
+
+
 class dmtp_profile(C.Structure):
     _fields_ = [("ms", C.c_double * 8), ("bytes", C.c_double * 8), ("flops", C.c_double * 8),
                 ("launches", C.c_int * 8), ("round_ms", C.c_double)]
@@ -137,6 +145,17 @@ def load_library(path: str = LIB_PATH):
         getattr(lib, "dmtp_gate_" + f).restype = C.c_int
     lib.dmtp_gate_free.argtypes = [P]
     lib.dmtp_gate_free.restype = None
+    lib.dmtp_vocab_create.argtypes = [C.c_int, C.c_int, C.POINTER(P)]
+    lib.dmtp_vocab_begin_request.argtypes = [P, P, C.c_int64, C.c_int]
+    lib.dmtp_vocab_picked.argtypes = [P, P, C.c_int64]
+    lib.dmtp_vocab_ids.argtypes = [P, P, C.POINTER(C.c_int)]
+    lib.dmtp_vocab_mask.argtypes = [P, P]
+    lib.dmtp_vocab_counts.argtypes = [P, P]
+    lib.dmtp_vocab_stats_read.argtypes = [P, C.POINTER(dmtp_vocab_stats)]
+    for f in ("create", "begin_request", "picked", "ids", "mask", "counts", "stats_read"):
+        getattr(lib, "dmtp_vocab_" + f).restype = C.c_int
+    lib.dmtp_vocab_free.argtypes = [P]
+    lib.dmtp_vocab_free.restype = None
     _lib = lib
     return lib
 
@@ -368,6 +387,67 @@ class DmtpGate:
         if self.g:
             self.lib.dmtp_gate_free(self.g)
             self.g = C.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class DmtpVocabList:
+    """The draft heads' frequent-token list of include/dmtp_vocab.h (host-only;
+    argument marshalling)."""
+
+    def __init__(self, vocab: int, size: int = 0):
+        self.lib = load_library()
+        self.vocab = int(vocab)
+        self.v = C.c_void_p()
+        _check(self.lib.dmtp_vocab_create(self.vocab, int(size), C.byref(self.v)),
+               "dmtp_vocab_create")
+
+    @staticmethod
+    def _ids(tokens):
+        a = np.ascontiguousarray(np.asarray(tokens, dtype=np.int64).reshape(-1))
+        if a.size and (a.min() < -2**31 or a.max() >= 2**31):
+            raise DmtpError(-1, "token id")
+        a = a.astype(np.int32)
+        return a, (a.ctypes.data if a.size else None)
+
+    def begin_request(self, prompt, new_conversation: bool = True):
+        a, ptr = self._ids(prompt)
+        _check(self.lib.dmtp_vocab_begin_request(self.v, ptr, a.size, int(new_conversation)),
+               "dmtp_vocab_begin_request")
+
+    def picked(self, tokens):
+        a, ptr = self._ids(tokens)
+        _check(self.lib.dmtp_vocab_picked(self.v, ptr, a.size), "dmtp_vocab_picked")
+
+    def ids(self) -> np.ndarray:
+        out = np.empty(self.vocab, dtype=np.int32)
+        n = C.c_int()
+        _check(self.lib.dmtp_vocab_ids(self.v, out.ctypes.data, C.byref(n)), "dmtp_vocab_ids")
+        return out[:n.value].copy()
+
+    def mask(self) -> np.ndarray:
+        out = np.empty(self.vocab, dtype=np.uint8)
+        _check(self.lib.dmtp_vocab_mask(self.v, out.ctypes.data), "dmtp_vocab_mask")
+        return out.astype(bool)
+
+    def counts(self) -> np.ndarray:
+        out = np.empty(self.vocab, dtype=np.int64)
+        _check(self.lib.dmtp_vocab_counts(self.v, out.ctypes.data), "dmtp_vocab_counts")
+        return out
+
+    def stats(self) -> dict:
+        st = dmtp_vocab_stats()
+        _check(self.lib.dmtp_vocab_stats_read(self.v, C.byref(st)), "dmtp_vocab_stats_read")
+        return {f: getattr(st, f) for f, _ in dmtp_vocab_stats._fields_}
+
+    def close(self):
+        if self.v:
+            self.lib.dmtp_vocab_free(self.v)
+            self.v = C.c_void_p()
 
     def __del__(self):
         try:

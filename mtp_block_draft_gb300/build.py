@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdmtp.so")
 
-SOURCES = ["dmtp.cu", "elementwise.cu", "attention.cu", "gemm_simt.cu", "gemm_tc.cu", "gdn.cu", "noalloc.cu", "attention_tc.cu", "head_tc.cu", "gate.cpp"]
+SOURCES = ["dmtp.cu", "elementwise.cu", "attention.cu", "gemm_simt.cu", "gemm_tc.cu", "gdn.cu", "noalloc.cu", "attention_tc.cu", "head_tc.cu", "gate.cpp", "vocab.cpp"]
 # host-only units whose double arithmetic must round the same on every host: no fused
 # multiply-adds (aarch64 compilers contract them by default)
 EXTRA = {"gate.cpp": ["-Xcompiler", "-ffp-contract=off"]}
