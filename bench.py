@@ -196,11 +196,13 @@ def acceptance(dh):
     """Per-position acceptance from the histogram deltas of the timed rounds: entry n
     counts sequence-rounds that accepted n drafts (accept length n + 1); p_len_ge[k - 1]
     is the cumulative P(accept length >= k) for k = 1..8 (the DMTP blog's cumulative
-    acceptance curve)."""
+    acceptance curve); first_candidate = 1 - hist[0] / sum (the DMTP blog's
+    first-candidate acceptance, section 8)."""
     dh = np.asarray(dh, dtype=np.int64)
     tot = max(1, int(dh.sum()))
     return {"hist_n_accepted": [int(x) for x in dh],
-            "p_len_ge": [float(dh[k - 1:].sum()) / tot for k in range(1, 9)]}
+            "p_len_ge": [float(dh[k - 1:].sum()) / tot for k in range(1, 9)],
+            "first_candidate": (1.0 - float(dh[0]) / tot) if dh.sum() else 0.0}
 
 
 def forced_accept(cfg, weights, prompts, warmup, steps):

@@ -7,6 +7,8 @@ import os
 import subprocess
 import sys
 
+import pytest
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
@@ -57,4 +59,6 @@ def test_acceptance_curve_from_histogram():
     a = bench.acceptance([4, 0, 3, 0, 0, 0, 2, 1])
     assert a["hist_n_accepted"] == [4, 0, 3, 0, 0, 0, 2, 1]
     assert a["p_len_ge"] == [1.0, 0.6, 0.6, 0.3, 0.3, 0.3, 0.3, 0.1]
+    assert a["first_candidate"] == pytest.approx(0.6)           # 1 - 4/10
     assert bench.acceptance([0] * 8)["p_len_ge"] == [0.0] * 8
+    assert bench.acceptance([0] * 8)["first_candidate"] == 0.0
