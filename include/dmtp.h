@@ -5,7 +5,7 @@
  * DMTP blog ("DMTP: A Better First Token for Block Drafting via MTP") states it in
  * §5 "Inference: MTP First, DFlash Second" and §6.1 "Separating Prediction from
  * State Advancement":
- *   a1  T1 = argmax H RMSNorm(h_MTP) from the cached MTP hidden state;
+ *   a1  T1 = argmax H RMSNorm(h_MTP), h_MTP kept from the previous round;
  *   a2  Delta = W [RMS_e(E(T1)); RMS_m(h_MTP)] (§3, the residual equation) and the
  *       eight drafter slots [E(A), E(T1) + Delta, E(MASK) x 6];
  *   a3  one block-bidirectional drafter forward -> T2..T7 (§2, §6.2);
@@ -139,9 +139,9 @@ typedef struct dmtp_ctx dmtp_ctx;
  * batch * 8 <= 256). Returns DMTP_EINVAL for an unsupported config. */
 int dmtp_workspace_size(const dmtp_config* cfg, int batch, size_t* bytes);
 
-/* Create a context and run the prefill ("Prefill initializes all three models'
- * states", DMTP §6.1): target over each prompt (KV, taps), A = the target's greedy
- * token after it, drafter context K/V, and MTP rows 1..P giving h_MTP.
+/* Create a context and run the prefill, which sets up the state of the target, the MTP
+ * module and the drafter (DMTP §6.1): target over each prompt (KV, taps), A = the
+ * target's greedy token after it, drafter context K/V, and MTP rows 1..P giving h_MTP.
  * workspace: device buffer of >= dmtp_workspace_size bytes, 256-byte aligned.
  * prompt_ids: host int32, the B prompts concatenated; prompt_lens: host int32 [B],
  * each >= 1. stream: a cudaStream_t (NULL: the default stream). Synchronises the

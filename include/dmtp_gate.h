@@ -1,17 +1,19 @@
 /*
- * dmtp_gate.h — draft-depth gate: how many drafts a verify carries.
+ * dmtp_gate.h — draft-depth gate: the number of drafts each verify checks.
  *
- * Source: colibri speculative-decoding doc, the gate paragraph (a verify of k drafts is
- * worth value(k) = E(k) / cost(k) plain decode steps, with
+ * Source: colibri speculative-decoding doc, the draft-depth gate paragraph and its
+ * per-step refinement. A verify of k drafts is scored as value(k) = E(k) / cost(k) plain
+ * decode steps, with
  *   E(k)    = 1 + a_1 + a_1 a_2 + ... + a_1 ... a_k,
  *   cost(k) = (T(k+1) + (k - 1) d) / T(1),
- * a_j the running probability that draft j is accepted when the drafts before it were,
- * T(n) the measured time of an n-row forward, d the measured time per draft past the
- * first; the gate drafts the k of largest value and only when it exceeds 1, models an
- * unmeasured row count as T(1)(1 + (n - 1) rho), probes one draft deeper every 16 picks
- * and takes a plain step after 64 forwards without one), and the paragraph on each
- * step's own drafts (a_j replaced by the acceptance measured for drafts of the same
- * probability, ten bins of p, and only the verify priced).
+ * where a_j estimates how often draft j survives given that the earlier drafts did,
+ * T(n) is the observed duration of an n-row forward and d the observed extra time of
+ * one more draft. The depth of highest value is verified when its value is above 1
+ * (else a plain step); unobserved row counts follow T(1)(1 + (n - 1) rho); every 16th
+ * decision looks one draft deeper and a plain step is forced after 64 multi-row
+ * forwards in a row. In the per-step form, each draft's own probability selects the
+ * acceptance observed for drafts of similar probability (ten bins) and only the verify
+ * is priced.
  *
  * Readings where the page leaves a step open (the same in the test oracle):
  *   - running averages (a_j, T(n), d) are exponential with weight 1/16; the first

@@ -2,19 +2,20 @@
  * dmtp_vocab.h — the frequent-token list the draft heads score instead of the whole
  * vocabulary.
  *
- * Source: colibri speculative-decoding doc, the paragraph on the list of tokens a draft
- * head scores: the `size` tokens of highest count (16000 by default), every token whose
- * count is at least 3/4 of the count of the last of those, and every token of the
- * current conversation; every prompt token read and every token picked adds 1 to its
- * count; all counts halve every 1024 counted tokens; the list is rebuilt when a request
- * starts and at every halving, and a picked token missing from it joins at once. The
- * verify still scores every token, so the committed output does not change. The DMTP
- * blog (section 6.5) names shortlisting before exact scoring as the next step for the
- * T1 head.
+ * Source: colibri speculative-decoding doc, the paragraph on the token list a draft head
+ * scores in place of the full vocabulary: the `size` most frequent tokens (16000 unless
+ * set), any other token whose frequency reaches three quarters of the smallest
+ * frequency among those, and the tokens of the conversation being served. Each prompt
+ * token and each committed pick raises its token's count by one, and all counts are
+ * halved once 1024 tokens have been counted since the last halving; the list is
+ * recomputed at each request start and after each halving, and an unlisted pick is
+ * added immediately. Verification still scores the full vocabulary, so the committed
+ * tokens are unaffected. The DMTP blog (section 6.5) names shortlisting before exact
+ * scoring as the next step for the T1 head.
  *
  * Readings where the page leaves a step open (the same in the test oracle): counts are
  * integers and halve by floor division; the 1024th counted token since the last halving
- * triggers it; the 3/4 rule is 4 count >= 3 count_last, count_last being the size-th
+ * triggers it; the three-quarters rule is 4 count >= 3 count_last, count_last the size-th
  * largest count (so ties never change the list; with fewer than `size` counted tokens it
  * is 0 and every token is listed); a request start clears the conversation when asked,
  * joins the prompt's tokens to it, counts them in order (a halving in between rebuilds)

@@ -630,7 +630,7 @@ void enqueue_round(dmtp_ctx* c, const Dbg& dbg, const int* forced) {
   RoundState& s = c->rs;
   const int B = c->B;
   launch(c, P_OTHER, 0, 0, [&] { op_round_begin(s, c->st); });
-  // a1: T1 from the cached MTP hidden
+  // a1: T1 from h_MTP as the previous round left it
   if (c->fp8)
     launch(c, P_OTHER, 0, 0, [&] { op_rmsnorm_e4m3(c->h_mtp, c->d, c->w.mtp_final_norm, c->t1q, c->d, c->t1qs, B, c->d, c->cfg.rms_eps, RowMap(), c->st); });
   else

@@ -1,7 +1,7 @@
-// Frequent-token list of the draft heads (host only): counts from prompts and picks,
-// halved every 1024 counted tokens; the list is the tokens counted at least 3/4 of the
-// size-th largest count plus the conversation's tokens (colibri speculative-decoding
-// doc's list paragraph; readings in dmtp_vocab.h).
+// Frequent-token list of the draft heads (host only): counts raised by prompt tokens and
+// picks and halved once 1024 have been counted; listed are the tokens whose count reaches
+// three quarters of the size-th largest, and the conversation's tokens (colibri
+// speculative-decoding doc, the token-list paragraph; readings in dmtp_vocab.h).
 #include <algorithm>
 #include <new>
 #include <vector>

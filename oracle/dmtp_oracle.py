@@ -502,7 +502,7 @@ class OracleModel:
         """One DMTP round on one sequence, in place on ``st``.
 
         Steps ([DMTP] §5 and §6.1):
-          a1 T1 = argmax H RMS_f(h_MTP) from the cached MTP hidden;
+          a1 T1 = argmax H RMS_f(h_MTP), h_MTP as the previous round left it;
           a2 Δ and the slots [E(A), E(T1)+Δ, E(MASK) x 6];
           a3 one block-drafter forward -> T2..T7;
           a4 target verify of rows [A, T1..T7] at positions a..a+7, each row by the
@@ -521,7 +521,7 @@ class OracleModel:
         where that id is within ``gate`` of the maximum it is taken instead (near-tie
         lock-step). ``depth``: how many drafts the verify carries (0..7; 7 is the DMTP
         round), or a callable (drafts, confidences) -> depth called after a3 with each
-        draft head's probability of its own pick (gate.head_confidence): the verify is
+        probability each draft head gives its own pick (gate.head_confidence): the verify is
         then rows [A, T1..T_depth] and at most depth drafts are accepted (colibri doc: a
         verify of k drafts is one forward of k + 1 rows). ``draft_list``: None, or a
         boolean mask [V] of the tokens the draft heads score (shortlist.VocabList.members,

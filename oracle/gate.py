@@ -1,28 +1,29 @@
 """Draft-depth gate (TEST INFRASTRUCTURE ONLY: imported by tests/ alone).
 
-colibri speculative-decoding doc, the gate that decides how many drafts a verify carries
-(the value(k) paragraph) and the paragraph on each step's own drafts, restated:
+colibri speculative-decoding doc, the draft-depth gate (the value(k) paragraph) and its
+per-step refinement (the paragraph on each step's own drafts), in this module's words:
 
-* a_j is the running probability that draft j is accepted when the drafts before it
-  were; it starts from a prior (0.8, 0.6, then 0.5 for a model's MTP head) and is an
-  average over about 16 verifies.
-* T(n) is the measured time of a forward of n rows; d the measured time a source spends
-  per draft past its first.
-* E(k) = 1 + a_1 + a_1 a_2 + ... + a_1 ... a_k tokens from a verify of k drafts;
-  cost(k) = (T(k+1) + (k - 1) d) / T(1) in plain decode steps; value(k) = E(k) / cost(k).
-  The gate drafts the k of largest value, and only when that value exceeds 1 (a plain
-  step is worth 1).
-* A row count not measured yet costs T(1) (1 + (n - 1) rho), rho fitted from the
-  multi-row forwards measured once T(1) is; rho = 0.5 until then.
-* Every 16 picks it tries one draft deeper than its best; after 64 forwards without a
-  plain step it takes one.
-* A verify settles `judged` drafts: the accepted ones plus, after a rejection, the
-  rejected one; drafts past it say nothing about a_j.
-* Per-step variant: when the source gives the probability p_j of each of this step's
-  drafts, a_j in E(k) becomes the acceptance the gate measured for drafts of that p: ten
-  bins of p, each starting at the bin's own p with the weight of two verifies, then fed
-  by every verify; since the drafts already exist, only their verify is priced:
-  cost(k) = T(k+1) / T(1).
+* a_j estimates how often draft j survives verification given that every earlier draft
+  of the same verify did; the estimates begin at 0.8, 0.6 and 0.5 (an MTP head's
+  starting values) and move as a running mean over roughly the last 16 verifies.
+* T(n) is the observed duration of an n-row forward; d is the observed extra time one
+  more draft costs its source beyond the first draft.
+* E(k) = 1 + a_1 + a_1 a_2 + ... + a_1 ... a_k is the expected number of tokens a verify
+  of k drafts commits; cost(k) = (T(k+1) + (k - 1) d) / T(1) expresses its time in plain
+  decode steps; value(k) = E(k) / cost(k). The gate verifies the depth of highest value,
+  and falls back to a plain step (worth exactly 1) unless that value is above 1.
+* Row counts with no observation are priced by the line T(1) (1 + (n - 1) rho), whose
+  slope rho is fitted to the observed multi-row forwards once T(1) is known (0.5 before).
+* To keep estimates alive the gate goes one draft past its choice on every 16th
+  decision, and to keep T(1) observed it forces a plain step once 64 forwards in a row
+  had several rows.
+* A settled verify reports how many drafts were judged: the accepted ones plus the first
+  rejected one, if any; later drafts carry no information about a_j.
+* Per-step form: a source that can rate every draft of the current step with a probability
+  p_j lets the gate replace a_j by the acceptance it has observed for drafts rated alike
+  (ten equal bins of p, each seeded with its own centre as if two verifies had shown it
+  and updated by every verify), and since those drafts are already written only their
+  verify is priced: cost(k) = T(k+1) / T(1).
 
 Readings where the page leaves a step open (the native gate takes the same ones):
   1. "an average over about 16 verifies" is an exponential average of weight 1/16 per
@@ -54,8 +55,9 @@ N_BINS = 10
 
 
 def head_confidence(logits, window: float = 20.0) -> float:
-    """A draft head's probability of its own (argmax) token: the softmax over the scores
-    within `window` of the best (the per-step paragraph's estimate for MTP heads),
+    """The probability a draft head gives its own (argmax) pick, normalised over the
+    scores no more than `window` below the best (the per-step paragraph's estimate for
+    MTP heads),
     1 / sum over {v : l_v >= l_max - window} of exp(l_v - l_max)."""
     l = np.asarray(logits, dtype=np.float64)
     m = float(l.max())

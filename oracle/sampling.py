@@ -4,9 +4,9 @@ INFRASTRUCTURE ONLY).
 [DMTP] "DMTP: A Better First Token for Block Drafting via MTP", §5: the experiments
 verify against the target alone, comparing each candidate in turn with the token the
 target samples there and keeping the matched prefix; §7 runs every method at temperature
-1. [colibri] verify contract: the picks are made from the exact logits, greedy or
-sampled, and drafts never feed the sampler, so a sample equal to a draft is an accepted
-draft.
+1. [colibri] verify contract: every pick, whether greedy or sampled, comes from the
+target's own full logits and the sampler never sees the drafts; a draft counts as
+accepted exactly when the target's sample equals it.
 
 Reading (the pages name no sampler or generator): the target's token at position p of
 sequence b is the Gumbel-max sample argmax_v (l_v / temperature + G_v) of its logits

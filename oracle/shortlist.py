@@ -1,27 +1,23 @@
 """Frequent-token shortlist for the draft heads (TEST INFRASTRUCTURE ONLY).
 
-colibri speculative-decoding doc, the paragraph on the list of tokens a draft head
-scores instead of the whole vocabulary, restated:
+colibri speculative-decoding doc, the paragraph on the token list a draft head scores
+in place of the full vocabulary, in this module's words:
 
-* The list holds the `size` tokens of highest count (16000 by default), every token whose
-  count is at least 3/4 of the count of the last of those, and every token of the
-  current conversation.
-* Every token read as part of a prompt and every token picked adds 1 to its count; all
-  counts halve every 1024 counted tokens.
-* The list is rebuilt when a request starts and at every halving; a picked token that is
-  not on the list joins it at once.
-* Verification still scores every token, so the committed output does not change: a
-  token missing from the list can only cost a draft.
-
-The DMTP blog (section 6.5) names a shortlist of candidates before exact scoring as the
-next step for the T1 head; here the draft heads (T1 from MTP, T2..T7 from the drafter)
-take the exact argmax of their logits over the list.
+* Listed tokens: the `size` most frequent ones (16000 unless set), any other token whose
+  frequency reaches three quarters of the smallest frequency among those, and any token
+  that occurs in the conversation being served.
+* Frequencies: each prompt token and each committed pick raises its token's count by
+  one; after every 1024 counted tokens all counts are halved.
+* Upkeep: the list is recomputed at the start of each request and after each halving; a
+  pick that is not listed is added immediately.
+* Verification scores the full vocabulary, so the committed tokens are unaffected; a
+  token left off the list can only cost a draft.
 
 Readings where the page leaves a step open (the native list takes the same ones):
   1. Counts are integers; halving is floor division by 2; the 1024th counted token since
      the last halving triggers it (the counter then restarts).
-  2. "The size tokens of highest count" order by count, then by id (lower first); the
-     3/4 rule compares 4 count >= 3 count_last exactly. When fewer than `size` tokens
+  2. The `size` most frequent tokens are ranked by count, then by id (lower first); the
+     three-quarters rule compares 4 count >= 3 count_last exactly. When fewer than `size` tokens
      have a positive count, the last count is 0 and every token qualifies (no counts:
      the whole vocabulary).
   3. A request start joins the prompt's tokens to the conversation (after clearing it

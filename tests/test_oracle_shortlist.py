@@ -3,7 +3,7 @@ counts (colibri speculative-decoding doc, the list a draft head scores):
 
 * counting and halving: 1023 counted tokens leave the counts, the 1024th halves them
   (floor) and rebuilds the list;
-* composition: the `size` highest counts, every count at least 3/4 of the last of those,
+* composition: the `size` highest counts, any count reaching three quarters of the smallest of them,
   and the conversation's tokens; membership does not depend on how equal counts order;
 * no counts yet: the whole vocabulary;
 * a picked token missing from the list joins at once and is counted;
