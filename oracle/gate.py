@@ -8,8 +8,8 @@ per-step refinement (the paragraph on each step's own drafts), in this module's 
   starting values) and move as a running mean over roughly the last 16 verifies.
 * T(n) is the observed duration of an n-row forward; d is the observed extra time one
   more draft costs its source beyond the first draft.
-* E(k) = 1 + a_1 + a_1 a_2 + ... + a_1 ... a_k is the expected number of tokens a verify
-  of k drafts commits; cost(k) = (T(k+1) + (k - 1) d) / T(1) expresses its time in plain
+* E(k) = 1 + a_1 + a_1 a_2 + ... + a_1 ... a_k is the expected count of committed
+  tokens when k drafts are checked at once; cost(k) = (T(k+1) + (k - 1) d) / T(1) expresses its time in plain
   decode steps; value(k) = E(k) / cost(k). The gate verifies the depth of highest value,
   and falls back to a plain step (worth exactly 1) unless that value is above 1.
 * Row counts with no observation are priced by the line T(1) (1 + (n - 1) rho), whose
