@@ -208,16 +208,31 @@ int dmtp_round_profile(dmtp_ctx* ctx, dmtp_profile* out);
  * [d_model]; h: device fp32 [rows][d_model]; ids: device int32 [rows]; stream: a
  * cudaStream_t or NULL. Limits: 1 <= rows <= DMTP_NOALLOC_MAX_ROWS,
  * 64 <= d_model <= DMTP_NOALLOC_MAX_DMODEL, d_model % 64 == 0; otherwise DMTP_EINVAL.
- * Its scratch is a fixed library-owned device array (about 0.5 MB, held by every GPU that
- * loads the library until exit). The first call on a device sets that device up (symbol
- * lookup, kernel attribute) and should come before any stream capture. Calls share the
+ * Its scratch is a fixed library-owned device array of DMTP_NOALLOC_MAX_ROWS x
+ * DMTP_NOALLOC_MAX_DMODEL bf16 elements plus DMTP_NOALLOC_MAX_ROWS 8-byte keys (262,400
+ * bytes, about 0.26 MB), held by every GPU that loads the library until exit. The first
+ * call on a device sets that device up (symbol lookup, kernel attribute) and should come
+ * before any stream capture; that set-up does not survive cudaDeviceReset. Calls share the
  * array: calls that may overlap on the GPU race and must be serialised by the caller.
- * Asynchronous on `stream`. */
+ * Returns DMTP_ECUDA, launching nothing, if a CUDA error is already pending on the
+ * calling thread (it is not cleared), and DMTP_ECUDA if a launch or the head's tensor-map
+ * encoding fails. Asynchronous on `stream`. */
 #define DMTP_NOALLOC_MAX_ROWS 32
 #define DMTP_NOALLOC_MAX_DMODEL 4096
 int dmtp_t1_head_noalloc(const void* head, const void* norm_gain, const float* h, int rows,
                          int vocab, int d_model, float eps, int32_t* ids, float* logits,
                          void* stream);
+
+/* Self-test of the device failure path (the bounded waits and device error word that
+ * every pipelined kernel uses; no counterpart on the pages, which describe failure tests
+ * of their own engines). Enqueues on the context's stream one kernel that waits, with the
+ * kernels' bounded mbarrier wait, on a barrier nothing arrives at; after limit_ns
+ * (1e3 .. 1e9 ns) the wait gives up, sets the timeout bit of the context's device error
+ * word and the kernel returns: nothing faults, traps or waits longer. The next call that
+ * reads the error word (dmtp_read_state) returns DMTP_EDEVICE and poisons the context,
+ * exactly as a real timeout inside a round would. Returns DMTP_EINVAL for a limit out of
+ * range, DMTP_ESTATE on a poisoned context, DMTP_ECUDA if the launch fails. */
+int dmtp_selftest_timeout(dmtp_ctx* ctx, uint64_t limit_ns);
 
 /* Release the context (host memory and the graph). Never fails; NULL is a no-op.
  * Does not free caller-owned device memory. */

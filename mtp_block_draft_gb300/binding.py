@@ -27,6 +27,7 @@ ERRORS = {0: "DMTP_OK", -1: "DMTP_EINVAL", -2: "DMTP_ENOMEM", -3: "DMTP_ECAPACIT
 EXPORTS = ("dmtp_workspace_size", "dmtp_init", "dmtp_round", "dmtp_round_host",
            "dmtp_read_state", "dmtp_round_launches", "dmtp_round_profile", "dmtp_free",
            "dmtp_strerror", "dmtp_t1_head_noalloc", "dmtp_prefill_stats",
+           "dmtp_selftest_timeout",
            "dmtp_gate_create", "dmtp_gate_forward", "dmtp_gate_draft_cost",
            "dmtp_gate_result", "dmtp_gate_pick", "dmtp_gate_pick_p", "dmtp_gate_read",
            "dmtp_gate_free", "dmtp_vocab_create", "dmtp_vocab_begin_request",
@@ -127,6 +128,8 @@ def load_library(path: str = LIB_PATH):
     lib.dmtp_prefill_stats.restype = C.c_int
     lib.dmtp_round_profile.argtypes = [P, C.POINTER(dmtp_profile)]
     lib.dmtp_round_profile.restype = C.c_int
+    lib.dmtp_selftest_timeout.argtypes = [P, C.c_uint64]
+    lib.dmtp_selftest_timeout.restype = C.c_int
     lib.dmtp_free.argtypes = [P]
     lib.dmtp_free.restype = None
     lib.dmtp_t1_head_noalloc.argtypes = [P, P, P, C.c_int, C.c_int, C.c_int, C.c_float, P, P, P]
@@ -319,6 +322,10 @@ class DmtpRound:
         _check(self.lib.dmtp_prefill_stats(self.ctx, C.byref(ms), C.byref(tok)),
                "dmtp_prefill_stats")
         return ms.value, tok.value
+
+    def selftest_timeout(self, limit_ns: int):
+        """dmtp_selftest_timeout: a bounded device wait that gives up after limit_ns."""
+        _check(self.lib.dmtp_selftest_timeout(self.ctx, int(limit_ns)), "dmtp_selftest_timeout")
 
     def launches_per_round(self) -> int:
         return int(self.lib.dmtp_round_launches(self.ctx))

@@ -231,19 +231,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Wait for the phase with the given parity; gives up after DMTP_WAIT_NS.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err) {
+// Wait for the phase with the given parity; gives up after limit_ns nanoseconds of the
+// global timer, sets the timeout bit of the error word and returns false.
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, unsigned* err,
+                                              uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 128; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer() - t0 > DMTP_WAIT_NS) {
+    if (global_timer() - t0 > limit_ns) {
       set_err(err, DMTP_ERR_TIMEOUT);
       return false;
     }
   }
+}
+// The kernels' wait: gives up after DMTP_WAIT_NS.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err) {
+  return mbar_wait_for(bar, parity, err, DMTP_WAIT_NS);
 }
 
 __device__ __forceinline__ uint64_t policy_evict_first() {

@@ -1324,6 +1324,14 @@ int dmtp_round_profile(dmtp_ctx* c, dmtp_profile* out) {
   return check_err(c);
 }
 
+int dmtp_selftest_timeout(dmtp_ctx* c, uint64_t limit_ns) {
+  if (!c) return DMTP_EINVAL;
+  if (c->poisoned) return DMTP_ESTATE;
+  if (limit_ns < 1000ull || limit_ns > 1000000000ull) return DMTP_EINVAL;
+  op_wait_selftest(c->err, (unsigned long long)limit_ns, c->st);
+  return cudaGetLastError() == cudaSuccess ? DMTP_OK : DMTP_ECUDA;
+}
+
 void dmtp_free(dmtp_ctx* c) {
   if (!c) return;
   if (c->graph) cudaGraphExecDestroy(c->graph);

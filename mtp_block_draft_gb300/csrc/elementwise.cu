@@ -744,4 +744,22 @@ void op_prefill_done(const RoundState& s, const int* plen, cudaStream_t st) {
   k_prefill_done<<<cdiv(s.B, 64), 64, 0, st>>>(s, plen);
 }
 
+
+// ---- failure-path self-test ---------------------------------------------------------
+// One thread waits, with the kernels' bounded wait (common.cuh), on an mbarrier of one
+// expected arrival that nothing arrives at: the wait gives up after limit_ns, sets the
+// timeout bit of the error word and the kernel returns. Nothing is in flight (no copy,
+// no MMA), so giving up leaves nothing behind.
+__global__ void k_wait_selftest(unsigned* err, unsigned long long limit_ns) {
+  __shared__ __align__(8) unsigned long long bar;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  fence_mbar_init();
+  mbar_wait_for(b, 0, err, limit_ns);
+}
+
+void op_wait_selftest(unsigned* err, unsigned long long limit_ns, cudaStream_t st) {
+  k_wait_selftest<<<1, 1, 0, st>>>(err, limit_ns);
+}
+
 }  // namespace dmtp

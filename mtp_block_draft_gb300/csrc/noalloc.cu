@@ -9,11 +9,16 @@
 // a file-scope __device__ array of fixed size that every GPU loading the library holds
 // until the process exits.
 //
+// The array holds 32 x 4096 bf16 operand elements and 32 eight-byte keys: 262,400 bytes
+// (about 0.26 MB) per GPU.
+//
 // The first call on a device sets up that device (it looks up the array's device address
 // with cudaGetSymbolAddress and raises the head kernel's shared-memory limit); make that
-// first call before any stream capture. All calls share the one array: calls that may
-// overlap on the GPU (other streams, other threads) race on it and must be serialised by
-// the caller.
+// first call before any stream capture. The set-up is kept per device index for the life
+// of the process and does not survive cudaDeviceReset (the context it was made in is
+// gone): a caller that resets a device must not call this entry point on it afterwards.
+// All calls share the one array: calls that may overlap on the GPU (other streams, other
+// threads) race on it and must be serialised by the caller.
 #include <mutex>
 
 #include "../../include/dmtp.h"
@@ -62,6 +67,9 @@ extern "C" int dmtp_t1_head_noalloc(const void* head, const void* norm_gain, con
   if (rows < 1 || rows > kMaxRows || d_model < 64 || d_model > kMaxD || d_model % 64 ||
       vocab < 1 || ((uintptr_t)head & 15))
     return DMTP_EINVAL;
+  // an error left pending by earlier work on this thread is reported, not cleared, and
+  // nothing is launched
+  if (cudaPeekAtLastError() != cudaSuccess) return DMTP_ECUDA;
   void* base = nullptr;
   int nsm = 0;
   int r = device_scratch(&base, &nsm);
@@ -70,13 +78,15 @@ extern "C" int dmtp_t1_head_noalloc(const void* head, const void* norm_gain, con
   void* X = base;
   unsigned long long* keys = (unsigned long long*)((char*)base + kOperandBytes);
   dmtp::HeadPlan plan;
-  // the round's LM-head kernel on the same single-bf16 operand
-  if (dmtp::head_plan(&plan, head, vocab, d_model, X, rows, nsm, 256, 8)) return DMTP_EINVAL;
+  // the round's LM-head kernel on the same single-bf16 operand; the shapes were checked
+  // above, so a failure here is the tensor-map encoding
+  if (dmtp::head_plan(&plan, head, vocab, d_model, X, rows, nsm, 256, 8)) return DMTP_ECUDA;
   // keys start at zero for the atomic max; the operand rows are fully rewritten
   if (cudaMemsetAsync(keys, 0, (size_t)rows * 8, st) != cudaSuccess) return DMTP_ECUDA;
   dmtp::op_rmsnorm(1, h, d_model, norm_gain, X, d_model, 0, nullptr, 0,
                    nullptr, 0, 0, rows, d_model, eps, dmtp::RowMap(), st);
   dmtp::op_head_tc(plan, keys, logits, vocab, nullptr, nullptr, st);
   dmtp::op_keys_to_ids(keys, rows, 1, ids, 1, 0, nullptr, 0, 0, st);
-  return cudaPeekAtLastError() == cudaSuccess ? DMTP_OK : DMTP_ECUDA;
+  // no error was pending on entry, so one now comes from these launches (consumed here)
+  return cudaGetLastError() == cudaSuccess ? DMTP_OK : DMTP_ECUDA;
 }

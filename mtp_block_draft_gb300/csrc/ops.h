@@ -111,6 +111,9 @@ void op_prefill_save_last(const float* hT, const int* plen, const int2* sched, f
 void op_prefill_final(const RoundState& s, const int* plen, const float* hlast, float* hT, int d,
                       cudaStream_t st);
 void op_prefill_done(const RoundState& s, const int* plen, cudaStream_t st);
+// Failure-path self-test: one bounded mbarrier wait that nothing satisfies gives up after
+// limit_ns and sets DMTP_ERR_TIMEOUT in err.
+void op_wait_selftest(unsigned* err, unsigned long long limit_ns, cudaStream_t st);
 
 // ---- attention.cu ------------------------------------------------------------------
 struct AttnArgs {

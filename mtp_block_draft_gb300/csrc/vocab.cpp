@@ -28,7 +28,7 @@ struct dmtp_vocab_list {
     // count_last: the size-th largest count (0 when size >= V is not reached by counts)
     int64_t last = 0;
     const int k = std::min(size, V);
-    scratch = counts;
+    std::copy(counts.begin(), counts.end(), scratch.begin());  // sized at creation
     std::nth_element(scratch.begin(), scratch.begin() + (k - 1), scratch.end(),
                      [](int64_t a, int64_t b) { return a > b; });
     last = scratch[k - 1];
@@ -62,6 +62,7 @@ int dmtp_vocab_create(int vocab, int size, dmtp_vocab_list** out) {
     v->V = vocab;
     v->size = size ? size : DMTP_VOCAB_DEFAULT_SIZE;
     v->counts.assign(vocab, 0);
+    v->scratch.assign(vocab, 0);  // rebuild() allocates nothing after creation
     v->member.assign(vocab, 1);  // before the first request: every token
     v->conv.assign(vocab, 0);
     v->listed = vocab;

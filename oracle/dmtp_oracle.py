@@ -25,10 +25,11 @@ drafter context K/V at position p is RoPE(Wk c_p, p), Wv c_p with
 c_p = RMS(W_fc [taps at p]); Gated DeltaNet uses L2-normalised q, k, sigmoid gates,
 no short convolution and no output scale.
 
-Storage: weights arrive already in the model's storage type; K/V caches are stored in
-it too (bf16 models keep a bf16 KV cache), so keys and values are rounded to bf16
-(through float32, as the kernels produce them) when written. Everything else,
-including the Gated DeltaNet state, is computed and kept in float64.
+Storage: weights arrive already in the model's storage type (bf16 values upcast).
+Every intermediate result, the K/V caches and the Gated DeltaNet state included, is
+computed and kept in float64: the oracle states the round's arithmetic, not a storage
+format. (``kv_store="bf16"`` rounds stored keys and values to bf16 instead; it serves
+only as a side check that the pins survive a bf16 cache.)
 """
 from __future__ import annotations
 
@@ -200,20 +201,25 @@ class OracleModel:
 
     def __init__(self, cfg, weights: dict, gate: float = 0.05, kv_store: str | None = None,
                  temperature: float = 0.0, sample_seed: int = 0,
-                 draft_head_fp8: bool = False):
-        """kv_store: storage type of every K/V cache ("bf16" or "fp32"); by default the
-        model's storage type (cfg.dtype). Stored keys and values are rounded to it when
-        written, as a bf16 KV cache holds them; every computation stays float64.
+                 draft_head_fp8: bool = False, chunk: int = 1024):
+        """kv_store: "fp32" (default: keys and values kept exactly, in float64) or
+        "bf16" (stored keys and values rounded to bf16 when written; a side check only).
         temperature > 0: the verify picks are target samples (sampling.py) with the given
         sampling seed; 0: argmax picks. draft_head_fp8: the T1 and drafter heads score
-        with the E4M3-quantised head (fp8.py); the verify head stays exact."""
+        with the E4M3-quantised head (fp8.py); the verify head stays exact. chunk: prompt
+        rows per block of the prefill (bounds the [rows, keys] score matrices)."""
         self.cfg = cfg
         self.temperature, self.sample_seed = float(temperature), int(sample_seed)
         self.W = {k: v.detach().to("cpu").double().numpy() if hasattr(v, "detach")
                   else np.asarray(v, dtype=F64) for k, v in weights.items()}
         self.gate = gate
-        self.kv_bf16 = (kv_store or cfg.dtype) == "bf16"
+        if kv_store not in (None, "fp32", "bf16"):
+            raise ValueError("kv_store: 'fp32' or 'bf16'")
+        self.kv_bf16 = kv_store == "bf16"
         self.draft_fp8 = bool(draft_head_fp8)
+        if int(chunk) < 1:
+            raise ValueError("chunk >= 1")
+        self.chunk = int(chunk)
         if self.draft_fp8:
             self.Hq, self.Hs = quantize_rows(self.W["head"])
         c = cfg
@@ -435,13 +441,24 @@ class OracleModel:
         P = len(prompt)
         st = self.empty_state()
         st.b = int(b)
-        hT, taps, _, _ = self.target_rows(st, prompt, 0, head=False)
+        # Rows go through in blocks of at most `chunk`: a row attends causally, so a block
+        # sees exactly the keys of the blocks before it and its own earlier rows; only the
+        # size of the score matrices changes.
+        C = self.chunk
+        hT, taps = [], []
+        for c0 in range(0, P, C):
+            h, t, _, _ = self.target_rows(st, prompt[c0:c0 + C], c0, head=False)
+            hT.append(h)
+            taps.append(t)
+        hT, taps = np.concatenate(hT), np.concatenate(taps)
         log = {"gaps": {}, "adopted": [], "mismatch": []}
         A = self._pick(hT[P - 1] @ self.W["head"].T, adopt_A, log, "A")
         self.prefill_log = log
         for j, (k, v) in enumerate(self.drafter_ctx_kv(taps, np.arange(P))):
             st.dft_K[j], st.dft_V[j] = k, v
-        out = self.mtp_rows(st, hT, prompt[1:] + [A], 1)
+        mtok = prompt[1:] + [A]
+        for c0 in range(0, P, C):
+            out = self.mtp_rows(st, hT[c0:c0 + C], mtok[c0:c0 + C], 1 + c0)
         st.h_mtp = out[-1].copy()
         st.a, st.A = P, A
         st.tokens = prompt + [A]

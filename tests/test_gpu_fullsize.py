@@ -35,11 +35,16 @@ def test_small_full_size_lockstep():
     ls.close()
 
 
-def test_b32_full_size_sampled_sequence():
+@pytest.mark.parametrize("which", ["shortest", "longest"])
+def test_b32_full_size_sampled_sequence(which):
+    """The full B32 batch on the GPU; the oracle follows its shortest (611 tokens) or its
+    longest (~4.1K tokens: segments spread over many CTAs of the persistent attention)
+    sequence."""
     from lockstep import Lockstep
     cfg = CONFIGS["b32"]
     prompts = make_prompts(cfg)
-    b = int(np.argmin([len(p) for p in prompts]))
+    lens = [len(p) for p in prompts]
+    b = int(np.argmin(lens) if which == "shortest" else np.argmax(lens))
     ls = Lockstep(cfg, make_weights(cfg, "cuda"), prompts, rounds=2, seqs=[b])
     for _ in range(2):
         ls.step(tol=TOL)
@@ -77,6 +82,27 @@ def test_hybrid_full_dims_lockstep():
     cfg = CONFIGS["hybrid"].replace(batch=2, ctx_lo=96, ctx_hi=160)
     ls = Lockstep(cfg, make_weights(cfg, "cuda"), make_prompts(cfg), rounds=3)
     for r in range(3):
+        ls.step(tol=TOL)
+    ls.close()
+
+
+LONG_NARROW = CONFIGS["long"].replace(name="long_narrow", vocab=5000, d_model=256, n_layers=2,
+                                     n_heads=8, n_kv_heads=2, head_dim=64, ffn=512)
+
+
+@pytest.mark.parametrize("batch,lo,hi", [(2, 9000, 12000), (1, 32768, 32768)])
+def test_long_context_lockstep(batch, lo, hi):
+    """The long-context workload's shape at reduced width against the oracle: prompts of
+    9-12K and of 32K (1024-token chunks repeated at random), so the drafter's
+    anchor-relative window (positions a - 4096 .. a - 1, DMTP blog §6.2) binds, and every
+    sequence's visible keys spread over many CTAs of the persistent split-K attention and
+    many partials of its merge."""
+    from lockstep import Lockstep
+    cfg = LONG_NARROW.replace(batch=batch, ctx_lo=lo, ctx_hi=hi)
+    prompts = make_prompts(cfg)
+    assert min(len(p) for p in prompts) - cfg.draft_window > 4000
+    ls = Lockstep(cfg, make_weights(cfg, "cuda"), prompts, rounds=3)
+    for _ in range(3):
         ls.step(tol=TOL)
     ls.close()
 

@@ -284,3 +284,35 @@ def test_temperature_validation():
             DmtpRound(TINY.replace(temperature=t), w, make_prompts(TINY), 256)
     with pytest.raises(DmtpError):  # E4M3 draft heads need a bf16 model
         DmtpRound(TINY.replace(draft_head_fp8=True), w, make_prompts(TINY), 256)
+
+
+def test_device_timeout_poisons_context():
+    """The device failure path with nothing faulted: a bounded wait that nothing satisfies
+    (dmtp_selftest_timeout, 50 us) gives up and sets the timeout bit; the host then reports
+    DMTP_EDEVICE, every later call DMTP_ESTATE, dmtp_free is clean, and a new context on
+    the same device runs rounds normally."""
+    from mtp_block_draft_gb300 import DmtpError, DmtpRound, default_max_ctx
+    w = make_weights(B32_R, "cuda")
+    prompts = make_prompts(B32_R)
+    g = DmtpRound(B32_R, w, prompts, default_max_ctx(prompts, 4))
+    g.round()
+    g.read_state()                                   # clean so far
+    with pytest.raises(DmtpError) as e:
+        g.selftest_timeout(10)                       # limit below 1 us: rejected
+    assert e.value.code == -1
+    g.selftest_timeout(50_000)
+    with pytest.raises(DmtpError) as e:
+        g.read_state()
+    assert e.value.code == -5                        # DMTP_EDEVICE
+    for call in (g.round, g.read_state, g.profile_round, lambda: g.selftest_timeout(50_000)):
+        with pytest.raises(DmtpError) as e:
+            call()
+        assert e.value.code == -6                    # DMTP_ESTATE
+    g.close()
+    torch.cuda.synchronize()
+    g2 = DmtpRound(B32_R, w, prompts, default_max_ctx(prompts, 4))
+    out = g2.alloc_out(ints=True)
+    g2.round(out)
+    kv, _, _ = g2.read_state()
+    assert (kv > np.array([len(p) for p in prompts])).all()
+    g2.close()

@@ -124,6 +124,39 @@ def test_drafter_pins_catch_slips(monkeypatch):
         monkeypatch.undo()
 
 
+def test_state_advance_pin_catches_a6_slips(monkeypatch):
+    """The round's state advance (a6): slips that only the rounds make (the prefill's own
+    calls start at position 0 or 1) must break state advance == prefill."""
+    ctx = O.OracleModel.drafter_ctx_kv
+    mtp = O.OracleModel.mtp_rows
+    in_round = lambda pos: int(np.asarray(pos).reshape(-1)[0]) > 0
+
+    monkeypatch.setattr(O.OracleModel, "drafter_ctx_kv",                         # taps row + 1
+                        lambda self, taps, pos: ctx(self, np.roll(taps, -1, axis=0)
+                                                    if in_round(pos) else taps, pos))
+    _fails(R.test_state_advance_equals_prefill, "tiny")
+    monkeypatch.undo()
+
+    monkeypatch.setattr(O.OracleModel, "drafter_ctx_kv",                         # position + 1
+                        lambda self, taps, pos: ctx(self, taps, np.asarray(pos) +
+                                                    (1 if in_round(pos) else 0)))
+    _fails(R.test_state_advance_equals_prefill, "tiny")
+    monkeypatch.undo()
+
+    monkeypatch.setattr(O.OracleModel, "mtp_rows",                               # token of p + 1
+                        lambda self, st, h, toks, pos0: mtp(
+                            self, st, h, list(toks[1:]) + [toks[-1]] if pos0 > 1 and
+                            st.a > 0 and pos0 == st.a + 1 else toks, pos0))
+    _fails(R.test_state_advance_equals_prefill, "tiny")
+    monkeypatch.undo()
+
+    monkeypatch.setattr(O.OracleModel, "mtp_rows",                               # h of row p
+                        lambda self, st, h, toks, pos0: mtp(
+                            self, st, np.roll(h, -1, axis=0) if pos0 > 1 and
+                            pos0 == st.a + 1 else h, toks, pos0))
+    _fails(R.test_state_advance_equals_prefill, "tiny_hybrid")
+
+
 def test_sampling_pin_catches_a_swapped_key(monkeypatch):
     ph = sampling_mod.philox4x32_10
     monkeypatch.setattr(S, "philox4x32_10", lambda ctr, key: ph(ctr, np.asarray(key)[::-1]))

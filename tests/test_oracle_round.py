@@ -272,6 +272,66 @@ def test_prefill_matches_one_row_steps(tiny, prompt):
         np.testing.assert_allclose(a.tgt_V[l], st.tgt_V[l], rtol=1e-11, atol=1e-12)
 
 
+def _assert_same_state(a, b, tol=1e-10):
+    """Two sequence states agree: positions, pending token, every cache and h_MTP."""
+    assert a.a == b.a and a.A == b.A
+    pairs = [(a.mtp_K, b.mtp_K), (a.mtp_V, b.mtp_V), (a.h_mtp, b.h_mtp)]
+    pairs += list(zip(a.dft_K, b.dft_K)) + list(zip(a.dft_V, b.dft_V))
+    for x, y in zip(a.tgt_K + a.tgt_V + a.gdn_S, b.tgt_K + b.tgt_V + b.gdn_S):
+        assert (x is None) == (y is None)
+        if x is not None:
+            pairs.append((x, y))
+    for x, y in pairs:
+        assert x.shape == y.shape
+        np.testing.assert_allclose(x, y, rtol=0, atol=tol)
+
+
+def test_prefill_in_blocks_matches_one_block(tiny, prompt):
+    """Prefill in row blocks (any block size) builds the state a single block builds:
+    causal rows see only earlier positions, so splitting the rows changes no value."""
+    one = tiny.prefill(prompt)
+    w = make_weights(TINY, "cpu")
+    for chunk in (1, 5, 16):
+        _assert_same_state(OracleModel(TINY, w, chunk=chunk).prefill(prompt), one, 1e-12)
+    st = tiny.empty_state()
+    for p, t in enumerate(prompt):
+        tiny.target_rows(st, [t], p, head=False)
+    for l in range(TINY.n_layers):
+        np.testing.assert_allclose(one.tgt_K[l], st.tgt_K[l], rtol=0, atol=1e-12)
+
+
+def _advance_rounds(m, prompt, greedy, rounds):
+    """Rounds with natural drafts and with drafts forced from the greedy stream with one
+    wrong row (every accepted length 0..7 occurs)."""
+    st = m.prefill(prompt)
+    for r in range(rounds):
+        if r % 3 == 0:
+            m.round(st)
+            continue
+        off = st.a - len(prompt)
+        d = list(greedy[off + 1: off + 8])
+        wrong = (r * 5) % 8
+        if wrong < 7:
+            d[wrong] = (d[wrong] + 1) % (m.cfg.vocab - 1)
+        m.round(st, forced=d)
+    return st
+
+
+@pytest.mark.parametrize("which", ["tiny", "tiny_hybrid"])
+def test_state_advance_equals_prefill(which):
+    """[DMTP] §6.1 and §6.3: the rounds advance the target KV (or recurrent state), the
+    drafter's context K/V, the MTP KV and h_MTP to exactly the state a prefill of the
+    prompt followed by the committed stream (the pending token A excluded) builds."""
+    cfg = TINY if which == "tiny" else HYB
+    m = OracleModel(cfg, make_weights(cfg, "cpu"))
+    prompt = make_prompts(cfg)[0][:40]
+    greedy = m.greedy_decode(prompt, 12 * 8 + 2)
+    st = _advance_rounds(m, prompt, greedy, 12)
+    assert st.tokens == list(prompt) + greedy[:len(st.tokens) - len(prompt)]
+    ref = m.prefill(st.tokens[:-1])
+    _assert_same_state(st, ref)
+
+
 @pytest.fixture(scope="module")
 def hyb():
     return OracleModel(HYB, make_weights(HYB, "cpu"))

@@ -4,8 +4,10 @@ afford an allocation's device synchronisation).
 
 It must give what step a1 of dmtp_round gives: run rounds with debug outputs, feed
 each round's starting h_MTP to the no-alloc entry point, and compare the picked ids
-(exactly) and the logits (within the suite's 2e-2) - two calls in a row, so the
-shared scratch array is reused. Sizes past the documented maximum are rejected.
+(exactly, on rows whose top-1 minus top-2 logit gap exceeds the suite's 0.05 near-tie
+gate: the round may time another head tile shape, whose rounding can flip a near tie)
+and the logits (within the suite's 2e-2) - two calls in a row, so the shared scratch
+array is reused. Sizes past the documented maximum are rejected.
 This file sorts last so that a run stopping at the first failure has run the rest.
 """
 import ctypes
@@ -22,6 +24,12 @@ pytestmark = pytest.mark.gpu
 CFG = CONFIGS["b32"].replace(name="b32_noalloc", vocab=5000, d_model=256, n_layers=2,
                              n_heads=8, n_kv_heads=2, head_dim=64, ffn=512, ctx_lo=40,
                              ctx_hi=120)
+
+
+def _clear_rows(logits):
+    """Rows whose top-1 minus top-2 logit exceeds the near-tie gate (0.05)."""
+    top2 = np.sort(logits, axis=1)[:, -2:]
+    return (top2[:, 1] - top2[:, 0]) > 0.05
 
 
 def _call(lib, w, h, rows, ids, logits, stream):
@@ -48,14 +56,19 @@ def test_noalloc_head_matches_round_a1():
         logits = torch.zeros((B, V), dtype=torch.float32, device="cuda")
         assert _call(lib, w, out["h_mtp"], B, ids, logits, stream) == 0
         torch.cuda.synchronize()
-        np.testing.assert_array_equal(ids.cpu().numpy(), out["drafts"][:, 0].cpu().numpy())
+        clear = _clear_rows(out["t1_logits"].cpu().numpy())
+        assert clear.sum() >= B // 2
+        np.testing.assert_array_equal(ids.cpu().numpy()[clear],
+                                      out["drafts"][:, 0].cpu().numpy()[clear])
         err = (logits - out["t1_logits"]).abs().max().item()
         assert err <= 2e-2, err
     # without logits, on a subset of rows
     ids = torch.full((5,), -7, dtype=torch.int32, device="cuda")
     assert _call(lib, w, out["h_mtp"], 5, ids, None, stream) == 0
     torch.cuda.synchronize()
-    np.testing.assert_array_equal(ids.cpu().numpy(), out["drafts"][:5, 0].cpu().numpy())
+    clear = _clear_rows(out["t1_logits"].cpu().numpy())[:5]
+    np.testing.assert_array_equal(ids.cpu().numpy()[clear],
+                                  out["drafts"][:5, 0].cpu().numpy()[clear])
     g.close()
 
 
