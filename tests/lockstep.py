@@ -27,7 +27,13 @@ def to_np(t):
 
 
 class Lockstep:
-    def __init__(self, cfg, weights_gpu: dict, prompts, rounds: int, seqs=None, max_ctx=None):
+    def __init__(self, cfg, weights_gpu: dict, prompts, rounds: int, seqs=None, max_ctx=None,
+                 kv_floor: bool = False):
+        """kv_floor: also run the oracle with its K/V caches rounded to bf16 (the GPU's
+        storage) on the same picks. Each float field must then be within `tol` of that
+        oracle (the kernels' arithmetic), and within `tol` plus the storage floor - the
+        distance between the two oracles on this field this round - of the exact oracle
+        (what a bf16 cache alone costs against exact K/V)."""
         from mtp_block_draft_gb300 import DmtpRound, default_max_ctx
         self.cfg = cfg
         self.prompts = prompts
@@ -46,6 +52,15 @@ class Lockstep:
             self.adopted += self.oracle.prefill_log["adopted"]
             assert st.A == int(A[b]) and st.a == int(kv[b]) == len(prompts[b])
             self.states[b] = st
+        self.floor_oracle, self.floor_states = None, {}
+        if kv_floor:
+            import copy
+            self.floor_oracle = copy.copy(self.oracle)  # same weights, bf16 K/V storage
+            self.floor_oracle.kv_bf16 = True
+            for b in self.seqs:
+                self.floor_states[b] = self.floor_oracle.prefill(prompts[b], adopt_A=int(A[b]),
+                                                                 b=b)
+                assert not self.floor_oracle.prefill_log["mismatch"]
         self.max_err = {}
 
     def _err(self, name, a, b):
@@ -53,7 +68,11 @@ class Lockstep:
         self.max_err[name] = max(self.max_err.get(name, 0.0), e)
         return e
 
-    def step(self, forced: np.ndarray | None = None, floats: bool = True, tol: float = 2e-2):
+    def step(self, forced: np.ndarray | None = None, floats: bool = True, tol: float = 2e-2,
+             draft_list: np.ndarray | None = None):
+        """draft_list: boolean mask [V] of the tokens the draft heads score (the list the
+        GPU context was given with set_draft_list); the draft logits are then compared at
+        the listed tokens only."""
         g = self.gpu
         out = g.alloc_out(ints=True, floats=floats)
         ft = None
@@ -69,7 +88,14 @@ class Lockstep:
                 adopt["T"] = o["drafts"][b]
             rec = self.oracle.round(self.states[b],
                                     forced=None if forced is None else forced[b],
-                                    adopt=adopt, want_logits=floats)
+                                    adopt=adopt, want_logits=floats, draft_list=draft_list)
+            frec = None
+            if self.floor_oracle is not None:
+                frec = self.floor_oracle.round(self.floor_states[b],
+                                               forced=None if forced is None else forced[b],
+                                               adopt=adopt, want_logits=floats,
+                                               draft_list=draft_list)
+                assert not frec["log"]["mismatch"], (b, frec["log"]["mismatch"])
             log = rec["log"]
             assert not log["mismatch"], (b, log["mismatch"])
             self.adopted += log["adopted"]
@@ -83,9 +109,12 @@ class Lockstep:
             assert int(o["snap_slot"][b]) == rec["snap_slot"]
             if floats:
                 fp8 = self.cfg.draft_head_fp8
+                listed = ((lambda x: x) if draft_list is None else
+                          (lambda x: np.asarray(x)[..., draft_list]))
                 for name, key in (("t1_logits", "t1_logits"), ("draft_logits", "draft_logits"),
                                   ("verify_logits", "verify_logits"), ("delta", "delta"),
                                   ("h_mtp", "h_mtp_in")):
+                    sel = listed if name in ("t1_logits", "draft_logits") else (lambda x: x)
                     if fp8 and name in ("t1_logits", "draft_logits"):
                         # quantised draft heads: within the interval the input difference
                         # allows (oracle/fp8.py), plus the float bar
@@ -93,14 +122,21 @@ class Lockstep:
                         ref, width = fp8_logit_bounds(hin, self.oracle.Hq, self.oracle.Hs,
                                                       FP8_INPUT_DELTA)
                         gpu = np.asarray(o[name][b], np.float64).reshape(ref.shape)
+                        ref, width, gpu = sel(ref), sel(width), sel(gpu)
                         excess = float(np.max(np.abs(gpu - ref) - width))
                         self.max_err[name + "_beyond_bound"] = max(
                             self.max_err.get(name + "_beyond_bound", -1e30), excess)
                         self._err(name, gpu, ref)
                         assert excess <= tol, (b, name, excess)
                         continue
-                    e = self._err(name, o[name][b], rec[key])
-                    assert e <= tol, (b, name, e)
+                    e = self._err(name, sel(o[name][b]), sel(rec[key]))
+                    if frec is None:
+                        assert e <= tol, (b, name, e)
+                        continue
+                    ef = self._err(name + "_vs_bf16kv_oracle", sel(o[name][b]), sel(frec[key]))
+                    floor = self._err(name + "_bf16kv_floor", sel(frec[key]), sel(rec[key]))
+                    assert ef <= tol, (b, name, "vs the bf16-KV oracle", ef)
+                    assert e <= tol + floor, (b, name, e, floor)
             recs[b] = rec
         return o, recs
 

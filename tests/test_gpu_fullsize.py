@@ -3,8 +3,12 @@
 * small (B=1, 2048-token prompt, vocab 32000): the whole batch in lock-step with the
   oracle.
 * B32 (32 sequences, prompts U[512, 4096], vocab 151936, 16 layers): the GPU runs the
-  full batch; the oracle computes one sampled sequence (the shortest prompt) by itself,
-  since sequences are independent.
+  full batch; the oracle computes one sampled sequence (the shortest or the longest
+  prompt) by itself, since sequences are independent.
+* At these sizes the bf16 K/V cache alone moves logits and h_MTP by about 2e-2 against
+  exact K/V (the oracle measures it: the same round with its caches rounded to bf16).
+  These tests therefore also run that bf16-storage oracle on the same picks: the GPU must
+  be within 2e-2 of it, and within 2e-2 plus that storage floor of the exact oracle.
 * hybrid (48 layers, 36 Gated DeltaNet with 32 heads of 128 x 128 state): full model
   dimensions against the oracle at a short prompt (the oracle's recurrence runs row by
   row), and the full 8 x 4096 batch through properties.
@@ -45,7 +49,7 @@ def test_b32_full_size_sampled_sequence(which):
     prompts = make_prompts(cfg)
     lens = [len(p) for p in prompts]
     b = int(np.argmin(lens) if which == "shortest" else np.argmax(lens))
-    ls = Lockstep(cfg, make_weights(cfg, "cuda"), prompts, rounds=2, seqs=[b])
+    ls = Lockstep(cfg, make_weights(cfg, "cuda"), prompts, rounds=2, seqs=[b], kv_floor=True)
     for _ in range(2):
         ls.step(tol=TOL)
     ls.close()
@@ -58,7 +62,7 @@ def test_b32_full_size_sampled_verification():
     cfg = CONFIGS["b32"].replace(temperature=1.0, sample_seed=12345)
     prompts = make_prompts(cfg)
     b = int(np.argmin([len(p) for p in prompts]))
-    ls = Lockstep(cfg, make_weights(cfg, "cuda"), prompts, rounds=2, seqs=[b])
+    ls = Lockstep(cfg, make_weights(cfg, "cuda"), prompts, rounds=2, seqs=[b], kv_floor=True)
     for _ in range(2):
         ls.step(tol=TOL)
     ls.close()
@@ -71,7 +75,7 @@ def test_b32_full_size_fp8_draft_heads():
     cfg = CONFIGS["b32"].replace(draft_head_fp8=True)
     prompts = make_prompts(cfg)
     b = int(np.argmin([len(p) for p in prompts]))
-    ls = Lockstep(cfg, make_weights(cfg, "cuda"), prompts, rounds=2, seqs=[b])
+    ls = Lockstep(cfg, make_weights(cfg, "cuda"), prompts, rounds=2, seqs=[b], kv_floor=True)
     for _ in range(2):
         ls.step(tol=TOL)
     ls.close()
@@ -80,7 +84,7 @@ def test_b32_full_size_fp8_draft_heads():
 def test_hybrid_full_dims_lockstep():
     from lockstep import Lockstep
     cfg = CONFIGS["hybrid"].replace(batch=2, ctx_lo=96, ctx_hi=160)
-    ls = Lockstep(cfg, make_weights(cfg, "cuda"), make_prompts(cfg), rounds=3)
+    ls = Lockstep(cfg, make_weights(cfg, "cuda"), make_prompts(cfg), rounds=3, kv_floor=True)
     for r in range(3):
         ls.step(tol=TOL)
     ls.close()
@@ -90,15 +94,18 @@ LONG_NARROW = CONFIGS["long"].replace(name="long_narrow", vocab=5000, d_model=25
                                      n_heads=8, n_kv_heads=2, head_dim=64, ffn=512)
 
 
-@pytest.mark.parametrize("batch,lo,hi", [(2, 9000, 12000), (1, 32768, 32768)])
-def test_long_context_lockstep(batch, lo, hi):
+@pytest.mark.parametrize("batch,lo,hi,heads", [(2, 9000, 12000, (8, 2)),
+                                               (1, 32768, 32768, (4, 1))])
+def test_long_context_lockstep(batch, lo, hi, heads):
     """The long-context workload's shape at reduced width against the oracle: prompts of
     9-12K and of 32K (1024-token chunks repeated at random), so the drafter's
     anchor-relative window (positions a - 4096 .. a - 1, DMTP blog §6.2) binds, and every
     sequence's visible keys spread over many CTAs of the persistent split-K attention and
-    many partials of its merge."""
+    many partials of its merge. The 32K case keeps the 32/4 workload's query group of four
+    with 4/1 heads, so that the oracle's prefill stays within minutes."""
     from lockstep import Lockstep
-    cfg = LONG_NARROW.replace(batch=batch, ctx_lo=lo, ctx_hi=hi)
+    cfg = LONG_NARROW.replace(batch=batch, ctx_lo=lo, ctx_hi=hi, n_heads=heads[0],
+                              n_kv_heads=heads[1])
     prompts = make_prompts(cfg)
     assert min(len(p) for p in prompts) - cfg.draft_window > 4000
     ls = Lockstep(cfg, make_weights(cfg, "cuda"), prompts, rounds=3)

@@ -57,7 +57,7 @@ def test_noalloc_head_matches_round_a1():
         assert _call(lib, w, out["h_mtp"], B, ids, logits, stream) == 0
         torch.cuda.synchronize()
         clear = _clear_rows(out["t1_logits"].cpu().numpy())
-        assert clear.sum() >= B // 2
+        assert clear.sum() >= B // 4
         np.testing.assert_array_equal(ids.cpu().numpy()[clear],
                                       out["drafts"][:, 0].cpu().numpy()[clear])
         err = (logits - out["t1_logits"]).abs().max().item()
