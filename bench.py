@@ -53,9 +53,10 @@ def _peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def _traffic(kernel: str, alg_bytes_per_launch: float):
-    """DRAM bytes per launch of `kernel` from the ncu captures summarised in profiles/
-    (DRAM / algorithmic ratio of that kernel), or None once the kernel source changed."""
+def _traffic(kernel: str, bytes_per_launch: float, impl_bytes_per_launch: float):
+    """DRAM bytes per launch of `kernel` from the ncu captures summarised in profiles/ (the
+    ratio of DRAM bytes to the bytes the record's basis counts: the method's bytes, or the
+    implementation's), or None once the kernel source changed."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
@@ -66,8 +67,10 @@ def _traffic(kernel: str, alg_bytes_per_launch: float):
     src = os.path.join(ROOT, rec["source"])
     if hashlib.sha1(open(src, "rb").read()).hexdigest() != rec["sha1"]:
         return None, "kernel changed since the ncu capture"
-    return alg_bytes_per_launch * rec["dram_over_algorithmic"], \
-        f"ncu DRAM/algorithmic ratio {rec['dram_over_algorithmic']} (profiles/{rec['capture']})"
+    basis = rec.get("basis", "method")
+    per = impl_bytes_per_launch if basis == "implementation" else bytes_per_launch
+    return per * rec["dram_over_algorithmic"], \
+        f"ncu DRAM / {basis} bytes {rec['dram_over_algorithmic']} (profiles/{rec['capture']})"
 
 
 class Clocks:
@@ -205,34 +208,67 @@ def acceptance(dh):
             "first_candidate": (1.0 - float(dh[0]) / tot) if dh.sum() else 0.0}
 
 
-def forced_accept(cfg, weights, prompts, warmup, steps):
+def forced_accept(cfg, weights, prompts, warmup, steps, max_iter=6):
     """Rounds with every draft accepted: the drafts are forced to the target's own greedy
-    continuation, collected first on a separate context by rounds whose drafts are forced
-    wrong (each commits exactly the greedy tokens up to its first rejection), then replayed
-    as the forced-draft graph on a fresh context from the same prompts. The histogram of
-    the timed rounds gives the accept length actually reached (8 unless a near tie in the
-    target's logits flips a pick between the two runs)."""
+    continuation, then replayed as the forced-draft graph on a fresh context from the same
+    prompts and timed. The continuation must be the one the replay itself computes: a
+    near tie in the target's logits can resolve differently when the same position is
+    computed as row 0 of a one-token round or as row s of an eight-row round (other
+    attention splits, other reduction orders). So the plan is refined to a fixed point:
+    a first plan comes from rounds whose drafts are forced wrong (each commits exactly
+    the next greedy token); each refinement replays the plan on a fresh context and, for
+    every sequence whose replay rejected a draft, keeps the committed tokens up to and
+    including the correction and continues that sequence with one-token rounds; once a
+    replay accepts every draft of every round, a fresh context replays it again, timed.
+    The histogram of the timed rounds gives the accept length reached."""
     import torch
     from mtp_block_draft_gb300 import DmtpRound
     B, V, R = len(prompts), cfg.vocab, warmup + steps
-    max_ctx = max(len(p) for p in prompts) + 8 * R + 64
-    g1 = DmtpRound(cfg, weights, prompts, max_ctx)
-    _, A, _ = g1.read_state()
-    streams = [[int(a)] for a in A]
+    need = 8 * R + 1
+    max_ctx = max(len(p) for p in prompts) + 8 * (need + 2) + 64
     forced = torch.empty((B, 7), dtype=torch.int32, device="cuda")
-    out = g1.alloc_out(ints=True, floats=False)
-    while min(len(st) for st in streams) < 8 * R + 1:
-        wrong = [[(st[-1] + 1 + j) % (V - 1) for j in range(7)] for st in streams]
-        forced.copy_(torch.tensor(wrong, dtype=torch.int32))
-        g1.round(out, forced=forced)
-        com, n = out["committed"].cpu().numpy(), out["n_accepted"].cpu().numpy()
-        for b in range(B):
-            streams[b] += [int(t) for t in com[b][:n[b] + 1]]
-    g1.close()
-    del g1
-    plan = torch.tensor([[[streams[b][8 * r + 1 + j] for j in range(7)] for b in range(B)]
-                         for r in range(R)], dtype=torch.int32, device="cuda")
-    torch.cuda.empty_cache()
+
+    def wrong(st):
+        return [(st[-1] + 1 + j) % (V - 1) for j in range(7)]
+
+    def run(plan):
+        """Replay `plan` (list per sequence of R rounds of 7 drafts, or None: all wrong);
+        returns the committed streams (each at least `need` tokens) and whether every
+        round of every sequence accepted all 7 drafts."""
+        g = DmtpRound(cfg, weights, prompts, max_ctx)
+        _, A, _ = g.read_state()
+        streams = [[int(a)] for a in A]
+        ok = [plan is not None] * B
+        out = g.alloc_out(ints=True, floats=False)
+        r = 0
+        while min(len(st) for st in streams) < need:
+            rows = []
+            for b in range(B):
+                on_plan = ok[b] and r < R
+                rows.append(plan[b][r] if on_plan else wrong(streams[b]))
+            forced.copy_(torch.tensor(rows, dtype=torch.int32))
+            g.round(out, forced=forced)
+            com, n = out["committed"].cpu().numpy(), out["n_accepted"].cpu().numpy()
+            for b in range(B):
+                streams[b] += [int(t) for t in com[b][:n[b] + 1]]
+                if ok[b] and r < R and n[b] < 7:
+                    ok[b] = False  # rejected: keep the correction, continue token by token
+            r += 1
+        g.close()
+        del g
+        torch.cuda.empty_cache()
+        return streams, all(ok)
+
+    def to_plan(streams):
+        return [[streams[b][8 * r + 1: 8 * r + 8] for r in range(R)] for b in range(B)]
+
+    streams, _ = run(None)
+    iters, converged = 0, False
+    while iters < max_iter and not converged:
+        iters += 1
+        streams, converged = run(to_plan(streams))
+    plan = torch.tensor([[to_plan(streams)[b][r] for b in range(B)] for r in range(R)],
+                        dtype=torch.int32, device="cuda")
     g2 = DmtpRound(cfg, weights, prompts, max_ctx)
     stream = g2.stream
     for r in range(warmup):
@@ -253,7 +289,9 @@ def forced_accept(cfg, weights, prompts, warmup, steps):
     rps = steps / (ms / 1e3)
     return {"rounds_per_s": rps, "mean_accept_len": mean_len, "tokens_per_s": B * rps * mean_len,
             "steps": steps, "warmup": warmup, "acceptance": acceptance(dh),
-            "drafts": "forced to the target's own greedy continuation (every draft accepted)"}
+            "plan_refinements": iters, "plan_converged": converged,
+            "drafts": "forced to the target's own greedy continuation as the replayed rounds "
+                      "compute it (every draft accepted)"}
 
 
 def fp8_draft_heads(cfg, weights, prompts, warmup, steps):
@@ -284,9 +322,56 @@ def fp8_draft_heads(cfg, weights, prompts, warmup, steps):
     rps = steps / (ms / 1e3)
     return {"rounds_per_s": rps, "ms_per_step": ms / steps, "mean_accept_len": mean_len,
             "tokens_per_s": len(prompts) * rps * mean_len, "steps": steps, "warmup": warmup,
-            "lm_head_ms_per_round": prof["lm_head"]["ms"],
+            "lm_head_ms_per_round": class_ms(prof, ms / steps, "lm_head"),
             "note": "T1 and drafter heads read an E4M3 copy of the vocabulary matrix "
                     "(per-row power-of-two scales); the verify head stays bf16"}
+
+
+def draft_list_round(cfg, weights, prompts, warmup, steps, size=16000):
+    """The same workload with the T1 and drafter heads over the colibri page's frequent-
+    token list (dmtp_set_draft_list; the verify head still scores every token): the list
+    is the native list (dmtp_vocab.h) after the batch's prompts (one list per batch: the
+    16000 most counted tokens, the three-quarters rule and every token of the
+    conversation) and the pending tokens, set once before the timed rounds (no upkeep
+    inside them); natural rounds, graph replayed, timed like the headline."""
+    import torch
+    from mtp_block_draft_gb300 import DmtpRound, DmtpVocabList
+    cl = cfg.replace(draft_list_cap=cfg.vocab)
+    R = warmup + steps
+    g = DmtpRound(cl, weights, prompts, max(len(p) for p in prompts) + 8 * R + 64)
+    vl = DmtpVocabList(cfg.vocab, size)
+    vl.begin_request(np.concatenate(prompts))
+    _, A, _ = g.read_state()
+    vl.picked(A)
+    ids = vl.ids()
+    g.set_draft_list(ids)
+    vl.close()
+    for _ in range(warmup):
+        g.round()
+    _, _, h0 = g.read_state()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(g.stream)
+    for _ in range(steps):
+        g.round()
+    e1.record(g.stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    _, _, h1 = g.read_state()
+    prof = g.profile_round()
+    g.close()
+    dh = (h1 - h0).astype(np.int64)
+    mean_len = float(np.sum((np.arange(8) + 1) * dh)) / max(1, int(dh.sum()))
+    rps = steps / (ms / 1e3)
+    return {"listed_tokens": int(len(ids)), "vocab": cfg.vocab, "rounds_per_s": rps,
+            "ms_per_step": ms / steps, "mean_accept_len": mean_len,
+            "tokens_per_s": len(prompts) * rps * mean_len, "steps": steps, "warmup": warmup,
+            "lm_head_ms_per_round": class_ms(prof, ms / steps, "lm_head"),
+            "lm_head_GB_per_round": prof["lm_head"]["bytes"] / 1e9,
+            "note": "T1 and drafter heads over the listed rows (a compact copy in the "
+                    "workspace); the verify head scores the whole vocabulary. With uniform "
+                    "random prompts the conversation alone lists most of the batch's prompt "
+                    "tokens"}
 
 
 def hybrid_round(warmup, steps, hbm_gbs):
@@ -321,7 +406,8 @@ def hybrid_round(warmup, steps, hbm_gbs):
     dh = (h1 - h0).astype(np.int64)
     mean_len = float(np.sum((np.arange(8) + 1) * dh)) / max(1, int(dh.sum()))
     rps = steps / (ms / 1e3)
-    gdn = prof["gdn"]
+    gdn = dict(prof["gdn"])
+    gdn["ms"] = class_ms(prof, ms / steps, "gdn")
     gdn_gbs = gdn["bytes"] / max(1e-12, gdn["ms"] / 1e3) / 1e9
     return {"workload": f"hybrid: B{len(prompts)}, {cfg.n_layers} layers "
                         f"({sum(cfg.layer_kinds)} Gated DeltaNet, H {cfg.gdn_heads}, "
@@ -332,6 +418,15 @@ def hybrid_round(warmup, steps, hbm_gbs):
                     "launches": int(gdn["launches"]), "GB/s": gdn_gbs,
                     "frac_of_hbm": gdn_gbs / hbm_gbs},
             "prefill_tokens_per_s": pf_tokens / (pf_ms / 1e3) if pf_ms > 0 else None}
+
+
+def class_ms(prof: dict, timed_round_ms: float, cls: str) -> float:
+    """A class's time in one profiled round (dmtp_round_profile), less the event-node cost
+    per launch: (profiled round - timed round) / launches, as for the main line."""
+    names = ("gemm", "lm_head", "attention", "gdn", "other")
+    n = sum(prof[c]["launches"] for c in names)
+    cost = max(0.0, prof["round_ms"] - timed_round_ms) / max(1, n)
+    return max(0.0, prof[cls]["ms"] - prof[cls]["launches"] * cost)
 
 
 def workload_name(cfg, B):
@@ -388,6 +483,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="b32")
+    ap.add_argument("--repeats", type=int, default=5,
+                    help="repeats of the timed K-step loop (at least; more while the timed "
+                         "region is shorter than ~1 s); the headline is their median")
+    ap.add_argument("--max-repeats", type=int, default=40)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--profile-rounds", type=int, default=3)
     ap.add_argument("--cpu-rounds", type=int, default=3)
@@ -396,6 +495,9 @@ def main():
                     help="timed rounds of the forced-accept run (0: skip)")
     ap.add_argument("--fp8-steps", type=int, default=100,
                     help="timed rounds of the run with E4M3 draft heads (0: skip)")
+    ap.add_argument("--list-steps", type=int, default=100,
+                    help="timed rounds of the run with the draft heads over the token list "
+                         "(0: skip)")
     ap.add_argument("--temperature", type=float, default=0.0,
                     help="0: greedy verification (the workloads' setting); > 0: target-only "
                          "sampled verification at this temperature")
@@ -412,7 +514,9 @@ def main():
     from synth import CONFIGS
     cfg = CONFIGS[args.config]
     if args.layers is not None:
-        cfg = cfg.replace(name=f"{cfg.name}-L{args.layers}", n_layers=args.layers)
+        kinds = tuple(cfg.layer_kinds[:args.layers]) if cfg.has_gdn else ()
+        cfg = cfg.replace(name=f"{cfg.name}-L{args.layers}", n_layers=args.layers,
+                          layer_kinds=kinds)
     if args.ctx is not None:
         cfg = cfg.replace(name=f"{cfg.name}-ctx{args.ctx[0]}-{args.ctx[1]}", ctx_lo=args.ctx[0],
                           ctx_hi=args.ctx[1])
@@ -437,38 +541,56 @@ def main():
     pcfg = rank_config(cfg, rank)
     prompts = make_prompts(pcfg)
     B = len(prompts)
-    total_rounds = args.warmup + args.steps + args.e2e_steps + args.profile_rounds + 8
+    max_reps = max(args.repeats, min(args.max_repeats, max(args.repeats, 2000 // args.steps)))
+    total_rounds = (args.warmup + max_reps * args.steps + args.e2e_steps + args.profile_rounds
+                    + 8)
     max_ctx = max(len(p) for p in prompts) + 8 * total_rounds + 32
     g = DmtpRound(cfg, weights, prompts, max_ctx)
     stream = g.stream
 
-    for _ in range(args.warmup):
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    for i in range(args.warmup):
+        if i == args.warmup - 2:
+            e0.record(stream)
         g.round()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    est_ms = max(1e-3, e0.elapsed_time(e1) / 2)  # the last two warm-up rounds
+    # Repeats of the K-step loop: at least args.repeats, and enough that the timed region
+    # lasts about a second, so the 200 ms clock sampler sees it (K = 20 rounds of 3 ms are
+    # shorter than one sample); the headline is the median repeat.
+    reps = int(min(max_reps, max(args.repeats, np.ceil(1000.0 / (args.steps * est_ms)))))
+    if world > 1:  # every rank runs the same number of repeats
+        r = torch.tensor([reps], dtype=torch.int64, device=dev)
+        dist.all_reduce(r, op=dist.ReduceOp.MAX)
+        reps = int(r.item())
     _, _, h0 = g.read_state()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     clocks = Clocks(local)
     clocks.ready()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
     # the profiler start/stop marks let an external profiler skip the prefill
     torch.cuda.cudart().cudaProfilerStart()
-    e0.record(stream)
-    for _ in range(args.steps):
-        g.round()
-    e1.record(stream)
+    ev[0].record(stream)
+    for r in range(reps):
+        for _ in range(args.steps):
+            g.round()
+        ev[r + 1].record(stream)
     torch.cuda.synchronize()
     torch.cuda.cudart().cudaProfilerStop()
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1)
+    rep_ms = [ev[r].elapsed_time(ev[r + 1]) for r in range(reps)]
+    ms = float(statistics.median(rep_ms))  # K steps
     _, _, h1 = g.read_state()
     dh = (h1 - h0).astype(np.int64)
-    tokens = int(np.sum((np.arange(8) + 1) * dh))
     seq_rounds = int(dh.sum())  # one histogram entry per sequence per round
-    mean_len = tokens / max(1, seq_rounds)
+    mean_len = float(np.sum((np.arange(8) + 1) * dh)) / max(1, seq_rounds)
+    tokens = B * args.steps * mean_len  # committed tokens of K steps at the mean length
 
     # e2e through the C ABI with host outputs (pinned), wall clock
     committed = torch.empty((B, 8), dtype=torch.int32, pin_memory=True).numpy()
@@ -484,12 +606,24 @@ def main():
     value = tok_all / (ms_all / 1e3)
     e2e_val = e2e_tok_all / e2e_s_all
 
-    # per-kernel-class profile of real rounds (events around each launch)
+    # per-kernel-class profile of real rounds: each round a captured graph with event nodes
+    # between its launches (dmtp_round_profile), so class times add up to the round
     hbm, tc_burst, tc_sus, peak_src = _peaks()
     prof = [g.profile_round() for _ in range(args.profile_rounds)]
     classes = ("gemm", "lm_head", "attention", "gdn", "other")
-    agg = {c: {k: sum(p[c][k] for p in prof) / len(prof) for k in ("ms", "bytes", "flops", "launches")}
+    agg = {c: {k: sum(p[c][k] for p in prof) / len(prof)
+               for k in ("ms", "bytes", "impl_bytes", "flops", "launches")}
            for c in classes}
+    # Each event node between launches costs a few microseconds of its own (the profiled
+    # graph runs longer than the timed one). That cost, the same for every launch, is
+    # (profiled round - timed round) / launches; it is taken off each launch, so the
+    # classes add up to the timed round. The raw event times are reported beside.
+    prof_round_ms = sum(p["round_ms"] for p in prof) / len(prof)
+    n_launch = sum(agg[c]["launches"] for c in classes)
+    ev_cost = max(0.0, prof_round_ms - ms / args.steps) / max(1.0, n_launch)
+    for c in classes:
+        agg[c]["ms_events"] = agg[c]["ms"]
+        agg[c]["ms"] = max(0.0, agg[c]["ms"] - agg[c]["launches"] * ev_cost)
     dom = max(classes, key=lambda c: agg[c]["ms"] if c != "other" else -1)
     a = agg[dom]
     launches = max(1.0, a["launches"])
@@ -503,21 +637,37 @@ def main():
                 "frac": tfs / tc_sus}
     else:
         roof = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm}
-    traffic, tsrc = _traffic(dom, a["bytes"] / launches)
+    traffic, tsrc = _traffic(dom, a["bytes"] / launches, a["impl_bytes"] / launches)
     roof.update({"kernel": dom, "traffic": traffic, "traffic_source": tsrc,
                  "peak_source": f"{peak_src} (MEASURED_PEAKS.json)"
                  if peak_src == "measured" else "fallback (profiling recipe)",
-                 "per_launch_bytes": a["bytes"] / launches})
+                 "per_launch_bytes": a["bytes"] / launches,
+                 "per_launch_impl_bytes": a["impl_bytes"] / launches,
+                 "timing": ("graph replay with event nodes between launches"
+                            if all(p["graph"] for p in prof) else
+                            "eager round, events between launches") +
+                           f", less {ev_cost * 1e3:.2f} us of event cost per launch",
+                 "achieved_with_event_cost": a["bytes"] / launches /
+                 (a["ms_events"] / 1e3 / launches) / 1e9})
     breakdown = {c: {"ms_per_round": round(agg[c]["ms"], 4),
+                     "ms_per_round_with_event_cost": round(agg[c]["ms_events"], 4),
                      "GB_per_round": round(agg[c]["bytes"] / 1e9, 4),
+                     "impl_GB_per_round": round(agg[c]["impl_bytes"] / 1e9, 4),
+                     "TFLOP_per_round": round(agg[c]["flops"] / 1e12, 4),
                      "launches": int(agg[c]["launches"]),
-                     "GB/s": round(agg[c]["bytes"] / max(1e-12, agg[c]["ms"] / 1e3) / 1e9, 1)}
+                     "GB/s": round(agg[c]["bytes"] / max(1e-12, agg[c]["ms"] / 1e3) / 1e9, 1),
+                     "frac_of_hbm": round(agg[c]["bytes"] / max(1e-12, agg[c]["ms"] / 1e3)
+                                          / 1e9 / hbm, 4)}
                  for c in classes}
-    prof_round_ms = sum(p["round_ms"] for p in prof) / len(prof)
+    breakdown["gemm"]["frac_of_tensor_sustained"] = round(
+        agg["gemm"]["flops"] / max(1e-12, agg["gemm"]["ms"] / 1e3) / 1e12 / tc_sus, 4)
+    breakdown["event_cost_us_per_launch"] = round(ev_cost * 1e3, 3)
     alg_bytes = sum(agg[c]["bytes"] for c in classes)
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_all / args.steps,
+            "repeats": {"n": reps, "statistic": "median",
+                        "ms_per_step": [round(x / args.steps, 5) for x in rep_ms]},
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded random weights N(0,0.02) and uniform prompt ids)",
             "config": {"workload": workload_name(cfg, B),
@@ -530,7 +680,9 @@ def main():
             "clocks": clk,
             "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": B * 8 * 4 + B * 4},
-            "gpu_launches": g.launches_per_round() * args.steps,
+            "gpu_launches": g.launches_per_round() * args.steps * reps,
+            "gpu_launches_note": f"launches in the timed region: {reps} repeats of "
+                                 f"{args.steps} rounds",
             "acceptance": acceptance(dh),
             "roofline": roof,
             "round_roofline": {"algorithmic_GB": alg_bytes / 1e9,
@@ -555,6 +707,8 @@ def main():
         line["forced_accept"] = forced_accept(cfg, weights, prompts, 4, args.forced_steps)
     if args.fp8_steps > 0 and world == 1 and cfg.dtype == "bf16" and cfg.d_model % 128 == 0:
         line["fp8_draft_heads"] = fp8_draft_heads(cfg, weights, prompts, 16, args.fp8_steps)
+    if args.list_steps > 0 and world == 1 and cfg.dtype == "bf16":
+        line["draft_list"] = draft_list_round(cfg, weights, prompts, 16, args.list_steps)
     if args.hybrid_steps > 0 and world == 1 and args.config == "b32" and args.layers is None:
         try:
             line["hybrid"] = hybrid_round(5, args.hybrid_steps, hbm)

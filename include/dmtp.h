@@ -76,7 +76,10 @@ extern "C" {
  * integer with max|row| <= 448 s, and q = round-to-nearest-even(row / s); each head input
  * row (the normalised hidden) is quantised the same way, and the draft logits are
  * s_x s_v (q_x . q_v). The verify head stays bf16, so the committed tokens do not
- * change; only the drafts (and so the acceptance) can. */
+ * change; only the drafts (and so the acceptance) can.
+ * draft_list_cap (bf16 models only; 0: off): capacity, in tokens, of the draft heads'
+ * token list (dmtp_set_draft_list); the workspace then holds a compact copy of that many
+ * head rows (bf16, or E4M3 with draft_head_fp8) and their ids. */
 typedef struct {
   int vocab, d_model, n_layers, n_heads, n_kv_heads, head_dim, ffn;
   int gdn_heads, gdn_dk, gdn_dv;
@@ -91,6 +94,7 @@ typedef struct {
   float temperature;
   uint64_t sample_seed;
   int draft_head_fp8;
+  int draft_list_cap;
 } dmtp_config;
 
 /* One decoder layer, row-major [out, in] device matrices of the config's dtype.
@@ -163,6 +167,21 @@ int dmtp_round(dmtp_ctx* ctx, const dmtp_round_out* out, const int32_t* forced_d
  * n_accepted [B] (either may be NULL) into host memory and synchronise. */
 int dmtp_round_host(dmtp_ctx* ctx, int32_t* committed_host, int32_t* n_accepted_host);
 
+/* Draft heads over a token list (the colibri speculative-decoding page's frequent-token
+ * list: the draft heads may score a list of tokens in place of the vocabulary, while the
+ * verification scores every token; DMTP blog §6.5 names the LM head as the cost to cut).
+ * From the next round on, T1 and the drafter's T2..T7 are the argmax of their logits over
+ * the listed tokens only (the lowest id on exact ties); the verify head, and so every
+ * committed token, is unchanged. ids: host int32, n strictly increasing token ids in
+ * [0, vocab), 1 <= n <= draft_list_cap; n = 0 turns the list off (full heads again).
+ * The call copies ids to the device and gathers the listed head rows into the
+ * workspace's compact copy, enqueued on the context's stream (the ids array may be reused
+ * on return). Upkeep of the list (counts, halvings, joined picks) is the caller's, e.g.
+ * dmtp_vocab.h. Debug logits of the draft heads are then written at the listed ids only.
+ * Returns DMTP_EINVAL (bad ids or n, or a context made with draft_list_cap 0),
+ * DMTP_ESTATE on a poisoned context, DMTP_ECUDA if a copy or launch fails. */
+int dmtp_set_draft_list(dmtp_ctx* ctx, const int32_t* ids, int n);
+
 /* Synchronise and read the state: kv_len [B], pending token A [B] (host arrays, each
  * may be NULL) and the acceptance histogram hist[k] = rounds that accepted k drafts
  * (host uint64 [8], may be NULL). Also reports DMTP_EDEVICE if a device check fired. */
@@ -184,19 +203,26 @@ int dmtp_prefill_stats(const dmtp_ctx* ctx, double* ms, int64_t* tokens);
 #define DMTP_PROF_GDN 3    /* Gated DeltaNet recurrence with snapshots             */
 #define DMTP_PROF_OTHER 4  /* norms, RoPE/KV writes, gathers, accept                */
 
-/* Per-class device time and algorithmic traffic of one round. ms: summed CUDA-event
- * durations of the class's launches (events recorded on the context's stream around
- * each launch); bytes/flops: what those launches must move/compute (weights and
- * tokens read once, visible K/V read once per sequence and layer, recurrent state
- * read once and written per snapshot); round_ms: the whole profiled round. */
+/* Per-class device time and traffic of one round. ms: summed durations of the class's
+ * launches, launch i lasting from the CUDA event recorded before it to the one recorded
+ * before the next launch (so the classes add up to round_ms); bytes/flops: what those
+ * launches must move/compute by the method (weights once; a projection's input and
+ * output rows once in the storage type; visible K/V once per sequence and layer;
+ * recurrent state read once and written per snapshot); impl_bytes: what the
+ * implementation moves instead (both halves of a split GEMM operand, fp32 accumulator
+ * reads and writes); round_ms: the whole profiled round; graph: 1 if the round ran as a
+ * captured CUDA graph with the events as graph nodes (launch gaps as in dmtp_round's
+ * graph), 0 if it ran eagerly (host launch gaps included). */
 typedef struct {
-  double ms[8], bytes[8], flops[8];
+  double ms[8], bytes[8], flops[8], impl_bytes[8];
   int launches[8];
   double round_ms;
+  int graph;
 } dmtp_profile;
 
-/* Run one real round (state advances as with dmtp_round) uncaptured, with CUDA events
- * around every launch, synchronise and fill *out. For measurement, not for speed. */
+/* Run one real round (state advances as with dmtp_round) as a freshly captured graph with
+ * event nodes between its launches (eagerly if the capture fails), synchronise and fill
+ * *out. For measurement, not for speed. */
 int dmtp_round_profile(dmtp_ctx* ctx, dmtp_profile* out);
 
 /* First-candidate head without any allocation (the pages have no counterpart; this

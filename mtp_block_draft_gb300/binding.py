@@ -27,7 +27,7 @@ ERRORS = {0: "DMTP_OK", -1: "DMTP_EINVAL", -2: "DMTP_ENOMEM", -3: "DMTP_ECAPACIT
 EXPORTS = ("dmtp_workspace_size", "dmtp_init", "dmtp_round", "dmtp_round_host",
            "dmtp_read_state", "dmtp_round_launches", "dmtp_round_profile", "dmtp_free",
            "dmtp_strerror", "dmtp_t1_head_noalloc", "dmtp_prefill_stats",
-           "dmtp_selftest_timeout",
+           "dmtp_selftest_timeout", "dmtp_set_draft_list",
            "dmtp_gate_create", "dmtp_gate_forward", "dmtp_gate_draft_cost",
            "dmtp_gate_result", "dmtp_gate_pick", "dmtp_gate_pick_p", "dmtp_gate_read",
            "dmtp_gate_free", "dmtp_vocab_create", "dmtp_vocab_begin_request",
@@ -50,7 +50,8 @@ class dmtp_config(C.Structure):
                 ("tap_layers", C.c_int * DMTP_MAX_TAPS), ("mask_id", C.c_int),
                 ("rms_eps", C.c_float), ("rope_theta", C.c_float), ("max_ctx", C.c_int),
                 ("max_batch", C.c_int), ("dtype", C.c_int), ("temperature", C.c_float),
-                ("sample_seed", C.c_uint64), ("draft_head_fp8", C.c_int)]
+                ("sample_seed", C.c_uint64), ("draft_head_fp8", C.c_int),
+                ("draft_list_cap", C.c_int)]
 
 
 _LAYER_FIELDS = ("attn_norm", "wqkv", "wo", "gdn_wqkv", "gdn_wa", "gdn_wb", "gdn_wo",
@@ -96,7 +97,8 @@ class dmtp_vocab_stats(C.Structure):
 
 class dmtp_profile(C.Structure):
     _fields_ = [("ms", C.c_double * 8), ("bytes", C.c_double * 8), ("flops", C.c_double * 8),
-                ("launches", C.c_int * 8), ("round_ms", C.c_double)]
+                ("impl_bytes", C.c_double * 8), ("launches", C.c_int * 8),
+                ("round_ms", C.c_double), ("graph", C.c_int)]
 
 
 _lib = None
@@ -128,6 +130,8 @@ def load_library(path: str = LIB_PATH):
     lib.dmtp_prefill_stats.restype = C.c_int
     lib.dmtp_round_profile.argtypes = [P, C.POINTER(dmtp_profile)]
     lib.dmtp_round_profile.restype = C.c_int
+    lib.dmtp_set_draft_list.argtypes = [P, P, C.c_int]
+    lib.dmtp_set_draft_list.restype = C.c_int
     lib.dmtp_selftest_timeout.argtypes = [P, C.c_uint64]
     lib.dmtp_selftest_timeout.restype = C.c_int
     lib.dmtp_free.argtypes = [P]
@@ -196,6 +200,7 @@ def make_config(cfg, max_ctx: int, max_batch: int | None = None) -> dmtp_config:
     c.temperature = cfg.temperature
     c.sample_seed = cfg.sample_seed
     c.draft_head_fp8 = 1 if cfg.draft_head_fp8 else 0
+    c.draft_list_cap = int(getattr(cfg, "draft_list_cap", 0))
     return c
 
 
@@ -309,10 +314,10 @@ class DmtpRound:
         summed device ms, algorithmic bytes and flops, and the launch count."""
         p = dmtp_profile()
         _check(self.lib.dmtp_round_profile(self.ctx, C.byref(p)), "dmtp_round_profile")
-        out = {"round_ms": p.round_ms}
+        out = {"round_ms": p.round_ms, "graph": bool(p.graph)}
         for i, name in enumerate(PROFILE_CLASSES):
             out[name] = {"ms": p.ms[i], "bytes": p.bytes[i], "flops": p.flops[i],
-                         "launches": p.launches[i]}
+                         "impl_bytes": p.impl_bytes[i], "launches": p.launches[i]}
         return out
 
     def prefill_stats(self) -> tuple[float, int]:
@@ -322,6 +327,13 @@ class DmtpRound:
         _check(self.lib.dmtp_prefill_stats(self.ctx, C.byref(ms), C.byref(tok)),
                "dmtp_prefill_stats")
         return ms.value, tok.value
+
+    def set_draft_list(self, ids):
+        """dmtp_set_draft_list: the draft heads score only these (strictly increasing)
+        token ids from the next round on; an empty list turns it off."""
+        a = np.ascontiguousarray(np.asarray(ids, dtype=np.int32).reshape(-1))
+        _check(self.lib.dmtp_set_draft_list(self.ctx, a.ctypes.data if a.size else None,
+                                            int(a.size)), "dmtp_set_draft_list")
 
     def selftest_timeout(self, limit_ns: int):
         """dmtp_selftest_timeout: a bounded device wait that gives up after limit_ns."""

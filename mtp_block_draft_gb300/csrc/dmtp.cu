@@ -96,6 +96,14 @@ struct dmtp_ctx {
   void *t1q, *dnq;
   float *t1qs, *dnqs;
   bool fp8;
+  // draft heads over a token list: compact head rows (bf16, or E4M3 with scales), their
+  // token ids, and the listed count on the device
+  int list_cap;
+  void* hc;
+  float* hcs;
+  int* hc_ids;
+  int* hc_n;
+  int list_n;  // listed tokens as last set (0: the list is off)
   float* hlast;
   int* prompts;
   int2* psched;  // prefill schedule: (sequence, chunk) of each row group of each step
@@ -111,6 +119,7 @@ struct dmtp_ctx {
   Gemm dkv[DMTP_MAX_DRAFT_LAYERS];
   Gemm fuse, head_t1, head_d, head_v, dfc, mproj;
   Gemm head_a;  // A after the prompt: the target's own (bf16) head on the T1 input rows
+  Gemm head_t1l, head_dl;  // the T1 and drafter heads over the token list
 
   cudaGraphExec_t graph;         // the round
   cudaGraphExec_t graph_forced;  // the round with drafts read from `forced`
@@ -123,9 +132,10 @@ struct dmtp_ctx {
   long prefill_tokens;   // prompt tokens it processed
   // per-launch event profiling (dmtp_round_profile only)
   bool prof;
+  bool prof_external;  // the events are recorded inside a stream capture (graph nodes)
   std::vector<cudaEvent_t> pev;
   std::vector<int> pcls;
-  std::vector<double> pbytes, pflops;
+  std::vector<double> pbytes, pflops, pimpl;
   std::vector<int> kv_host;  // kv_len at the start of the profiled round
 };
 
@@ -157,7 +167,8 @@ int derive(dmtp_ctx* c, const dmtp_config* cfg, int B) {
       f.draft_window < 0 || !(f.temperature == 0.f || (f.temperature >= 1e-4f &&
                                                         f.temperature <= 3.0e38f)) ||
       (f.draft_head_fp8 != 0 && f.draft_head_fp8 != 1) ||
-      (f.draft_head_fp8 && (f.dtype != 1 || f.d_model % 128)))
+      (f.draft_head_fp8 && (f.dtype != 1 || f.d_model % 128)) || f.draft_list_cap < 0 ||
+      f.draft_list_cap > f.vocab || (f.draft_list_cap > 0 && f.dtype != 1))
     return DMTP_EINVAL;
   const int grp = f.n_heads / f.n_kv_heads;
   const int QN = 8 * grp;
@@ -169,6 +180,7 @@ int derive(dmtp_ctx* c, const dmtp_config* cfg, int B) {
   c->M = 8 * B;
   c->dt = f.dtype;
   c->fp8 = f.draft_head_fp8 != 0;
+  c->list_cap = f.draft_list_cap;
   c->d = f.d_model;
   c->V = f.vocab;
   c->F = f.ffn;
@@ -287,6 +299,16 @@ size_t layout(dmtp_ctx* c, char* base) {
     c->dnq = b.take<char>((size_t)6 * B * d);
     c->dnqs = b.take<float>((size_t)6 * B * 4);
   }
+  c->hc = nullptr;
+  c->hcs = nullptr;
+  c->hc_ids = c->hc_n = nullptr;
+  if (c->list_cap) {
+    const size_t cpad = ((size_t)c->list_cap + 255) / 256 * 256;  // scales read tile-wide
+    c->hc = b.take<char>(cpad * d * (c->fp8 ? 1 : 2));
+    if (c->fp8) c->hcs = b.take<float>(cpad * 4);
+    c->hc_ids = b.take<int>(cpad * 4);
+    c->hc_n = b.take<int>(4);
+  }
   c->hlast = b.take<float>(B * d * 4);
   c->forced = b.take<int>(B * 7 * 4);
   RoundState& s = c->rs;
@@ -377,23 +399,29 @@ int plan_layer(dmtp_ctx* c, LayerPlans& p, const dmtp_layer_weights& w, int kind
 // ---------------------------------------------------------------------------------
 enum { P_GEMM = 0, P_HEAD = 1, P_ATTN = 2, P_GDN = 3, P_OTHER = 4 };
 
-// Wraps one launch: counts it and, when profiling, brackets it with CUDA events on
-// the launching stream and records its class and algorithmic bytes / flops.
+// Profiling events: one before every launch and one after the last, so launch i takes
+// the time between event i and event i + 1 and the launches' times add up to the round.
+// Inside a stream capture they become event-record nodes of the graph.
+inline void prof_event(dmtp_ctx* c, size_t i) {
+  if (c->prof_external)
+    cudaEventRecordWithFlags(c->pev[i], c->st, cudaEventRecordExternal);
+  else
+    cudaEventRecord(c->pev[i], c->st);
+}
+
+// Wraps one launch: counts it and, when profiling, records the event before it, its
+// class, its algorithmic (method) bytes and flops, and the bytes the implementation moves
+// (impl: e.g. the second bf16 half of a split operand and fp32 accumulator traffic).
 template <typename F>
-inline void launch(dmtp_ctx* c, int cls, double bytes, double flops, F&& f) {
-  if (c->prof) {
-    const size_t i = c->pcls.size();
-    while (c->pev.size() < 2 * (i + 1)) {
-      cudaEvent_t e;
-      cudaEventCreate(&e);
-      c->pev.push_back(e);
-    }
-    cudaEventRecord(c->pev[2 * i], c->st);
+inline void launch(dmtp_ctx* c, int cls, double bytes, double flops, F&& f,
+                   double impl = -1.0) {
+  if (c->prof && c->pcls.size() + 1 < c->pev.size()) {
+    prof_event(c, c->pcls.size());
     f();
-    cudaEventRecord(c->pev[2 * i + 1], c->st);
     c->pcls.push_back(cls);
     c->pbytes.push_back(bytes);
     c->pflops.push_back(flops);
+    c->pimpl.push_back(impl < 0 ? bytes : impl);
   } else {
     f();
   }
@@ -402,16 +430,19 @@ inline void launch(dmtp_ctx* c, int cls, double bytes, double flops, F&& f) {
 
 inline double esz(const dmtp_ctx* c) { return c->dt ? 2.0 : 4.0; }
 
-// algorithmic bytes of out[M,N] (+)= X[M,K] W[N,K]^T: weights and tokens read once,
-// the fp32 output read and written once
+// out[M,N] (+)= X[M,K] W[N,K]^T. Method bytes: the weights, the input rows and the output
+// rows once each in the storage type. Implementation bytes: the weights, both halves of
+// a split operand, and the fp32 output read and written.
 void gemm_acc(dmtp_ctx* c, const Gemm& g, float* out, int ldo) {
-  const double bytes = ((double)g.N * g.K + (double)g.M * g.K) * esz(c) + 8.0 * g.M * g.N;
+  const double bytes = ((double)g.N * g.K + (double)g.M * g.K + (double)g.M * g.N) * esz(c);
+  const double impl = ((double)g.N * g.K + (double)g.M * g.K * (g.split && c->dt ? 2 : 1)) *
+                          esz(c) + 8.0 * g.M * g.N;
   launch(c, P_GEMM, bytes, 2.0 * g.M * g.N * g.K, [&] {
     if (c->dt == 1)
       op_gemm_tc_acc(g.tc, out, ldo, c->err, c->st);
     else
       op_gemm_simt_acc((const float*)g.W, (const float*)g.X, g.N, g.K, g.M, out, ldo, c->st);
-  });
+  }, impl);
 }
 
 // The verify head's sampling: row m = b*8 + j of sequence b at position pos0[b] + j.
@@ -434,11 +465,16 @@ void gemm_argmax(dmtp_ctx* c, const Gemm& g, unsigned long long* keys, float* lo
   });
 }
 
+// Gate/up GEMM with the SwiGLU epilogue: method bytes are the weights, the input rows and
+// the F-wide output rows once; the implementation reads both input halves and writes both
+// output halves.
 void gemm_swiglu(dmtp_ctx* c, const Gemm& g, void* h, long h_lo) {
-  const double bytes = ((double)g.N * g.K + (double)g.M * g.K * 2) * esz(c) +
-                       (double)g.M * (g.N / 2) * esz(c) * 2;
+  const double bytes = ((double)g.N * g.K + (double)g.M * g.K + (double)g.M * (g.N / 2)) *
+                       esz(c);
+  const double impl = ((double)g.N * g.K + (double)g.M * g.K * 2) * esz(c) +
+                      (double)g.M * (g.N / 2) * esz(c) * 2;
   launch(c, P_GEMM, bytes, 2.0 * g.M * g.N * g.K,
-         [&] { op_gemm_tc_swiglu(g.tc, h, h_lo, c->err, c->st); });
+         [&] { op_gemm_tc_swiglu(g.tc, h, h_lo, c->err, c->st); }, impl);
 }
 
 void zero(dmtp_ctx* c, void* p, size_t bytes) { cudaMemsetAsync(p, 0, bytes, c->st); }
@@ -635,8 +671,11 @@ void enqueue_round(dmtp_ctx* c, const Dbg& dbg, const int* forced) {
     launch(c, P_OTHER, 0, 0, [&] { op_rmsnorm_e4m3(c->h_mtp, c->d, c->w.mtp_final_norm, c->t1q, c->d, c->t1qs, B, c->d, c->cfg.rms_eps, RowMap(), c->st); });
   else
     norm(c, c->h_mtp, c->w.mtp_final_norm, c->t1in, nullptr, nullptr, B, RowMap(), false);
-  gemm_argmax(c, c->head_t1, s.keys, dbg.t1);
-  launch(c, P_OTHER, 0, 0, [&] { op_keys_to_ids(s.keys, B, 1, s.drafts, 7, 0, forced, 7, 0, c->st); });
+  // the draft heads score the token list when one is set (dmtp_set_draft_list)
+  const bool listed = c->list_n > 0;
+  const int* lmap = listed ? c->hc_ids : nullptr;
+  gemm_argmax(c, listed ? c->head_t1l : c->head_t1, s.keys, dbg.t1);
+  launch(c, P_OTHER, 0, 0, [&] { op_keys_to_ids(s.keys, B, 1, s.drafts, 7, 0, forced, 7, 0, c->st, lmap); });
   // a2: Delta = W [RMS_e(E(T1)); RMS_m(h_MTP)]; slots [E(A), E(T1)+Delta, E(MASK) x 6]
   ConcatPart pe, pm;
   pe.tok = s.drafts;  // T1 of sequence b is drafts[b*7]
@@ -664,8 +703,8 @@ void enqueue_round(dmtp_ctx* c, const Dbg& dbg, const int* forced) {
     launch(c, P_OTHER, 0, 0, [&] { op_rmsnorm_e4m3(c->x, c->d, c->w.dft_final_norm, c->dnq, c->d, c->dnqs, 6 * B, c->d, c->cfg.rms_eps, m6, c->st); });
   else
     norm(c, c->x, c->w.dft_final_norm, c->dn, nullptr, nullptr, 6 * B, m6, false);
-  gemm_argmax(c, c->head_d, s.keys + B, dbg.dl);
-  launch(c, P_OTHER, 0, 0, [&] { op_keys_to_ids(s.keys + B, B, 6, s.drafts, 7, 1, forced, 7, 1, c->st); });
+  gemm_argmax(c, listed ? c->head_dl : c->head_d, s.keys + B, dbg.dl);
+  launch(c, P_OTHER, 0, 0, [&] { op_keys_to_ids(s.keys + B, B, 6, s.drafts, 7, 1, forced, 7, 1, c->st, lmap); });
   // a4: target verify of [A, T1..T7]
   launch(c, P_OTHER, 0, 0, [&] { op_verify_tokens(s, c->st); });
   target_forward(c, true);
@@ -791,7 +830,7 @@ int autotune(dmtp_ctx* c, const void* flush, size_t flush_bytes) {
   }
   collect(c->mtp, all);
   for (Gemm* g : {&c->fuse, &c->head_t1, &c->head_d, &c->head_v, &c->head_a, &c->dfc,
-                  &c->mproj})
+                  &c->mproj, &c->head_t1l, &c->head_dl})
     all.push_back(g);
   const size_t scratch = (size_t)c->M * 2 * c->F;  // floats of the gate/up accumulator
   cudaEvent_t e0, e1;
@@ -1012,6 +1051,26 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
     pr |= plan(c, c->head_t1, w->head, c->V, c->d, c->t1in, B, true, false);
     pr |= plan(c, c->head_d, w->head, c->V, c->d, c->dn, 6 * B, true, false);
   }
+  if (c->list_cap) {  // the same heads over the compact rows of the token list
+    for (Gemm* g : {&c->head_t1l, &c->head_dl}) {
+      const bool t1 = g == &c->head_t1l;
+      g->argmax = true;
+      g->split = false;
+      g->W = c->hc;
+      g->N = c->list_cap;
+      g->K = c->d;
+      g->M = t1 ? B : 6 * B;
+      if (c->fp8) {
+        g->X = t1 ? c->t1q : c->dnq;
+        pr |= head_plan_e4m3(&g->hp, c->hc, c->hcs, c->list_cap, c->d, g->X,
+                             t1 ? c->t1qs : c->dnqs, g->M, c->nsm, 256, 8) ? DMTP_EINVAL : 0;
+      } else {
+        g->X = t1 ? c->t1in : c->dn;
+        pr |= head_plan(&g->hp, c->hc, c->list_cap, c->d, g->X, g->M, c->nsm, 256, 8)
+                  ? DMTP_EINVAL : 0;
+      }
+    }
+  }
   pr |= plan(c, c->head_a, w->head, c->V, c->d, c->t1in, B, true, false);
   pr |= plan(c, c->head_v, w->head, c->V, c->d, c->hTn, M, true, false);
   pr |= plan(c, c->dfc, w->dft_fc, c->d, c->ntap * c->d, c->taps, M, false);
@@ -1062,6 +1121,13 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
       return r;
     }
   }
+  // the list heads score the first *hc_n compact rows and map rows to ids (after the
+  // tile choice above, which re-plans without them)
+  for (Gemm* g : {&c->head_t1l, &c->head_dl}) {
+    g->hp.vdev = c->hc_n;
+    g->hp.vmap = c->hc_ids;
+  }
+  c->list_n = 0;
   zero(c, c->err, 4);
   zero(c, s.hist, 64);
   zero(c, s.keys, (size_t)B * 16 * 8);
@@ -1292,36 +1358,92 @@ int dmtp_round_profile(dmtp_ctx* c, dmtp_profile* out) {
     return DMTP_ECUDA;
   const int mx = *std::max_element(c->kv_host.begin(), c->kv_host.end());
   if (mx + 16 >= c->maxc) return DMTP_ECAPACITY;
-  cudaEvent_t e0, e1;
-  cudaEventCreate(&e0);
-  cudaEventCreate(&e1);
-  c->prof = true;
-  c->pcls.clear();
-  c->pbytes.clear();
-  c->pflops.clear();
-  c->launches = 0;
-  cudaEventRecord(e0, c->st);
-  enqueue_round(c, Dbg{nullptr, nullptr, nullptr}, nullptr);
-  cudaEventRecord(e1, c->st);
-  c->prof = false;
+  while (c->pev.size() < 2048) {  // more than one round's launches, made before any capture
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return DMTP_ECUDA;
+    c->pev.push_back(e);
+  }
+  auto record = [&]() {
+    c->prof = true;
+    c->pcls.clear();
+    c->pbytes.clear();
+    c->pflops.clear();
+    c->pimpl.clear();
+    c->launches = 0;
+    enqueue_round(c, Dbg{nullptr, nullptr, nullptr}, nullptr);
+    prof_event(c, c->pcls.size());  // after the last launch
+    c->prof = false;
+  };
+  // The round as a CUDA graph with event-record nodes between its launches, replayed once
+  // on the context's stream: launch times as in the timed graph, without host launch gaps.
+  // If the capture fails, the round runs eagerly with the same events.
+  bool graph_ok = false;
+  if (c->cap_st || cudaStreamCreateWithFlags(&c->cap_st, cudaStreamNonBlocking) == cudaSuccess) {
+    cudaStream_t user = c->st;
+    c->st = c->cap_st;
+    c->prof_external = true;
+    cudaGraph_t g = nullptr;
+    cudaGraphExec_t ge = nullptr;
+    if (cudaStreamBeginCapture(c->st, cudaStreamCaptureModeThreadLocal) == cudaSuccess) {
+      record();
+      const cudaError_t ce = cudaStreamEndCapture(c->st, &g);
+      if (ce == cudaSuccess && cudaGraphInstantiate(&ge, g, 0) == cudaSuccess) graph_ok = true;
+    }
+    c->st = user;
+    c->prof_external = false;
+    if (g) cudaGraphDestroy(g);
+    if (graph_ok) {
+      graph_ok = cudaGraphLaunch(ge, c->st) == cudaSuccess;
+      if (!graph_ok) return DMTP_ECUDA;  // nothing of the round ran twice: report and stop
+    }
+    if (ge) cudaGraphExecDestroy(ge);
+    cudaGetLastError();  // a failed capture leaves no sticky error; clear its record
+  }
+  if (!graph_ok) record();
   c->kv_bound = std::max<long>(c->kv_bound, mx) + 8;
   if (cudaStreamSynchronize(c->st) != cudaSuccess) return DMTP_ECUDA;
   memset(out, 0, sizeof(*out));
-  for (size_t i = 0; i < c->pcls.size(); ++i) {
+  const size_t n = c->pcls.size();
+  for (size_t i = 0; i < n; ++i) {
     float ms = 0.f;
-    cudaEventElapsedTime(&ms, c->pev[2 * i], c->pev[2 * i + 1]);
+    if (cudaEventElapsedTime(&ms, c->pev[i], c->pev[i + 1]) != cudaSuccess) return DMTP_ECUDA;
     const int k = c->pcls[i];
     out->ms[k] += ms;
     out->bytes[k] += c->pbytes[i];
+    out->impl_bytes[k] += c->pimpl[i];
     out->flops[k] += c->pflops[i];
     out->launches[k] += 1;
   }
   float tot = 0.f;
-  cudaEventElapsedTime(&tot, e0, e1);
+  if (n && cudaEventElapsedTime(&tot, c->pev[0], c->pev[n]) != cudaSuccess) return DMTP_ECUDA;
   out->round_ms = tot;
-  cudaEventDestroy(e0);
-  cudaEventDestroy(e1);
+  out->graph = graph_ok ? 1 : 0;
   return check_err(c);
+}
+
+int dmtp_set_draft_list(dmtp_ctx* c, const int32_t* ids, int n) {
+  if (!c) return DMTP_EINVAL;
+  if (c->poisoned) return DMTP_ESTATE;
+  if (!c->list_cap || n < 0 || n > c->list_cap || (n > 0 && !ids)) return DMTP_EINVAL;
+  for (int i = 0; i < n; ++i)
+    if (ids[i] < 0 || ids[i] >= c->V || (i > 0 && ids[i] <= ids[i - 1])) return DMTP_EINVAL;
+  if ((n > 0) != (c->list_n > 0)) {  // the heads change: capture the round graphs again
+    if (c->graph) cudaGraphExecDestroy(c->graph);
+    if (c->graph_forced) cudaGraphExecDestroy(c->graph_forced);
+    c->graph = c->graph_forced = nullptr;
+  }
+  c->list_n = n;
+  if (n == 0) return DMTP_OK;
+  // pageable host sources: each copy has left the caller's memory when the call returns
+  if (cudaMemcpyAsync(c->hc_ids, ids, (size_t)n * 4, cudaMemcpyHostToDevice, c->st) !=
+          cudaSuccess ||
+      cudaMemcpyAsync(c->hc_n, &c->list_n, 4, cudaMemcpyHostToDevice, c->st) != cudaSuccess)
+    return DMTP_ECUDA;
+  if (c->fp8)
+    op_gather_rows(c->h8, c->hc, (size_t)c->d, c->hc_ids, n, c->h8s, c->hcs, c->st);
+  else
+    op_gather_rows(c->w.head, c->hc, (size_t)c->d * 2, c->hc_ids, n, nullptr, nullptr, c->st);
+  return cudaGetLastError() == cudaSuccess ? DMTP_OK : DMTP_ECUDA;
 }
 
 int dmtp_selftest_timeout(dmtp_ctx* c, uint64_t limit_ns) {

@@ -590,20 +590,39 @@ void op_round_begin(const RoundState& s, cudaStream_t st) {
 
 __global__ void k_keys_to_ids(const unsigned long long* __restrict__ keys, int B, int per,
                               int* dst, int dst_stride, int dst_off, const int* forced,
-                              int forced_stride, int forced_off) {
+                              int forced_stride, int forced_off, const int* map) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= B * per) return;
   const int b = i / per, j = i % per;
   int id = argmax_key_index(keys[i]);
+  if (map) id = id >= 0 ? map[id] : id;  // a list row -> its token id
   if (forced) id = forced[b * forced_stride + forced_off + j];
   dst[b * dst_stride + dst_off + j] = id;
 }
 
 void op_keys_to_ids(const unsigned long long* keys, int B, int per, int* dst, int dst_stride,
                     int dst_off, const int* forced, int forced_stride, int forced_off,
-                    cudaStream_t st) {
+                    cudaStream_t st, const int* map) {
   k_keys_to_ids<<<cdiv(B * per, 128), 128, 0, st>>>(keys, B, per, dst, dst_stride, dst_off,
-                                                    forced, forced_stride, forced_off);
+                                                    forced, forced_stride, forced_off, map);
+}
+
+// One CTA per listed row: 16-byte copies of the row, and its scale.
+__global__ void k_gather_rows(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                              int row16, const int* __restrict__ ids, const float* src_s,
+                              float* dst_s) {
+  const int i = blockIdx.x;
+  const long r = ids[i];
+  for (int c = threadIdx.x; c < row16; c += blockDim.x)
+    dst[(long)i * row16 + c] = __ldg(src + r * row16 + c);
+  if (dst_s && threadIdx.x == 0) dst_s[i] = src_s[r];
+}
+
+void op_gather_rows(const void* src, void* dst, size_t row_bytes, const int* ids, int n,
+                    const float* src_s, float* dst_s, cudaStream_t st) {
+  if (n < 1) return;
+  k_gather_rows<<<n, 128, 0, st>>>((const uint4*)src, (uint4*)dst, (int)(row_bytes / 16), ids,
+                                   src_s, dst_s);
 }
 
 __global__ void k_verify_tokens(RoundState s) {

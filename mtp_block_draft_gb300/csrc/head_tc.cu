@@ -40,6 +40,8 @@ struct HeadArgs {
   unsigned* err;
   const float* wscale;  // E4M3 operands: per vocabulary row scale (padded past V)
   const float* xscale;  // E4M3 operands: per token row scale
+  const int* vdev;      // token list: rows scored (device, read at launch), else null
+  const int* vmap;      // token list: token id of each row (debug logits), else null
 };
 
 // D[tmem] (+)= A[smem] * B[smem]^T, E4M3 inputs, fp32 accumulate (kind::f8f6f4).
@@ -127,6 +129,10 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = a.K / kBK;
   const uint32_t xbytes = (uint32_t)a.MT * kRowB;
+  // rows scored: the vocabulary, or the first *vdev rows of a token list (same value for
+  // every thread, so every role walks the same tiles)
+  const int V = a.vdev ? max(0, min(a.V, __ldg(a.vdev))) : a.V;
+  const int tiles = a.vdev ? (V + NV - 1) / NV : a.tiles;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
@@ -154,7 +160,7 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
       const uint64_t pw = policy_evict_first(), px = policy_evict_last();
       int it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < a.tiles && ok; t += gridDim.x) {
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % S;
           if (!mbar_wait(smem_u32(&empty[s]), ((it / S) & 1) ^ 1, a.err)) {
@@ -178,7 +184,7 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
       const uint32_t idesc = FP8 ? umma_idesc_e4m3(128, NV) : umma_idesc_bf16(128, NV);
       int it = 0, tl = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < a.tiles && ok; t += gridDim.x, ++tl) {
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++tl) {
         const int buf = tl % NB;
         // the epilogue has drained this buffer's previous tile
         if (!mbar_wait(smem_u32(&acc_empty[buf]), ((tl / NB) & 1) ^ 1, a.err)) break;
@@ -234,12 +240,12 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
       }
     }
     int tl = 0;
-    for (int t = blockIdx.x; t < a.tiles; t += gridDim.x, ++tl) {
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++tl) {
       const int buf = tl % NB;
       if (!mbar_wait(smem_u32(&acc_full[buf]), (tl / NB) & 1, a.err)) break;
       tc_fence_after();
       const int n0 = t * NV;
-      const int lim = a.V - n0;  // valid columns of this tile
+      const int lim = V - n0;  // valid columns of this tile
 #pragma unroll
       for (int h = 0; h < TH; ++h) {
         const uint32_t tb = tmem + buf * ACC + h * NV + ((uint32_t)(q * 32) << 16);
@@ -251,14 +257,15 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
           tmem_wait_ld16(r0);
           reg_fence16(r1);
           if (a.logits && m[h] < a.M) {  // debug copy of the logits
-            float* lp = a.logits + (long)m[h] * a.ldl + n0 + c;
+            float* lr = a.logits + (long)m[h] * a.ldl;
             const float xs = FP8 ? a.xscale[m[h]] : 1.f;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              const float w0 = FP8 ? a.wscale[n0 + c + j] * xs : 1.f;
-              const float w1 = FP8 ? a.wscale[n0 + c + 16 + j] * xs : 1.f;
-              if (c + j < lim) lp[j] = __uint_as_float(r0[j]) * w0;
-              if (c + 16 + j < lim) lp[16 + j] = __uint_as_float(r1[j]) * w1;
+              const int v0 = n0 + c + j, v1 = n0 + c + 16 + j;
+              const float w0 = FP8 ? a.wscale[v0] * xs : 1.f;
+              const float w1 = FP8 ? a.wscale[v1] * xs : 1.f;
+              if (c + j < lim) lr[a.vmap ? a.vmap[v0] : v0] = __uint_as_float(r0[j]) * w0;
+              if (c + 16 + j < lim) lr[a.vmap ? a.vmap[v1] : v1] = __uint_as_float(r1[j]) * w1;
             }
           }
           if (c + 32 <= lim) {
@@ -331,6 +338,7 @@ int plan_common(HeadPlan* p, const void* W, int V, int K, const void* X, int M, 
   p->smem = head_smem(nv, p->TH, st);
   p->fp8 = 0;
   p->wscale = p->xscale = nullptr;
+  p->vdev = p->vmap = nullptr;
   return p->smem > kHeadSmemBudget ? -10 : 0;
 }
 
@@ -387,7 +395,8 @@ void op_head_tc(const HeadPlan& p, unsigned long long* keys, float* logits, long
   // the E4M3 draft heads never sample (only the verify head does)
   const bool sample = !p.fp8 && smp && smp->scale2 > 0.f;
   const HeadArgs a{p.V,  p.K,    p.M,   p.MT, p.stages, p.tiles,
-                   keys, logits, ldl,   sample ? *smp : SampleArgs{}, err, p.wscale, p.xscale};
+                   keys, logits, ldl,   sample ? *smp : SampleArgs{}, err, p.wscale, p.xscale,
+                   p.vdev, p.vmap};
   if (p.NV == 128)
     p.TH == 1 ? launch<128, 1>(p, a, sample, st) : launch<128, 2>(p, a, sample, st);
   else

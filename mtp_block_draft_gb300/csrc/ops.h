@@ -94,10 +94,15 @@ struct RoundState {
   unsigned* err;
 };
 void op_round_begin(const RoundState& s, cudaStream_t st);
-// keys -> ids: dst[b*dst_stride + dst_off + j] = id(keys[b*per + j]) (or forced value)
+// keys -> ids: dst[b*dst_stride + dst_off + j] = id(keys[b*per + j]) (or forced value);
+// map (optional): the key's index is a row of a token list, whose id is map[index]
 void op_keys_to_ids(const unsigned long long* keys, int B, int per, int* dst, int dst_stride,
                     int dst_off, const int* forced, int forced_stride, int forced_off,
-                    cudaStream_t st);
+                    cudaStream_t st, const int* map = nullptr);
+// Token list of the draft heads: dst row i = src row ids[i] (row_bytes each, a multiple of
+// 16, 16-byte aligned rows) for i < n; with scale arrays, dst_s[i] = src_s[ids[i]].
+void op_gather_rows(const void* src, void* dst, size_t row_bytes, const int* ids, int n,
+                    const float* src_s, float* dst_s, cudaStream_t st);
 void op_verify_tokens(const RoundState& s, cudaStream_t st);
 void op_accept(const RoundState& s, cudaStream_t st);
 // h_mtp[b] = x[b*8 + cnt[b]-1]
@@ -241,6 +246,11 @@ struct HeadPlan {
   int fp8;                       // E4M3 operands (draft heads)
   const float *wscale, *xscale;  // E4M3 row scales of W (padded past V) and of X
   size_t smem;
+  // A token list in place of the vocabulary (draft heads): W holds V rows of capacity,
+  // of which the first *vdev (read on the device at launch) are scored; vmap[i] is the
+  // token id of row i, where the debug logits go. Both null: the full vocabulary.
+  const int* vdev;
+  const int* vmap;
 };
 // ew: epilogue warps (4 or 8)
 int head_plan(HeadPlan* p, const void* W, int V, int K, const void* X, int M, int nsm, int nv,

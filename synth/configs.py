@@ -68,6 +68,8 @@ class DmtpConfig:
     sample_seed: int = 0
     # the T1 and drafter heads read an E4M3 copy of the head (bf16 models only)
     draft_head_fp8: bool = False
+    # capacity of the draft heads' token list (0: no list; bf16 models only)
+    draft_list_cap: int = 0
 
     def __post_init__(self):
         if not self.layer_kinds:

@@ -316,3 +316,57 @@ def test_device_timeout_poisons_context():
     kv, _, _ = g2.read_state()
     assert (kv > np.array([len(p) for p in prompts])).all()
     g2.close()
+
+
+# the draft heads over a token list (colibri frequent-token list): a small batch of short
+# prompts, so the list (conversation tokens plus the most counted) is a few hundred of
+# the 5000 tokens and most verify picks join it as they are committed
+B32_RL = B32_R.replace(name="b32_r_list", batch=4, ctx_lo=40, ctx_hi=80, draft_list_cap=5000)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_draft_heads_over_token_list(fp8):
+    """T1 and T2..T7 are the argmax over the listed tokens (dmtp_set_draft_list), the
+    verify still scores every token: lock-step against the oracle's round(draft_list=...)
+    with the list kept by the native list (dmtp_vocab.h), joined picks appended each
+    round; then the list is turned off and the full heads come back."""
+    from lockstep import Lockstep
+    from mtp_block_draft_gb300 import DmtpError, DmtpVocabList
+    cfg = B32_RL.replace(draft_head_fp8=fp8)
+    prompts = make_prompts(cfg)
+    ls = Lockstep(cfg, make_weights(cfg, "cuda"), prompts, rounds=8)
+    vl = DmtpVocabList(cfg.vocab, 100)
+    vl.begin_request(np.concatenate(prompts))
+    _, A, _ = ls.gpu.read_state()
+    vl.picked(A)
+    moved, sizes = 0, []
+    for _ in range(6):
+        ids, mask = vl.ids(), vl.mask()
+        sizes.append(len(ids))
+        ls.gpu.set_draft_list(ids)
+        o, recs = ls.step(tol=TOL, draft_list=mask)
+        for b, rec in recs.items():
+            assert all(mask[t] for t in rec["drafts"])
+            moved += int(not mask[int(np.argmax(rec["t1_logits"]))])
+        vl.picked(np.concatenate([o["committed"][b][:o["n_accepted"][b] + 1]
+                                  for b in range(cfg.batch)]))
+    assert moved > 0 and sizes[0] < cfg.vocab // 4 and sizes[-1] > sizes[0]
+    with pytest.raises(DmtpError) as e:
+        ls.gpu.set_draft_list([5, 5, 7])          # not strictly increasing
+    assert e.value.code == -1
+    with pytest.raises(DmtpError):
+        ls.gpu.set_draft_list([cfg.vocab])        # out of range
+    ls.gpu.set_draft_list([])                    # off: the full heads again
+    ls.step(tol=TOL)
+    ls.close()
+    vl.close()
+
+
+def test_draft_list_needs_capacity():
+    from mtp_block_draft_gb300 import DmtpError, DmtpRound, default_max_ctx
+    prompts = make_prompts(B32_R)
+    g = DmtpRound(B32_R, make_weights(B32_R, "cuda"), prompts, default_max_ctx(prompts, 2))
+    with pytest.raises(DmtpError) as e:
+        g.set_draft_list([1, 2, 3])
+    assert e.value.code == -1
+    g.close()
