@@ -79,7 +79,13 @@ extern "C" {
  * change; only the drafts (and so the acceptance) can.
  * draft_list_cap (bf16 models only; 0: off): capacity, in tokens, of the draft heads'
  * token list (dmtp_set_draft_list); the workspace then holds a compact copy of that many
- * head rows (bf16, or E4M3 with draft_head_fp8) and their ids. */
+ * head rows (bf16, or E4M3 with draft_head_fp8) and their ids.
+ * variable_depth (0 or 1): 1 also builds the GEMM plans of verifies that carry fewer
+ * drafts (dmtp_round_depth with depth 0..6; more work at dmtp_init, no more memory).
+ * draft_confidence (0 or 1; bf16 models): 1 makes the T1 and drafter heads also compute
+ * each draft's confidence, the probability the head gives its own pick over the scores
+ * within 20 of its best, 1 / sum exp(l_v - l_max) over those (the colibri page's
+ * per-step estimate for the draft-depth gate; dmtp_round_out.draft_conf). */
 typedef struct {
   int vocab, d_model, n_layers, n_heads, n_kv_heads, head_dim, ffn;
   int gdn_heads, gdn_dk, gdn_dv;
@@ -95,6 +101,8 @@ typedef struct {
   uint64_t sample_seed;
   int draft_head_fp8;
   int draft_list_cap;
+  int variable_depth;
+  int draft_confidence;
 } dmtp_config;
 
 /* One decoder layer, row-major [out, in] device matrices of the config's dtype.
@@ -131,10 +139,14 @@ typedef struct {
  * [B] (installed snapshot row, -1 for attention-only targets). Float debug fields
  * (fp32): t1_logits [B][V], draft_logits [B][6][V], verify_logits [B][8][V], delta
  * [B][d] (Delta of this round), h_mtp [B][d] (the h_MTP this round started from).
- * Requesting a float debug field runs the round uncaptured (same kernels). */
+ * Requesting a float debug field runs the round uncaptured (same kernels). draft_conf
+ * [B][7] (fp32; a context made with draft_confidence = 1, else DMTP_EINVAL): the
+ * confidence of the heads' own picks for T1..T7 (of the list's tokens when a draft list
+ * is set; forced drafts do not change it); it does not stop the graph. */
 typedef struct {
   int32_t *committed, *n_accepted, *drafts, *picks, *kv_len, *mtp_len, *snap_slot;
   float *t1_logits, *draft_logits, *verify_logits, *delta, *h_mtp;
+  float* draft_conf;
 } dmtp_round_out;
 
 typedef struct dmtp_ctx dmtp_ctx;
@@ -162,6 +174,21 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
  * round eagerly instead. Returns DMTP_ECAPACITY if a sequence might pass
  * max_ctx - 8 (checked on the host before launch). Asynchronous. */
 int dmtp_round(dmtp_ctx* ctx, const dmtp_round_out* out, const int32_t* forced_drafts);
+
+/* A round whose verify carries only the first `depth` drafts (0..7; 7 is dmtp_round):
+ * the colibri speculative-decoding page's draft-depth gate picks how many drafts the
+ * next verify carries, and a verify of k drafts is one forward of the pending token and
+ * its k drafts. The MTP head and the drafter still propose T1..T7 (drafts [B][7]); the
+ * target verifies rows [A, T1..T_depth] only, as B (depth + 1) rows (its GEMMs, attention
+ * and recurrence do that much work); at most `depth` drafts are accepted (n <= depth) and
+ * a recurrent layer keeps the state after row `depth` live, swapping snapshot n in when
+ * n < depth. Outputs as dmtp_round, except picks [B][8] holds g_0..g_depth (-1 after)
+ * and verify_logits holds B (depth + 1) rows of V, sequence-major ([B][depth + 1][V]).
+ * Depths below 7 need a context made with variable_depth = 1 (DMTP_EINVAL otherwise, or
+ * for a depth outside 0..7). Each depth (and forced mode) is captured as its own graph
+ * on first use. */
+int dmtp_round_depth(dmtp_ctx* ctx, const dmtp_round_out* out, const int32_t* forced_drafts,
+                     int depth);
 
 /* One round with host outputs: enqueue the round, copy committed [B][8] and
  * n_accepted [B] (either may be NULL) into host memory and synchronise. */

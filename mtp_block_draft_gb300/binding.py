@@ -27,7 +27,7 @@ ERRORS = {0: "DMTP_OK", -1: "DMTP_EINVAL", -2: "DMTP_ENOMEM", -3: "DMTP_ECAPACIT
 EXPORTS = ("dmtp_workspace_size", "dmtp_init", "dmtp_round", "dmtp_round_host",
            "dmtp_read_state", "dmtp_round_launches", "dmtp_round_profile", "dmtp_free",
            "dmtp_strerror", "dmtp_t1_head_noalloc", "dmtp_prefill_stats",
-           "dmtp_selftest_timeout", "dmtp_set_draft_list",
+           "dmtp_selftest_timeout", "dmtp_set_draft_list", "dmtp_round_depth",
            "dmtp_gate_create", "dmtp_gate_forward", "dmtp_gate_draft_cost",
            "dmtp_gate_result", "dmtp_gate_pick", "dmtp_gate_pick_p", "dmtp_gate_read",
            "dmtp_gate_free", "dmtp_vocab_create", "dmtp_vocab_begin_request",
@@ -51,7 +51,8 @@ class dmtp_config(C.Structure):
                 ("rms_eps", C.c_float), ("rope_theta", C.c_float), ("max_ctx", C.c_int),
                 ("max_batch", C.c_int), ("dtype", C.c_int), ("temperature", C.c_float),
                 ("sample_seed", C.c_uint64), ("draft_head_fp8", C.c_int),
-                ("draft_list_cap", C.c_int)]
+                ("draft_list_cap", C.c_int), ("variable_depth", C.c_int),
+                ("draft_confidence", C.c_int)]
 
 
 _LAYER_FIELDS = ("attn_norm", "wqkv", "wo", "gdn_wqkv", "gdn_wa", "gdn_wb", "gdn_wo",
@@ -74,7 +75,7 @@ class dmtp_weights(C.Structure):
 
 
 _OUT_INT = ("committed", "n_accepted", "drafts", "picks", "kv_len", "mtp_len", "snap_slot")
-_OUT_FLOAT = ("t1_logits", "draft_logits", "verify_logits", "delta", "h_mtp")
+_OUT_FLOAT = ("t1_logits", "draft_logits", "verify_logits", "delta", "h_mtp", "draft_conf")
 
 
 class dmtp_round_out(C.Structure):
@@ -120,6 +121,8 @@ def load_library(path: str = LIB_PATH):
     lib.dmtp_init.restype = C.c_int
     lib.dmtp_round.argtypes = [P, C.POINTER(dmtp_round_out), P]
     lib.dmtp_round.restype = C.c_int
+    lib.dmtp_round_depth.argtypes = [P, C.POINTER(dmtp_round_out), P, C.c_int]
+    lib.dmtp_round_depth.restype = C.c_int
     lib.dmtp_round_host.argtypes = [P, P, P]
     lib.dmtp_round_host.restype = C.c_int
     lib.dmtp_read_state.argtypes = [P, P, P, P]
@@ -201,6 +204,8 @@ def make_config(cfg, max_ctx: int, max_batch: int | None = None) -> dmtp_config:
     c.sample_seed = cfg.sample_seed
     c.draft_head_fp8 = 1 if cfg.draft_head_fp8 else 0
     c.draft_list_cap = int(getattr(cfg, "draft_list_cap", 0))
+    c.variable_depth = 1 if getattr(cfg, "variable_depth", False) else 0
+    c.draft_confidence = 1 if getattr(cfg, "draft_confidence", False) else 0
     return c
 
 
@@ -267,15 +272,20 @@ class DmtpRound:
         self.device = dev
 
     # ---- rounds ----------------------------------------------------------------------
-    def round(self, out: dict | None = None, forced=None):
+    def round(self, out: dict | None = None, forced=None, depth: int = 7):
         """Enqueue one round. out: name -> preallocated CUDA tensor (fields of
-        dmtp_round_out); forced: CUDA int32 [B, 7] or None."""
+        dmtp_round_out); forced: CUDA int32 [B, 7] or None; depth: drafts the verify
+        carries (dmtp_round_depth; 7 is dmtp_round)."""
         o = dmtp_round_out()
         if out:
             for k, t in out.items():
                 setattr(o, k, t.data_ptr())
         f = C.c_void_p(forced.data_ptr()) if forced is not None else None
-        _check(self.lib.dmtp_round(self.ctx, C.byref(o), f), "dmtp_round")
+        if depth == 7:
+            _check(self.lib.dmtp_round(self.ctx, C.byref(o), f), "dmtp_round")
+        else:
+            _check(self.lib.dmtp_round_depth(self.ctx, C.byref(o), f, int(depth)),
+                   "dmtp_round_depth")
 
     def alloc_out(self, ints=True, floats=False):
         import torch
@@ -290,6 +300,8 @@ class DmtpRound:
         if floats:
             fs = {"t1_logits": (B, V), "draft_logits": (B, 6, V), "verify_logits": (B, 8, V),
                   "delta": (B, d), "h_mtp": (B, d)}
+            if getattr(self.cfg, "draft_confidence", False):
+                fs["draft_conf"] = (B, 7)
             for k, s in fs.items():
                 out[k] = torch.empty(s, dtype=torch.float32, device=dev)
         return out

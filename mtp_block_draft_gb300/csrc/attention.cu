@@ -31,7 +31,7 @@ __global__ void __launch_bounds__(256) k_attn_partial(AttnArgs a) {
   const int base = a.base[b];
   int lo = a.lo_fixed;
   if (a.window > 0) lo = max(lo, base - a.window);
-  const int hi_max = base + 7;
+  const int hi_max = base + a.rows - 1;
   const int k_begin = max(lo, chunk_id * a.chunk);
   const int k_end = min((chunk_id + 1) * a.chunk, hi_max + 1);
   const long pidx = ((long)b * a.hkv + g) * a.nchunk + chunk_id;
@@ -47,10 +47,13 @@ __global__ void __launch_bounds__(256) k_attn_partial(AttnArgs a) {
   const float scale = rsqrtf((float)hd);
 
   float qr[kMaxDPT], acc[kMaxDPT];
-  const float* qp = a.q + ((long)(b * 8 + s) * a.hq + h) * hd;
+  // query rows past the sequence's rows (a verify of fewer drafts) compute on zeros and
+  // are never merged
+  const bool live = s < a.rows;
+  const float* qp = a.q + ((long)(b * a.rows + (live ? s : 0)) * a.hq + h) * hd;
 #pragma unroll
   for (int i = 0; i < kMaxDPT; ++i) {
-    qr[i] = (i < DPT) ? qp[sub + TPQ * i] * scale : 0.f;
+    qr[i] = (i < DPT && live) ? qp[sub + TPQ * i] * scale : 0.f;
     acc[i] = 0.f;
   }
   float m = -INFINITY, l = 0.f;
@@ -112,12 +115,12 @@ __global__ void __launch_bounds__(256) k_attn_partial(AttnArgs a) {
 template <typename T>
 __global__ void k_attn_merge(AttnArgs a) {
   const int mrow = blockIdx.x, h = blockIdx.y;
-  const int b = mrow >> 3, s = mrow & 7;
+  const int b = mrow / a.rows, s = mrow % a.rows;
   const int grp = a.hq / a.hkv, g = h / grp, hh = h % grp, qi = s * grp + hh, QN = 8 * grp;
   const int base = a.base[b];
   int lo = a.lo_fixed;
   if (a.window > 0) lo = max(lo, base - a.window);
-  const int c0 = lo / a.chunk, c1 = min(a.nchunk - 1, (base + 7) / a.chunk);
+  const int c0 = lo / a.chunk, c1 = min(a.nchunk - 1, (base + a.rows - 1) / a.chunk);
   const long p0 = ((long)b * a.hkv + g) * a.nchunk;
   float M = -INFINITY;
   for (int c = c0; c <= c1; ++c) M = fmaxf(M, a.part_ml[((p0 + c) * QN + qi) * 2]);
@@ -145,12 +148,12 @@ __global__ void __launch_bounds__(256) k_attn_merge_w(AttnArgs a) {
   const int h = blockIdx.y * 8 + warp;
   if (h >= a.hq) return;
   const int mrow = blockIdx.x;
-  const int b = mrow >> 3, s = mrow & 7;
+  const int b = mrow / a.rows, s = mrow % a.rows;
   const int grp = a.hq / a.hkv, g = h / grp, hh = h % grp, qi = s * grp + hh, QN = 8 * grp;
   const int base = a.base[b];
   int lo = a.lo_fixed;
   if (a.window > 0) lo = max(lo, base - a.window);
-  const int c0 = lo / a.chunk, c1 = min(a.nchunk - 1, (base + 7) / a.chunk);
+  const int c0 = lo / a.chunk, c1 = min(a.nchunk - 1, (base + a.rows - 1) / a.chunk);
   const long p0 = ((long)b * a.hkv + g) * a.nchunk;
   const float* ml = a.part_ml + (p0 * QN + qi) * 2;  // chunk c at ml[c * QN * 2]
   float M = -INFINITY;
@@ -200,7 +203,7 @@ static bool merge_w(const AttnArgs& a, cudaStream_t st) {
   const unsigned eo = sizeof(T) * 4;
   if (a.hd % 32 || !aligned_to(a.part_o, 16) || !aligned_to(a.out, eo) || a.out_lo % 4)
     return false;
-  dim3 g(a.B * 8, (a.hq + 7) / 8);
+  dim3 g(a.B * a.rows, (a.hq + 7) / 8);
   switch (a.hd / 32) {
     case 1: k_attn_merge_w<T, 1><<<g, 256, 0, st>>>(a); return true;
     case 2: k_attn_merge_w<T, 2><<<g, 256, 0, st>>>(a); return true;
@@ -221,7 +224,7 @@ void op_attention(int dt, const AttnArgs& a, cudaStream_t st) {
 
 void op_attention_merge(int dt, const AttnArgs& a, cudaStream_t st) {
   if (dt ? merge_w<bf16>(a, st) : merge_w<float>(a, st)) return;
-  dim3 g2(a.B * 8, a.hq);
+  dim3 g2(a.B * a.rows, a.hq);
   if (dt)
     k_attn_merge<bf16><<<g2, 128, 0, st>>>(a);
   else

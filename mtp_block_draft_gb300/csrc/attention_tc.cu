@@ -103,7 +103,8 @@ __device__ __forceinline__ void tmem_scale(uint32_t taddr, int n, float f) {
 }
 
 
-// First visible key of a sequence whose block rows start at `base`; the last is base+7.
+// First visible key of a sequence whose block rows start at `base`; the last is
+// base + rows - 1.
 __device__ __forceinline__ int vis_lo(const AttnArgs& a, int base) {
   int lo = a.lo_fixed;
   if (a.window > 0) lo = max(lo, base - a.window);
@@ -111,7 +112,7 @@ __device__ __forceinline__ int vis_lo(const AttnArgs& a, int base) {
 }
 // Visible key tiles of a sequence (tile size tk).
 __device__ __forceinline__ int vis_tiles(const AttnArgs& a, int base, int tk) {
-  return (base + 7) / tk - vis_lo(a, base) / tk + 1;
+  return (base + a.rows - 1) / tk - vis_lo(a, base) / tk + 1;
 }
 
 // Shared-memory plan (TK keys per tile, NST stages). P (128 rows x TK keys) of tile t is
@@ -148,7 +149,7 @@ __global__ void __launch_bounds__(320, 1)
   constexpr int KQ = TK / 4;  // keys per softmax thread (a quarter of the tile)
   constexpr float kLog2e = 1.4426950408889634f;
   extern __shared__ uint8_t smem_raw[];
-  const int grp = a.hq / a.hkv, QN = 8 * grp, B = a.B, hkv = a.hkv;
+  const int grp = a.hq / a.hkv, QN = a.rows * grp, B = a.B, hkv = a.hkv;
   uint64_t* bars = (uint64_t*)smem_raw;
   float* sMax = (float*)(bars + 32);  // [2 tiles][4 quarters][64] tile maxima (log2)
   float* sL = sMax + 512;             // [4][64] running sums at the end of a piece
@@ -376,7 +377,7 @@ __global__ void __launch_bounds__(320, 1)
       uint32_t w[NW];
       if (r < QN) {
         const int s_ = r / grp, hh = r % grp;
-        const bf16* src = (const bf16*)a.qs + ((long)(b * 8 + s_) * a.hq + g * grp + hh) * HD +
+        const bf16* src = (const bf16*)a.qs + ((long)(b * a.rows + s_) * a.hq + g * grp + hh) * HD +
                           (lrow >= 64 ? a.qs_lo : 0) + hf * (HD / 2);
 #pragma unroll
         for (int i = 0; i < NW; i += 4) {
@@ -411,8 +412,8 @@ __global__ void __launch_bounds__(320, 1)
     for (long x = x0; x < x1; ++p) {
       int b, g, kt0, nt, base;
       piece(x, b, g, kt0, nt, base);
-      const int lo = vis_lo(a, base), k_end = base + 8;
-      const int row_hi = a.causal ? base + srow : base + 7;
+      const int lo = vis_lo(a, base), k_end = base + a.rows;
+      const int row_hi = a.causal ? base + srow : base + a.rows - 1;
       float m = -INFINITY, l = 0.f;  // reference max and running sum, log2 units
       // Every iteration runs both named barriers (bar 3: swap posted, bar 4: maxima
       // posted) on every thread, whether or not a wait timed out, so they complete.
@@ -596,8 +597,8 @@ __global__ void __launch_bounds__(256) k_attn_merge_p(AttnArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y * 8 + warp;
   if (h >= a.hq) return;
-  const int mrow = blockIdx.x, b = mrow >> 3, s = mrow & 7;
-  const int grp = a.hq / a.hkv, g = h / grp, hh = h % grp, qi = s * grp + hh, QN = 8 * grp;
+  const int mrow = blockIdx.x, b = mrow / a.rows, s = mrow % a.rows;
+  const int grp = a.hq / a.hkv, g = h / grp, hh = h % grp, qi = s * grp + hh, QN = a.rows * grp;
   const int TK = a.ptk, G = a.pgrid;
   int pre = 0, tot = 0;
   for (int bb = lane; bb < a.B; bb += 32) {
@@ -680,14 +681,15 @@ int attn_tc_init_attributes() {
 void op_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV,
                      const CUtensorMap& tmQh, const CUtensorMap& tmQl, unsigned* err,
                      cudaStream_t st) {
-  if (a.B > kAttnMaxB || a.pgrid < 1 || a.ptk != kAttnTile) return;  // excluded by the caller
+  if (a.B > kAttnMaxB || a.pgrid < 1 || a.ptk != kAttnTile || a.rows < 1 || a.rows > 8)
+    return;  // excluded by the caller
   if (a.hd == 128)
     k_attn_tc<128, kTK128, kNST128><<<a.pgrid, 320, Smem<128, kTK128, kNST128>::kBytes, st>>>(
         tmK, tmV, tmQh, tmQl, a, err);
   else
     k_attn_tc<64, kTK64, kNST64><<<a.pgrid, 320, Smem<64, kTK64, kNST64>::kBytes, st>>>(
         tmK, tmV, tmQh, tmQl, a, err);
-  dim3 g(a.B * 8, (a.hq + 7) / 8);
+  dim3 g(a.B * a.rows, (a.hq + 7) / 8);
   if (a.hd == 128)
     k_attn_merge_p<4><<<g, 256, 0, st>>>(a);
   else

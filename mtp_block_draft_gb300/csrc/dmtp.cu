@@ -38,6 +38,14 @@ struct LayerPlans {
   Gemm gq, ga, gb, go;         // Gated DeltaNet projections
 };
 
+// The GEMMs of a verify that carries depth drafts: G = depth + 1 rows per sequence
+// (B G token rows) through the target, its head and a6's drafter-context projections.
+struct VerifyPlans {
+  LayerPlans tgt[DMTP_MAX_LAYERS];
+  Gemm head_v, dfc;
+  Gemm dkv[DMTP_MAX_DRAFT_LAYERS];
+};
+
 }  // namespace
 
 struct dmtp_ctx {
@@ -104,6 +112,11 @@ struct dmtp_ctx {
   int* hc_ids;
   int* hc_n;
   int list_n;  // listed tokens as last set (0: the list is off)
+  // the draft heads' confidence: per-thread partials of the T1 and drafter heads, and the
+  // combined confidence of T1..T7 [B][7]
+  bool conf_on;
+  float2 *conf_t1, *conf_d;
+  float* dconf;
   float* hlast;
   int* prompts;
   int2* psched;  // prefill schedule: (sequence, chunk) of each row group of each step
@@ -121,8 +134,10 @@ struct dmtp_ctx {
   Gemm head_a;  // A after the prompt: the target's own (bf16) head on the T1 input rows
   Gemm head_t1l, head_dl;  // the T1 and drafter heads over the token list
 
-  cudaGraphExec_t graph;         // the round
-  cudaGraphExec_t graph_forced;  // the round with drafts read from `forced`
+  cudaGraphExec_t graph[8];         // the round, per verify depth (7: the DMTP round)
+  cudaGraphExec_t graph_forced[8];  // the round with drafts read from `forced`
+  bool depths;                      // plans for verifies of 0..6 drafts were built
+  VerifyPlans* vp[8];               // [G] for G = 1..7 rows per sequence (G = 8: tgt etc.)
   cudaStream_t cap_st;  // private stream the round is captured on (the caller's may be NULL)
   bool poisoned;
   long kv_bound;
@@ -137,6 +152,17 @@ struct dmtp_ctx {
   std::vector<int> pcls;
   std::vector<double> pbytes, pflops, pimpl;
   std::vector<int> kv_host;  // kv_len at the start of the profiled round
+
+  ~dmtp_ctx() {
+    for (VerifyPlans* v : vp) delete v;
+  }
+  void drop_graphs() {
+    for (int k = 0; k < 8; ++k) {
+      if (graph[k]) cudaGraphExecDestroy(graph[k]);
+      if (graph_forced[k]) cudaGraphExecDestroy(graph_forced[k]);
+      graph[k] = graph_forced[k] = nullptr;
+    }
+  }
 };
 
 // ---------------------------------------------------------------------------------
@@ -168,7 +194,10 @@ int derive(dmtp_ctx* c, const dmtp_config* cfg, int B) {
                                                         f.temperature <= 3.0e38f)) ||
       (f.draft_head_fp8 != 0 && f.draft_head_fp8 != 1) ||
       (f.draft_head_fp8 && (f.dtype != 1 || f.d_model % 128)) || f.draft_list_cap < 0 ||
-      f.draft_list_cap > f.vocab || (f.draft_list_cap > 0 && f.dtype != 1))
+      f.draft_list_cap > f.vocab || (f.draft_list_cap > 0 && f.dtype != 1) ||
+      (f.variable_depth != 0 && f.variable_depth != 1) ||
+      (f.draft_confidence != 0 && f.draft_confidence != 1) ||
+      (f.draft_confidence && f.dtype != 1))
     return DMTP_EINVAL;
   const int grp = f.n_heads / f.n_kv_heads;
   const int QN = 8 * grp;
@@ -181,6 +210,7 @@ int derive(dmtp_ctx* c, const dmtp_config* cfg, int B) {
   c->dt = f.dtype;
   c->fp8 = f.draft_head_fp8 != 0;
   c->list_cap = f.draft_list_cap;
+  c->conf_on = f.draft_confidence != 0;
   c->d = f.d_model;
   c->V = f.vocab;
   c->F = f.ffn;
@@ -308,6 +338,13 @@ size_t layout(dmtp_ctx* c, char* base) {
     if (c->fp8) c->hcs = b.take<float>(cpad * 4);
     c->hc_ids = b.take<int>(cpad * 4);
     c->hc_n = b.take<int>(4);
+  }
+  c->conf_t1 = c->conf_d = nullptr;
+  c->dconf = nullptr;
+  if (c->conf_on) {  // at most two partials per CTA (8 epilogue warps), one CTA per SM
+    c->conf_t1 = b.take<float2>((size_t)2 * c->attn_grid * B * 8);
+    c->conf_d = b.take<float2>((size_t)2 * c->attn_grid * 6 * B * 8);
+    c->dconf = b.take<float>(B * 7 * 4);
   }
   c->hlast = b.take<float>(B * d * 4);
   c->forced = b.take<int>(B * 7 * 4);
@@ -445,20 +482,22 @@ void gemm_acc(dmtp_ctx* c, const Gemm& g, float* out, int ldo) {
   }, impl);
 }
 
-// The verify head's sampling: row m = b*8 + j of sequence b at position pos0[b] + j.
-SampleArgs verify_sampling(const dmtp_ctx* c) {
+// The verify head's sampling: row m = b*G + j of sequence b at position pos0[b] + j (G
+// verify rows per sequence).
+SampleArgs verify_sampling(const dmtp_ctx* c, int G = 8) {
   return SampleArgs{1.4426950408889634f / c->cfg.temperature, (uint32_t)c->cfg.sample_seed,
-                    (uint32_t)(c->cfg.sample_seed >> 32), c->rs.pos0, 8};
+                    (uint32_t)(c->cfg.sample_seed >> 32), c->rs.pos0, G};
 }
 
-// smp: the verify head's sampled picks (nullptr: argmax picks)
+// smp: the verify head's sampled picks (nullptr: argmax picks); conf: the head's
+// confidence partials (bf16 path, greedy heads), or null
 void gemm_argmax(dmtp_ctx* c, const Gemm& g, unsigned long long* keys, float* logits,
-                 const SampleArgs* smp = nullptr) {
+                 const SampleArgs* smp = nullptr, float2* conf = nullptr) {
   const double ew = (c->dt == 1 && g.hp.fp8) ? 1.0 : esz(c);  // bytes per operand element
   const double bytes = ((double)g.N * g.K + (double)g.M * g.K) * ew + 8.0 * g.M;
   launch(c, P_HEAD, bytes, 2.0 * g.M * g.N * g.K, [&] {
     if (c->dt == 1)
-      op_head_tc(g.hp, keys, logits, c->V, smp, c->err, c->st);
+      op_head_tc(g.hp, keys, logits, c->V, smp, c->err, c->st, conf);
     else
       op_gemm_simt_argmax((const float*)g.W, (const float*)g.X, g.N, g.K, g.M, keys, logits,
                           c->V, smp, c->st);
@@ -481,9 +520,7 @@ void zero(dmtp_ctx* c, void* p, size_t bytes) { cudaMemsetAsync(p, 0, bytes, c->
 
 // element offset of the remainder half of an operand with `mt` padded rows of `ld`
 inline long lo_of(const dmtp_ctx* c, int mt, int ld) { return c->dt ? (long)mt * ld : 0; }
-inline int mt_of_rows(const dmtp_ctx* c, int rows) {
-  return rows == c->M ? c->mt8 : (rows == 6 * c->B ? c->mt6 : c->mt1);
-}
+inline int mt_of_rows(const dmtp_ctx*, int rows) { return tc_mt(rows); }
 
 // zero / nz: also clears the first nz floats of each of the `rows` rows of zero (the
 // accumulator of the GEMM that reads y), instead of a separate memset.
@@ -492,7 +529,7 @@ void norm(dmtp_ctx* c, const float* x, const void* g, void* y, float* y32, void*
   launch(c, P_OTHER, 0, 0, [&] {
     const int mt = mt_of_rows(c, rows);
     op_rmsnorm(c->dt, x, c->d, g, y, c->d, split ? lo_of(c, mt, c->d) : 0, y32, c->d, tap,
-               c->ntap * c->d, lo_of(c, c->mt8, c->ntap * c->d), rows, c->d, c->cfg.rms_eps,
+               c->ntap * c->d, lo_of(c, mt, c->ntap * c->d), rows, c->d, c->cfg.rms_eps,
                map, c->st, zero, nz, nz);
   });
 }
@@ -510,27 +547,28 @@ struct AttnSpec {
   int mode_base;  // 1: base = kv_len at round start (target, drafter); 2: kv_len + 1 (MTP)
 };
 
-// MLP block: x += down(SwiGLU(gate/up(RMS(x)))).
-void mlp(dmtp_ctx* c, const LayerPlans& p, const dmtp_layer_weights& w, float* xr) {
-  const int M = c->M;
+// MLP block over M rows: x += down(SwiGLU(gate/up(RMS(x)))).
+void mlp(dmtp_ctx* c, const LayerPlans& p, const dmtp_layer_weights& w, float* xr, int M) {
+  const int mt = mt_of_rows(c, M);
   if (p.gu.swiglu) {
     norm(c, xr, w.mlp_norm, c->xn, nullptr, nullptr, M);
-    gemm_swiglu(c, p.gu, c->hmid, lo_of(c, c->mt8, c->F));
+    gemm_swiglu(c, p.gu, c->hmid, lo_of(c, mt, c->F));
   } else {
     norm(c, xr, w.mlp_norm, c->xn, nullptr, nullptr, M, RowMap(), true, c->gu, 2 * c->F);
     gemm_acc(c, p.gu, c->gu, 2 * c->F);
-    launch(c, P_OTHER, 0, 0, [&] { op_swiglu(c->dt, c->gu, c->hmid, lo_of(c, c->mt8, c->F), M, c->F, c->st); });
+    launch(c, P_OTHER, 0, 0, [&] { op_swiglu(c->dt, c->gu, c->hmid, lo_of(c, mt, c->F), M, c->F, c->st); });
   }
   gemm_acc(c, p.down, xr, c->d);
 }
 
+// Attention layer over rg rows per sequence (M = B rg rows; 8 but in a shorter verify).
 void attn_layer(dmtp_ctx* c, const LayerPlans& p, const dmtp_layer_weights& w, float* xr,
-                const AttnSpec& a, void* tap_in) {
-  const int M = c->M;
+                const AttnSpec& a, void* tap_in, int rg = 8) {
+  const int M = c->B * rg;
   norm(c, xr, w.attn_norm, c->xn, nullptr, tap_in, M, RowMap(), true, c->qkv, c->qkvd);
   gemm_acc(c, p.qkv, c->qkv, c->qkvd);
   launch(c, P_OTHER, 0, 0, [&] { op_rope_kv(c->dt, c->qkv, c->qkvd, 0, c->qd, c->qd + c->kvd, c->q, c->attn_tc ? c->qs : nullptr, (long)M * c->qd, a.Kc, a.Vc, a.base, c->rs.cseq, c->rope,
-             M, c->hq, c->hkv, c->hd, c->maxc, c->err, c->st); });
+             M, c->hq, c->hkv, c->hd, c->maxc, c->err, c->st, rg); });
   AttnArgs aa;
   aa.Kc = a.Kc;
   aa.Vc = a.Vc;
@@ -538,7 +576,7 @@ void attn_layer(dmtp_ctx* c, const LayerPlans& p, const dmtp_layer_weights& w, f
   aa.part_o = c->part_o;
   aa.part_ml = c->part_ml;
   aa.out = c->att;
-  aa.out_lo = lo_of(c, c->mt8, c->qd);
+  aa.out_lo = lo_of(c, mt_of_rows(c, M), c->qd);
   aa.base = a.base;
   aa.cseq = c->rs.cseq;
   aa.causal = a.causal;
@@ -552,7 +590,8 @@ void attn_layer(dmtp_ctx* c, const LayerPlans& p, const dmtp_layer_weights& w, f
   aa.chunk = c->attn_chunk;
   aa.nchunk = c->attn_nchunk;
   aa.qs = c->qs;
-  aa.qs_lo = (long)c->M * c->qd;
+  aa.qs_lo = (long)M * c->qd;
+  aa.rows = rg;
   aa.pgrid = c->attn_grid;
   aa.ptk = kAttnTile;
   double kv_bytes = 0;
@@ -563,9 +602,9 @@ void attn_layer(dmtp_ctx* c, const LayerPlans& p, const dmtp_layer_weights& w, f
       const int base = a.mode_base == 2 ? a0 + 1 : a0;
       int lo = a.lo_fixed;
       if (a.window > 0) lo = std::max(lo, base - a.window);
-      kv_bytes += (double)(base + 8 - lo) * c->kvd * esz(c) * 2;
+      kv_bytes += (double)(base + rg - lo) * c->kvd * esz(c) * 2;
     }
-    kv_bytes += (double)c->M * c->qd * esz(c) * 2;  // q in, o out
+    kv_bytes += (double)M * c->qd * esz(c) * 2;  // q in, o out
   }
   launch(c, P_ATTN, kv_bytes, 0, [&] {
     if (c->attn_tc)
@@ -575,13 +614,13 @@ void attn_layer(dmtp_ctx* c, const LayerPlans& p, const dmtp_layer_weights& w, f
   });
   c->launches += 1;  // partial + merge
   gemm_acc(c, p.o, xr, c->d);
-  mlp(c, p, w, xr);
+  mlp(c, p, w, xr, M);
 }
 
-void gdn_layer(dmtp_ctx* c, int l, float* xr, void* tap_in, bool snapshots) {
-  const LayerPlans& p = c->tgt[l];
+void gdn_layer(dmtp_ctx* c, const LayerPlans& p, int l, float* xr, void* tap_in, bool snapshots,
+               int rg) {
   const dmtp_layer_weights& w = c->w.layers[l];
-  const int M = c->M, gi = c->gdn_index[l];
+  const int M = c->B * rg, gi = c->gdn_index[l];
   const int nqkv = c->gH * (2 * c->gdk + c->gdv);
   norm(c, xr, w.attn_norm, c->xn, nullptr, tap_in, M, RowMap(), true, c->qkv, c->gld);
   gemm_acc(c, p.gq, c->qkv, c->gld);
@@ -596,7 +635,8 @@ void gdn_layer(dmtp_ctx* c, int l, float* xr, void* tap_in, bool snapshots) {
   ga.rows_valid = c->rs.rows_valid;
   ga.snapshots = snapshots ? 1 : 0;
   ga.out = c->att;
-  ga.out_lo = lo_of(c, c->mt8, c->gH * c->gdv);
+  ga.out_lo = lo_of(c, mt_of_rows(c, M), c->gH * c->gdv);
+  ga.rows = rg;
   ga.B = c->B;
   ga.H = c->gH;
   ga.dk = c->gdk;
@@ -605,48 +645,56 @@ void gdn_layer(dmtp_ctx* c, int l, float* xr, void* tap_in, bool snapshots) {
   const double st_bytes = (double)c->B * c->gH * c->gdv * c->gdk * 4 * (snapshots ? 9 : 2);
   launch(c, P_GDN, st_bytes, 0, [&] { op_gdn(c->dt, ga, c->st); });
   gemm_acc(c, p.go, xr, c->d);
-  mlp(c, p, w, xr);
+  mlp(c, p, w, xr, M);
 }
 
-// target forward over the 8 rows of every sequence (tokens in rs.tok, positions pos0+s);
-// leaves the final-normed hidden in hT32 (fp32) and hTn (operand type), taps filled.
-void target_forward(dmtp_ctx* c, bool snapshots) {
-  const int M = c->M;
+// target forward over rg rows of every sequence (8; fewer in a verify of fewer drafts):
+// tokens in rs.tok, row m = b rg + s at position pos0[b] + s; leaves the final-normed
+// hidden in hT32 (fp32) and hTn (operand type), taps filled. tgt: the layers' GEMM plans
+// for B rg rows.
+void target_forward(dmtp_ctx* c, bool snapshots, int rg, const LayerPlans* tgt) {
+  const int M = c->B * rg;
   launch(c, P_OTHER, 0, 0, [&] { op_embed(c->dt, c->w.emb, c->rs.tok, c->V, c->x, M, c->d, c->err, c->st); });
   for (int l = 0; l < c->L; ++l) {
     void* tap_in = l > 0 ? tap_ptr(c, c->tap_of_layer[l - 1]) : nullptr;
     if (c->cfg.layer_kind[l] == 0) {
       AttnSpec a{c->tK[l], c->tV[l], &c->tmK[l], &c->tmV[l], c->rs.pos0, 1, 0, 0, 1};
-      attn_layer(c, c->tgt[l], c->w.layers[l], c->x, a, tap_in);
+      attn_layer(c, tgt[l], c->w.layers[l], c->x, a, tap_in, rg);
     } else {
-      gdn_layer(c, l, c->x, tap_in, snapshots);
+      gdn_layer(c, tgt[l], l, c->x, tap_in, snapshots, rg);
     }
   }
   norm(c, c->x, c->w.final_norm, c->hTn, c->hT32, tap_ptr(c, c->tap_of_layer[c->L - 1]), M,
        RowMap(), false);
 }
 
-// a6 (and each prefill chunk): drafter context K/V at positions pos0+s from the taps,
-// then the MTP rows (token mtp_tok, hidden hT32 row) at positions mtp_base+s.
-void drafter_ctx(dmtp_ctx* c) {
-  const int M = c->M;
+// a6 (and each prefill chunk): drafter context K/V at positions pos0+s from the taps of
+// the rg rows per sequence (dfc / dkv: their GEMM plans for B rg rows), then the MTP rows
+// (token mtp_tok, hidden hT32 row) at positions mtp_base+s.
+void drafter_ctx(dmtp_ctx* c, int rg, const Gemm& dfc, const Gemm* dkv) {
+  const int M = c->B * rg;
   zero(c, c->cacc, (size_t)M * c->d * 4);
-  gemm_acc(c, c->dfc, c->cacc, c->d);
+  gemm_acc(c, dfc, c->cacc, c->d);
   norm(c, c->cacc, c->w.dft_norm_c, c->cn, nullptr, nullptr, M, RowMap(), true, c->qkv,
        2 * c->kvd);
   for (int j = 0; j < c->Ld; ++j) {
     if (j > 0) zero(c, c->qkv, (size_t)M * 2 * c->kvd * 4);
-    gemm_acc(c, c->dkv[j], c->qkv, 2 * c->kvd);
+    gemm_acc(c, dkv[j], c->qkv, 2 * c->kvd);
     launch(c, P_OTHER, 0, 0, [&] { op_rope_kv(c->dt, c->qkv, 2 * c->kvd, -1, 0, c->kvd, nullptr, nullptr, 0, c->dK[j], c->dV[j],
-               c->rs.pos0, c->rs.cseq, c->rope, M, c->hq, c->hkv, c->hd, c->maxc, c->err, c->st); });
+               c->rs.pos0, c->rs.cseq, c->rope, M, c->hq, c->hkv, c->hd, c->maxc, c->err, c->st, rg); });
   }
 }
 
-void mtp_advance(dmtp_ctx* c) {
+// The MTP advance always runs 8 rows per sequence; its target hidden rows come from a
+// step of rg rows per sequence (hT32 row b rg + s; rows past the step's are never
+// committed and land in the MTP cache's stale tail).
+void mtp_advance(dmtp_ctx* c, int rg = 8) {
   const int M = c->M;
   ConcatPart ph, pe;
   ph.src32 = c->hT32;
   ph.ld = c->d;
+  ph.map.out_group = 8;
+  ph.map.in_group = rg;
   ph.g = c->w.mtp_norm_h;
   pe.tok = c->rs.mtp_tok;
   pe.g = c->w.mtp_norm_e;
@@ -662,7 +710,12 @@ struct Dbg {
   float *t1, *dl, *vl;
 };
 
-void enqueue_round(dmtp_ctx* c, const Dbg& dbg, const int* forced) {
+// One round whose verify carries `depth` drafts (0..7; 7: the DMTP round): rows
+// [A, T1..T_depth] at G = depth + 1 rows per sequence (colibri page: a verify of k drafts
+// is one forward of the token and its k drafts).
+void enqueue_round(dmtp_ctx* c, const Dbg& dbg, const int* forced, int depth = 7) {
+  const int G = depth + 1;
+  const VerifyPlans* vp = G < 8 ? c->vp[G] : nullptr;
   RoundState& s = c->rs;
   const int B = c->B;
   launch(c, P_OTHER, 0, 0, [&] { op_round_begin(s, c->st); });
@@ -674,8 +727,11 @@ void enqueue_round(dmtp_ctx* c, const Dbg& dbg, const int* forced) {
   // the draft heads score the token list when one is set (dmtp_set_draft_list)
   const bool listed = c->list_n > 0;
   const int* lmap = listed ? c->hc_ids : nullptr;
-  gemm_argmax(c, listed ? c->head_t1l : c->head_t1, s.keys, dbg.t1);
+  const Gemm& ht1 = listed ? c->head_t1l : c->head_t1;
+  gemm_argmax(c, ht1, s.keys, dbg.t1, nullptr, c->conf_t1);
   launch(c, P_OTHER, 0, 0, [&] { op_keys_to_ids(s.keys, B, 1, s.drafts, 7, 0, forced, 7, 0, c->st, lmap); });
+  if (c->conf_on)  // the T1 head's probability of its own pick (colibri per-step gate)
+    launch(c, P_OTHER, 0, 0, [&] { op_conf_combine(ht1.hp, c->conf_t1, 1, c->dconf, 7, 0, c->st); });
   // a2: Delta = W [RMS_e(E(T1)); RMS_m(h_MTP)]; slots [E(A), E(T1)+Delta, E(MASK) x 6]
   ConcatPart pe, pm;
   pe.tok = s.drafts;  // T1 of sequence b is drafts[b*7]
@@ -703,23 +759,27 @@ void enqueue_round(dmtp_ctx* c, const Dbg& dbg, const int* forced) {
     launch(c, P_OTHER, 0, 0, [&] { op_rmsnorm_e4m3(c->x, c->d, c->w.dft_final_norm, c->dnq, c->d, c->dnqs, 6 * B, c->d, c->cfg.rms_eps, m6, c->st); });
   else
     norm(c, c->x, c->w.dft_final_norm, c->dn, nullptr, nullptr, 6 * B, m6, false);
-  gemm_argmax(c, listed ? c->head_dl : c->head_d, s.keys + B, dbg.dl);
+  const Gemm& hd = listed ? c->head_dl : c->head_d;
+  gemm_argmax(c, hd, s.keys + B, dbg.dl, nullptr, c->conf_d);
   launch(c, P_OTHER, 0, 0, [&] { op_keys_to_ids(s.keys + B, B, 6, s.drafts, 7, 1, forced, 7, 1, c->st, lmap); });
-  // a4: target verify of [A, T1..T7]
-  launch(c, P_OTHER, 0, 0, [&] { op_verify_tokens(s, c->st); });
-  target_forward(c, true);
+  if (c->conf_on)
+    launch(c, P_OTHER, 0, 0, [&] { op_conf_combine(hd.hp, c->conf_d, 6, c->dconf, 7, 1, c->st); });
+  // a4: target verify of [A, T1..T_depth]
+  launch(c, P_OTHER, 0, 0, [&] { op_verify_tokens(s, depth, c->st); });
+  target_forward(c, true, G, vp ? vp->tgt : c->tgt);
+  const Gemm& hv = vp ? vp->head_v : c->head_v;
   if (c->cfg.temperature > 0.f) {  // target-only sampled verification (DMTP §5)
-    const SampleArgs smp = verify_sampling(c);
-    gemm_argmax(c, c->head_v, s.keys + 7 * B, dbg.vl, &smp);
+    const SampleArgs smp = verify_sampling(c, G);
+    gemm_argmax(c, hv, s.keys + 7 * B, dbg.vl, &smp);
   } else {
-    gemm_argmax(c, c->head_v, s.keys + 7 * B, dbg.vl);
+    gemm_argmax(c, hv, s.keys + 7 * B, dbg.vl);
   }
-  launch(c, P_OTHER, 0, 0, [&] { op_keys_to_ids(s.keys + 7 * B, B, 8, s.g, 8, 0, nullptr, 0, 0, c->st); });
+  launch(c, P_OTHER, 0, 0, [&] { op_keys_to_ids(s.keys + 7 * B, B, G, s.g, 8, 0, nullptr, 0, 0, c->st); });
   // a5: prefix acceptance, commit, watermarks, snapshot swap
-  launch(c, P_OTHER, 0, 0, [&] { op_accept(s, c->st); });
+  launch(c, P_OTHER, 0, 0, [&] { op_accept(s, depth, c->st); });
   // a6: drafter context and MTP advance over the committed rows
-  drafter_ctx(c);
-  mtp_advance(c);
+  drafter_ctx(c, G, vp ? vp->dfc : c->dfc, vp ? vp->dkv : c->dkv);
+  mtp_advance(c, G);
 }
 
 int check_err(dmtp_ctx* c) {
@@ -809,7 +869,7 @@ float time_swiglu(dmtp_ctx* c, const TcPlan& p, const void* flush, size_t flush_
   for (int rep = 0; rep < 3; ++rep) {
     op_l2_flush(flush, flush_bytes, c->err, c->st);
     cudaEventRecord(e0, c->st);
-    op_gemm_tc_swiglu(p, c->hmid, (long)c->mt8 * c->F, c->err, c->st);
+    op_gemm_tc_swiglu(p, c->hmid, (long)p.MT * c->F, c->err, c->st);
     cudaEventRecord(e1, c->st);
     float ms = 1e30f;
     if (cudaEventSynchronize(e1) != cudaSuccess ||
@@ -832,6 +892,14 @@ int autotune(dmtp_ctx* c, const void* flush, size_t flush_bytes) {
   for (Gemm* g : {&c->fuse, &c->head_t1, &c->head_d, &c->head_v, &c->head_a, &c->dfc,
                   &c->mproj, &c->head_t1l, &c->head_dl})
     all.push_back(g);
+  for (int G = 1; G < 8; ++G) {
+    VerifyPlans* v = c->vp[G];
+    if (!v) continue;
+    for (int l = 0; l < c->L; ++l) collect(v->tgt[l], all);
+    all.push_back(&v->head_v);
+    all.push_back(&v->dfc);
+    for (int j = 0; j < c->Ld; ++j) all.push_back(&v->dkv[j]);
+  }
   const size_t scratch = (size_t)c->M * 2 * c->F;  // floats of the gate/up accumulator
   cudaEvent_t e0, e1;
   if (cudaEventCreate(&e0) != cudaSuccess) return DMTP_ECUDA;
@@ -848,8 +916,10 @@ int autotune(dmtp_ctx* c, const void* flush, size_t flush_bytes) {
     if (!g->W) continue;
     if (!g->swiglu && !g->argmax && (size_t)g->M * g->N > scratch) continue;  // default shape
     // the verify head under sampled verification runs the sampling epilogue
-    const bool sample = g == &c->head_v && c->cfg.temperature > 0.f;
-    const SampleArgs smp = sample ? verify_sampling(c) : SampleArgs{};
+    bool vhead = g == &c->head_v;
+    for (int G = 1; G < 8; ++G) vhead = vhead || (c->vp[G] && g == &c->vp[G]->head_v);
+    const bool sample = vhead && c->cfg.temperature > 0.f;
+    const SampleArgs smp = sample ? verify_sampling(c, g->M / c->B) : SampleArgs{};
     const bool fp8 = g->argmax && g->hp.fp8;
     const TuneKey key{dev, g->N, g->K, g->M, g->split, g->argmax, g->swiglu, sample, fp8};
     const TuneChoice* hit = nullptr;
@@ -981,8 +1051,7 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
   }
   c->w = *w;
   c->st = (cudaStream_t)stream;
-  c->graph = nullptr;
-  c->graph_forced = nullptr;
+  for (int k = 0; k < 8; ++k) c->graph[k] = c->graph_forced[k] = nullptr;
   c->poisoned = false;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1075,6 +1144,27 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
   pr |= plan(c, c->head_v, w->head, c->V, c->d, c->hTn, M, true, false);
   pr |= plan(c, c->dfc, w->dft_fc, c->d, c->ntap * c->d, c->taps, M, false);
   pr |= plan(c, c->mproj, w->mtp_proj, c->d, 2 * c->d, c->z, M, false);
+  c->depths = cfg->variable_depth != 0;
+  if (c->depths) {  // verifies of 0..6 drafts: G = 1..7 rows per sequence
+    for (int G = 1; G < 8; ++G) {
+      VerifyPlans* v = new (std::nothrow) VerifyPlans();
+      if (!v) {
+        delete c;
+        return DMTP_ENOMEM;
+      }
+      c->vp[G] = v;
+      const int MG = B * G;
+      for (int l = 0; l < c->L; ++l)
+        pr |= plan_layer(c, v->tgt[l], w->layers[l], cfg->layer_kind[l], MG);
+      pr |= plan(c, v->head_v, w->head, c->V, c->d, c->hTn, MG, true, false);
+      pr |= plan(c, v->dfc, w->dft_fc, c->d, c->ntap * c->d, c->taps, MG, false);
+      for (int j = 0; j < c->Ld; ++j) {
+        const char* wk = (const char*)w->dft[j].wqkv;
+        pr |= plan(c, v->dkv[j], wk ? wk + (size_t)c->qd * c->d * (c->dt ? 2 : 4) : nullptr,
+                   2 * c->kvd, c->d, c->cn, MG, false);
+      }
+    }
+  }
   if (pr) {
     delete c;
     return DMTP_EINVAL;
@@ -1186,9 +1276,9 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
     return fail_prefill();
   for (int t = 0; t < nsteps; ++t) {
     op_prefill_chunk(s, c->prompts, c->plen, c->maxc, c->psched + (size_t)t * B, st);
-    target_forward(c, false);
+    target_forward(c, false, 8, c->tgt);
     op_prefill_save_last(c->hT32, c->plen, c->psched + (size_t)t * B, c->hlast, B, c->d, st);
-    drafter_ctx(c);
+    drafter_ctx(c, 8, c->dfc, c->dkv);
     mtp_advance(c);
     if ((t & 63) == 63 && cudaStreamSynchronize(st) != cudaSuccess) return fail_prefill();
   }
@@ -1232,7 +1322,12 @@ static int copy_out(dmtp_ctx* c, void* dst, const void* src, size_t bytes) {
 }
 
 int dmtp_round(dmtp_ctx* c, const dmtp_round_out* out, const int32_t* forced) {
-  if (!c) return DMTP_EINVAL;
+  return dmtp_round_depth(c, out, forced, 7);
+}
+
+int dmtp_round_depth(dmtp_ctx* c, const dmtp_round_out* out, const int32_t* forced, int depth) {
+  if (!c || depth < 0 || depth > 7 || (depth < 7 && !c->depths)) return DMTP_EINVAL;
+  if (out && out->draft_conf && !c->conf_on) return DMTP_EINVAL;
   if (c->poisoned) return DMTP_ESTATE;
   const int B = c->B;
   if (c->kv_bound + 16 >= c->maxc) {
@@ -1259,12 +1354,12 @@ int dmtp_round(dmtp_ctx* c, const dmtp_round_out* out, const int32_t* forced) {
   }
   if (eager) {
     c->launches = 0;
-    enqueue_round(c, dbg, forced ? c->forced : nullptr);
+    enqueue_round(c, dbg, forced ? c->forced : nullptr, depth);
     c->round_launches = c->launches;
   } else {
-    // one graph per mode; forced drafts are read from the context's own buffer, which
-    // the copy above fills before the replay
-    cudaGraphExec_t& graph = forced ? c->graph_forced : c->graph;
+    // one graph per mode and depth; forced drafts are read from the context's own buffer,
+    // which the copy above fills before the replay
+    cudaGraphExec_t& graph = forced ? c->graph_forced[depth] : c->graph[depth];
     if (!graph) {
       // capture records work without running it, on a private stream (the legacy
       // default stream cannot be captured); the graph is then replayed on c->st
@@ -1278,7 +1373,7 @@ int dmtp_round(dmtp_ctx* c, const dmtp_round_out* out, const int32_t* forced) {
         return DMTP_ECUDA;
       }
       c->launches = 0;
-      enqueue_round(c, dbg, forced ? c->forced : nullptr);
+      enqueue_round(c, dbg, forced ? c->forced : nullptr, depth);
       c->round_launches = c->launches;
       const cudaError_t ce = cudaStreamEndCapture(c->st, &g);
       c->st = user;
@@ -1305,6 +1400,7 @@ int dmtp_round(dmtp_ctx* c, const dmtp_round_out* out, const int32_t* forced) {
     e |= copy_out(c, out->snap_slot, s.snap_slot, (size_t)B * 4);
     e |= copy_out(c, out->delta, c->delta, (size_t)B * c->d * 4);
     e |= copy_out(c, out->mtp_len, s.mtp_len, (size_t)B * 4);
+    if (out->draft_conf) e |= copy_out(c, out->draft_conf, c->dconf, (size_t)B * 7 * 4);
     if (e) return DMTP_ECUDA;
   }
   return DMTP_OK;
@@ -1427,11 +1523,7 @@ int dmtp_set_draft_list(dmtp_ctx* c, const int32_t* ids, int n) {
   if (!c->list_cap || n < 0 || n > c->list_cap || (n > 0 && !ids)) return DMTP_EINVAL;
   for (int i = 0; i < n; ++i)
     if (ids[i] < 0 || ids[i] >= c->V || (i > 0 && ids[i] <= ids[i - 1])) return DMTP_EINVAL;
-  if ((n > 0) != (c->list_n > 0)) {  // the heads change: capture the round graphs again
-    if (c->graph) cudaGraphExecDestroy(c->graph);
-    if (c->graph_forced) cudaGraphExecDestroy(c->graph_forced);
-    c->graph = c->graph_forced = nullptr;
-  }
+  if ((n > 0) != (c->list_n > 0)) c->drop_graphs();  // the heads change: capture again
   c->list_n = n;
   if (n == 0) return DMTP_OK;
   // pageable host sources: each copy has left the caller's memory when the call returns
@@ -1456,8 +1548,7 @@ int dmtp_selftest_timeout(dmtp_ctx* c, uint64_t limit_ns) {
 
 void dmtp_free(dmtp_ctx* c) {
   if (!c) return;
-  if (c->graph) cudaGraphExecDestroy(c->graph);
-  if (c->graph_forced) cudaGraphExecDestroy(c->graph_forced);
+  c->drop_graphs();
   if (c->cap_st) cudaStreamDestroy(c->cap_st);
   for (cudaEvent_t e : c->pev) cudaEventDestroy(e);
   delete c;

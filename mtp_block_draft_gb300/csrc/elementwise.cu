@@ -403,8 +403,8 @@ __global__ void k_rope_kv(const float* __restrict__ src, int ld, int q_off, int 
                           T* __restrict__ Kc, T* __restrict__ Vc,
                           const int* __restrict__ base, const int* __restrict__ cseq,
                           const float2* __restrict__ tab, int hq, int hkv, int hd, int max_ctx,
-                          unsigned* err) {
-  const int m = blockIdx.x, b = m >> 3, s = m & 7;
+                          unsigned* err, int rg) {
+  const int m = blockIdx.x, b = m / rg, s = m % rg;
   const int cb = cseq ? cseq[b] : b;  // cache sequence of the row group
   const int pos = base[b] + s;
   const int half = hd / 2;
@@ -443,21 +443,21 @@ __global__ void k_rope_kv(const float* __restrict__ src, int ld, int q_off, int 
   }
 }
 
-// Vector form (rows = 8 per sequence, hd % 8 == 0, aligned rows): CTAs 0..rows-1 rotate
+// Vector form (rg rows per sequence, hd % 8 == 0, aligned rows): CTAs 0..rows-1 rotate
 // q and K of one row, four pairs per thread, 16-byte loads and 8/16-byte stores; CTAs
-// rows.. write the transposed V of one (sequence, kv head) for the sequence's 8 rows,
-// thread (dim, row) with the row fastest, so that the 8 new positions of a dimension
-// are one contiguous run.
+// rows.. write the transposed V of one (sequence, kv head) for the sequence's rg rows,
+// thread (dim, row) with the row fastest, so that the new positions of a dimension are
+// one contiguous run.
 template <typename T>
 __global__ void __launch_bounds__(256)
     k_rope_kv4(const float* __restrict__ src, int ld, int q_off, int k_off, int v_off,
                float* __restrict__ q_out, bf16* __restrict__ q_split, long q_lo,
                T* __restrict__ Kc, T* __restrict__ Vc, const int* __restrict__ base,
                const int* __restrict__ cseq, const float2* __restrict__ tab, int rows, int hq,
-               int hkv, int hd, int max_ctx, unsigned* err) {
+               int hkv, int hd, int max_ctx, unsigned* err, int rg) {
   const int half = hd / 2, nquad = half / 4;
   if ((int)blockIdx.x < rows) {
-    const int m = blockIdx.x, b = m >> 3, s = m & 7;
+    const int m = blockIdx.x, b = m / rg, s = m % rg;
     const int pos = base[b] + s;
     const bool pos_ok = pos >= 0 && pos < max_ctx;
     if (!pos_ok && threadIdx.x == 0) set_err(err, DMTP_ERR_POS);
@@ -495,11 +495,11 @@ __global__ void __launch_bounds__(256)
   } else {
     const int b = (blockIdx.x - rows) / hkv, h = (blockIdx.x - rows) % hkv;
     const int p0 = base[b], cb = cseq ? cseq[b] : b;
-    for (int idx = threadIdx.x; idx < hd * 8; idx += blockDim.x) {
-      const int s = idx & 7, i = idx >> 3;
+    for (int idx = threadIdx.x; idx < hd * rg; idx += blockDim.x) {
+      const int s = idx % rg, i = idx / rg;
       const int pos = p0 + s;
       if (pos < 0 || pos >= max_ctx) continue;  // reported by the row CTAs
-      const float v = src[(long)(b * 8 + s) * ld + v_off + h * hd + i];
+      const float v = src[(long)(b * rg + s) * ld + v_off + h * hd + i];
       Vc[(((long)cb * hkv + h) * (max_ctx / 64) + pos / 64) * hd * 64 + (long)i * 64 + pos % 64] =
           from_f32<T>(v);
     }
@@ -509,32 +509,33 @@ __global__ void __launch_bounds__(256)
 void op_rope_kv(int dt, const float* src, int ld, int q_off, int k_off, int v_off, float* q_out,
                 void* q_split, long q_lo, void* Kc, void* Vc, const int* base, const int* cseq,
                 const float2* tab, int rows, int hq, int hkv, int hd, int max_ctx, unsigned* err,
-                cudaStream_t st) {
+                cudaStream_t st, int rg) {
   const unsigned ek = dt ? 8 : 16;
-  const bool vec = rows % 8 == 0 && hd % 8 == 0 && ld % 4 == 0 && aligned_to(src, 16) &&
+  if (rg < 1 || rg > 8 || rows % rg) return;  // the host only passes whole row groups
+  const bool vec = hd % 8 == 0 && ld % 4 == 0 && aligned_to(src, 16) &&
                    aligned_to(tab, 16) && k_off % 4 == 0 && aligned_to(Kc, ek) &&
                    (q_off < 0 || (q_off % 4 == 0 &&
                                   (q_split ? aligned_to(q_split, 8) && q_lo % 4 == 0
                                            : aligned_to(q_out, 16))));
   if (vec) {
     if (dt)
-      k_rope_kv4<bf16><<<rows + rows / 8 * hkv, 256, 0, st>>>(
+      k_rope_kv4<bf16><<<rows + rows / rg * hkv, 256, 0, st>>>(
           src, ld, q_off, k_off, v_off, q_out, (bf16*)q_split, q_lo, (bf16*)Kc, (bf16*)Vc, base,
-          cseq, tab, rows, hq, hkv, hd, max_ctx, err);
+          cseq, tab, rows, hq, hkv, hd, max_ctx, err, rg);
     else
-      k_rope_kv4<float><<<rows + rows / 8 * hkv, 256, 0, st>>>(
+      k_rope_kv4<float><<<rows + rows / rg * hkv, 256, 0, st>>>(
           src, ld, q_off, k_off, v_off, q_out, nullptr, 0, (float*)Kc, (float*)Vc, base, cseq,
-          tab, rows, hq, hkv, hd, max_ctx, err);
+          tab, rows, hq, hkv, hd, max_ctx, err, rg);
     return;
   }
   if (dt)
     k_rope_kv<bf16><<<rows, 256, 0, st>>>(src, ld, q_off, k_off, v_off, q_out, (bf16*)q_split,
                                           q_lo, (bf16*)Kc, (bf16*)Vc, base, cseq, tab, hq, hkv,
-                                          hd, max_ctx, err);
+                                          hd, max_ctx, err, rg);
   else
     k_rope_kv<float><<<rows, 256, 0, st>>>(src, ld, q_off, k_off, v_off, q_out, nullptr, 0,
                                            (float*)Kc, (float*)Vc, base, cseq, tab, hq, hkv, hd,
-                                           max_ctx, err);
+                                           max_ctx, err, rg);
 }
 
 // L2 flush: read `bytes` (a multiple of 16) of device memory; the sum is only written if
@@ -625,28 +626,33 @@ void op_gather_rows(const void* src, void* dst, size_t row_bytes, const int* ids
                                    src_s, dst_s);
 }
 
-__global__ void k_verify_tokens(RoundState s) {
+__global__ void k_verify_tokens(RoundState s, int depth) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= s.B * 8) return;
-  const int b = i >> 3, r = i & 7;
-  s.tok[i] = (r == 0) ? s.A[b] : s.drafts[b * 7 + r - 1];
+  const int G = depth + 1, b = i >> 3, j = i & 7;
+  if (i < s.B * G) {
+    const int bb = i / G, r = i % G;
+    s.tok[i] = (r == 0) ? s.A[bb] : s.drafts[bb * 7 + r - 1];
+  }
+  if (j > depth) s.g[b * 8 + j] = -1;  // no pick past the verified rows
+  if (j == 0) s.rows_valid[b] = G;
 }
 
-void op_verify_tokens(const RoundState& s, cudaStream_t st) {
-  k_verify_tokens<<<cdiv(s.B * 8, 256), 256, 0, st>>>(s);
+void op_verify_tokens(const RoundState& s, int depth, cudaStream_t st) {
+  k_verify_tokens<<<cdiv(s.B * 8, 256), 256, 0, st>>>(s, depth);
 }
 
 // Greedy prefix acceptance ([DMTP] §5): n = longest prefix with T_j == g_{j-1};
 // commit T_1..T_n and the target's pick g_n; kv_len <- pos0 + n + 1; A <- g_n.
 // Also prepares the MTP advance rows (tokens x_{pos0+1+s} = committed[s]) and swaps
 // the GDN snapshot slot n in as the live state (pointer swap, nothing copied).
-__global__ void k_accept(RoundState s) {
+__global__ void k_accept(RoundState s, int depth) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= s.B) return;
   const int* T = s.drafts + b * 7;
   const int* g = s.g + b * 8;
   int n = 0;
-  while (n < 7 && T[n] == g[n]) ++n;
+  while (n < depth && T[n] == g[n]) ++n;
   int* c = s.committed + b * 8;
   for (int j = 0; j < 8; ++j) c[j] = (j < n) ? T[j] : (j == n ? g[n] : -1);
   for (int j = 0; j < 8; ++j) s.mtp_tok[b * 8 + j] = (j <= n) ? c[j] : g[n];
@@ -659,7 +665,7 @@ __global__ void k_accept(RoundState s) {
   s.mtp_cnt[b] = n + 1;
   s.snap_slot[b] = s.n_gdn > 0 ? n : -1;
   atomicAdd(&s.hist[n], 1ull);
-  if (n < 7) {
+  if (n < depth) {  // the live state is the one after row `depth`; slot n holds row n's
     for (int l = 0; l < s.n_gdn; ++l) {
       int* live = s.gdn_live + l * s.B + b;
       int* slot = s.gdn_slot + ((long)l * s.B + b) * 8;
@@ -670,8 +676,8 @@ __global__ void k_accept(RoundState s) {
   }
 }
 
-void op_accept(const RoundState& s, cudaStream_t st) {
-  k_accept<<<cdiv(s.B, 64), 64, 0, st>>>(s);
+void op_accept(const RoundState& s, int depth, cudaStream_t st) {
+  k_accept<<<cdiv(s.B, 64), 64, 0, st>>>(s, depth);
 }
 
 __global__ void k_gather_hmtp(const float* __restrict__ x, const int* __restrict__ cnt,

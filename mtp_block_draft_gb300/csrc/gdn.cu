@@ -1,4 +1,5 @@
-// Gated DeltaNet recurrence over the 8 verify rows with per-row state snapshots.
+// Gated DeltaNet recurrence over the verify rows (8, or fewer in a verify of fewer
+// drafts) with per-row state snapshots.
 //
 // Per head: q, k L2-normalised; alpha = sigmoid(a), beta = sigmoid(b);
 //   S <- alpha * S (I - beta k k^T) + beta v k^T  =  alpha * S + u k^T,
@@ -43,8 +44,8 @@ __global__ void __launch_bounds__(256) k_gdn(GdnArgs a) {
 #pragma unroll
   for (int c = 0; c < 64; ++c) S[c] = (c < cpt) ? Sl[c] : 0.f;
   const int nv = a.rows_valid[b];
-  for (int r = 0; r < 8; ++r) {
-    const float* row = a.qkvab + (long)(b * 8 + r) * a.ld;
+  for (int r = 0; r < a.rows; ++r) {
+    const float* row = a.qkvab + (long)(b * a.rows + r) * a.ld;
     const float qv = threadIdx.x < dk ? row[h * dk + threadIdx.x] : 0.f;
     const float kv = threadIdx.x < dk ? row[a.H * dk + h * dk + threadIdx.x] : 0.f;
     const float qn = block_sum(qv * qv, red);
@@ -72,8 +73,8 @@ __global__ void __launch_bounds__(256) k_gdn(GdnArgs a) {
     for (int c = 0; c < 64; ++c)
       if (c < cpt) o += S[c] * qs[j0 + c];
     for (int w = TPR >> 1; w > 0; w >>= 1) o += __shfl_xor_sync(0xffffffffu, o, w);
-    if (sub == 0) store_act((T*)a.out + (long)(b * 8 + r) * a.H * dv + h * dv + i, a.out_lo, o);
-    if (a.snapshots && r < 7) {
+    if (sub == 0) store_act((T*)a.out + (long)(b * a.rows + r) * a.H * dv + h * dv + i, a.out_lo, o);
+    if (a.snapshots && r < a.rows - 1) {
       float* Sd = Sbuf + ((long)a.slot[b * 8 + r] * a.H + h) * hstride + (long)i * dk + j0;
 #pragma unroll
       for (int c = 0; c < 64; ++c)
@@ -134,8 +135,8 @@ __global__ void __launch_bounds__(128, 4) k_gdn_cols(GdnArgs a) {
   const int b = bh / H, h = bh % H;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // warp w prepares rows w and w + 4
-  for (int r = w; r < 8; r += 4) {
-    const float* row = a.qkvab + (long)(b * 8 + r) * a.ld;
+  for (int r = w; r < a.rows; r += 4) {
+    const float* row = a.qkvab + (long)(b * a.rows + r) * a.ld;
     float q[CW], k[CW];
     load_cw<CW>(row + h * DK + CW * lane, q);
     load_cw<CW>(row + H * DK + h * DK + CW * lane, k);
@@ -175,7 +176,7 @@ __global__ void __launch_bounds__(128, 4) k_gdn_cols(GdnArgs a) {
   for (int t = 0; t < 16; ++t) load_cw<CW>(Sbuf + (long)live * H * hs + off + t * DK, S[t]);
   const int nv = a.rows_valid[b];
   const int t_own = lane & 15;
-  for (int r = 0; r < 8; ++r) {
+  for (int r = 0; r < a.rows; ++r) {
     float k[CW], q[CW];
     load_cw<CW>(&ks[r][CW * lane], k);
     load_cw<CW>(&qs[r][CW * lane], q);
@@ -198,7 +199,7 @@ __global__ void __launch_bounds__(128, 4) k_gdn_cols(GdnArgs a) {
     const float u_own = __shfl_sync(0xffffffffu, u, t_own);
     const bool upd = r < nv;
     if (lane >= 16)
-      store_act((T*)a.out + (long)(b * 8 + r) * H * dv + h * dv + i0 + t_own, a.out_lo,
+      store_act((T*)a.out + (long)(b * a.rows + r) * H * dv + h * dv + i0 + t_own, a.out_lo,
                 upd ? al * x + u_own * kqs[r] : x);
     if (upd) {
 #pragma unroll
@@ -208,7 +209,7 @@ __global__ void __launch_bounds__(128, 4) k_gdn_cols(GdnArgs a) {
         for (int c = 0; c < CW; ++c) S[t][c] = al * S[t][c] + ut * k[c];
       }
     }
-    if (a.snapshots && r < 7) {
+    if (a.snapshots && r < a.rows - 1) {
       float* Sd = Sbuf + (long)a.slot[b * 8 + r] * H * hs + off;
 #pragma unroll
       for (int t = 0; t < 16; ++t) store_cw<CW>(Sd + t * DK, S[t]);
@@ -220,6 +221,7 @@ __global__ void __launch_bounds__(128, 4) k_gdn_cols(GdnArgs a) {
 }
 
 void op_gdn(int dt, const GdnArgs& a, cudaStream_t st) {
+  if (a.rows < 1 || a.rows > 8) return;  // the host passes 1..8 rows per sequence
   const bool cols = (a.dk == 64 || a.dk == 128) && a.dv % 64 == 0 && a.ld % 4 == 0 &&
                     aligned_to(a.qkvab, 16) && aligned_to(a.states, 16);
   if (cols) {

@@ -42,7 +42,31 @@ struct HeadArgs {
   const float* xscale;  // E4M3 operands: per token row scale
   const int* vdev;      // token list: rows scored (device, read at launch), else null
   const int* vmap;      // token list: token id of each row (debug logits), else null
+  float2* conf;         // confidence partials [grid * EW/4][M] (max, windowed sum), or null
 };
+
+// Window of the head confidence: scores more than this far below the best are left out
+// of the normalising sum (the colibri page's per-step estimate for MTP-style heads).
+constexpr float kConfWindow = 20.f;
+
+// Running (max, sum of exp(l - max) over l >= max - window) of one token row over 16
+// columns: lim valid columns; FP8: the accumulators times the column scales and the row's
+// own scale xs give the logits.
+template <bool FP8>
+__device__ __forceinline__ void conf16(const uint32_t (&r)[16], int n0, int lim, float xs,
+                                       const float* wscale, float& cm, float& cs) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    if (j >= lim) break;
+    const float x = __uint_as_float(r[j]) * (FP8 ? wscale[n0 + j] * xs : 1.f);
+    if (x > cm) {
+      cs = cs * __expf(cm - x) + 1.f;  // cm = -inf: cs = 0 * 0 + 1
+      cm = x;
+    } else if (x >= cm - kConfWindow) {
+      cs += __expf(x - cm);
+    }
+  }
+}
 
 // D[tmem] (+)= A[smem] * B[smem]^T, E4M3 inputs, fp32 accumulate (kind::f8f6f4).
 __device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
@@ -226,11 +250,13 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
     const int q = warp & 3;           // TMEM lane quarter this warp may read
     const int grp = (warp - 2) >> 2;  // which of the quarter's EW / 4 warps
     int m[TH], pos[TH], seq[TH], bidx[TH];
-    float best[TH];
+    float best[TH], cm[TH], cs[TH];
 #pragma unroll
     for (int h = 0; h < TH; ++h) {
       m[h] = h * 128 + q * 32 + lane;
       best[h] = -__int_as_float(0x7f800000);  // -inf
+      cm[h] = best[h];
+      cs[h] = 0.f;
       bidx[h] = -1;
       pos[h] = seq[h] = 0;
       if (SAMPLE) {
@@ -268,6 +294,11 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
               if (c + 16 + j < lim) lr[a.vmap ? a.vmap[v1] : v1] = __uint_as_float(r1[j]) * w1;
             }
           }
+          if (a.conf && m[h] < a.M) {  // the head's confidence (greedy draft heads)
+            const float xs = FP8 ? a.xscale[m[h]] : 1.f;
+            conf16<FP8>(r0, n0 + c, lim - c, xs, a.wscale, cm[h], cs[h]);
+            conf16<FP8>(r1, n0 + c + 16, lim - c - 16, xs, a.wscale, cm[h], cs[h]);
+          }
           if (c + 32 <= lim) {
             scan16<SAMPLE, true, FP8>(r0, n0 + c, 0, best[h], bidx[h], a.smp, pos[h], seq[h],
                                       a.wscale);
@@ -289,6 +320,12 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
 #pragma unroll
     for (int h = 0; h < TH; ++h)
       if (m[h] < a.M && bidx[h] >= 0) atomicMax(&a.keys[m[h]], argmax_key(best[h], bidx[h]));
+    if (a.conf) {  // this thread's partial of its rows, combined by op_conf_combine
+      const long part = (long)blockIdx.x * (EW / 4) + grp;
+#pragma unroll
+      for (int h = 0; h < TH; ++h)
+        if (m[h] < a.M) a.conf[part * a.M + m[h]] = make_float2(cm[h], cs[h]);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -391,16 +428,45 @@ void launch(const HeadPlan& p, const HeadArgs& a, bool sample, cudaStream_t st) 
 }
 
 void op_head_tc(const HeadPlan& p, unsigned long long* keys, float* logits, long ldl,
-                const SampleArgs* smp, unsigned* err, cudaStream_t st) {
+                const SampleArgs* smp, unsigned* err, cudaStream_t st, float2* conf) {
   // the E4M3 draft heads never sample (only the verify head does)
   const bool sample = !p.fp8 && smp && smp->scale2 > 0.f;
   const HeadArgs a{p.V,  p.K,    p.M,   p.MT, p.stages, p.tiles,
                    keys, logits, ldl,   sample ? *smp : SampleArgs{}, err, p.wscale, p.xscale,
-                   p.vdev, p.vmap};
+                   p.vdev, p.vmap, sample ? nullptr : conf};
   if (p.NV == 128)
     p.TH == 1 ? launch<128, 1>(p, a, sample, st) : launch<128, 2>(p, a, sample, st);
   else
     p.TH == 1 ? launch<256, 1>(p, a, sample, st) : launch<256, 2>(p, a, sample, st);
+}
+
+}  // namespace dmtp
+
+namespace dmtp {
+
+// Confidence of each head row from the partials: M* = the largest partial maximum, S =
+// sum over partials within the window of M* of sum_i exp(max_i - M*), conf = 1 / S.
+// Row m goes to dst[(m / per) * stride + off + m % per].
+__global__ void k_conf_combine(const float2* __restrict__ parts, int nparts, int M, int per,
+                               float* dst, int stride, int off) {
+  const int m = blockIdx.x * blockDim.x + threadIdx.x;
+  if (m >= M) return;
+  float mx = -__int_as_float(0x7f800000);
+  for (int i = 0; i < nparts; ++i) mx = fmaxf(mx, parts[(long)i * M + m].x);
+  float S = 0.f;
+  for (int i = 0; i < nparts; ++i) {
+    const float2 p = parts[(long)i * M + m];
+    if (p.y > 0.f && p.x >= mx - kConfWindow) S += p.y * __expf(p.x - mx);
+  }
+  dst[(m / per) * stride + off + m % per] = S > 0.f ? 1.f / S : 0.f;
+}
+
+int head_conf_parts(const HeadPlan& p) { return p.grid * (p.ew / 4); }
+
+void op_conf_combine(const HeadPlan& p, const float2* parts, int per, float* dst, int stride,
+                     int off, cudaStream_t st) {
+  k_conf_combine<<<(p.M + 127) / 128, 128, 0, st>>>(parts, head_conf_parts(p), p.M, per, dst,
+                                                     stride, off);
 }
 
 }  // namespace dmtp

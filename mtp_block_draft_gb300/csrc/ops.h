@@ -55,13 +55,14 @@ void op_build_slots(int dt, const void* E, int vocab, const int* A, const int* d
 // write target that is never written in practice.
 void op_l2_flush(const void* buf, size_t bytes, unsigned* sink, cudaStream_t st);
 void op_swiglu(int dt, const float* gu, void* h, long h_lo, int rows, int F, cudaStream_t st);
-// RoPE (table) + cache write. src rows m = b*8 + s at position base[b] + s.
+// RoPE (table) + cache write. src rows m = b*rg + s at position base[b] + s (rg rows per
+// sequence: 8, or fewer in a verify of fewer drafts).
 // q_off < 0: no q. q_out fp32 [rows][hq][hd], or, when q_split != null (bf16 models),
 // q as a bf16 pair: hi at q_split, remainder at q_split + q_lo (elements).
 void op_rope_kv(int dt, const float* src, int ld, int q_off, int k_off, int v_off, float* q_out,
                 void* q_split, long q_lo, void* Kc, void* Vc, const int* base, const int* cseq,
                 const float2* tab, int rows, int hq, int hkv, int hd, int max_ctx, unsigned* err,
-                cudaStream_t st);
+                cudaStream_t st, int rg = 8);
 // fp32 -> dt copy of rows (with row map)
 void op_cast_rows(int dt, const float* x, int ldx, void* y, int ldy, long y_lo, int rows, int d,
                   RowMap map, cudaStream_t st);
@@ -103,8 +104,12 @@ void op_keys_to_ids(const unsigned long long* keys, int B, int per, int* dst, in
 // 16, 16-byte aligned rows) for i < n; with scale arrays, dst_s[i] = src_s[ids[i]].
 void op_gather_rows(const void* src, void* dst, size_t row_bytes, const int* ids, int n,
                     const float* src_s, float* dst_s, cudaStream_t st);
-void op_verify_tokens(const RoundState& s, cudaStream_t st);
-void op_accept(const RoundState& s, cudaStream_t st);
+// Verify rows of a round that carries `depth` drafts (0..7): rows [A, T1..T_depth] of each
+// sequence, row m = b*(depth+1) + r; picks past the depth cleared to -1; rows_valid set.
+void op_verify_tokens(const RoundState& s, int depth, cudaStream_t st);
+// Prefix acceptance over the first `depth` drafts (n <= depth); the live recurrent state
+// is the one after row depth, so slot n is swapped in when n < depth.
+void op_accept(const RoundState& s, int depth, cudaStream_t st);
 // h_mtp[b] = x[b*8 + cnt[b]-1]
 void op_gather_hmtp(const float* x, const int* cnt, float* h_mtp, int B, int d, cudaStream_t st);
 // Prefill step: row group pb takes chunk sched[pb] = (sequence, chunk of 8 positions);
@@ -139,6 +144,8 @@ struct AttnArgs {
   long qs_lo;          // ... and remainder at qs + qs_lo
   int pgrid;           // tensor-core path: persistent CTAs; partials [pgrid + B*hkv]
   int ptk;             // tensor-core path: keys per tile (kAttnTile)
+  int rows = 8;        // rows per sequence (a verify of fewer drafts has fewer): row m of
+                       // q / out is sequence m / rows at position base + m % rows
 };
 void op_attention(int dt, const AttnArgs& a, cudaStream_t st);
 void op_attention_merge(int dt, const AttnArgs& a, cudaStream_t st);
@@ -263,8 +270,16 @@ int head_plan_e4m3(HeadPlan* p, const void* W8, const float* wscale, int V, int 
                    const void* X8, const float* xscale, int M, int nsm, int nv, int ew);
 // logits (optional, fp32 [M][ldl]) receives the raw logits; smp: sampled picks (nullptr:
 // argmax of the logits). keys must hold zeros (or earlier keys to combine with).
+// conf (optional, greedy heads only): per-thread partials of the head's confidence, the
+// probability it gives its own pick over the scores within 20 of the best (max and
+// windowed sum; head_conf_parts(p) x M float2), combined by op_conf_combine.
 void op_head_tc(const HeadPlan& p, unsigned long long* keys, float* logits, long ldl,
-                const SampleArgs* smp, unsigned* err, cudaStream_t st);
+                const SampleArgs* smp, unsigned* err, cudaStream_t st, float2* conf = nullptr);
+int head_conf_parts(const HeadPlan& p);
+// dst[(m / per) * stride + off + m % per] = 1 / sum over the scores within 20 of the best
+// of exp(score - best), row m of the head's M rows.
+void op_conf_combine(const HeadPlan& p, const float2* parts, int per, float* dst, int stride,
+                     int off, cudaStream_t st);
 int head_init_attributes();
 
 // ---- gdn.cu ----------------------------------------------------------------------------
@@ -275,7 +290,8 @@ struct GdnArgs {
   const int* live;       // [B]
   const int* slot;       // [B][8]
   const int* rows_valid; // [B]
-  int snapshots;         // 1: write the state after each row r < 7 to buffer slot[b][r]
+  int snapshots;         // 1: write the state after each row r < rows-1 to slot[b][r]
+  int rows = 8;          // rows per sequence (row m of qkvab / out: sequence m / rows)
   void* out;             // [B*8][H*dv] dt
   long out_lo;           // element offset of the remainder half (0: none)
   int B, H, dk, dv;

@@ -575,10 +575,14 @@ class OracleModel:
                                      log, f"T{s + 2}"))
         if forced is not None:
             drafts = [T1] + [int(t) for t in forced[1:7]]
-        if callable(depth):
+        if callable(depth) or want_logits:
+            # each head's probability of its own pick over the scores it makes (the listed
+            # tokens when a list is set), within the window of its best
             from .gate import head_confidence
-            conf = [head_confidence(t1_logits)] + [head_confidence(dlog[s]) for s in range(6)]
+            conf = [head_confidence(listed(t1_logits))] + [head_confidence(listed(dlog[s]))
+                                                          for s in range(6)]
             rec["draft_confidence"] = conf
+        if callable(depth):
             depth = depth(list(drafts), conf)
         depth = int(depth)
         if not 0 <= depth <= 7:

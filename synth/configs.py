@@ -70,6 +70,10 @@ class DmtpConfig:
     draft_head_fp8: bool = False
     # capacity of the draft heads' token list (0: no list; bf16 models only)
     draft_list_cap: int = 0
+    # the context can run verifies of fewer drafts (round depth 0..6)
+    variable_depth: bool = False
+    # the draft heads also report the confidence of their picks
+    draft_confidence: bool = False
 
     def __post_init__(self):
         if not self.layer_kinds:

@@ -69,32 +69,42 @@ class Lockstep:
         return e
 
     def step(self, forced: np.ndarray | None = None, floats: bool = True, tol: float = 2e-2,
-             draft_list: np.ndarray | None = None):
+             draft_list: np.ndarray | None = None, depth: int = 7):
         """draft_list: boolean mask [V] of the tokens the draft heads score (the list the
         GPU context was given with set_draft_list); the draft logits are then compared at
-        the listed tokens only."""
+        the listed tokens only. depth: drafts the verify carries (dmtp_round_depth): the
+        picks past it must be -1 and the verify logits come as B (depth + 1) rows."""
         g = self.gpu
         out = g.alloc_out(ints=True, floats=floats)
         ft = None
         if forced is not None:
             ft = torch.as_tensor(np.asarray(forced, np.int32), device=g.device)
-        g.round(out, forced=ft)
+        g.round(out, forced=ft, depth=depth)
         torch.cuda.synchronize()
         o = {k: to_np(v) for k, v in out.items()}
+        G = depth + 1
+        if floats:  # sequence-major [B][G][V] at the start of the buffer
+            V = self.cfg.vocab
+            o["verify_logits"] = o["verify_logits"].reshape(-1)[:self.gpu.B * G * V].reshape(
+                self.gpu.B, G, V)
+        picks_all = o["picks"]
+        o["picks"] = picks_all[:, :G]
         recs = {}
         for b in self.seqs:
             adopt = {"g": o["picks"][b]}
             if forced is None:
                 adopt["T"] = o["drafts"][b]
+            assert all(int(x) == -1 for x in picks_all[b][G:]), (b, picks_all[b])
             rec = self.oracle.round(self.states[b],
                                     forced=None if forced is None else forced[b],
-                                    adopt=adopt, want_logits=floats, draft_list=draft_list)
+                                    adopt=adopt, want_logits=floats, draft_list=draft_list,
+                                    depth=depth)
             frec = None
             if self.floor_oracle is not None:
                 frec = self.floor_oracle.round(self.floor_states[b],
                                                forced=None if forced is None else forced[b],
                                                adopt=adopt, want_logits=floats,
-                                               draft_list=draft_list)
+                                               draft_list=draft_list, depth=depth)
                 assert not frec["log"]["mismatch"], (b, frec["log"]["mismatch"])
             log = rec["log"]
             assert not log["mismatch"], (b, log["mismatch"])
@@ -137,6 +147,14 @@ class Lockstep:
                     floor = self._err(name + "_bf16kv_floor", sel(frec[key]), sel(rec[key]))
                     assert ef <= tol, (b, name, "vs the bf16-KV oracle", ef)
                     assert e <= tol + floor, (b, name, e, floor)
+            if floats and "draft_conf" in o:
+                # confidence 1 / sum exp(l - l_max): logits within tol of the oracle's move
+                # each term's exponent by at most 2 tol
+                ref = np.asarray(rec["draft_confidence"], np.float64)
+                rel = np.abs(np.asarray(o["draft_conf"][b], np.float64) - ref) / ref
+                self.max_err["draft_conf_rel"] = max(self.max_err.get("draft_conf_rel", 0.0),
+                                                     float(rel.max()))
+                assert rel.max() <= np.expm1(2 * tol), (b, "draft_conf", rel.max())
             recs[b] = rec
         return o, recs
 

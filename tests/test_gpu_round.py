@@ -370,3 +370,80 @@ def test_draft_list_needs_capacity():
         g.set_draft_list([1, 2, 3])
     assert e.value.code == -1
     g.close()
+
+
+# verifies of fewer drafts (colibri draft-depth gate): rounds at depths 0..7
+DEPTHS = (7, 3, 0, 5, 1, 6, 2, 4, 0, 7)
+
+
+def _greedy_next(ls, b, n):
+    """The next n tokens of plain greedy decoding from the oracle's state of sequence b."""
+    st = ls.states[b].clone()
+    out, tok, pos = [], st.A, st.a
+    for _ in range(n):
+        _, _, logits, _ = ls.oracle.target_rows(st, [tok], pos)
+        tok, pos = int(np.argmax(logits[0])), pos + 1
+        out.append(tok)
+    return out
+
+
+@pytest.mark.parametrize("name", ["tiny", "b32_r", "hybrid_r"])
+def test_variable_depth_rounds(name):
+    """dmtp_round_depth at every depth 0..7, natural drafts and drafts forced to the greedy
+    continuation with one wrong row, in lock-step with the oracle's round(depth=k): at most
+    k drafts accepted, the verify over k + 1 rows, a recurrent target's slot n swapped in
+    below depth k and the live state kept at n = k."""
+    from lockstep import Lockstep
+    base = {"tiny": TINY, "b32_r": B32_R.replace(batch=8), "hybrid_r": HYB_R}[name]
+    cfg = base.replace(name=base.name + "_depth", variable_depth=True)
+    ls = Lockstep(cfg, make_weights(cfg, "cuda"), make_prompts(cfg), rounds=len(DEPTHS))
+    seen = set()
+    for r, depth in enumerate(DEPTHS):
+        forced = None
+        if r % 2 == 1:
+            forced = np.array([_greedy_next(ls, b, 7) for b in range(cfg.batch)], np.int32)
+            w = (3 * r) % 8
+            if w < 7:
+                forced[:, w] = (forced[:, w] + 1) % (cfg.vocab - 1)
+        o, recs = ls.step(forced=forced, depth=depth, tol=TOL)
+        for b, rec in recs.items():
+            assert rec["n"] <= depth and int(o["n_accepted"][b]) == rec["n"]
+            seen.add((depth, rec["n"]))
+    assert any(n == d and d > 0 for d, n in seen)     # a full accept below depth 7
+    assert any(0 < n < d for d, n in seen)            # a rejection inside a short verify
+    ls.close()
+
+
+def test_depth_needs_variable_depth_context():
+    from mtp_block_draft_gb300 import DmtpError, DmtpRound, default_max_ctx
+    prompts = make_prompts(B32_R)
+    g = DmtpRound(B32_R, make_weights(B32_R, "cuda"), prompts, default_max_ctx(prompts, 2))
+    for depth in (3, -1, 8):
+        with pytest.raises(DmtpError) as e:
+            g.round(depth=depth)
+        assert e.value.code == -1
+    g.round(depth=7)
+    g.close()
+
+
+@pytest.mark.parametrize("variant", ["bf16", "fp8", "list"])
+def test_draft_confidence(variant):
+    """The draft heads' confidence of their own picks (draft_confidence; the colibri
+    page's per-step estimate: 1 / sum of exp(l - l_max) over the scores within 20 of the
+    best), per draft T1..T7, against the oracle's head_confidence: bf16 heads, E4M3 heads,
+    and heads over a token list (the sum over the listed tokens)."""
+    from lockstep import Lockstep
+    cfg = B32_R.replace(name="b32_r_conf", batch=4, ctx_lo=40, ctx_hi=80, draft_confidence=True,
+                        draft_head_fp8=variant == "fp8",
+                        draft_list_cap=B32_R.vocab if variant == "list" else 0)
+    ls = Lockstep(cfg, make_weights(cfg, "cuda"), make_prompts(cfg), rounds=4)
+    mask = None
+    if variant == "list":
+        ids = np.arange(0, cfg.vocab, 7, dtype=np.int32)  # every 7th token
+        mask = np.zeros(cfg.vocab, bool)
+        mask[ids] = True
+        ls.gpu.set_draft_list(ids)
+    for _ in range(3):
+        o, recs = ls.step(tol=TOL, draft_list=mask)
+        assert (o["draft_conf"] > 0).all() and (o["draft_conf"] <= 1).all()
+    ls.close()
