@@ -344,8 +344,17 @@ def draft_list_round(cfg, weights, prompts, warmup, steps, size=16000):
     _, A, _ = g.read_state()
     vl.picked(A)
     ids = vl.ids()
-    g.set_draft_list(ids)
+    rule_listed = int(len(ids))
     vl.close()
+    kind = "the page's rule"
+    if len(ids) > cfg.vocab // 2:
+        # Uniform random prompts: halvings every 1024 counted tokens leave almost every
+        # count at 0 or 1, so the rule lists (nearly) every token. Time the page's default
+        # list size instead: the `size` most counted prompt tokens (ties to the lower id).
+        cnt = np.bincount(np.concatenate(prompts), minlength=cfg.vocab)
+        ids = np.sort(np.lexsort((np.arange(cfg.vocab), -cnt))[:size]).astype(np.int32)
+        kind = f"the {size} most counted prompt tokens (the page's default list size)"
+    g.set_draft_list(ids)
     for _ in range(warmup):
         g.round()
     _, _, h0 = g.read_state()
@@ -363,7 +372,8 @@ def draft_list_round(cfg, weights, prompts, warmup, steps, size=16000):
     dh = (h1 - h0).astype(np.int64)
     mean_len = float(np.sum((np.arange(8) + 1) * dh)) / max(1, int(dh.sum()))
     rps = steps / (ms / 1e3)
-    return {"listed_tokens": int(len(ids)), "vocab": cfg.vocab, "rounds_per_s": rps,
+    return {"listed_tokens": int(len(ids)), "list": kind, "rule_listed": rule_listed,
+            "vocab": cfg.vocab, "rounds_per_s": rps,
             "ms_per_step": ms / steps, "mean_accept_len": mean_len,
             "tokens_per_s": len(prompts) * rps * mean_len, "steps": steps, "warmup": warmup,
             "lm_head_ms_per_round": class_ms(prof, ms / steps, "lm_head"),
@@ -372,6 +382,48 @@ def draft_list_round(cfg, weights, prompts, warmup, steps, size=16000):
                     "workspace); the verify head scores the whole vocabulary. With uniform "
                     "random prompts the conversation alone lists most of the batch's prompt "
                     "tokens"}
+
+
+def depth_rounds(cfg, weights, prompts, warmup=4, steps=30):
+    """Round time at each verify depth k = 0..7 (dmtp_round_depth: the verify carries k
+    drafts as B (k + 1) rows), graph replays timed with CUDA events, at this batch and at
+    batch 1 (the batch's first prompt); then the native draft-depth gate (colibri page)
+    fed with T(n) = the round time at depth n - 1 and the page's MTP-head starting
+    acceptances picks a depth for each batch."""
+    import torch
+    from mtp_block_draft_gb300 import DmtpGate, DmtpRound
+    cd = cfg.replace(variable_depth=True)
+    res = {}
+    for label, ps in ((f"B{len(prompts)}", prompts), ("B1", prompts[:1])):
+        R = 8 * (warmup + steps) + 8
+        g = DmtpRound(cd, weights, ps, max(len(p) for p in ps) + 8 * R + 64)
+        ms = []
+        for depth in range(8):
+            for _ in range(warmup):
+                g.round(depth=depth)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(g.stream)
+            for _ in range(steps):
+                g.round(depth=depth)
+            e1.record(g.stream)
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1) / steps)
+        g.close()
+        del g
+        gate = DmtpGate(7)
+        for n in range(1, 9):
+            gate.forward(n, ms[n - 1] / 1e3)
+        k, v = gate.pick(7)
+        st = gate.read()
+        gate.close()
+        res[label] = {"round_ms_by_depth": [round(x, 4) for x in ms],
+                      "gate_pick": {"depth": k, "value": v, "rho": st["rho"],
+                                    "acceptance_priors": st["a"][:3]}}
+    res["note"] = ("T(n) = whole-round time at depth n - 1: the drafting part (MTP head, "
+                   "fusion, block drafter) is the same at every depth; the gate runs on the "
+                   "page's starting acceptances (trained-model values), not on the random "
+                   "weights' near-zero acceptance")
+    return res
 
 
 def hybrid_round(warmup, steps, hbm_gbs):
@@ -479,7 +531,7 @@ def run_reference(args, cfg):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="b32")
@@ -495,6 +547,8 @@ def main():
                     help="timed rounds of the forced-accept run (0: skip)")
     ap.add_argument("--fp8-steps", type=int, default=100,
                     help="timed rounds of the run with E4M3 draft heads (0: skip)")
+    ap.add_argument("--depth-steps", type=int, default=30,
+                    help="timed rounds per verify depth 0..7 at B32 and B1 (0: skip)")
     ap.add_argument("--list-steps", type=int, default=100,
                     help="timed rounds of the run with the draft heads over the token list "
                          "(0: skip)")
@@ -707,6 +761,8 @@ def main():
         line["forced_accept"] = forced_accept(cfg, weights, prompts, 4, args.forced_steps)
     if args.fp8_steps > 0 and world == 1 and cfg.dtype == "bf16" and cfg.d_model % 128 == 0:
         line["fp8_draft_heads"] = fp8_draft_heads(cfg, weights, prompts, 16, args.fp8_steps)
+    if args.depth_steps > 0 and world == 1:
+        line["depth"] = depth_rounds(cfg, weights, prompts, 4, args.depth_steps)
     if args.list_steps > 0 and world == 1 and cfg.dtype == "bf16":
         line["draft_list"] = draft_list_round(cfg, weights, prompts, 16, args.list_steps)
     if args.hybrid_steps > 0 and world == 1 and args.config == "b32" and args.layers is None:
