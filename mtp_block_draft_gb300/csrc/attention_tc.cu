@@ -114,6 +114,15 @@ __device__ __forceinline__ int vis_lo(const AttnArgs& a, int base) {
 __device__ __forceinline__ int vis_tiles(const AttnArgs& a, int base, int tk) {
   return (base + a.rows - 1) / tk - vis_lo(a, base) / tk + 1;
 }
+// Work units of a (sequence, kv head) segment in the even split over the CTAs: its key
+// tiles plus kPieceCost units standing for the fixed cost of a piece (writing the
+// queries, reading out O and writing a partial: about three tiles' time), so that a CTA
+// whose range crosses more segment starts is given fewer key tiles. The overhead units
+// come first in each segment and carry no keys.
+constexpr int kPieceCost = 3;
+__device__ __forceinline__ int seg_units(const AttnArgs& a, int base, int tk) {
+  return vis_tiles(a, base, tk) + kPieceCost;
+}
 
 // Shared-memory plan (TK keys per tile, NST stages). P (128 rows x TK keys) of tile t is
 // written into the K area of its stage when that is large enough (K(t) is dead once S(t)
@@ -161,7 +170,7 @@ __global__ void __launch_bounds__(320, 1)
     int carry = 0;
     if (ln == 0) s_pref[0] = 0;
     for (int b0 = 0; b0 < B; b0 += 32) {
-      int v = b0 + ln < B ? vis_tiles(a, a.base[b0 + ln], TK) : 0;
+      int v = b0 + ln < B ? seg_units(a, a.base[b0 + ln], TK) : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int u = __shfl_up_sync(0xffffffffu, v, o);
@@ -175,23 +184,45 @@ __global__ void __launch_bounds__(320, 1)
   const long T = (long)hkv * s_pref[B];
   const long x0 = T * blockIdx.x / gridDim.x, x1 = T * (blockIdx.x + 1) / gridDim.x;
   if (x0 >= x1) return;
-  // the piece that starts at global tile x: sequence b, kv head g, first key tile kt0
-  // (absolute), tile count nt, and the sequence's base position
-  auto piece = [&](long x, int& b, int& g, int& kt0, int& nt, int& base) {
+  // The piece that starts at unit x: sequence b, kv head g, first key tile kt0 (absolute),
+  // key tile count nt (0 when the piece holds only a segment's overhead units), the
+  // sequence's base position, and the units it spans (adv).
+  struct Pc {
+    int b, g, kt0, nt, base;
+    long adv;
+  };
+  auto piece_at = [&](long x) -> Pc {
+    Pc q;
     int lo_b = 0, hi_b = B;  // largest b with hkv * s_pref[b] <= x
     while (hi_b - lo_b > 1) {
       const int mid = (lo_b + hi_b) >> 1;
       if ((long)hkv * s_pref[mid] <= x) lo_b = mid; else hi_b = mid;
     }
-    b = lo_b;
-    const int nb = s_pref[b + 1] - s_pref[b];
-    const long r = x - (long)hkv * s_pref[b];
-    g = (int)(r / nb);
-    const int off = (int)(r % nb);
-    base = a.base[b];
-    kt0 = vis_lo(a, base) / TK + off;
-    nt = (int)min((long)(nb - off), x1 - x);
+    q.b = lo_b;
+    const int nu = s_pref[q.b + 1] - s_pref[q.b];  // units of one segment of sequence b
+    const long r = x - (long)hkv * s_pref[q.b];
+    q.g = (int)(r / nu);
+    const int off = (int)(r % nu);
+    q.adv = min((long)(nu - off), x1 - x);
+    const int first = max(off, kPieceCost);  // first unit that is a key tile
+    q.nt = (int)max(0L, off + q.adv - first);
+    q.base = a.base[q.b];
+    q.kt0 = vis_lo(a, q.base) / TK + (first - kPieceCost);
+    return q;
   };
+  // the first piece at or after unit x that has key tiles (x1 if none)
+  auto first_piece = [&](long x, Pc& q) -> long {
+    while (x < x1) {
+      q = piece_at(x);
+      if (q.nt > 0) return x;
+      x += q.adv;
+    }
+    return x1;
+  };
+  {
+    Pc q;
+    if (first_piece(x0, q) >= x1) return;  // only overhead units: nothing to do
+  }
 
   uint8_t* sm = smem_raw + L::kSmall;
   sm += (1024 - (smem_u32(sm) & 1023)) & 1023;
@@ -253,9 +284,9 @@ __global__ void __launch_bounds__(320, 1)
       const uint64_t pol = policy_evict_first();
       int gt = 0;
       bool ok = true;
-      for (long x = x0; x < x1 && ok;) {
-        int b, g, kt0, nt, base;
-        piece(x, b, g, kt0, nt, base);
+      Pc pc;
+      for (long x = first_piece(x0, pc); x < x1 && ok; x = first_piece(x + pc.adv, pc)) {
+        const int b = pc.b, g = pc.g, kt0 = pc.kt0, nt = pc.nt;
         const int cb = a.cseq ? a.cseq[b] : b;  // cache sequence of the row group
         const long krow0 = ((long)cb * hkv + g) * a.max_ctx;
         const long vblk0 = ((long)cb * hkv + g) * (a.max_ctx / 64);  // 64-key V^T blocks
@@ -273,7 +304,6 @@ __global__ void __launch_bounds__(320, 1)
           tma_load_3d(smem_u32(st), &tmK, 0, (int)(krow0 + key0), 0, full, pol);
           tma_load_3d(smem_u32(st + L::kKTile), &tmV, 0, 0, (int)(vblk0 + key0 / 64), full, pol);
         }
-        x += nt;
       }
       for (int j = (gt > NST ? gt - NST : 0); j < gt; ++j)
         mbar_wait(smem_u32(&kv_full[j % NST]), (j / NST) & 1, err);
@@ -301,9 +331,9 @@ __global__ void __launch_bounds__(320, 1)
       };
       int gt = 0, p = 0;
       bool ok = true;
-      for (long x = x0; x < x1 && ok; ++p) {
-        int b, g, kt0, nt, base;
-        piece(x, b, g, kt0, nt, base);
+      Pc pc;
+      for (long x = first_piece(x0, pc); x < x1 && ok; x = first_piece(x + pc.adv, pc), ++p) {
+        const int nt = pc.nt;
         ok = mbar_wait(smem_u32(q_full), p & 1, err);
         if (!ok) break;
         tc_fence_after();
@@ -346,7 +376,6 @@ __global__ void __launch_bounds__(320, 1)
         if (!ok) break;
         umma_commit(smem_u32(pfin));
         gt += nt;
-        x += nt;
       }
       umma_commit(smem_u32(fin));  // all issued MMAs complete before TMEM is freed
     }
@@ -402,16 +431,15 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_before();
       mbar_arrive(smem_u32(q_full));
     };
+    Pc pc;
     {
-      int b, g, kt0, nt, base;
-      piece(x0, b, g, kt0, nt, base);
-      write_q(b, g, 0);
+      first_piece(x0, pc);
+      write_q(pc.b, pc.g, 0);
     }
     // Every thread runs the same pieces and the same named barriers, whether or not a
     // wait timed out (then the work is skipped), so the barriers always complete.
-    for (long x = x0; x < x1; ++p) {
-      int b, g, kt0, nt, base;
-      piece(x, b, g, kt0, nt, base);
+    for (long x = first_piece(x0, pc); x < x1; x = first_piece(x + pc.adv, pc), ++p) {
+      const int b = pc.b, g = pc.g, kt0 = pc.kt0, nt = pc.nt, base = pc.base;
       const int lo = vis_lo(a, base), k_end = base + a.rows;
       const int row_hi = a.causal ? base + srow : base + a.rows - 1;
       float m = -INFINITY, l = 0.f;  // reference max and running sum, log2 units
@@ -531,10 +559,9 @@ __global__ void __launch_bounds__(320, 1)
       // ---- end of the piece ----
       // the next piece's queries into the other Q buffer first, so that its first S is
       // computed while this piece's O is read out and written
-      if (x + nt < x1) {
-        int b2, g2, kt2, nt2, base2;
-        piece(x + nt, b2, g2, kt2, nt2, base2);
-        write_q(b2, g2, (p + 1) & 1);
+      {
+        Pc nx;
+        if (first_piece(x + pc.adv, nx) < x1) write_q(nx.b, nx.g, (p + 1) & 1);
       }
       // O once its last P V completed
       float O[HALF];
@@ -577,7 +604,6 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_before();
       mbar_arrive(smem_u32(o_drained));
       gt += nt;
-      x += nt;
     }
   }
   __syncwarp();
@@ -600,9 +626,9 @@ __global__ void __launch_bounds__(256) k_attn_merge_p(AttnArgs a) {
   const int mrow = blockIdx.x, b = mrow / a.rows, s = mrow % a.rows;
   const int grp = a.hq / a.hkv, g = h / grp, hh = h % grp, qi = s * grp + hh, QN = a.rows * grp;
   const int TK = a.ptk, G = a.pgrid;
-  int pre = 0, tot = 0;
+  int pre = 0, tot = 0;  // units of the sequences before b, of all sequences
   for (int bb = lane; bb < a.B; bb += 32) {
-    const int n = vis_tiles(a, a.base[bb], TK);
+    const int n = seg_units(a, a.base[bb], TK);
     tot += n;
     if (bb < b) pre += n;
   }
@@ -612,7 +638,9 @@ __global__ void __launch_bounds__(256) k_attn_merge_p(AttnArgs a) {
   }
   const long T = (long)a.hkv * tot;
   const int nb = vis_tiles(a, a.base[b], TK);
-  const long xf = (long)a.hkv * pre + (long)g * nb, xl = xf + nb - 1;
+  // the segment's first and last key-tile units (its overhead units come first)
+  const long xf = (long)a.hkv * pre + (long)g * (nb + kPieceCost) + kPieceCost,
+             xl = xf + nb - 1;
   // CTA i covers [floor(T i / G), floor(T (i+1) / G)): the owner of x is
   // floor(((x + 1) G - 1) / T)
   const int c0 = (int)(((xf + 1) * G - 1) / T), c1 = (int)(((xl + 1) * G - 1) / T);
