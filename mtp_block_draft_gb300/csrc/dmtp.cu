@@ -789,6 +789,9 @@ int check_err(dmtp_ctx* c) {
   if (cudaStreamSynchronize(c->st) != cudaSuccess) return DMTP_ECUDA;
   if (e) {
     c->poisoned = true;
+    if (getenv("DMTP_VERBOSE"))
+      fprintf(stderr, "dmtp: device error word 0x%x (1 token id, 2 KV position, 4 wait timed "
+              "out, 8 snapshot slot)\n", e);
     return DMTP_EDEVICE;
   }
   return DMTP_OK;
