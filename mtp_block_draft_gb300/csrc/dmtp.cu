@@ -1294,7 +1294,9 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
   mtp_advance(c);
   op_prefill_done(s, c->plen, st);
   if (pe1) cudaEventRecord(pe1, st);
-  cudaError_t ce = cudaStreamSynchronize(st);
+  // a launch that failed (e.g. for its resources) leaves no device error word: ask for it
+  cudaError_t ce = cudaGetLastError();
+  if (ce == cudaSuccess) ce = cudaStreamSynchronize(st);
   c->prefill_ms = -1.0;
   c->prefill_tokens = total;
   if (pe1) {
