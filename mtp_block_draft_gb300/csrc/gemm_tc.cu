@@ -12,10 +12,11 @@
 // split-K parts and the residual add into the residual stream need no other pass);
 // outputs a tensor map cannot describe fall back to per-element fp32 atomics.
 //
-// Pipeline per CTA (128 threads):
+// Pipeline per CTA (256 threads):
 //   warp 0 lane 0: TMA producer, weights with L2 evict-first, tokens evict-last;
 //   warp 1 lane 0: MMA issuer, 4 x (M=128, N=MT, K=16) per 64-wide k block;
-//   warp 2: TMEM allocation; all 4 warps: epilogue (TMEM lane = weight row).
+//   warp 2: TMEM allocation; all 8 warps: epilogue (TMEM lane = weight row; warps w and
+//   w + 4 read the same lane quarter and take alternate 16-column chunks of the tokens).
 // The gate/up GEMM pairs gate and up rows in one CTA and writes silu(g) u as the next
 // GEMM's bf16 pair with one TMA store.
 // Stages are 64-element (128 B) k slices with 128-byte swizzle.
@@ -89,7 +90,7 @@ __host__ __device__ inline uint32_t tmem_cols_for(int cols) {
 // step and weight half) and MERGED are compile-time copies of a.wide, (merged ? 1 : nx)
 // and a.merged, so that the issue loop and the epilogue have no runtime trip counts.
 template <int EPI, int WIDE, int NMMA, bool MERGED>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(256, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
               const __grid_constant__ CUtensorMap tmO, TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -106,6 +107,8 @@ __global__ void __launch_bounds__(128, 1)
   uint32_t* tmem_slot = (uint32_t*)(accum + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // epilogue: TMEM lane quarter of this warp, and its first 16-column token chunk
+  const int wq = warp & 3, c_first = (warp >> 2) * 16;
   // grid: (token halves, weight tiles, K splits); CTAs sharing a weight tile are
   // adjacent in launch order, so its second read comes from L2
   const int mrow0 = blockIdx.x * a.mct;
@@ -209,12 +212,12 @@ __global__ void __launch_bounds__(128, 1)
         __syncthreads();
       }
       if (okb) {
-        const uint32_t tbase = tmem + h * a.acc_cols + ((uint32_t)(warp * 32) << 16);
-        for (int c = 0; c < a.mct; c += 16) {
+        const uint32_t tbase = tmem + h * a.acc_cols + ((uint32_t)(wq * 32) << 16);
+        for (int c = c_first; c < a.mct; c += 32) {
           float v[16];
           acc_ld16<MERGED>(tbase + c, a.mct, v);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) stg[(c + j) * kHalfN + warp * 32 + lane] = v[j];
+          for (int j = 0; j < 16; ++j) stg[(c + j) * kHalfN + wq * 32 + lane] = v[j];
         }
       }
       fence_proxy_async_smem();
@@ -229,9 +232,9 @@ __global__ void __launch_bounds__(128, 1)
     if (ok) {
 #pragma unroll
       for (int h = 0; h < WIDE; ++h) {
-        const int n = n0 + h * kHalfN + warp * 32 + lane;
-        const uint32_t tbase = tmem + h * a.acc_cols + ((uint32_t)(warp * 32) << 16);
-        for (int c = 0; c < a.mct; c += 16) {
+        const int n = n0 + h * kHalfN + wq * 32 + lane;
+        const uint32_t tbase = tmem + h * a.acc_cols + ((uint32_t)(wq * 32) << 16);
+        for (int c = c_first; c < a.mct; c += 32) {
           float v[16];
           acc_ld16<MERGED>(tbase + c, a.mct, v);
           if (n < a.N) {
@@ -249,11 +252,11 @@ __global__ void __launch_bounds__(128, 1)
     // features] in the idle stage ring and written by one 3-D TMA store
     const bool okb = __syncthreads_and(ok);
     bf16* sh = reinterpret_cast<bf16*>(smem);
-    const int row = warp * 32 + lane;
+    const int row = wq * 32 + lane;
     if (okb) {
-      const uint32_t tg = tmem + ((uint32_t)(warp * 32) << 16);
+      const uint32_t tg = tmem + ((uint32_t)(wq * 32) << 16);
       const uint32_t tu = tg + a.acc_cols;
-      for (int c = 0; c < a.mct; c += 16) {
+      for (int c = c_first; c < a.mct; c += 32) {
         uint32_t rg[16], ru[16], rgl[16], rul[16];
         tmem_ld16_raw(tg + c, rg);
         tmem_ld16_raw(tu + c, ru);
@@ -291,10 +294,10 @@ __global__ void __launch_bounds__(128, 1)
     }
   } else if (EPI == 2) {
     if (ok) {
-      const int n = n0 + warp * 32 + lane;  // feature
-      const uint32_t tg = tmem + ((uint32_t)(warp * 32) << 16);
+      const int n = n0 + wq * 32 + lane;  // feature
+      const uint32_t tg = tmem + ((uint32_t)(wq * 32) << 16);
       const uint32_t tu = tg + a.acc_cols;
-      for (int c = 0; c < a.mct; c += 16) {
+      for (int c = c_first; c < a.mct; c += 32) {
         uint32_t rg[16], ru[16], rgl[16], rul[16];
         tmem_ld16_raw(tg + c, rg);
         tmem_ld16_raw(tu + c, ru);
@@ -583,7 +586,7 @@ void op_gemm_tc_swiglu(const TcPlan& p, void* h, long h_lo, unsigned* err, cudaS
            p.split, p.xbox,  p.nx,    p.x3d,    p.merged, p.acc_cols, nullptr,
            0,       tma,     (bf16*)h, h_lo,    p.F,      err};
   dim3 grid(p.msplit, (p.F + kHalfN - 1) / kHalfN, 1);
-  kernel_for<2>(p)<<<grid, 128, p.smem, st>>>(p.tmW, p.tmX, tmO, a);
+  kernel_for<2>(p)<<<grid, 256, p.smem, st>>>(p.tmW, p.tmX, tmO, a);
 }
 
 void op_gemm_tc_acc(const TcPlan& p, float* out, int ldo, unsigned* err, cudaStream_t st) {
@@ -598,7 +601,7 @@ void op_gemm_tc_acc(const TcPlan& p, float* out, int ldo, unsigned* err, cudaStr
            p.split, p.xbox,  p.nx,    p.x3d,    p.merged, p.acc_cols, out,
            ldo,     tma,     nullptr, 0,        0,        err};
   dim3 grid(p.msplit, (p.N + kHalfN * p.wide - 1) / (kHalfN * p.wide), p.splits);
-  kernel_for<0>(p)<<<grid, 128, p.smem, st>>>(p.tmW, p.tmX, tmO, a);
+  kernel_for<0>(p)<<<grid, 256, p.smem, st>>>(p.tmW, p.tmX, tmO, a);
 }
 
 }  // namespace dmtp
