@@ -116,10 +116,11 @@ __device__ __forceinline__ int vis_tiles(const AttnArgs& a, int base, int tk) {
 }
 // Work units of a (sequence, kv head) segment in the even split over the CTAs: its key
 // tiles plus kPieceCost units standing for the fixed cost of a piece (writing the
-// queries, reading out O and writing a partial: about three tiles' time), so that a CTA
-// whose range crosses more segment starts is given fewer key tiles. The overhead units
-// come first in each segment and carry no keys.
-constexpr int kPieceCost = 3;
+// queries, reading out O and writing a partial: about three to four tiles' time), so
+// that a CTA whose range crosses more segment starts is given fewer key tiles. The
+// overhead units come first in each segment and carry no keys. Five units gave the
+// shortest B32 launches (2: 45.9, 3: 44.3, 5: 42.7, 7: 43.9, 10: 47.8 us).
+constexpr int kPieceCost = 5;
 __device__ __forceinline__ int seg_units(const AttnArgs& a, int base, int tk) {
   return vis_tiles(a, base, tk) + kPieceCost;
 }
