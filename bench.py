@@ -220,9 +220,12 @@ def forced_accept(cfg, weights, prompts, warmup, steps, max_iter=6):
     every sequence whose replay rejected a draft, keeps the committed tokens up to and
     including the correction and continues that sequence with one-token rounds; once a
     replay accepts every draft of every round, a fresh context replays it again, timed.
-    The histogram of the timed rounds gives the accept length reached."""
+    The histogram of the timed rounds gives the accept length reached. The contexts are
+    deterministic (fixed-order K-part sums), so a replay reproduces its plan bit for bit
+    and the timed rounds include that option's cost."""
     import torch
     from mtp_block_draft_gb300 import DmtpRound
+    cfg = cfg.replace(deterministic=cfg.dtype == "bf16")
     B, V, R = len(prompts), cfg.vocab, warmup + steps
     need = 8 * R + 1
     max_ctx = max(len(p) for p in prompts) + 8 * (need + 2) + 64
@@ -290,6 +293,7 @@ def forced_accept(cfg, weights, prompts, warmup, steps, max_iter=6):
     return {"rounds_per_s": rps, "mean_accept_len": mean_len, "tokens_per_s": B * rps * mean_len,
             "steps": steps, "warmup": warmup, "acceptance": acceptance(dh),
             "plan_refinements": iters, "plan_converged": converged,
+            "deterministic": bool(cfg.deterministic),
             "drafts": "forced to the target's own greedy continuation as the replayed rounds "
                       "compute it (every draft accepted)"}
 

@@ -85,7 +85,13 @@ extern "C" {
  * draft_confidence (0 or 1; bf16 models): 1 makes the T1 and drafter heads also compute
  * each draft's confidence, the probability the head gives its own pick over the scores
  * within 20 of its best, 1 / sum exp(l_v - l_max) over those (the colibri page's
- * per-step estimate for the draft-depth gate; dmtp_round_out.draft_conf). */
+ * per-step estimate for the draft-depth gate; dmtp_round_out.draft_conf).
+ * deterministic (0 or 1; bf16 models): 1 makes every round bitwise reproducible: the
+ * GEMMs whose K range is split over several CTAs sum the parts in a fixed order (each part
+ * writes its tile to workspace scratch, waits, bounded, for the tile's other parts, all
+ * resident in one wave, and adds the parts in order into one slice of the output) instead
+ * of adding them into the output in arrival order. Costs ~9% of a B32 round and ~40 MB of
+ * workspace; two contexts with the same inputs then produce identical bits. */
 typedef struct {
   int vocab, d_model, n_layers, n_heads, n_kv_heads, head_dim, ffn;
   int gdn_heads, gdn_dk, gdn_dv;
@@ -103,6 +109,7 @@ typedef struct {
   int draft_list_cap;
   int variable_depth;
   int draft_confidence;
+  int deterministic;
 } dmtp_config;
 
 /* One decoder layer, row-major [out, in] device matrices of the config's dtype.

@@ -52,7 +52,7 @@ class dmtp_config(C.Structure):
                 ("max_batch", C.c_int), ("dtype", C.c_int), ("temperature", C.c_float),
                 ("sample_seed", C.c_uint64), ("draft_head_fp8", C.c_int),
                 ("draft_list_cap", C.c_int), ("variable_depth", C.c_int),
-                ("draft_confidence", C.c_int)]
+                ("draft_confidence", C.c_int), ("deterministic", C.c_int)]
 
 
 _LAYER_FIELDS = ("attn_norm", "wqkv", "wo", "gdn_wqkv", "gdn_wa", "gdn_wb", "gdn_wo",
@@ -206,6 +206,7 @@ def make_config(cfg, max_ctx: int, max_batch: int | None = None) -> dmtp_config:
     c.draft_list_cap = int(getattr(cfg, "draft_list_cap", 0))
     c.variable_depth = 1 if getattr(cfg, "variable_depth", False) else 0
     c.draft_confidence = 1 if getattr(cfg, "draft_confidence", False) else 0
+    c.deterministic = 1 if getattr(cfg, "deterministic", False) else 0
     return c
 
 

@@ -118,6 +118,11 @@ struct dmtp_ctx {
   float2 *conf_t1, *conf_d;
   float* dconf;
   float* hlast;
+  // fixed-order K-part sums of the split GEMMs: one partial tile per CTA of a wave, and a
+  // counter per output tile
+  float* gpart;
+  int* gcnt;
+  size_t gpart_floats;
   int* prompts;
   int2* psched;  // prefill schedule: (sequence, chunk) of each row group of each step
   int* plen;
@@ -197,7 +202,7 @@ int derive(dmtp_ctx* c, const dmtp_config* cfg, int B) {
       f.draft_list_cap > f.vocab || (f.draft_list_cap > 0 && f.dtype != 1) ||
       (f.variable_depth != 0 && f.variable_depth != 1) ||
       (f.draft_confidence != 0 && f.draft_confidence != 1) ||
-      (f.draft_confidence && f.dtype != 1))
+      (f.draft_confidence && f.dtype != 1) || (f.deterministic != 0 && f.deterministic != 1))
     return DMTP_EINVAL;
   const int grp = f.n_heads / f.n_kv_heads;
   const int QN = 8 * grp;
@@ -347,6 +352,15 @@ size_t layout(dmtp_ctx* c, char* base) {
     c->dconf = b.take<float>(B * 7 * 4);
   }
   c->hlast = b.take<float>(B * d * 4);
+  if (c->dt == 1 && c->cfg.deterministic) {  // a tile: at most 256 weight x 256 token rows
+    c->gpart_floats = (size_t)c->attn_grid * 256 * 256;
+    c->gpart = b.take<float>(c->gpart_floats * 4);
+    c->gcnt = b.take<int>((size_t)c->attn_grid * 4);
+  } else {
+    c->gpart_floats = 0;
+    c->gpart = nullptr;
+    c->gcnt = nullptr;
+  }
   c->forced = b.take<int>(B * 7 * 4);
   RoundState& s = c->rs;
   s.kv_len = b.take<int>(B * 4);
@@ -832,8 +846,18 @@ void collect(LayerPlans& p, std::vector<Gemm*>& v) {
   for (Gemm* g : {&p.qkv, &p.o, &p.gu, &p.down, &p.gq, &p.ga, &p.gb, &p.go}) v.push_back(g);
 }
 
-float time_plan(dmtp_ctx* c, const TcPlan& p, const void* flush, size_t flush_bytes,
+// the plan with the fixed-order K-part scratch of the context (deterministic contexts)
+TcPlan with_parts(const dmtp_ctx* c, TcPlan p) {
+  if (!c->gpart) return p;
+  p.part = c->gpart;
+  p.tile_cnt = c->gcnt;
+  p.part_floats = c->gpart_floats;
+  return p;
+}
+
+float time_plan(dmtp_ctx* c, const TcPlan& p0, const void* flush, size_t flush_bytes,
                 cudaEvent_t e0, cudaEvent_t e1) {
+  const TcPlan p = with_parts(c, p0);
   float best = 1e30f;
   for (int rep = 0; rep < 3; ++rep) {
     op_l2_flush(flush, flush_bytes, c->err, c->st);
@@ -1022,6 +1046,8 @@ int autotune(dmtp_ctx* c, const void* flush, size_t flush_bytes) {
   }
   cudaEventDestroy(e0);
   cudaEventDestroy(e1);
+  for (Gemm* g : all)  // every projection GEMM sums its K parts in a fixed order
+    if (!g->argmax) g->tc = with_parts(c, g->tc);
   if (cudaStreamSynchronize(c->st) != cudaSuccess) return DMTP_ECUDA;
   return rc;
 }

@@ -10,7 +10,12 @@
 // SMs idle, the K range (split-K). Each CTA stages its output tile in the idle stage ring
 // and adds it into the output with one TMA bulk reduction (element-wise atomic, so the
 // split-K parts and the residual add into the residual stream need no other pass);
-// outputs a tensor map cannot describe fall back to per-element fp32 atomics.
+// outputs a tensor map cannot describe fall back to per-element fp32 atomics. With a K
+// split and a partial scratch (and a grid of at most one wave: every CTA resident at
+// once), the K parts are summed in a fixed order instead, so the result does not depend
+// on which part finishes first: each part writes its tile to the scratch, counts itself
+// in at its tile's counter, waits (bounded) for the tile's other parts, and then adds the
+// parts 0, 1, ... of one slice of the tile's token rows into `out`.
 //
 // Pipeline per CTA (256 threads):
 //   warp 0 lane 0: TMA producer, weights with L2 evict-first, tokens evict-last;
@@ -62,7 +67,26 @@ struct TcArgs {
   long h_lo;
   int F;           // EPI 2: gate rows 0..F-1, up rows F..2F-1 of W
   unsigned* err;
+  float* part;     // deterministic split-K: per-CTA partial tiles [grid][WIDE][mct][128]
+  int* tile_cnt;   // ... and a counter per output tile, zero between launches
+  long stage_bytes;  // bytes of the stage ring (the parts' slices are gathered there)
 };
+
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from global
+// memory into this CTA's shared memory, completing on an mbarrier.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 
 // 16 accumulator columns of this warp's lanes at taddr, plus (merged) the lo columns
 // mct further: both loads in flight before one wait.
@@ -105,6 +129,7 @@ __global__ void __launch_bounds__(256, 1)
   uint64_t* empty = full + S;
   uint64_t* accum = empty + S;
   uint32_t* tmem_slot = (uint32_t*)(accum + 1);
+  uint64_t* sumbar = accum + 2;  // the K parts' slices landed (fixed-order sum)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // epilogue: TMEM lane quarter of this warp, and its first 16-column token chunk
@@ -124,6 +149,7 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(smem_u32(&empty[i]), 1);
     }
     mbar_init(smem_u32(accum), 1);
+    mbar_init(smem_u32(sumbar), 1);
     fence_mbar_init();
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
@@ -199,7 +225,95 @@ __global__ void __launch_bounds__(256, 1)
   bool ok = mbar_wait(smem_u32(accum), 0, a.err);
   ok = __all_sync(0xffffffffu, ok);
   tc_fence_after();
-  if (EPI == 0 && a.tma_out) {
+  if (EPI == 0 && a.part && gridDim.z > 1) {
+    // ---- K parts summed in a fixed order ----
+    const int S = gridDim.z, z = blockIdx.z;
+    const long tile = (long)blockIdx.y * gridDim.x + blockIdx.x;
+    const long tile_elems = (long)WIDE * kHalfN * a.mct;
+    // this part's tile, [half][token][128 rows] (a warp's stores are 128 contiguous bytes)
+    float* mine = a.part + (tile * S + z) * tile_elems;
+    if (ok) {
+#pragma unroll
+      for (int h = 0; h < WIDE; ++h) {
+        const uint32_t tbase = tmem + h * a.acc_cols + ((uint32_t)(wq * 32) << 16);
+        for (int c = c_first; c < a.mct; c += 32) {
+          float v[16];
+          acc_ld16<MERGED>(tbase + c, a.mct, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            mine[((long)h * a.mct + c + j) * kHalfN + wq * 32 + lane] = v[j];
+        }
+      }
+    }
+    __threadfence();
+    __syncthreads();
+    __shared__ int s_go;
+    if (threadIdx.x == 0) {
+      int* cnt = a.tile_cnt + tile;
+      atomicAdd(cnt, 1);
+      bool arrived = true;
+      const uint64_t t0 = global_timer();
+      while (ld_acquire(cnt) < S) {  // every part of the tile is resident (one wave)
+        if (global_timer() - t0 > DMTP_WAIT_NS) {
+          set_err(a.err, DMTP_ERR_TIMEOUT);
+          arrived = false;
+          break;
+        }
+      }
+      s_go = arrived && ok;
+    }
+    __syncthreads();
+    // this part sums token rows [t0, t1) of the tile over the parts 0..S-1, in order; the
+    // parts' slices of those rows (one contiguous run per part and weight half) are
+    // gathered into the idle stage ring by bulk copies, all in flight at once
+    const int t0 = (int)((long)a.mct * z / S), t1 = (int)((long)a.mct * (z + 1) / S);
+    const int nt = t1 - t0, per_tok = WIDE * kHalfN;
+    const uint32_t slice_b = (uint32_t)nt * kHalfN * 4;
+    const float* base = a.part + tile * S * tile_elems;
+    float* sl = reinterpret_cast<float*>(smem);
+    bool got = s_go && nt > 0 && (long)S * WIDE * slice_b <= a.stage_bytes;
+    if (got) {
+      if (threadIdx.x == 0) {
+        // the other parts' tiles were written by the generic proxy: order them before
+        // these async-proxy reads
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        mbar_expect_tx(smem_u32(sumbar), (uint32_t)(S * WIDE) * slice_b);
+        for (int q = 0; q < S; ++q)
+#pragma unroll
+          for (int h = 0; h < WIDE; ++h)
+            bulk_g2s(smem_u32(sl + (size_t)(q * WIDE + h) * nt * kHalfN),
+                     base + q * tile_elems + ((long)h * a.mct + t0) * kHalfN, slice_b,
+                     smem_u32(sumbar));
+      }
+      got = __syncthreads_and(mbar_wait(smem_u32(sumbar), 0, a.err));
+    }
+    if (got) {
+      for (int idx = threadIdx.x; idx < nt * per_tok; idx += blockDim.x) {
+        const int tok = idx / per_tok, f = idx % per_tok;
+        const int h = f / kHalfN, r = f % kHalfN;
+        const int m = mrow0 + t0 + tok, n = n0 + h * kHalfN + r;
+        if (m >= a.M || n >= a.N) continue;
+        float acc = a.out[(long)m * a.ldo + n];
+        for (int q = 0; q < S; ++q) acc += sl[((size_t)(q * WIDE + h) * nt + tok) * kHalfN + r];
+        a.out[(long)m * a.ldo + n] = acc;
+      }
+    } else if (s_go) {  // the slices do not fit the ring: read them from L2 directly
+      __threadfence();
+      for (int idx = threadIdx.x; idx < nt * per_tok; idx += blockDim.x) {
+        const int tok = t0 + idx / per_tok, f = idx % per_tok;
+        const int h = f / kHalfN, r = f % kHalfN;
+        const int m = mrow0 + tok, n = n0 + h * kHalfN + r;
+        if (m >= a.M || n >= a.N) continue;
+        float acc = a.out[(long)m * a.ldo + n];
+        const float* pp = base + ((long)h * a.mct + tok) * kHalfN + r;
+        for (int q = 0; q < S; ++q) acc += __ldcg(pp + q * tile_elems);
+        a.out[(long)m * a.ldo + n] = acc;
+      }
+    }
+    __syncthreads();
+    // the last part out resets the counter for the next launch
+    if (threadIdx.x == 0 && atomicAdd(a.tile_cnt + tile, 1) == 2 * S - 1) a.tile_cnt[tile] = 0;
+  } else if (EPI == 0 && a.tma_out) {
     // Each weight half's [mct tokens][128 rows] fp32 tile is staged in the idle stage
     // buffers (rows = TMEM lanes: a warp's stores are contiguous) and added into `out`
     // by one TMA bulk reduction, in place of mct scattered atomics per thread.
@@ -457,7 +571,7 @@ int tc_make_tmap3s(CUtensorMap* tm, const void* base, uint64_t d0, uint64_t d1, 
 
 static size_t smem_bytes(int wide, int xrows, int stages) {
   size_t b = 1024 + (size_t)stages * (wide * kHalfBytes + (size_t)xrows * kBlockK * 2);
-  b += (2 * stages + 2) * 8;
+  b += (2 * stages + 3) * 8;
   return b;
 }
 
@@ -516,7 +630,14 @@ int tc_plan_shape(TcPlan* p, const void* W, int N, int K, const void* X, int M, 
       }
     }
   }
+  // a K split stays within one wave of CTAs (its parts are summed in a fixed order by
+  // parts that must all be resident at once)
+  if (best > 1) best = std::max(1, std::min(best, nsm / tiles));
   p->splits = best;
+  p->nsm = nsm;
+  p->part = nullptr;
+  p->tile_cnt = nullptr;
+  p->part_floats = 0;
   int r = tc_make_tmap(&p->tmW, W, (uint64_t)N, (uint64_t)K, (uint32_t)(kHalfN * wide));
   if (r) return r;
   // split: the tensor spans both halves (rows >= M of each half are ignored columns);
@@ -584,7 +705,7 @@ void op_gemm_tc_swiglu(const TcPlan& p, void* h, long h_lo, unsigned* err, cudaS
                              (uint64_t)h_lo * 2, kHalfN, (uint32_t)p.mct, 2) == 0;
   TcArgs a{p.N,     p.K,     p.M,     p.MT,     p.stages, p.wide, p.mct,
            p.split, p.xbox,  p.nx,    p.x3d,    p.merged, p.acc_cols, nullptr,
-           0,       tma,     (bf16*)h, h_lo,    p.F,      err};
+           0,       tma,     (bf16*)h, h_lo,    p.F,      err,      nullptr, nullptr, 0};
   dim3 grid(p.msplit, (p.F + kHalfN - 1) / kHalfN, 1);
   kernel_for<2>(p)<<<grid, 256, p.smem, st>>>(p.tmW, p.tmX, tmO, a);
 }
@@ -597,10 +718,15 @@ void op_gemm_tc_acc(const TcPlan& p, float* out, int ldo, unsigned* err, cudaStr
   if (p.stage_area >= (size_t)p.mct * kHalfN * 4 && ldo % 4 == 0 && aligned_to(out, 16))
     tma = tc_make_tmap_f32(&tmO, out, (uint64_t)p.M, (uint64_t)p.N, (uint64_t)ldo, kHalfN,
                            (uint32_t)p.mct) == 0;
+  dim3 grid(p.msplit, (p.N + kHalfN * p.wide - 1) / (kHalfN * p.wide), p.splits);
+  // the fixed-order K-part sum needs every CTA resident at once: one wave, one CTA per SM
+  const bool det = p.part && p.tile_cnt && p.splits > 1 &&
+                   (long)grid.x * grid.y * grid.z <= p.nsm &&
+                   (size_t)grid.x * grid.y * grid.z * p.wide * kHalfN * p.mct <= p.part_floats;
   TcArgs a{p.N,     p.K,     p.M,     p.MT,     p.stages, p.wide, p.mct,
            p.split, p.xbox,  p.nx,    p.x3d,    p.merged, p.acc_cols, out,
-           ldo,     tma,     nullptr, 0,        0,        err};
-  dim3 grid(p.msplit, (p.N + kHalfN * p.wide - 1) / (kHalfN * p.wide), p.splits);
+           ldo,     tma,     nullptr, 0,        0,        err,
+           det ? p.part : nullptr, det ? p.tile_cnt : nullptr, (long)p.stage_area};
   kernel_for<0>(p)<<<grid, 256, p.smem, st>>>(p.tmW, p.tmX, tmO, a);
 }
 

@@ -201,6 +201,13 @@ struct TcPlan {
   int swiglu, F;  // SwiGLU epilogue: W = [gate; up] of F rows each
   size_t smem;
   size_t stage_area;  // bytes of the stage ring (reused to stage output tiles)
+  int nsm;            // SMs of the device (one CTA per SM)
+  // Fixed-order K-part sums (K split within one wave): partial-tile scratch of
+  // part_floats floats and a counter per output tile (zeroed once, left zero by every
+  // launch); null: the parts add into the output in arrival order.
+  float* part;
+  int* tile_cnt;
+  size_t part_floats;
 };
 // Padded token rows of an M-row operand (multiple of 16, >= 16).
 int tc_mt(int M);

@@ -74,6 +74,8 @@ class DmtpConfig:
     variable_depth: bool = False
     # the draft heads also report the confidence of their picks
     draft_confidence: bool = False
+    # bitwise-reproducible rounds (split GEMMs sum their K parts in a fixed order)
+    deterministic: bool = False
 
     def __post_init__(self):
         if not self.layer_kinds:

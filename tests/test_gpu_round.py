@@ -447,3 +447,28 @@ def test_draft_confidence(variant):
         o, recs = ls.step(tol=TOL, draft_list=mask)
         assert (o["draft_conf"] > 0).all() and (o["draft_conf"] <= 1).all()
     ls.close()
+
+
+def test_rounds_are_bitwise_reproducible():
+    """With deterministic = 1, two contexts from the same weights and prompts give
+    bitwise-identical rounds: every split GEMM sums its K parts in a fixed order, the
+    attention merges its partials in CTA order, and the argmax keys break ties by index,
+    so nothing depends on which CTA finishes first."""
+    from mtp_block_draft_gb300 import DmtpRound, default_max_ctx
+    cfg = B32_R.replace(name="b32_r_det", deterministic=True)
+    w = make_weights(cfg, "cuda")
+    prompts = make_prompts(cfg)
+    outs = []
+    for _ in range(2):
+        g = DmtpRound(cfg, w, prompts, default_max_ctx(prompts, 4))
+        rec = []
+        for _ in range(3):
+            o = g.alloc_out(ints=True, floats=True)
+            g.round(o)
+            torch.cuda.synchronize()
+            rec.append({k: v.cpu().numpy().copy() for k, v in o.items()})
+        g.close()
+        outs.append(rec)
+    for r0, r1 in zip(*outs):
+        for k in r0:
+            np.testing.assert_array_equal(r0[k], r1[k], err_msg=k)
