@@ -275,6 +275,11 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // Up to here the CTA read only the sequences' base positions, which the launch before
+  // this one (the RoPE / KV-row writer) does not write and lets this launch begin only
+  // after its own wait; the queries and the new K/V rows come after the wait.
+  pdl_trigger();
+  pdl_wait();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tO = tmem + 2 * TK;
   auto tQb = [&](int buf) -> uint32_t { return tO + HD + (uint32_t)buf * (HD / 2); };
@@ -621,6 +626,8 @@ __global__ void __launch_bounds__(320, 1)
 // (CTA, segment) partials of a segment are those of the CTAs whose tile ranges meet it.
 template <int DPL>
 __global__ void __launch_bounds__(256) k_attn_merge_p(AttnArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y * 8 + warp;
   if (h >= a.hq) return;
@@ -713,16 +720,16 @@ void op_attention_tc(const AttnArgs& a, const CUtensorMap& tmK, const CUtensorMa
   if (a.B > kAttnMaxB || a.pgrid < 1 || a.ptk != kAttnTile || a.rows < 1 || a.rows > 8)
     return;  // excluded by the caller
   if (a.hd == 128)
-    k_attn_tc<128, kTK128, kNST128><<<a.pgrid, 320, Smem<128, kTK128, kNST128>::kBytes, st>>>(
-        tmK, tmV, tmQh, tmQl, a, err);
+    launch_pdl(k_attn_tc<128, kTK128, kNST128>, a.pgrid, 320, Smem<128, kTK128, kNST128>::kBytes,
+               st, tmK, tmV, tmQh, tmQl, a, err);
   else
-    k_attn_tc<64, kTK64, kNST64><<<a.pgrid, 320, Smem<64, kTK64, kNST64>::kBytes, st>>>(
-        tmK, tmV, tmQh, tmQl, a, err);
+    launch_pdl(k_attn_tc<64, kTK64, kNST64>, a.pgrid, 320, Smem<64, kTK64, kNST64>::kBytes, st,
+               tmK, tmV, tmQh, tmQl, a, err);
   dim3 g(a.B * a.rows, (a.hq + 7) / 8);
   if (a.hd == 128)
-    k_attn_merge_p<4><<<g, 256, 0, st>>>(a);
+    launch_pdl(k_attn_merge_p<4>, g, 256, 0, st, a);
   else
-    k_attn_merge_p<2><<<g, 256, 0, st>>>(a);
+    launch_pdl(k_attn_merge_p<2>, g, 256, 0, st, a);
 }
 
 }  // namespace dmtp

@@ -23,6 +23,45 @@
 
 typedef __nv_bfloat16 bf16;
 
+// ---------------------------------------------------------------------------------
+// Programmatic dependent launch (griddepcontrol). A kernel launched with launch_pdl()
+// may begin while the kernel before it in the stream is still running: its CTAs set up
+// shared memory, barriers and TMEM, and may read the constant weights, but nothing that
+// an earlier launch writes, until pdl_wait() returns (the previous grid has completed
+// and its writes are visible). pdl_trigger() lets the next launch begin; a CTA that
+// allocates TMEM calls it only after its allocation, so that a successor's CTA never
+// holds the columns a running CTA is still waiting for. Both are no-ops in a kernel
+// launched without the attribute.
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+namespace dmtp {
+extern thread_local bool g_pdl_prev;  // ops.h
+bool pdl_enabled();
+
+// Launch `k` (a kernel that calls pdl_wait() before touching memory that earlier
+// launches write) allowing programmatic overlap with the previous kernel of `st`.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = (g_pdl_prev && pdl_enabled()) ? 1 : 0;
+  g_pdl_prev = true;
+  return cudaLaunchKernelEx(&cfg, k, static_cast<KArgs>(args)...);
+}
+}  // namespace dmtp
+
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(bf16 x) { return __bfloat162float(x); }
 template <typename T> __device__ __forceinline__ T from_f32(float x);

@@ -458,6 +458,7 @@ inline void prof_event(dmtp_ctx* c, size_t i) {
     cudaEventRecordWithFlags(c->pev[i], c->st, cudaEventRecordExternal);
   else
     cudaEventRecord(c->pev[i], c->st);
+  pdl_fence();
 }
 
 // Wraps one launch: counts it and, when profiling, records the event before it, its
@@ -530,7 +531,10 @@ void gemm_swiglu(dmtp_ctx* c, const Gemm& g, void* h, long h_lo) {
          [&] { op_gemm_tc_swiglu(g.tc, h, h_lo, c->err, c->st); }, impl);
 }
 
-void zero(dmtp_ctx* c, void* p, size_t bytes) { cudaMemsetAsync(p, 0, bytes, c->st); }
+void zero(dmtp_ctx* c, void* p, size_t bytes) {
+  cudaMemsetAsync(p, 0, bytes, c->st);
+  pdl_fence();
+}
 
 // element offset of the remainder half of an operand with `mt` padded rows of `ld`
 inline long lo_of(const dmtp_ctx* c, int mt, int ld) { return c->dt ? (long)mt * ld : 0; }
@@ -732,6 +736,7 @@ void enqueue_round(dmtp_ctx* c, const Dbg& dbg, const int* forced, int depth = 7
   const VerifyPlans* vp = G < 8 ? c->vp[G] : nullptr;
   RoundState& s = c->rs;
   const int B = c->B;
+  pdl_fence();  // the round's first launch follows host copies: no programmatic overlap
   launch(c, P_OTHER, 0, 0, [&] { op_round_begin(s, c->st); });
   // a1: T1 from h_MTP as the previous round left it
   if (c->fp8)
@@ -862,6 +867,7 @@ float time_plan(dmtp_ctx* c, const TcPlan& p0, const void* flush, size_t flush_b
   for (int rep = 0; rep < 3; ++rep) {
     op_l2_flush(flush, flush_bytes, c->err, c->st);
     cudaEventRecord(e0, c->st);
+    pdl_fence();
     op_gemm_tc_acc(p, c->gu, p.N, c->err, c->st);
     cudaEventRecord(e1, c->st);
     float ms = 1e30f;
@@ -879,6 +885,7 @@ float time_head(dmtp_ctx* c, const HeadPlan& p, const SampleArgs* smp, const voi
   for (int rep = 0; rep < 3; ++rep) {
     op_l2_flush(flush, flush_bytes, c->err, c->st);
     cudaEventRecord(e0, c->st);
+    pdl_fence();
     op_head_tc(p, c->rs.keys, nullptr, 0, smp, c->err, c->st);
     cudaEventRecord(e1, c->st);
     float ms = 1e30f;
@@ -896,6 +903,7 @@ float time_swiglu(dmtp_ctx* c, const TcPlan& p, const void* flush, size_t flush_
   for (int rep = 0; rep < 3; ++rep) {
     op_l2_flush(flush, flush_bytes, c->err, c->st);
     cudaEventRecord(e0, c->st);
+    pdl_fence();
     op_gemm_tc_swiglu(p, c->hmid, (long)p.MT * c->F, c->err, c->st);
     cudaEventRecord(e1, c->st);
     float ms = 1e30f;
@@ -1303,6 +1311,7 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
   if (cudaMemcpyAsync(c->psched, sched.data(), sched.size() * sizeof(int2),
                       cudaMemcpyHostToDevice, st) != cudaSuccess)
     return fail_prefill();
+  pdl_fence();
   for (int t = 0; t < nsteps; ++t) {
     op_prefill_chunk(s, c->prompts, c->plen, c->maxc, c->psched + (size_t)t * B, st);
     target_forward(c, false, 8, c->tgt);

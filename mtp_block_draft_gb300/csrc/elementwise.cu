@@ -5,10 +5,21 @@
 //
 // Memory-bound and tiny next to the weight/KV sweeps; one CTA per row, vectorised
 // where the row length allows.
+#include <stdlib.h>
+
 #include "common.cuh"
 #include "ops.h"
 
 namespace dmtp {
+
+thread_local bool g_pdl_prev = false;
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("DMTP_PDL");
+    return !(e && e[0] == '0');
+  }();
+  return on;
+}
 
 static inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 
@@ -28,6 +39,8 @@ __global__ void k_rmsnorm(const float* __restrict__ x, int ldx, const T* __restr
                           int ld32, T* __restrict__ tap, int ldtap, long tap_lo, int d,
                           float eps, RowMap map, float* __restrict__ zero, int ldz, int nz) {
   __shared__ float red[32];
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x;
   const float* xr = x + (long)map_row(r, map) * ldx;
   float ss = 0.f;
@@ -56,6 +69,8 @@ __global__ void __launch_bounds__(128)
                 T* __restrict__ tap, int ldtap, long tap_lo, int d, float eps, RowMap map,
                 float* __restrict__ zero, int ldz, int nz) {
   __shared__ float red[32];
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x, d4 = d >> 2;
   const float* xr = x + (long)map_row(r, map) * ldx;
   float4 v[NV];
@@ -102,14 +117,14 @@ static void rmsnorm_t(const float* x, int ldx, const T* g, T* y, int ldy, long y
                    (!tap || (aligned_to(tap, ea) && ldtap % 4 == 0 && tap_lo % 4 == 0)) &&
                    (!zero || (aligned_to(zero, 16) && ldz % 4 == 0 && nz % 4 == 0));
   if (!vec) {
-    k_rmsnorm<T><<<rows, 256, 0, st>>>(x, ldx, g, y, ldy, y_lo, y32, ld32, tap, ldtap, tap_lo, d,
-                                       eps, map, zero, ldz, nz);
+    launch_pdl(k_rmsnorm<T>, rows, 256, 0, st, x, ldx, g, y, ldy, y_lo, y32, ld32, tap, ldtap,
+               tap_lo, d, eps, map, zero, ldz, nz);
     return;
   }
   const int nv = (d / 4 + 127) / 128;
-#define DMTP_RMS_V(NV)                                                                        \
-  k_rmsnorm_v<T, NV><<<rows, 128, 0, st>>>(x, ldx, g, y, ldy, y_lo, y32, ld32, tap, ldtap,    \
-                                           tap_lo, d, eps, map, zero, ldz, nz)
+#define DMTP_RMS_V(NV)                                                                     \
+  launch_pdl(k_rmsnorm_v<T, NV>, rows, 128, 0, st, x, ldx, g, y, ldy, y_lo, y32, ld32, tap, \
+             ldtap, tap_lo, d, eps, map, zero, ldz, nz)
   if (nv <= 1)
     DMTP_RMS_V(1);
   else if (nv <= 2)
@@ -141,6 +156,8 @@ __global__ void __launch_bounds__(256) k_quant_rows_e4m3(const bf16* __restrict_
                                                          uint8_t* __restrict__ q,
                                                          float* __restrict__ qs) {
   __shared__ float red[32];
+  pdl_trigger();
+  pdl_wait();
   const long r = blockIdx.x;
   const bf16* w = W + r * d;
   float amax = 0.f;
@@ -169,6 +186,8 @@ __global__ void __launch_bounds__(128) k_rmsnorm_e4m3(const float* __restrict__ 
                                                       float* __restrict__ qs, int d, float eps,
                                                       RowMap map) {
   __shared__ float red[32];
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x, d4 = d >> 2;
   const float* xr = x + (long)map_row(r, map) * ldx;
   float4 v[NV];
@@ -211,9 +230,9 @@ void op_rmsnorm_e4m3(const float* x, int ldx, const void* g, void* q, int ldq, f
                      int rows, int d, float eps, RowMap map, cudaStream_t st) {
   if (rows <= 0) return;
   const int nv = (d / 4 + 127) / 128;
-#define DMTP_RMS_Q(NV_)                                                                      \
-  k_rmsnorm_e4m3<NV_><<<rows, 128, 0, st>>>(x, ldx, (const bf16*)g, (uint8_t*)q, ldq, qs, d, \
-                                            eps, map)
+#define DMTP_RMS_Q(NV_)                                                                   \
+  launch_pdl(k_rmsnorm_e4m3<NV_>, rows, 128, 0, st, x, ldx, (const bf16*)g, (uint8_t*)q, ldq, \
+             qs, d, eps, map)
   if (nv <= 1)
     DMTP_RMS_Q(1);
   else if (nv <= 2)
@@ -285,6 +304,8 @@ template <typename T>
 __global__ void k_concat_rms2(const T* E, int vocab, ConcatPart a, ConcatPart b, T* z, long z_lo,
                               int d, float eps, unsigned* err) {
   __shared__ float red[32];
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x;
   rms_part<T>(E, vocab, a, r, z + (long)r * 2 * d, z_lo, d, eps, err, red);
   __syncthreads();
@@ -294,11 +315,11 @@ __global__ void k_concat_rms2(const T* E, int vocab, ConcatPart a, ConcatPart b,
 void op_concat_rms2(int dt, const void* E, int vocab, ConcatPart a, ConcatPart b, void* z,
                     long z_lo, int rows, int d, float eps, unsigned* err, cudaStream_t st) {
   if (dt)
-    k_concat_rms2<bf16><<<rows, 256, 0, st>>>((const bf16*)E, vocab, a, b, (bf16*)z, z_lo, d,
-                                              eps, err);
+    launch_pdl(k_concat_rms2<bf16>, rows, 256, 0, st, (const bf16*)E, vocab, a, b, (bf16*)z, z_lo,
+               d, eps, err);
   else
-    k_concat_rms2<float><<<rows, 256, 0, st>>>((const float*)E, vocab, a, b, (float*)z, z_lo, d,
-                                               eps, err);
+    launch_pdl(k_concat_rms2<float>, rows, 256, 0, st, (const float*)E, vocab, a, b, (float*)z,
+               z_lo, d, eps, err);
 }
 
 // ---------------------------------------------------------------------------------
@@ -455,6 +476,10 @@ __global__ void __launch_bounds__(256)
                T* __restrict__ Kc, T* __restrict__ Vc, const int* __restrict__ base,
                const int* __restrict__ cseq, const float2* __restrict__ tab, int rows, int hq,
                int hkv, int hd, int max_ctx, unsigned* err, int rg) {
+  // the attention launched next reads the round's positions before its own wait: let it
+  // begin only once everything before this launch has completed
+  pdl_wait();
+  pdl_trigger();
   const int half = hd / 2, nquad = half / 4;
   if ((int)blockIdx.x < rows) {
     const int m = blockIdx.x, b = m / rg, s = m % rg;
@@ -518,14 +543,15 @@ void op_rope_kv(int dt, const float* src, int ld, int q_off, int k_off, int v_of
                                   (q_split ? aligned_to(q_split, 8) && q_lo % 4 == 0
                                            : aligned_to(q_out, 16))));
   if (vec) {
+    const int grid = rows + rows / rg * hkv;
     if (dt)
-      k_rope_kv4<bf16><<<rows + rows / rg * hkv, 256, 0, st>>>(
-          src, ld, q_off, k_off, v_off, q_out, (bf16*)q_split, q_lo, (bf16*)Kc, (bf16*)Vc, base,
-          cseq, tab, rows, hq, hkv, hd, max_ctx, err, rg);
+      launch_pdl(k_rope_kv4<bf16>, grid, 256, 0, st, src, ld, q_off, k_off, v_off, q_out,
+                 (bf16*)q_split, q_lo, (bf16*)Kc, (bf16*)Vc, base, cseq, tab, rows, hq, hkv, hd,
+                 max_ctx, err, rg);
     else
-      k_rope_kv4<float><<<rows + rows / rg * hkv, 256, 0, st>>>(
-          src, ld, q_off, k_off, v_off, q_out, nullptr, 0, (float*)Kc, (float*)Vc, base, cseq,
-          tab, rows, hq, hkv, hd, max_ctx, err, rg);
+      launch_pdl(k_rope_kv4<float>, grid, 256, 0, st, src, ld, q_off, k_off, v_off, q_out,
+                 (bf16*)nullptr, 0L, (float*)Kc, (float*)Vc, base, cseq, tab, rows, hq, hkv, hd,
+                 max_ctx, err, rg);
     return;
   }
   if (dt)

@@ -159,22 +159,39 @@ __global__ void __launch_bounds__(256, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the next launch may begin (this CTA holds its TMEM); everything but the producer's
+  // weight requests waits here for the previous launch
+  pdl_trigger();
+  if (!(warp == 0 && lane == 0)) pdl_wait();
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------
     const uint64_t pw = policy_evict_first(), px = policy_evict_last();
-    int issued = 0;
-    for (int kb = kb0; kb < kb1; ++kb, ++issued) {
-      const int s = issued % S;
-      const uint32_t ph = (issued / S) & 1;
-      if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, a.err)) break;
-      mbar_expect_tx(smem_u32(&full[s]), wbytes + xbytes);
+    auto load_w = [&](int s, int kb) {
       if (EPI == 2) {  // gate rows n0.. and up rows F + n0.., one 128-row box each
         tma_load_2d(smem_u32(sW + s * wbytes), &tmW, kb * kBlockK, n0, smem_u32(&full[s]), pw);
         tma_load_2d(smem_u32(sW + s * wbytes + kHalfBytes), &tmW, kb * kBlockK, a.F + n0,
                     smem_u32(&full[s]), pw);
       } else {
         tma_load_2d(smem_u32(sW + s * wbytes), &tmW, kb * kBlockK, n0, smem_u32(&full[s]), pw);
+      }
+    };
+    // The weights are constant: the first stages' weight slices are requested before the
+    // wait for the previous launch (whose tail they overlap), the token rows after it.
+    const int pre = min(S, kb1 - kb0);
+    for (int i = 0; i < pre; ++i) {
+      mbar_expect_tx(smem_u32(&full[i]), wbytes + xbytes);
+      load_w(i, kb0 + i);
+    }
+    pdl_wait();
+    int issued = 0;
+    for (int kb = kb0; kb < kb1; ++kb, ++issued) {
+      const int s = issued % S;
+      if (issued >= pre) {
+        const uint32_t ph = (issued / S) & 1;
+        if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, a.err)) break;
+        mbar_expect_tx(smem_u32(&full[s]), wbytes + xbytes);
+        load_w(s, kb);
       }
       // one box of [hi; lo] rows, or hi rows then (split) remainder rows: one 3-D
       // request over both halves, or a request per half
@@ -707,7 +724,7 @@ void op_gemm_tc_swiglu(const TcPlan& p, void* h, long h_lo, unsigned* err, cudaS
            p.split, p.xbox,  p.nx,    p.x3d,    p.merged, p.acc_cols, nullptr,
            0,       tma,     (bf16*)h, h_lo,    p.F,      err,      nullptr, nullptr, 0};
   dim3 grid(p.msplit, (p.F + kHalfN - 1) / kHalfN, 1);
-  kernel_for<2>(p)<<<grid, 256, p.smem, st>>>(p.tmW, p.tmX, tmO, a);
+  launch_pdl(kernel_for<2>(p), grid, 256, p.smem, st, p.tmW, p.tmX, tmO, a);
 }
 
 void op_gemm_tc_acc(const TcPlan& p, float* out, int ldo, unsigned* err, cudaStream_t st) {
@@ -727,7 +744,7 @@ void op_gemm_tc_acc(const TcPlan& p, float* out, int ldo, unsigned* err, cudaStr
            p.split, p.xbox,  p.nx,    p.x3d,    p.merged, p.acc_cols, out,
            ldo,     tma,     nullptr, 0,        0,        err,
            det ? p.part : nullptr, det ? p.tile_cnt : nullptr, (long)p.stage_area};
-  kernel_for<0>(p)<<<grid, 256, p.smem, st>>>(p.tmW, p.tmX, tmO, a);
+  launch_pdl(kernel_for<0>(p), grid, 256, p.smem, st, p.tmW, p.tmX, tmO, a);
 }
 
 }  // namespace dmtp

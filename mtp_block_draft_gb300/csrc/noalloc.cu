@@ -83,6 +83,7 @@ extern "C" int dmtp_t1_head_noalloc(const void* head, const void* norm_gain, con
   if (dmtp::head_plan(&plan, head, vocab, d_model, X, rows, nsm, 256, 8)) return DMTP_ECUDA;
   // keys start at zero for the atomic max; the operand rows are fully rewritten
   if (cudaMemsetAsync(keys, 0, (size_t)rows * 8, st) != cudaSuccess) return DMTP_ECUDA;
+  dmtp::pdl_fence();  // the next launch follows a memset: no programmatic overlap
   dmtp::op_rmsnorm(1, h, d_model, norm_gain, X, d_model, 0, nullptr, 0,
                    nullptr, 0, 0, rows, d_model, eps, dmtp::RowMap(), st);
   dmtp::op_head_tc(plan, keys, logits, vocab, nullptr, nullptr, st);

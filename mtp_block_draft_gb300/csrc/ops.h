@@ -10,6 +10,14 @@
 
 namespace dmtp {
 
+// Programmatic dependent launch bookkeeping (launch_pdl in common.cuh): whether the
+// previous operation this host thread enqueued was a kernel launch, since a programmatic
+// edge needs a kernel on both sides. Memsets, copies and event records in a stream that
+// also gets launch_pdl() launches call pdl_fence() after themselves.
+extern thread_local bool g_pdl_prev;
+bool pdl_enabled();  // process-wide: the environment variable DMTP_PDL=0 turns it off
+inline void pdl_fence() { g_pdl_prev = false; }
+
 // Row mapping shared by the row-wise kernels: output row r reads input row
 //   (r / out_group) * in_group + in_offset + (r % out_group).
 struct RowMap {
