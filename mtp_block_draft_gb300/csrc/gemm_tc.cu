@@ -333,15 +333,17 @@ __global__ void __launch_bounds__(256, 1)
   } else if (EPI == 0 && a.tma_out) {
     // Each weight half's [mct tokens][128 rows] fp32 tile is staged in the idle stage
     // buffers (rows = TMEM lanes: a warp's stores are contiguous) and added into `out`
-    // by one TMA bulk reduction, in place of mct scattered atomics per thread.
+    // by one TMA bulk reduction, in place of mct scattered atomics per thread. Where the
+    // ring holds both halves' tiles, both reductions are in flight at once.
     const bool okb = __syncthreads_and(ok);
-    float* stg = reinterpret_cast<float*>(smem);
+    const bool both = a.stage_bytes >= (long)WIDE * a.mct * kHalfN * 4;
 #pragma unroll
     for (int h = 0; h < WIDE; ++h) {
-      if (h > 0) {  // the previous reduction has read the staging tile
+      if (h > 0 && !both) {  // the previous reduction has read the staging tile
         if (threadIdx.x == 0) bulk_wait_read0();
         __syncthreads();
       }
+      float* stg = reinterpret_cast<float*>(smem) + (both ? (long)h * a.mct * kHalfN : 0);
       if (okb) {
         const uint32_t tbase = tmem + h * a.acc_cols + ((uint32_t)(wq * 32) << 16);
         for (int c = c_first; c < a.mct; c += 32) {
@@ -409,7 +411,7 @@ __global__ void __launch_bounds__(256, 1)
             u += __uint_as_float(rul[j]);
           }
           // silu(g) u = g sigmoid(g) u
-          const float v = g * __frcp_rn(1.f + __expf(-g)) * u;
+          const float v = __fdividef(g, 1.f + __expf(-g)) * u;
           const bf16 hi = __float2bfloat16_rn(v);
           sh[(c + j) * kHalfN + row] = hi;
           sh[(a.mct + c + j) * kHalfN + row] = __float2bfloat16_rn(v - __bfloat162float(hi));
@@ -453,7 +455,7 @@ __global__ void __launch_bounds__(256, 1)
             }
             // silu(g) u = g sigmoid(g) u
             if (m < a.M)
-              store_act(a.h + (long)m * a.F + n, a.h_lo, g * __frcp_rn(1.f + __expf(-g)) * u);
+              store_act(a.h + (long)m * a.F + n, a.h_lo, __fdividef(g, 1.f + __expf(-g)) * u);
           }
         }
       }
