@@ -841,6 +841,7 @@ struct TuneKey {
 struct TuneChoice {
   int wide, msplit, splits;  // projection GEMMs
   int nv, ew;                // LM heads: vocabulary rows per tile, epilogue warps
+  int pair;                  // projection GEMMs: CTA pairs (M = 256 MMAs over two SMs)
 };
 // Choices are kept for the life of the process: a later context on the same device
 // reuses them (same kernels, same reduction order, no second timing pass).
@@ -943,6 +944,10 @@ int autotune(dmtp_ctx* c, const void* flush, size_t flush_bytes) {
     return DMTP_ECUDA;
   }
   const bool verbose = getenv("DMTP_VERBOSE") != nullptr;
+  // DMTP_GEMM_PAIRS=1 / 0: projection GEMMs with split operands always / never run as CTA
+  // pairs where the shape allows (a test of either kernel form); unset: the faster one
+  const char* pairs_env = getenv("DMTP_GEMM_PAIRS");
+  const int force_pair = pairs_env ? (pairs_env[0] == '1' ? 1 : 0) : -1;
   int dev = 0;
   cudaGetDevice(&dev);
   std::lock_guard<std::mutex> lk(g_tune_mu);
@@ -959,7 +964,7 @@ int autotune(dmtp_ctx* c, const void* flush, size_t flush_bytes) {
     const TuneKey key{dev, g->N, g->K, g->M, g->split, g->argmax, g->swiglu, sample, fp8};
     const TuneChoice* hit = nullptr;
     for (auto& e : g_tune)
-      if (e.first == key) hit = &e.second;
+      if (e.first == key && force_pair < 0) hit = &e.second;
     // a head plan with another tile and warp count, same operands
     auto replan = [&](HeadPlan* p, int nv, int ew) {
       return fp8 ? head_plan_e4m3(p, g->W, g->hp.wscale, g->N, g->K, g->X, g->hp.xscale, g->M,
@@ -972,32 +977,34 @@ int autotune(dmtp_ctx* c, const void* flush, size_t flush_bytes) {
     }
     if (hit) {
       const int r = g->swiglu ? tc_plan_swiglu(&g->tc, g->W, c->F, g->K, g->X, g->M, c->nsm,
-                                               g->split, hit->msplit)
+                                               g->split, hit->msplit, hit->pair)
                               : tc_plan_shape(&g->tc, g->W, g->N, g->K, g->X, g->M, c->nsm,
                                               g->split, hit->wide, hit->msplit,
-                                              hit->splits);
+                                              hit->splits, hit->pair);
       if (r) rc = DMTP_EINVAL;
       continue;
     }
-    if (g->swiglu) {  // tile shape: one to four token parts; no K split
+    if (g->swiglu) {  // tile shape: one to four token parts, CTA pairs or not; no K split
       TcPlan best_p = g->tc;
-      float best_t = time_swiglu(c, g->tc, flush, flush_bytes, e0, e1);
-      for (int ms = 1; ms <= 4; ++ms) {
-        TcPlan p;
-        if (ms == g->tc.msplit ||
-            tc_plan_swiglu(&p, g->W, c->F, g->K, g->X, g->M, c->nsm, g->split, ms))
-          continue;
-        const float t = time_swiglu(c, p, flush, flush_bytes, e0, e1);
-        if (t < best_t) {
-          best_t = t;
-          best_p = p;
+      float best_t = force_pair == 1 ? 1e30f : time_swiglu(c, g->tc, flush, flush_bytes, e0, e1);
+      for (int pair = 0; pair <= (g->split ? 1 : 0); ++pair)
+        for (int ms = 1; ms <= 4; ++ms) {
+          TcPlan p;
+          if ((force_pair >= 0 && pair != force_pair) ||
+              (ms == g->tc.msplit && pair == g->tc.pair) ||
+              tc_plan_swiglu(&p, g->W, c->F, g->K, g->X, g->M, c->nsm, g->split, ms, pair))
+            continue;
+          const float t = time_swiglu(c, p, flush, flush_bytes, e0, e1);
+          if (t < best_t) {
+            best_t = t;
+            best_p = p;
+          }
         }
-      }
       g->tc = best_p;
-      g_tune.push_back({key, TuneChoice{2, best_p.msplit, 1, 0, 0}});
+      if (force_pair < 0) g_tune.push_back({key, TuneChoice{2, best_p.msplit, 1, 0, 0, best_p.pair}});
       if (verbose)
-        fprintf(stderr, "dmtp: gate/up F=%d K=%d M=%d: %d token part(s), %.1f us\n", c->F,
-                g->K, g->M, best_p.msplit, best_t * 1e3f);
+        fprintf(stderr, "dmtp: gate/up F=%d K=%d M=%d: %d token part(s)%s, %.1f us\n", c->F,
+                g->K, g->M, best_p.msplit, best_p.pair ? ", CTA pairs" : "", best_t * 1e3f);
       continue;
     }
     if (g->argmax) {  // LM head: vocabulary tile of 128 or 256 rows, 4 or 8 epilogue warps
@@ -1014,43 +1021,51 @@ int autotune(dmtp_ctx* c, const void* flush, size_t flush_bytes) {
           }
         }
       g->hp = best_p;
-      g_tune.push_back({key, TuneChoice{0, 0, 0, best_p.NV, best_p.ew}});
+      g_tune.push_back({key, TuneChoice{0, 0, 0, best_p.NV, best_p.ew, 0}});
       if (verbose)
         fprintf(stderr, "dmtp: head V=%d K=%d M=%d%s%s: %d vocabulary rows per tile, %d "
                 "epilogue warps, %.1f us\n", g->N, g->K, g->M, sample ? " sampled" : "",
                 fp8 ? " e4m3" : "", best_p.NV, best_p.ew, best_t * 1e3f);
       continue;
     }
-    TuneChoice best{g->tc.wide, g->tc.msplit, g->tc.splits, 0, 0};
-    float best_ms = time_plan(c, g->tc, flush, flush_bytes, e0, e1);
-    for (int wide = 1; wide <= 2; ++wide)
-      for (int ms = 1; ms <= 4; ++ms) {
-        TcPlan p0;
-        if (tc_plan_shape(&p0, g->W, g->N, g->K, g->X, g->M, c->nsm, g->split, wide, ms, 0))
-          continue;
-        const int cand[3] = {p0.splits, std::max(1, p0.splits / 2),
-                             std::min(32, 2 * p0.splits)};
-        for (int i = 0; i < 3; ++i) {
-          if (i > 0 && (cand[i] == cand[0] || (i == 2 && cand[2] == cand[1]))) continue;
-          TcPlan p;
-          if (tc_plan_shape(&p, g->W, g->N, g->K, g->X, g->M, c->nsm, g->split, wide, ms,
-                            cand[i]))
+    TuneChoice best{g->tc.wide, g->tc.msplit, g->tc.splits, 0, 0, g->tc.pair};
+    float best_ms = force_pair == 1 ? 1e30f : time_plan(c, g->tc, flush, flush_bytes, e0, e1);
+    for (int pair = 0; pair <= (g->split ? 1 : 0); ++pair)
+      for (int wide = 1; wide <= 2; ++wide)
+        for (int ms = 1; ms <= 4; ++ms) {
+          TcPlan p0;
+          if ((force_pair >= 0 && pair != force_pair) ||
+              tc_plan_shape(&p0, g->W, g->N, g->K, g->X, g->M, c->nsm, g->split, wide, ms, 0,
+                            pair))
             continue;
-          const float t = time_plan(c, p, flush, flush_bytes, e0, e1);
-          if (t < best_ms) {
-            best_ms = t;
-            best = TuneChoice{wide, ms, p.splits, 0, 0};
+          const int cand[3] = {p0.splits, std::max(1, p0.splits / 2),
+                               std::min(32, 2 * p0.splits)};
+          for (int i = 0; i < 3; ++i) {
+            if (i > 0 && (cand[i] == cand[0] || (i == 2 && cand[2] == cand[1]))) continue;
+            TcPlan p;
+            if (tc_plan_shape(&p, g->W, g->N, g->K, g->X, g->M, c->nsm, g->split, wide, ms,
+                              cand[i], pair))
+              continue;
+            const float t = time_plan(c, p, flush, flush_bytes, e0, e1);
+            if (t < best_ms) {
+              best_ms = t;
+              best = TuneChoice{wide, ms, p.splits, 0, 0, pair};
+            }
           }
         }
-      }
+    if (best_ms >= 1e30f) {  // forced pairs, none of this shape: the plan from planning
+      best = TuneChoice{g->tc.wide, g->tc.msplit, g->tc.splits, 0, 0, g->tc.pair};
+      best_ms = 0.f;
+    }
     if (tc_plan_shape(&g->tc, g->W, g->N, g->K, g->X, g->M, c->nsm, g->split, best.wide,
-                      best.msplit, best.splits))
+                      best.msplit, best.splits, best.pair))
       rc = DMTP_EINVAL;
-    g_tune.push_back({key, best});
+    if (force_pair < 0) g_tune.push_back({key, best});
     if (verbose)
-      fprintf(stderr, "dmtp: gemm N=%d K=%d M=%d%s: %d x 128 weight rows, %d token part(s), "
+      fprintf(stderr, "dmtp: gemm N=%d K=%d M=%d%s: %d x 128 weight rows%s, %d token part(s), "
               "%d K split(s), %.1f us\n", g->N, g->K, g->M, g->split ? " split" : "",
-              best.wide, best.msplit, best.splits, best_ms * 1e3f);
+              best.wide, best.pair ? " (CTA pairs)" : "", best.msplit, best.splits,
+              best_ms * 1e3f);
   }
   cudaEventDestroy(e0);
   cudaEventDestroy(e1);

@@ -113,10 +113,11 @@ __host__ __device__ inline uint32_t tmem_cols_for(int cols) {
 // epilogue writes silu(g) * u as the next GEMM's bf16 pair). WIDE, NMMA (MMAs per k
 // step and weight half) and MERGED are compile-time copies of a.wide, (merged ? 1 : nx)
 // and a.merged, so that the issue loop and the epilogue have no runtime trip counts.
-template <int EPI, int WIDE, int NMMA, bool MERGED>
+template <int EPI, int WIDE, int NMMA, bool MERGED, bool PAIR>
 __global__ void __launch_bounds__(256, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
               const __grid_constant__ CUtensorMap tmO, TcArgs a) {
+  static_assert(!PAIR || (MERGED && NMMA == 1), "CTA pairs take the merged [hi; lo] operand");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);  // 1024-B aligned tiles
@@ -132,12 +133,18 @@ __global__ void __launch_bounds__(256, 1)
   uint64_t* sumbar = accum + 2;  // the K parts' slices landed (fixed-order sum)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // CTA pair: rank 0 issues the MMAs of both; its full barriers count both CTAs' loads
+  const uint32_t rank = PAIR ? cluster_rank() : 0u;
   // epilogue: TMEM lane quarter of this warp, and its first 16-column token chunk
   const int wq = warp & 3, c_first = (warp >> 2) * 16;
   // grid: (token halves, weight tiles, K splits); CTAs sharing a weight tile are
   // adjacent in launch order, so its second read comes from L2
-  const int mrow0 = blockIdx.x * a.mct;
-  const int n0 = blockIdx.y * kHalfN * (EPI == 2 ? 1 : WIDE);
+  // (a pair's two CTAs are adjacent in x, the cluster dimension: x = 2 part + rank, and
+  // y counts pairs of weight tiles)
+  const int part = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int wtile = PAIR ? (int)(blockIdx.y * 2 + rank) : (int)blockIdx.y;
+  const int mrow0 = part * a.mct;
+  const int n0 = wtile * kHalfN * (EPI == 2 ? 1 : WIDE);
   const int nkb = a.K / kBlockK;
   const int kb0 = (int)((long)blockIdx.z * nkb / gridDim.z);
   const int kb1 = (int)((long)(blockIdx.z + 1) * nkb / gridDim.z);
@@ -154,9 +161,16 @@ __global__ void __launch_bounds__(256, 1)
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
   }
-  if (warp == 2) tmem_alloc(smem_u32(tmem_slot), ncols);
+  if (warp == 2) {
+    if (PAIR)
+      tmem_alloc_pair(smem_u32(tmem_slot), ncols);
+    else
+      tmem_alloc(smem_u32(tmem_slot), ncols);
+  }
   tc_fence_before();
   __syncthreads();
+  // a pair's barriers are initialised before either CTA signals the other's
+  if (PAIR) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // the next launch may begin (this CTA holds its TMEM); everything but the producer's
@@ -167,20 +181,31 @@ __global__ void __launch_bounds__(256, 1)
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------
     const uint64_t pw = policy_evict_first(), px = policy_evict_last();
+    // a pair's loads (this CTA's weight rows and its half of the token columns: the hi
+    // rows in CTA 0, the remainder rows in CTA 1) complete on CTA 0's full barrier
+    const uint32_t stage_bytes = (PAIR ? 2u : 1u) * (wbytes + xbytes);
+    auto full_bar = [&](int s) {
+      return PAIR ? smem_in_rank(smem_u32(&full[s]), 0) : smem_u32(&full[s]);
+    };
+    auto load = [&](uint32_t dst, const CUtensorMap* tm, int x, int y, int s, uint64_t pol) {
+      if (PAIR)
+        tma_load_2d_pair(dst, tm, x, y, full_bar(s), pol);
+      else
+        tma_load_2d(dst, tm, x, y, smem_u32(&full[s]), pol);
+    };
     auto load_w = [&](int s, int kb) {
       if (EPI == 2) {  // gate rows n0.. and up rows F + n0.., one 128-row box each
-        tma_load_2d(smem_u32(sW + s * wbytes), &tmW, kb * kBlockK, n0, smem_u32(&full[s]), pw);
-        tma_load_2d(smem_u32(sW + s * wbytes + kHalfBytes), &tmW, kb * kBlockK, a.F + n0,
-                    smem_u32(&full[s]), pw);
+        load(smem_u32(sW + s * wbytes), &tmW, kb * kBlockK, n0, s, pw);
+        load(smem_u32(sW + s * wbytes + kHalfBytes), &tmW, kb * kBlockK, a.F + n0, s, pw);
       } else {
-        tma_load_2d(smem_u32(sW + s * wbytes), &tmW, kb * kBlockK, n0, smem_u32(&full[s]), pw);
+        load(smem_u32(sW + s * wbytes), &tmW, kb * kBlockK, n0, s, pw);
       }
     };
     // The weights are constant: the first stages' weight slices are requested before the
     // wait for the previous launch (whose tail they overlap), the token rows after it.
     const int pre = min(S, kb1 - kb0);
     for (int i = 0; i < pre; ++i) {
-      mbar_expect_tx(smem_u32(&full[i]), wbytes + xbytes);
+      if (rank == 0) mbar_expect_tx(smem_u32(&full[i]), stage_bytes);
       load_w(i, kb0 + i);
     }
     pdl_wait();
@@ -190,8 +215,12 @@ __global__ void __launch_bounds__(256, 1)
       if (issued >= pre) {
         const uint32_t ph = (issued / S) & 1;
         if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, a.err)) break;
-        mbar_expect_tx(smem_u32(&full[s]), wbytes + xbytes);
+        if (rank == 0) mbar_expect_tx(smem_u32(&full[s]), stage_bytes);
         load_w(s, kb);
+      }
+      if (PAIR) {
+        load(smem_u32(sX + s * xbytes), &tmX, kb * kBlockK, (int)rank * a.MT + mrow0, s, px);
+        continue;
       }
       // one box of [hi; lo] rows, or hi rows then (split) remainder rows: one 3-D
       // request over both halves, or a request per half
@@ -203,14 +232,17 @@ __global__ void __launch_bounds__(256, 1)
           tma_load_2d(smem_u32(sX + s * xbytes + j * a.xbox * kBlockK * 2), &tmX, kb * kBlockK,
                       j * a.MT + mrow0, smem_u32(&full[s]), px);
     }
-    // drain: every stage's last issued load has landed before the CTA may exit
-    for (int j = (issued > S ? issued - S : 0); j < issued; ++j)
-      mbar_wait(smem_u32(&full[j % S]), (j / S) & 1, a.err);
-  } else if (warp == 1 && lane == 0) {
+    // drain: every stage's last issued load has landed before the CTA may exit (a pair's
+    // loads all complete on CTA 0's barriers, and CTA 1 exits after CTA 0 has drained)
+    if (rank == 0)
+      for (int j = (issued > S ? issued - S : 0); j < issued; ++j)
+        mbar_wait(smem_u32(&full[j % S]), (j / S) & 1, a.err);
+  } else if (warp == 1 && lane == 0 && rank == 0) {
     // ---------------- MMA issuer ----------------
     // merged: N = 2*mct over [hi; lo] (lo accumulates in columns mct..); otherwise the
     // nx token loads each get an MMA of N = mct into the same accumulator columns
-    const uint32_t idesc = umma_idesc_bf16(kHalfN, MERGED ? 2 * a.mct : a.mct);
+    // a pair: M = 256 (128 weight rows per CTA), N = 2 mct over [hi (CTA 0); lo (CTA 1)]
+    const uint32_t idesc = umma_idesc_bf16(PAIR ? 2 * kHalfN : kHalfN, MERGED ? 2 * a.mct : a.mct);
     int it = 0;
     for (int kb = kb0; kb < kb1; ++kb, ++it) {
       const int s = it % S;
@@ -229,12 +261,23 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
         for (int h = 0; h < WIDE; ++h)
 #pragma unroll
-          for (int j = 0; j < NMMA; ++j)
-            umma_bf16(tmem + h * a.acc_cols, dw[h] + 2 * k, dx[j] + 2 * k, idesc,
-                      (kb > kb0 || k > 0 || j > 0) ? 1u : 0u);
-      umma_commit(smem_u32(&empty[s]));
+          for (int j = 0; j < NMMA; ++j) {
+            const uint32_t acc = (kb > kb0 || k > 0 || j > 0) ? 1u : 0u;
+            if (PAIR)
+              umma_bf16_pair(tmem + h * a.acc_cols, dw[h] + 2 * k, dx[j] + 2 * k, idesc, acc);
+            else
+              umma_bf16(tmem + h * a.acc_cols, dw[h] + 2 * k, dx[j] + 2 * k, idesc, acc);
+          }
+      if (PAIR)
+        umma_commit_pair(smem_u32(&empty[s]));
+      else
+        umma_commit(smem_u32(&empty[s]));
     }
-    umma_commit(smem_u32(accum));  // always: the epilogue waits on it
+    // always: the epilogues wait on it
+    if (PAIR)
+      umma_commit_pair(smem_u32(accum));
+    else
+      umma_commit(smem_u32(accum));
   }
   __syncwarp();
 
@@ -463,9 +506,15 @@ __global__ void __launch_bounds__(256, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // neither CTA of a pair frees its TMEM or exits while the other may still signal its
+  // barriers or read its shared memory
+  if (PAIR) cluster_sync_all();
   if (warp == 2) {
     tc_fence_after();
-    tmem_dealloc(tmem, ncols);
+    if (PAIR)
+      tmem_dealloc_pair(tmem, ncols);
+    else
+      tmem_dealloc(tmem, ncols);
   }
 }
 
@@ -599,9 +648,9 @@ static constexpr size_t kSmemBudget = 200 * 1024;
 int tc_mt(int M) { return std::max(16, (M + 15) / 16 * 16); }
 
 int tc_plan_shape(TcPlan* p, const void* W, int N, int K, const void* X, int M, int nsm,
-                  bool split, int wide, int msplit, int splits) {
+                  bool split, int wide, int msplit, int splits, int pair) {
   if (M < 1 || M > 256 || K % kBlockK || N < 1 || (wide != 1 && wide != 2) || msplit < 1 ||
-      msplit > 4)
+      msplit > 4 || (pair && !split))
     return -10;
   p->N = N;
   p->K = K;
@@ -625,6 +674,12 @@ int tc_plan_shape(TcPlan* p, const void* W, int N, int K, const void* X, int M, 
     p->nx = split ? 2 : 1;
   }
   p->merged = split && 2 * p->mct <= 256;
+  p->pair = pair ? 1 : 0;
+  if (pair) {  // each CTA of a pair loads one half of its token part: one box of mct rows
+    if (!p->merged) return -10;
+    p->xbox = p->mct;
+    p->nx = 1;
+  }
   p->acc_cols = p->merged ? 2 * p->mct : p->mct;
   if (wide * p->acc_cols > 512) return -10;
   const int xrows = p->xbox * p->nx;
@@ -634,7 +689,9 @@ int tc_plan_shape(TcPlan* p, const void* W, int N, int K, const void* X, int M, 
   p->smem = smem_bytes(wide, xrows, st);
   p->stage_area = (size_t)st * (wide * kHalfBytes + (size_t)xrows * kBlockK * 2);
   if (p->smem > kSmemBudget) return -10;
-  const int tiles = (N + kHalfN * wide - 1) / (kHalfN * wide) * msplit;
+  int ytiles = (N + kHalfN * wide - 1) / (kHalfN * wide);
+  if (pair) ytiles += ytiles & 1;  // whole pairs (a last odd tile reads zeros, writes nothing)
+  const int tiles = ytiles * msplit;
   const int nkb = K / kBlockK;
   int best = splits > 0 ? std::min(splits, nkb) : 1;
   if (splits <= 0) {
@@ -662,6 +719,8 @@ int tc_plan_shape(TcPlan* p, const void* W, int N, int K, const void* X, int M, 
   // split: the tensor spans both halves (rows >= M of each half are ignored columns);
   // two boxes per stage become one 3-D request over {k, row, half}
   p->x3d = split && p->nx == 2;
+  if (pair)  // the [hi; lo] rows as one 2-D tensor: CTA r of a pair reads rows r MT + ..
+    return tc_make_tmap(&p->tmX, X, (uint64_t)2 * p->MT, (uint64_t)K, (uint32_t)p->mct);
   if (p->x3d)
     return tc_make_tmap3s(&p->tmX, X, (uint64_t)K, (uint64_t)p->MT, 2, (uint64_t)K * 2,
                           (uint64_t)p->MT * K * 2, (uint32_t)p->xbox, 2);
@@ -671,8 +730,8 @@ int tc_plan_shape(TcPlan* p, const void* W, int N, int K, const void* X, int M, 
 }
 
 int tc_plan_swiglu(TcPlan* p, const void* W, int F, int K, const void* X, int M, int nsm,
-                   bool split, int msplit) {
-  int r = tc_plan_shape(p, W, 2 * F, K, X, M, nsm, split, 2, msplit, 1);
+                   bool split, int msplit, int pair) {
+  int r = tc_plan_shape(p, W, 2 * F, K, X, M, nsm, split, 2, msplit, 1, pair);
   if (r) return r;
   p->swiglu = 1;
   p->F = F;
@@ -690,23 +749,29 @@ static void (*kernel_for(const TcPlan& p))(const CUtensorMap, const CUtensorMap,
                                              const CUtensorMap, TcArgs) {
   const int nmma = p.merged ? 1 : p.nx;
   if (EPI == 2) {
-    if (p.merged) return k_gemm_tc<2, 2, 1, true>;
-    return nmma == 1 ? k_gemm_tc<2, 2, 1, false> : k_gemm_tc<2, 2, 2, false>;
+    if (p.pair) return k_gemm_tc<2, 2, 1, true, true>;
+    if (p.merged) return k_gemm_tc<2, 2, 1, true, false>;
+    return nmma == 1 ? k_gemm_tc<2, 2, 1, false, false> : k_gemm_tc<2, 2, 2, false, false>;
   }
   if (p.wide == 1) {
-    if (p.merged) return k_gemm_tc<EPI, 1, 1, true>;
-    return nmma == 1 ? k_gemm_tc<EPI, 1, 1, false> : k_gemm_tc<EPI, 1, 2, false>;
+    if (p.pair) return k_gemm_tc<EPI, 1, 1, true, true>;
+    if (p.merged) return k_gemm_tc<EPI, 1, 1, true, false>;
+    return nmma == 1 ? k_gemm_tc<EPI, 1, 1, false, false> : k_gemm_tc<EPI, 1, 2, false, false>;
   }
-  if (p.merged) return k_gemm_tc<EPI, 2, 1, true>;
-  return nmma == 1 ? k_gemm_tc<EPI, 2, 1, false> : k_gemm_tc<EPI, 2, 2, false>;
+  if (p.pair) return k_gemm_tc<EPI, 2, 1, true, true>;
+  if (p.merged) return k_gemm_tc<EPI, 2, 1, true, false>;
+  return nmma == 1 ? k_gemm_tc<EPI, 2, 1, false, false> : k_gemm_tc<EPI, 2, 2, false, false>;
 }
 
 int tc_init_attributes() {
   const int bytes = (int)(kSmemBudget + 8 * 1024);
   void (*ks[])(const CUtensorMap, const CUtensorMap, const CUtensorMap, TcArgs) = {
-      k_gemm_tc<0, 1, 1, true>,  k_gemm_tc<0, 1, 1, false>, k_gemm_tc<0, 1, 2, false>,
-      k_gemm_tc<0, 2, 1, true>,  k_gemm_tc<0, 2, 1, false>, k_gemm_tc<0, 2, 2, false>,
-      k_gemm_tc<2, 2, 1, true>,  k_gemm_tc<2, 2, 1, false>, k_gemm_tc<2, 2, 2, false>};
+      k_gemm_tc<0, 1, 1, true, false>,  k_gemm_tc<0, 1, 1, false, false>,
+      k_gemm_tc<0, 1, 2, false, false>, k_gemm_tc<0, 2, 1, true, false>,
+      k_gemm_tc<0, 2, 1, false, false>, k_gemm_tc<0, 2, 2, false, false>,
+      k_gemm_tc<2, 2, 1, true, false>,  k_gemm_tc<2, 2, 1, false, false>,
+      k_gemm_tc<2, 2, 2, false, false>, k_gemm_tc<0, 1, 1, true, true>,
+      k_gemm_tc<0, 2, 1, true, true>,   k_gemm_tc<2, 2, 1, true, true>};
   for (auto k : ks)
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
         cudaSuccess)
@@ -725,8 +790,11 @@ void op_gemm_tc_swiglu(const TcPlan& p, void* h, long h_lo, unsigned* err, cudaS
   TcArgs a{p.N,     p.K,     p.M,     p.MT,     p.stages, p.wide, p.mct,
            p.split, p.xbox,  p.nx,    p.x3d,    p.merged, p.acc_cols, nullptr,
            0,       tma,     (bf16*)h, h_lo,    p.F,      err,      nullptr, nullptr, 0};
-  dim3 grid(p.msplit, (p.F + kHalfN - 1) / kHalfN, 1);
-  launch_pdl(kernel_for<2>(p), grid, 256, p.smem, st, p.tmW, p.tmX, tmO, a);
+  const int gy = (p.F + kHalfN - 1) / kHalfN;
+  // CTA pairs: clusters of two along x (x = 2 token part + rank, y = pairs of weight tiles)
+  dim3 grid = p.pair ? dim3(2 * p.msplit, (gy + 1) / 2, 1) : dim3(p.msplit, gy, 1);
+  launch_pdl_cluster(kernel_for<2>(p), grid, 256, p.smem, st, dim3(p.pair ? 2 : 1, 1, 1), p.tmW,
+                     p.tmX, tmO, a);
 }
 
 void op_gemm_tc_acc(const TcPlan& p, float* out, int ldo, unsigned* err, cudaStream_t st) {
@@ -737,7 +805,8 @@ void op_gemm_tc_acc(const TcPlan& p, float* out, int ldo, unsigned* err, cudaStr
   if (p.stage_area >= (size_t)p.mct * kHalfN * 4 && ldo % 4 == 0 && aligned_to(out, 16))
     tma = tc_make_tmap_f32(&tmO, out, (uint64_t)p.M, (uint64_t)p.N, (uint64_t)ldo, kHalfN,
                            (uint32_t)p.mct) == 0;
-  dim3 grid(p.msplit, (p.N + kHalfN * p.wide - 1) / (kHalfN * p.wide), p.splits);
+  const int gy = (p.N + kHalfN * p.wide - 1) / (kHalfN * p.wide);
+  dim3 grid = p.pair ? dim3(2 * p.msplit, (gy + 1) / 2, p.splits) : dim3(p.msplit, gy, p.splits);
   // the fixed-order K-part sum needs every CTA resident at once: one wave, one CTA per SM
   const bool det = p.part && p.tile_cnt && p.splits > 1 &&
                    (long)grid.x * grid.y * grid.z <= p.nsm &&
@@ -746,7 +815,8 @@ void op_gemm_tc_acc(const TcPlan& p, float* out, int ldo, unsigned* err, cudaStr
            p.split, p.xbox,  p.nx,    p.x3d,    p.merged, p.acc_cols, out,
            ldo,     tma,     nullptr, 0,        0,        err,
            det ? p.part : nullptr, det ? p.tile_cnt : nullptr, (long)p.stage_area};
-  launch_pdl(kernel_for<0>(p), grid, 256, p.smem, st, p.tmW, p.tmX, tmO, a);
+  launch_pdl_cluster(kernel_for<0>(p), grid, 256, p.smem, st, dim3(p.pair ? 2 : 1, 1, 1), p.tmW,
+                     p.tmX, tmO, a);
 }
 
 }  // namespace dmtp

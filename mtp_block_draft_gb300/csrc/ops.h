@@ -205,6 +205,8 @@ struct TcPlan {
   int xbox, nx;   // X rows per box, boxes per stage
   int x3d;        // the two halves' boxes as one 3-D request
   int merged;     // hi and lo in one MMA of 2*mct columns
+  int pair;       // CTA pairs along the weight tiles: one M = 256 MMA over two SMs, each
+                  // CTA loading its weight rows and one half (hi or lo) of the tokens
   int acc_cols;   // TMEM columns per accumulator
   int swiglu, F;  // SwiGLU epilogue: W = [gate; up] of F rows each
   size_t smem;
@@ -247,11 +249,12 @@ int tc_plan(TcPlan* p, const void* W, int N, int K, const void* X, int M, int ns
 // rows n0.. with up rows F + n0.. (two accumulators) and writes h = silu(g) * u, a bf16
 // pair [M][F] (remainder at h + h_lo), so no fp32 output or separate SwiGLU pass.
 int tc_plan_swiglu(TcPlan* p, const void* W, int F, int K, const void* X, int M, int nsm,
-                   bool split, int msplit);
+                   bool split, int msplit, int pair = 0);
 void op_gemm_tc_swiglu(const TcPlan& p, void* h, long h_lo, unsigned* err, cudaStream_t st);
-// tc_plan with the tile shape given: wide (1, 2), msplit (1..4) and splits (<= 0: chosen).
+// tc_plan with the tile shape given: wide (1, 2), msplit (1..4), splits (<= 0: chosen) and
+// pair (1: CTA pairs, split operands whose token part fits one MMA, 2 mct <= 256).
 int tc_plan_shape(TcPlan* p, const void* W, int N, int K, const void* X, int M, int nsm,
-                  bool split, int wide, int msplit, int splits);
+                  bool split, int wide, int msplit, int splits, int pair = 0);
 // out[m*ldo + n] += (X W^T)[m][n] for the plan's M x N (out fp32, zeroed or holding the
 // residual; K parts and CTAs add element-wise atomically).
 void op_gemm_tc_acc(const TcPlan& p, float* out, int ldo, unsigned* err, cudaStream_t st);

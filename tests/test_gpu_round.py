@@ -98,6 +98,18 @@ def test_b32_shape_bf16_ragged():
     ls.close()
 
 
+@pytest.mark.parametrize("pairs", ["1", "0"])
+def test_b32_shape_gemm_kernel_forms(monkeypatch, pairs):
+    """Every projection GEMM with a split operand as CTA pairs (one M = 256 MMA over two
+    SMs, each CTA loading one half of the token columns), then never: both kernel forms
+    in lock-step, whichever the timing picks."""
+    monkeypatch.setenv("DMTP_GEMM_PAIRS", pairs)
+    ls = _lockstep(B32_R, 2)
+    for _ in range(2):
+        ls.step(tol=TOL)
+    ls.close()
+
+
 def test_b32_shape_graph_rounds_ints_only():
     """Rounds without float outputs replay the captured CUDA graph."""
     ls = _lockstep(B32_R, 4, seqs=[0, 5, 31])
