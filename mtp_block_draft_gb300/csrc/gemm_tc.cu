@@ -113,70 +113,45 @@ __host__ __device__ inline uint32_t tmem_cols_for(int cols) {
 // epilogue writes silu(g) * u as the next GEMM's bf16 pair). WIDE, NMMA (MMAs per k
 // step and weight half) and MERGED are compile-time copies of a.wide, (merged ? 1 : nx)
 // and a.merged, so that the issue loop and the epilogue have no runtime trip counts.
+// One GEMM pass of a CTA over its tile (bx, by, bz) of a (gx, *, gz) tile grid: TMA
+// producer, MMA issuer and epilogue, on shared memory (stage ring at smem) and barriers
+// already initialised, with `tmem` allocated. grid_dep: the pass reads the previous
+// launch's outputs, so everything but the producer's weight requests waits for the grid
+// dependency first (programmatic launch).
+struct GemmBars {
+  uint64_t *full, *empty, *accum, *sumbar;
+};
+
 template <int EPI, int WIDE, int NMMA, bool MERGED, bool PAIR>
-__global__ void __launch_bounds__(256, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-              const __grid_constant__ CUtensorMap tmO, TcArgs a) {
-  static_assert(!PAIR || (MERGED && NMMA == 1), "CTA pairs take the merged [hi; lo] operand");
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem =
-      smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);  // 1024-B aligned tiles
+__device__ __forceinline__ void gemm_pass(const CUtensorMap* tmW, const CUtensorMap* tmX,
+                                          const CUtensorMap* tmO, const TcArgs& a,
+                                          uint8_t* smem, GemmBars bars, uint32_t tmem,
+                                          uint32_t rank, int bx, int by, int bz, int gx, int gz,
+                                          bool grid_dep) {
   const int S = a.stages;
   const uint32_t wbytes = (uint32_t)WIDE * kHalfBytes;
   const uint32_t xbytes = (uint32_t)a.xbox * a.nx * kBlockK * 2;
   uint8_t* sW = smem;
   uint8_t* sX = smem + S * wbytes;
-  uint64_t* full = (uint64_t*)(sX + S * xbytes);
-  uint64_t* empty = full + S;
-  uint64_t* accum = empty + S;
-  uint32_t* tmem_slot = (uint32_t*)(accum + 1);
-  uint64_t* sumbar = accum + 2;  // the K parts' slices landed (fixed-order sum)
-
+  uint64_t* full = bars.full;
+  uint64_t* empty = bars.empty;
+  uint64_t* accum = bars.accum;
+  uint64_t* sumbar = bars.sumbar;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // CTA pair: rank 0 issues the MMAs of both; its full barriers count both CTAs' loads
-  const uint32_t rank = PAIR ? cluster_rank() : 0u;
   // epilogue: TMEM lane quarter of this warp, and its first 16-column token chunk
   const int wq = warp & 3, c_first = (warp >> 2) * 16;
   // grid: (token halves, weight tiles, K splits); CTAs sharing a weight tile are
   // adjacent in launch order, so its second read comes from L2
   // (a pair's two CTAs are adjacent in x, the cluster dimension: x = 2 part + rank, and
   // y counts pairs of weight tiles)
-  const int part = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-  const int wtile = PAIR ? (int)(blockIdx.y * 2 + rank) : (int)blockIdx.y;
+  const int part = PAIR ? (bx >> 1) : bx;
+  const int wtile = PAIR ? (by * 2 + (int)rank) : by;
   const int mrow0 = part * a.mct;
   const int n0 = wtile * kHalfN * (EPI == 2 ? 1 : WIDE);
   const int nkb = a.K / kBlockK;
-  const int kb0 = (int)((long)blockIdx.z * nkb / gridDim.z);
-  const int kb1 = (int)((long)(blockIdx.z + 1) * nkb / gridDim.z);
-  const uint32_t ncols = tmem_cols_for(WIDE * a.acc_cols);
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < S; ++i) {
-      mbar_init(smem_u32(&full[i]), 1);
-      mbar_init(smem_u32(&empty[i]), 1);
-    }
-    mbar_init(smem_u32(accum), 1);
-    mbar_init(smem_u32(sumbar), 1);
-    fence_mbar_init();
-    tma_prefetch_desc(&tmW);
-    tma_prefetch_desc(&tmX);
-  }
-  if (warp == 2) {
-    if (PAIR)
-      tmem_alloc_pair(smem_u32(tmem_slot), ncols);
-    else
-      tmem_alloc(smem_u32(tmem_slot), ncols);
-  }
-  tc_fence_before();
-  __syncthreads();
-  // a pair's barriers are initialised before either CTA signals the other's
-  if (PAIR) cluster_sync_all();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  // the next launch may begin (this CTA holds its TMEM); everything but the producer's
-  // weight requests waits here for the previous launch
-  pdl_trigger();
-  if (!(warp == 0 && lane == 0)) pdl_wait();
+  const int kb0 = (int)((long)bz * nkb / gz);
+  const int kb1 = (int)((long)(bz + 1) * nkb / gz);
+  if (grid_dep && !(warp == 0 && lane == 0)) pdl_wait();
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------
@@ -195,10 +170,10 @@ __global__ void __launch_bounds__(256, 1)
     };
     auto load_w = [&](int s, int kb) {
       if (EPI == 2) {  // gate rows n0.. and up rows F + n0.., one 128-row box each
-        load(smem_u32(sW + s * wbytes), &tmW, kb * kBlockK, n0, s, pw);
-        load(smem_u32(sW + s * wbytes + kHalfBytes), &tmW, kb * kBlockK, a.F + n0, s, pw);
+        load(smem_u32(sW + s * wbytes), tmW, kb * kBlockK, n0, s, pw);
+        load(smem_u32(sW + s * wbytes + kHalfBytes), tmW, kb * kBlockK, a.F + n0, s, pw);
       } else {
-        load(smem_u32(sW + s * wbytes), &tmW, kb * kBlockK, n0, s, pw);
+        load(smem_u32(sW + s * wbytes), tmW, kb * kBlockK, n0, s, pw);
       }
     };
     // The weights are constant: the first stages' weight slices are requested before the
@@ -208,7 +183,7 @@ __global__ void __launch_bounds__(256, 1)
       if (rank == 0) mbar_expect_tx(smem_u32(&full[i]), stage_bytes);
       load_w(i, kb0 + i);
     }
-    pdl_wait();
+    if (grid_dep) pdl_wait();
     int issued = 0;
     for (int kb = kb0; kb < kb1; ++kb, ++issued) {
       const int s = issued % S;
@@ -219,17 +194,17 @@ __global__ void __launch_bounds__(256, 1)
         load_w(s, kb);
       }
       if (PAIR) {
-        load(smem_u32(sX + s * xbytes), &tmX, kb * kBlockK, (int)rank * a.MT + mrow0, s, px);
+        load(smem_u32(sX + s * xbytes), tmX, kb * kBlockK, (int)rank * a.MT + mrow0, s, px);
         continue;
       }
       // one box of [hi; lo] rows, or hi rows then (split) remainder rows: one 3-D
       // request over both halves, or a request per half
       if (a.x3d)
-        tma_load_3d(smem_u32(sX + s * xbytes), &tmX, kb * kBlockK, mrow0, 0, smem_u32(&full[s]),
+        tma_load_3d(smem_u32(sX + s * xbytes), tmX, kb * kBlockK, mrow0, 0, smem_u32(&full[s]),
                     px);
       else
         for (int j = 0; j < a.nx; ++j)
-          tma_load_2d(smem_u32(sX + s * xbytes + j * a.xbox * kBlockK * 2), &tmX, kb * kBlockK,
+          tma_load_2d(smem_u32(sX + s * xbytes + j * a.xbox * kBlockK * 2), tmX, kb * kBlockK,
                       j * a.MT + mrow0, smem_u32(&full[s]), px);
     }
     // drain: every stage's last issued load has landed before the CTA may exit (a pair's
@@ -285,10 +260,10 @@ __global__ void __launch_bounds__(256, 1)
   bool ok = mbar_wait(smem_u32(accum), 0, a.err);
   ok = __all_sync(0xffffffffu, ok);
   tc_fence_after();
-  if (EPI == 0 && a.part && gridDim.z > 1) {
+  if (EPI == 0 && a.part && gz > 1) {
     // ---- K parts summed in a fixed order ----
-    const int S = gridDim.z, z = blockIdx.z;
-    const long tile = (long)blockIdx.y * gridDim.x + blockIdx.x;
+    const int S = gz, z = bz;
+    const long tile = (long)by * gx + bx;
     const long tile_elems = (long)WIDE * kHalfN * a.mct;
     // this part's tile, [half][token][128 rows] (a warp's stores are 128 contiguous bytes)
     float* mine = a.part + (tile * S + z) * tile_elems;
@@ -399,7 +374,7 @@ __global__ void __launch_bounds__(256, 1)
       fence_proxy_async_smem();
       __syncthreads();
       if (threadIdx.x == 0 && okb && n0 + h * kHalfN < a.N && mrow0 < a.M) {
-        tma_reduce_add_2d(&tmO, n0 + h * kHalfN, mrow0, smem_u32(stg));
+        tma_reduce_add_2d(tmO, n0 + h * kHalfN, mrow0, smem_u32(stg));
         bulk_commit();
       }
     }
@@ -464,7 +439,7 @@ __global__ void __launch_bounds__(256, 1)
     fence_proxy_async_smem();
     __syncthreads();
     if (threadIdx.x == 0 && okb && n0 < a.F && mrow0 < a.M) {
-      tma_store_3d(&tmO, n0, mrow0, 0, smem_u32(sh));
+      tma_store_3d(tmO, n0, mrow0, 0, smem_u32(sh));
       bulk_commit();
       bulk_wait_read0();
     }
@@ -504,6 +479,58 @@ __global__ void __launch_bounds__(256, 1)
       }
     }
   }
+}
+
+template <int EPI, int WIDE, int NMMA, bool MERGED, bool PAIR>
+__global__ void __launch_bounds__(256, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+              const __grid_constant__ CUtensorMap tmO, TcArgs a) {
+  static_assert(!PAIR || (MERGED && NMMA == 1), "CTA pairs take the merged [hi; lo] operand");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem =
+      smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);  // 1024-B aligned tiles
+  const int S = a.stages;
+  const uint32_t wbytes = (uint32_t)WIDE * kHalfBytes;
+  const uint32_t xbytes = (uint32_t)a.xbox * a.nx * kBlockK * 2;
+  uint64_t* full = (uint64_t*)(smem + S * (wbytes + xbytes));
+  uint64_t* empty = full + S;
+  uint64_t* accum = empty + S;
+  uint32_t* tmem_slot = (uint32_t*)(accum + 1);
+  uint64_t* sumbar = accum + 2;  // the K parts' slices landed (fixed-order sum)
+  const int warp = threadIdx.x >> 5;
+  // CTA pair: rank 0 issues the MMAs of both; its full barriers count both CTAs' loads
+  const uint32_t rank = PAIR ? cluster_rank() : 0u;
+  const uint32_t ncols = tmem_cols_for(WIDE * a.acc_cols);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(smem_u32(&full[i]), 1);
+      mbar_init(smem_u32(&empty[i]), 1);
+    }
+    mbar_init(smem_u32(accum), 1);
+    mbar_init(smem_u32(sumbar), 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == 2) {
+    if (PAIR)
+      tmem_alloc_pair(smem_u32(tmem_slot), ncols);
+    else
+      tmem_alloc(smem_u32(tmem_slot), ncols);
+  }
+  tc_fence_before();
+  __syncthreads();
+  // a pair's barriers are initialised before either CTA signals the other's
+  if (PAIR) cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // the next launch may begin (this CTA holds its TMEM)
+  pdl_trigger();
+  gemm_pass<EPI, WIDE, NMMA, MERGED, PAIR>(&tmW, &tmX, &tmO, a, smem,
+                                           GemmBars{full, empty, accum, sumbar}, tmem, rank,
+                                           blockIdx.x, blockIdx.y, blockIdx.z, gridDim.x,
+                                           gridDim.z, true);
   tc_fence_before();
   __syncthreads();
   // neither CTA of a pair frees its TMEM or exits while the other may still signal its
@@ -779,42 +806,60 @@ int tc_init_attributes() {
   return 0;
 }
 
-void op_gemm_tc_swiglu(const TcPlan& p, void* h, long h_lo, unsigned* err, cudaStream_t st) {
+// Kernel arguments, output tensor map and grid of the SwiGLU (gate/up) GEMM.
+static void swiglu_args(const TcPlan& p, void* h, long h_lo, unsigned* err, TcArgs* a,
+                        CUtensorMap* tmO, dim3* grid) {
   // the TMA-store epilogue when the [hi | lo] tile fits the stage buffers
-  CUtensorMap tmO = p.tmW;
+  *tmO = p.tmW;
   int tma = 0;
   if (p.stage_area >= (size_t)p.mct * kHalfN * 4 && h_lo > 0 && aligned_to(h, 16) &&
       (p.F * 2) % 16 == 0 && (h_lo * 2) % 16 == 0)
-    tma = tc_make_tmap3s_box(&tmO, h, (uint64_t)p.F, (uint64_t)p.M, 2, (uint64_t)p.F * 2,
+    tma = tc_make_tmap3s_box(tmO, h, (uint64_t)p.F, (uint64_t)p.M, 2, (uint64_t)p.F * 2,
                              (uint64_t)h_lo * 2, kHalfN, (uint32_t)p.mct, 2) == 0;
-  TcArgs a{p.N,     p.K,     p.M,     p.MT,     p.stages, p.wide, p.mct,
-           p.split, p.xbox,  p.nx,    p.x3d,    p.merged, p.acc_cols, nullptr,
-           0,       tma,     (bf16*)h, h_lo,    p.F,      err,      nullptr, nullptr, 0};
+  *a = TcArgs{p.N,     p.K,     p.M,     p.MT,     p.stages, p.wide, p.mct,
+              p.split, p.xbox,  p.nx,    p.x3d,    p.merged, p.acc_cols, nullptr,
+              0,       tma,     (bf16*)h, h_lo,    p.F,      err,      nullptr, nullptr, 0};
   const int gy = (p.F + kHalfN - 1) / kHalfN;
   // CTA pairs: clusters of two along x (x = 2 token part + rank, y = pairs of weight tiles)
-  dim3 grid = p.pair ? dim3(2 * p.msplit, (gy + 1) / 2, 1) : dim3(p.msplit, gy, 1);
+  *grid = p.pair ? dim3(2 * p.msplit, (gy + 1) / 2, 1) : dim3(p.msplit, gy, 1);
+}
+
+// The same for a GEMM adding into an fp32 output (part: the fixed-order K-part sums).
+static void acc_args(const TcPlan& p, float* out, int ldo, unsigned* err, TcArgs* a,
+                     CUtensorMap* tmO, dim3* grid) {
+  // the TMA bulk-reduction epilogue when a weight half's tile fits the stage buffers and
+  // out can be described by a tensor map; else per-element atomics
+  *tmO = p.tmW;
+  int tma = 0;
+  if (p.stage_area >= (size_t)p.mct * kHalfN * 4 && ldo % 4 == 0 && aligned_to(out, 16))
+    tma = tc_make_tmap_f32(tmO, out, (uint64_t)p.M, (uint64_t)p.N, (uint64_t)ldo, kHalfN,
+                           (uint32_t)p.mct) == 0;
+  const int gy = (p.N + kHalfN * p.wide - 1) / (kHalfN * p.wide);
+  *grid = p.pair ? dim3(2 * p.msplit, (gy + 1) / 2, p.splits) : dim3(p.msplit, gy, p.splits);
+  // the fixed-order K-part sum needs every CTA resident at once: one wave, one CTA per SM
+  const long ctas = (long)grid->x * grid->y * grid->z;
+  const bool det = p.part && p.tile_cnt && p.splits > 1 && ctas <= p.nsm &&
+                   (size_t)ctas * p.wide * kHalfN * p.mct <= p.part_floats;
+  *a = TcArgs{p.N,     p.K,     p.M,     p.MT,     p.stages, p.wide, p.mct,
+              p.split, p.xbox,  p.nx,    p.x3d,    p.merged, p.acc_cols, out,
+              ldo,     tma,     nullptr, 0,        0,        err,
+              det ? p.part : nullptr, det ? p.tile_cnt : nullptr, (long)p.stage_area};
+}
+
+void op_gemm_tc_swiglu(const TcPlan& p, void* h, long h_lo, unsigned* err, cudaStream_t st) {
+  TcArgs a;
+  CUtensorMap tmO;
+  dim3 grid;
+  swiglu_args(p, h, h_lo, err, &a, &tmO, &grid);
   launch_pdl_cluster(kernel_for<2>(p), grid, 256, p.smem, st, dim3(p.pair ? 2 : 1, 1, 1), p.tmW,
                      p.tmX, tmO, a);
 }
 
 void op_gemm_tc_acc(const TcPlan& p, float* out, int ldo, unsigned* err, cudaStream_t st) {
-  // the TMA bulk-reduction epilogue when a weight half's tile fits the stage buffers and
-  // out can be described by a tensor map; else per-element atomics
-  CUtensorMap tmO = p.tmW;
-  int tma = 0;
-  if (p.stage_area >= (size_t)p.mct * kHalfN * 4 && ldo % 4 == 0 && aligned_to(out, 16))
-    tma = tc_make_tmap_f32(&tmO, out, (uint64_t)p.M, (uint64_t)p.N, (uint64_t)ldo, kHalfN,
-                           (uint32_t)p.mct) == 0;
-  const int gy = (p.N + kHalfN * p.wide - 1) / (kHalfN * p.wide);
-  dim3 grid = p.pair ? dim3(2 * p.msplit, (gy + 1) / 2, p.splits) : dim3(p.msplit, gy, p.splits);
-  // the fixed-order K-part sum needs every CTA resident at once: one wave, one CTA per SM
-  const bool det = p.part && p.tile_cnt && p.splits > 1 &&
-                   (long)grid.x * grid.y * grid.z <= p.nsm &&
-                   (size_t)grid.x * grid.y * grid.z * p.wide * kHalfN * p.mct <= p.part_floats;
-  TcArgs a{p.N,     p.K,     p.M,     p.MT,     p.stages, p.wide, p.mct,
-           p.split, p.xbox,  p.nx,    p.x3d,    p.merged, p.acc_cols, out,
-           ldo,     tma,     nullptr, 0,        0,        err,
-           det ? p.part : nullptr, det ? p.tile_cnt : nullptr, (long)p.stage_area};
+  TcArgs a;
+  CUtensorMap tmO;
+  dim3 grid;
+  acc_args(p, out, ldo, err, &a, &tmO, &grid);
   launch_pdl_cluster(kernel_for<0>(p), grid, 256, p.smem, st, dim3(p.pair ? 2 : 1, 1, 1), p.tmW,
                      p.tmX, tmO, a);
 }
