@@ -294,6 +294,11 @@ int dmtp_t1_head_noalloc(const void* head, const void* norm_gain, const float* h
  * range, DMTP_ESTATE on a poisoned context, DMTP_ECUDA if the launch fails. */
 int dmtp_selftest_timeout(dmtp_ctx* ctx, uint64_t limit_ns);
 
+/* The device error word that poisoned the context (0 while it is not poisoned by one):
+ * bit 1 a token id outside [0, V), 2 a KV write past max_ctx, 4 a bounded wait that gave
+ * up, 8 a snapshot slot outside [0, 8). NULL gives 0. */
+uint32_t dmtp_error_word(const dmtp_ctx* ctx);
+
 /* Release the context (host memory and the graph). Never fails; NULL is a no-op.
  * Does not free caller-owned device memory. */
 void dmtp_free(dmtp_ctx* ctx);

@@ -28,6 +28,7 @@ EXPORTS = ("dmtp_workspace_size", "dmtp_init", "dmtp_round", "dmtp_round_host",
            "dmtp_read_state", "dmtp_round_launches", "dmtp_round_profile", "dmtp_free",
            "dmtp_strerror", "dmtp_t1_head_noalloc", "dmtp_prefill_stats",
            "dmtp_selftest_timeout", "dmtp_set_draft_list", "dmtp_round_depth",
+           "dmtp_error_word",
            "dmtp_gate_create", "dmtp_gate_forward", "dmtp_gate_draft_cost",
            "dmtp_gate_result", "dmtp_gate_pick", "dmtp_gate_pick_p", "dmtp_gate_read",
            "dmtp_gate_free", "dmtp_vocab_create", "dmtp_vocab_begin_request",
@@ -137,6 +138,8 @@ def load_library(path: str = LIB_PATH):
     lib.dmtp_set_draft_list.restype = C.c_int
     lib.dmtp_selftest_timeout.argtypes = [P, C.c_uint64]
     lib.dmtp_selftest_timeout.restype = C.c_int
+    lib.dmtp_error_word.argtypes = [P]
+    lib.dmtp_error_word.restype = C.c_uint32
     lib.dmtp_free.argtypes = [P]
     lib.dmtp_free.restype = None
     lib.dmtp_t1_head_noalloc.argtypes = [P, P, P, C.c_int, C.c_int, C.c_int, C.c_float, P, P, P]
@@ -171,15 +174,18 @@ def load_library(path: str = LIB_PATH):
 
 
 class DmtpError(RuntimeError):
-    def __init__(self, code: int, what: str):
+    def __init__(self, code: int, what: str, word: int = 0):
         msg = load_library().dmtp_strerror(code).decode()
-        super().__init__(f"{what}: {ERRORS.get(code, code)} ({msg})")
+        extra = f"; device error word 0x{word:x}" if word else ""
+        super().__init__(f"{what}: {ERRORS.get(code, code)} ({msg}{extra})")
         self.code = code
+        self.word = word
 
 
-def _check(code: int, what: str):
+def _check(code: int, what: str, ctx=None):
     if code != 0:
-        raise DmtpError(code, what)
+        word = int(load_library().dmtp_error_word(ctx)) if ctx else 0
+        raise DmtpError(code, what, word)
 
 
 def make_config(cfg, max_ctx: int, max_batch: int | None = None) -> dmtp_config:
@@ -283,10 +289,10 @@ class DmtpRound:
                 setattr(o, k, t.data_ptr())
         f = C.c_void_p(forced.data_ptr()) if forced is not None else None
         if depth == 7:
-            _check(self.lib.dmtp_round(self.ctx, C.byref(o), f), "dmtp_round")
+            _check(self.lib.dmtp_round(self.ctx, C.byref(o), f), "dmtp_round", self.ctx)
         else:
             _check(self.lib.dmtp_round_depth(self.ctx, C.byref(o), f, int(depth)),
-                   "dmtp_round_depth")
+                   "dmtp_round_depth", self.ctx)
 
     def alloc_out(self, ints=True, floats=False):
         import torch
@@ -311,7 +317,7 @@ class DmtpRound:
         """One round with host outputs (pinned or pageable numpy int32 arrays)."""
         cp = committed.ctypes.data_as(C.c_void_p) if committed is not None else None
         npt = n_acc.ctypes.data_as(C.c_void_p) if n_acc is not None else None
-        _check(self.lib.dmtp_round_host(self.ctx, cp, npt), "dmtp_round_host")
+        _check(self.lib.dmtp_round_host(self.ctx, cp, npt), "dmtp_round_host", self.ctx)
 
     def read_state(self):
         kv = np.zeros(self.B, np.int32)
@@ -319,7 +325,8 @@ class DmtpRound:
         hist = np.zeros(8, np.uint64)
         _check(self.lib.dmtp_read_state(self.ctx, kv.ctypes.data_as(C.c_void_p),
                                         A.ctypes.data_as(C.c_void_p),
-                                        hist.ctypes.data_as(C.c_void_p)), "dmtp_read_state")
+                                        hist.ctypes.data_as(C.c_void_p)), "dmtp_read_state",
+               self.ctx)
         return kv, A, hist
 
     def profile_round(self) -> dict:

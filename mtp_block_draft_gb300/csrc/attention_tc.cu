@@ -143,7 +143,10 @@ struct Smem {
   // barriers, tile maxima [2][4][64], running sums [4][64], tile-count prefix [B + 1]
   static constexpr uint32_t kSmall = 256 + 2048 + 1024 + 4 * (kAttnMaxB + 1);
   static constexpr uint32_t kBig = NST * kStage + kP + kX;  // 1024-aligned region
-  static constexpr uint32_t kBytes = (kSmall + 1023) / 1024 * 1024 + kBig;
+  // the big region starts at the first 1024-byte boundary past kSmall: room for any base
+  // address (a CTA sharing its SM with another kernel's CTAs, under programmatic launch,
+  // gets a dynamic shared memory base that is not 1024-aligned)
+  static constexpr uint32_t kBytes = (kSmall + 1024 + kBig + 127) / 128 * 128;
   static_assert(kBytes <= 232448, "shared memory plan exceeds 227 KB");
 };
 
@@ -277,9 +280,10 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   // Up to here the CTA read only the sequences' base positions, which the launch before
   // this one (the RoPE / KV-row writer) does not write and lets this launch begin only
-  // after its own wait; the queries and the new K/V rows come after the wait. The K/V
-  // producer waits lazily: tiles wholly below a sequence's base position (keys of earlier
-  // rounds) fill the first stages while the previous launch drains.
+  // after its own wait; the queries and the new K/V rows come after the wait. In a round
+  // (a.early_kv) the K/V producer waits lazily: tiles wholly below a sequence's base
+  // position (keys of earlier rounds) fill the first stages while the previous launch
+  // drains.
   pdl_trigger();
   if (!(warp == 8 && lane == 0)) pdl_wait();
   const uint32_t tmem = *tmem_slot;
@@ -300,8 +304,9 @@ __global__ void __launch_bounds__(320, 1)
         const long vblk0 = ((long)cb * hkv + g) * (a.max_ctx / 64);  // 64-key V^T blocks
         for (int t = 0; t < nt; ++t, ++gt) {
           // a stage's second use, or keys at or past the base position (this round's
-          // rows, written by the previous launch): after the grid dependency
-          if (!waited && (gt >= NST || (kt0 + t + 1) * TK > pc.base)) {
+          // rows, written by the previous launch), or a prefill step (whose row groups of
+          // one prompt write keys below each other's base): after the grid dependency
+          if (!waited && (!a.early_kv || gt >= NST || (kt0 + t + 1) * TK > pc.base)) {
             pdl_wait();
             waited = true;
           }

@@ -145,6 +145,8 @@ struct dmtp_ctx {
   VerifyPlans* vp[8];               // [G] for G = 1..7 rows per sequence (G = 8: tgt etc.)
   cudaStream_t cap_st;  // private stream the round is captured on (the caller's may be NULL)
   bool poisoned;
+  bool prefilling;  // the prompt's chunks are being enqueued (several row groups per prompt)
+  unsigned err_word;  // the device error word that poisoned it
   long kv_bound;
   int launches;
   int round_launches;
@@ -597,6 +599,7 @@ void attn_layer(dmtp_ctx* c, const LayerPlans& p, const dmtp_layer_weights& w, f
   aa.out_lo = lo_of(c, mt_of_rows(c, M), c->qd);
   aa.base = a.base;
   aa.cseq = c->rs.cseq;
+  aa.early_kv = c->prefilling ? 0 : 1;
   aa.causal = a.causal;
   aa.lo_fixed = a.lo_fixed;
   aa.window = a.window;
@@ -808,6 +811,7 @@ int check_err(dmtp_ctx* c) {
   if (cudaStreamSynchronize(c->st) != cudaSuccess) return DMTP_ECUDA;
   if (e) {
     c->poisoned = true;
+    c->err_word = e;
     if (getenv("DMTP_VERBOSE"))
       fprintf(stderr, "dmtp: device error word 0x%x (1 token id, 2 KV position, 4 wait timed "
               "out, 8 snapshot slot)\n", e);
@@ -1105,6 +1109,8 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
   c->st = (cudaStream_t)stream;
   for (int k = 0; k < 8; ++k) c->graph[k] = c->graph_forced[k] = nullptr;
   c->poisoned = false;
+  c->prefilling = false;
+  c->err_word = 0;
   int dev = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&c->nsm, cudaDevAttrMultiProcessorCount, dev);
@@ -1327,6 +1333,7 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
                       cudaMemcpyHostToDevice, st) != cudaSuccess)
     return fail_prefill();
   pdl_fence();
+  c->prefilling = true;
   for (int t = 0; t < nsteps; ++t) {
     op_prefill_chunk(s, c->prompts, c->plen, c->maxc, c->psched + (size_t)t * B, st);
     target_forward(c, false, 8, c->tgt);
@@ -1343,6 +1350,7 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
   op_prefill_final(s, c->plen, c->hlast, c->hT32, c->d, st);
   mtp_advance(c);
   op_prefill_done(s, c->plen, st);
+  c->prefilling = false;
   if (pe1) cudaEventRecord(pe1, st);
   // a launch that failed (e.g. for its resources) leaves no device error word: ask for it
   cudaError_t ce = cudaGetLastError();
@@ -1592,6 +1600,8 @@ int dmtp_set_draft_list(dmtp_ctx* c, const int32_t* ids, int n) {
     op_gather_rows(c->w.head, c->hc, (size_t)c->d * 2, c->hc_ids, n, nullptr, nullptr, c->st);
   return cudaGetLastError() == cudaSuccess ? DMTP_OK : DMTP_ECUDA;
 }
+
+uint32_t dmtp_error_word(const dmtp_ctx* c) { return c ? c->err_word : 0u; }
 
 int dmtp_selftest_timeout(dmtp_ctx* c, uint64_t limit_ns) {
   if (!c) return DMTP_EINVAL;

@@ -316,6 +316,7 @@ def test_device_timeout_poisons_context():
     with pytest.raises(DmtpError) as e:
         g.read_state()
     assert e.value.code == -5                        # DMTP_EDEVICE
+    assert e.value.word == 4                         # the timeout bit, nothing else
     for call in (g.round, g.read_state, g.profile_round, lambda: g.selftest_timeout(50_000)):
         with pytest.raises(DmtpError) as e:
             call()
