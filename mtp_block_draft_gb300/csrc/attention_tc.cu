@@ -280,12 +280,9 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   // Up to here the CTA read only the sequences' base positions, which the launch before
   // this one (the RoPE / KV-row writer) does not write and lets this launch begin only
-  // after its own wait; the queries and the new K/V rows come after the wait. In a round
-  // (a.early_kv) the K/V producer waits lazily: tiles wholly below a sequence's base
-  // position (keys of earlier rounds) fill the first stages while the previous launch
-  // drains.
+  // after its own wait; the queries and the K/V tiles come after the wait.
   pdl_trigger();
-  if (!(warp == 8 && lane == 0)) pdl_wait();
+  pdl_wait();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tO = tmem + 2 * TK;
   auto tQb = [&](int buf) -> uint32_t { return tO + HD + (uint32_t)buf * (HD / 2); };
@@ -295,7 +292,7 @@ __global__ void __launch_bounds__(320, 1)
       // ---------------- K/V producer: every tile of the range, in order ----------------
       const uint64_t pol = policy_evict_first();
       int gt = 0;
-      bool ok = true, waited = false;
+      bool ok = true;
       Pc pc;
       for (long x = first_piece(x0, pc); x < x1 && ok; x = first_piece(x + pc.adv, pc)) {
         const int b = pc.b, g = pc.g, kt0 = pc.kt0, nt = pc.nt;
@@ -303,13 +300,6 @@ __global__ void __launch_bounds__(320, 1)
         const long krow0 = ((long)cb * hkv + g) * a.max_ctx;
         const long vblk0 = ((long)cb * hkv + g) * (a.max_ctx / 64);  // 64-key V^T blocks
         for (int t = 0; t < nt; ++t, ++gt) {
-          // a stage's second use, or keys at or past the base position (this round's
-          // rows, written by the previous launch), or a prefill step (whose row groups of
-          // one prompt write keys below each other's base): after the grid dependency
-          if (!waited && (!a.early_kv || gt >= NST || (kt0 + t + 1) * TK > pc.base)) {
-            pdl_wait();
-            waited = true;
-          }
           const int s = gt % NST;
           if (!mbar_wait(smem_u32(&kv_empty[s]), ((gt / NST) & 1) ^ 1, err)) {
             ok = false;
@@ -326,7 +316,6 @@ __global__ void __launch_bounds__(320, 1)
       }
       for (int j = (gt > NST ? gt - NST : 0); j < gt; ++j)
         mbar_wait(smem_u32(&kv_full[j % NST]), (j / NST) & 1, err);
-      if (!waited) pdl_wait();
     }
   } else if (warp == 9) {
     if (lane == 0) {

@@ -145,7 +145,6 @@ struct dmtp_ctx {
   VerifyPlans* vp[8];               // [G] for G = 1..7 rows per sequence (G = 8: tgt etc.)
   cudaStream_t cap_st;  // private stream the round is captured on (the caller's may be NULL)
   bool poisoned;
-  bool prefilling;  // the prompt's chunks are being enqueued (several row groups per prompt)
   unsigned err_word;  // the device error word that poisoned it
   long kv_bound;
   int launches;
@@ -599,7 +598,6 @@ void attn_layer(dmtp_ctx* c, const LayerPlans& p, const dmtp_layer_weights& w, f
   aa.out_lo = lo_of(c, mt_of_rows(c, M), c->qd);
   aa.base = a.base;
   aa.cseq = c->rs.cseq;
-  aa.early_kv = c->prefilling ? 0 : 1;
   aa.causal = a.causal;
   aa.lo_fixed = a.lo_fixed;
   aa.window = a.window;
@@ -1109,7 +1107,6 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
   c->st = (cudaStream_t)stream;
   for (int k = 0; k < 8; ++k) c->graph[k] = c->graph_forced[k] = nullptr;
   c->poisoned = false;
-  c->prefilling = false;
   c->err_word = 0;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1333,7 +1330,6 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
                       cudaMemcpyHostToDevice, st) != cudaSuccess)
     return fail_prefill();
   pdl_fence();
-  c->prefilling = true;
   for (int t = 0; t < nsteps; ++t) {
     op_prefill_chunk(s, c->prompts, c->plen, c->maxc, c->psched + (size_t)t * B, st);
     target_forward(c, false, 8, c->tgt);
@@ -1350,7 +1346,6 @@ int dmtp_init(const dmtp_config* cfg, const dmtp_weights* w, void* workspace, si
   op_prefill_final(s, c->plen, c->hlast, c->hT32, c->d, st);
   mtp_advance(c);
   op_prefill_done(s, c->plen, st);
-  c->prefilling = false;
   if (pe1) cudaEventRecord(pe1, st);
   // a launch that failed (e.g. for its resources) leaves no device error word: ask for it
   cudaError_t ce = cudaGetLastError();

@@ -152,9 +152,6 @@ struct AttnArgs {
   long qs_lo;          // ... and remainder at qs + qs_lo
   int pgrid;           // tensor-core path: persistent CTAs; partials [pgrid + B*hkv]
   int ptk;             // tensor-core path: keys per tile (kAttnTile)
-  int early_kv = 0;    // 1: each row group is its own cache sequence and the launch before
-                       // writes only keys >= base (a round's forwards), so key tiles wholly
-                       // below base may load before the grid dependency resolves
   int rows = 8;        // rows per sequence (a verify of fewer drafts has fewer): row m of
                        // q / out is sequence m / rows at position base + m % rows
 };
