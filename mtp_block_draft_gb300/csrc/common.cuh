@@ -28,9 +28,8 @@ typedef __nv_bfloat16 bf16;
 // ---------------------------------------------------------------------------------
 // Programmatic dependent launch (griddepcontrol). A kernel launched with launch_pdl()
 // may begin while the kernel before it in the stream is still running: its CTAs set up
-// shared memory, barriers and TMEM, and may read the constant weights, but nothing that
-// an earlier launch writes, until pdl_wait() returns (the previous grid has completed
-// and its writes are visible). pdl_trigger() lets the next launch begin; a CTA that
+// shared memory, barriers and TMEM, but read nothing that an earlier launch writes until
+// pdl_wait() returns (the previous grid has completed and its writes are visible). pdl_trigger() lets the next launch begin; a CTA that
 // allocates TMEM calls it only after its allocation, so that a successor's CTA never
 // holds the columns a running CTA is still waiting for. Both are no-ops in a kernel
 // launched without the attribute.

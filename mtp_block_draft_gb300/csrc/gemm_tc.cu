@@ -116,8 +116,8 @@ __host__ __device__ inline uint32_t tmem_cols_for(int cols) {
 // One GEMM pass of a CTA over its tile (bx, by, bz) of a (gx, *, gz) tile grid: TMA
 // producer, MMA issuer and epilogue, on shared memory (stage ring at smem) and barriers
 // already initialised, with `tmem` allocated. grid_dep: the pass reads the previous
-// launch's outputs, so everything but the producer's weight requests waits for the grid
-// dependency first (programmatic launch).
+// launch's outputs, so every thread first waits for the grid dependency (programmatic
+// launch).
 struct GemmBars {
   uint64_t *full, *empty, *accum, *sumbar;
 };
@@ -151,7 +151,7 @@ __device__ __forceinline__ void gemm_pass(const CUtensorMap* tmW, const CUtensor
   const int nkb = a.K / kBlockK;
   const int kb0 = (int)((long)bz * nkb / gz);
   const int kb1 = (int)((long)(bz + 1) * nkb / gz);
-  if (grid_dep && !(warp == 0 && lane == 0)) pdl_wait();
+  if (grid_dep) pdl_wait();
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------
@@ -176,23 +176,13 @@ __device__ __forceinline__ void gemm_pass(const CUtensorMap* tmW, const CUtensor
         load(smem_u32(sW + s * wbytes), tmW, kb * kBlockK, n0, s, pw);
       }
     };
-    // The weights are constant: the first stages' weight slices are requested before the
-    // wait for the previous launch (whose tail they overlap), the token rows after it.
-    const int pre = min(S, kb1 - kb0);
-    for (int i = 0; i < pre; ++i) {
-      if (rank == 0) mbar_expect_tx(smem_u32(&full[i]), stage_bytes);
-      load_w(i, kb0 + i);
-    }
-    if (grid_dep) pdl_wait();
     int issued = 0;
     for (int kb = kb0; kb < kb1; ++kb, ++issued) {
       const int s = issued % S;
-      if (issued >= pre) {
-        const uint32_t ph = (issued / S) & 1;
-        if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, a.err)) break;
-        if (rank == 0) mbar_expect_tx(smem_u32(&full[s]), stage_bytes);
-        load_w(s, kb);
-      }
+      const uint32_t ph = (issued / S) & 1;
+      if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, a.err)) break;
+      if (rank == 0) mbar_expect_tx(smem_u32(&full[s]), stage_bytes);
+      load_w(s, kb);
       if (PAIR) {
         load(smem_u32(sX + s * xbytes), tmX, kb * kBlockK, (int)rank * a.MT + mrow0, s, px);
         continue;

@@ -177,41 +177,27 @@ __global__ void __launch_bounds__(64 + 32 * EW, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // the next launch may begin (this CTA holds its TMEM); everything but the producer's
-  // weight requests waits here for the previous launch (the token list's length, read
-  // above, is set before a round starts)
+  // the next launch may begin (this CTA holds its TMEM); then the grid dependency (the
+  // token list's length, read above, is set before a round starts)
   pdl_trigger();
-  if (!(warp == 0 && lane == 0)) pdl_wait();
+  pdl_wait();
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer ----------------
       const uint64_t pw = policy_evict_first(), px = policy_evict_last();
-      // The weights are constant: the first stages' vocabulary slices are requested before
-      // the wait for the previous launch, the token rows (written by it) after.
-      const int my_tiles =
-          (int)blockIdx.x < tiles ? (tiles - (int)blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-      const int pre = min(S, my_tiles * nkb);
-      for (int i = 0; i < pre; ++i) {
-        mbar_expect_tx(smem_u32(&full[i]), kWBytes + xbytes);
-        tma_load_2d(smem_u32(sW + (size_t)i * kWBytes), &tmW, (i % nkb) * kBK,
-                    (blockIdx.x + (i / nkb) * gridDim.x) * NV, smem_u32(&full[i]), pw);
-      }
-      pdl_wait();
       int it = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % S;
-          if (it >= pre) {
-            if (!mbar_wait(smem_u32(&empty[s]), ((it / S) & 1) ^ 1, a.err)) {
-              ok = false;
-              break;
-            }
-            mbar_expect_tx(smem_u32(&full[s]), kWBytes + xbytes);
-            tma_load_2d(smem_u32(sW + (size_t)s * kWBytes), &tmW, kb * kBK, t * NV,
-                        smem_u32(&full[s]), pw);
+          if (!mbar_wait(smem_u32(&empty[s]), ((it / S) & 1) ^ 1, a.err)) {
+            ok = false;
+            break;
           }
+          mbar_expect_tx(smem_u32(&full[s]), kWBytes + xbytes);
+          tma_load_2d(smem_u32(sW + (size_t)s * kWBytes), &tmW, kb * kBK, t * NV,
+                      smem_u32(&full[s]), pw);
           tma_load_2d(smem_u32(sX + (size_t)s * kXSlot), &tmX, kb * kBK, 0, smem_u32(&full[s]),
                       px);
         }
