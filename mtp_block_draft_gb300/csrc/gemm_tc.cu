@@ -26,6 +26,16 @@
 // GEMM's bf16 pair with one TMA store.
 // Stages are 64-element (128 B) k slices with 128-byte swizzle.
 //
+// CTA pairs (a plan option): two CTAs of a cluster, adjacent in x, run one M = 256
+// tcgen05.mma.cta_group::2 per k step. Each holds its own 128 (or 256) weight rows and
+// one half of the merged [hi; lo] token columns (CTA 0 the hi rows, CTA 1 the
+// remainders), so each SM loads and reads half the token bytes; both CTAs' loads complete
+// on CTA 0's barriers, CTA 0 issues the MMAs and its commits arrive on both CTAs'
+// barriers, and each CTA's epilogue reads its own rows from its own TMEM.
+//
+// Launched with programmatic serialisation (common.cuh): barrier set-up and the TMEM
+// allocation overlap the previous kernel, every load follows the grid dependency.
+//
 // Split activations: the token operand may come as two bf16 halves, X = X_hi + X_lo
 // (X_lo = the rounding remainder of X_hi), stored as 2*MT rows [hi; lo]. Both halves
 // are multiplied by the same weight tile (one TMA load of W). Up to 128 token rows the
