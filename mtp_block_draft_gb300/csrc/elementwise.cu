@@ -258,6 +258,8 @@ __device__ __forceinline__ int checked_tok(int t, int vocab, unsigned* err) {
 template <typename T>
 __global__ void k_embed(const T* __restrict__ E, const int* __restrict__ tok, int vocab,
                         float* __restrict__ x, int d, unsigned* err) {
+  pdl_trigger();
+  pdl_wait();
   const int m = blockIdx.x;
   const int t = checked_tok(tok[m], vocab, err);
   const T* e = E + (long)t * d;
@@ -267,9 +269,9 @@ __global__ void k_embed(const T* __restrict__ E, const int* __restrict__ tok, in
 void op_embed(int dt, const void* E, const int* tok, int vocab, float* x, int rows, int d,
               unsigned* err, cudaStream_t st) {
   if (dt)
-    k_embed<bf16><<<rows, 256, 0, st>>>((const bf16*)E, tok, vocab, x, d, err);
+    launch_pdl(k_embed<bf16>, rows, 256, 0, st, (const bf16*)E, tok, vocab, x, d, err);
   else
-    k_embed<float><<<rows, 256, 0, st>>>((const float*)E, tok, vocab, x, d, err);
+    launch_pdl(k_embed<float>, rows, 256, 0, st, (const float*)E, tok, vocab, x, d, err);
 }
 
 // ---------------------------------------------------------------------------------
@@ -329,6 +331,8 @@ template <typename T>
 __global__ void k_build_slots(const T* __restrict__ E, int vocab, const int* __restrict__ A,
                               const int* __restrict__ drafts, const float* __restrict__ delta,
                               int mask_id, float* __restrict__ x, int d, unsigned* err) {
+  pdl_trigger();
+  pdl_wait();
   const int m = blockIdx.x, b = m >> 3, s = m & 7;
   int t = (s == 0) ? A[b] : (s == 1 ? drafts[b * 7] : mask_id);
   t = checked_tok(t, vocab, err);
@@ -344,11 +348,11 @@ void op_build_slots(int dt, const void* E, int vocab, const int* A, const int* d
                     const float* delta, int mask_id, float* x, int B, int d, unsigned* err,
                     cudaStream_t st) {
   if (dt)
-    k_build_slots<bf16><<<B * 8, 256, 0, st>>>((const bf16*)E, vocab, A, drafts, delta, mask_id,
-                                               x, d, err);
+    launch_pdl(k_build_slots<bf16>, B * 8, 256, 0, st, (const bf16*)E, vocab, A, drafts, delta,
+               mask_id, x, d, err);
   else
-    k_build_slots<float><<<B * 8, 256, 0, st>>>((const float*)E, vocab, A, drafts, delta,
-                                                mask_id, x, d, err);
+    launch_pdl(k_build_slots<float>, B * 8, 256, 0, st, (const float*)E, vocab, A, drafts, delta,
+               mask_id, x, d, err);
 }
 
 // ---------------------------------------------------------------------------------
@@ -586,6 +590,8 @@ void op_l2_flush(const void* buf, size_t bytes, unsigned* sink, cudaStream_t st)
 template <typename T>
 __global__ void k_cast_rows(const float* __restrict__ x, int ldx, T* __restrict__ y, int ldy,
                             long y_lo, int d, RowMap map) {
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x;
   const float* xr = x + (long)map_row(r, map) * ldx;
   for (int i = threadIdx.x; i < d; i += blockDim.x) store_act(y + (long)r * ldy + i, y_lo, xr[i]);
@@ -594,9 +600,9 @@ __global__ void k_cast_rows(const float* __restrict__ x, int ldx, T* __restrict_
 void op_cast_rows(int dt, const float* x, int ldx, void* y, int ldy, long y_lo, int rows, int d,
                   RowMap map, cudaStream_t st) {
   if (dt)
-    k_cast_rows<bf16><<<rows, 256, 0, st>>>(x, ldx, (bf16*)y, ldy, y_lo, d, map);
+    launch_pdl(k_cast_rows<bf16>, rows, 256, 0, st, x, ldx, (bf16*)y, ldy, y_lo, d, map);
   else
-    k_cast_rows<float><<<rows, 256, 0, st>>>(x, ldx, (float*)y, ldy, y_lo, d, map);
+    launch_pdl(k_cast_rows<float>, rows, 256, 0, st, x, ldx, (float*)y, ldy, y_lo, d, map);
 }
 
 // ---------------------------------------------------------------------------------
@@ -618,6 +624,8 @@ void op_round_begin(const RoundState& s, cudaStream_t st) {
 __global__ void k_keys_to_ids(const unsigned long long* __restrict__ keys, int B, int per,
                               int* dst, int dst_stride, int dst_off, const int* forced,
                               int forced_stride, int forced_off, const int* map) {
+  pdl_trigger();
+  pdl_wait();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= B * per) return;
   const int b = i / per, j = i % per;
@@ -630,8 +638,8 @@ __global__ void k_keys_to_ids(const unsigned long long* __restrict__ keys, int B
 void op_keys_to_ids(const unsigned long long* keys, int B, int per, int* dst, int dst_stride,
                     int dst_off, const int* forced, int forced_stride, int forced_off,
                     cudaStream_t st, const int* map) {
-  k_keys_to_ids<<<cdiv(B * per, 128), 128, 0, st>>>(keys, B, per, dst, dst_stride, dst_off,
-                                                    forced, forced_stride, forced_off, map);
+  launch_pdl(k_keys_to_ids, cdiv(B * per, 128), 128, 0, st, keys, B, per, dst, dst_stride,
+             dst_off, forced, forced_stride, forced_off, map);
 }
 
 // One CTA per listed row: 16-byte copies of the row, and its scale.
@@ -653,6 +661,8 @@ void op_gather_rows(const void* src, void* dst, size_t row_bytes, const int* ids
 }
 
 __global__ void k_verify_tokens(RoundState s, int depth) {
+  pdl_trigger();
+  pdl_wait();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= s.B * 8) return;
   const int G = depth + 1, b = i >> 3, j = i & 7;
@@ -665,7 +675,7 @@ __global__ void k_verify_tokens(RoundState s, int depth) {
 }
 
 void op_verify_tokens(const RoundState& s, int depth, cudaStream_t st) {
-  k_verify_tokens<<<cdiv(s.B * 8, 256), 256, 0, st>>>(s, depth);
+  launch_pdl(k_verify_tokens, cdiv(s.B * 8, 256), 256, 0, st, s, depth);
 }
 
 // Greedy prefix acceptance ([DMTP] §5): n = longest prefix with T_j == g_{j-1};
@@ -673,6 +683,8 @@ void op_verify_tokens(const RoundState& s, int depth, cudaStream_t st) {
 // Also prepares the MTP advance rows (tokens x_{pos0+1+s} = committed[s]) and swaps
 // the GDN snapshot slot n in as the live state (pointer swap, nothing copied).
 __global__ void k_accept(RoundState s, int depth) {
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= s.B) return;
   const int* T = s.drafts + b * 7;
@@ -703,18 +715,20 @@ __global__ void k_accept(RoundState s, int depth) {
 }
 
 void op_accept(const RoundState& s, int depth, cudaStream_t st) {
-  k_accept<<<cdiv(s.B, 64), 64, 0, st>>>(s, depth);
+  launch_pdl(k_accept, cdiv(s.B, 64), 64, 0, st, s, depth);
 }
 
 __global__ void k_gather_hmtp(const float* __restrict__ x, const int* __restrict__ cnt,
                               float* __restrict__ h, int d) {
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x;
   const int r = b * 8 + max(0, min(7, cnt[b] - 1));
   for (int i = threadIdx.x; i < d; i += blockDim.x) h[(long)b * d + i] = x[(long)r * d + i];
 }
 
 void op_gather_hmtp(const float* x, const int* cnt, float* h, int B, int d, cudaStream_t st) {
-  k_gather_hmtp<<<B, 256, 0, st>>>(x, cnt, h, d);
+  launch_pdl(k_gather_hmtp, B, 256, 0, st, x, cnt, h, d);
 }
 
 // Prefill step: row group pb covers 8 positions of one prompt, chunk sched[pb] =

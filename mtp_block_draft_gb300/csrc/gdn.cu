@@ -126,6 +126,8 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
 
 template <typename T, int CW>
 __global__ void __launch_bounds__(128, 4) k_gdn_cols(GdnArgs a) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int DK = 32 * CW;
   __shared__ __align__(16) float qs[8][DK], ks[8][DK];
   __shared__ float vs[8][64], als[8], bes[8], kqs[8];
@@ -228,14 +230,14 @@ void op_gdn(int dt, const GdnArgs& a, cudaStream_t st) {
     const int grid = a.B * a.H * (a.dv / 64);
     if (a.dk == 128) {
       if (dt)
-        k_gdn_cols<bf16, 4><<<grid, 128, 0, st>>>(a);
+        launch_pdl(k_gdn_cols<bf16, 4>, grid, 128, 0, st, a);
       else
-        k_gdn_cols<float, 4><<<grid, 128, 0, st>>>(a);
+        launch_pdl(k_gdn_cols<float, 4>, grid, 128, 0, st, a);
     } else {
       if (dt)
-        k_gdn_cols<bf16, 2><<<grid, 128, 0, st>>>(a);
+        launch_pdl(k_gdn_cols<bf16, 2>, grid, 128, 0, st, a);
       else
-        k_gdn_cols<float, 2><<<grid, 128, 0, st>>>(a);
+        launch_pdl(k_gdn_cols<float, 2>, grid, 128, 0, st, a);
     }
     return;
   }

@@ -454,6 +454,8 @@ namespace dmtp {
 // Row m goes to dst[(m / per) * stride + off + m % per].
 __global__ void k_conf_combine(const float2* __restrict__ parts, int nparts, int M, int per,
                                float* dst, int stride, int off) {
+  pdl_trigger();
+  pdl_wait();
   const int m = blockIdx.x * blockDim.x + threadIdx.x;
   if (m >= M) return;
   float mx = -__int_as_float(0x7f800000);
@@ -470,8 +472,8 @@ int head_conf_parts(const HeadPlan& p) { return p.grid * (p.ew / 4); }
 
 void op_conf_combine(const HeadPlan& p, const float2* parts, int per, float* dst, int stride,
                      int off, cudaStream_t st) {
-  k_conf_combine<<<(p.M + 127) / 128, 128, 0, st>>>(parts, head_conf_parts(p), p.M, per, dst,
-                                                     stride, off);
+  launch_pdl(k_conf_combine, (p.M + 127) / 128, 128, 0, st, parts, head_conf_parts(p), p.M, per,
+             dst, stride, off);
 }
 
 }  // namespace dmtp
