@@ -129,6 +129,22 @@ def test_init_rejects_empty_prompt_and_unaligned_workspace(lib):
     assert r == -1 and not ctx.value
 
 
+def test_deterministic_option_and_error_word(lib):
+    """deterministic takes 0 or 1 and adds the fixed-order K-part scratch to a bf16
+    workspace; the error word of no context is 0."""
+    cfg = CONFIGS["b32"]
+    n0, n1 = ctypes.c_size_t(), ctypes.c_size_t()
+    c = make_config(cfg, 5000)
+    assert lib.dmtp_workspace_size(ctypes.byref(c), 32, ctypes.byref(n0)) == 0
+    c.deterministic = 1
+    assert lib.dmtp_workspace_size(ctypes.byref(c), 32, ctypes.byref(n1)) == 0
+    assert n1.value > n0.value
+    c.deterministic = 2
+    assert lib.dmtp_workspace_size(ctypes.byref(c), 32, ctypes.byref(n1)) == -1
+    lib.dmtp_error_word.restype = ctypes.c_uint32
+    assert lib.dmtp_error_word(None) == 0
+
+
 def test_workspace_size_grows_with_batch_and_context(lib):
     """Odd and even batches alike: more sequences or a longer context never need less."""
     cfg = CONFIGS["b32"]
